@@ -1,0 +1,420 @@
+"""Benchmark of the FSDP FlatParameter step on GB300.
+
+One step = one pass of the whole hot path over one unit: the fused
+reduce-scatter + AdamW + cast over all N emulated ranks' blocks, then the
+all-gather(s) of the updated compute-dtype shards into the N full buffers
+(twice for the 70B unit: before forward and before backward). Flatten/pad and
+the unflatten views are set-up (once per unit) and are not in the step.
+
+Default workload: the Llama-70B-style block unit (855,654,400 parameters, N=8,
+bf16 gradients ~N(0, 1e-4), AdamW lr 3e-5, wd 0.1, two all-gathers per step),
+the largest unit of the set, on which the fused kernel's HBM-bandwidth target
+is stated. Inputs are synthetic (seeded), resident in HBM, and far larger
+than L2.
+
+Printed (rank 0, one JSON line): value = algorithmic bytes of the step / step
+time (GB/s, whole job over all ranks); roofline of the fused kernel (its own
+CUDA-event time inside the timed region); e2e through the Python binding with
+pinned host buffers; the CPU oracle timed on the host cores; clocks sampled
+during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Under torchrun each rank runs its own unit on its own GPU (independent
+units: weak scaling, no data-path collective); rank 0 prints the MAX step
+time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused RS+AdamW+cast GB/s and params/s per FSDP unit vs HBM roofline, 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD_NAMES = {
+    "tiny": "tiny_unit_4099_n2",
+    "gpt2_small": "gpt2_small_block_unit_n8",
+    "gpt2_large": "gpt2_large_block_unit_n2_fp16",
+    "gpt3_13b": "gpt3_13b_block_unit_n8",
+    "llama70b": "llama70b_block_unit_n8",
+}
+RSA_SOURCES = ("sharded_fsdp_reduce_gb300/csrc/rsa_impl.cuh", "sharded_fsdp_reduce_gb300/csrc/common.cuh")
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def step_bytes(P_pad: int, world: int, gsize: int, osize: int, gathers: int, n_dst: int):
+    """Algorithmic bytes: fused kernel per launch, all-gathers per step."""
+    rsa = P_pad * (world * gsize + 3 * (4 + 4) + osize)
+    ag = gathers * P_pad * osize * (1 + n_dst)
+    return rsa, ag
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in RSA_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """Per-launch DRAM traffic of the fused kernel from a committed ncu summary,
+    or None when there is none for this workload or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", f"rsa_{workload}_ncu.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_sha256")):
+                k, v = line.split(":", 1)
+                vals[k.strip().lstrip("- ")] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.reader.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
+
+def oracle_sample_run(cfg, n_elems: int, steps: int, warmup: int, time_budget_s: float | None):
+    """The oracle as it stands, on an n_elems-element unit with the workload's
+    N, dtypes, distributions and gathers. Returns (GB/s, elapsed, steps run, threads)."""
+    import numpy as np
+    import torch
+
+    import fsdp_inputs as fi
+    import oracle as orc
+
+    threads = os.cpu_count() or 1
+    orc.set_threads(threads)
+    N = cfg.world
+    P_pad = orc.padded_numel(n_elems, N)
+    S = P_pad // N
+    master = orc.flatten_pad([fi.gen_master(cfg, numel=n_elems).numpy()], N)
+    m = np.zeros(P_pad, np.float32)
+    v = np.zeros(P_pad, np.float32)
+
+    def host_grad(r, t):
+        g = fi.gen_grad(cfg, r, t, numel=n_elems)
+        arr = g.numpy() if g.dtype == torch.float32 else g.view(torch.int16).numpy().view(np.uint16)
+        return orc.flatten_pad([arr], N)
+
+    grads = [host_grad(r, 1) for r in range(N)]
+    gsize = 4 if cfg.grad_dtype == "f32" else 2
+    osize = 4 if cfg.out_dtype == "f32" else 2
+    rsa_b, ag_b = step_bytes(P_pad, N, gsize, osize, cfg.gathers, N)
+
+    def one_step(t):
+        hp = orc.hparams(cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay, t, cfg.grad_scale)
+        shards, _ = orc.fsdp_step(grads, cfg.grad_dtype, N, master, m, v, cfg.out_dtype, hp)
+        pieces = [shards[r * S:(r + 1) * S] for r in range(N)]
+        for _ in range(cfg.gathers):
+            for _dst in range(N):  # one gathered buffer per emulated rank
+                orc.all_gather(pieces, N)
+
+    for t in range(1, warmup + 1):
+        one_step(t)
+    t0 = time.perf_counter()
+    done = 0
+    while done < steps or (time_budget_s is not None and time.perf_counter() - t0 < time_budget_s):
+        one_step(warmup + done + 1)
+        done += 1
+        if time_budget_s is None and done >= steps:
+            break
+    el = time.perf_counter() - t0
+    return (rsa_b + ag_b) * done / el / 1e9, el, done, threads
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import fsdp_inputs as fi
+    import sharded_fsdp_reduce_gb300 as F
+    from sharded_fsdp_reduce_gb300 import build as _build
+
+    rank, local_rank, world_size = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (GB300); there is no CPU path")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world_size > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or not os.path.exists(os.path.join(ROOT, "sharded_fsdp_reduce_gb300", "libfsdpreduce.so")):
+        _build.build()
+    if world_size > 1:
+        dist.barrier()
+    F._lib.load()
+
+    cfg = fi.CONFIGS[args.config]
+    N = cfg.world
+    gdt, odt = fi.torch_dtype(cfg.grad_dtype), fi.torch_dtype(cfg.out_dtype)
+    unit = F.FlatParamUnit(cfg.params, N, gdt, odt, device=dev)
+    P_pad = unit.padded_numel
+    seed = 100_000 * rank  # each GPU owns a different unit
+    unit.load_master([fi.gen_master(cfg, device=dev, seed_base=seed)])
+    for r in range(N):
+        unit.load_grad(r, [fi.gen_grad(cfg, r, 1, device=dev, seed_base=seed)])
+    torch.cuda.synchronize()
+    rsa_b, ag_b = unit.step_bytes(cfg.gathers)
+
+    def hp(t):
+        return F.AdamWHParams(cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay, t, cfg.grad_scale)
+
+    stream = torch.cuda.current_stream()
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        unit.step(hp(t), gathers=cfg.gathers)
+    torch.cuda.synchronize()
+
+    # ---- timed region (device time, CUDA events on the launching stream)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world_size > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clocks:
+        time.sleep(0.25)  # let the sampler start before the timed launches
+        start.record(stream)
+        for i in range(K):
+            t += 1
+            ev[i][0].record(stream)
+            unit.reduce_scatter_adam_cast(hp(t))
+            ev[i][1].record(stream)
+            for _ in range(cfg.gathers):
+                unit.all_gather()
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world_size > 1:
+        dist.barrier()
+    step_ms = start.elapsed_time(end) / K
+    rsa_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    launches = K * (1 + cfg.gathers)
+
+    # ---- end to end through the binding: pinned host grads in, params out
+    Ke = max(3, min(args.e2e_steps, K))
+    host_grads = [torch.empty(P_pad, dtype=gdt, pin_memory=True) for _ in range(N)]
+    for r in range(N):
+        host_grads[r].copy_(unit.grads[r])
+    host_out = torch.empty(P_pad, dtype=odt, pin_memory=True)
+    h2d = sum(g.numel() * g.element_size() for g in host_grads)
+    d2h = host_out.numel() * host_out.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world_size > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(Ke):
+        t += 1
+        for r in range(N):
+            unit.grads[r].copy_(host_grads[r], non_blocking=True)
+        unit.step(hp(t), gathers=cfg.gathers)
+        host_out.copy_(unit.shard_out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+
+    if world_size > 1:
+        red = torch.tensor([step_ms, rsa_ms, e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(red, op=dist.ReduceOp.MAX)
+        step_ms, rsa_ms, e2e_ms = red.tolist()
+
+    if rank != 0:
+        if world_size > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peak()
+    achieved = rsa_b / (rsa_ms * 1e-3) / 1e9
+    workload = WORKLOAD_NAMES[cfg.name]
+    traffic = recorded_traffic(workload)
+    total_bytes = (rsa_b + ag_b) * world_size
+    result = {
+        "metric": METRIC,
+        "value": round(total_bytes / (step_ms * 1e-3) / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world_size,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; no dataset or weights)",
+        "config": {
+            "workload": workload, "params": unit.numel, "padded_numel": P_pad, "world": N,
+            "grad_dtype": cfg.grad_dtype, "out_dtype": cfg.out_dtype, "gathers_per_step": cfg.gathers,
+            "bytes_per_step": rsa_b + ag_b, "fused_bytes_per_launch": rsa_b,
+            "l2": "inputs larger than L2 (no flush needed)" if rsa_b > 4 * 129e6 else "L2 flushed",
+            "units_per_gpu": 1,
+        },
+        "params_per_s": round(P_pad * world_size / (step_ms * 1e-3), 1),
+        "fused_params_per_s": round(P_pad / (rsa_ms * 1e-3), 1),
+        "roofline": {
+            "bound": "hbm", "kernel": "rsa_kernel (fused reduce-scatter + AdamW + cast)",
+            "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "fused_ms": round(rsa_ms, 4),
+        },
+        "e2e": {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 3), "steps": Ke,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+    }
+    if world_size == 1 and not args.no_cpu_baseline:
+        n_s = min(unit.numel, args.cpu_sample)
+        gbs, el, done, threads = oracle_sample_run(cfg, n_s, 1, 1, args.cpu_seconds)
+        result["cpu_baseline"] = {
+            "value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{done} steps of a {n_s}-element unit with the workload's N, dtypes, distributions and "
+                      f"all-gathers ({el:.1f} s)"}
+    print(json.dumps(result), flush=True)
+    if world_size > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args):
+    import fsdp_inputs as fi
+
+    rank, _, world_size = dist_env()
+    if rank != 0:
+        return  # the CPU oracle runs on rank 0 only
+    cfg = fi.CONFIGS[args.config]
+    n_s = min(fi.unit_numel(cfg), args.ref_sample)
+    gbs, el, done, threads = oracle_sample_run(cfg, n_s, args.steps, args.warmup, None)
+    workload = WORKLOAD_NAMES[cfg.name]
+    sample = f"each step: a {n_s}-element unit with the workload's N, dtypes, distributions and all-gathers"
+    print(json.dumps({
+        "impl": "reference",
+        "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world_size,
+        "steps": done, "warmup": args.warmup, "ms_per_step": round(el / done * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; no dataset or weights)",
+        "config": {"workload": workload, "world": cfg.world, "grad_dtype": cfg.grad_dtype,
+                   "out_dtype": cfg.out_dtype, "gathers_per_step": cfg.gathers, "sample_numel": n_s},
+        "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="llama70b", choices=sorted(WORKLOAD_NAMES))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=1 << 24, help="elements in the CPU-baseline sample")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline time budget")
+    ap.add_argument("--ref-sample", type=int, default=1 << 22, help="elements per reference-arm step")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    _, _, world_size = dist_env()
+    if args.gpus != world_size:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world_size}: launch N>1 with torchrun")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

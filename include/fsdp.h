@@ -1,0 +1,182 @@
+/*
+ * fsdp.h -- C ABI of libfsdpreduce.so, the FSDP FlatParameter step on one
+ * GB300 (sm_103a).
+ *
+ * One FSDP unit's step, as the sources describe it:
+ *   "Fully Sharded Data Parallel: faster AI training with fewer GPUs"
+ *   (techreport.ngo), "From all-reduce to sharded parameters": the DDP
+ *   all-reduce splits into a reduce-scatter (gradients summed in equal blocks,
+ *   block r to rank r) and an all-gather; each rank updates only its own
+ *   shard of the weights; the result is identical to DDP.
+ *   "FSDP (Fully Sharded Data Parallel)" (vanos001.github.io), "The Sharding
+ *   Scheme", "The Per-Layer Communication", "Mixed Precision and FSDP":
+ *   P/N parameter, gradient and fp32 Adam-state shards per rank; all-gather
+ *   before forward and backward, reduce-scatter after backward; bf16 compute
+ *   copy with fp32 master weights.
+ *   "Data Parallelism" (vanos001.github.io), "The Basic Protocol":
+ *   G_avg = (1/N) sum_i G_i; W = W - lr * Adam(G_avg, m, v).
+ *   "fairseq ... FSDP 实战指南" (zskr.cn), "参数定义与底层实现" and
+ *   "限制与兼容性说明": fp32 reduce-scatter option, fp16 compute dtype, and
+ *   exactness for pointwise optimizers such as AdamW.
+ *
+ * Emulation. The N ranks of one unit live in one GPU's memory: rank q's
+ * gradient is its own flat buffer; the fp32 master, exp_avg (m) and
+ * exp_avg_sq (v) of all ranks are the concatenation of the N shards, so rank
+ * r's shard is elements [r*S, (r+1)*S) of each, S = P_pad / N. A call may
+ * emulate any contiguous subset of ranks [rank_begin, rank_end).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named "device" are CUDA device addresses of the current device;
+ *    pointer arrays themselves (grads, srcs, full_bufs) are HOST arrays of
+ *    device addresses. The caller owns every buffer; the library allocates
+ *    no device memory and keeps no state besides a per-device cache of the
+ *    SM count.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Device work is enqueued on it and the call returns without
+ *    synchronizing.
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call returns an error status and enqueues nothing. A launch
+ *    failure returns FSDP_ERR_CUDA; fsdp_last_cuda_error() then gives the
+ *    cudaError_t value. Nothing aborts, traps or prints.
+ *  - Element pointers must be aligned to their element size. Any such
+ *    alignment works; 16-byte-aligned bases take the vectorised path.
+ */
+#ifndef FSDP_H
+#define FSDP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FSDP_MAX_WORLD 64 /* largest N (emulated ranks) and largest all-gather fan-out */
+#define FSDP_MAX_NDIM 8   /* largest rank of an original parameter's shape */
+
+typedef enum {
+    FSDP_OK = 0,
+    FSDP_ERR_INVALID_ARG = 1,       /* null pointer, bad size, bad range, aliasing, ... */
+    FSDP_ERR_ALIGNMENT = 2,         /* a pointer not aligned to its element size */
+    FSDP_ERR_CUDA = 3,              /* a CUDA call or kernel launch failed */
+    FSDP_ERR_UNSUPPORTED_DTYPE = 4  /* dtype not accepted by this entry point */
+} fsdp_status;
+
+typedef enum { FSDP_F32 = 0, FSDP_BF16 = 1, FSDP_F16 = 2 } fsdp_dtype;
+
+/* A view of one original parameter inside a FlatParameter ("FSDP (Fully
+ * Sharded Data Parallel)", "Common Pitfalls": use_orig_params keeps
+ * named-parameter access as views into the flat parameter). */
+typedef struct {
+    int32_t ndim;
+    int32_t reserved;               /* 0 */
+    int64_t shape[FSDP_MAX_NDIM];   /* dims beyond ndim are 0 */
+    int64_t offset;                 /* first element inside the flat buffer */
+    int64_t numel;                  /* product of shape[0..ndim) (1 for ndim 0) */
+} fsdp_view;
+
+/* AdamW hyperparameters of one step. One parameter group per unit: the same
+ * values apply to every element, biases and norm weights included ("Fully
+ * Sharded Data Parallel: ...", "Harnessing FSDP's full power", item 3). */
+typedef struct {
+    float lr;
+    float beta1;
+    float beta2;
+    float eps;
+    float weight_decay;  /* decoupled: p <- p * (1 - lr * weight_decay) */
+    int64_t step;        /* t, 1 on the first step */
+    float grad_scale;    /* static loss scale the gradients carry; 1 if none */
+} fsdp_adamw_hparams;
+
+/* ceil(numel / world) * world: the FlatParameter length after zero padding
+ * at the end, so that it splits into `world` equal shards. Returns -1 when
+ * numel < 0 or world < 1. Host only. */
+int64_t fsdp_padded_numel(int64_t numel, int world);
+
+/* Layout of a FlatParameter, host only, touches no GPU.
+ * shapes: the n_tensors shapes concatenated (ndims[k] entries for tensor k,
+ * in registration order; ndims[k] in [0, FSDP_MAX_NDIM], negative dims are
+ * invalid). Writes n_tensors views (offset = sum of the previous numels, no
+ * gaps) to views_out and the padded length to *padded_numel_out.
+ * Source: "Fully Sharded Data Parallel: ...", "Harnessing FSDP's full
+ * power", item 3 (a unit's parameters are flattened into a single tensor);
+ * "FSDP (Fully Sharded Data Parallel)", "Common Pitfalls" (views of the
+ * original parameters). */
+fsdp_status fsdp_unflatten_views(const int64_t *shapes, const int32_t *ndims, int n_tensors,
+                                 int world, fsdp_view *views_out, int64_t *padded_numel_out);
+
+/* Flatten and pad (device). Copies n_tensors contiguous device tensors of
+ * `dtype` (srcs[k] holds numels[k] elements) back to back into dst_flat and
+ * zero-fills the padding [sum(numels), dst_numel). dst_numel must equal
+ * fsdp_padded_numel(sum(numels), world). Sources must not overlap dst_flat.
+ * views_out (host, may be NULL) receives one 1-D view per tensor.
+ * Same sources as fsdp_unflatten_views. */
+fsdp_status fsdp_flatten_pad(const void *const *srcs, const int64_t *numels, int n_tensors,
+                             fsdp_dtype dtype, int world, void *dst_flat, int64_t dst_numel,
+                             fsdp_view *views_out, void *stream);
+
+/* The fused reduce-scatter + AdamW + cast (device), for emulated ranks
+ * r in [rank_begin, rank_end), i in [0, S), j = r*S + i:
+ *   acc  = G_0[j] + G_1[j] + ... + G_{N-1}[j]   fp32, ranks in order 0..N-1
+ *   g    = acc * c,            c = fp32(1 / (N * grad_scale))
+ *   p    = master[j] * fp32(1 - lr*weight_decay)
+ *   m    = beta1 * m[j] + fp32(1 - beta1) * g
+ *   v    = beta2 * v[j] + fp32(1 - beta2) * (g * g)
+ *   p    = p - alpha * (m / (sqrt(v) / b2s + eps)),
+ *          alpha = fp32(lr / (1 - beta1^t)), b2s = fp32(sqrt(1 - beta2^t))
+ *   master[j], exp_avg[j], exp_avg_sq[j] = p, m, v   (in place)
+ *   shard_out[j] = p rounded to nearest even in out_dtype
+ * every operation rounded to fp32 on its own (no fused multiply-add); the
+ * scalars are computed in double and rounded once. Elements outside the
+ * emulated ranks' blocks are not touched.
+ * Sources: the reduce-scatter is "From all-reduce to sharded parameters"
+ * (first figure caption) with the average of "The Basic Protocol" and the
+ * fp32 accumulation of --fp32-reduce-scatter; the update is the pointwise
+ * AdamW step on the local shard ("限制与兼容性说明", second figure caption
+ * of "From all-reduce to sharded parameters"); the cast is the compute copy
+ * of "Mixed Precision and FSDP". The AdamW formula, the reduction order and
+ * the single multiply by c are this library's reading (the pages print none).
+ *
+ *   grads        host array of `world` device pointers, each padded_numel
+ *                elements of grad_dtype (F32, BF16 or F16); read only.
+ *   padded_numel P_pad, a multiple of world (0 is a no-op).
+ *   master, exp_avg, exp_avg_sq   device fp32, padded_numel each, in place.
+ *   shard_out    device, padded_numel elements of out_dtype (F32, BF16,
+ *                F16); must not overlap the gradients or the state.
+ *   hp           host; step >= 1, grad_scale > 0.
+ *   rank_begin, rank_end   0 <= rank_begin <= rank_end <= world.
+ *   nonfinite_count  device uint32 or NULL: incremented by the number of
+ *                elements whose averaged gradient g is not finite (reported,
+ *                never skipped); the caller zeroes it.
+ */
+fsdp_status fsdp_reduce_scatter_adam_cast(const void *const *grads, fsdp_dtype grad_dtype,
+                                          int world, int64_t padded_numel, float *master,
+                                          float *exp_avg, float *exp_avg_sq, void *shard_out,
+                                          fsdp_dtype out_dtype, const fsdp_adamw_hparams *hp,
+                                          int rank_begin, int rank_end,
+                                          uint32_t *nonfinite_count, void *stream);
+
+/* All-gather (device): every destination receives the whole rank-ordered
+ * concatenation of the shards, full_k[j] = shard_out[j] for j < padded_numel,
+ * k < n_dst. Rank r's shard is shard_out[r*S, (r+1)*S), so the copy is the
+ * all-gather of "From all-reduce to sharded parameters" (first figure
+ * caption) and of "The Per-Layer Communication" (before forward and before
+ * backward), one destination per emulated rank.
+ *   shard_out    device, padded_numel elements of dtype (any of the three).
+ *   full_bufs    host array of n_dst device pointers (1 <= n_dst <=
+ *                FSDP_MAX_WORLD), padded_numel elements each; they must not
+ *                overlap shard_out or each other.
+ *   world        N; padded_numel must be a multiple of it. */
+fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
+                            int64_t padded_numel, void *const *full_bufs, int n_dst, void *stream);
+
+/* Human-readable name of a status. Never NULL. */
+const char *fsdp_status_string(fsdp_status status);
+
+/* cudaError_t value behind the calling thread's last FSDP_ERR_CUDA (0 if none). */
+int fsdp_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FSDP_H */

@@ -1,0 +1,81 @@
+"""ctypes loader for libfsdpreduce.so and the C structs of include/fsdp.h.
+
+Loading fails loudly (RuntimeError) when the library has not been built: there
+is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfsdpreduce.so")
+
+FSDP_MAX_WORLD = 64
+FSDP_MAX_NDIM = 8
+
+FSDP_OK = 0
+FSDP_ERR_INVALID_ARG = 1
+FSDP_ERR_ALIGNMENT = 2
+FSDP_ERR_CUDA = 3
+FSDP_ERR_UNSUPPORTED_DTYPE = 4
+
+FSDP_F32, FSDP_BF16, FSDP_F16 = 0, 1, 2
+
+# every symbol include/fsdp.h declares
+EXPORTS = (
+    "fsdp_padded_numel",
+    "fsdp_unflatten_views",
+    "fsdp_flatten_pad",
+    "fsdp_reduce_scatter_adam_cast",
+    "fsdp_all_gather",
+    "fsdp_status_string",
+    "fsdp_last_cuda_error",
+)
+
+
+class FsdpView(ctypes.Structure):
+    _fields_ = [("ndim", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * FSDP_MAX_NDIM), ("offset", ctypes.c_int64),
+                ("numel", ctypes.c_int64)]
+
+
+class FsdpAdamwHparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64),
+                ("grad_scale", ctypes.c_float)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load the in-tree CUDA library (build it first with ``build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: the CUDA library must be built "
+                "(python -c 'import __graft_entry__ as g; g.build()'); there is no fallback")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        sigs = {
+            "fsdp_padded_numel": (i64, [i64, i32]),
+            "fsdp_unflatten_views": (i32, [vp, vp, i32, i32, ctypes.POINTER(FsdpView), ctypes.POINTER(i64)]),
+            "fsdp_flatten_pad": (i32, [vp, vp, i32, i32, i32, vp, i64, ctypes.POINTER(FsdpView), vp]),
+            "fsdp_reduce_scatter_adam_cast": (i32, [vp, i32, i32, i64, vp, vp, vp, vp, i32,
+                                                    ctypes.POINTER(FsdpAdamwHparams), i32, i32, vp, vp]),
+            "fsdp_all_gather": (i32, [vp, i32, i32, i64, vp, i32, vp]),
+            "fsdp_status_string": (ctypes.c_char_p, [i32]),
+            "fsdp_last_cuda_error": (i32, []),
+        }
+        for name, (res, args) in sigs.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib

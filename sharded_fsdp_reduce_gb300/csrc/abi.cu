@@ -1,0 +1,259 @@
+// abi.cu -- the extern "C" entry points of libfsdpreduce.so (declared in
+// include/fsdp.h): argument validation, the per-step scalars, and dispatch to
+// the kernels. Every check runs on the host before anything is enqueued.
+#include <math.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "common.cuh"
+
+namespace fsdp {
+
+namespace {
+thread_local int g_last_cuda_error = 0;
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];  // per device ordinal, 0 = not queried
+}  // namespace
+
+fsdp_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return FSDP_OK;
+    g_last_cuda_error = static_cast<int>(e);
+    return FSDP_ERR_CUDA;
+}
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+    const int slot = dev < kMaxDevices ? dev : 0;
+    int n = g_sm_count[slot].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+        g_sm_count[slot].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+namespace {
+
+// Per-step scalars from the hyperparameters: computed in double, rounded
+// once to float (the kernel then works in fp32 only).
+AdamScalars make_scalars(const fsdp_adamw_hparams &h, int world) {
+    const double t = static_cast<double>(h.step);
+    AdamScalars s;
+    s.c = static_cast<float>(1.0 / (static_cast<double>(world) * static_cast<double>(h.grad_scale)));
+    s.decay = static_cast<float>(1.0 - static_cast<double>(h.lr) * static_cast<double>(h.weight_decay));
+    s.beta1 = h.beta1;
+    s.beta2 = h.beta2;
+    s.omb1 = static_cast<float>(1.0 - static_cast<double>(h.beta1));
+    s.omb2 = static_cast<float>(1.0 - static_cast<double>(h.beta2));
+    s.alpha = static_cast<float>(static_cast<double>(h.lr) / (1.0 - pow(static_cast<double>(h.beta1), t)));
+    s.b2s = static_cast<float>(sqrt(1.0 - pow(static_cast<double>(h.beta2), t)));
+    s.eps = h.eps;
+    return s;
+}
+
+bool mul_overflows(int64_t a, int64_t b) { return a != 0 && b > INT64_MAX / a; }
+
+}  // namespace
+}  // namespace fsdp
+
+using namespace fsdp;
+
+extern "C" {
+
+int64_t fsdp_padded_numel(int64_t numel, int world) {
+    if (numel < 0 || world < 1) return -1;
+    int64_t shards = numel / world;
+    if (shards * world < numel) shards += 1;
+    return shards * world;
+}
+
+fsdp_status fsdp_unflatten_views(const int64_t *shapes, const int32_t *ndims, int n_tensors, int world,
+                                 fsdp_view *views_out, int64_t *padded_numel_out) {
+    if (n_tensors < 0 || world < 1 || !padded_numel_out) return FSDP_ERR_INVALID_ARG;
+    if (n_tensors > 0 && (!ndims || !views_out)) return FSDP_ERR_INVALID_ARG;
+    int64_t at = 0;
+    for (int k = 0; k < n_tensors; ++k) {
+        if (ndims[k] < 0 || ndims[k] > FSDP_MAX_NDIM) return FSDP_ERR_INVALID_ARG;
+        if (ndims[k] > 0 && !shapes) return FSDP_ERR_INVALID_ARG;
+    }
+    int64_t offset = 0;
+    for (int k = 0; k < n_tensors; ++k) {
+        fsdp_view v;
+        memset(&v, 0, sizeof(v));
+        v.ndim = ndims[k];
+        int64_t numel = 1;
+        for (int d = 0; d < ndims[k]; ++d) {
+            const int64_t dim = shapes[at + d];
+            if (dim < 0 || mul_overflows(numel, dim)) return FSDP_ERR_INVALID_ARG;
+            v.shape[d] = dim;
+            numel *= dim;
+        }
+        at += ndims[k];
+        if (offset > INT64_MAX - numel) return FSDP_ERR_INVALID_ARG;
+        v.offset = offset;
+        v.numel = numel;
+        offset += numel;
+        views_out[k] = v;
+    }
+    const int64_t padded = fsdp_padded_numel(offset, world);
+    if (padded < 0) return FSDP_ERR_INVALID_ARG;
+    *padded_numel_out = padded;
+    return FSDP_OK;
+}
+
+fsdp_status fsdp_flatten_pad(const void *const *srcs, const int64_t *numels, int n_tensors, fsdp_dtype dtype,
+                             int world, void *dst_flat, int64_t dst_numel, fsdp_view *views_out,
+                             void *stream) {
+    if (!dtype_valid(dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
+    if (n_tensors < 0 || world < 1 || dst_numel < 0) return FSDP_ERR_INVALID_ARG;
+    if (n_tensors > 0 && (!srcs || !numels)) return FSDP_ERR_INVALID_ARG;
+    const size_t es = static_cast<size_t>(dtype_size(dtype));
+    int64_t total = 0;
+    for (int k = 0; k < n_tensors; ++k) {
+        if (numels[k] < 0 || total > INT64_MAX - numels[k]) return FSDP_ERR_INVALID_ARG;
+        if (numels[k] > 0 && !srcs[k]) return FSDP_ERR_INVALID_ARG;
+        total += numels[k];
+    }
+    const int64_t padded = fsdp_padded_numel(total, world);
+    if (padded != dst_numel || mul_overflows(padded, static_cast<int64_t>(es))) return FSDP_ERR_INVALID_ARG;
+    if (padded > 0 && !dst_flat) return FSDP_ERR_INVALID_ARG;
+    if (dst_flat && !aligned(dst_flat, es)) return FSDP_ERR_ALIGNMENT;
+    for (int k = 0; k < n_tensors; ++k) {
+        if (numels[k] == 0) continue;
+        if (!aligned(srcs[k], es)) return FSDP_ERR_ALIGNMENT;
+        if (overlaps(srcs[k], numels[k] * es, dst_flat, padded * es)) return FSDP_ERR_INVALID_ARG;
+    }
+    if (views_out) {
+        int64_t off = 0;
+        for (int k = 0; k < n_tensors; ++k) {
+            fsdp_view v;
+            memset(&v, 0, sizeof(v));
+            v.ndim = 1;
+            v.shape[0] = numels[k];
+            v.offset = off;
+            v.numel = numels[k];
+            views_out[k] = v;
+            off += numels[k];
+        }
+    }
+    // segments: each tensor, then the zero padding
+    FlattenArgs a;
+    memset(&a, 0, sizeof(a));
+    a.dst = dst_flat;
+    a.elem_size = static_cast<int>(es);
+    int64_t off = 0;
+    for (int k = 0; k <= n_tensors; ++k) {
+        const bool pad = k == n_tensors;
+        const int64_t n = pad ? padded - total : numels[k];
+        if (n > 0) {
+            a.src[a.count] = pad ? nullptr : srcs[k];
+            a.dst_byte_off[a.count] = off * static_cast<int64_t>(es);
+            a.nbytes[a.count] = n * static_cast<int64_t>(es);
+            a.count += 1;
+        }
+        off += n;
+        if (a.count == FlattenArgs::kBatch || (pad && a.count > 0)) {
+            const fsdp_status st = launch_flatten(a, static_cast<cudaStream_t>(stream));
+            if (st != FSDP_OK) return st;
+            a.count = 0;
+        }
+    }
+    return FSDP_OK;
+}
+
+fsdp_status fsdp_reduce_scatter_adam_cast(const void *const *grads, fsdp_dtype grad_dtype, int world,
+                                          int64_t padded_numel, float *master, float *exp_avg,
+                                          float *exp_avg_sq, void *shard_out, fsdp_dtype out_dtype,
+                                          const fsdp_adamw_hparams *hp, int rank_begin, int rank_end,
+                                          uint32_t *nonfinite_count, void *stream) {
+    if (!dtype_valid(grad_dtype) || !dtype_valid(out_dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
+    if (world < 1 || world > FSDP_MAX_WORLD || !grads || !hp) return FSDP_ERR_INVALID_ARG;
+    if (padded_numel < 0 || padded_numel % world != 0) return FSDP_ERR_INVALID_ARG;
+    if (rank_begin < 0 || rank_begin > rank_end || rank_end > world) return FSDP_ERR_INVALID_ARG;
+    if (hp->step < 1 || !(hp->grad_scale > 0.0f) || !isfinite(hp->grad_scale)) return FSDP_ERR_INVALID_ARG;
+    if (mul_overflows(padded_numel, 4)) return FSDP_ERR_INVALID_ARG;
+    const int64_t S = padded_numel / world;
+    const int64_t begin = static_cast<int64_t>(rank_begin) * S, end = static_cast<int64_t>(rank_end) * S;
+    if (begin == end) return FSDP_OK;
+    if (!master || !exp_avg || !exp_avg_sq || !shard_out) return FSDP_ERR_INVALID_ARG;
+    const size_t gs = static_cast<size_t>(dtype_size(grad_dtype)), os = static_cast<size_t>(dtype_size(out_dtype));
+    const size_t state_bytes = static_cast<size_t>(padded_numel) * 4;
+    if (!aligned(master, 4) || !aligned(exp_avg, 4) || !aligned(exp_avg_sq, 4) || !aligned(shard_out, os))
+        return FSDP_ERR_ALIGNMENT;
+    if (nonfinite_count && !aligned(nonfinite_count, 4)) return FSDP_ERR_ALIGNMENT;
+    const void *state[3] = {master, exp_avg, exp_avg_sq};
+    for (int i = 0; i < 3; ++i) {
+        for (int k = i + 1; k < 3; ++k)
+            if (overlaps(state[i], state_bytes, state[k], state_bytes)) return FSDP_ERR_INVALID_ARG;
+        if (overlaps(state[i], state_bytes, shard_out, padded_numel * os)) return FSDP_ERR_INVALID_ARG;
+    }
+    RsaArgs a;
+    memset(&a, 0, sizeof(a));
+    for (int q = 0; q < world; ++q) {
+        if (!grads[q]) return FSDP_ERR_INVALID_ARG;
+        if (!aligned(grads[q], gs)) return FSDP_ERR_ALIGNMENT;
+        if (overlaps(grads[q], padded_numel * gs, shard_out, padded_numel * os)) return FSDP_ERR_INVALID_ARG;
+        for (int i = 0; i < 3; ++i)
+            if (overlaps(grads[q], padded_numel * gs, state[i], state_bytes)) return FSDP_ERR_INVALID_ARG;
+        a.grads[q] = grads[q];
+    }
+    a.master = master;
+    a.m = exp_avg;
+    a.v = exp_avg_sq;
+    a.out = shard_out;
+    a.nonfinite = nonfinite_count;
+    a.begin = begin;
+    a.end = end;
+    a.s = make_scalars(*hp, world);
+    a.world = world;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (grad_dtype) {
+        case FSDP_BF16: return launch_rsa_bf16(a, out_dtype, s);
+        case FSDP_F16: return launch_rsa_f16(a, out_dtype, s);
+        default: return launch_rsa_f32(a, out_dtype, s);
+    }
+}
+
+fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world, int64_t padded_numel,
+                            void *const *full_bufs, int n_dst, void *stream) {
+    if (!dtype_valid(dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
+    if (world < 1 || padded_numel < 0 || padded_numel % world != 0) return FSDP_ERR_INVALID_ARG;
+    if (n_dst < 1 || n_dst > FSDP_MAX_WORLD || !full_bufs) return FSDP_ERR_INVALID_ARG;
+    const size_t es = static_cast<size_t>(dtype_size(dtype));
+    if (mul_overflows(padded_numel, static_cast<int64_t>(es))) return FSDP_ERR_INVALID_ARG;
+    if (padded_numel == 0) return FSDP_OK;
+    const size_t nbytes = static_cast<size_t>(padded_numel) * es;
+    if (!shard_out) return FSDP_ERR_INVALID_ARG;
+    if (!aligned(shard_out, es)) return FSDP_ERR_ALIGNMENT;
+    GatherArgs a;
+    memset(&a, 0, sizeof(a));
+    a.src = shard_out;
+    a.nbytes = static_cast<int64_t>(nbytes);
+    a.n_dst = n_dst;
+    for (int d = 0; d < n_dst; ++d) {
+        if (!full_bufs[d]) return FSDP_ERR_INVALID_ARG;
+        if (!aligned(full_bufs[d], es)) return FSDP_ERR_ALIGNMENT;
+        if (overlaps(full_bufs[d], nbytes, shard_out, nbytes)) return FSDP_ERR_INVALID_ARG;
+        for (int e = 0; e < d; ++e)
+            if (overlaps(full_bufs[d], nbytes, full_bufs[e], nbytes)) return FSDP_ERR_INVALID_ARG;
+        a.dst[d] = full_bufs[d];
+    }
+    return launch_gather(a, static_cast<cudaStream_t>(stream));
+}
+
+const char *fsdp_status_string(fsdp_status status) {
+    switch (status) {
+        case FSDP_OK: return "FSDP_OK";
+        case FSDP_ERR_INVALID_ARG: return "FSDP_ERR_INVALID_ARG: invalid argument";
+        case FSDP_ERR_ALIGNMENT: return "FSDP_ERR_ALIGNMENT: pointer not aligned to its element size";
+        case FSDP_ERR_CUDA: return "FSDP_ERR_CUDA: a CUDA call or kernel launch failed";
+        case FSDP_ERR_UNSUPPORTED_DTYPE: return "FSDP_ERR_UNSUPPORTED_DTYPE: unsupported dtype";
+        default: return "FSDP_ERR_UNKNOWN: unknown status";
+    }
+}
+
+int fsdp_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

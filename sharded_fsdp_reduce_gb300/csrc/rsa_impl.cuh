@@ -1,0 +1,232 @@
+// rsa_impl.cuh -- the fused reduce-scatter + AdamW + cast kernel ("K_RSA").
+//
+// One pass over the emulated ranks' blocks [begin, end) of the FlatParameter.
+// For each element j it reads the N gradient values G_q[j] (rank order), the
+// fp32 master / exp_avg / exp_avg_sq, and writes the three updated state
+// values and the compute-dtype copy. Nothing else is read or written, so the
+// algorithmic traffic per element is N*sizeof(grad) + 3*(4+4) + sizeof(out)
+// bytes and the kernel is bound by HBM bandwidth (about 0.4 flop per byte).
+//
+// Sources: "Fully Sharded Data Parallel: faster AI training with fewer GPUs",
+// "From all-reduce to sharded parameters" (reduce-scatter by rank block, local
+// shard update); "Data Parallelism", "The Basic Protocol" (average by 1/N, then
+// the Adam step); "fairseq ... FSDP 实战指南", "参数定义与底层实现"
+// (--fp32-reduce-scatter) and "限制与兼容性说明" (pointwise optimizers);
+// "FSDP (Fully Sharded Data Parallel)", "Mixed Precision and FSDP" (fp32
+// master and state, bf16 compute copy).
+//
+// Layout per thread and iteration: 8 consecutive elements. Each rank's 8
+// bf16/fp16 gradients are one 16-byte load; master, m and v are two 16-byte
+// loads each; the 8 outputs are one 16-byte store. All loads of an iteration
+// are issued before any arithmetic so that each thread keeps N+6 16-byte
+// requests in flight. Elements before the first 8-aligned index and after the
+// last one (and every element when a base pointer is not 16-byte aligned) go
+// through the scalar path, which performs the same operations in the same
+// order.
+#pragma once
+
+#include "common.cuh"
+
+namespace fsdp {
+namespace rsa {
+
+constexpr int kThreads = 256;
+
+// AdamW on one element; each operation is rounded on its own (no FMA), in the
+// order of the documented definition.
+__device__ __forceinline__ void adamw(float g, float &p, float &m, float &v, const AdamScalars &s) {
+    p = __fmul_rn(p, s.decay);
+    m = __fadd_rn(__fmul_rn(s.beta1, m), __fmul_rn(s.omb1, g));
+    v = __fadd_rn(__fmul_rn(s.beta2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
+    const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.b2s), s.eps);
+    p = __fsub_rn(p, __fmul_rn(s.alpha, __fdiv_rn(m, denom)));
+}
+
+__device__ __forceinline__ uint32_t nonfinite(float g) { return isfinite(g) ? 0u : 1u; }
+
+// One element through the plain path.
+template <int GD, int OD>
+__device__ __forceinline__ uint32_t scalar_elem(const RsaArgs &a, int world, int64_t j) {
+    float acc = Dtype<GD>::load(a.grads[0], j);
+    for (int q = 1; q < world; ++q) acc = __fadd_rn(acc, Dtype<GD>::load(a.grads[q], j));
+    const float g = __fmul_rn(acc, a.s.c);
+    float p = a.master[j], m = a.m[j], v = a.v[j];
+    adamw(g, p, m, v, a.s);
+    a.master[j] = p;
+    a.m[j] = m;
+    a.v[j] = v;
+    Dtype<OD>::store(a.out, j, p);
+    return nonfinite(g);
+}
+
+// Average, AdamW and cast of one 8-element chunk whose gradient sum is acc.
+template <int OD>
+__device__ __forceinline__ uint32_t finish_chunk(const RsaArgs &a, int64_t j0, const float *acc,
+                                                 float4 p0, float4 p1, float4 m0, float4 m1,
+                                                 float4 v0, float4 v1) {
+    float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t bad = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float g = __fmul_rn(acc[e], a.s.c);
+        bad += nonfinite(g);
+        adamw(g, p[e], m[e], v[e], a.s);
+    }
+    st_state(a.master + j0, make_float4(p[0], p[1], p[2], p[3]));
+    st_state(a.master + j0 + 4, make_float4(p[4], p[5], p[6], p[7]));
+    st_state(a.m + j0, make_float4(m[0], m[1], m[2], m[3]));
+    st_state(a.m + j0 + 4, make_float4(m[4], m[5], m[6], m[7]));
+    st_state(a.v + j0, make_float4(v[0], v[1], v[2], v[3]));
+    st_state(a.v + j0 + 4, make_float4(v[4], v[5], v[6], v[7]));
+    if constexpr (OD == FSDP_F32) {
+        float *o = static_cast<float *>(a.out) + j0;
+        st_state(o, make_float4(p[0], p[1], p[2], p[3]));
+        st_state(o + 4, make_float4(p[4], p[5], p[6], p[7]));
+    } else {
+        const uint4 o = make_uint4(pack2<OD>(p[0], p[1]), pack2<OD>(p[2], p[3]),
+                                   pack2<OD>(p[4], p[5]), pack2<OD>(p[6], p[7]));
+        st_stream(static_cast<uint16_t *>(a.out) + j0, o);
+    }
+    return bad;
+}
+
+// Gradient registers of one 8-element chunk: one 16-byte word per rank for
+// bf16/fp16, two for fp32.
+template <int NW, int GD> struct GradRegs {
+    static constexpr int kWords = GD == FSDP_F32 ? 2 : 1;
+    uint4 w[NW > 0 ? NW : 1][kWords];
+};
+
+template <int GD>
+__device__ __forceinline__ void load_grad8(const void *gq, int64_t j0, uint4 *w) {
+    if constexpr (GD == FSDP_F32) {
+        w[0] = ld_stream(static_cast<const float *>(gq) + j0);
+        w[1] = ld_stream(static_cast<const float *>(gq) + j0 + 4);
+    } else {
+        w[0] = ld_stream(static_cast<const uint16_t *>(gq) + j0);
+    }
+}
+
+template <int GD> __device__ __forceinline__ void widen8(const uint4 *w, float *f) {
+    if constexpr (GD == FSDP_F32) {
+        const uint32_t u[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(u[e]);
+    } else {
+        unpack8<GD>(w[0], f);
+    }
+}
+
+template <int NW, int GD, int OD>
+__device__ __forceinline__ uint32_t vec_chunk(const RsaArgs &a, int world, int64_t j0) {
+    float acc[8];
+    if constexpr (NW > 0) {
+        // every load of the chunk (N gradient words, then the state) is in
+        // flight before the first add
+        GradRegs<NW, GD> r;
+#pragma unroll
+        for (int q = 0; q < NW; ++q) load_grad8<GD>(a.grads[q], j0, r.w[q]);
+        const float4 p0 = ld_state(a.master + j0), p1 = ld_state(a.master + j0 + 4);
+        const float4 m0 = ld_state(a.m + j0), m1 = ld_state(a.m + j0 + 4);
+        const float4 v0 = ld_state(a.v + j0), v1 = ld_state(a.v + j0 + 4);
+        widen8<GD>(r.w[0], acc);
+#pragma unroll
+        for (int q = 1; q < NW; ++q) {
+            float f[8];
+            widen8<GD>(r.w[q], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
+        }
+        return finish_chunk<OD>(a, j0, acc, p0, p1, m0, m1, v0, v1);
+    } else {
+        for (int q = 0; q < world; ++q) {
+            uint4 w[GradRegs<1, GD>::kWords];
+            load_grad8<GD>(a.grads[q], j0, w);
+            float f[8];
+            widen8<GD>(w, f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = q == 0 ? f[e] : __fadd_rn(acc[e], f[e]);
+        }
+        const float4 p0 = ld_state(a.master + j0), p1 = ld_state(a.master + j0 + 4);
+        const float4 m0 = ld_state(a.m + j0), m1 = ld_state(a.m + j0 + 4);
+        const float4 v0 = ld_state(a.v + j0), v1 = ld_state(a.v + j0 + 4);
+        return finish_chunk<OD>(a, j0, acc, p0, p1, m0, m1, v0, v1);
+    }
+}
+
+// Grid-stride over nchunks 8-element chunks starting at vbegin, then the
+// scalar elements [begin, vbegin) and [vend, end). With nchunks = 0 and
+// vbegin = vend = end every element takes the scalar path.
+template <int NW, int GD, int OD>
+__global__ void __launch_bounds__(kThreads)
+    rsa_kernel(const __grid_constant__ RsaArgs a, int64_t vbegin, int64_t nchunks, int64_t vend) {
+    const int world = NW > 0 ? NW : a.world;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    uint32_t bad = 0;
+    for (int64_t k = tid; k < nchunks; k += stride) bad += vec_chunk<NW, GD, OD>(a, world, vbegin + 8 * k);
+    const int64_t nhead = vbegin - a.begin;
+    const int64_t nrest = nhead + (a.end - vend);
+    for (int64_t e = tid; e < nrest; e += stride) {
+        const int64_t j = e < nhead ? a.begin + e : vend + (e - nhead);
+        bad += scalar_elem<GD, OD>(a, world, j);
+    }
+    if (a.nonfinite != nullptr) {
+        const uint32_t total = __reduce_add_sync(0xffffffffu, bad);
+        if ((threadIdx.x & 31) == 0 && total) atomicAdd(a.nonfinite, total);
+    }
+}
+
+template <int NW, int GD, int OD>
+fsdp_status launch_typed(const RsaArgs &a, cudaStream_t stream) {
+    static int blocks_per_sm = 0;  // occupancy of this instantiation (one device type)
+    if (blocks_per_sm == 0) {
+        int b = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, rsa_kernel<NW, GD, OD>, kThreads, 0);
+        if (e != cudaSuccess) return cuda_status(e);
+        blocks_per_sm = b > 0 ? b : 1;
+    }
+    bool vec = aligned(a.master, 16) && aligned(a.m, 16) && aligned(a.v, 16) && aligned(a.out, 16);
+    for (int q = 0; q < a.world; ++q) vec = vec && aligned(a.grads[q], 16);
+    int64_t vbegin = a.end, vend = a.end, nchunks = 0;
+    if (vec) {
+        vbegin = (a.begin + 7) / 8 * 8;
+        vend = a.end / 8 * 8;
+        if (vend > vbegin) {
+            nchunks = (vend - vbegin) / 8;
+        } else {
+            vbegin = vend = a.end;
+        }
+    }
+    const int64_t items = nchunks + (vbegin - a.begin) + (a.end - vend);
+    const int64_t need = (items + kThreads - 1) / kThreads;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
+    const int grid = static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
+    rsa_kernel<NW, GD, OD><<<grid, kThreads, 0, stream>>>(a, vbegin, nchunks, vend);
+    return check_launch();
+}
+
+template <int GD, int OD>
+fsdp_status launch_world(const RsaArgs &a, cudaStream_t stream) {
+    switch (a.world) {
+        case 2: return launch_typed<2, GD, OD>(a, stream);
+        case 4: return launch_typed<4, GD, OD>(a, stream);
+        case 8: return launch_typed<8, GD, OD>(a, stream);
+        default: return launch_typed<0, GD, OD>(a, stream);
+    }
+}
+
+template <int GD>
+fsdp_status launch_grad(const RsaArgs &a, int out_dtype, cudaStream_t stream) {
+    switch (out_dtype) {
+        case FSDP_BF16: return launch_world<GD, FSDP_BF16>(a, stream);
+        case FSDP_F16: return launch_world<GD, FSDP_F16>(a, stream);
+        case FSDP_F32: return launch_world<GD, FSDP_F32>(a, stream);
+        default: return FSDP_ERR_UNSUPPORTED_DTYPE;
+    }
+}
+
+}  // namespace rsa
+}  // namespace fsdp

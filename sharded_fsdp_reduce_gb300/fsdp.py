@@ -1,0 +1,188 @@
+"""Python binding of the C ABI in include/fsdp.h, one function per entry point
+with the same name. Argument marshalling only: every step of the path runs in
+the CUDA library; these functions turn torch tensors into device pointers and
+sizes, pass the current CUDA stream, and raise FsdpError on a non-OK status.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+from . import _lib
+from ._lib import FsdpAdamwHparams, FsdpView
+
+__all__ = [
+    "AdamWHParams", "FsdpError", "View",
+    "fsdp_padded_numel", "fsdp_unflatten_views", "fsdp_flatten_pad",
+    "fsdp_reduce_scatter_adam_cast", "fsdp_all_gather", "fsdp_status_string",
+    "fsdp_last_cuda_error", "dtype_code",
+]
+
+_DTYPES = {torch.float32: _lib.FSDP_F32, torch.bfloat16: _lib.FSDP_BF16, torch.float16: _lib.FSDP_F16}
+
+
+class FsdpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = fsdp_status_string(status)
+        if status == _lib.FSDP_ERR_CUDA:
+            msg += f" (cudaError {fsdp_last_cuda_error()})"
+        super().__init__(f"{where}: {msg}")
+        self.status = status
+
+
+@dataclasses.dataclass(frozen=True)
+class AdamWHParams:
+    lr: float
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.0
+    step: int = 1
+    grad_scale: float = 1.0
+
+    def to_c(self) -> FsdpAdamwHparams:
+        return FsdpAdamwHparams(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay,
+                                int(self.step), self.grad_scale)
+
+
+@dataclasses.dataclass(frozen=True)
+class View:
+    offset: int
+    numel: int
+    shape: Tuple[int, ...]
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    try:
+        return _DTYPES[dt]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {dt}; expected float32, bfloat16 or float16") from None
+
+
+def _check(status: int, where: str) -> None:
+    if status != _lib.FSDP_OK:
+        raise FsdpError(status, where)
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _ptrs(ts: Sequence[torch.Tensor], name: str):
+    return (ctypes.c_void_p * len(ts))(*[_dev(t, f"{name}[{i}]") for i, t in enumerate(ts)])
+
+
+def _views(c_views, n) -> List[View]:
+    return [View(int(c_views[k].offset), int(c_views[k].numel),
+                 tuple(int(c_views[k].shape[d]) for d in range(c_views[k].ndim))) for k in range(n)]
+
+
+def fsdp_status_string(status: int) -> str:
+    return _lib.load().fsdp_status_string(int(status)).decode()
+
+
+def fsdp_last_cuda_error() -> int:
+    return int(_lib.load().fsdp_last_cuda_error())
+
+
+def fsdp_padded_numel(numel: int, world: int) -> int:
+    return int(_lib.load().fsdp_padded_numel(int(numel), int(world)))
+
+
+def fsdp_unflatten_views(shapes: Sequence[Sequence[int]], world: int) -> Tuple[List[View], int]:
+    """Views (offset, numel, shape) of the parameters in a FlatParameter and its padded length."""
+    n = len(shapes)
+    dims = [int(d) for s in shapes for d in s]
+    c_dims = (ctypes.c_int64 * max(len(dims), 1))(*dims)
+    c_nd = (ctypes.c_int32 * max(n, 1))(*[len(s) for s in shapes])
+    c_views = (FsdpView * max(n, 1))()
+    padded = ctypes.c_int64(0)
+    _check(_lib.load().fsdp_unflatten_views(c_dims, c_nd, n, int(world), c_views, ctypes.byref(padded)),
+           "fsdp_unflatten_views")
+    return _views(c_views, n), int(padded.value)
+
+
+def fsdp_flatten_pad(tensors: Sequence[torch.Tensor], world: int, out: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, List[View]]:
+    """Flatten the tensors (one dtype, CUDA, contiguous) into a zero-padded flat buffer."""
+    if not tensors:
+        raise ValueError("fsdp_flatten_pad needs at least one tensor")
+    dt = tensors[0].dtype
+    if any(t.dtype != dt for t in tensors):
+        raise TypeError("all tensors of a unit must share one dtype")
+    total = sum(t.numel() for t in tensors)
+    padded = fsdp_padded_numel(total, world)
+    if out is None:
+        out = torch.empty(padded, dtype=dt, device=tensors[0].device)
+    elif out.dtype != dt or out.numel() != padded:
+        raise ValueError(f"out must hold {padded} elements of {dt}")
+    n = len(tensors)
+    c_views = (FsdpView * n)()
+    numels = (ctypes.c_int64 * n)(*[t.numel() for t in tensors])
+    _check(_lib.load().fsdp_flatten_pad(_ptrs(tensors, "tensors"), numels, n, dtype_code(dt), int(world),
+                                        _dev(out, "out"), out.numel(), c_views, _stream(stream)),
+           "fsdp_flatten_pad")
+    return out, _views(c_views, n)
+
+
+def fsdp_reduce_scatter_adam_cast(grads: Sequence[torch.Tensor], master: torch.Tensor, exp_avg: torch.Tensor,
+                                  exp_avg_sq: torch.Tensor, shard_out: torch.Tensor, hparams: AdamWHParams,
+                                  rank_begin: int = 0, rank_end: Optional[int] = None,
+                                  nonfinite_count: Optional[torch.Tensor] = None,
+                                  stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Fused reduce-scatter + AdamW + cast for the emulated ranks [rank_begin, rank_end).
+
+    grads: N tensors (or the rows of an [N, P_pad] tensor) of one dtype.
+    master / exp_avg / exp_avg_sq: fp32 [P_pad], updated in place.
+    shard_out: [P_pad] of the compute dtype; rank r writes [r*S, (r+1)*S).
+    nonfinite_count: optional CUDA uint32/int32 scalar, incremented by the
+    number of non-finite averaged gradient elements.
+    """
+    world = len(grads)
+    P_pad = master.numel()
+    gdt = grads[0].dtype if world else torch.bfloat16
+    for i, g in enumerate(grads):
+        if g.numel() != P_pad or g.dtype != gdt:
+            raise ValueError(f"grads[{i}] must hold {P_pad} elements of {gdt}")
+    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
+        if t.dtype != torch.float32 or t.numel() != P_pad:
+            raise ValueError(f"{name} must be float32 with {P_pad} elements")
+    if shard_out.numel() != P_pad:
+        raise ValueError(f"shard_out must hold {P_pad} elements")
+    nf = 0
+    if nonfinite_count is not None:
+        if nonfinite_count.dtype not in (torch.int32, torch.uint32) or nonfinite_count.numel() < 1:
+            raise ValueError("nonfinite_count must be a CUDA int32/uint32 tensor")
+        nf = _dev(nonfinite_count, "nonfinite_count")
+    hp = hparams.to_c()
+    rb = int(rank_begin)
+    re = world if rank_end is None else int(rank_end)
+    _check(_lib.load().fsdp_reduce_scatter_adam_cast(
+        _ptrs(grads, "grads") if world else None, dtype_code(gdt), world, P_pad,
+        _dev(master, "master"), _dev(exp_avg, "exp_avg"), _dev(exp_avg_sq, "exp_avg_sq"),
+        _dev(shard_out, "shard_out"), dtype_code(shard_out.dtype), ctypes.byref(hp), rb, re,
+        nf or None, _stream(stream)), "fsdp_reduce_scatter_adam_cast")
+
+
+def fsdp_all_gather(shard_out: torch.Tensor, full_bufs: Sequence[torch.Tensor], world: int,
+                    stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy the rank-ordered shards (shard_out, [P_pad]) into every full buffer."""
+    P_pad = shard_out.numel()
+    for i, f in enumerate(full_bufs):
+        if f.numel() != P_pad or f.dtype != shard_out.dtype:
+            raise ValueError(f"full_bufs[{i}] must hold {P_pad} elements of {shard_out.dtype}")
+    _check(_lib.load().fsdp_all_gather(_dev(shard_out, "shard_out"), dtype_code(shard_out.dtype), int(world),
+                                       P_pad, _ptrs(full_bufs, "full_bufs"), len(full_bufs), _stream(stream)),
+           "fsdp_all_gather")

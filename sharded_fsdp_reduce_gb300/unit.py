@@ -1,0 +1,86 @@
+"""One FSDP unit (FlatParameter) with N emulated ranks in one GPU's memory,
+and its stream-ordered step.
+
+The buffers are plain torch allocations; every operation on them is a call
+into the CUDA library. Per rank q: its flat gradient buffer (P_pad elements of
+the gradient dtype) and its gathered full-parameter buffer (P_pad elements of
+the compute dtype). Shared by all ranks, as the concatenation of their shards:
+the fp32 master weights, exp_avg (m), exp_avg_sq (v) and the compute-dtype
+shards (shard_out); rank r's shard is [r*S, (r+1)*S).
+
+The step of one unit ("FSDP (Fully Sharded Data Parallel)", "The Per-Layer
+Communication"; "Fully Sharded Data Parallel: faster AI training with fewer
+GPUs", "From all-reduce to sharded parameters"): the gradients are
+reduce-scattered, each rank's shard is updated by AdamW and cast, and the
+updated shards are all-gathered for the next forward (and, with
+reshard-after-forward, once more for the backward).
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import torch
+
+from .fsdp import (AdamWHParams, View, fsdp_all_gather, fsdp_flatten_pad, fsdp_reduce_scatter_adam_cast,
+                   fsdp_unflatten_views)
+
+
+class FlatParamUnit:
+    def __init__(self, params: Sequence[Tuple[str, Tuple[int, ...]]], world: int, grad_dtype: torch.dtype,
+                 out_dtype: torch.dtype, device="cuda", n_full: Optional[int] = None):
+        self.names = [n for n, _ in params]
+        self.shapes = [tuple(s) for _, s in params]
+        self.world = int(world)
+        self.views, self.padded_numel = fsdp_unflatten_views(self.shapes, self.world)
+        self.numel = sum(math.prod(s) for s in self.shapes)
+        self.shard_numel = self.padded_numel // self.world
+        self.device = torch.device(device)
+        P = self.padded_numel
+        self.grads = [torch.zeros(P, dtype=grad_dtype, device=self.device) for _ in range(self.world)]
+        self.master = torch.zeros(P, dtype=torch.float32, device=self.device)
+        self.exp_avg = torch.zeros(P, dtype=torch.float32, device=self.device)
+        self.exp_avg_sq = torch.zeros(P, dtype=torch.float32, device=self.device)
+        self.shard_out = torch.zeros(P, dtype=out_dtype, device=self.device)
+        nf = self.world if n_full is None else int(n_full)
+        self.full = [torch.zeros(P, dtype=out_dtype, device=self.device) for _ in range(nf)]
+
+    # ---------------------------------------------------------------- set-up
+
+    def load_master(self, tensors: Sequence[torch.Tensor], stream=None) -> None:
+        """Flatten the unit's initial fp32 parameters into the master buffer."""
+        fsdp_flatten_pad(list(tensors), self.world, out=self.master, stream=stream)
+
+    def load_grad(self, rank: int, tensors: Sequence[torch.Tensor], stream=None) -> None:
+        """Flatten rank ``rank``'s per-parameter gradients into its flat buffer (pad zeroed)."""
+        fsdp_flatten_pad(list(tensors), self.world, out=self.grads[rank], stream=stream)
+
+    def param_views(self, flat: torch.Tensor) -> Dict[str, torch.Tensor]:
+        """The original parameters as views into a flat buffer (pad not visible)."""
+        return {n: flat.narrow(0, v.offset, v.numel).view(v.shape) for n, v in zip(self.names, self.views)}
+
+    # ---------------------------------------------------------------- the step
+
+    def reduce_scatter_adam_cast(self, hp: AdamWHParams, rank_begin: int = 0, rank_end: Optional[int] = None,
+                                 nonfinite_count: Optional[torch.Tensor] = None, stream=None) -> None:
+        fsdp_reduce_scatter_adam_cast(self.grads, self.master, self.exp_avg, self.exp_avg_sq, self.shard_out,
+                                      hp, rank_begin, rank_end, nonfinite_count, stream)
+
+    def all_gather(self, stream=None) -> None:
+        fsdp_all_gather(self.shard_out, self.full, self.world, stream)
+
+    def step(self, hp: AdamWHParams, gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None,
+             stream=None) -> None:
+        """Reduce-scatter + AdamW + cast, then ``gathers`` all-gathers, in stream order."""
+        self.reduce_scatter_adam_cast(hp, nonfinite_count=nonfinite_count, stream=stream)
+        for _ in range(gathers):
+            self.all_gather(stream)
+
+    def step_bytes(self, gathers: int = 1) -> Tuple[int, int]:
+        """Algorithmic bytes of one step: (fused kernel, all-gathers)."""
+        gs = self.grads[0].element_size()
+        os_ = self.shard_out.element_size()
+        P = self.padded_numel
+        rsa = P * (self.world * gs + 3 * (4 + 4) + os_)
+        ag = gathers * P * os_ * (1 + len(self.full))
+        return rsa, ag

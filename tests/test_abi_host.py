@@ -1,0 +1,178 @@
+"""Host-side checks of the C ABI: the library loads, exports every function the
+header declares, and its host-only functions (layout, status strings, argument
+validation that returns before any CUDA call) behave as documented. No GPU is
+needed and no device work is enqueued: every call here is rejected on the host
+or is host-only.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    from sharded_fsdp_reduce_gb300 import _lib
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "fsdp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fsdp_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    from sharded_fsdp_reduce_gb300 import _lib
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    assert sorted(_lib.EXPORTS) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_padded_numel_matches_oracle(lib, orc):
+    for world in (1, 2, 3, 7, 8, 64):
+        for numel in list(range(0, 40)) + [4099, 7087872, 855654400, 2**40 + 3]:
+            assert lib.fsdp_padded_numel(numel, world) == orc.padded_numel(numel, world)
+    assert lib.fsdp_padded_numel(-1, 2) == -1
+    assert lib.fsdp_padded_numel(3, 0) == -1
+
+
+def test_unflatten_views_match_oracle_offsets(orc):
+    import fsdp_inputs as fi
+    import sharded_fsdp_reduce_gb300 as F
+    for cfg in fi.CONFIGS.values():
+        shapes = [s for _, s in cfg.params]
+        views, padded = F.fsdp_unflatten_views(shapes, cfg.world)
+        numels = [int(np.prod(s)) for s in shapes]
+        np.testing.assert_array_equal([v.offset for v in views], orc.view_offsets(numels))
+        assert [v.numel for v in views] == numels
+        assert [v.shape for v in views] == [tuple(s) for s in shapes]
+        assert padded == orc.padded_numel(sum(numels), cfg.world)
+
+
+def test_unflatten_views_edge_cases():
+    import sharded_fsdp_reduce_gb300 as F
+    views, padded = F.fsdp_unflatten_views([(), (0,), (3, 0), (5,)], 4)
+    assert [v.numel for v in views] == [1, 0, 0, 5]
+    assert [v.offset for v in views] == [0, 1, 1, 1]
+    assert padded == 8
+    views, padded = F.fsdp_unflatten_views([], 3)
+    assert views == [] and padded == 0
+    with pytest.raises(F.FsdpError):
+        F.fsdp_unflatten_views([(2, -1)], 2)
+    with pytest.raises(F.FsdpError):
+        F.fsdp_unflatten_views([(1,) * 9], 2)
+    with pytest.raises(F.FsdpError):
+        F.fsdp_unflatten_views([(3,)], 0)
+    with pytest.raises(F.FsdpError):
+        F.fsdp_unflatten_views([(2**62,), (2**62,)], 1)  # offset overflow
+
+
+def test_status_strings(lib):
+    from sharded_fsdp_reduce_gb300 import _lib
+    for code in range(5):
+        assert lib.fsdp_status_string(code).decode().startswith(
+            ["FSDP_OK", "FSDP_ERR_INVALID_ARG", "FSDP_ERR_ALIGNMENT", "FSDP_ERR_CUDA",
+             "FSDP_ERR_UNSUPPORTED_DTYPE"][code])
+    assert lib.fsdp_status_string(99).decode().startswith("FSDP_ERR_UNKNOWN")
+    assert lib.fsdp_last_cuda_error() == 0
+    assert _lib.FSDP_OK == 0
+
+
+# ---------------------------------------------------------------- validation (host only)
+
+FAKE = 0x7f0000000000  # never dereferenced: every call below fails validation first
+
+
+def _rsa(lib, **kw):
+    from sharded_fsdp_reduce_gb300 import _lib
+    world = kw.get("world", 2)
+    P = kw.get("P", 16)
+    grads = kw.get("grads", [FAKE + 0x100000 * (q + 1) for q in range(world)])
+    garr = None if grads is None else (ctypes.c_void_p * max(len(grads), 1))(*grads)
+    hp = kw.get("hp", _lib.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0))
+    return lib.fsdp_reduce_scatter_adam_cast(
+        garr, kw.get("gdt", 1), world, P, kw.get("master", FAKE + 0x1000000), kw.get("m", FAKE + 0x2000000),
+        kw.get("v", FAKE + 0x3000000), kw.get("out", FAKE + 0x4000000), kw.get("odt", 1),
+        None if hp is None else ctypes.byref(hp), kw.get("rb", 0), kw.get("re", world),
+        kw.get("nf", None), None)
+
+
+def test_rsa_rejects_invalid_arguments(lib):
+    from sharded_fsdp_reduce_gb300 import _lib
+    E = _lib
+    assert _rsa(lib, gdt=7) == E.FSDP_ERR_UNSUPPORTED_DTYPE
+    assert _rsa(lib, odt=-1) == E.FSDP_ERR_UNSUPPORTED_DTYPE
+    assert _rsa(lib, world=0, grads=[]) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, world=65, grads=[FAKE] * 65) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, grads=None) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, hp=None) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, P=15) == E.FSDP_ERR_INVALID_ARG            # not a multiple of N
+    assert _rsa(lib, P=-2) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, rb=1, re=0) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, rb=0, re=3) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, rb=-1) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, hp=E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 0, 1.0)) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, hp=E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 0.0)) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, hp=E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, float("inf"))) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, master=None) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, out=None) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, grads=[FAKE, None]) == E.FSDP_ERR_INVALID_ARG
+    # misalignment to the element size
+    assert _rsa(lib, master=FAKE + 0x1000002) == E.FSDP_ERR_ALIGNMENT
+    assert _rsa(lib, out=FAKE + 0x4000001) == E.FSDP_ERR_ALIGNMENT
+    assert _rsa(lib, grads=[FAKE + 1, FAKE + 0x100000]) == E.FSDP_ERR_ALIGNMENT
+    assert _rsa(lib, nf=FAKE + 2) == E.FSDP_ERR_ALIGNMENT
+    # aliasing: shard_out inside a state buffer, state buffers overlapping, grads on the state
+    assert _rsa(lib, out=FAKE + 0x1000000 + 16) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, m=FAKE + 0x1000000 + 8) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, grads=[FAKE + 0x3000000, FAKE]) == E.FSDP_ERR_INVALID_ARG
+    assert _rsa(lib, grads=[FAKE + 0x4000000, FAKE]) == E.FSDP_ERR_INVALID_ARG
+    # empty work is a no-op that succeeds without touching anything
+    assert _rsa(lib, P=0) == E.FSDP_OK
+    assert _rsa(lib, rb=1, re=1) == E.FSDP_OK
+    assert lib.fsdp_last_cuda_error() == 0
+
+
+def test_all_gather_rejects_invalid_arguments(lib):
+    from sharded_fsdp_reduce_gb300 import _lib as E
+    arr = lambda *p: (ctypes.c_void_p * len(p))(*p)
+    ag = lambda src, dt, world, P, dsts, n: lib.fsdp_all_gather(src, dt, world, P, dsts, n, None)
+    assert ag(FAKE, 9, 2, 16, arr(FAKE + 4096), 1) == E.FSDP_ERR_UNSUPPORTED_DTYPE
+    assert ag(FAKE, 1, 0, 16, arr(FAKE + 4096), 1) == E.FSDP_ERR_INVALID_ARG
+    assert ag(FAKE, 1, 2, 15, arr(FAKE + 4096), 1) == E.FSDP_ERR_INVALID_ARG
+    assert ag(FAKE, 1, 2, 16, arr(FAKE + 4096), 0) == E.FSDP_ERR_INVALID_ARG
+    assert ag(FAKE, 1, 2, 16, None, 1) == E.FSDP_ERR_INVALID_ARG
+    assert ag(None, 1, 2, 16, arr(FAKE + 4096), 1) == E.FSDP_ERR_INVALID_ARG
+    assert ag(FAKE + 1, 1, 2, 16, arr(FAKE + 4096), 1) == E.FSDP_ERR_ALIGNMENT
+    assert ag(FAKE, 1, 2, 16, arr(FAKE + 4097), 1) == E.FSDP_ERR_ALIGNMENT
+    assert ag(FAKE, 1, 2, 16, arr(FAKE + 16), 1) == E.FSDP_ERR_INVALID_ARG      # overlaps the source
+    assert ag(FAKE, 1, 2, 16, arr(FAKE + 4096, FAKE + 4100), 2) == E.FSDP_ERR_INVALID_ARG  # dsts overlap
+    assert ag(FAKE, 1, 2, 16, arr(FAKE + 4096, None), 2) == E.FSDP_ERR_INVALID_ARG
+    assert ag(FAKE, 1, 2, 0, arr(FAKE + 4096), 1) == E.FSDP_OK                   # empty: no-op
+
+
+def test_flatten_rejects_invalid_arguments(lib):
+    from sharded_fsdp_reduce_gb300 import _lib as E
+    arr = lambda *p: (ctypes.c_void_p * len(p))(*p)
+    i64 = lambda *n: (ctypes.c_int64 * len(n))(*n)
+    fl = lambda srcs, numels, n, dt, world, dst, dn: lib.fsdp_flatten_pad(srcs, numels, n, dt, world, dst, dn,
+                                                                          None, None)
+    assert fl(arr(FAKE), i64(5), 1, 3, 2, FAKE + 4096, 6) == E.FSDP_ERR_UNSUPPORTED_DTYPE
+    assert fl(arr(FAKE), i64(5), 1, 1, 2, FAKE + 4096, 5) == E.FSDP_ERR_INVALID_ARG   # dst_numel != padded
+    assert fl(arr(FAKE), i64(5), 1, 1, 0, FAKE + 4096, 5) == E.FSDP_ERR_INVALID_ARG
+    assert fl(arr(FAKE), i64(-5), 1, 1, 2, FAKE + 4096, 0) == E.FSDP_ERR_INVALID_ARG
+    assert fl(arr(None), i64(5), 1, 1, 2, FAKE + 4096, 6) == E.FSDP_ERR_INVALID_ARG
+    assert fl(arr(FAKE), i64(5), 1, 1, 2, None, 6) == E.FSDP_ERR_INVALID_ARG
+    assert fl(arr(FAKE + 1), i64(5), 1, 1, 2, FAKE + 4096, 6) == E.FSDP_ERR_ALIGNMENT
+    assert fl(arr(FAKE), i64(5), 1, 0, 2, FAKE + 4098, 6) == E.FSDP_ERR_ALIGNMENT    # f32 dst on 2 bytes
+    assert fl(arr(FAKE + 4), i64(5), 1, 1, 2, FAKE, 6) == E.FSDP_ERR_INVALID_ARG     # source inside dst
+    assert fl(None, None, 0, 1, 2, None, 0) == E.FSDP_OK                              # nothing to do

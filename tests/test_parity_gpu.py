@@ -1,0 +1,368 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small units are compared element by element over their whole parity
+trajectory; the 13B and 70B units run at full size in the launch
+configuration the bench uses and are compared on sampled elements (the step
+is pointwise, so the oracle computes each sampled element on its own), plus
+the all-gather property full_k == shard_out at every element.
+
+Bars: layout, gathered buffers and everything integer bit-exact; fp32 master,
+exp_avg, exp_avg_sq within 1e-6 relative; bf16/fp16 outputs within 1 ulp.
+The kernel performs the oracle's operations in the oracle's order, so the
+results are in fact expected to be identical; test_bit_exact checks that.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fsdp_inputs as fi
+from gpu_util import assert_out_close, assert_state_close, host
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def F():
+    import __graft_entry__ as g
+    g.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import sharded_fsdp_reduce_gb300 as F
+    return F
+
+
+def hp_for(F, cfg, t):
+    return F.AdamWHParams(cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay, t, cfg.grad_scale)
+
+
+def ohp_for(orc, cfg, t):
+    return orc.hparams(cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay, t, cfg.grad_scale)
+
+
+def split_views(unit, flat):
+    return [flat.narrow(0, v.offset, v.numel).contiguous() for v in unit.views]
+
+
+def new_unit(F, cfg, **kw):
+    return F.FlatParamUnit(cfg.params, cfg.world, fi.torch_dtype(cfg.grad_dtype), fi.torch_dtype(cfg.out_dtype),
+                           device=DEV, **kw)
+
+
+# ------------------------------------------------------------------ whole trajectories
+
+@pytest.mark.parametrize("name", ["tiny", "gpt2_small", "gpt2_large"])
+def test_config_trajectory_elementwise(F, orc, name):
+    cfg = fi.CONFIGS[name]
+    N = cfg.world
+    unit = new_unit(F, cfg)
+    master = fi.gen_master(cfg)
+    unit.load_master(split_views(unit, master.to(DEV)))
+    p_o = orc.flatten_pad([master.numpy()], N)
+    m_o = np.zeros_like(p_o)
+    v_o = np.zeros_like(p_o)
+    np.testing.assert_array_equal(host(unit.master), p_o)
+    for t in range(1, cfg.steps + 1):
+        grads = [fi.gen_grad(cfg, r, t) for r in range(N)]
+        for r in range(N):
+            unit.load_grad(r, split_views(unit, grads[r].to(DEV)))
+        g_o = [orc.flatten_pad([host(g)], N) for g in grads]
+        for r in range(N):
+            np.testing.assert_array_equal(host(unit.grads[r]), g_o[r])  # flatten + zero pad, bit-exact
+        unit.step(hp_for(F, cfg, t), gathers=cfg.gathers)
+        shards_o, full_o = orc.fsdp_step(g_o, cfg.grad_dtype, N, p_o, m_o, v_o, cfg.out_dtype, ohp_for(orc, cfg, t))
+        torch.cuda.synchronize()
+        assert_state_close(host(unit.master), p_o, f"{name} master t={t}")
+        assert_state_close(host(unit.exp_avg), m_o, f"{name} exp_avg t={t}")
+        assert_state_close(host(unit.exp_avg_sq), v_o, f"{name} exp_avg_sq t={t}")
+        assert_out_close(host(unit.shard_out), shards_o, cfg.out_dtype, f"{name} shard_out t={t}")
+        for k, f in enumerate(unit.full):
+            assert torch.equal(f, unit.shard_out), f"{name} full[{k}] t={t}"
+        P = unit.numel
+        assert not host(unit.master)[P:].any() and not host(unit.shard_out)[P:].any()  # pad stays zero
+
+
+def test_bit_exact(F, orc):
+    cfg = fi.CONFIGS["gpt2_small"]
+    N = cfg.world
+    unit = new_unit(F, cfg)
+    master = fi.gen_master(cfg)
+    unit.load_master([master.to(DEV)])
+    p_o = master.numpy().copy()
+    m_o = np.zeros_like(p_o)
+    v_o = np.zeros_like(p_o)
+    for t in (1, 2, 3):
+        grads = [fi.gen_grad(cfg, r, t) for r in range(N)]
+        for r in range(N):
+            unit.load_grad(r, [grads[r].to(DEV)])
+        unit.step(hp_for(F, cfg, t))
+        shards_o, _ = orc.fsdp_step([host(g) for g in grads], cfg.grad_dtype, N, p_o, m_o, v_o, cfg.out_dtype,
+                                    ohp_for(orc, cfg, t))
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host(unit.master).view(np.uint32), p_o.view(np.uint32))
+        np.testing.assert_array_equal(host(unit.exp_avg).view(np.uint32), m_o.view(np.uint32))
+        np.testing.assert_array_equal(host(unit.exp_avg_sq).view(np.uint32), v_o.view(np.uint32))
+        np.testing.assert_array_equal(host(unit.shard_out), shards_o)
+
+
+def _sample_indices(P_pad, N, k, seed):
+    S = P_pad // N
+    rng = np.random.default_rng(seed)
+    idx = [rng.integers(0, P_pad, size=k)]
+    for r in range(N):  # both ends of every rank block, and the last element
+        idx.append(np.arange(r * S, r * S + 64))
+        idx.append(np.arange((r + 1) * S - 64, (r + 1) * S))
+    return np.unique(np.concatenate(idx)).astype(np.int64)
+
+
+@pytest.mark.parametrize("name", ["gpt3_13b", "llama70b"])
+def test_full_size_sampled(F, orc, name):
+    cfg = fi.CONFIGS[name]
+    N = cfg.world
+    unit = new_unit(F, cfg)
+    assert unit.padded_numel == unit.numel  # these units need no padding
+    unit.load_master([fi.gen_master(cfg, device=DEV)])
+    idx = _sample_indices(unit.padded_numel, N, 1 << 20, 7)
+    idx_t = torch.from_numpy(idx).to(DEV)
+    p_s = unit.master[idx_t].cpu().numpy()
+    m_s = np.zeros_like(p_s)
+    v_s = np.zeros_like(p_s)
+    for t in range(1, cfg.steps + 1):
+        for r in range(N):
+            g = fi.gen_grad(cfg, r, t, device=DEV)
+            unit.load_grad(r, [g])
+            del g
+        g_s = [host(unit.grads[r][idx_t]) for r in range(N)]
+        unit.step(hp_for(F, cfg, t), gathers=cfg.gathers)
+        s = orc.scalars(ohp_for(orc, cfg, t), N)
+        g_avg = orc.all_reduce_avg(g_s, cfg.grad_dtype, N, s.c)
+        orc.adamw(p_s, m_s, v_s, g_avg, s)
+        out_s = orc.cast_out(p_s, cfg.out_dtype)
+        torch.cuda.synchronize()
+        assert_state_close(host(unit.master[idx_t]), p_s, f"{name} master t={t}")
+        assert_state_close(host(unit.exp_avg[idx_t]), m_s, f"{name} exp_avg t={t}")
+        assert_state_close(host(unit.exp_avg_sq[idx_t]), v_s, f"{name} exp_avg_sq t={t}")
+        assert_out_close(host(unit.shard_out[idx_t]), out_s, cfg.out_dtype, f"{name} shard_out t={t}")
+        for k, f in enumerate(unit.full):
+            assert torch.equal(f, unit.shard_out), f"{name} full[{k}] t={t}"
+    del unit
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ sizes, dtypes, edge cases
+
+def _run_flat(F, orc, world, P, gfmt, ofmt, steps=2, scale=1.0, seed=0, offset=0, n_dst=None):
+    """Unit of one P-element tensor; tensors may start `offset` elements into
+    larger allocations (offset 1 disables the 16-byte vector path)."""
+    rng = np.random.default_rng(seed)
+    P_pad = orc.padded_numel(P, world)
+    gdt, odt = fi.torch_dtype(gfmt), fi.torch_dtype(ofmt)
+
+    def alloc(n, dt):
+        return torch.zeros(n + offset, dtype=dt, device=DEV)[offset:]
+
+    grads = [alloc(P_pad, gdt) for _ in range(world)]
+    master, m, v = (alloc(P_pad, torch.float32) for _ in range(3))
+    out = alloc(P_pad, odt)
+    fulls = [alloc(P_pad, odt) for _ in range(world if n_dst is None else n_dst)]
+    p0 = rng.uniform(-0.1, 0.1, P).astype(np.float32)
+    F.fsdp_flatten_pad([torch.from_numpy(p0).to(DEV)], world, out=master)
+    p_o = orc.flatten_pad([p0], world)
+    m_o = np.zeros(P_pad, np.float32)
+    v_o = np.zeros(P_pad, np.float32)
+    for t in range(1, steps + 1):
+        rows = [torch.from_numpy((rng.standard_normal(P) * 1e-2 * scale).astype(np.float32)).to(gdt)
+                for _ in range(world)]
+        for r in range(world):
+            F.fsdp_flatten_pad([rows[r].to(DEV)], world, out=grads[r])
+        hp = F.AdamWHParams(1e-3, 0.9, 0.999, 1e-8, 0.01, t, scale)
+        F.fsdp_reduce_scatter_adam_cast(grads, master, m, v, out, hp)
+        F.fsdp_all_gather(out, fulls, world)
+        g_o = [orc.flatten_pad([host(r_)], world) for r_ in rows]
+        shards_o, full_o = orc.fsdp_step(g_o, gfmt, world, p_o, m_o, v_o, ofmt,
+                                         orc.hparams(1e-3, 0.9, 0.999, 1e-8, 0.01, t, scale))
+        torch.cuda.synchronize()
+        assert_state_close(host(master), p_o, "master")
+        assert_state_close(host(m), m_o, "exp_avg")
+        assert_state_close(host(v), v_o, "exp_avg_sq")
+        assert_out_close(host(out), shards_o, ofmt, "shard_out")
+        for f in fulls:
+            np.testing.assert_array_equal(host(f).view(np.uint8), host(out).view(np.uint8))
+        assert not p_o[P:].any() and not host(master)[P:].any()
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 8])
+@pytest.mark.parametrize("P", [1, 2, 7, 8, 9, 17, 4099, 8 * 127 + 5])
+def test_odd_sizes_bf16(F, orc, world, P):
+    _run_flat(F, orc, world, P, "bf16", "bf16", seed=P * 10 + world)
+
+
+@pytest.mark.parametrize("gfmt,ofmt,scale", [("f16", "f16", 1024.0), ("f32", "f32", 1.0), ("bf16", "f32", 1.0),
+                                             ("f32", "bf16", 1.0), ("f16", "bf16", 1.0), ("bf16", "f16", 1.0)])
+@pytest.mark.parametrize("world,P", [(2, 4099), (8, 8 * 1000 + 3), (4, 4 * 33)])
+def test_dtype_combinations(F, orc, gfmt, ofmt, scale, world, P):
+    _run_flat(F, orc, world, P, gfmt, ofmt, scale=scale, seed=world + P)
+
+
+@pytest.mark.parametrize("gfmt,ofmt", [("bf16", "bf16"), ("f32", "f16")])
+@pytest.mark.parametrize("world,P", [(2, 4099), (8, 8 * 200 + 1), (5, 1234)])
+def test_unaligned_pointers_take_the_scalar_path(F, orc, gfmt, ofmt, world, P):
+    _run_flat(F, orc, world, P, gfmt, ofmt, offset=1, seed=3)
+
+
+def test_all_gather_fanouts(F, orc):
+    for n_dst in (1, 2, 3, 8, 13):
+        _run_flat(F, orc, 4, 4 * 77 + 1, "bf16", "bf16", steps=1, n_dst=n_dst, seed=n_dst)
+
+
+def test_rank_subrange_touches_only_its_blocks(F, orc):
+    cfg = fi.CONFIGS["tiny"]
+    world, P = 4, 4 * 2050 - 3  # S = 2050: block starts are not 8-aligned
+    rng = np.random.default_rng(11)
+    P_pad = orc.padded_numel(P, world)
+    S = P_pad // world
+    grads = [torch.from_numpy(orc.flatten_pad([(rng.standard_normal(P) * 1e-2).astype(np.float32)], world))
+             .to(torch.bfloat16).to(DEV) for _ in range(world)]
+    master = torch.from_numpy(orc.flatten_pad([rng.uniform(-0.1, 0.1, P).astype(np.float32)], world)).to(DEV)
+    m = torch.full((P_pad,), 1e-3, device=DEV)
+    v = torch.full((P_pad,), 1e-6, device=DEV)
+    out = torch.full((P_pad,), 7.0, dtype=torch.bfloat16, device=DEV)
+    before = [host(x) for x in (master, m, v, out)]
+    hp = F.AdamWHParams(1e-3, 0.9, 0.999, 1e-8, 0.01, 3)
+    F.fsdp_reduce_scatter_adam_cast(grads, master, m, v, out, hp, rank_begin=1, rank_end=3)
+    p_o, m_o, v_o = before[0].copy(), before[1].copy(), before[2].copy()
+    shards_o, _ = orc.fsdp_step([host(g) for g in grads], "bf16", world, p_o, m_o, v_o, "bf16",
+                                orc.hparams(1e-3, 0.9, 0.999, 1e-8, 0.01, 3))
+    torch.cuda.synchronize()
+    after = [host(x) for x in (master, m, v, out)]
+    inside = slice(S, 3 * S)
+    for k, (b, a) in enumerate(zip(before, after)):
+        np.testing.assert_array_equal(a[:S], b[:S])  # rank 0's block untouched
+        np.testing.assert_array_equal(a[3 * S:], b[3 * S:])  # rank 3's block untouched
+    assert_state_close(after[0][inside], p_o[inside], "master")
+    assert_state_close(after[1][inside], m_o[inside], "exp_avg")
+    assert_state_close(after[2][inside], v_o[inside], "exp_avg_sq")
+    assert_out_close(after[3][inside], shards_o[inside], "bf16", "shard_out")
+
+
+def test_determinism(F):
+    cfg = fi.CONFIGS["gpt2_small"]
+    results = []
+    for _ in range(2):
+        unit = new_unit(F, cfg)
+        unit.load_master([fi.gen_master(cfg, device=DEV)])
+        for t in (1, 2):
+            for r in range(cfg.world):
+                unit.load_grad(r, [fi.gen_grad(cfg, r, t, device=DEV)])
+            unit.step(hp_for(F, cfg, t))
+        torch.cuda.synchronize()
+        results.append([x.clone() for x in (unit.master, unit.exp_avg, unit.exp_avg_sq, unit.shard_out)])
+    for a, b in zip(*results):
+        assert torch.equal(a.view(torch.int8) if a.dtype != torch.float32 else a.view(torch.int32),
+                           b.view(torch.int8) if b.dtype != torch.float32 else b.view(torch.int32))
+
+
+def test_canary_guard_bands(F, orc):
+    # every array sits between guard bands of NaN bit patterns; the step and the
+    # gather must write inside their arrays only, and the pad must stay zero
+    world, P, G = 8, 8 * 1001 - 5, 64
+    P_pad = orc.padded_numel(P, world)
+    rng = np.random.default_rng(5)
+    CAN16, CAN32 = 0x7fc1, 0x7fc00001
+
+    def guarded(n, dt):
+        if dt == torch.float32:
+            buf = torch.full((n + 2 * G,), CAN32, dtype=torch.int32, device=DEV).view(torch.float32)
+        else:
+            buf = torch.full((n + 2 * G,), CAN16, dtype=torch.int16, device=DEV).view(dt)
+        return buf, buf[G:G + n]
+
+    bufs = {}
+    for name, dt in [("master", torch.float32), ("m", torch.float32), ("v", torch.float32),
+                     ("out", torch.bfloat16)] + [(f"g{q}", torch.bfloat16) for q in range(world)] + \
+                    [(f"f{q}", torch.bfloat16) for q in range(world)]:
+        bufs[name] = guarded(P_pad, dt)
+    grads = [bufs[f"g{q}"][1] for q in range(world)]
+    for q in range(world):
+        F.fsdp_flatten_pad([torch.from_numpy((rng.standard_normal(P) * 1e-3).astype(np.float32))
+                            .to(torch.bfloat16).to(DEV)], world, out=grads[q])
+    F.fsdp_flatten_pad([torch.from_numpy(rng.uniform(-0.1, 0.1, P).astype(np.float32)).to(DEV)], world,
+                       out=bufs["master"][1])
+    bufs["m"][1].zero_()
+    bufs["v"][1].zero_()
+    F.fsdp_reduce_scatter_adam_cast(grads, bufs["master"][1], bufs["m"][1], bufs["v"][1], bufs["out"][1],
+                                    F.AdamWHParams(1e-3, 0.9, 0.999, 1e-8, 0.01, 1))
+    F.fsdp_all_gather(bufs["out"][1], [bufs[f"f{q}"][1] for q in range(world)], world)
+    torch.cuda.synchronize()
+    for name, (buf, inner) in bufs.items():
+        if buf.dtype == torch.float32:
+            raw, can = buf.view(torch.int32).cpu().numpy().view(np.uint32), CAN32
+        else:
+            raw, can = buf.view(torch.int16).cpu().numpy().view(np.uint16), CAN16
+        assert (raw[:G] == can).all() and (raw[G + P_pad:] == can).all(), f"guard band of {name} overwritten"
+    for name in ("master", "m", "v", "out"):
+        assert not host(bufs[name][1])[P:].any(), f"pad of {name} not zero"
+
+
+def test_nonfinite_counter(F, orc):
+    world, P = 2, 1024
+    rng = np.random.default_rng(9)
+    rows = (rng.standard_normal((world, P)) * 1e-2).astype(np.float32)
+    rows[0, 10] = np.inf
+    rows[1, 20] = np.nan
+    rows[0, 30] = 3e38
+    rows[1, 30] = 3e38   # finite inputs whose fp32 sum overflows
+    rows[0, 40] = np.inf
+    rows[1, 40] = -np.inf
+    grads = [torch.from_numpy(r).to(torch.bfloat16).to(DEV) for r in rows]
+    g_avg = orc.all_reduce_avg([host(g) for g in grads], "bf16", world, 0.5)
+    expect = int(np.count_nonzero(~np.isfinite(g_avg)))
+    assert expect == 4
+    master = torch.zeros(P, device=DEV)
+    m = torch.zeros(P, device=DEV)
+    v = torch.zeros(P, device=DEV)
+    out = torch.zeros(P, dtype=torch.bfloat16, device=DEV)
+    cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for _ in range(2):
+        F.fsdp_reduce_scatter_adam_cast(grads, master, m, v, out, F.AdamWHParams(1e-3), nonfinite_count=cnt)
+    assert int(cnt.item()) == 2 * expect
+
+
+def test_flatten_many_tensors_and_views(F, orc):
+    rng = np.random.default_rng(21)
+    for dt, fmt in ((torch.float32, "f32"), (torch.bfloat16, "bf16"), (torch.float16, "f16")):
+        sizes = [int(s) for s in rng.integers(0, 300, size=70)] + [1, 4099, 0]
+        world = 8
+        host_parts = [rng.standard_normal(s).astype(np.float32) for s in sizes]
+        parts = [torch.from_numpy(h).to(dt).to(DEV) for h in host_parts]
+        # unaligned sources: every other tensor starts one element into its allocation
+        parts = [torch.cat([torch.zeros(1, dtype=dt, device=DEV), p])[1:] if i % 2 else p
+                 for i, p in enumerate(parts)]
+        P_pad = orc.padded_numel(sum(sizes), world)
+        dst = torch.full((P_pad,), float("nan"), dtype=dt, device=DEV)
+        flat, views = F.fsdp_flatten_pad(parts, world, out=dst)
+        want = orc.flatten_pad([host(p) for p in parts], world)
+        np.testing.assert_array_equal(host(flat), want)
+        np.testing.assert_array_equal([v.offset for v in views], orc.view_offsets(sizes))
+        assert [v.numel for v in views] == sizes
+
+
+def test_invalid_calls_enqueue_nothing(F):
+    P = 64
+    grads = [torch.ones(P, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    master = torch.full((P,), 0.5, device=DEV)
+    m = torch.zeros(P, device=DEV)
+    v = torch.zeros(P, device=DEV)
+    out = torch.zeros(P, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(F.FsdpError):
+        F.fsdp_reduce_scatter_adam_cast(grads, master, m, v, out, F.AdamWHParams(1e-3, step=0))
+    with pytest.raises(F.FsdpError):
+        F.fsdp_reduce_scatter_adam_cast(grads, master, m, v, out, F.AdamWHParams(1e-3), rank_begin=2, rank_end=1)
+    with pytest.raises(F.FsdpError):
+        F.fsdp_reduce_scatter_adam_cast(grads, master, m, master, out, F.AdamWHParams(1e-3))  # v aliases master
+    with pytest.raises(ValueError):
+        F.fsdp_reduce_scatter_adam_cast(grads, master, m, v, out[:10], F.AdamWHParams(1e-3))
+    torch.cuda.synchronize()
+    assert torch.equal(master, torch.full((P,), 0.5, device=DEV))
+    assert not m.any() and not v.any() and not out.any()
+    assert F.fsdp_last_cuda_error() == 0
