@@ -27,6 +27,7 @@ time over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -158,6 +159,16 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(values, device):
+    """Element-wise MAX of per-rank timings over the process group (every rank
+    gets the result)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
 
 def oracle_sample_run(cfg, n_elems: int, steps: int, warmup: int, time_budget_s: float | None):
@@ -211,6 +222,18 @@ def oracle_sample_run(cfg, n_elems: int, steps: int, warmup: int, time_budget_s:
 
 # ---------------------------------------------------------------- our arm
 
+def workload_config(args):
+    """The unit to run: a named workload, or (--numel) a one-tensor unit of the
+    same N, dtypes, distributions and gathers with fewer parameters."""
+    import fsdp_inputs as fi
+    cfg = fi.CONFIGS[args.config]
+    name = WORKLOAD_NAMES[cfg.name]
+    if args.numel:
+        cfg = dataclasses.replace(cfg, params=(("flat", (int(args.numel),)),))
+        name = f"{name}_numel{int(args.numel)}"
+    return cfg, name
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -232,7 +255,7 @@ def run_ours(args):
         dist.barrier()
     F._lib.load()
 
-    cfg = fi.CONFIGS[args.config]
+    cfg, workload = workload_config(args)
     N = cfg.world
     gdt, odt = fi.torch_dtype(cfg.grad_dtype), fi.torch_dtype(cfg.out_dtype)
     unit = F.FlatParamUnit(cfg.params, N, gdt, odt, device=dev)
@@ -303,9 +326,7 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1) / Ke
 
     if world_size > 1:
-        red = torch.tensor([step_ms, rsa_ms, e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(red, op=dist.ReduceOp.MAX)
-        step_ms, rsa_ms, e2e_ms = red.tolist()
+        step_ms, rsa_ms, e2e_ms = max_over_ranks([step_ms, rsa_ms, e2e_ms], dev)
 
     if rank != 0:
         if world_size > 1:
@@ -315,7 +336,6 @@ def run_ours(args):
 
     peak, peak_kind = measured_peak()
     achieved = rsa_b / (rsa_ms * 1e-3) / 1e9
-    workload = WORKLOAD_NAMES[cfg.name]
     traffic = recorded_traffic(workload)
     total_bytes = (rsa_b + ag_b) * world_size
     result = {
@@ -373,10 +393,9 @@ def run_reference(args):
     rank, _, world_size = dist_env()
     if rank != 0:
         return  # the CPU oracle runs on rank 0 only
-    cfg = fi.CONFIGS[args.config]
+    cfg, workload = workload_config(args)
     n_s = min(fi.unit_numel(cfg), args.ref_sample)
     gbs, el, done, threads = oracle_sample_run(cfg, n_s, args.steps, args.warmup, None)
-    workload = WORKLOAD_NAMES[cfg.name]
     sample = f"each step: a {n_s}-element unit with the workload's N, dtypes, distributions and all-gathers"
     print(json.dumps({
         "impl": "reference",
@@ -399,6 +418,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="llama70b", choices=sorted(WORKLOAD_NAMES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--numel", type=int, default=0,
+                    help="replace the unit by one flat tensor of this many parameters (small profiling cases)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=1 << 24, help="elements in the CPU-baseline sample")
