@@ -175,6 +175,14 @@ const char *fsdp_status_string(fsdp_status status);
 /* cudaError_t value behind the calling thread's last FSDP_ERR_CUDA (0 if none). */
 int fsdp_last_cuda_error(void);
 
+/* Diagnostics of the bulk-copy (TMA) pipelines. Their waits on shared-memory
+ * barriers are bounded (about one second); a wait that gives up makes its
+ * kernel return early, leaving that call's output incomplete, and is counted
+ * on the current device. This call synchronizes the current device, writes
+ * the count accumulated since the previous call to *count_out (host) and
+ * resets it. The count is 0 in normal operation. */
+fsdp_status fsdp_take_wait_timeouts(uint32_t *count_out);
+
 #ifdef __cplusplus
 }
 #endif

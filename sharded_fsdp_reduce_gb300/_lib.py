@@ -32,6 +32,7 @@ EXPORTS = (
     "fsdp_all_gather",
     "fsdp_status_string",
     "fsdp_last_cuda_error",
+    "fsdp_take_wait_timeouts",
 )
 
 
@@ -72,6 +73,7 @@ def load() -> ctypes.CDLL:
             "fsdp_all_gather": (i32, [vp, i32, i32, i64, vp, i32, vp]),
             "fsdp_status_string": (ctypes.c_char_p, [i32]),
             "fsdp_last_cuda_error": (i32, []),
+            "fsdp_take_wait_timeouts": (i32, [ctypes.POINTER(ctypes.c_uint32)]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)

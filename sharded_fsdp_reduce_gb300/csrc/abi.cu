@@ -256,4 +256,12 @@ const char *fsdp_status_string(fsdp_status status) {
 
 int fsdp_last_cuda_error(void) { return g_last_cuda_error; }
 
+fsdp_status fsdp_take_wait_timeouts(uint32_t *count_out) {
+    if (!count_out) return FSDP_ERR_INVALID_ARG;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_status(e);
+    *count_out = take_gather_wait_timeouts();
+    return FSDP_OK;
+}
+
 }  // extern "C"

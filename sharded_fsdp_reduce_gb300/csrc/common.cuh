@@ -167,6 +167,9 @@ struct GatherArgs {
 
 fsdp_status launch_gather(const GatherArgs &a, cudaStream_t stream);
 
+// Read and reset the count of bounded waits that gave up in the gather kernels.
+uint32_t take_gather_wait_timeouts();
+
 struct FlattenArgs {
     static constexpr int kBatch = 32;
     const void *src[kBatch];  // NULL: zero fill

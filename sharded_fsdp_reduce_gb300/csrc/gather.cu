@@ -7,11 +7,20 @@
 // figure caption; "FSDP (Fully Sharded Data Parallel)", "The Per-Layer
 // Communication": gathered before forward and again before backward).
 //
-// Each thread reads one 16-byte word of the source once and writes it to the
-// n_dst destinations, so the traffic is (1 + n_dst) * P_pad * sizeof(dtype)
-// bytes and the kernel is HBM-write bound. A tail shorter than 16 bytes (and
-// the whole copy when a pointer is not 16-byte aligned) moves in 2-byte units.
+// The traffic is (1 + n_dst) * P_pad * sizeof(dtype) bytes: the source is
+// read once and written n_dst times, so the copy is HBM-write bound.
+//
+// Main path (all pointers 16-byte aligned, at least kTmaMinBytes): a TMA
+// pipeline. One thread per CTA loads a tile of the source into shared memory
+// with a 1-D bulk copy (completion counted on an mbarrier), then issues one
+// bulk store of that shared tile per destination; kStages tiles are in
+// flight per CTA. One instruction moves a whole tile, so the store stream is
+// not limited by per-thread store issue the way 16-byte stores from every
+// thread are. Fallback (unaligned pointers, small copies): every thread loads
+// one 16-byte word and stores it to every destination; a tail shorter than
+// 16 bytes moves in 2-byte units.
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace fsdp {
 namespace {
@@ -42,6 +51,111 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// ---------------------------------------------------------------- TMA path
+
+#ifndef FSDP_GATHER_TILE
+#define FSDP_GATHER_TILE 16384
+#endif
+#ifndef FSDP_GATHER_STAGES
+#define FSDP_GATHER_STAGES 4
+#endif
+constexpr int kTile = FSDP_GATHER_TILE;      // bytes per bulk tile (multiple of 16)
+constexpr int kStages = FSDP_GATHER_STAGES;  // tiles in flight per CTA
+constexpr int kTmaThreads = 32;
+constexpr int64_t kTmaMinBytes = 1 << 20;
+constexpr long long kWaitLimitCycles = 1ll << 31;  // ~1 s at 2 GHz
+
+// Bounded mbarrier waits that gave up (a kernel then returns early).
+__device__ uint32_t g_gather_wait_timeouts;
+
+template <int ND>
+__global__ void __launch_bounds__(kTmaThreads)
+    gather_tma_kernel(const __grid_constant__ GatherArgs a, int64_t bulk_bytes) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t bar[kStages];
+    const char *src = static_cast<const char *>(a.src);
+    // bytes after the bulk part (< 16, a multiple of 2): lanes of CTA 0
+    if (blockIdx.x == 0) {
+        const int64_t tail_units = (a.nbytes - bulk_bytes) / 2;
+        for (int64_t u = threadIdx.x; u < tail_units; u += blockDim.x) {
+            const uint16_t x = *reinterpret_cast<const uint16_t *>(src + bulk_bytes + 2 * u);
+            for (int d = 0; d < a.n_dst; ++d)
+                *reinterpret_cast<uint16_t *>(static_cast<char *>(a.dst[d]) + bulk_bytes + 2 * u) = x;
+        }
+    }
+    if (threadIdx.x != 0) return;
+    const int n = ND > 0 ? ND : a.n_dst;
+    const int64_t ntiles = (bulk_bytes + kTile - 1) / kTile;
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t mine = ntiles > first ? (ntiles - first + step - 1) / step : 0;
+    if (mine == 0) return;
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) tma::mbar_init(&bar[s], 1);
+    tma::fence_mbar_init();
+
+    auto tile_bytes = [&](int64_t t) -> uint32_t {
+        const int64_t left = bulk_bytes - t * kTile;
+        return static_cast<uint32_t>(left < kTile ? left : kTile);
+    };
+    auto load = [&](int64_t it) {
+        const int s = static_cast<int>(it % kStages);
+        const int64_t t = first + it * step;
+        const uint32_t bytes = tile_bytes(t);
+        tma::mbar_arrive_expect_tx(&bar[s], bytes);
+        tma::bulk_load(smem + s * kTile, src + t * kTile, bytes, &bar[s]);
+    };
+
+    for (int64_t it = 0; it < mine && it < kStages; ++it) load(it);
+    uint32_t parity = 0;  // bit s: parity of stage s's next phase
+    for (int64_t it = 0; it < mine; ++it) {
+        const int s = static_cast<int>(it % kStages);
+        if (!tma::mbar_wait_bounded(&bar[s], (parity >> s) & 1u, kWaitLimitCycles)) {
+            atomicAdd(&g_gather_wait_timeouts, 1u);
+            tma::bulk_wait<0>();
+            return;
+        }
+        parity ^= 1u << s;
+        const int64_t t = first + it * step;
+        const uint32_t bytes = tile_bytes(t);
+        if constexpr (ND > 0) {
+#pragma unroll
+            for (int d = 0; d < ND; ++d) tma::bulk_store(static_cast<char *>(a.dst[d]) + t * kTile, smem + s * kTile, bytes);
+        } else {
+            for (int d = 0; d < n; ++d) tma::bulk_store(static_cast<char *>(a.dst[d]) + t * kTile, smem + s * kTile, bytes);
+        }
+        tma::bulk_commit();
+        // the previous tile's stores have read their stage once at most one
+        // group (this tile's) still reads shared memory; refill that stage
+        if (it >= 1 && it - 1 + kStages < mine) {
+            tma::bulk_wait_read<1>();
+            load(it - 1 + kStages);
+        }
+    }
+    tma::bulk_wait<0>();
+}
+
+template <int ND>
+fsdp_status launch_tma(const GatherArgs &a, cudaStream_t stream) {
+    static int blocks_per_sm = 0;
+    const int smem = kStages * kTile;
+    if (blocks_per_sm == 0) {
+        cudaError_t e = cudaFuncSetAttribute(gather_tma_kernel<ND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return cuda_status(e);
+        int b = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, gather_tma_kernel<ND>, kTmaThreads, smem);
+        if (e != cudaSuccess) return cuda_status(e);
+        blocks_per_sm = b > 0 ? b : 1;
+    }
+    const int64_t bulk = a.nbytes / 16 * 16;
+    const int64_t ntiles = (bulk + kTile - 1) / kTile;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
+    const int grid = static_cast<int>(ntiles < cap ? (ntiles > 0 ? ntiles : 1) : cap);
+    gather_tma_kernel<ND><<<grid, kTmaThreads, smem, stream>>>(a, bulk);
+    return check_launch();
+}
+
+// ---------------------------------------------------------------- vector path
+
 template <int ND>
 fsdp_status launch_nd(const GatherArgs &a, cudaStream_t stream) {
     static int blocks_per_sm = 0;
@@ -53,6 +167,7 @@ fsdp_status launch_nd(const GatherArgs &a, cudaStream_t stream) {
     }
     bool vec = aligned(a.src, 16);
     for (int d = 0; d < a.n_dst; ++d) vec = vec && aligned(a.dst[d], 16);
+    if (vec && a.nbytes >= kTmaMinBytes) return launch_tma<ND>(a, stream);
     const int64_t nvec = vec ? a.nbytes / 16 : 0;
     const int64_t tail_units = (a.nbytes - 16 * nvec) / 2;
     const int64_t items = nvec + tail_units;
@@ -64,6 +179,13 @@ fsdp_status launch_nd(const GatherArgs &a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+uint32_t take_gather_wait_timeouts() {
+    uint32_t n = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&n, g_gather_wait_timeouts, sizeof(n)) != cudaSuccess) return 0;
+    cudaMemcpyToSymbol(g_gather_wait_timeouts, &zero, sizeof(zero));
+    return n;
+}
 
 fsdp_status launch_gather(const GatherArgs &a, cudaStream_t stream) {
     switch (a.n_dst) {

@@ -30,7 +30,15 @@
 namespace fsdp {
 namespace rsa {
 
-constexpr int kThreads = 256;
+// Launch shape (compile-time tunables; the defaults are the measured best).
+#ifndef FSDP_RSA_THREADS
+#define FSDP_RSA_THREADS 256
+#endif
+#ifndef FSDP_RSA_MIN_BLOCKS
+#define FSDP_RSA_MIN_BLOCKS 1
+#endif
+constexpr int kThreads = FSDP_RSA_THREADS;
+constexpr int kMinBlocks = FSDP_RSA_MIN_BLOCKS;
 
 // AdamW on one element; each operation is rounded on its own (no FMA), in the
 // order of the documented definition.
@@ -160,7 +168,7 @@ __device__ __forceinline__ uint32_t vec_chunk(const RsaArgs &a, int world, int64
 // scalar elements [begin, vbegin) and [vend, end). With nchunks = 0 and
 // vbegin = vend = end every element takes the scalar path.
 template <int NW, int GD, int OD>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
     rsa_kernel(const __grid_constant__ RsaArgs a, int64_t vbegin, int64_t nchunks, int64_t vend) {
     const int world = NW > 0 ? NW : a.world;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;

@@ -18,7 +18,7 @@ __all__ = [
     "AdamWHParams", "FsdpError", "View",
     "fsdp_padded_numel", "fsdp_unflatten_views", "fsdp_flatten_pad",
     "fsdp_reduce_scatter_adam_cast", "fsdp_all_gather", "fsdp_status_string",
-    "fsdp_last_cuda_error", "dtype_code",
+    "fsdp_last_cuda_error", "fsdp_take_wait_timeouts", "dtype_code",
 ]
 
 _DTYPES = {torch.float32: _lib.FSDP_F32, torch.bfloat16: _lib.FSDP_BF16, torch.float16: _lib.FSDP_F16}
@@ -95,6 +95,13 @@ def fsdp_status_string(status: int) -> str:
 
 def fsdp_last_cuda_error() -> int:
     return int(_lib.load().fsdp_last_cuda_error())
+
+
+def fsdp_take_wait_timeouts() -> int:
+    """Bounded in-kernel waits that gave up since the last call (synchronizes the device)."""
+    n = ctypes.c_uint32(0)
+    _check(_lib.load().fsdp_take_wait_timeouts(ctypes.byref(n)), "fsdp_take_wait_timeouts")
+    return int(n.value)
 
 
 def fsdp_padded_numel(numel: int, world: int) -> int:

@@ -44,6 +44,7 @@ class FlatParamUnit:
         self.shard_out = torch.zeros(P, dtype=out_dtype, device=self.device)
         nf = self.world if n_full is None else int(n_full)
         self.full = [torch.zeros(P, dtype=out_dtype, device=self.device) for _ in range(nf)]
+        self._host = None
 
     # ---------------------------------------------------------------- set-up
 
@@ -76,6 +77,19 @@ class FlatParamUnit:
         for _ in range(gathers):
             self.all_gather(stream)
 
+    def step_from_host(self, host_grads: Sequence[torch.Tensor], host_out: torch.Tensor, hp: AdamWHParams,
+                       gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None) -> None:
+        """One step whose N gradient buffers come from pinned host memory and
+        whose compute-dtype parameters (shard_out, all ranks' shards) go back
+        to pinned host memory. Asynchronous; consecutive calls overlap: the
+        host-to-device copy of a step runs on its own stream into a second
+        set of gradient buffers while the previous step's kernels and
+        device-to-host copy run. host_out is complete once the current stream
+        is synchronized (or after the next call's kernels have started)."""
+        if self._host is None:
+            self._host = _HostPipeline(self)
+        self._host.step(host_grads, host_out, hp, gathers, nonfinite_count)
+
     def step_bytes(self, gathers: int = 1) -> Tuple[int, int]:
         """Algorithmic bytes of one step: (fused kernel, all-gathers)."""
         gs = self.grads[0].element_size()
@@ -84,3 +98,45 @@ class FlatParamUnit:
         rsa = P * (self.world * gs + 3 * (4 + 4) + os_)
         ag = gathers * P * os_ * (1 + len(self.full))
         return rsa, ag
+
+
+class _HostPipeline:
+    """Stream plumbing of FlatParamUnit.step_from_host: two gradient-buffer
+    sets, a copy-in stream, a copy-out stream, and events that order each
+    buffer's reuse after the work that reads it."""
+
+    def __init__(self, unit: FlatParamUnit):
+        self.unit = unit
+        self.sets = [unit.grads, [torch.empty_like(g) for g in unit.grads]]
+        self.read_done = [None, None]   # compute finished reading set k
+        self.out_read = None            # copy-out finished reading shard_out
+        self.copy_in = torch.cuda.Stream(device=unit.device)
+        self.copy_out = torch.cuda.Stream(device=unit.device)
+        self.i = 0
+
+    def step(self, host_grads, host_out, hp, gathers, nonfinite_count):
+        u = self.unit
+        if len(host_grads) != u.world:
+            raise ValueError(f"need {u.world} host gradient buffers")
+        k = self.i % 2
+        gset = self.sets[k]
+        compute = torch.cuda.current_stream(u.device)
+        if self.read_done[k] is not None:
+            self.copy_in.wait_event(self.read_done[k])
+        with torch.cuda.stream(self.copy_in):
+            for g, h in zip(gset, host_grads):
+                g.copy_(h, non_blocking=True)
+        compute.wait_stream(self.copy_in)
+        if self.out_read is not None:
+            compute.wait_event(self.out_read)   # shard_out is about to be rewritten
+        fsdp_reduce_scatter_adam_cast(gset, u.master, u.exp_avg, u.exp_avg_sq, u.shard_out, hp,
+                                      nonfinite_count=nonfinite_count, stream=compute)
+        self.read_done[k] = compute.record_event()
+        self.copy_out.wait_event(self.read_done[k])
+        with torch.cuda.stream(self.copy_out):
+            host_out.copy_(u.shard_out, non_blocking=True)
+        self.out_read = self.copy_out.record_event()
+        for _ in range(gathers):
+            fsdp_all_gather(u.shard_out, u.full, u.world, stream=compute)
+        compute.wait_stream(self.copy_out)  # the step ends when its result is on the host
+        self.i += 1

@@ -176,3 +176,8 @@ def test_flatten_rejects_invalid_arguments(lib):
     assert fl(arr(FAKE), i64(5), 1, 0, 2, FAKE + 4098, 6) == E.FSDP_ERR_ALIGNMENT    # f32 dst on 2 bytes
     assert fl(arr(FAKE + 4), i64(5), 1, 1, 2, FAKE, 6) == E.FSDP_ERR_INVALID_ARG     # source inside dst
     assert fl(None, None, 0, 1, 2, None, 0) == E.FSDP_OK                              # nothing to do
+
+
+def test_take_wait_timeouts_rejects_null(lib):
+    from sharded_fsdp_reduce_gb300 import _lib as E
+    assert lib.fsdp_take_wait_timeouts(None) == E.FSDP_ERR_INVALID_ARG

@@ -366,3 +366,47 @@ def test_invalid_calls_enqueue_nothing(F):
     assert torch.equal(master, torch.full((P,), 0.5, device=DEV))
     assert not m.any() and not v.any() and not out.any()
     assert F.fsdp_last_cuda_error() == 0
+    assert F.fsdp_take_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32, torch.float16])
+@pytest.mark.parametrize("numel,n_dst", [((1 << 20) + 3, 8), (5 * (1 << 19) + 1, 3), ((1 << 21) + 7, 1),
+                                         (3 * (1 << 20), 13), ((1 << 20) + 4096 * 3 + 5, 2)])
+def test_all_gather_bulk_copy_path(F, dt, numel, n_dst):
+    # >= 1 MB with 16-byte aligned pointers takes the TMA pipeline; the sizes
+    # leave a partial last tile and (for odd element counts) a tail below 16 bytes
+    world = 1
+    src = torch.randn(numel, device=DEV).to(dt)
+    fulls = [torch.full((numel,), float("nan"), device=DEV).to(dt) for _ in range(n_dst)]
+    F.fsdp_all_gather(src, fulls, world)
+    for k, f in enumerate(fulls):
+        assert torch.equal(f.view(torch.int16 if dt != torch.float32 else torch.int32),
+                           src.view(torch.int16 if dt != torch.float32 else torch.int32)), k
+    assert F.fsdp_take_wait_timeouts() == 0
+
+
+def test_step_from_host_matches_device_steps(F):
+    # the pipelined host-buffer step (two gradient-buffer sets, copy streams)
+    # must give the same bits as stepping on device-resident gradients
+    cfg = fi.CONFIGS["gpt2_small"]
+    N = cfg.world
+    a, b = new_unit(F, cfg), new_unit(F, cfg)
+    master = fi.gen_master(cfg, device=DEV)
+    a.load_master([master])
+    b.load_master([master])
+    T = 5
+    host = [[fi.gen_grad(cfg, r, t).pin_memory() for r in range(N)] for t in range(1, T + 1)]
+    outs = [torch.empty(a.padded_numel, dtype=a.shard_out.dtype, pin_memory=True) for _ in range(T)]
+    for t in range(1, T + 1):
+        a.step_from_host(host[t - 1], outs[t - 1], hp_for(F, cfg, t), gathers=2)
+    torch.cuda.synchronize()
+    for t in range(1, T + 1):
+        for r in range(N):
+            b.grads[r].copy_(host[t - 1][r])
+        b.step(hp_for(F, cfg, t), gathers=2)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[t - 1].view(torch.int16), b.shard_out.cpu().view(torch.int16)), t
+    for x, y in ((a.master, b.master), (a.exp_avg, b.exp_avg), (a.exp_avg_sq, b.exp_avg_sq)):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    for f in a.full:
+        assert torch.equal(f.view(torch.int16), b.shard_out.view(torch.int16))
