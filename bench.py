@@ -327,8 +327,31 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1) / Ke
     launches += Ke * (1 + cfg.gathers)
 
+    # ---- variants of the same step (same byte model): the first all-gather
+    # fused into the update kernel; and the no-reshard mode (one gather kept
+    # for forward and backward, fused)
+    variants = {}
+    if not args.no_variants:
+        for vname, vg in (("fused_gather", cfg.gathers), ("no_reshard_fused", 1)):
+            for _ in range(3):
+                t += 1
+                unit.step(hp(t), gathers=vg, fuse_gather=True)
+            v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            v0.record(stream)
+            for _ in range(K):
+                t += 1
+                unit.step(hp(t), gathers=vg, fuse_gather=True)
+            v1.record(stream)
+            torch.cuda.synchronize()
+            vms = v0.elapsed_time(v1) / K
+            launches += K * vg
+            variants[vname] = {"gathers_per_step": vg, "ms_per_step": round(vms, 4)}
+
     if world_size > 1:
         step_ms, rsa_ms, e2e_ms = max_over_ranks([step_ms, rsa_ms, e2e_ms], dev)
+        for v in variants.values():
+            v["ms_per_step"] = max_over_ranks([v["ms_per_step"]], dev)[0]
 
     if rank != 0:
         if world_size > 1:
@@ -372,6 +395,10 @@ def run_ours(args):
                 "ms_per_step": round(e2e_ms, 3), "steps": Ke,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
+        "variants": {k: dict(v, value=round(world_size * (rsa_b + P_pad * unit.shard_out.element_size()
+                                                           * (1 + len(unit.full)) * v["gathers_per_step"])
+                                            / (v["ms_per_step"] * 1e-3) / 1e9, 2))
+                     for k, v in variants.items()},
         "clocks": clocks.summary(),
     }
     if world_size == 1 and not args.no_cpu_baseline:
@@ -424,6 +451,7 @@ def main(argv=None):
                     help="replace the unit by one flat tensor of this many parameters (small profiling cases)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variants", action="store_true", help="skip the fused-gather variant timings")
     ap.add_argument("--cpu-sample", type=int, default=1 << 24, help="elements in the CPU-baseline sample")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline time budget")
     ap.add_argument("--ref-sample", type=int, default=1 << 22, help="elements per reference-arm step")

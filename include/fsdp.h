@@ -155,6 +155,28 @@ fsdp_status fsdp_reduce_scatter_adam_cast(const void *const *grads, fsdp_dtype g
                                           int rank_begin, int rank_end,
                                           uint32_t *nonfinite_count, void *stream);
 
+/* The fused update with the all-gather fused in (device): everything
+ * fsdp_reduce_scatter_adam_cast does for the emulated ranks [rank_begin,
+ * rank_end), and every updated compute-dtype element is also stored to each
+ * of the n_dst gathered buffers: full_k[j] = out[j] for j in those ranks'
+ * blocks, k < n_dst. With all ranks emulated this equals
+ * fsdp_reduce_scatter_adam_cast followed by fsdp_all_gather, without
+ * reading shard_out back. shard_out may be NULL (not written): the
+ * no-reshard mode keeps the gathered parameters instead of the shard
+ * ("Fully Sharded Data Parallel: ...", "Adoption paths for FSDP":
+ * --no-reshard-after-forward; "fairseq ... FSDP 实战指南", "参数定义与底层实现":
+ * reshard_after_forward).
+ *   full_bufs    host array of n_dst device pointers (1 <= n_dst <=
+ *                FSDP_MAX_WORLD), padded_numel elements of out_dtype each;
+ *                no written buffer may overlap another or the gradients.
+ * Other arguments and errors as fsdp_reduce_scatter_adam_cast. */
+fsdp_status fsdp_reduce_scatter_adam_cast_gather(const void *const *grads, fsdp_dtype grad_dtype,
+                                                 int world, int64_t padded_numel, float *master,
+                                                 float *exp_avg, float *exp_avg_sq, void *shard_out,
+                                                 fsdp_dtype out_dtype, void *const *full_bufs, int n_dst,
+                                                 const fsdp_adamw_hparams *hp, int rank_begin,
+                                                 int rank_end, uint32_t *nonfinite_count, void *stream);
+
 /* All-gather (device): every destination receives the whole rank-ordered
  * concatenation of the shards, full_k[j] = shard_out[j] for j < padded_numel,
  * k < n_dst. Rank r's shard is shard_out[r*S, (r+1)*S), so the copy is the

@@ -29,6 +29,7 @@ EXPORTS = (
     "fsdp_unflatten_views",
     "fsdp_flatten_pad",
     "fsdp_reduce_scatter_adam_cast",
+    "fsdp_reduce_scatter_adam_cast_gather",
     "fsdp_all_gather",
     "fsdp_status_string",
     "fsdp_last_cuda_error",
@@ -70,6 +71,8 @@ def load() -> ctypes.CDLL:
             "fsdp_flatten_pad": (i32, [vp, vp, i32, i32, i32, vp, i64, ctypes.POINTER(FsdpView), vp]),
             "fsdp_reduce_scatter_adam_cast": (i32, [vp, i32, i32, i64, vp, vp, vp, vp, i32,
                                                     ctypes.POINTER(FsdpAdamwHparams), i32, i32, vp, vp]),
+            "fsdp_reduce_scatter_adam_cast_gather": (i32, [vp, i32, i32, i64, vp, vp, vp, vp, i32, vp, i32,
+                                                           ctypes.POINTER(FsdpAdamwHparams), i32, i32, vp, vp]),
             "fsdp_all_gather": (i32, [vp, i32, i32, i64, vp, i32, vp]),
             "fsdp_status_string": (ctypes.c_char_p, [i32]),
             "fsdp_last_cuda_error": (i32, []),

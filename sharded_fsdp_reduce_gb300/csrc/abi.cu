@@ -163,40 +163,56 @@ fsdp_status fsdp_flatten_pad(const void *const *srcs, const int64_t *numels, int
     return FSDP_OK;
 }
 
-fsdp_status fsdp_reduce_scatter_adam_cast(const void *const *grads, fsdp_dtype grad_dtype, int world,
-                                          int64_t padded_numel, float *master, float *exp_avg,
-                                          float *exp_avg_sq, void *shard_out, fsdp_dtype out_dtype,
-                                          const fsdp_adamw_hparams *hp, int rank_begin, int rank_end,
-                                          uint32_t *nonfinite_count, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Validation and launch shared by the fused update with and without the fused
+// all-gather (full_bufs / n_dst; shard_out may then be NULL).
+fsdp_status rsa_entry(const void *const *grads, fsdp_dtype grad_dtype, int world, int64_t padded_numel,
+                      float *master, float *exp_avg, float *exp_avg_sq, void *shard_out, fsdp_dtype out_dtype,
+                      void *const *full_bufs, int n_dst, const fsdp_adamw_hparams *hp, int rank_begin,
+                      int rank_end, uint32_t *nonfinite_count, void *stream) {
     if (!dtype_valid(grad_dtype) || !dtype_valid(out_dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
     if (world < 1 || world > FSDP_MAX_WORLD || !grads || !hp) return FSDP_ERR_INVALID_ARG;
     if (padded_numel < 0 || padded_numel % world != 0) return FSDP_ERR_INVALID_ARG;
     if (rank_begin < 0 || rank_begin > rank_end || rank_end > world) return FSDP_ERR_INVALID_ARG;
     if (hp->step < 1 || !(hp->grad_scale > 0.0f) || !isfinite(hp->grad_scale)) return FSDP_ERR_INVALID_ARG;
+    if (n_dst < 0 || n_dst > FSDP_MAX_WORLD || (n_dst > 0 && !full_bufs)) return FSDP_ERR_INVALID_ARG;
     if (mul_overflows(padded_numel, 4)) return FSDP_ERR_INVALID_ARG;
     const int64_t S = padded_numel / world;
     const int64_t begin = static_cast<int64_t>(rank_begin) * S, end = static_cast<int64_t>(rank_end) * S;
     if (begin == end) return FSDP_OK;
-    if (!master || !exp_avg || !exp_avg_sq || !shard_out) return FSDP_ERR_INVALID_ARG;
+    if (!master || !exp_avg || !exp_avg_sq || (!shard_out && n_dst == 0)) return FSDP_ERR_INVALID_ARG;
     const size_t gs = static_cast<size_t>(dtype_size(grad_dtype)), os = static_cast<size_t>(dtype_size(out_dtype));
     const size_t state_bytes = static_cast<size_t>(padded_numel) * 4;
+    const size_t out_bytes = static_cast<size_t>(padded_numel) * os;
     if (!aligned(master, 4) || !aligned(exp_avg, 4) || !aligned(exp_avg_sq, 4) || !aligned(shard_out, os))
         return FSDP_ERR_ALIGNMENT;
     if (nonfinite_count && !aligned(nonfinite_count, 4)) return FSDP_ERR_ALIGNMENT;
-    const void *state[3] = {master, exp_avg, exp_avg_sq};
-    for (int i = 0; i < 3; ++i) {
-        for (int k = i + 1; k < 3; ++k)
-            if (overlaps(state[i], state_bytes, state[k], state_bytes)) return FSDP_ERR_INVALID_ARG;
-        if (overlaps(state[i], state_bytes, shard_out, padded_numel * os)) return FSDP_ERR_INVALID_ARG;
+    // every written buffer: master, m, v, shard_out (if any), the gathered buffers
+    const void *written[3 + 1 + FSDP_MAX_WORLD];
+    size_t wbytes[3 + 1 + FSDP_MAX_WORLD];
+    int nw = 0;
+    written[nw] = master; wbytes[nw++] = state_bytes;
+    written[nw] = exp_avg; wbytes[nw++] = state_bytes;
+    written[nw] = exp_avg_sq; wbytes[nw++] = state_bytes;
+    if (shard_out) { written[nw] = shard_out; wbytes[nw++] = out_bytes; }
+    for (int d = 0; d < n_dst; ++d) {
+        if (!full_bufs[d]) return FSDP_ERR_INVALID_ARG;
+        if (!aligned(full_bufs[d], os)) return FSDP_ERR_ALIGNMENT;
+        written[nw] = full_bufs[d]; wbytes[nw++] = out_bytes;
     }
+    for (int i = 0; i < nw; ++i)
+        for (int k = i + 1; k < nw; ++k)
+            if (overlaps(written[i], wbytes[i], written[k], wbytes[k])) return FSDP_ERR_INVALID_ARG;
     RsaArgs a;
     memset(&a, 0, sizeof(a));
     for (int q = 0; q < world; ++q) {
         if (!grads[q]) return FSDP_ERR_INVALID_ARG;
         if (!aligned(grads[q], gs)) return FSDP_ERR_ALIGNMENT;
-        if (overlaps(grads[q], padded_numel * gs, shard_out, padded_numel * os)) return FSDP_ERR_INVALID_ARG;
-        for (int i = 0; i < 3; ++i)
-            if (overlaps(grads[q], padded_numel * gs, state[i], state_bytes)) return FSDP_ERR_INVALID_ARG;
+        for (int i = 0; i < nw; ++i)
+            if (overlaps(grads[q], padded_numel * gs, written[i], wbytes[i])) return FSDP_ERR_INVALID_ARG;
         a.grads[q] = grads[q];
     }
     a.master = master;
@@ -208,12 +224,39 @@ fsdp_status fsdp_reduce_scatter_adam_cast(const void *const *grads, fsdp_dtype g
     a.end = end;
     a.s = make_scalars(*hp, world);
     a.world = world;
+    a.n_full = n_dst;
+    for (int d = 0; d < n_dst; ++d) a.full[d] = full_bufs[d];
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (grad_dtype) {
         case FSDP_BF16: return launch_rsa_bf16(a, out_dtype, s);
         case FSDP_F16: return launch_rsa_f16(a, out_dtype, s);
         default: return launch_rsa_f32(a, out_dtype, s);
     }
+}
+
+}  // namespace
+
+extern "C" {
+
+fsdp_status fsdp_reduce_scatter_adam_cast(const void *const *grads, fsdp_dtype grad_dtype, int world,
+                                          int64_t padded_numel, float *master, float *exp_avg,
+                                          float *exp_avg_sq, void *shard_out, fsdp_dtype out_dtype,
+                                          const fsdp_adamw_hparams *hp, int rank_begin, int rank_end,
+                                          uint32_t *nonfinite_count, void *stream) {
+    if (!shard_out && padded_numel > 0 && rank_begin < rank_end) return FSDP_ERR_INVALID_ARG;
+    return rsa_entry(grads, grad_dtype, world, padded_numel, master, exp_avg, exp_avg_sq, shard_out, out_dtype,
+                     nullptr, 0, hp, rank_begin, rank_end, nonfinite_count, stream);
+}
+
+fsdp_status fsdp_reduce_scatter_adam_cast_gather(const void *const *grads, fsdp_dtype grad_dtype, int world,
+                                                 int64_t padded_numel, float *master, float *exp_avg,
+                                                 float *exp_avg_sq, void *shard_out, fsdp_dtype out_dtype,
+                                                 void *const *full_bufs, int n_dst,
+                                                 const fsdp_adamw_hparams *hp, int rank_begin, int rank_end,
+                                                 uint32_t *nonfinite_count, void *stream) {
+    if (n_dst < 1) return FSDP_ERR_INVALID_ARG;
+    return rsa_entry(grads, grad_dtype, world, padded_numel, master, exp_avg, exp_avg_sq, shard_out, out_dtype,
+                     full_bufs, n_dst, hp, rank_begin, rank_end, nonfinite_count, stream);
 }
 
 fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world, int64_t padded_numel,

@@ -151,9 +151,13 @@ struct RsaArgs {
     int64_t end;     // one past the last
     AdamScalars s;
     int world;
+    // fused all-gather: also store every output element to full[0..n_full)
+    void *full[FSDP_MAX_WORLD];
+    int n_full;
 };
 
 // One translation unit per gradient dtype (rsa_bf16.cu, rsa_f16.cu, rsa_f32.cu).
+// a.n_full > 0 selects the variant with the fused all-gather.
 fsdp_status launch_rsa_bf16(const RsaArgs &a, int out_dtype, cudaStream_t stream);
 fsdp_status launch_rsa_f16(const RsaArgs &a, int out_dtype, cudaStream_t stream);
 fsdp_status launch_rsa_f32(const RsaArgs &a, int out_dtype, cudaStream_t stream);

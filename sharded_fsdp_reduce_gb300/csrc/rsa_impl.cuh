@@ -15,6 +15,11 @@
 // "FSDP (Fully Sharded Data Parallel)", "Mixed Precision and FSDP" (fp32
 // master and state, bf16 compute copy).
 //
+// Variant with the fused all-gather (GATHER = true): every output element is
+// also stored to the n_full gathered buffers, so the updated shards reach
+// every emulated rank's full buffer in the same pass, without re-reading
+// shard_out (which may then be omitted).
+//
 // Layout per thread and iteration: 8 consecutive elements. Each rank's 8
 // bf16/fp16 gradients are one 16-byte load; master, m and v are two 16-byte
 // loads each; the 8 outputs are one 16-byte store. All loads of an iteration
@@ -53,7 +58,7 @@ __device__ __forceinline__ void adamw(float g, float &p, float &m, float &v, con
 __device__ __forceinline__ uint32_t nonfinite(float g) { return isfinite(g) ? 0u : 1u; }
 
 // One element through the plain path.
-template <int GD, int OD>
+template <int GD, int OD, bool GATHER>
 __device__ __forceinline__ uint32_t scalar_elem(const RsaArgs &a, int world, int64_t j) {
     float acc = Dtype<GD>::load(a.grads[0], j);
     for (int q = 1; q < world; ++q) acc = __fadd_rn(acc, Dtype<GD>::load(a.grads[q], j));
@@ -63,12 +68,15 @@ __device__ __forceinline__ uint32_t scalar_elem(const RsaArgs &a, int world, int
     a.master[j] = p;
     a.m[j] = m;
     a.v[j] = v;
-    Dtype<OD>::store(a.out, j, p);
+    if (a.out != nullptr) Dtype<OD>::store(a.out, j, p);
+    if constexpr (GATHER) {
+        for (int d = 0; d < a.n_full; ++d) Dtype<OD>::store(a.full[d], j, p);
+    }
     return nonfinite(g);
 }
 
 // Average, AdamW and cast of one 8-element chunk whose gradient sum is acc.
-template <int OD>
+template <int OD, bool GATHER>
 __device__ __forceinline__ uint32_t finish_chunk(const RsaArgs &a, int64_t j0, const float *acc,
                                                  float4 p0, float4 p1, float4 m0, float4 m1,
                                                  float4 v0, float4 v1) {
@@ -89,13 +97,24 @@ __device__ __forceinline__ uint32_t finish_chunk(const RsaArgs &a, int64_t j0, c
     st_state(a.v + j0, make_float4(v[0], v[1], v[2], v[3]));
     st_state(a.v + j0 + 4, make_float4(v[4], v[5], v[6], v[7]));
     if constexpr (OD == FSDP_F32) {
-        float *o = static_cast<float *>(a.out) + j0;
-        st_state(o, make_float4(p[0], p[1], p[2], p[3]));
-        st_state(o + 4, make_float4(p[4], p[5], p[6], p[7]));
+        const float4 lo = make_float4(p[0], p[1], p[2], p[3]), hi = make_float4(p[4], p[5], p[6], p[7]);
+        if (a.out != nullptr) {
+            st_state(static_cast<float *>(a.out) + j0, lo);
+            st_state(static_cast<float *>(a.out) + j0 + 4, hi);
+        }
+        if constexpr (GATHER) {
+            for (int d = 0; d < a.n_full; ++d) {
+                st_state(static_cast<float *>(a.full[d]) + j0, lo);
+                st_state(static_cast<float *>(a.full[d]) + j0 + 4, hi);
+            }
+        }
     } else {
         const uint4 o = make_uint4(pack2<OD>(p[0], p[1]), pack2<OD>(p[2], p[3]),
                                    pack2<OD>(p[4], p[5]), pack2<OD>(p[6], p[7]));
-        st_stream(static_cast<uint16_t *>(a.out) + j0, o);
+        if (a.out != nullptr) st_stream(static_cast<uint16_t *>(a.out) + j0, o);
+        if constexpr (GATHER) {
+            for (int d = 0; d < a.n_full; ++d) st_stream(static_cast<uint16_t *>(a.full[d]) + j0, o);
+        }
     }
     return bad;
 }
@@ -127,7 +146,7 @@ template <int GD> __device__ __forceinline__ void widen8(const uint4 *w, float *
     }
 }
 
-template <int NW, int GD, int OD>
+template <int NW, int GD, int OD, bool GATHER>
 __device__ __forceinline__ uint32_t vec_chunk(const RsaArgs &a, int world, int64_t j0) {
     float acc[8];
     if constexpr (NW > 0) {
@@ -147,7 +166,7 @@ __device__ __forceinline__ uint32_t vec_chunk(const RsaArgs &a, int world, int64
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
         }
-        return finish_chunk<OD>(a, j0, acc, p0, p1, m0, m1, v0, v1);
+        return finish_chunk<OD, GATHER>(a, j0, acc, p0, p1, m0, m1, v0, v1);
     } else {
         for (int q = 0; q < world; ++q) {
             uint4 w[GradRegs<1, GD>::kWords];
@@ -160,26 +179,26 @@ __device__ __forceinline__ uint32_t vec_chunk(const RsaArgs &a, int world, int64
         const float4 p0 = ld_state(a.master + j0), p1 = ld_state(a.master + j0 + 4);
         const float4 m0 = ld_state(a.m + j0), m1 = ld_state(a.m + j0 + 4);
         const float4 v0 = ld_state(a.v + j0), v1 = ld_state(a.v + j0 + 4);
-        return finish_chunk<OD>(a, j0, acc, p0, p1, m0, m1, v0, v1);
+        return finish_chunk<OD, GATHER>(a, j0, acc, p0, p1, m0, m1, v0, v1);
     }
 }
 
 // Grid-stride over nchunks 8-element chunks starting at vbegin, then the
 // scalar elements [begin, vbegin) and [vend, end). With nchunks = 0 and
 // vbegin = vend = end every element takes the scalar path.
-template <int NW, int GD, int OD>
+template <int NW, int GD, int OD, bool GATHER>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
     rsa_kernel(const __grid_constant__ RsaArgs a, int64_t vbegin, int64_t nchunks, int64_t vend) {
     const int world = NW > 0 ? NW : a.world;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     uint32_t bad = 0;
-    for (int64_t k = tid; k < nchunks; k += stride) bad += vec_chunk<NW, GD, OD>(a, world, vbegin + 8 * k);
+    for (int64_t k = tid; k < nchunks; k += stride) bad += vec_chunk<NW, GD, OD, GATHER>(a, world, vbegin + 8 * k);
     const int64_t nhead = vbegin - a.begin;
     const int64_t nrest = nhead + (a.end - vend);
     for (int64_t e = tid; e < nrest; e += stride) {
         const int64_t j = e < nhead ? a.begin + e : vend + (e - nhead);
-        bad += scalar_elem<GD, OD>(a, world, j);
+        bad += scalar_elem<GD, OD, GATHER>(a, world, j);
     }
     if (a.nonfinite != nullptr) {
         const uint32_t total = __reduce_add_sync(0xffffffffu, bad);
@@ -187,17 +206,19 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     }
 }
 
-template <int NW, int GD, int OD>
+template <int NW, int GD, int OD, bool GATHER>
 fsdp_status launch_typed(const RsaArgs &a, cudaStream_t stream) {
     static int blocks_per_sm = 0;  // occupancy of this instantiation (one device type)
     if (blocks_per_sm == 0) {
         int b = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, rsa_kernel<NW, GD, OD>, kThreads, 0);
+        cudaError_t e =
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, rsa_kernel<NW, GD, OD, GATHER>, kThreads, 0);
         if (e != cudaSuccess) return cuda_status(e);
         blocks_per_sm = b > 0 ? b : 1;
     }
     bool vec = aligned(a.master, 16) && aligned(a.m, 16) && aligned(a.v, 16) && aligned(a.out, 16);
     for (int q = 0; q < a.world; ++q) vec = vec && aligned(a.grads[q], 16);
+    for (int d = 0; d < a.n_full; ++d) vec = vec && aligned(a.full[d], 16);
     int64_t vbegin = a.end, vend = a.end, nchunks = 0;
     if (vec) {
         vbegin = (a.begin + 7) / 8 * 8;
@@ -212,26 +233,31 @@ fsdp_status launch_typed(const RsaArgs &a, cudaStream_t stream) {
     const int64_t need = (items + kThreads - 1) / kThreads;
     const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
     const int grid = static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
-    rsa_kernel<NW, GD, OD><<<grid, kThreads, 0, stream>>>(a, vbegin, nchunks, vend);
+    rsa_kernel<NW, GD, OD, GATHER><<<grid, kThreads, 0, stream>>>(a, vbegin, nchunks, vend);
     return check_launch();
 }
 
-template <int GD, int OD>
+template <int GD, int OD, bool GATHER>
 fsdp_status launch_world(const RsaArgs &a, cudaStream_t stream) {
     switch (a.world) {
-        case 2: return launch_typed<2, GD, OD>(a, stream);
-        case 4: return launch_typed<4, GD, OD>(a, stream);
-        case 8: return launch_typed<8, GD, OD>(a, stream);
-        default: return launch_typed<0, GD, OD>(a, stream);
+        case 2: return launch_typed<2, GD, OD, GATHER>(a, stream);
+        case 4: return launch_typed<4, GD, OD, GATHER>(a, stream);
+        case 8: return launch_typed<8, GD, OD, GATHER>(a, stream);
+        default: return launch_typed<0, GD, OD, GATHER>(a, stream);
     }
+}
+
+template <int GD, int OD>
+fsdp_status launch_gather_flag(const RsaArgs &a, cudaStream_t stream) {
+    return a.n_full > 0 ? launch_world<GD, OD, true>(a, stream) : launch_world<GD, OD, false>(a, stream);
 }
 
 template <int GD>
 fsdp_status launch_grad(const RsaArgs &a, int out_dtype, cudaStream_t stream) {
     switch (out_dtype) {
-        case FSDP_BF16: return launch_world<GD, FSDP_BF16>(a, stream);
-        case FSDP_F16: return launch_world<GD, FSDP_F16>(a, stream);
-        case FSDP_F32: return launch_world<GD, FSDP_F32>(a, stream);
+        case FSDP_BF16: return launch_gather_flag<GD, FSDP_BF16>(a, stream);
+        case FSDP_F16: return launch_gather_flag<GD, FSDP_F16>(a, stream);
+        case FSDP_F32: return launch_gather_flag<GD, FSDP_F32>(a, stream);
         default: return FSDP_ERR_UNSUPPORTED_DTYPE;
     }
 }

@@ -17,7 +17,8 @@ from ._lib import FsdpAdamwHparams, FsdpView
 __all__ = [
     "AdamWHParams", "FsdpError", "View",
     "fsdp_padded_numel", "fsdp_unflatten_views", "fsdp_flatten_pad",
-    "fsdp_reduce_scatter_adam_cast", "fsdp_all_gather", "fsdp_status_string",
+    "fsdp_reduce_scatter_adam_cast", "fsdp_reduce_scatter_adam_cast_gather", "fsdp_all_gather",
+    "fsdp_status_string",
     "fsdp_last_cuda_error", "fsdp_take_wait_timeouts", "dtype_code",
 ]
 
@@ -181,6 +182,44 @@ def fsdp_reduce_scatter_adam_cast(grads: Sequence[torch.Tensor], master: torch.T
         _dev(master, "master"), _dev(exp_avg, "exp_avg"), _dev(exp_avg_sq, "exp_avg_sq"),
         _dev(shard_out, "shard_out"), dtype_code(shard_out.dtype), ctypes.byref(hp), rb, re,
         nf or None, _stream(stream)), "fsdp_reduce_scatter_adam_cast")
+
+
+def fsdp_reduce_scatter_adam_cast_gather(grads: Sequence[torch.Tensor], master: torch.Tensor,
+                                         exp_avg: torch.Tensor, exp_avg_sq: torch.Tensor,
+                                         shard_out: Optional[torch.Tensor], full_bufs: Sequence[torch.Tensor],
+                                         hparams: AdamWHParams, rank_begin: int = 0,
+                                         rank_end: Optional[int] = None,
+                                         nonfinite_count: Optional[torch.Tensor] = None,
+                                         stream: Optional[torch.cuda.Stream] = None) -> None:
+    """The fused update with the all-gather fused in: as fsdp_reduce_scatter_adam_cast,
+    and each updated element is also written to every buffer of full_bufs.
+    shard_out may be None (not written)."""
+    world = len(grads)
+    P_pad = master.numel()
+    if not full_bufs:
+        raise ValueError("full_bufs must hold at least one buffer")
+    odt = full_bufs[0].dtype
+    for i, f in enumerate(full_bufs):
+        if f.numel() != P_pad or f.dtype != odt:
+            raise ValueError(f"full_bufs[{i}] must hold {P_pad} elements of {odt}")
+    if shard_out is not None and (shard_out.numel() != P_pad or shard_out.dtype != odt):
+        raise ValueError(f"shard_out must hold {P_pad} elements of {odt}")
+    gdt = grads[0].dtype if world else torch.bfloat16
+    for i, g in enumerate(grads):
+        if g.numel() != P_pad or g.dtype != gdt:
+            raise ValueError(f"grads[{i}] must hold {P_pad} elements of {gdt}")
+    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
+        if t.dtype != torch.float32 or t.numel() != P_pad:
+            raise ValueError(f"{name} must be float32 with {P_pad} elements")
+    nf = _dev(nonfinite_count, "nonfinite_count") if nonfinite_count is not None else None
+    hp = hparams.to_c()
+    re = world if rank_end is None else int(rank_end)
+    _check(_lib.load().fsdp_reduce_scatter_adam_cast_gather(
+        _ptrs(grads, "grads") if world else None, dtype_code(gdt), world, P_pad,
+        _dev(master, "master"), _dev(exp_avg, "exp_avg"), _dev(exp_avg_sq, "exp_avg_sq"),
+        _dev(shard_out, "shard_out") if shard_out is not None else None, dtype_code(odt),
+        _ptrs(full_bufs, "full_bufs"), len(full_bufs), ctypes.byref(hp), int(rank_begin), re, nf,
+        _stream(stream)), "fsdp_reduce_scatter_adam_cast_gather")
 
 
 def fsdp_all_gather(shard_out: torch.Tensor, full_bufs: Sequence[torch.Tensor], world: int,

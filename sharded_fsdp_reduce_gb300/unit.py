@@ -23,7 +23,7 @@ from typing import Dict, List, Optional, Sequence, Tuple
 import torch
 
 from .fsdp import (AdamWHParams, View, fsdp_all_gather, fsdp_flatten_pad, fsdp_reduce_scatter_adam_cast,
-                   fsdp_unflatten_views)
+                   fsdp_reduce_scatter_adam_cast_gather, fsdp_unflatten_views)
 
 
 class FlatParamUnit:
@@ -71,9 +71,19 @@ class FlatParamUnit:
         fsdp_all_gather(self.shard_out, self.full, self.world, stream)
 
     def step(self, hp: AdamWHParams, gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None,
-             stream=None) -> None:
-        """Reduce-scatter + AdamW + cast, then ``gathers`` all-gathers, in stream order."""
-        self.reduce_scatter_adam_cast(hp, nonfinite_count=nonfinite_count, stream=stream)
+             stream=None, fuse_gather: bool = False) -> None:
+        """Reduce-scatter + AdamW + cast, then ``gathers`` all-gathers, in stream order.
+
+        gathers=2 is reshard-after-forward (gathered before forward and again
+        before backward), gathers=1 the no-reshard mode. With fuse_gather the
+        first gather is written by the update kernel itself."""
+        if fuse_gather and gathers >= 1:
+            fsdp_reduce_scatter_adam_cast_gather(self.grads, self.master, self.exp_avg, self.exp_avg_sq,
+                                                 self.shard_out, self.full, hp, nonfinite_count=nonfinite_count,
+                                                 stream=stream)
+            gathers -= 1
+        else:
+            self.reduce_scatter_adam_cast(hp, nonfinite_count=nonfinite_count, stream=stream)
         for _ in range(gathers):
             self.all_gather(stream)
 

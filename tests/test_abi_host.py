@@ -181,3 +181,25 @@ def test_flatten_rejects_invalid_arguments(lib):
 def test_take_wait_timeouts_rejects_null(lib):
     from sharded_fsdp_reduce_gb300 import _lib as E
     assert lib.fsdp_take_wait_timeouts(None) == E.FSDP_ERR_INVALID_ARG
+
+
+def test_fused_gather_rejects_invalid_arguments(lib):
+    from sharded_fsdp_reduce_gb300 import _lib as E
+    arr = lambda *p: (ctypes.c_void_p * len(p))(*p)
+    hp = E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+    g = arr(FAKE + 0x100000, FAKE + 0x200000)
+
+    def call(out, fulls, n, **kw):
+        return lib.fsdp_reduce_scatter_adam_cast_gather(g, 1, 2, 16, FAKE + 0x1000000, FAKE + 0x2000000,
+                                                        FAKE + 0x3000000, out, 1, fulls, n, ctypes.byref(hp),
+                                                        0, 2, None, None)
+    assert call(FAKE + 0x4000000, arr(FAKE + 0x5000000), 0) == E.FSDP_ERR_INVALID_ARG   # no destination
+    assert call(FAKE + 0x4000000, None, 1) == E.FSDP_ERR_INVALID_ARG
+    assert call(FAKE + 0x4000000, arr(None), 1) == E.FSDP_ERR_INVALID_ARG
+    assert call(FAKE + 0x4000000, arr(FAKE + 0x5000001), 1) == E.FSDP_ERR_ALIGNMENT
+    assert call(FAKE + 0x4000000, arr(FAKE + 0x4000010), 1) == E.FSDP_ERR_INVALID_ARG  # overlaps shard_out
+    assert call(None, arr(FAKE + 0x1000000), 1) == E.FSDP_ERR_INVALID_ARG              # overlaps master
+    assert call(None, arr(FAKE + 0x100010), 1) == E.FSDP_ERR_INVALID_ARG               # overlaps a gradient
+    assert call(None, arr(FAKE + 0x5000000, FAKE + 0x5000008), 2) == E.FSDP_ERR_INVALID_ARG
+    assert lib.fsdp_reduce_scatter_adam_cast(g, 1, 2, 16, FAKE + 0x1000000, FAKE + 0x2000000, FAKE + 0x3000000,
+                                             None, 1, ctypes.byref(hp), 0, 2, None, None) == E.FSDP_ERR_INVALID_ARG

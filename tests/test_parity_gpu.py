@@ -410,3 +410,105 @@ def test_step_from_host_matches_device_steps(F):
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
     for f in a.full:
         assert torch.equal(f.view(torch.int16), b.shard_out.view(torch.int16))
+
+
+# ------------------------------------------------------------------ fused all-gather (f1)
+
+@pytest.mark.parametrize("name", ["tiny", "gpt2_small", "gpt2_large"])
+def test_fused_gather_matches_oracle_and_unfused(F, orc, name):
+    cfg = fi.CONFIGS[name]
+    N = cfg.world
+    a, b = new_unit(F, cfg), new_unit(F, cfg)
+    master = fi.gen_master(cfg)
+    for u in (a, b):
+        u.load_master([master.to(DEV)] if u.padded_numel == u.numel else split_views(u, master.to(DEV)))
+    p_o = orc.flatten_pad([master.numpy()], N)
+    m_o = np.zeros_like(p_o)
+    v_o = np.zeros_like(p_o)
+    for t in range(1, 4):
+        grads = [fi.gen_grad(cfg, r, t) for r in range(N)]
+        for u in (a, b):
+            for r in range(N):
+                u.load_grad(r, split_views(u, grads[r].to(DEV)))
+        a.step(hp_for(F, cfg, t), gathers=cfg.gathers, fuse_gather=True)
+        b.step(hp_for(F, cfg, t), gathers=cfg.gathers)
+        _, full_o = orc.fsdp_step([orc.flatten_pad([host(g)], N) for g in grads], cfg.grad_dtype, N, p_o, m_o, v_o,
+                                  cfg.out_dtype, ohp_for(orc, cfg, t))
+        torch.cuda.synchronize()
+        assert_state_close(host(a.master), p_o, "master")
+        for f in a.full:
+            assert_out_close(host(f), full_o, cfg.out_dtype, "full")
+        for x, y in zip((a.master, a.exp_avg, a.exp_avg_sq), (b.master, b.exp_avg, b.exp_avg_sq)):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+        assert torch.equal(a.shard_out.view(torch.int16), b.shard_out.view(torch.int16))
+        for fa, fb in zip(a.full, b.full):
+            assert torch.equal(fa.view(torch.int16), fb.view(torch.int16))
+
+
+@pytest.mark.parametrize("offset", [0, 1])
+@pytest.mark.parametrize("world,P,ofmt", [(2, 4099, "bf16"), (3, 1000, "f16"), (8, 8 * 300 + 5, "f32")])
+def test_fused_gather_without_shard_and_unaligned(F, orc, offset, world, P, ofmt):
+    rng = np.random.default_rng(P + world + offset)
+    P_pad = orc.padded_numel(P, world)
+    odt = fi.torch_dtype(ofmt)
+
+    def alloc(n, dt):
+        return torch.zeros(n + offset, dtype=dt, device=DEV)[offset:]
+
+    rows = (rng.standard_normal((world, P)) * 1e-2).astype(np.float32)
+    g_o = [orc.flatten_pad([r], world) for r in rows]
+    grads = [alloc(P_pad, torch.float32) for _ in range(world)]
+    for g, r in zip(grads, g_o):
+        g.copy_(torch.from_numpy(r))
+    p0 = orc.flatten_pad([rng.uniform(-0.1, 0.1, P).astype(np.float32)], world)
+    master, m, v = (alloc(P_pad, torch.float32) for _ in range(3))
+    master.copy_(torch.from_numpy(p0))
+    fulls = [alloc(P_pad, odt) for _ in range(world + 1)]
+    F.fsdp_reduce_scatter_adam_cast_gather(grads, master, m, v, None, fulls, F.AdamWHParams(1e-3, weight_decay=0.01))
+    p_o, m_o, v_o = p0.copy(), np.zeros_like(p0), np.zeros_like(p0)
+    _, full_o = orc.fsdp_step(g_o, "f32", world, p_o, m_o, v_o, ofmt, orc.hparams(1e-3, 0.9, 0.999, 1e-8, 0.01, 1))
+    torch.cuda.synchronize()
+    assert_state_close(host(master), p_o, "master")
+    assert_state_close(host(m), m_o, "exp_avg")
+    assert_state_close(host(v), v_o, "exp_avg_sq")
+    for f in fulls:
+        assert_out_close(host(f), full_o, ofmt, "full")
+
+
+def test_fused_gather_rank_subrange(F, orc):
+    world, P = 4, 4 * 2050
+    rng = np.random.default_rng(3)
+    grads = [torch.from_numpy((rng.standard_normal(P) * 1e-2).astype(np.float32)).to(torch.bfloat16).to(DEV)
+             for _ in range(world)]
+    master = torch.from_numpy(rng.uniform(-0.1, 0.1, P).astype(np.float32)).to(DEV)
+    m = torch.zeros(P, device=DEV)
+    v = torch.zeros(P, device=DEV)
+    out = torch.zeros(P, dtype=torch.bfloat16, device=DEV)
+    fulls = [torch.full((P,), 3.0, dtype=torch.bfloat16, device=DEV) for _ in range(world)]
+    ref_master, ref_m, ref_v, ref_out = master.clone(), m.clone(), v.clone(), out.clone()
+    hp = F.AdamWHParams(1e-3, weight_decay=0.01)
+    F.fsdp_reduce_scatter_adam_cast_gather(grads, master, m, v, out, fulls, hp, rank_begin=1, rank_end=3)
+    F.fsdp_reduce_scatter_adam_cast(grads, ref_master, ref_m, ref_v, ref_out, hp, rank_begin=1, rank_end=3)
+    torch.cuda.synchronize()
+    S = P // world
+    assert torch.equal(master, ref_master) and torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    for f in fulls:
+        assert torch.equal(f[S:3 * S].view(torch.int16), ref_out[S:3 * S].view(torch.int16))
+        assert (f[:S] == 3.0).all() and (f[3 * S:] == 3.0).all()
+
+
+def test_fused_gather_rejects_bad_arguments(F):
+    P = 64
+    grads = [torch.ones(P, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    master, m, v = (torch.zeros(P, device=DEV) for _ in range(3))
+    out = torch.zeros(P, dtype=torch.bfloat16, device=DEV)
+    fulls = [torch.zeros(P, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    hp = F.AdamWHParams(1e-3)
+    with pytest.raises(ValueError):
+        F.fsdp_reduce_scatter_adam_cast_gather(grads, master, m, v, out, [], hp)
+    with pytest.raises(F.FsdpError):  # a gathered buffer aliasing shard_out
+        F.fsdp_reduce_scatter_adam_cast_gather(grads, master, m, v, out, [fulls[0], out], hp)
+    with pytest.raises(F.FsdpError):  # gathered buffers overlapping each other
+        F.fsdp_reduce_scatter_adam_cast_gather(grads, master, m, v, None, [fulls[0], fulls[0]], hp)
+    torch.cuda.synchronize()
+    assert not master.any() and not out.any() and not fulls[0].any()
