@@ -21,6 +21,8 @@ import threading
 import numpy as np
 
 F32, BF16, F16 = 0, 1, 2
+OPT_ADAMW, OPT_SGD, OPT_ADAMAX, OPT_ADADELTA = 0, 1, 2, 3
+OPTIMIZERS = {"adamw": OPT_ADAMW, "sgd": OPT_SGD, "adamax": OPT_ADAMAX, "adadelta": OPT_ADADELTA}
 _DT = {"f32": F32, "bf16": BF16, "f16": F16}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -86,6 +88,9 @@ def _load():
                                     ctypes.POINTER(HParams), vp]),
             "orc_ddp_step": (i32, [vp, i32, i64, i64, vp, vp, vp, i32, vp,
                                    ctypes.POINTER(HParams), vp]),
+            "orc_reduce_scatter_lowp": (None, [vp, i32, i64, i64, i64, f32, vp]),
+            "orc_step_ex": (i32, [i32, i32, vp, i32, i64, i64, vp, vp, vp, i32, i32, vp, vp,
+                                  ctypes.POINTER(HParams), vp]),
             "orc_all_reduce_avg_f64": (None, [vp, i32, i64, i64, ctypes.c_double, vp]),
             "orc_adamw_f64": (None, [vp, vp, vp, vp, i64, ctypes.POINTER(HParams)]),
         }
@@ -248,6 +253,35 @@ def ddp_step(grads, grad_fmt: str, world: int, master, m, v, out_fmt: str, hp: H
     if rc:
         raise ValueError("oracle ddp_step: bad arguments")
     return full
+
+
+def reduce_scatter_lowp(grads, grad_fmt: str, world: int, rank: int, c: float) -> np.ndarray:
+    """Block `rank` of the reduce-scatter summed in the gradient dtype."""
+    padded = grads[0].size
+    S = shard_numel(padded, world)
+    out = np.empty(S, dtype=np.float32)
+    _load().orc_reduce_scatter_lowp(_ptr_array(grads), _DT[grad_fmt], world, S, rank, c, _ptr(out))
+    return out
+
+
+def step_ex(optimizer: str, reduce_lowp: bool, grads, grad_fmt: str, world: int, param, s0, s1, state_fmt: str,
+            out_fmt: str, hp: HParams):
+    """General step (optimizer, reduce precision, state precision), ranks in
+    turn then the all-gather. Updates param/s0/s1 in place (numpy arrays of
+    the state format: float32, or uint16 bits for bf16/f16; s1 None for SGD).
+    Returns (shards_out, gathered full buffer)."""
+    padded = param.size
+    S = shard_numel(padded, world)
+    shards = np.empty(padded, dtype=np_storage(out_fmt))
+    full = np.empty(padded, dtype=np_storage(out_fmt))
+    scratch = np.empty(max(S, 1), dtype=np.float32)
+    rc = _load().orc_step_ex(OPTIMIZERS[optimizer], int(bool(reduce_lowp)), _ptr_array(grads), _DT[grad_fmt],
+                             world, padded, _ptr(param), _ptr(s0), _ptr(s1) if s1 is not None else None,
+                             _DT[state_fmt], _DT[out_fmt], _ptr(shards), _ptr(full), ctypes.byref(hp),
+                             _ptr(scratch))
+    if rc:
+        raise ValueError("oracle step_ex: bad arguments")
+    return shards, full
 
 
 def all_reduce_avg_f64(grads, grad_fmt: str, world: int, grad_scale: float = 1.0) -> np.ndarray:

@@ -55,6 +55,9 @@
  *  R6 cast: IEEE round-to-nearest-even; overflow to infinity; NaN stays a
  *     (quiet) NaN.
  *  R7 m = v = 0 before step 1; t counts from 1.
+ *  R17-R19 the SGD-momentum, Adamax and Adadelta rules of orc_step_ex.
+ *  R20 a reduce-scatter in the gradient dtype rounds every partial sum.
+ *  R21 low-precision state: widen, update in fp32, round each value back.
  */
 #include <math.h>
 #include <stdint.h>
@@ -383,6 +386,149 @@ int orc_ddp_step(const void *const *G, int grad_dtype, int64_t N, int64_t P_pad,
     orc_all_reduce_avg(G, grad_dtype, N, P_pad, s.c, g_scratch);
     orc_adamw(master, m, v, g_scratch, P_pad, &s);
     orc_cast(master, P_pad, out_dtype, out_full);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* variants of the step (the "next" rows)                               */
+/* ------------------------------------------------------------------ */
+
+/* Optimizers. [FAIR] "限制与兼容性说明": FSDP is compatible with the
+ * pointwise optimizers (Adam, AdamW, Adadelta, Adamax, SGD, ...); [ANN]
+ * "Where FSDP goes next": tested with SGD and Adam. The pages print none of
+ * the update rules; these are the textbook rules (readings R17-R19):
+ *  SGD with momentum mu (no dampening), L2 weight decay added to the gradient:
+ *     d = g + wd*p;  b = d on the first step, else b = mu*b + d;  p = p - lr*b
+ *  Adamax (Kingma & Ba, the infinity-norm variant of Adam), L2 decay:
+ *     d = g + wd*p;  m = b1*m + (1-b1)*d;  u = max(b2*u, |d| + eps) (NaN if
+ *     either side is NaN);  p = p - alpha * (m/u), alpha = lr/(1-b1^t) as
+ *     for AdamW
+ *  Adadelta (Zeiler), lr multiplier, L2 decay, rho = beta1:
+ *     d = g + wd*p;  s = rho*s + (1-rho)*(d*d);
+ *     delta = (sqrt(a + eps) / sqrt(s + eps)) * d;  a = rho*a + (1-rho)*(delta*delta);
+ *     p = p - lr*delta */
+#define ORC_OPT_ADAMW 0
+#define ORC_OPT_SGD 1
+#define ORC_OPT_ADAMAX 2
+#define ORC_OPT_ADADELTA 3
+
+static int opt_states(int opt) { return opt == ORC_OPT_SGD ? 1 : 2; }
+
+/* One element of one optimizer, fp32, one rounding per operation. */
+static void update_elem(int opt, float g, float *p, float *s0, float *s1, const orc_scalars *s,
+                        const orc_hparams *h) {
+    float pi = *p;
+    if (opt == ORC_OPT_ADAMW) {
+        float mi = *s0, vi = *s1;
+        pi = pi * s->decay;
+        mi = s->beta1 * mi + s->one_minus_beta1 * g;
+        vi = s->beta2 * vi + s->one_minus_beta2 * (g * g);
+        float denom = sqrtf(vi) / s->b2s + s->eps;
+        pi = pi - s->alpha * (mi / denom);
+        *s0 = mi;
+        *s1 = vi;
+    } else if (opt == ORC_OPT_SGD) {
+        float d = g + h->weight_decay * pi;
+        float b = h->step == 1 ? d : h->beta1 * *s0 + d;
+        pi = pi - h->lr * b;
+        *s0 = b;
+    } else if (opt == ORC_OPT_ADAMAX) {
+        float d = g + h->weight_decay * pi;
+        float mi = s->beta1 * *s0 + s->one_minus_beta1 * d;
+        float a = s->beta2 * *s1, b = fabsf(d) + s->eps;
+        float ui = (a > b || a != a) ? a : b; /* max, NaN if either side is NaN */
+        pi = pi - s->alpha * (mi / ui);
+        *s0 = mi;
+        *s1 = ui;
+    } else { /* ORC_OPT_ADADELTA */
+        float d = g + h->weight_decay * pi;
+        float sq = s->beta1 * *s0 + s->one_minus_beta1 * (d * d);
+        float delta = (sqrtf(*s1 + s->eps) / sqrtf(sq + s->eps)) * d;
+        float acc = s->beta1 * *s1 + s->one_minus_beta1 * (delta * delta);
+        pi = pi - h->lr * delta;
+        *s0 = sq;
+        *s1 = acc;
+    }
+    *p = pi;
+}
+
+static float load_as_f32(const void *base, int dtype, int64_t j) { return grad_at(base, dtype, j); }
+
+static void store_from_f32(void *base, int dtype, int64_t j, float x) {
+    if (dtype == ORC_F32)
+        ((float *)base)[j] = x;
+    else if (dtype == ORC_BF16)
+        ((uint16_t *)base)[j] = orc_f32_to_bf16(x);
+    else
+        ((uint16_t *)base)[j] = orc_f32_to_f16(x);
+}
+
+static float round_to(int dtype, float x) {
+    if (dtype == ORC_BF16) return orc_bf16_to_f32(orc_f32_to_bf16(x));
+    if (dtype == ORC_F16) return orc_f16_to_f32(orc_f32_to_f16(x));
+    return x;
+}
+
+/* Reduce-scatter summed in the gradient dtype: the default without
+ * --fp32-reduce-scatter ([FAIR] "参数定义与底层实现"), and the "FP16
+ * reduce-scatter on gradients" of [ANN] "Harnessing FSDP's full power" item 4.
+ * Reading R20: ranks in order, each partial sum computed in fp32 and rounded
+ * to the gradient dtype; then g = acc * c in fp32. */
+void orc_reduce_scatter_lowp(const void *const *G, int grad_dtype, int64_t N, int64_t S, int64_t rank, float c,
+                             float *g) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < S; ++i) {
+        int64_t j = rank * S + i;
+        float acc = grad_at(G[0], grad_dtype, j);
+        for (int64_t q = 1; q < N; ++q) acc = round_to(grad_dtype, acc + grad_at(G[q], grad_dtype, j));
+        g[i] = acc * c;
+    }
+}
+
+/* The step with a chosen optimizer, reduce precision and state precision,
+ * all N ranks emulated in turn, then the all-gather ([GUIDE] "The Per-Layer
+ * Communication").
+ *  state_dtype ORC_F32: `param` is the fp32 master; the shard written to
+ *     shards_out is its cast to out_dtype.
+ *  state_dtype ORC_BF16 / ORC_F16 ([GUIDE] "Mixed Precision and FSDP":
+ *     without fp32 master, params and Adam state in bf16; [ANN] item 4: FP16
+ *     master weights): `param` and the states are stored in that dtype, each
+ *     element widened to fp32, updated as above, rounded back (R21); the
+ *     param itself is the shard (out_dtype must equal state_dtype).
+ * s1 may be NULL for SGD. g_scratch holds S floats. Returns nonzero on bad
+ * arguments. */
+int orc_step_ex(int opt, int reduce_lowp, const void *const *G, int grad_dtype, int64_t N, int64_t P_pad,
+                void *param, void *s0, void *s1, int state_dtype, int out_dtype, void *shards_out,
+                void *out_full, const orc_hparams *h, float *g_scratch) {
+    orc_scalars sc;
+    int64_t S = orc_shard_numel(P_pad, N);
+    if (S < 0 || orc_scalars_from_hparams(h, N, &sc) || opt < 0 || opt > 3) return 1;
+    if (state_dtype != ORC_F32 && out_dtype != state_dtype) return 1;
+    if (opt_states(opt) == 2 && !s1) return 1;
+    int es = dtype_size(out_dtype);
+    const void *shard_ptrs[4096];
+    if (N > 4096) return 1;
+    for (int64_t r = 0; r < N; ++r) {
+        if (reduce_lowp)
+            orc_reduce_scatter_lowp(G, grad_dtype, N, S, r, sc.c, g_scratch);
+        else
+            orc_reduce_scatter(G, grad_dtype, N, S, r, sc.c, g_scratch);
+        unsigned char *shard_r = (unsigned char *)shards_out + (size_t)(r * S) * es;
+#pragma omp parallel for schedule(static)
+        for (int64_t i = 0; i < S; ++i) {
+            int64_t j = r * S + i;
+            float p = load_as_f32(param, state_dtype, j);
+            float a = load_as_f32(s0, state_dtype, j);
+            float b = s1 ? load_as_f32(s1, state_dtype, j) : 0.0f;
+            update_elem(opt, g_scratch[i], &p, &a, &b, &sc, h);
+            store_from_f32(param, state_dtype, j, p);
+            store_from_f32(s0, state_dtype, j, a);
+            if (s1) store_from_f32(s1, state_dtype, j, b);
+            store_from_f32(shard_r, out_dtype, i, p);
+        }
+        shard_ptrs[r] = shard_r;
+    }
+    orc_all_gather(shard_ptrs, es, N, S, out_full);
     return 0;
 }
 
