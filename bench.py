@@ -348,6 +348,46 @@ def run_ours(args):
             launches += K * vg
             variants[vname] = {"gathers_per_step": vg, "ms_per_step": round(vms, 4)}
 
+    # ---- the variant steps' kernels on the same unit (each on its own byte
+    # model: N*grad + (1 + states)*(read + write) + out)
+    kernels = {}
+    if not args.no_variants:
+        P = P_pad
+        gb = unit.grads[0].element_size()
+        low = [unit.master.to(torch.bfloat16), torch.zeros(P, dtype=torch.bfloat16, device=dev),
+               torch.zeros(P, dtype=torch.bfloat16, device=dev)]
+        vsets = {
+            "adamw_grad_dtype_reduce": ("adamw", True, unit.master, unit.exp_avg, unit.exp_avg_sq, unit.shard_out),
+            "adamw_bf16_state": ("adamw", False, low[0], low[1], low[2], None),
+            "sgd_momentum": ("sgd", False, unit.master, unit.exp_avg, None, unit.shard_out),
+            "adamax": ("adamax", False, unit.master, unit.exp_avg, unit.exp_avg_sq, unit.shard_out),
+            "adadelta": ("adadelta", False, unit.master, unit.exp_avg, unit.exp_avg_sq, unit.shard_out),
+        }
+        for vname, (opt, lowp, prm, s0, s1, out) in vsets.items():
+            ss = prm.element_size()
+            nstates = 1 + (s0 is not None) + (s1 is not None)
+            nbytes = P * (N * gb + nstates * 2 * ss + (out.element_size() if out is not None else 0))
+            lrv = 1.0 if opt == "adadelta" else cfg.lr
+
+            def run(tt, opt=opt, lowp=lowp, prm=prm, s0=s0, s1=s1, out=out, lrv=lrv):
+                F.fsdp_reduce_scatter_step(unit.grads, prm, s0, s1, out,
+                                           F.StepConfig(opt, lrv, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay,
+                                                        tt, cfg.grad_scale, reduce_dtype=gdt if lowp else None))
+            for i in range(3):
+                run(i + 1)
+            k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            k0.record(stream)
+            for i in range(K):
+                run(i + 4)
+            k1.record(stream)
+            torch.cuda.synchronize()
+            kms = k0.elapsed_time(k1) / K
+            launches += K
+            kernels[vname] = {"ms": round(kms, 4), "bytes_per_launch": nbytes,
+                              "achieved_GBs": round(nbytes / (kms * 1e-3) / 1e9, 1)}
+        del low
+
     if world_size > 1:
         step_ms, rsa_ms, e2e_ms = max_over_ranks([step_ms, rsa_ms, e2e_ms], dev)
         for v in variants.values():
@@ -399,6 +439,8 @@ def run_ours(args):
                                                            * (1 + len(unit.full)) * v["gathers_per_step"])
                                             / (v["ms_per_step"] * 1e-3) / 1e9, 2))
                      for k, v in variants.items()},
+        "variant_kernels": {k: dict(v, frac=round(v["achieved_GBs"] / measured_peak()[0], 4))
+                            for k, v in kernels.items()},
         "clocks": clocks.summary(),
     }
     if world_size == 1 and not args.no_cpu_baseline:

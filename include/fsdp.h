@@ -63,6 +63,16 @@ typedef enum {
 
 typedef enum { FSDP_F32 = 0, FSDP_BF16 = 1, FSDP_F16 = 2 } fsdp_dtype;
 
+/* Pointwise optimizers of fsdp_reduce_scatter_step ("fairseq ... FSDP
+ * 实战指南", "限制与兼容性说明": FSDP works with Adam, AdamW, Adadelta,
+ * Adamax, SGD and other pointwise optimizers). */
+typedef enum {
+    FSDP_OPT_ADAMW = 0,     /* states: exp_avg, exp_avg_sq */
+    FSDP_OPT_SGD = 1,       /* state: momentum buffer (state1 unused) */
+    FSDP_OPT_ADAMAX = 2,    /* states: exp_avg, exp_inf */
+    FSDP_OPT_ADADELTA = 3   /* states: square_avg, acc_delta */
+} fsdp_optimizer;
+
 /* A view of one original parameter inside a FlatParameter ("FSDP (Fully
  * Sharded Data Parallel)", "Common Pitfalls": use_orig_params keeps
  * named-parameter access as views into the flat parameter). */
@@ -86,6 +96,19 @@ typedef struct {
     int64_t step;        /* t, 1 on the first step */
     float grad_scale;    /* static loss scale the gradients carry; 1 if none */
 } fsdp_adamw_hparams;
+
+/* Configuration of one variant step (fsdp_reduce_scatter_step). */
+typedef struct {
+    int32_t optimizer;     /* fsdp_optimizer */
+    int32_t reduce_dtype;  /* fsdp_dtype: FSDP_F32 (fp32 reduce-scatter) or the gradient dtype */
+    float lr;
+    float beta1;           /* AdamW/Adamax beta1; SGD momentum; Adadelta rho */
+    float beta2;           /* AdamW/Adamax beta2 (unused otherwise) */
+    float eps;             /* AdamW/Adamax/Adadelta epsilon (unused by SGD) */
+    float weight_decay;    /* AdamW: decoupled; SGD/Adamax/Adadelta: wd*p added to the gradient */
+    int64_t step;          /* t, 1 on the first step */
+    float grad_scale;      /* static loss scale the gradients carry; 1 if none */
+} fsdp_step_config;
 
 /* ceil(numel / world) * world: the FlatParameter length after zero padding
  * at the end, so that it splits into `world` equal shards. Returns -1 when
@@ -176,6 +199,46 @@ fsdp_status fsdp_reduce_scatter_adam_cast_gather(const void *const *grads, fsdp_
                                                  fsdp_dtype out_dtype, void *const *full_bufs, int n_dst,
                                                  const fsdp_adamw_hparams *hp, int rank_begin,
                                                  int rank_end, uint32_t *nonfinite_count, void *stream);
+
+/* The variant steps (device): the fused reduce-scatter + optimizer step +
+ * cast with a choice of optimizer, reduction precision and state precision,
+ * for emulated ranks [rank_begin, rank_end), i in [0, S), j = r*S + i:
+ *   acc = G_0[j]; acc = acc + G_q[j] for q = 1..N-1, in fp32; with
+ *         reduce_dtype equal to the gradient dtype every partial sum is
+ *         rounded to that dtype (the reduce-scatter without
+ *         --fp32-reduce-scatter, "参数定义与底层实现"; the FP16 reduce-scatter of
+ *         "Harnessing FSDP's full power", item 4)
+ *   g   = acc * fp32(1 / (N * grad_scale))
+ *   then, one fp32 rounding per operation (wd = weight_decay):
+ *   AdamW:    as fsdp_reduce_scatter_adam_cast
+ *   SGD:      d = g + wd*p; b = d if step == 1 else beta1*b + d; p = p - lr*b
+ *   Adamax:   d = g + wd*p; m = beta1*m + fp32(1-beta1)*d;
+ *             u = max(beta2*u, |d| + eps) (NaN if either side is NaN);
+ *             p = p - fp32(lr/(1-beta1^t)) * (m/u)
+ *   Adadelta: d = g + wd*p; s = beta1*s + fp32(1-beta1)*(d*d);
+ *             delta = (sqrt(a + eps)/sqrt(s + eps))*d;
+ *             a = beta1*a + fp32(1-beta1)*(delta*delta); p = p - lr*delta
+ * The rules are the textbook ones; the pages name the optimizers only.
+ *   state_dtype FSDP_F32: param is the fp32 master, state0/state1 fp32, and
+ *     shard_out (out_dtype, required) receives p rounded to nearest even.
+ *   state_dtype FSDP_BF16 / FSDP_F16: param, state0 and state1 hold that
+ *     dtype with no fp32 master ("Mixed Precision and FSDP": pure bf16;
+ *     "Harnessing FSDP's full power", item 4: FP16 master weights); each
+ *     value is widened, updated in fp32 and rounded to nearest even when
+ *     stored; param is itself the rank's compute-dtype shard, so shard_out
+ *     must be NULL and out_dtype equal to state_dtype.
+ *   grads        host array of `world` device pointers, padded_numel each.
+ *   param, state0, state1   device, padded_numel elements each, in place;
+ *                state1 must be NULL for SGD and non-NULL otherwise.
+ *   cfg          host; step >= 1, grad_scale > 0, optimizer and
+ *                reduce_dtype as above.
+ * Other arguments, in-place rules and errors as
+ * fsdp_reduce_scatter_adam_cast. */
+fsdp_status fsdp_reduce_scatter_step(const void *const *grads, fsdp_dtype grad_dtype, int world,
+                                     int64_t padded_numel, void *param, void *state0, void *state1,
+                                     fsdp_dtype state_dtype, void *shard_out, fsdp_dtype out_dtype,
+                                     const fsdp_step_config *cfg, int rank_begin, int rank_end,
+                                     uint32_t *nonfinite_count, void *stream);
 
 /* All-gather (device): every destination receives the whole rank-ordered
  * concatenation of the shards, full_k[j] = shard_out[j] for j < padded_numel,

@@ -22,6 +22,7 @@ FSDP_ERR_CUDA = 3
 FSDP_ERR_UNSUPPORTED_DTYPE = 4
 
 FSDP_F32, FSDP_BF16, FSDP_F16 = 0, 1, 2
+FSDP_OPT_ADAMW, FSDP_OPT_SGD, FSDP_OPT_ADAMAX, FSDP_OPT_ADADELTA = 0, 1, 2, 3
 
 # every symbol include/fsdp.h declares
 EXPORTS = (
@@ -30,6 +31,7 @@ EXPORTS = (
     "fsdp_flatten_pad",
     "fsdp_reduce_scatter_adam_cast",
     "fsdp_reduce_scatter_adam_cast_gather",
+    "fsdp_reduce_scatter_step",
     "fsdp_all_gather",
     "fsdp_status_string",
     "fsdp_last_cuda_error",
@@ -47,6 +49,12 @@ class FsdpAdamwHparams(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
                 ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64),
                 ("grad_scale", ctypes.c_float)]
+
+
+class FsdpStepConfig(ctypes.Structure):
+    _fields_ = [("optimizer", ctypes.c_int32), ("reduce_dtype", ctypes.c_int32), ("lr", ctypes.c_float),
+                ("beta1", ctypes.c_float), ("beta2", ctypes.c_float), ("eps", ctypes.c_float),
+                ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64), ("grad_scale", ctypes.c_float)]
 
 
 _lock = threading.Lock()
@@ -73,6 +81,8 @@ def load() -> ctypes.CDLL:
                                                     ctypes.POINTER(FsdpAdamwHparams), i32, i32, vp, vp]),
             "fsdp_reduce_scatter_adam_cast_gather": (i32, [vp, i32, i32, i64, vp, vp, vp, vp, i32, vp, i32,
                                                            ctypes.POINTER(FsdpAdamwHparams), i32, i32, vp, vp]),
+            "fsdp_reduce_scatter_step": (i32, [vp, i32, i32, i64, vp, vp, vp, i32, vp, i32,
+                                               ctypes.POINTER(FsdpStepConfig), i32, i32, vp, vp]),
             "fsdp_all_gather": (i32, [vp, i32, i32, i64, vp, i32, vp]),
             "fsdp_status_string": (ctypes.c_char_p, [i32]),
             "fsdp_last_cuda_error": (i32, []),

@@ -55,6 +55,24 @@ AdamScalars make_scalars(const fsdp_adamw_hparams &h, int world) {
 
 bool mul_overflows(int64_t a, int64_t b) { return a != 0 && b > INT64_MAX / a; }
 
+StepScalars make_step_scalars(const fsdp_step_config &c, int world) {
+    const double t = static_cast<double>(c.step);
+    StepScalars k;
+    k.c = static_cast<float>(1.0 / (static_cast<double>(world) * static_cast<double>(c.grad_scale)));
+    k.decay = static_cast<float>(1.0 - static_cast<double>(c.lr) * static_cast<double>(c.weight_decay));
+    k.beta1 = c.beta1;
+    k.beta2 = c.beta2;
+    k.omb1 = static_cast<float>(1.0 - static_cast<double>(c.beta1));
+    k.omb2 = static_cast<float>(1.0 - static_cast<double>(c.beta2));
+    k.alpha = static_cast<float>(static_cast<double>(c.lr) / (1.0 - pow(static_cast<double>(c.beta1), t)));
+    k.b2s = static_cast<float>(sqrt(1.0 - pow(static_cast<double>(c.beta2), t)));
+    k.eps = c.eps;
+    k.lr = c.lr;
+    k.wd = c.weight_decay;
+    k.first_step = c.step == 1 ? 1 : 0;
+    return k;
+}
+
 }  // namespace
 }  // namespace fsdp
 
@@ -257,6 +275,67 @@ fsdp_status fsdp_reduce_scatter_adam_cast_gather(const void *const *grads, fsdp_
     if (n_dst < 1) return FSDP_ERR_INVALID_ARG;
     return rsa_entry(grads, grad_dtype, world, padded_numel, master, exp_avg, exp_avg_sq, shard_out, out_dtype,
                      full_bufs, n_dst, hp, rank_begin, rank_end, nonfinite_count, stream);
+}
+
+fsdp_status fsdp_reduce_scatter_step(const void *const *grads, fsdp_dtype grad_dtype, int world,
+                                     int64_t padded_numel, void *param, void *state0, void *state1,
+                                     fsdp_dtype state_dtype, void *shard_out, fsdp_dtype out_dtype,
+                                     const fsdp_step_config *cfg, int rank_begin, int rank_end,
+                                     uint32_t *nonfinite_count, void *stream) {
+    if (!dtype_valid(grad_dtype) || !dtype_valid(out_dtype) || !dtype_valid(state_dtype))
+        return FSDP_ERR_UNSUPPORTED_DTYPE;
+    if (world < 1 || world > FSDP_MAX_WORLD || !grads || !cfg) return FSDP_ERR_INVALID_ARG;
+    if (cfg->optimizer < FSDP_OPT_ADAMW || cfg->optimizer > FSDP_OPT_ADADELTA) return FSDP_ERR_INVALID_ARG;
+    if (cfg->reduce_dtype != FSDP_F32 && cfg->reduce_dtype != grad_dtype) return FSDP_ERR_UNSUPPORTED_DTYPE;
+    if (state_dtype != FSDP_F32 && out_dtype != state_dtype) return FSDP_ERR_UNSUPPORTED_DTYPE;
+    if (padded_numel < 0 || padded_numel % world != 0) return FSDP_ERR_INVALID_ARG;
+    if (rank_begin < 0 || rank_begin > rank_end || rank_end > world) return FSDP_ERR_INVALID_ARG;
+    if (cfg->step < 1 || !(cfg->grad_scale > 0.0f) || !isfinite(cfg->grad_scale)) return FSDP_ERR_INVALID_ARG;
+    if (mul_overflows(padded_numel, 4)) return FSDP_ERR_INVALID_ARG;
+    const bool sgd = cfg->optimizer == FSDP_OPT_SGD;
+    if (sgd ? state1 != nullptr : state1 == nullptr) return FSDP_ERR_INVALID_ARG;
+    if (state_dtype == FSDP_F32 ? shard_out == nullptr : shard_out != nullptr) return FSDP_ERR_INVALID_ARG;
+    const int64_t S = padded_numel / world;
+    const int64_t begin = static_cast<int64_t>(rank_begin) * S, end = static_cast<int64_t>(rank_end) * S;
+    if (begin == end) return FSDP_OK;
+    if (!param || !state0) return FSDP_ERR_INVALID_ARG;
+    const size_t gs = static_cast<size_t>(dtype_size(grad_dtype)), ss = static_cast<size_t>(dtype_size(state_dtype));
+    const size_t os = static_cast<size_t>(dtype_size(out_dtype));
+    if (!aligned(param, ss) || !aligned(state0, ss) || !aligned(state1, ss) || !aligned(shard_out, os))
+        return FSDP_ERR_ALIGNMENT;
+    if (nonfinite_count && !aligned(nonfinite_count, 4)) return FSDP_ERR_ALIGNMENT;
+    const void *written[4] = {param, state0, state1, shard_out};
+    const size_t wbytes[4] = {padded_numel * ss, padded_numel * ss, state1 ? padded_numel * ss : 0,
+                              shard_out ? padded_numel * os : 0};
+    for (int i = 0; i < 4; ++i)
+        for (int k = i + 1; k < 4; ++k)
+            if (overlaps(written[i], wbytes[i], written[k], wbytes[k])) return FSDP_ERR_INVALID_ARG;
+    StepArgs a;
+    memset(&a, 0, sizeof(a));
+    for (int q = 0; q < world; ++q) {
+        if (!grads[q]) return FSDP_ERR_INVALID_ARG;
+        if (!aligned(grads[q], gs)) return FSDP_ERR_ALIGNMENT;
+        for (int i = 0; i < 4; ++i)
+            if (overlaps(grads[q], padded_numel * gs, written[i], wbytes[i])) return FSDP_ERR_INVALID_ARG;
+        a.grads[q] = grads[q];
+    }
+    a.param = param;
+    a.s0 = state0;
+    a.s1 = state1;
+    a.out = shard_out;
+    a.nonfinite = nonfinite_count;
+    a.begin = begin;
+    a.end = end;
+    a.k = make_step_scalars(*cfg, world);
+    a.world = world;
+    a.reduce_lowp = cfg->reduce_dtype != FSDP_F32 ? 1 : 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (cfg->optimizer) {
+        case FSDP_OPT_ADAMW: return launch_step_adamw(a, grad_dtype, out_dtype, state_dtype, s);
+        case FSDP_OPT_SGD: return launch_step_sgd(a, grad_dtype, out_dtype, state_dtype, s);
+        case FSDP_OPT_ADAMAX: return launch_step_adamax(a, grad_dtype, out_dtype, state_dtype, s);
+        default: return launch_step_adadelta(a, grad_dtype, out_dtype, state_dtype, s);
+    }
 }
 
 fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world, int64_t padded_numel,

@@ -162,6 +162,41 @@ fsdp_status launch_rsa_bf16(const RsaArgs &a, int out_dtype, cudaStream_t stream
 fsdp_status launch_rsa_f16(const RsaArgs &a, int out_dtype, cudaStream_t stream);
 fsdp_status launch_rsa_f32(const RsaArgs &a, int out_dtype, cudaStream_t stream);
 
+// Scalars of the variant steps (computed in double on the host, rounded once).
+struct StepScalars {
+    float c;             // 1 / (N * grad_scale)
+    float decay;         // AdamW: 1 - lr * wd
+    float beta1, beta2;
+    float omb1, omb2;    // 1 - beta1, 1 - beta2
+    float alpha;         // AdamW, Adamax: lr / (1 - beta1^t)
+    float b2s;           // AdamW: sqrt(1 - beta2^t)
+    float eps;
+    float lr;
+    float wd;
+    int first_step;      // SGD: t == 1
+};
+
+struct StepArgs {
+    const void *grads[FSDP_MAX_WORLD];
+    void *param;     // fp32 master, or the bf16/fp16 parameter shard
+    void *s0;
+    void *s1;        // NULL for SGD
+    void *out;       // compute-dtype shard when the state is fp32, else NULL
+    uint32_t *nonfinite;
+    int64_t begin;
+    int64_t end;
+    StepScalars k;
+    int world;
+    int reduce_lowp; // sum in the gradient dtype
+};
+
+// One translation unit per optimizer (step_adamw.cu, step_sgd.cu, ...).
+fsdp_status launch_step_adamw(const StepArgs &a, int grad_dtype, int out_dtype, int state_dtype, cudaStream_t s);
+fsdp_status launch_step_sgd(const StepArgs &a, int grad_dtype, int out_dtype, int state_dtype, cudaStream_t s);
+fsdp_status launch_step_adamax(const StepArgs &a, int grad_dtype, int out_dtype, int state_dtype, cudaStream_t s);
+fsdp_status launch_step_adadelta(const StepArgs &a, int grad_dtype, int out_dtype, int state_dtype,
+                                 cudaStream_t s);
+
 struct GatherArgs {
     const void *src;
     void *dst[FSDP_MAX_WORLD];

@@ -1,0 +1,291 @@
+// step_impl.cuh -- the fused reduce-scatter + optimizer step + cast for the
+// variant steps: other pointwise optimizers (SGD with momentum, Adamax,
+// Adadelta, and AdamW), a reduce-scatter summed in the gradient dtype, and a
+// parameter + state kept in bf16/fp16 without an fp32 master.
+//
+// Sources: "fairseq ... FSDP 实战指南", "限制与兼容性说明" (FSDP works with
+// the pointwise optimizers Adam, AdamW, Adadelta, Adamax, SGD) and
+// "参数定义与底层实现" (--fp32-reduce-scatter is off by default: the reduction
+// then runs in the gradient dtype); "Fully Sharded Data Parallel: faster AI
+// training with fewer GPUs", "Harnessing FSDP's full power", item 4 (FP16
+// master weights and FP16 reduce-scatter); "FSDP (Fully Sharded Data
+// Parallel)", "Mixed Precision and FSDP" (pure bf16: params and Adam state
+// in bf16, no fp32 master). The update rules are the textbook ones (the
+// pages print none):
+//   SGD (momentum mu = beta1): d = g + wd*p; b = d on the first step, else
+//       b = mu*b + d; p = p - lr*b
+//   Adamax: d = g + wd*p; m = b1*m + (1-b1)*d; u = max(b2*u, |d| + eps) (NaN
+//       if either side is); p = p - alpha*(m/u), alpha = lr/(1-b1^t)
+//   Adadelta (rho = beta1): d = g + wd*p; s = rho*s + (1-rho)*(d*d);
+//       delta = (sqrt(a+eps)/sqrt(s+eps))*d; a = rho*a + (1-rho)*(delta*delta);
+//       p = p - lr*delta
+//   AdamW: as the main kernel (decoupled decay, bias-corrected, eps outside).
+// Every operation is rounded to fp32 on its own. A gradient-dtype reduction
+// rounds each partial sum to the gradient dtype. Low-precision state is
+// widened, updated in fp32 and rounded (RNE) when stored; the parameter
+// buffer is then the rank's compute-dtype shard itself.
+//
+// Same memory schedule as the main kernel: per thread and iteration 8
+// consecutive elements, every load of the chunk issued before any
+// arithmetic, a scalar path for heads, tails and unaligned pointers.
+#pragma once
+
+#include "rsa_impl.cuh"
+
+namespace fsdp {
+namespace step {
+
+constexpr int kThreads = 256;
+
+template <int OPT> struct Opt;
+template <> struct Opt<FSDP_OPT_ADAMW> { static constexpr int kStates = 2; };
+template <> struct Opt<FSDP_OPT_SGD> { static constexpr int kStates = 1; };
+template <> struct Opt<FSDP_OPT_ADAMAX> { static constexpr int kStates = 2; };
+template <> struct Opt<FSDP_OPT_ADADELTA> { static constexpr int kStates = 2; };
+
+template <int OPT>
+__device__ __forceinline__ void update(float g, float &p, float &s0, float &s1, const StepScalars &k) {
+    if constexpr (OPT == FSDP_OPT_ADAMW) {
+        p = __fmul_rn(p, k.decay);
+        s0 = __fadd_rn(__fmul_rn(k.beta1, s0), __fmul_rn(k.omb1, g));
+        s1 = __fadd_rn(__fmul_rn(k.beta2, s1), __fmul_rn(k.omb2, __fmul_rn(g, g)));
+        const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(s1), k.b2s), k.eps);
+        p = __fsub_rn(p, __fmul_rn(k.alpha, __fdiv_rn(s0, denom)));
+    } else if constexpr (OPT == FSDP_OPT_SGD) {
+        const float d = __fadd_rn(g, __fmul_rn(k.wd, p));
+        s0 = k.first_step ? d : __fadd_rn(__fmul_rn(k.beta1, s0), d);
+        p = __fsub_rn(p, __fmul_rn(k.lr, s0));
+    } else if constexpr (OPT == FSDP_OPT_ADAMAX) {
+        const float d = __fadd_rn(g, __fmul_rn(k.wd, p));
+        s0 = __fadd_rn(__fmul_rn(k.beta1, s0), __fmul_rn(k.omb1, d));
+        const float a = __fmul_rn(k.beta2, s1), b = __fadd_rn(fabsf(d), k.eps);
+        s1 = (a > b || a != a) ? a : b;
+        p = __fsub_rn(p, __fmul_rn(k.alpha, __fdiv_rn(s0, s1)));
+    } else {  // FSDP_OPT_ADADELTA
+        const float d = __fadd_rn(g, __fmul_rn(k.wd, p));
+        s0 = __fadd_rn(__fmul_rn(k.beta1, s0), __fmul_rn(k.omb1, __fmul_rn(d, d)));
+        const float delta =
+            __fmul_rn(__fdiv_rn(__fsqrt_rn(__fadd_rn(s1, k.eps)), __fsqrt_rn(__fadd_rn(s0, k.eps))), d);
+        s1 = __fadd_rn(__fmul_rn(k.beta1, s1), __fmul_rn(k.omb1, __fmul_rn(delta, delta)));
+        p = __fsub_rn(p, __fmul_rn(k.lr, delta));
+    }
+}
+
+// x rounded to the gradient dtype and back (a partial sum of a reduction in
+// that dtype).
+template <int GD> __device__ __forceinline__ float round_to(float x) {
+    if constexpr (GD == FSDP_BF16) return __bfloat162float(__float2bfloat16_rn(x));
+    else if constexpr (GD == FSDP_F16) return __half2float(__float2half_rn(x));
+    else return x;
+}
+
+// 8 consecutive values of a buffer in dtype DT <-> floats.
+template <int DT> struct Words { uint4 w[DT == FSDP_F32 ? 2 : 1]; };
+
+template <int DT, bool STATE> __device__ __forceinline__ Words<DT> load8(const void *base, int64_t j0) {
+    Words<DT> r;
+    if constexpr (DT == FSDP_F32) {
+        const float *p = static_cast<const float *>(base) + j0;
+        if constexpr (STATE) {
+            const float4 a = ld_state(p), b = ld_state(p + 4);
+            r.w[0] = make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(a.z), __float_as_uint(a.w));
+            r.w[1] = make_uint4(__float_as_uint(b.x), __float_as_uint(b.y), __float_as_uint(b.z), __float_as_uint(b.w));
+        } else {
+            r.w[0] = ld_stream(p);
+            r.w[1] = ld_stream(p + 4);
+        }
+    } else {
+        const uint16_t *p = static_cast<const uint16_t *>(base) + j0;
+        if constexpr (STATE) {
+            const float4 a = ld_state(reinterpret_cast<const float *>(p));
+            r.w[0] = make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(a.z), __float_as_uint(a.w));
+        } else {
+            r.w[0] = ld_stream(p);
+        }
+    }
+    return r;
+}
+
+template <int DT> __device__ __forceinline__ void widen(const Words<DT> &x, float *f) { rsa::widen8<DT>(x.w, f); }
+
+template <int DT> __device__ __forceinline__ void store8(void *base, int64_t j0, const float *f) {
+    if constexpr (DT == FSDP_F32) {
+        float *p = static_cast<float *>(base) + j0;
+        st_state(p, make_float4(f[0], f[1], f[2], f[3]));
+        st_state(p + 4, make_float4(f[4], f[5], f[6], f[7]));
+    } else {
+        st_stream(static_cast<uint16_t *>(base) + j0,
+                  make_uint4(pack2<DT>(f[0], f[1]), pack2<DT>(f[2], f[3]), pack2<DT>(f[4], f[5]), pack2<DT>(f[6], f[7])));
+    }
+}
+
+template <int OPT, int NW, int GD, int OD, int SD>
+__device__ __forceinline__ uint32_t vec_chunk(const StepArgs &a, int world, int64_t j0) {
+    constexpr int K = Opt<OPT>::kStates;
+    float acc[8];
+    Words<SD> pw, s0w, s1w;
+    if constexpr (NW > 0) {
+        rsa::GradRegs<NW, GD> r;
+#pragma unroll
+        for (int q = 0; q < NW; ++q) rsa::load_grad8<GD>(a.grads[q], j0, r.w[q]);
+        pw = load8<SD, true>(a.param, j0);
+        s0w = load8<SD, true>(a.s0, j0);
+        if constexpr (K == 2) s1w = load8<SD, true>(a.s1, j0);
+        rsa::widen8<GD>(r.w[0], acc);
+#pragma unroll
+        for (int q = 1; q < NW; ++q) {
+            float f[8];
+            rsa::widen8<GD>(r.w[q], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                acc[e] = __fadd_rn(acc[e], f[e]);
+                if (a.reduce_lowp) acc[e] = round_to<GD>(acc[e]);
+            }
+        }
+    } else {
+        for (int q = 0; q < world; ++q) {
+            uint4 w[rsa::GradRegs<1, GD>::kWords];
+            rsa::load_grad8<GD>(a.grads[q], j0, w);
+            float f[8];
+            rsa::widen8<GD>(w, f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (q == 0) {
+                    acc[e] = f[e];
+                } else {
+                    acc[e] = __fadd_rn(acc[e], f[e]);
+                    if (a.reduce_lowp) acc[e] = round_to<GD>(acc[e]);
+                }
+            }
+        }
+        pw = load8<SD, true>(a.param, j0);
+        s0w = load8<SD, true>(a.s0, j0);
+        if constexpr (K == 2) s1w = load8<SD, true>(a.s1, j0);
+    }
+    float p[8], s0[8], s1[8];
+    widen<SD>(pw, p);
+    widen<SD>(s0w, s0);
+    if constexpr (K == 2) {
+        widen<SD>(s1w, s1);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s1[e] = 0.0f;
+    }
+    uint32_t bad = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float g = __fmul_rn(acc[e], a.k.c);
+        bad += rsa::nonfinite(g);
+        update<OPT>(g, p[e], s0[e], s1[e], a.k);
+    }
+    store8<SD>(a.param, j0, p);
+    store8<SD>(a.s0, j0, s0);
+    if constexpr (K == 2) store8<SD>(a.s1, j0, s1);
+    if constexpr (SD == FSDP_F32) store8<OD>(a.out, j0, p);
+    return bad;
+}
+
+template <int OPT, int GD, int OD, int SD>
+__device__ __forceinline__ uint32_t scalar_elem(const StepArgs &a, int world, int64_t j) {
+    constexpr int K = Opt<OPT>::kStates;
+    float acc = Dtype<GD>::load(a.grads[0], j);
+    for (int q = 1; q < world; ++q) {
+        acc = __fadd_rn(acc, Dtype<GD>::load(a.grads[q], j));
+        if (a.reduce_lowp) acc = round_to<GD>(acc);
+    }
+    const float g = __fmul_rn(acc, a.k.c);
+    float p = Dtype<SD>::load(a.param, j), s0 = Dtype<SD>::load(a.s0, j);
+    float s1 = K == 2 ? Dtype<SD>::load(a.s1, j) : 0.0f;
+    update<OPT>(g, p, s0, s1, a.k);
+    Dtype<SD>::store(a.param, j, p);
+    Dtype<SD>::store(a.s0, j, s0);
+    if constexpr (K == 2) Dtype<SD>::store(a.s1, j, s1);
+    if constexpr (SD == FSDP_F32) Dtype<OD>::store(a.out, j, p);
+    return rsa::nonfinite(g);
+}
+
+template <int OPT, int NW, int GD, int OD, int SD>
+__global__ void __launch_bounds__(kThreads)
+    step_kernel(const __grid_constant__ StepArgs a, int64_t vbegin, int64_t nchunks, int64_t vend) {
+    const int world = NW > 0 ? NW : a.world;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    uint32_t bad = 0;
+    for (int64_t c = tid; c < nchunks; c += stride) bad += vec_chunk<OPT, NW, GD, OD, SD>(a, world, vbegin + 8 * c);
+    const int64_t nhead = vbegin - a.begin;
+    const int64_t nrest = nhead + (a.end - vend);
+    for (int64_t e = tid; e < nrest; e += stride) {
+        const int64_t j = e < nhead ? a.begin + e : vend + (e - nhead);
+        bad += scalar_elem<OPT, GD, OD, SD>(a, world, j);
+    }
+    if (a.nonfinite != nullptr) {
+        const uint32_t total = __reduce_add_sync(0xffffffffu, bad);
+        if ((threadIdx.x & 31) == 0 && total) atomicAdd(a.nonfinite, total);
+    }
+}
+
+template <int OPT, int NW, int GD, int OD, int SD>
+fsdp_status launch_typed(const StepArgs &a, cudaStream_t stream) {
+    static int blocks_per_sm = 0;
+    if (blocks_per_sm == 0) {
+        int b = 0;
+        cudaError_t e =
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, step_kernel<OPT, NW, GD, OD, SD>, kThreads, 0);
+        if (e != cudaSuccess) return cuda_status(e);
+        blocks_per_sm = b > 0 ? b : 1;
+    }
+    bool vec = aligned(a.param, 16) && aligned(a.s0, 16) && aligned(a.s1, 16) && aligned(a.out, 16);
+    for (int q = 0; q < a.world; ++q) vec = vec && aligned(a.grads[q], 16);
+    int64_t vbegin = a.end, vend = a.end, nchunks = 0;
+    if (vec) {
+        vbegin = (a.begin + 7) / 8 * 8;
+        vend = a.end / 8 * 8;
+        if (vend > vbegin) {
+            nchunks = (vend - vbegin) / 8;
+        } else {
+            vbegin = vend = a.end;
+        }
+    }
+    const int64_t items = nchunks + (vbegin - a.begin) + (a.end - vend);
+    const int64_t need = (items + kThreads - 1) / kThreads;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
+    const int grid = static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
+    step_kernel<OPT, NW, GD, OD, SD><<<grid, kThreads, 0, stream>>>(a, vbegin, nchunks, vend);
+    return check_launch();
+}
+
+template <int OPT, int GD, int OD, int SD>
+fsdp_status launch_world(const StepArgs &a, cudaStream_t stream) {
+    switch (a.world) {
+        case 2: return launch_typed<OPT, 2, GD, OD, SD>(a, stream);
+        case 8: return launch_typed<OPT, 8, GD, OD, SD>(a, stream);
+        default: return launch_typed<OPT, 0, GD, OD, SD>(a, stream);
+    }
+}
+
+// (state dtype, out dtype) pairs: fp32 master with any compute dtype, or a
+// bf16/fp16 parameter that is its own shard.
+template <int OPT, int GD>
+fsdp_status launch_dtypes(const StepArgs &a, int out_dtype, int state_dtype, cudaStream_t stream) {
+    if (state_dtype == FSDP_F32) {
+        switch (out_dtype) {
+            case FSDP_BF16: return launch_world<OPT, GD, FSDP_BF16, FSDP_F32>(a, stream);
+            case FSDP_F16: return launch_world<OPT, GD, FSDP_F16, FSDP_F32>(a, stream);
+            default: return launch_world<OPT, GD, FSDP_F32, FSDP_F32>(a, stream);
+        }
+    }
+    if (state_dtype == FSDP_BF16) return launch_world<OPT, GD, FSDP_BF16, FSDP_BF16>(a, stream);
+    return launch_world<OPT, GD, FSDP_F16, FSDP_F16>(a, stream);
+}
+
+template <int OPT>
+fsdp_status launch_opt(const StepArgs &a, int grad_dtype, int out_dtype, int state_dtype, cudaStream_t stream) {
+    switch (grad_dtype) {
+        case FSDP_BF16: return launch_dtypes<OPT, FSDP_BF16>(a, out_dtype, state_dtype, stream);
+        case FSDP_F16: return launch_dtypes<OPT, FSDP_F16>(a, out_dtype, state_dtype, stream);
+        default: return launch_dtypes<OPT, FSDP_F32>(a, out_dtype, state_dtype, stream);
+    }
+}
+
+}  // namespace step
+}  // namespace fsdp

@@ -12,10 +12,10 @@ from typing import List, Optional, Sequence, Tuple
 import torch
 
 from . import _lib
-from ._lib import FsdpAdamwHparams, FsdpView
+from ._lib import FsdpAdamwHparams, FsdpStepConfig, FsdpView
 
 __all__ = [
-    "AdamWHParams", "FsdpError", "View",
+    "AdamWHParams", "StepConfig", "OPTIMIZERS", "FsdpError", "View", "fsdp_reduce_scatter_step",
     "fsdp_padded_numel", "fsdp_unflatten_views", "fsdp_flatten_pad",
     "fsdp_reduce_scatter_adam_cast", "fsdp_reduce_scatter_adam_cast_gather", "fsdp_all_gather",
     "fsdp_status_string",
@@ -47,6 +47,31 @@ class AdamWHParams:
     def to_c(self) -> FsdpAdamwHparams:
         return FsdpAdamwHparams(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay,
                                 int(self.step), self.grad_scale)
+
+
+OPTIMIZERS = {"adamw": _lib.FSDP_OPT_ADAMW, "sgd": _lib.FSDP_OPT_SGD, "adamax": _lib.FSDP_OPT_ADAMAX,
+              "adadelta": _lib.FSDP_OPT_ADADELTA}
+
+
+@dataclasses.dataclass(frozen=True)
+class StepConfig:
+    """fsdp_step_config: optimizer ("adamw", "sgd", "adamax", "adadelta"), the
+    reduction dtype (None = fp32 reduce-scatter, else the gradient dtype) and
+    the hyperparameters (beta1 is SGD's momentum and Adadelta's rho)."""
+    optimizer: str
+    lr: float
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.0
+    step: int = 1
+    grad_scale: float = 1.0
+    reduce_dtype: Optional[torch.dtype] = None
+
+    def to_c(self, grad_dtype: torch.dtype) -> FsdpStepConfig:
+        rd = _lib.FSDP_F32 if self.reduce_dtype is None else dtype_code(self.reduce_dtype)
+        return FsdpStepConfig(OPTIMIZERS[self.optimizer], rd, self.lr, self.beta1, self.beta2, self.eps,
+                              self.weight_decay, int(self.step), self.grad_scale)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -220,6 +245,39 @@ def fsdp_reduce_scatter_adam_cast_gather(grads: Sequence[torch.Tensor], master: 
         _dev(shard_out, "shard_out") if shard_out is not None else None, dtype_code(odt),
         _ptrs(full_bufs, "full_bufs"), len(full_bufs), ctypes.byref(hp), int(rank_begin), re, nf,
         _stream(stream)), "fsdp_reduce_scatter_adam_cast_gather")
+
+
+def fsdp_reduce_scatter_step(grads: Sequence[torch.Tensor], param: torch.Tensor, state0: torch.Tensor,
+                             state1: Optional[torch.Tensor], shard_out: Optional[torch.Tensor], config: StepConfig,
+                             rank_begin: int = 0, rank_end: Optional[int] = None,
+                             nonfinite_count: Optional[torch.Tensor] = None,
+                             stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Variant step: fused reduce-scatter + (AdamW | SGD | Adamax | Adadelta) + cast.
+
+    param/state0/state1: [P_pad], fp32 (then shard_out receives the cast) or
+    all bf16/fp16 (then param is the shard and shard_out must be None).
+    state1 is None for SGD."""
+    world = len(grads)
+    P_pad = param.numel()
+    gdt = grads[0].dtype if world else torch.bfloat16
+    for i, g in enumerate(grads):
+        if g.numel() != P_pad or g.dtype != gdt:
+            raise ValueError(f"grads[{i}] must hold {P_pad} elements of {gdt}")
+    sdt = param.dtype
+    for name, t in (("state0", state0), ("state1", state1)):
+        if t is not None and (t.dtype != sdt or t.numel() != P_pad):
+            raise ValueError(f"{name} must hold {P_pad} elements of {sdt}")
+    if shard_out is not None and shard_out.numel() != P_pad:
+        raise ValueError(f"shard_out must hold {P_pad} elements")
+    odt = shard_out.dtype if shard_out is not None else sdt
+    nf = _dev(nonfinite_count, "nonfinite_count") if nonfinite_count is not None else None
+    cfg = config.to_c(gdt)
+    re = world if rank_end is None else int(rank_end)
+    _check(_lib.load().fsdp_reduce_scatter_step(
+        _ptrs(grads, "grads") if world else None, dtype_code(gdt), world, P_pad, _dev(param, "param"),
+        _dev(state0, "state0"), _dev(state1, "state1") if state1 is not None else None, dtype_code(sdt),
+        _dev(shard_out, "shard_out") if shard_out is not None else None, dtype_code(odt), ctypes.byref(cfg),
+        int(rank_begin), re, nf, _stream(stream)), "fsdp_reduce_scatter_step")
 
 
 def fsdp_all_gather(shard_out: torch.Tensor, full_bufs: Sequence[torch.Tensor], world: int,

@@ -203,3 +203,31 @@ def test_fused_gather_rejects_invalid_arguments(lib):
     assert call(None, arr(FAKE + 0x5000000, FAKE + 0x5000008), 2) == E.FSDP_ERR_INVALID_ARG
     assert lib.fsdp_reduce_scatter_adam_cast(g, 1, 2, 16, FAKE + 0x1000000, FAKE + 0x2000000, FAKE + 0x3000000,
                                              None, 1, ctypes.byref(hp), 0, 2, None, None) == E.FSDP_ERR_INVALID_ARG
+
+
+def test_variant_step_rejects_invalid_arguments(lib):
+    from sharded_fsdp_reduce_gb300 import _lib as E
+    arr = lambda *p: (ctypes.c_void_p * len(p))(*p)
+    g = arr(FAKE + 0x100000, FAKE + 0x200000)
+
+    def call(opt=0, rd=0, sdt=0, odt=1, p=FAKE + 0x1000000, s0=FAKE + 0x2000000, s1=FAKE + 0x3000000,
+             out=FAKE + 0x4000000, step=1, P=16, gdt=1):
+        cfg = E.FsdpStepConfig(opt, rd, 1e-3, 0.9, 0.999, 1e-8, 0.0, step, 1.0)
+        return lib.fsdp_reduce_scatter_step(g, gdt, 2, P, p, s0, s1, sdt, out, odt, ctypes.byref(cfg), 0, 2, None,
+                                            None)
+    assert call(opt=4) == E.FSDP_ERR_INVALID_ARG
+    assert call(opt=-1) == E.FSDP_ERR_INVALID_ARG
+    assert call(rd=2) == E.FSDP_ERR_UNSUPPORTED_DTYPE            # f16 reduction of bf16 gradients
+    assert call(sdt=1, odt=2, out=None) == E.FSDP_ERR_UNSUPPORTED_DTYPE  # bf16 state, f16 out
+    assert call(sdt=7) == E.FSDP_ERR_UNSUPPORTED_DTYPE
+    assert call(opt=1) == E.FSDP_ERR_INVALID_ARG                 # SGD with a second state
+    assert call(opt=2, s1=None) == E.FSDP_ERR_INVALID_ARG        # Adamax without one
+    assert call(sdt=1, odt=1) == E.FSDP_ERR_INVALID_ARG          # bf16 state with a shard_out
+    assert call(out=None) == E.FSDP_ERR_INVALID_ARG              # fp32 state without shard_out
+    assert call(step=0) == E.FSDP_ERR_INVALID_ARG
+    assert call(P=15) == E.FSDP_ERR_INVALID_ARG
+    assert call(p=FAKE + 0x1000002) == E.FSDP_ERR_ALIGNMENT
+    assert call(s0=FAKE + 0x1000000 + 8) == E.FSDP_ERR_INVALID_ARG   # state overlaps the param
+    assert call(out=FAKE + 0x100000) == E.FSDP_ERR_INVALID_ARG       # shard_out on a gradient
+    assert call(P=0) == E.FSDP_OK
+    assert lib.fsdp_last_cuda_error() == 0
