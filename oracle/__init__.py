@@ -27,22 +27,31 @@ _DT = {"f32": F32, "bf16": BF16, "f16": F16}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fsdp_oracle.c")
-_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+# FSDP_ORACLE_LIB points the tests at another build of fsdp_oracle.c (the
+# mutation test plants one mistake per build and expects the pins to fail).
+_LIB_PATH = os.environ.get("FSDP_ORACLE_LIB") or os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
 
-def build(force: bool = False) -> str:
-    """Compile ``fsdp_oracle.c`` into ``liboracle.so`` (gcc, no FMA contraction)."""
-    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
-        return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+def compile_source(src: str, out: str) -> str:
+    """gcc build of an oracle source file (no FMA contraction, no fast-math)."""
+    tmp = out + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
            "-ffp-contract=off", "-fno-fast-math", "-Wall", "-Wextra", "-Wno-unused-parameter",
-           _SRC, "-o", tmp, "-lm"]
+           src, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile ``fsdp_oracle.c`` into ``liboracle.so``."""
+    if os.environ.get("FSDP_ORACLE_LIB"):
+        return _LIB_PATH
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    return compile_source(_SRC, _LIB_PATH)
 
 
 class HParams(ctypes.Structure):
