@@ -368,6 +368,9 @@ def run_ours(args):
             nstates = 1 + (s0 is not None) + (s1 is not None)
             nbytes = P * (N * gb + nstates * 2 * ss + (out.element_size() if out is not None else 0))
             lrv = 1.0 if opt == "adadelta" else cfg.lr
+            for st in (s0, s1):  # each optimizer starts from its own zero state
+                if st is not None:
+                    st.zero_()
 
             def run(tt, opt=opt, lowp=lowp, prm=prm, s0=s0, s1=s1, out=out, lrv=lrv):
                 F.fsdp_reduce_scatter_step(unit.grads, prm, s0, s1, out,
