@@ -292,12 +292,12 @@ fsdp_status fsdp_reduce_scatter_step(const void *const *grads, fsdp_dtype grad_d
     if (rank_begin < 0 || rank_begin > rank_end || rank_end > world) return FSDP_ERR_INVALID_ARG;
     if (cfg->step < 1 || !(cfg->grad_scale > 0.0f) || !isfinite(cfg->grad_scale)) return FSDP_ERR_INVALID_ARG;
     if (mul_overflows(padded_numel, 4)) return FSDP_ERR_INVALID_ARG;
-    const bool sgd = cfg->optimizer == FSDP_OPT_SGD;
-    if (sgd ? state1 != nullptr : state1 == nullptr) return FSDP_ERR_INVALID_ARG;
-    if (state_dtype == FSDP_F32 ? shard_out == nullptr : shard_out != nullptr) return FSDP_ERR_INVALID_ARG;
     const int64_t S = padded_numel / world;
     const int64_t begin = static_cast<int64_t>(rank_begin) * S, end = static_cast<int64_t>(rank_end) * S;
     if (begin == end) return FSDP_OK;
+    const bool sgd = cfg->optimizer == FSDP_OPT_SGD;
+    if (sgd ? state1 != nullptr : state1 == nullptr) return FSDP_ERR_INVALID_ARG;
+    if (state_dtype == FSDP_F32 ? shard_out == nullptr : shard_out != nullptr) return FSDP_ERR_INVALID_ARG;
     if (!param || !state0) return FSDP_ERR_INVALID_ARG;
     const size_t gs = static_cast<size_t>(dtype_size(grad_dtype)), ss = static_cast<size_t>(dtype_size(state_dtype));
     const size_t os = static_cast<size_t>(dtype_size(out_dtype));

@@ -512,3 +512,72 @@ def test_fused_gather_rejects_bad_arguments(F):
         F.fsdp_reduce_scatter_adam_cast_gather(grads, master, m, v, None, [fulls[0], fulls[0]], hp)
     torch.cuda.synchronize()
     assert not master.any() and not out.any() and not fulls[0].any()
+
+
+# ------------------------------------------------------------------ maximum and empty sizes
+
+def test_unit_beyond_2_pow_31_elements(F, orc):
+    # P_pad > 2^31: 64-bit indexing in the fused kernel, the bulk-copy gather
+    # and flatten; sampled comparison around the 2^31 boundary, the rank
+    # block boundary and random elements
+    world = 2
+    P = (1 << 31) + 24
+    grads = [torch.empty(P, dtype=torch.bfloat16, device=DEV) for _ in range(world)]
+    for r, g in enumerate(grads):
+        gen = torch.Generator(device=DEV)
+        gen.manual_seed(40 + r)
+        g.copy_(torch.randn(P, generator=gen, device=DEV).mul_(1e-3))
+    master = torch.empty(P, device=DEV)
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(39)
+    src = torch.rand(P, generator=gen, device=DEV).mul_(0.2).sub_(0.1)
+    F.fsdp_flatten_pad([src], world, out=master)
+    assert torch.equal(master, src)
+    del src
+    m = torch.zeros(P, device=DEV)
+    v = torch.zeros(P, device=DEV)
+    out = torch.empty(P, dtype=torch.bfloat16, device=DEV)
+    fulls = [torch.empty(P, dtype=torch.bfloat16, device=DEV) for _ in range(world)]
+    rng = np.random.default_rng(41)
+    S = P // world
+    idx = np.unique(np.concatenate([rng.integers(0, P, 1 << 18), np.arange((1 << 31) - 64, P),
+                                    np.arange(S - 64, S + 64), np.arange(64)]))
+    idx_t = torch.from_numpy(idx).to(DEV)
+    p_s = host(master[idx_t])
+    g_s = [host(g[idx_t]) for g in grads]
+    hp = F.AdamWHParams(1e-3, weight_decay=0.01)
+    F.fsdp_reduce_scatter_adam_cast(grads, master, m, v, out, hp)
+    F.fsdp_all_gather(out, fulls, world)
+    s = orc.scalars(orc.hparams(1e-3, 0.9, 0.999, 1e-8, 0.01, 1), world)
+    g_avg = orc.all_reduce_avg(g_s, "bf16", world, s.c)
+    m_s = np.zeros_like(p_s)
+    v_s = np.zeros_like(p_s)
+    orc.adamw(p_s, m_s, v_s, g_avg, s)
+    torch.cuda.synchronize()
+    assert_state_close(host(master[idx_t]), p_s, "master")
+    assert_state_close(host(m[idx_t]), m_s, "exp_avg")
+    assert_out_close(host(out[idx_t]), orc.cast_out(p_s, "bf16"), "bf16", "shard_out")
+    for f in fulls:
+        assert torch.equal(f.view(torch.int16), out.view(torch.int16))
+    assert F.fsdp_take_wait_timeouts() == 0
+    del grads, master, m, v, out, fulls
+    torch.cuda.empty_cache()
+
+
+def test_maximum_world_64(F, orc):
+    _run_flat(F, orc, 64, 64 * 37 + 11, "bf16", "bf16", steps=2, seed=64)
+    _run_flat(F, orc, 64, 64 * 1024, "f16", "f16", steps=1, scale=1024.0, seed=65)
+
+
+def test_empty_unit_is_a_no_op(F):
+    e32 = torch.empty(0, device=DEV)
+    e16 = torch.empty(0, dtype=torch.bfloat16, device=DEV)
+    F.fsdp_reduce_scatter_adam_cast([e16, e16], e32, e32.clone(), e32.clone(), e16.clone(), F.AdamWHParams(1e-3))
+    F.fsdp_all_gather(e16, [e16.clone()], 2)
+    F.fsdp_reduce_scatter_step([e16, e16], e32, e32.clone(), e32.clone(), e16.clone(), F.StepConfig("adamw", 1e-3))
+    flat, views = F.fsdp_flatten_pad([e16], 4)
+    assert flat.numel() == 0 and views[0].numel == 0
+    views, padded = F.fsdp_unflatten_views([(0,), (3, 0)], 8)
+    assert padded == 0
+    torch.cuda.synchronize()
+    assert F.fsdp_last_cuda_error() == 0
