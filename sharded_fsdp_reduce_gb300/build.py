@@ -21,8 +21,12 @@ BUILD = os.path.join(ROOT, "_build", "fsdpreduce")
 LIB = os.path.join(PKG, "libfsdpreduce.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
-              "-I", INCLUDE, "-I", CSRC]
+# Host code: hidden visibility (only the extern "C" entry points, marked
+# FSDP_API, are exported) and no GNU-unique symbols, so that the statics of
+# template instantiations stay private to this library even when another
+# build of it is loaded into the same process.
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden,-fno-gnu-unique",
+              "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 
 
 def nvcc() -> str:

@@ -8,6 +8,10 @@
 
 #include "common.cuh"
 
+// The library's exported symbols: the C ABI of include/fsdp.h and nothing else
+// (everything else is built with hidden visibility).
+#define FSDP_API __attribute__((visibility("default")))
+
 namespace fsdp {
 
 namespace {
@@ -80,14 +84,14 @@ using namespace fsdp;
 
 extern "C" {
 
-int64_t fsdp_padded_numel(int64_t numel, int world) {
+FSDP_API int64_t fsdp_padded_numel(int64_t numel, int world) {
     if (numel < 0 || world < 1) return -1;
     int64_t shards = numel / world;
     if (shards * world < numel) shards += 1;
     return shards * world;
 }
 
-fsdp_status fsdp_unflatten_views(const int64_t *shapes, const int32_t *ndims, int n_tensors, int world,
+FSDP_API fsdp_status fsdp_unflatten_views(const int64_t *shapes, const int32_t *ndims, int n_tensors, int world,
                                  fsdp_view *views_out, int64_t *padded_numel_out) {
     if (n_tensors < 0 || world < 1 || !padded_numel_out) return FSDP_ERR_INVALID_ARG;
     if (n_tensors > 0 && (!ndims || !views_out)) return FSDP_ERR_INVALID_ARG;
@@ -121,7 +125,7 @@ fsdp_status fsdp_unflatten_views(const int64_t *shapes, const int32_t *ndims, in
     return FSDP_OK;
 }
 
-fsdp_status fsdp_flatten_pad(const void *const *srcs, const int64_t *numels, int n_tensors, fsdp_dtype dtype,
+FSDP_API fsdp_status fsdp_flatten_pad(const void *const *srcs, const int64_t *numels, int n_tensors, fsdp_dtype dtype,
                              int world, void *dst_flat, int64_t dst_numel, fsdp_view *views_out,
                              void *stream) {
     if (!dtype_valid(dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
@@ -256,7 +260,7 @@ fsdp_status rsa_entry(const void *const *grads, fsdp_dtype grad_dtype, int world
 
 extern "C" {
 
-fsdp_status fsdp_reduce_scatter_adam_cast(const void *const *grads, fsdp_dtype grad_dtype, int world,
+FSDP_API fsdp_status fsdp_reduce_scatter_adam_cast(const void *const *grads, fsdp_dtype grad_dtype, int world,
                                           int64_t padded_numel, float *master, float *exp_avg,
                                           float *exp_avg_sq, void *shard_out, fsdp_dtype out_dtype,
                                           const fsdp_adamw_hparams *hp, int rank_begin, int rank_end,
@@ -266,7 +270,7 @@ fsdp_status fsdp_reduce_scatter_adam_cast(const void *const *grads, fsdp_dtype g
                      nullptr, 0, hp, rank_begin, rank_end, nonfinite_count, stream);
 }
 
-fsdp_status fsdp_reduce_scatter_adam_cast_gather(const void *const *grads, fsdp_dtype grad_dtype, int world,
+FSDP_API fsdp_status fsdp_reduce_scatter_adam_cast_gather(const void *const *grads, fsdp_dtype grad_dtype, int world,
                                                  int64_t padded_numel, float *master, float *exp_avg,
                                                  float *exp_avg_sq, void *shard_out, fsdp_dtype out_dtype,
                                                  void *const *full_bufs, int n_dst,
@@ -277,7 +281,7 @@ fsdp_status fsdp_reduce_scatter_adam_cast_gather(const void *const *grads, fsdp_
                      full_bufs, n_dst, hp, rank_begin, rank_end, nonfinite_count, stream);
 }
 
-fsdp_status fsdp_reduce_scatter_step(const void *const *grads, fsdp_dtype grad_dtype, int world,
+FSDP_API fsdp_status fsdp_reduce_scatter_step(const void *const *grads, fsdp_dtype grad_dtype, int world,
                                      int64_t padded_numel, void *param, void *state0, void *state1,
                                      fsdp_dtype state_dtype, void *shard_out, fsdp_dtype out_dtype,
                                      const fsdp_step_config *cfg, int rank_begin, int rank_end,
@@ -338,7 +342,7 @@ fsdp_status fsdp_reduce_scatter_step(const void *const *grads, fsdp_dtype grad_d
     }
 }
 
-fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world, int64_t padded_numel,
+FSDP_API fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world, int64_t padded_numel,
                             void *const *full_bufs, int n_dst, void *stream) {
     if (!dtype_valid(dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
     if (world < 1 || padded_numel < 0 || padded_numel % world != 0) return FSDP_ERR_INVALID_ARG;
@@ -365,7 +369,7 @@ fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world, 
     return launch_gather(a, static_cast<cudaStream_t>(stream));
 }
 
-const char *fsdp_status_string(fsdp_status status) {
+FSDP_API const char *fsdp_status_string(fsdp_status status) {
     switch (status) {
         case FSDP_OK: return "FSDP_OK";
         case FSDP_ERR_INVALID_ARG: return "FSDP_ERR_INVALID_ARG: invalid argument";
@@ -376,13 +380,13 @@ const char *fsdp_status_string(fsdp_status status) {
     }
 }
 
-int fsdp_last_cuda_error(void) { return g_last_cuda_error; }
+FSDP_API int fsdp_last_cuda_error(void) { return g_last_cuda_error; }
 
-fsdp_status fsdp_take_wait_timeouts(uint32_t *count_out) {
+FSDP_API fsdp_status fsdp_take_wait_timeouts(uint32_t *count_out) {
     if (!count_out) return FSDP_ERR_INVALID_ARG;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_status(e);
-    *count_out = take_gather_wait_timeouts();
+    *count_out = take_gather_wait_timeouts() + take_rsa_tma_wait_timeouts_bf16() + take_rsa_tma_wait_timeouts_f16();
     return FSDP_OK;
 }
 

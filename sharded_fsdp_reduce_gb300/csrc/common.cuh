@@ -206,8 +206,11 @@ struct GatherArgs {
 
 fsdp_status launch_gather(const GatherArgs &a, cudaStream_t stream);
 
-// Read and reset the count of bounded waits that gave up in the gather kernels.
+// Read and reset the count of bounded waits that gave up in the gather kernels
+// and in the shared-memory-staged fused kernels.
 uint32_t take_gather_wait_timeouts();
+uint32_t take_rsa_tma_wait_timeouts_bf16();
+uint32_t take_rsa_tma_wait_timeouts_f16();
 
 struct FlattenArgs {
     static constexpr int kBatch = 32;

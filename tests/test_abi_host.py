@@ -231,3 +231,17 @@ def test_variant_step_rejects_invalid_arguments(lib):
     assert call(out=FAKE + 0x100000) == E.FSDP_ERR_INVALID_ARG       # shard_out on a gradient
     assert call(P=0) == E.FSDP_OK
     assert lib.fsdp_last_cuda_error() == 0
+
+
+def test_exports_nothing_but_the_c_abi(lib):
+    # host code is built with hidden visibility: the dynamic symbol table holds
+    # the declared entry points and nothing else
+    import shutil
+    import subprocess
+    from sharded_fsdp_reduce_gb300 import _lib
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = sorted(line.split()[-1] for line in out.stdout.splitlines() if " T " in line)
+    assert exported == declared_functions()
