@@ -29,7 +29,7 @@ fsdp_status cuda_status(cudaError_t e) {
 int sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
-    const int slot = dev < kMaxDevices ? dev : 0;
+    const int slot = dev < kMaxDevices ? dev : 0;  // beyond 64 devices: slot 0's count (same part assumed)
     int n = g_sm_count[slot].load(std::memory_order_relaxed);
     if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;

@@ -114,6 +114,23 @@ template <> __device__ __forceinline__ uint32_t pack2<FSDP_F16>(float a, float b
 // SM count of the current device, cached per device.
 int sm_count();
 
+// Ordinal of the current device (0 if it cannot be read).
+inline int current_device() {
+    int dev = 0;
+    return cudaGetDevice(&dev) == cudaSuccess && dev >= 0 ? dev : 0;
+}
+
+// One-time per-device settings of a kernel (its shared-memory opt-in): a
+// flag per device ordinal.
+struct PerDeviceOnce {
+    static constexpr int kMaxDevices = 64;
+    bool done[kMaxDevices] = {};
+    bool is_done(int dev) const { return dev < kMaxDevices ? done[dev] : false; }
+    void mark(int dev) {
+        if (dev < kMaxDevices) done[dev] = true;
+    }
+};
+
 // Record the CUDA error behind an FSDP_ERR_CUDA for fsdp_last_cuda_error().
 fsdp_status cuda_status(cudaError_t e);
 

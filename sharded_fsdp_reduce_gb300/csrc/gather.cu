@@ -137,12 +137,17 @@ __global__ void __launch_bounds__(kTmaThreads)
 template <int ND>
 fsdp_status launch_tma(const GatherArgs &a, cudaStream_t stream) {
     static int blocks_per_sm = 0;
+    static PerDeviceOnce configured;  // the opt-in is a per-device function attribute
     const int smem = kStages * kTile;
-    if (blocks_per_sm == 0) {
+    const int dev = current_device();
+    if (!configured.is_done(dev)) {
         cudaError_t e = cudaFuncSetAttribute(gather_tma_kernel<ND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return cuda_status(e);
+        configured.mark(dev);
+    }
+    if (blocks_per_sm == 0) {
         int b = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, gather_tma_kernel<ND>, kTmaThreads, smem);
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, gather_tma_kernel<ND>, kTmaThreads, smem);
         if (e != cudaSuccess) return cuda_status(e);
         blocks_per_sm = b > 0 ? b : 1;
     }

@@ -177,13 +177,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int NW, int GD, int OD>
 fsdp_status launch(const RsaArgs &a, int64_t first_elem, int64_t ntiles, cudaStream_t stream) {
     using L = Stage<NW, GD, OD>;
-    static bool configured = false;
+    static PerDeviceOnce configured;  // the opt-in is a per-device function attribute
     const int smem = kStages * L::kBytes;
-    if (!configured) {
+    const int dev = current_device();
+    if (!configured.is_done(dev)) {
         cudaError_t e = cudaFuncSetAttribute(rsa_tma_kernel<NW, GD, OD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              smem);
         if (e != cudaSuccess) return cuda_status(e);
-        configured = true;
+        configured.mark(dev);
     }
     const int64_t cap = sm_count();
     const int grid = static_cast<int>(ntiles < cap ? ntiles : cap);
