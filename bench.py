@@ -50,8 +50,7 @@ WORKLOAD_NAMES = {
     "gpt3_13b": "gpt3_13b_block_unit_n8",
     "llama70b": "llama70b_block_unit_n8",
 }
-RSA_SOURCES = ("sharded_fsdp_reduce_gb300/csrc/rsa_impl.cuh", "sharded_fsdp_reduce_gb300/csrc/rsa_tma.cuh",
-               "sharded_fsdp_reduce_gb300/csrc/tma.cuh", "sharded_fsdp_reduce_gb300/csrc/common.cuh")
+RSA_SOURCES = ("sharded_fsdp_reduce_gb300/csrc/rsa_impl.cuh", "sharded_fsdp_reduce_gb300/csrc/common.cuh")
 
 
 # ---------------------------------------------------------------- helpers
@@ -430,7 +429,7 @@ def run_ours(args):
         "params_per_s": round(P_pad * world_size / (step_ms * 1e-3), 1),
         "fused_params_per_s": round(P_pad / (rsa_ms * 1e-3), 1),
         "roofline": {
-            "bound": "hbm", "kernel": "rsa_tma_kernel (fused reduce-scatter + AdamW + cast, TMA-staged)",
+            "bound": "hbm", "kernel": "rsa_kernel (fused reduce-scatter + AdamW + cast)",
             "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
             "fused_ms": round(rsa_ms, 4),

@@ -386,7 +386,7 @@ FSDP_API fsdp_status fsdp_take_wait_timeouts(uint32_t *count_out) {
     if (!count_out) return FSDP_ERR_INVALID_ARG;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_status(e);
-    *count_out = take_gather_wait_timeouts() + take_rsa_tma_wait_timeouts_bf16() + take_rsa_tma_wait_timeouts_f16();
+    *count_out = take_gather_wait_timeouts();
     return FSDP_OK;
 }
 

@@ -134,6 +134,18 @@ struct PerDeviceOnce {
 // Record the CUDA error behind an FSDP_ERR_CUDA for fsdp_last_cuda_error().
 fsdp_status cuda_status(cudaError_t e);
 
+// Grid of a non-persistent elementwise launch: enough blocks for about
+// `per_thread` work items per thread, but never less than one resident wave
+// (`wave` blocks) unless there is less work than that, and at least 1.
+inline int grid_for(int64_t items, int threads, int per_thread, int64_t wave) {
+    const int64_t need = (items + threads - 1) / threads;  // one item per thread
+    const int64_t want = (items + int64_t(threads) * per_thread - 1) / (int64_t(threads) * per_thread);
+    int64_t g = want > wave ? want : (need < wave ? need : wave);
+    if (g < 1) g = 1;
+    if (g > 0x7fffffff) g = 0x7fffffff;
+    return static_cast<int>(g);
+}
+
 // Check the launch that was just enqueued.
 inline fsdp_status check_launch() { return cuda_status(cudaGetLastError()); }
 
@@ -223,11 +235,8 @@ struct GatherArgs {
 
 fsdp_status launch_gather(const GatherArgs &a, cudaStream_t stream);
 
-// Read and reset the count of bounded waits that gave up in the gather kernels
-// and in the shared-memory-staged fused kernels.
+// Read and reset the count of bounded waits that gave up in the gather kernels.
 uint32_t take_gather_wait_timeouts();
-uint32_t take_rsa_tma_wait_timeouts_bf16();
-uint32_t take_rsa_tma_wait_timeouts_f16();
 
 struct FlattenArgs {
     static constexpr int kBatch = 32;

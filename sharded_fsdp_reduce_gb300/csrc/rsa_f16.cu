@@ -6,5 +6,4 @@ namespace fsdp {
 fsdp_status launch_rsa_f16(const RsaArgs &a, int out_dtype, cudaStream_t stream) {
     return rsa::launch_grad<FSDP_F16>(a, out_dtype, stream);
 }
-uint32_t take_rsa_tma_wait_timeouts_f16() { return rsa_tma::take_wait_timeouts(); }
 }  // namespace fsdp

@@ -27,7 +27,8 @@
 //
 // Same memory schedule as the main kernel: per thread and iteration 8
 // consecutive elements, every load of the chunk issued before any
-// arithmetic, a scalar path for heads, tails and unaligned pointers.
+// arithmetic, a scalar path for heads, tails and unaligned pointers, and a
+// non-persistent grid of about two chunks per thread.
 #pragma once
 
 #include "rsa_impl.cuh"
@@ -36,6 +37,7 @@ namespace fsdp {
 namespace step {
 
 constexpr int kThreads = 256;
+constexpr int kChunksPerThread = 2;  // grid sizing as the main kernel (not persistent)
 
 template <int OPT> struct Opt;
 template <> struct Opt<FSDP_OPT_ADAMW> { static constexpr int kStates = 2; };
@@ -247,9 +249,7 @@ fsdp_status launch_typed(const StepArgs &a, cudaStream_t stream) {
         }
     }
     const int64_t items = nchunks + (vbegin - a.begin) + (a.end - vend);
-    const int64_t need = (items + kThreads - 1) / kThreads;
-    const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
-    const int grid = static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
+    const int grid = grid_for(items, kThreads, kChunksPerThread, static_cast<int64_t>(sm_count()) * blocks_per_sm);
     step_kernel<OPT, NW, GD, OD, SD><<<grid, kThreads, 0, stream>>>(a, vbegin, nchunks, vend);
     return check_launch();
 }
