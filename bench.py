@@ -94,9 +94,10 @@ def recorded_traffic(workload: str):
     vals = {}
     with open(path) as f:
         for line in f:
-            if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_sha256")):
+            line = line.strip().lstrip("-").strip()  # markdown list items
+            if ":" in line and line.startswith(("traffic_bytes_per_launch", "kernel_source_sha256")):
                 k, v = line.split(":", 1)
-                vals[k.strip().lstrip("- ")] = v.strip().strip("`")
+                vals[k.strip()] = v.strip().strip("`")
     if vals.get("kernel_source_sha256") != kernel_source_hash():
         return None
     try:

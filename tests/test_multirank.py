@@ -63,3 +63,13 @@ def test_reference_arm_prints_on_rank0_only(tmp_path):
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["value"] > 0
+
+
+def test_recorded_traffic_matches_current_kernel_source():
+    # the committed ncu summary of the fused kernel carries the hash of the
+    # kernel sources it was measured on; bench.py reports its traffic only
+    # while that hash matches
+    import bench
+    t = bench.recorded_traffic("llama70b_block_unit_n8")
+    assert t is not None, "profiles/ summary missing or taken on another version of the kernel"
+    assert 0.99 * 42 * 855654400 <= t <= 1.01 * 42 * 855654400
