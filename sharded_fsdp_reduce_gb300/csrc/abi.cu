@@ -6,7 +6,7 @@
 
 #include <atomic>
 
-#include "common.cuh"
+#include "host.cuh"
 
 // The library's exported symbols: the C ABI of include/fsdp.h and nothing else
 // (everything else is built with hidden visibility).

@@ -1,4 +1,6 @@
-// common.cuh -- internal helpers of libfsdpreduce.so (not part of the ABI).
+// common.cuh -- device-side helpers of libfsdpreduce.so and the argument
+// structs its kernels receive (not part of the ABI). Host plumbing lives in
+// host.cuh.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -109,55 +111,7 @@ template <> __device__ __forceinline__ uint32_t pack2<FSDP_F16>(float a, float b
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// ---------------------------------------------------------------- host plumbing
-
-// SM count of the current device, cached per device.
-int sm_count();
-
-// Ordinal of the current device (0 if it cannot be read).
-inline int current_device() {
-    int dev = 0;
-    return cudaGetDevice(&dev) == cudaSuccess && dev >= 0 ? dev : 0;
-}
-
-// One-time per-device settings of a kernel (its shared-memory opt-in): a
-// flag per device ordinal.
-struct PerDeviceOnce {
-    static constexpr int kMaxDevices = 64;
-    bool done[kMaxDevices] = {};
-    bool is_done(int dev) const { return dev < kMaxDevices ? done[dev] : false; }
-    void mark(int dev) {
-        if (dev < kMaxDevices) done[dev] = true;
-    }
-};
-
-// Record the CUDA error behind an FSDP_ERR_CUDA for fsdp_last_cuda_error().
-fsdp_status cuda_status(cudaError_t e);
-
-// Grid of a non-persistent elementwise launch: enough blocks for about
-// `per_thread` work items per thread, but never less than one resident wave
-// (`wave` blocks) unless there is less work than that, and at least 1.
-inline int grid_for(int64_t items, int threads, int per_thread, int64_t wave) {
-    const int64_t need = (items + threads - 1) / threads;  // one item per thread
-    const int64_t want = (items + int64_t(threads) * per_thread - 1) / (int64_t(threads) * per_thread);
-    int64_t g = want > wave ? want : (need < wave ? need : wave);
-    if (g < 1) g = 1;
-    if (g > 0x7fffffff) g = 0x7fffffff;
-    return static_cast<int>(g);
-}
-
-// Check the launch that was just enqueued.
-inline fsdp_status check_launch() { return cuda_status(cudaGetLastError()); }
-
-inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// Byte ranges [a, a+na) and [b, b+nb) overlap.
-inline bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
-    uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return na && nb && x < y + nb && y < x + na;
-}
-
-// ---------------------------------------------------------------- kernel entry points (internal)
+// ---------------------------------------------------------------- kernel arguments
 
 struct AdamScalars {
     float c;         // 1 / (N * grad_scale)
@@ -185,11 +139,6 @@ struct RsaArgs {
     int n_full;
 };
 
-// One translation unit per gradient dtype (rsa_bf16.cu, rsa_f16.cu, rsa_f32.cu).
-// a.n_full > 0 selects the variant with the fused all-gather.
-fsdp_status launch_rsa_bf16(const RsaArgs &a, int out_dtype, cudaStream_t stream);
-fsdp_status launch_rsa_f16(const RsaArgs &a, int out_dtype, cudaStream_t stream);
-fsdp_status launch_rsa_f32(const RsaArgs &a, int out_dtype, cudaStream_t stream);
 
 // Scalars of the variant steps (computed in double on the host, rounded once).
 struct StepScalars {
@@ -219,12 +168,6 @@ struct StepArgs {
     int reduce_lowp; // sum in the gradient dtype
 };
 
-// One translation unit per optimizer (step_adamw.cu, step_sgd.cu, ...).
-fsdp_status launch_step_adamw(const StepArgs &a, int grad_dtype, int out_dtype, int state_dtype, cudaStream_t s);
-fsdp_status launch_step_sgd(const StepArgs &a, int grad_dtype, int out_dtype, int state_dtype, cudaStream_t s);
-fsdp_status launch_step_adamax(const StepArgs &a, int grad_dtype, int out_dtype, int state_dtype, cudaStream_t s);
-fsdp_status launch_step_adadelta(const StepArgs &a, int grad_dtype, int out_dtype, int state_dtype,
-                                 cudaStream_t s);
 
 struct GatherArgs {
     const void *src;
@@ -233,10 +176,6 @@ struct GatherArgs {
     int n_dst;
 };
 
-fsdp_status launch_gather(const GatherArgs &a, cudaStream_t stream);
-
-// Read and reset the count of bounded waits that gave up in the gather kernels.
-uint32_t take_gather_wait_timeouts();
 
 struct FlattenArgs {
     static constexpr int kBatch = 32;
@@ -248,6 +187,5 @@ struct FlattenArgs {
     int elem_size;
 };
 
-fsdp_status launch_flatten(const FlattenArgs &a, cudaStream_t stream);
 
 }  // namespace fsdp

@@ -6,7 +6,7 @@
 // module's parameters are flattened into a single tensor). One launch handles
 // up to FlattenArgs::kBatch segments, one per blockIdx.y; a segment with a
 // NULL source is zero-filled. Runs once per unit at set-up.
-#include "common.cuh"
+#include "host.cuh"
 
 namespace fsdp {
 namespace {

@@ -19,7 +19,7 @@
 // thread are. Fallback (unaligned pointers, small copies): every thread loads
 // one 16-byte word and stores it to every destination; a tail shorter than
 // 16 bytes moves in 2-byte units.
-#include "common.cuh"
+#include "host.cuh"
 #include "tma.cuh"
 
 namespace fsdp {
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kTmaThreads)
 
 template <int ND>
 fsdp_status launch_tma(const GatherArgs &a, cudaStream_t stream) {
-    static int blocks_per_sm = 0;
+    static std::atomic<int> occupancy{0};
     static PerDeviceOnce configured;  // the opt-in is a per-device function attribute
     const int smem = kStages * kTile;
     const int dev = current_device();
@@ -152,12 +152,9 @@ fsdp_status launch_tma(const GatherArgs &a, cudaStream_t stream) {
         if (e != cudaSuccess) return cuda_status(e);
         configured.mark(dev);
     }
-    if (blocks_per_sm == 0) {
-        int b = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, gather_tma_kernel<ND>, kTmaThreads, smem);
-        if (e != cudaSuccess) return cuda_status(e);
-        blocks_per_sm = b > 0 ? b : 1;
-    }
+    int blocks_per_sm = 1;
+    const fsdp_status so = cached_occupancy(occupancy, gather_tma_kernel<ND>, kTmaThreads, smem, &blocks_per_sm);
+    if (so != FSDP_OK) return so;
     const int64_t bulk = a.nbytes / 16 * 16;
     const int64_t ntiles = (bulk + kTile - 1) / kTile;
     const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm * FSDP_GATHER_GRID_MULT;
@@ -170,13 +167,10 @@ fsdp_status launch_tma(const GatherArgs &a, cudaStream_t stream) {
 
 template <int ND>
 fsdp_status launch_nd(const GatherArgs &a, cudaStream_t stream) {
-    static int blocks_per_sm = 0;
-    if (blocks_per_sm == 0) {
-        int b = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, gather_kernel<ND>, kThreads, 0);
-        if (e != cudaSuccess) return cuda_status(e);
-        blocks_per_sm = b > 0 ? b : 1;
-    }
+    static std::atomic<int> occupancy{0};
+    int blocks_per_sm = 1;
+    const fsdp_status so = cached_occupancy(occupancy, gather_kernel<ND>, kThreads, 0, &blocks_per_sm);
+    if (so != FSDP_OK) return so;
     bool vec = aligned(a.src, 16);
     for (int d = 0; d < a.n_dst; ++d) vec = vec && aligned(a.dst[d], 16);
     if (vec && a.nbytes >= kTmaMinBytes) return launch_tma<ND>(a, stream);

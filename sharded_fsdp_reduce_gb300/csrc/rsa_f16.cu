@@ -1,6 +1,6 @@
 // rsa_f16.cu -- instantiations of the fused reduce-scatter + AdamW + cast
 // kernel for f16 gradients (all output dtypes, N in {2, 4, 8} and generic N).
-#include "rsa_impl.cuh"
+#include "rsa_launch.cuh"
 
 namespace fsdp {
 fsdp_status launch_rsa_f16(const RsaArgs &a, int out_dtype, cudaStream_t stream) {

@@ -29,11 +29,8 @@
 // through the scalar path, which performs the same operations in the same
 // order.
 //
-// Grid. Not persistent: the grid is sized for about kChunksPerThread chunks
-// per thread (at least one resident wave), so many more CTAs than fit on the
-// GPU at once run in waves. Measured on the 70B and 13B units this is 7-8 %
-// faster than a grid of exactly one resident wave striding over the whole
-// range (e.g. 4.97 ms against 5.39-5.53 ms on the 70B unit).
+// The launch code (grid sizing, dispatch over N and dtypes) is in
+// rsa_launch.cuh.
 #pragma once
 
 #include "common.cuh"
@@ -48,12 +45,8 @@ namespace rsa {
 #ifndef FSDP_RSA_MIN_BLOCKS
 #define FSDP_RSA_MIN_BLOCKS 1
 #endif
-#ifndef FSDP_RSA_CPT
-#define FSDP_RSA_CPT 2
-#endif
 constexpr int kThreads = FSDP_RSA_THREADS;
 constexpr int kMinBlocks = FSDP_RSA_MIN_BLOCKS;
-constexpr int kChunksPerThread = FSDP_RSA_CPT;
 
 // AdamW on one element; each operation is rounded on its own (no FMA), in the
 // order of the documented definition.
@@ -213,60 +206,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     if (a.nonfinite != nullptr) {
         const uint32_t total = __reduce_add_sync(0xffffffffu, bad);
         if ((threadIdx.x & 31) == 0 && total) atomicAdd(a.nonfinite, total);
-    }
-}
-
-template <int NW, int GD, int OD, bool GATHER>
-fsdp_status launch_typed(const RsaArgs &a, cudaStream_t stream) {
-    static int blocks_per_sm = 0;  // occupancy of this instantiation (one device type)
-    if (blocks_per_sm == 0) {
-        int b = 0;
-        cudaError_t e =
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, rsa_kernel<NW, GD, OD, GATHER>, kThreads, 0);
-        if (e != cudaSuccess) return cuda_status(e);
-        blocks_per_sm = b > 0 ? b : 1;
-    }
-    bool vec = aligned(a.master, 16) && aligned(a.m, 16) && aligned(a.v, 16) && aligned(a.out, 16);
-    for (int q = 0; q < a.world; ++q) vec = vec && aligned(a.grads[q], 16);
-    for (int d = 0; d < a.n_full; ++d) vec = vec && aligned(a.full[d], 16);
-    int64_t vbegin = a.end, vend = a.end, nchunks = 0;
-    if (vec) {
-        vbegin = (a.begin + 7) / 8 * 8;
-        vend = a.end / 8 * 8;
-        if (vend > vbegin) {
-            nchunks = (vend - vbegin) / 8;
-        } else {
-            vbegin = vend = a.end;
-        }
-    }
-    const int64_t items = nchunks + (vbegin - a.begin) + (a.end - vend);
-    const int grid = grid_for(items, kThreads, kChunksPerThread, static_cast<int64_t>(sm_count()) * blocks_per_sm);
-    rsa_kernel<NW, GD, OD, GATHER><<<grid, kThreads, 0, stream>>>(a, vbegin, nchunks, vend);
-    return check_launch();
-}
-
-template <int GD, int OD, bool GATHER>
-fsdp_status launch_world(const RsaArgs &a, cudaStream_t stream) {
-    switch (a.world) {
-        case 2: return launch_typed<2, GD, OD, GATHER>(a, stream);
-        case 4: return launch_typed<4, GD, OD, GATHER>(a, stream);
-        case 8: return launch_typed<8, GD, OD, GATHER>(a, stream);
-        default: return launch_typed<0, GD, OD, GATHER>(a, stream);
-    }
-}
-
-template <int GD, int OD>
-fsdp_status launch_gather_flag(const RsaArgs &a, cudaStream_t stream) {
-    return a.n_full > 0 ? launch_world<GD, OD, true>(a, stream) : launch_world<GD, OD, false>(a, stream);
-}
-
-template <int GD>
-fsdp_status launch_grad(const RsaArgs &a, int out_dtype, cudaStream_t stream) {
-    switch (out_dtype) {
-        case FSDP_BF16: return launch_gather_flag<GD, FSDP_BF16>(a, stream);
-        case FSDP_F16: return launch_gather_flag<GD, FSDP_F16>(a, stream);
-        case FSDP_F32: return launch_gather_flag<GD, FSDP_F32>(a, stream);
-        default: return FSDP_ERR_UNSUPPORTED_DTYPE;
     }
 }
 

@@ -31,6 +31,7 @@
 // non-persistent grid of about two chunks per thread.
 #pragma once
 
+#include "host.cuh"
 #include "rsa_impl.cuh"
 
 namespace fsdp {
@@ -228,14 +229,10 @@ __global__ void __launch_bounds__(kThreads)
 
 template <int OPT, int NW, int GD, int OD, int SD>
 fsdp_status launch_typed(const StepArgs &a, cudaStream_t stream) {
-    static int blocks_per_sm = 0;
-    if (blocks_per_sm == 0) {
-        int b = 0;
-        cudaError_t e =
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, step_kernel<OPT, NW, GD, OD, SD>, kThreads, 0);
-        if (e != cudaSuccess) return cuda_status(e);
-        blocks_per_sm = b > 0 ? b : 1;
-    }
+    static std::atomic<int> occupancy{0};
+    int blocks_per_sm = 1;
+    const fsdp_status so = cached_occupancy(occupancy, step_kernel<OPT, NW, GD, OD, SD>, kThreads, 0, &blocks_per_sm);
+    if (so != FSDP_OK) return so;
     bool vec = aligned(a.param, 16) && aligned(a.s0, 16) && aligned(a.s1, 16) && aligned(a.out, 16);
     for (int q = 0; q < a.world; ++q) vec = vec && aligned(a.grads[q], 16);
     int64_t vbegin = a.end, vend = a.end, nchunks = 0;
