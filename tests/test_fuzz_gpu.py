@@ -1,0 +1,126 @@
+"""Seeded random configurations of the fused step against the oracle: world
+size, unit size, gradient/output dtypes, emulated rank subrange, pointer
+offsets (vector or scalar path), the fused all-gather and the variant
+optimizers, several steps each. Bars as in the other parity tests."""
+import numpy as np
+import pytest
+import torch
+
+import fsdp_inputs as fi
+from gpu_util import assert_out_close, assert_state_close, host
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+FMTS = ["bf16", "f16", "f32"]
+
+
+@pytest.fixture(scope="module")
+def F():
+    import __graft_entry__ as g
+    g.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import sharded_fsdp_reduce_gb300 as F
+    return F
+
+
+def _case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    world = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
+    P = int(rng.integers(1, 40000))
+    gfmt, ofmt = str(rng.choice(FMTS)), str(rng.choice(FMTS))
+    rb = int(rng.integers(0, world))
+    re = int(rng.integers(rb + 1, world + 1))
+    offset = int(rng.choice([0, 0, 1]))
+    gather = bool(rng.integers(0, 2))
+    scale = 1024.0 if gfmt == "f16" else 1.0
+    return rng, world, P, gfmt, ofmt, rb, re, offset, gather, scale
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_fuzz_fused_step(F, orc, seed):
+    rng, world, P, gfmt, ofmt, rb, re, offset, gather, scale = _case(seed)
+    P_pad = orc.padded_numel(P, world)
+    S = P_pad // world
+    gdt, odt = fi.torch_dtype(gfmt), fi.torch_dtype(ofmt)
+
+    def alloc(n, dt):
+        return torch.zeros(n + offset, dtype=dt, device=DEV)[offset:]
+
+    grads = [alloc(P_pad, gdt) for _ in range(world)]
+    master, m, v = (alloc(P_pad, torch.float32) for _ in range(3))
+    out = alloc(P_pad, odt)
+    fulls = [alloc(P_pad, odt) for _ in range(world)] if gather else []
+    p0 = orc.flatten_pad([rng.uniform(-0.1, 0.1, P).astype(np.float32)], world)
+    master.copy_(torch.from_numpy(p0))
+    p_o, m_o, v_o = p0.copy(), np.zeros(P_pad, np.float32), np.zeros(P_pad, np.float32)
+    lo, hi = rb * S, re * S
+    for t in (1, 2):
+        rows = []
+        for r in range(world):
+            x = torch.from_numpy(orc.flatten_pad([(rng.standard_normal(P) * 1e-2 * scale).astype(np.float32)], world))
+            rows.append(x.to(gdt))
+            grads[r].copy_(rows[-1].to(DEV))
+        hp = F.AdamWHParams(1e-3, 0.9, 0.999, 1e-8, 0.01, t, scale)
+        if gather:
+            F.fsdp_reduce_scatter_adam_cast_gather(grads, master, m, v, out, fulls, hp, rank_begin=rb, rank_end=re)
+        else:
+            F.fsdp_reduce_scatter_adam_cast(grads, master, m, v, out, hp, rank_begin=rb, rank_end=re)
+        # the oracle updates every rank; only [lo, hi) is compared, the rest must be untouched
+        before = p_o.copy(), m_o.copy(), v_o.copy()
+        shards_o, _ = orc.fsdp_step([host(x) for x in rows], gfmt, world, p_o, m_o, v_o, ofmt,
+                                    orc.hparams(1e-3, 0.9, 0.999, 1e-8, 0.01, t, scale))
+        for arr, old in zip((p_o, m_o, v_o), before):  # ranks outside the subrange keep their state
+            arr[:lo] = old[:lo]
+            arr[hi:] = old[hi:]
+        torch.cuda.synchronize()
+        tag = f"seed={seed} N={world} P={P} {gfmt}->{ofmt} ranks=[{rb},{re}) off={offset} gather={gather} t={t}"
+        assert_state_close(host(master), p_o, "master " + tag)
+        assert_state_close(host(m), m_o, "exp_avg " + tag)
+        assert_state_close(host(v), v_o, "exp_avg_sq " + tag)
+        assert_out_close(host(out)[lo:hi], shards_o[lo:hi], ofmt, "shard_out " + tag)
+        for f in fulls:
+            np.testing.assert_array_equal(host(f)[lo:hi].view(np.uint8), host(out)[lo:hi].view(np.uint8))
+    if rb > 0 or re < world:
+        assert not host(out)[:lo].view(np.uint8).any() and not host(out)[hi:].view(np.uint8).any()
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_fuzz_variant_step(F, orc, seed):
+    rng = np.random.default_rng(5000 + seed)
+    opt = str(rng.choice(["adamw", "sgd", "adamax", "adadelta"]))
+    world = int(rng.choice([1, 2, 3, 8]))
+    P = int(rng.integers(1, 30000))
+    gfmt = str(rng.choice(FMTS))
+    sfmt = str(rng.choice(["f32", "bf16", "f16"]))
+    ofmt = str(rng.choice(FMTS)) if sfmt == "f32" else sfmt
+    lowp = bool(rng.integers(0, 2)) and gfmt != "f32"
+    scale = 1024.0 if gfmt == "f16" else 1.0
+    lr, b1, b2, eps, wd = {"adamw": (1e-3, 0.9, 0.999, 1e-8, 0.01), "sgd": (1e-2, 0.9, 0.0, 0.0, 1e-2),
+                           "adamax": (2e-3, 0.9, 0.999, 1e-8, 1e-2), "adadelta": (1.0, 0.9, 0.0, 1e-6, 1e-2)}[opt]
+    P_pad = orc.padded_numel(P, world)
+    gdt, sdt = fi.torch_dtype(gfmt), fi.torch_dtype(sfmt)
+    ns = 1 if opt == "sgd" else 2
+    grads = [torch.zeros(P_pad, dtype=gdt, device=DEV) for _ in range(world)]
+    p0 = torch.from_numpy(orc.flatten_pad([rng.uniform(-0.1, 0.1, P).astype(np.float32)], world)).to(sdt)
+    param = p0.to(DEV)
+    states = [torch.zeros(P_pad, dtype=sdt, device=DEV) for _ in range(ns)]
+    out = torch.zeros(P_pad, dtype=fi.torch_dtype(ofmt), device=DEV) if sfmt == "f32" else None
+    p_o = host(p0)
+    s_o = [np.zeros(P_pad, orc.np_storage(sfmt)) for _ in range(ns)]
+    for t in (1, 2, 3):
+        rows = [torch.from_numpy(orc.flatten_pad([(rng.standard_normal(P) * 1e-2 * scale).astype(np.float32)],
+                                                 world)).to(gdt) for _ in range(world)]
+        for g, r in zip(grads, rows):
+            g.copy_(r.to(DEV))
+        cfg = F.StepConfig(opt, lr, b1, b2, eps, wd, t, scale, reduce_dtype=gdt if lowp else None)
+        F.fsdp_reduce_scatter_step(grads, param, states[0], states[1] if ns == 2 else None, out, cfg)
+        shards_o, _ = orc.step_ex(opt, lowp, [host(r) for r in rows], gfmt, world, p_o, s_o[0],
+                                  s_o[1] if ns == 2 else None, sfmt, ofmt, orc.hparams(lr, b1, b2, eps, wd, t, scale))
+        torch.cuda.synchronize()
+        tag = f"seed={seed} {opt} N={world} P={P} {gfmt} state={sfmt} out={ofmt} lowp={lowp} t={t}"
+        cmp = assert_state_close if sfmt == "f32" else (lambda a, b, w: assert_out_close(a, b, sfmt, w))
+        cmp(host(param), p_o, "param " + tag)
+        for k in range(ns):
+            cmp(host(states[k]), s_o[k], f"state{k} " + tag)
+        if out is not None:
+            assert_out_close(host(out), shards_o, ofmt, "shard_out " + tag)
