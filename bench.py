@@ -304,17 +304,26 @@ def run_ours(args):
     launches = K * (1 + cfg.gathers)  # kernels of ours in the timed regions (device step, then e2e)
 
     # ---- end to end through the binding's host-buffer step: every step copies
-    # its N gradient buffers in from pinned host memory and its compute-dtype
-    # parameters back out (consecutive steps overlap their copies and kernels)
+    # its N gradient buffers in from pinned host memory and reads the step's
+    # result back: its non-finite-gradient count (the metric a trainer checks
+    # every step; the gathered parameters stay on the GPU for the next
+    # forward). --e2e-read-params reads the compute-dtype parameters instead.
+    # Consecutive steps overlap their copies and kernels.
     Ke = max(3, min(args.e2e_steps, K))
     host_grads = [torch.empty(P_pad, dtype=gdt, pin_memory=True) for _ in range(N)]
     for r in range(N):
         host_grads[r].copy_(unit.grads[r])
-    host_out = torch.empty(P_pad, dtype=odt, pin_memory=True)
+    counter = torch.zeros(1, dtype=torch.int32, device=dev)
+    if args.e2e_read_params:
+        host_out, host_nf = torch.empty(P_pad, dtype=odt, pin_memory=True), None
+        d2h = host_out.numel() * host_out.element_size()
+    else:
+        host_out, host_nf = None, torch.zeros(1, dtype=torch.int32, pin_memory=True)
+        d2h = host_nf.numel() * host_nf.element_size()
     h2d = sum(g.numel() * g.element_size() for g in host_grads)
-    d2h = host_out.numel() * host_out.element_size()
     t += 1
-    unit.step_from_host(host_grads, host_out, hp(t), gathers=cfg.gathers)  # sets up the streams
+    unit.step_from_host(host_grads, host_out, hp(t), gathers=cfg.gathers, nonfinite_count=counter,
+                        host_nonfinite=host_nf)  # sets up the streams
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if world_size > 1:
@@ -322,10 +331,13 @@ def run_ours(args):
     e0.record(stream)
     for _ in range(Ke):
         t += 1
-        unit.step_from_host(host_grads, host_out, hp(t), gathers=cfg.gathers)
+        unit.step_from_host(host_grads, host_out, hp(t), gathers=cfg.gathers, nonfinite_count=counter,
+                            host_nonfinite=host_nf)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / Ke
+    if host_nf is not None and int(host_nf.item()) != 0:
+        raise RuntimeError("e2e steps reported non-finite gradients")
     launches += Ke * (1 + cfg.gathers)
 
     # ---- variants of the same step (same byte model): the first all-gather
@@ -437,7 +449,8 @@ def run_ours(args):
         },
         "e2e": {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 3), "steps": Ke,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "d2h": "compute-dtype parameters" if args.e2e_read_params else "non-finite gradient count"},
         "gpu_launches": launches,
         "variants": {k: dict(v, value=round(world_size * (rsa_b + P_pad * unit.shard_out.element_size()
                                                            * (1 + len(unit.full)) * v["gathers_per_step"])
@@ -497,6 +510,8 @@ def main(argv=None):
                     help="replace the unit by one flat tensor of this many parameters (small profiling cases)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-read-params", action="store_true",
+                    help="e2e reads the compute-dtype parameters back each step instead of the step's metric")
     ap.add_argument("--no-variants", action="store_true", help="skip the fused-gather variant timings")
     ap.add_argument("--cpu-sample", type=int, default=1 << 24, help="elements in the CPU-baseline sample")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline time budget")

@@ -87,18 +87,23 @@ class FlatParamUnit:
         for _ in range(gathers):
             self.all_gather(stream)
 
-    def step_from_host(self, host_grads: Sequence[torch.Tensor], host_out: torch.Tensor, hp: AdamWHParams,
-                       gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None) -> None:
-        """One step whose N gradient buffers come from pinned host memory and
-        whose compute-dtype parameters (shard_out, all ranks' shards) go back
-        to pinned host memory. Asynchronous; consecutive calls overlap: the
-        host-to-device copy of a step runs on its own stream into a second
-        set of gradient buffers while the previous step's kernels and
-        device-to-host copy run. host_out is complete once the current stream
-        is synchronized (or after the next call's kernels have started)."""
+    def step_from_host(self, host_grads: Sequence[torch.Tensor], host_out: Optional[torch.Tensor], hp: AdamWHParams,
+                       gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None,
+                       host_nonfinite: Optional[torch.Tensor] = None) -> None:
+        """One step whose N gradient buffers come from pinned host memory.
+        Its results go back to pinned host memory as asked: host_out receives
+        the compute-dtype parameters (shard_out, all ranks' shards);
+        host_nonfinite receives the step's count of non-finite averaged
+        gradients (nonfinite_count is then required; it is zeroed first).
+        Asynchronous; consecutive calls overlap: the host-to-device copy of a
+        step runs on its own stream into a second set of gradient buffers
+        while the previous step's kernels and device-to-host copies run. The
+        host buffers are complete once the current stream is synchronized."""
+        if host_nonfinite is not None and nonfinite_count is None:
+            raise ValueError("host_nonfinite needs a device nonfinite_count")
         if self._host is None:
             self._host = _HostPipeline(self)
-        self._host.step(host_grads, host_out, hp, gathers, nonfinite_count)
+        self._host.step(host_grads, host_out, hp, gathers, nonfinite_count, host_nonfinite)
 
     def step_bytes(self, gathers: int = 1) -> Tuple[int, int]:
         """Algorithmic bytes of one step: (fused kernel, all-gathers)."""
@@ -124,7 +129,7 @@ class _HostPipeline:
         self.copy_out = torch.cuda.Stream(device=unit.device)
         self.i = 0
 
-    def step(self, host_grads, host_out, hp, gathers, nonfinite_count):
+    def step(self, host_grads, host_out, hp, gathers, nonfinite_count, host_nonfinite):
         u = self.unit
         if len(host_grads) != u.world:
             raise ValueError(f"need {u.world} host gradient buffers")
@@ -138,13 +143,18 @@ class _HostPipeline:
                 g.copy_(h, non_blocking=True)
         compute.wait_stream(self.copy_in)
         if self.out_read is not None:
-            compute.wait_event(self.out_read)   # shard_out is about to be rewritten
+            compute.wait_event(self.out_read)   # shard_out / the counter are about to be rewritten
+        if host_nonfinite is not None:
+            nonfinite_count.zero_()
         fsdp_reduce_scatter_adam_cast(gset, u.master, u.exp_avg, u.exp_avg_sq, u.shard_out, hp,
                                       nonfinite_count=nonfinite_count, stream=compute)
         self.read_done[k] = compute.record_event()
         self.copy_out.wait_event(self.read_done[k])
         with torch.cuda.stream(self.copy_out):
-            host_out.copy_(u.shard_out, non_blocking=True)
+            if host_out is not None:
+                host_out.copy_(u.shard_out, non_blocking=True)
+            if host_nonfinite is not None:
+                host_nonfinite.copy_(nonfinite_count, non_blocking=True)
         self.out_read = self.copy_out.record_event()
         for _ in range(gathers):
             fsdp_all_gather(u.shard_out, u.full, u.world, stream=compute)

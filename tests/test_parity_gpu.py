@@ -581,3 +581,28 @@ def test_empty_unit_is_a_no_op(F):
     assert padded == 0
     torch.cuda.synchronize()
     assert F.fsdp_last_cuda_error() == 0
+
+
+def test_step_from_host_metric_readback(F):
+    # the host-buffer step can hand back the step's non-finite count instead of
+    # the parameters; planted non-finite gradients show up in it
+    cfg = fi.CONFIGS["tiny"]
+    N = cfg.world
+    unit = new_unit(F, cfg)
+    unit.load_master(split_views(unit, fi.gen_master(cfg).to(DEV)))
+    counter = torch.zeros(1, dtype=torch.int32, device=DEV)
+    results, keep = [], []
+    for t in (1, 2, 3):
+        host = [fi.gen_grad(cfg, r, t) for r in range(N)]
+        padded = [torch.zeros(unit.padded_numel, dtype=host[0].dtype).pin_memory() for _ in range(N)]
+        for h, p in zip(host, padded):
+            p[:h.numel()].copy_(h)
+        if t == 2:
+            padded[0][5] = float("inf")
+            padded[1][9] = float("nan")
+        out = torch.zeros(1, dtype=torch.int32).pin_memory()
+        unit.step_from_host(padded, None, hp_for(F, cfg, t), nonfinite_count=counter, host_nonfinite=out)
+        results.append(out)
+        keep.append(padded)  # host buffers stay alive until the copies are done
+    torch.cuda.synchronize()
+    assert [int(r.item()) for r in results] == [0, 2, 0]
