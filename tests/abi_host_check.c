@@ -1,0 +1,63 @@
+/* Plain-C client of include/fsdp.h: compiled with gcc -std=c11 -Wall -Werror
+ * and linked against libfsdpreduce.so by tests/test_c_client.py. It calls
+ * only host-side entry points and argument checks that return before any
+ * CUDA work, so it runs without a GPU. Prints "ok" and exits 0 on success. */
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "fsdp.h"
+
+#define CHECK(cond)                                                 \
+    do {                                                            \
+        if (!(cond)) {                                              \
+            fprintf(stderr, "check failed: %s (line %d)\n", #cond, __LINE__); \
+            return 1;                                               \
+        }                                                           \
+    } while (0)
+
+int main(void) {
+    CHECK(fsdp_padded_numel(4099, 2) == 4100);
+    CHECK(fsdp_padded_numel(855654400, 8) == 855654400);
+    CHECK(fsdp_padded_numel(-1, 2) == -1);
+
+    /* the tiny unit's layout: w[64,64], b[3] */
+    const int64_t shapes[] = {64, 64, 3};
+    const int32_t ndims[] = {2, 1};
+    fsdp_view views[2];
+    int64_t padded = 0;
+    CHECK(fsdp_unflatten_views(shapes, ndims, 2, 2, views, &padded) == FSDP_OK);
+    CHECK(padded == 4100);
+    CHECK(views[0].offset == 0 && views[0].numel == 4096 && views[0].ndim == 2 && views[0].shape[1] == 64);
+    CHECK(views[1].offset == 4096 && views[1].numel == 3 && views[1].shape[0] == 3);
+
+    CHECK(strncmp(fsdp_status_string(FSDP_OK), "FSDP_OK", 7) == 0);
+    CHECK(strncmp(fsdp_status_string(FSDP_ERR_ALIGNMENT), "FSDP_ERR_ALIGNMENT", 18) == 0);
+
+    /* argument checks that fail on the host before any CUDA call */
+    fsdp_adamw_hparams hp = {1e-3f, 0.9f, 0.999f, 1e-8f, 0.0f, 0 /* step 0: invalid */, 1.0f};
+    const void *grads[2] = {(const void *)0x100000, (const void *)0x200000};
+    CHECK(fsdp_reduce_scatter_adam_cast(grads, FSDP_BF16, 2, 16, (float *)0x1000000, (float *)0x2000000,
+                                        (float *)0x3000000, (void *)0x4000000, FSDP_BF16, &hp, 0, 2, NULL,
+                                        NULL) == FSDP_ERR_INVALID_ARG);
+    hp.step = 1;
+    CHECK(fsdp_reduce_scatter_adam_cast(grads, (fsdp_dtype)7, 2, 16, (float *)0x1000000, (float *)0x2000000,
+                                        (float *)0x3000000, (void *)0x4000000, FSDP_BF16, &hp, 0, 2, NULL,
+                                        NULL) == FSDP_ERR_UNSUPPORTED_DTYPE);
+    void *dst[1] = {(void *)0x5000001};
+    CHECK(fsdp_all_gather((const void *)0x4000000, FSDP_BF16, 2, 16, dst, 1, NULL) == FSDP_ERR_ALIGNMENT);
+    fsdp_step_config cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.optimizer = FSDP_OPT_SGD;
+    cfg.reduce_dtype = FSDP_F32;
+    cfg.lr = 1e-2f;
+    cfg.step = 1;
+    cfg.grad_scale = 1.0f;
+    CHECK(fsdp_reduce_scatter_step(grads, FSDP_BF16, 2, 16, (void *)0x1000000, (void *)0x2000000,
+                                   (void *)0x3000000 /* SGD takes one state */, FSDP_F32, (void *)0x4000000,
+                                   FSDP_BF16, &cfg, 0, 2, NULL, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_take_wait_timeouts(NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_last_cuda_error() == 0);
+    printf("ok\n");
+    return 0;
+}

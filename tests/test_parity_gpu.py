@@ -606,3 +606,48 @@ def test_step_from_host_metric_readback(F):
         keep.append(padded)  # host buffers stay alive until the copies are done
     torch.cuda.synchronize()
     assert [int(r.item()) for r in results] == [0, 2, 0]
+
+
+def test_concurrent_host_threads(F):
+    # two host threads step their own units on their own streams at once (the
+    # library's launch caches are shared); results equal sequential runs
+    import threading
+    cfgs = [fi.CONFIGS["gpt2_small"], fi.CONFIGS["gpt2_large"]]
+
+    def make(cfg):
+        u = new_unit(F, cfg)
+        u.load_master([fi.gen_master(cfg, device=DEV)])
+        for r in range(cfg.world):
+            u.load_grad(r, [fi.gen_grad(cfg, r, 1, device=DEV)])
+        return u
+
+    def run(u, cfg, stream, errors):
+        try:
+            with torch.cuda.stream(stream):
+                for t in range(1, 6):
+                    u.step(hp_for(F, cfg, t), gathers=2, stream=stream, fuse_gather=(t % 2 == 0))
+            stream.synchronize()
+        except Exception as e:  # surfaced below
+            errors.append(e)
+
+    seq = [make(c) for c in cfgs]
+    for u, c in zip(seq, cfgs):
+        run(u, c, torch.cuda.current_stream(), [])
+    torch.cuda.synchronize()
+    par = [make(c) for c in cfgs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in cfgs]
+    errors = []
+    threads = [threading.Thread(target=run, args=(u, c, s, errors)) for u, c, s in zip(par, cfgs, streams)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for a, b in zip(seq, par):
+        for x, y in ((a.master, b.master), (a.exp_avg, b.exp_avg), (a.exp_avg_sq, b.exp_avg_sq)):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+        assert torch.equal(a.shard_out.view(torch.int16), b.shard_out.view(torch.int16))
+        for f, g in zip(a.full, b.full):
+            assert torch.equal(f.view(torch.int16), g.view(torch.int16))
