@@ -466,3 +466,4 @@ def test_tiny_trajectory_within_fp64_shadow(orc):
         orc.adamw_f64(p64, m64, v64, g64, hp)
         assert np.all(np.abs(p32 - p64) <= t * 4 * u * (np.abs(p64) + cfg.lr))
         assert np.all(np.abs(v32 - v64) <= (t * 6 * u + 2e-6) * v64 + 1e-45)
+
