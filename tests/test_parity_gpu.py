@@ -651,3 +651,39 @@ def test_concurrent_host_threads(F):
         assert torch.equal(a.shard_out.view(torch.int16), b.shard_out.view(torch.int16))
         for f, g in zip(a.full, b.full):
             assert torch.equal(f.view(torch.int16), g.view(torch.int16))
+
+
+@pytest.mark.parametrize("ofmt", ["bf16", "f16"])
+def test_cast_exhaustive_through_the_kernel(F, orc, ofmt):
+    # with lr = 0, weight decay 0 and zero gradients the update leaves every
+    # fp32 master value as it is (p*1 - 0*(0/eps)), so the kernel's output is
+    # the cast of the master: all 2^32 fp32 bit patterns, in 2^30 chunks,
+    # against the oracle's cast (itself pinned on all patterns against torch)
+    n = 1 << 30
+    odt = fi.torch_dtype(ofmt)
+    exp_mask, man_mask = (0x7f80, 0x007f) if ofmt == "bf16" else (0x7c00, 0x03ff)
+    grads = [torch.zeros(n, dtype=torch.bfloat16, device=DEV)]
+    master = torch.empty(n, dtype=torch.float32, device=DEV)
+    m = torch.empty(n, device=DEV)
+    v = torch.empty(n, device=DEV)
+    out = torch.empty(n, dtype=odt, device=DEV)
+    ramp = np.arange(n, dtype=np.uint32)
+    hp = F.AdamWHParams(0.0, weight_decay=0.0)
+    for chunk in range(4):
+        bits = ramp + np.uint32(chunk * n)
+        master.copy_(torch.from_numpy(bits.view(np.float32)))
+        m.zero_()
+        v.zero_()
+        F.fsdp_reduce_scatter_adam_cast(grads, master, m, v, out, hp)
+        want = orc.cast(bits.view(np.float32), ofmt)
+        got = host(out)
+        nan_in = ((bits & 0x7f800000) == 0x7f800000) & ((bits & 0x007fffff) != 0)
+        nan_out = ((got & exp_mask) == exp_mask) & ((got & man_mask) != 0)
+        assert np.array_equal(nan_in, nan_out), chunk
+        got[nan_in] = 0
+        want[nan_in] = 0
+        if not np.array_equal(got, want):
+            i = int(np.flatnonzero(got != want)[0])
+            raise AssertionError(f"{ofmt}: pattern {hex(int(bits[i]))} -> {hex(int(got[i]))}, oracle {hex(int(want[i]))}")
+    del grads, master, m, v, out
+    torch.cuda.empty_cache()
