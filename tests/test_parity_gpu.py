@@ -687,3 +687,47 @@ def test_cast_exhaustive_through_the_kernel(F, orc, ofmt):
             raise AssertionError(f"{ofmt}: pattern {hex(int(bits[i]))} -> {hex(int(got[i]))}, oracle {hex(int(want[i]))}")
     del grads, master, m, v, out
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("gfmt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("lr", [1e-3, 1.0, 3e38])
+def test_extreme_values_match_the_oracle(F, orc, gfmt, lr):
+    # special master values x special gradients: zeros of both signs,
+    # subnormals, the extremes of each format, infinities and NaN, through the
+    # divide and square-root slow paths; bit-exact, NaN positions equal
+    rng = np.random.default_rng(77)
+    f32 = np.float32
+    specials_p = np.array([0.0, -0.0, 1e-45, -1e-45, 1e-40, 1.17549435e-38, -1.17549435e-38, 1e-20, 0.1, -0.1,
+                           1.0, 65504.0, 3.38953139e38, -3.38953139e38, np.inf, -np.inf, np.nan], f32)
+    specials_g = np.array([0.0, -0.0, 1e-45, 5.96e-8, 6.1e-5, 1e-3, -1e-3, 1.0, 3.0e4, 65504.0, -65504.0,
+                           3.38953139e38, np.inf, -np.inf, np.nan], f32)
+    world = 2
+    P = len(specials_p) * len(specials_g)
+    p0 = np.repeat(specials_p, len(specials_g)).astype(f32)
+    g_all = np.tile(specials_g, len(specials_p)).astype(f32)
+    rows = [g_all, (rng.standard_normal(P) * 1e-3).astype(f32)]  # rank 1 adds ordinary noise
+    P_pad = orc.padded_numel(P, world)
+    tdt = fi.torch_dtype(gfmt)
+    grads_t = [torch.from_numpy(orc.flatten_pad([r], world)).to(tdt) for r in rows]
+    grads = [g.to(DEV) for g in grads_t]
+    master = torch.from_numpy(orc.flatten_pad([p0], world)).to(DEV)
+    m = torch.zeros(P_pad, device=DEV)
+    v = torch.zeros(P_pad, device=DEV)
+    out = torch.empty(P_pad, dtype=torch.bfloat16, device=DEV)
+    p_o, m_o, v_o = host(master), np.zeros(P_pad, f32), np.zeros(P_pad, f32)
+    for t in (1, 2):
+        hp = F.AdamWHParams(lr, 0.9, 0.999, 1e-8, 0.01, t)
+        F.fsdp_reduce_scatter_adam_cast(grads, master, m, v, out, hp)
+        shards_o, _ = orc.fsdp_step([host(g) for g in grads_t], gfmt, world, p_o, m_o, v_o, "bf16",
+                                    orc.hparams(lr, 0.9, 0.999, 1e-8, 0.01, t))
+        torch.cuda.synchronize()
+        for name, got, want in (("master", host(master), p_o), ("exp_avg", host(m), m_o),
+                                ("exp_avg_sq", host(v), v_o)):
+            gn, wn = np.isnan(got), np.isnan(want)
+            assert np.array_equal(gn, wn), f"{name} NaN positions t={t}"
+            np.testing.assert_array_equal(got[~gn].view(np.uint32), want[~wn].view(np.uint32), f"{name} t={t}")
+        ob = host(out)
+        onan = ((ob & 0x7f80) == 0x7f80) & ((ob & 0x7f) != 0)
+        wnan = ((shards_o & 0x7f80) == 0x7f80) & ((shards_o & 0x7f) != 0)
+        assert np.array_equal(onan, wnan)
+        np.testing.assert_array_equal(ob[~onan], shards_o[~wnan])
