@@ -43,6 +43,7 @@ if ROOT not in sys.path:
 
 METRIC = "fused RS+AdamW+cast GB/s and params/s per FSDP unit vs HBM roofline, 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, the ~8 TB/s nominal figure
 WORKLOAD_NAMES = {
     "tiny": "tiny_unit_4099_n2",
     "gpt2_small": "gpt2_small_block_unit_n8",
@@ -75,6 +76,34 @@ def measured_peak():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_info() -> dict:
+    """Host name and CPU model of the machine the oracle is timed on."""
+    import platform
+    import socket
+    import subprocess
+
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"host": socket.gethostname(), "cpu_model": model or platform.machine(),
+            "host_cpus": os.cpu_count()}
 
 
 def kernel_source_hash() -> str:
@@ -446,6 +475,7 @@ def run_ours(args):
             "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
             "fused_ms": round(rsa_ms, 4),
+            "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
         },
         "e2e": {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 3), "steps": Ke,
@@ -466,7 +496,7 @@ def run_ours(args):
         result["cpu_baseline"] = {
             "value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{done} steps of a {n_s}-element unit with the workload's N, dtypes, distributions and "
-                      f"all-gathers ({el:.1f} s)"}
+                      f"all-gathers ({el:.1f} s)", **host_info()}
     print(json.dumps(result), flush=True)
     if world_size > 1:
         dist.barrier()
@@ -494,7 +524,7 @@ def run_reference(args):
         "config": {"workload": workload, "world": cfg.world, "grad_dtype": cfg.grad_dtype,
                    "out_dtype": cfg.out_dtype, "gathers_per_step": cfg.gathers, "sample_numel": n_s},
         "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, **host_info()},
         "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
