@@ -10,7 +10,8 @@ Default workload: the Llama-70B-style block unit (855,654,400 parameters, N=8,
 bf16 gradients ~N(0, 1e-4), AdamW lr 3e-5, wd 0.1, two all-gathers per step),
 the largest unit of the set, on which the fused kernel's HBM-bandwidth target
 is stated. Inputs are synthetic (seeded), resident in HBM, and far larger
-than L2.
+than L2; for the small units (--config gpt2_small, gpt2_large, tiny) L2 is
+flushed before every timed step, outside that step's CUDA events.
 
 Printed (rank 0, one JSON line): value = algorithmic bytes of the step / step
 time (GB/s, whole job over all ranks); roofline of the fused kernel (its own
@@ -189,6 +190,64 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class L2Flush:
+    """Between timed iterations of units whose working set is not far larger
+    than L2: write a buffer of twice L2, then read another of twice L2, so
+    that L2 holds neither the unit's data nor dirty lines of the flush."""
+
+    FAR_LARGER = 16  # units moving more than 16 x L2 per kernel need no flush
+
+    def __init__(self, device, work_bytes: int):
+        import torch
+
+        props = torch.cuda.get_device_properties(device)
+        self.l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
+        self.active = work_bytes <= self.FAR_LARGER * self.l2
+        if self.active:
+            n = 2 * self.l2 // 4
+            self.w = torch.empty(n, dtype=torch.int32, device=device)
+            self.r = torch.ones(n, dtype=torch.int32, device=device)
+            self.k = 0
+
+    def __call__(self):
+        if self.active:
+            self.k += 1
+            self.w.fill_(self.k)
+            self.r.sum()
+
+    def describe(self) -> str:
+        if self.active:
+            return (f"L2 flushed before every timed launch or step ({2 * self.l2 >> 20} MiB written, then "
+                    f"{2 * self.l2 >> 20} MiB read); each timed between its own CUDA events")
+        return "inputs larger than L2 (no flush needed)"
+
+
+def timed_calls(fn, K: int, stream, flush: L2Flush) -> float:
+    """Mean device time of fn() over K calls (ms): one pair of events around
+    all K calls, or, with the flush active, a pair around each call."""
+    import torch
+
+    torch.cuda.synchronize()
+    if not flush.active:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(K):
+            fn(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / K
+    evs = []
+    for i in range(K):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn(i)
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / K
+
+
 def max_over_ranks(values, device):
     """Element-wise MAX of per-rank timings over the process group (every rank
     gets the result)."""
@@ -309,7 +368,8 @@ def run_ours(args):
 
     # ---- timed region (device time, CUDA events on the launching stream)
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    flush = L2Flush(dev, rsa_b)
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world_size > 1:
         dist.barrier()
@@ -319,17 +379,22 @@ def run_ours(args):
         start.record(stream)
         for i in range(K):
             t += 1
+            flush()
             ev[i][0].record(stream)
             unit.reduce_scatter_adam_cast(hp(t))
             ev[i][1].record(stream)
             for _ in range(cfg.gathers):
                 unit.all_gather()
+            ev[i][2].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
     if world_size > 1:
         dist.barrier()
-    step_ms = start.elapsed_time(end) / K
-    rsa_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    if flush.active:  # the flushes between steps are not step time
+        step_ms = sum(a.elapsed_time(c) for a, _, c in ev) / K
+    else:
+        step_ms = start.elapsed_time(end) / K
+    rsa_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / K
     launches = K * (1 + cfg.gathers)  # kernels of ours in the timed regions (device step, then e2e)
 
     # ---- end to end through the binding's host-buffer step: every step copies
@@ -378,15 +443,10 @@ def run_ours(args):
             for _ in range(3):
                 t += 1
                 unit.step(hp(t), gathers=vg, fuse_gather=True)
-            v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            v0.record(stream)
-            for _ in range(K):
-                t += 1
-                unit.step(hp(t), gathers=vg, fuse_gather=True)
-            v1.record(stream)
-            torch.cuda.synchronize()
-            vms = v0.elapsed_time(v1) / K
+            t0 = t
+            vms = timed_calls(lambda i, vg=vg: unit.step(hp(t0 + 1 + i), gathers=vg, fuse_gather=True),
+                              K, stream, flush)
+            t += K
             launches += K * vg
             variants[vname] = {"gathers_per_step": vg, "ms_per_step": round(vms, 4)}
 
@@ -420,14 +480,7 @@ def run_ours(args):
                                                         tt, cfg.grad_scale, reduce_dtype=gdt if lowp else None))
             for i in range(3):
                 run(i + 1)
-            k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            k0.record(stream)
-            for i in range(K):
-                run(i + 4)
-            k1.record(stream)
-            torch.cuda.synchronize()
-            kms = k0.elapsed_time(k1) / K
+            kms = timed_calls(lambda i, run=run: run(i + 4), K, stream, flush)
             launches += K
             kernels[vname] = {"ms": round(kms, 4), "bytes_per_launch": nbytes,
                               "achieved_GBs": round(nbytes / (kms * 1e-3) / 1e9, 1)}
@@ -465,7 +518,7 @@ def run_ours(args):
             "workload": workload, "params": unit.numel, "padded_numel": P_pad, "world": N,
             "grad_dtype": cfg.grad_dtype, "out_dtype": cfg.out_dtype, "gathers_per_step": cfg.gathers,
             "bytes_per_step": rsa_b + ag_b, "fused_bytes_per_launch": rsa_b,
-            "l2": "inputs larger than L2 (no flush needed)" if rsa_b > 4 * 129e6 else "L2 flushed",
+            "l2": flush.describe(),
             "units_per_gpu": 1,
         },
         "params_per_s": round(P_pad * world_size / (step_ms * 1e-3), 1),
