@@ -486,6 +486,36 @@ def run_ours(args):
                               "achieved_GBs": round(nbytes / (kms * 1e-3) / 1e9, 1)}
         del low
 
+    # ---- offload mode: master, m and v in pinned host memory, updated in
+    # place by the same fused kernel over the host link (12 B read and 12 B
+    # written per element there; gradients and the shard stay in HBM)
+    offload = None
+    if not args.no_variants and not args.no_offload:
+        try:
+            hstate = [torch.zeros(P_pad, dtype=torch.float32, pin_memory=True) for _ in range(3)]
+        except RuntimeError as e:  # not enough page-locked host memory
+            offload = {"unavailable": str(e).splitlines()[0][:200]}
+        else:
+            hstate[0].copy_(unit.master)
+            torch.cuda.synchronize()
+
+            def run_off(i):
+                F.fsdp_reduce_scatter_adam_cast(unit.grads, *hstate, unit.shard_out, hp(i + 1))
+
+            for i in range(3):
+                run_off(i)
+            Ko = max(3, min(K, 5))
+            oms = timed_calls(lambda i: run_off(i + 3), Ko, stream, flush)
+            launches += Ko
+            link_b = P_pad * 3 * (4 + 4)
+            hbm_b = P_pad * (N * unit.grads[0].element_size() + unit.shard_out.element_size())
+            offload = {"ms": round(oms, 3), "launches": Ko, "host_link_bytes_per_launch": link_b,
+                       "hbm_bytes_per_launch": hbm_b,
+                       "host_link_GBs": round(link_b / (oms * 1e-3) / 1e9, 1),
+                       "host_link_GBs_per_direction": round(link_b / 2 / (oms * 1e-3) / 1e9, 1),
+                       "slowdown_vs_device_state": round(oms / rsa_ms, 2)}
+            del hstate
+
     if world_size > 1:
         step_ms, rsa_ms, e2e_ms = max_over_ranks([step_ms, rsa_ms, e2e_ms], dev)
         for v in variants.values():
@@ -541,6 +571,7 @@ def run_ours(args):
                      for k, v in variants.items()},
         "variant_kernels": {k: dict(v, frac=round(v["achieved_GBs"] / measured_peak()[0], 4))
                             for k, v in kernels.items()},
+        "offload_state_on_host": offload,
         "clocks": clocks.summary(),
     }
     if world_size == 1 and not args.no_cpu_baseline:
@@ -596,6 +627,8 @@ def main(argv=None):
     ap.add_argument("--e2e-read-params", action="store_true",
                     help="e2e reads the compute-dtype parameters back each step instead of the step's metric")
     ap.add_argument("--no-variants", action="store_true", help="skip the fused-gather variant timings")
+    ap.add_argument("--no-offload", action="store_true",
+                    help="skip the offload-mode timing (state in pinned host memory)")
     ap.add_argument("--cpu-sample", type=int, default=1 << 24, help="elements in the CPU-baseline sample")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline time budget")
     ap.add_argument("--ref-sample", type=int, default=1 << 22, help="elements per reference-arm step")

@@ -31,6 +31,14 @@
  *    device addresses. The caller owns every buffer; the library allocates
  *    no device memory and keeps no state besides a per-device cache of the
  *    SM count.
+ *  - Offload. Where an argument says "device or mapped host", the buffer
+ *    may also be page-locked host memory mapped into the device's address
+ *    space (cudaHostAlloc, or cudaHostRegister with mapping; the same
+ *    address under unified addressing). The kernel then reads and writes it
+ *    over the host link: the optimizer state and fp32 master kept in CPU
+ *    memory ("FSDP (Fully Sharded Data Parallel)", "CPU Offloading";
+ *    "fairseq ... FSDP 实战指南", --cpu-offload), updated by the same kernel.
+ *    The other buffers must be device memory.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream). Device work is enqueued on it and the call returns without
  *    synchronizing.
@@ -159,10 +167,12 @@ fsdp_status fsdp_flatten_pad(const void *const *srcs, const int64_t *numels, int
  * of "Mixed Precision and FSDP". The AdamW formula, the reduction order and
  * the single multiply by c are this library's reading (the pages print none).
  *
- *   grads        host array of `world` device pointers, each padded_numel
- *                elements of grad_dtype (F32, BF16 or F16); read only.
+ *   grads        host array of `world` pointers (device or mapped host),
+ *                each padded_numel elements of grad_dtype (F32, BF16 or
+ *                F16); read only.
  *   padded_numel P_pad, a multiple of world (0 is a no-op).
- *   master, exp_avg, exp_avg_sq   device fp32, padded_numel each, in place.
+ *   master, exp_avg, exp_avg_sq   fp32 (device or mapped host),
+ *                padded_numel each, in place.
  *   shard_out    device, padded_numel elements of out_dtype (F32, BF16,
  *                F16); must not overlap the gradients or the state.
  *   hp           host; step >= 1, grad_scale > 0.
@@ -227,9 +237,11 @@ fsdp_status fsdp_reduce_scatter_adam_cast_gather(const void *const *grads, fsdp_
  *     value is widened, updated in fp32 and rounded to nearest even when
  *     stored; param is itself the rank's compute-dtype shard, so shard_out
  *     must be NULL and out_dtype equal to state_dtype.
- *   grads        host array of `world` device pointers, padded_numel each.
- *   param, state0, state1   device, padded_numel elements each, in place;
- *                state1 must be NULL for SGD and non-NULL otherwise.
+ *   grads        host array of `world` pointers (device or mapped host),
+ *                padded_numel each.
+ *   param, state0, state1   device or mapped host, padded_numel elements
+ *                each, in place; state1 must be NULL for SGD and non-NULL
+ *                otherwise.
  *   cfg          host; step >= 1, grad_scale > 0, optimizer and
  *                reduce_dtype as above.
  * Other arguments, in-place rules and errors as

@@ -106,8 +106,20 @@ def _dev(t: torch.Tensor, name: str) -> int:
     return t.data_ptr()
 
 
-def _ptrs(ts: Sequence[torch.Tensor], name: str):
-    return (ctypes.c_void_p * len(ts))(*[_dev(t, f"{name}[{i}]") for i, t in enumerate(ts)])
+def _mem(t: torch.Tensor, name: str) -> int:
+    """A buffer the update kernels stream through: CUDA memory, or page-locked
+    host memory (mapped into the device's address space; the kernel then
+    reads and writes it over the host link, the offload mode)."""
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or (t.device.type == "cpu" and t.is_pinned())):
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _ptrs(ts: Sequence[torch.Tensor], name: str, host_ok: bool = False):
+    get = _mem if host_ok else _dev
+    return (ctypes.c_void_p * len(ts))(*[get(t, f"{name}[{i}]") for i, t in enumerate(ts)])
 
 
 def _views(c_views, n) -> List[View]:
@@ -179,7 +191,9 @@ def fsdp_reduce_scatter_adam_cast(grads: Sequence[torch.Tensor], master: torch.T
 
     grads: N tensors (or the rows of an [N, P_pad] tensor) of one dtype.
     master / exp_avg / exp_avg_sq: fp32 [P_pad], updated in place.
-    shard_out: [P_pad] of the compute dtype; rank r writes [r*S, (r+1)*S).
+    grads, master, exp_avg and exp_avg_sq may be pinned host tensors (the
+    offload mode: the kernel streams them over the host link).
+    shard_out: [P_pad] of the compute dtype, CUDA; rank r writes [r*S, (r+1)*S).
     nonfinite_count: optional CUDA uint32/int32 scalar, incremented by the
     number of non-finite averaged gradient elements.
     """
@@ -202,11 +216,11 @@ def fsdp_reduce_scatter_adam_cast(grads: Sequence[torch.Tensor], master: torch.T
     hp = hparams.to_c()
     rb = int(rank_begin)
     re = world if rank_end is None else int(rank_end)
-    _check(_lib.load().fsdp_reduce_scatter_adam_cast(
-        _ptrs(grads, "grads") if world else None, dtype_code(gdt), world, P_pad,
-        _dev(master, "master"), _dev(exp_avg, "exp_avg"), _dev(exp_avg_sq, "exp_avg_sq"),
-        _dev(shard_out, "shard_out"), dtype_code(shard_out.dtype), ctypes.byref(hp), rb, re,
-        nf or None, _stream(stream)), "fsdp_reduce_scatter_adam_cast")
+    args = (_ptrs(grads, "grads", host_ok=True) if world else None, dtype_code(gdt), world, P_pad,
+            _mem(master, "master"), _mem(exp_avg, "exp_avg"), _mem(exp_avg_sq, "exp_avg_sq"),
+            _dev(shard_out, "shard_out"), dtype_code(shard_out.dtype), ctypes.byref(hp), rb, re,
+            nf or None, _stream(stream))
+    _check(_lib.load().fsdp_reduce_scatter_adam_cast(*args), "fsdp_reduce_scatter_adam_cast")
 
 
 def fsdp_reduce_scatter_adam_cast_gather(grads: Sequence[torch.Tensor], master: torch.Tensor,
@@ -239,12 +253,12 @@ def fsdp_reduce_scatter_adam_cast_gather(grads: Sequence[torch.Tensor], master: 
     nf = _dev(nonfinite_count, "nonfinite_count") if nonfinite_count is not None else None
     hp = hparams.to_c()
     re = world if rank_end is None else int(rank_end)
-    _check(_lib.load().fsdp_reduce_scatter_adam_cast_gather(
-        _ptrs(grads, "grads") if world else None, dtype_code(gdt), world, P_pad,
-        _dev(master, "master"), _dev(exp_avg, "exp_avg"), _dev(exp_avg_sq, "exp_avg_sq"),
-        _dev(shard_out, "shard_out") if shard_out is not None else None, dtype_code(odt),
-        _ptrs(full_bufs, "full_bufs"), len(full_bufs), ctypes.byref(hp), int(rank_begin), re, nf,
-        _stream(stream)), "fsdp_reduce_scatter_adam_cast_gather")
+    args = (_ptrs(grads, "grads", host_ok=True) if world else None, dtype_code(gdt), world, P_pad,
+            _mem(master, "master"), _mem(exp_avg, "exp_avg"), _mem(exp_avg_sq, "exp_avg_sq"),
+            _dev(shard_out, "shard_out") if shard_out is not None else None, dtype_code(odt),
+            _ptrs(full_bufs, "full_bufs"), len(full_bufs), ctypes.byref(hp), int(rank_begin), re, nf,
+            _stream(stream))
+    _check(_lib.load().fsdp_reduce_scatter_adam_cast_gather(*args), "fsdp_reduce_scatter_adam_cast_gather")
 
 
 def fsdp_reduce_scatter_step(grads: Sequence[torch.Tensor], param: torch.Tensor, state0: torch.Tensor,
@@ -256,7 +270,8 @@ def fsdp_reduce_scatter_step(grads: Sequence[torch.Tensor], param: torch.Tensor,
 
     param/state0/state1: [P_pad], fp32 (then shard_out receives the cast) or
     all bf16/fp16 (then param is the shard and shard_out must be None).
-    state1 is None for SGD."""
+    state1 is None for SGD. grads, param and the states may be pinned host
+    tensors (offload mode)."""
     world = len(grads)
     P_pad = param.numel()
     gdt = grads[0].dtype if world else torch.bfloat16
@@ -273,11 +288,11 @@ def fsdp_reduce_scatter_step(grads: Sequence[torch.Tensor], param: torch.Tensor,
     nf = _dev(nonfinite_count, "nonfinite_count") if nonfinite_count is not None else None
     cfg = config.to_c(gdt)
     re = world if rank_end is None else int(rank_end)
-    _check(_lib.load().fsdp_reduce_scatter_step(
-        _ptrs(grads, "grads") if world else None, dtype_code(gdt), world, P_pad, _dev(param, "param"),
-        _dev(state0, "state0"), _dev(state1, "state1") if state1 is not None else None, dtype_code(sdt),
-        _dev(shard_out, "shard_out") if shard_out is not None else None, dtype_code(odt), ctypes.byref(cfg),
-        int(rank_begin), re, nf, _stream(stream)), "fsdp_reduce_scatter_step")
+    args = (_ptrs(grads, "grads", host_ok=True) if world else None, dtype_code(gdt), world, P_pad,
+            _mem(param, "param"), _mem(state0, "state0"), _mem(state1, "state1") if state1 is not None else None,
+            dtype_code(sdt), _dev(shard_out, "shard_out") if shard_out is not None else None, dtype_code(odt),
+            ctypes.byref(cfg), int(rank_begin), re, nf, _stream(stream))
+    _check(_lib.load().fsdp_reduce_scatter_step(*args), "fsdp_reduce_scatter_step")
 
 
 def fsdp_all_gather(shard_out: torch.Tensor, full_bufs: Sequence[torch.Tensor], world: int,

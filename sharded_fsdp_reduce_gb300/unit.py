@@ -8,6 +8,13 @@ the compute dtype). Shared by all ranks, as the concatenation of their shards:
 the fp32 master weights, exp_avg (m), exp_avg_sq (v) and the compute-dtype
 shards (shard_out); rank r's shard is [r*S, (r+1)*S).
 
+Offload mode (state_on_host=True): master, exp_avg and exp_avg_sq live in
+pinned host memory instead of HBM ("FSDP (Fully Sharded Data Parallel)", "CPU
+Offloading"; "fairseq ... FSDP 实战指南", --cpu-offload keeps the optimizer
+state and the FP32 copy of the model on the CPU). The same update kernel
+reads and writes them in place over the host link; the gradients, the
+compute-dtype shards and the gathered buffers stay in HBM.
+
 The step of one unit ("FSDP (Fully Sharded Data Parallel)", "The Per-Layer
 Communication"; "Fully Sharded Data Parallel: faster AI training with fewer
 GPUs", "From all-reduce to sharded parameters"): the gradients are
@@ -28,7 +35,8 @@ from .fsdp import (AdamWHParams, View, fsdp_all_gather, fsdp_flatten_pad, fsdp_r
 
 class FlatParamUnit:
     def __init__(self, params: Sequence[Tuple[str, Tuple[int, ...]]], world: int, grad_dtype: torch.dtype,
-                 out_dtype: torch.dtype, device="cuda", n_full: Optional[int] = None):
+                 out_dtype: torch.dtype, device="cuda", n_full: Optional[int] = None,
+                 state_on_host: bool = False):
         self.names = [n for n, _ in params]
         self.shapes = [tuple(s) for _, s in params]
         self.world = int(world)
@@ -38,9 +46,12 @@ class FlatParamUnit:
         self.device = torch.device(device)
         P = self.padded_numel
         self.grads = [torch.zeros(P, dtype=grad_dtype, device=self.device) for _ in range(self.world)]
-        self.master = torch.zeros(P, dtype=torch.float32, device=self.device)
-        self.exp_avg = torch.zeros(P, dtype=torch.float32, device=self.device)
-        self.exp_avg_sq = torch.zeros(P, dtype=torch.float32, device=self.device)
+        self.state_on_host = bool(state_on_host)
+        if self.state_on_host:
+            state = [torch.zeros(P, dtype=torch.float32, pin_memory=True) for _ in range(3)]
+        else:
+            state = [torch.zeros(P, dtype=torch.float32, device=self.device) for _ in range(3)]
+        self.master, self.exp_avg, self.exp_avg_sq = state
         self.shard_out = torch.zeros(P, dtype=out_dtype, device=self.device)
         nf = self.world if n_full is None else int(n_full)
         self.full = [torch.zeros(P, dtype=out_dtype, device=self.device) for _ in range(nf)]
@@ -50,7 +61,14 @@ class FlatParamUnit:
 
     def load_master(self, tensors: Sequence[torch.Tensor], stream=None) -> None:
         """Flatten the unit's initial fp32 parameters into the master buffer."""
-        fsdp_flatten_pad(list(tensors), self.world, out=self.master, stream=stream)
+        if not self.state_on_host:
+            fsdp_flatten_pad(list(tensors), self.world, out=self.master, stream=stream)
+            return
+        flat, _ = fsdp_flatten_pad(list(tensors), self.world, stream=stream)
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        with torch.cuda.stream(s):
+            self.master.copy_(flat, non_blocking=True)
+            flat.record_stream(s)
 
     def load_grad(self, rank: int, tensors: Sequence[torch.Tensor], stream=None) -> None:
         """Flatten rank ``rank``'s per-parameter gradients into its flat buffer (pad zeroed)."""

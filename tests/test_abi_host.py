@@ -245,3 +245,23 @@ def test_exports_nothing_but_the_c_abi(lib):
     out = subprocess.run([nm, "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True, check=True)
     exported = sorted(line.split()[-1] for line in out.stdout.splitlines() if " T " in line)
     assert exported == declared_functions()
+
+
+def test_binding_refuses_unpinned_host_tensors(lib):
+    # the kernels stream device memory or pinned (mapped) host memory only;
+    # the binding refuses an ordinary host tensor before calling the library
+    import torch
+    import sharded_fsdp_reduce_gb300 as F
+    P = 8
+    g = [torch.ones(P, dtype=torch.bfloat16)] * 2
+    st = [torch.zeros(P) for _ in range(3)]
+    out = torch.zeros(P, dtype=torch.bfloat16)
+    hp = F.AdamWHParams(1e-3, step=1)
+    with pytest.raises(ValueError, match="grads"):
+        F.fsdp_reduce_scatter_adam_cast(g, *st, out, hp)
+    with pytest.raises(ValueError):
+        F.fsdp_reduce_scatter_adam_cast_gather(g, *st, None, [out], hp)
+    with pytest.raises(ValueError, match="grads"):
+        F.fsdp_reduce_scatter_step(g, st[0], st[1], st[2], out, F.StepConfig("adamw", 1e-3))
+    with pytest.raises(ValueError, match="shard_out"):
+        F.fsdp_all_gather(out, [out.clone()], 2)
