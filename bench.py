@@ -248,6 +248,60 @@ def timed_calls(fn, K: int, stream, flush: L2Flush) -> float:
     return sum(a.elapsed_time(b) for a, b in evs) / K
 
 
+def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20):
+    """Host enqueue time and device time per model step of n_units GPT-2 small
+    block units (one gather each), stepped by a Python loop over the units and
+    by one native fsdp_step_units call. Returns (result, timed launches)."""
+    import torch
+
+    cfg = fi.CONFIGS["gpt2_small"]
+    gdt, odt = fi.torch_dtype(cfg.grad_dtype), fi.torch_dtype(cfg.out_dtype)
+    units = []
+    for k in range(n_units):
+        u = F.FlatParamUnit(cfg.params, cfg.world, gdt, odt, device=dev)
+        u.load_master([fi.gen_master(cfg, device=dev, seed_base=7000 + k)])
+        for r in range(cfg.world):
+            u.load_grad(r, [fi.gen_grad(cfg, r, 1, device=dev, seed_base=7000 + k)])
+        units.append(u)
+    seq = F.UnitSequence(units)
+    t = [0]
+
+    def hp():
+        t[0] += 1
+        return F.AdamWHParams(cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay, t[0], cfg.grad_scale)
+
+    def python_loop():
+        h = hp()
+        for u in units:
+            u.step(h, gathers=cfg.gathers)
+
+    def native():
+        seq.step(hp(), gathers=cfg.gathers)
+
+    out = {}
+    for name, fn in (("python_loop", python_loop), ("native", native)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            fn()
+        t1 = time.perf_counter()
+        b.record(stream)
+        torch.cuda.synchronize()
+        out[name] = {"host_enqueue_ms_per_step": round((t1 - t0) * 1e3 / steps, 4),
+                     "device_ms_per_step": round(a.elapsed_time(b) / steps, 4)}
+    rsa_b, ag_b = seq.step_bytes(cfg.gathers)
+    out["bytes_per_step"] = rsa_b + ag_b
+    out["native_GBs"] = round((rsa_b + ag_b) / (out["native"]["device_ms_per_step"] * 1e-3) / 1e9, 1)
+    out["launches_per_step"] = n_units * (1 + cfg.gathers)
+    del seq, units
+    torch.cuda.empty_cache()
+    return out, 2 * steps * n_units * (1 + cfg.gathers)
+
+
 def max_over_ranks(values, device):
     """Element-wise MAX of per-rank timings over the process group (every rank
     gets the result)."""
@@ -516,6 +570,14 @@ def run_ours(args):
                        "slowdown_vs_device_state": round(oms / rsa_ms, 2)}
             del hstate
 
+    # ---- the per-unit driver on a whole small model (12 GPT-2 small block
+    # units, the blocks of a GPT-2 small model): a Python loop over
+    # FlatParamUnit.step against one native fsdp_step_units call per step
+    driver = None
+    if not args.no_variants and not args.no_driver:
+        driver, n_launch = measure_driver(F, fi, dev, stream)
+        launches += n_launch
+
     if world_size > 1:
         step_ms, rsa_ms, e2e_ms = max_over_ranks([step_ms, rsa_ms, e2e_ms], dev)
         for v in variants.values():
@@ -572,6 +634,7 @@ def run_ours(args):
         "variant_kernels": {k: dict(v, frac=round(v["achieved_GBs"] / measured_peak()[0], 4))
                             for k, v in kernels.items()},
         "offload_state_on_host": offload,
+        "driver_gpt2_small_model_12_units": driver,
         "clocks": clocks.summary(),
     }
     if world_size == 1 and not args.no_cpu_baseline:
@@ -627,6 +690,8 @@ def main(argv=None):
     ap.add_argument("--e2e-read-params", action="store_true",
                     help="e2e reads the compute-dtype parameters back each step instead of the step's metric")
     ap.add_argument("--no-variants", action="store_true", help="skip the fused-gather variant timings")
+    ap.add_argument("--no-driver", action="store_true",
+                    help="skip the per-unit driver timing on a 12-unit GPT-2 small model")
     ap.add_argument("--no-offload", action="store_true",
                     help="skip the offload-mode timing (state in pinned host memory)")
     ap.add_argument("--cpu-sample", type=int, default=1 << 24, help="elements in the CPU-baseline sample")

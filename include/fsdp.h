@@ -118,6 +118,22 @@ typedef struct {
     float grad_scale;      /* static loss scale the gradients carry; 1 if none */
 } fsdp_step_config;
 
+/* The buffers of one FSDP unit (one FlatParameter) for fsdp_step_units,
+ * laid out as the single-unit entry points take them. Caller-owned. */
+typedef struct {
+    const void *const *grads;    /* host array of `world` pointers (device or mapped host), padded_numel each */
+    void *const *full_bufs;      /* host array of n_full device pointers, padded_numel each (NULL if n_full == 0) */
+    float *master;               /* fp32, device or mapped host, padded_numel */
+    float *exp_avg;              /* fp32, device or mapped host, padded_numel */
+    float *exp_avg_sq;           /* fp32, device or mapped host, padded_numel */
+    void *shard_out;             /* device, padded_numel elements of out_dtype */
+    int64_t padded_numel;        /* a multiple of world (0: the unit is skipped) */
+    int32_t world;               /* N, 1..FSDP_MAX_WORLD */
+    int32_t grad_dtype;          /* fsdp_dtype */
+    int32_t out_dtype;           /* fsdp_dtype */
+    int32_t n_full;              /* 0..FSDP_MAX_WORLD */
+} fsdp_unit;
+
 /* ceil(numel / world) * world: the FlatParameter length after zero padding
  * at the end, so that it splits into `world` equal shards. Returns -1 when
  * numel < 0 or world < 1. Host only. */
@@ -265,6 +281,29 @@ fsdp_status fsdp_reduce_scatter_step(const void *const *grads, fsdp_dtype grad_d
  *   world        N; padded_numel must be a multiple of it. */
 fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
                             int64_t padded_numel, void *const *full_bufs, int n_dst, void *stream);
+
+/* The step of a whole model (device): its FSDP units in order, each one's
+ * fused reduce-scatter + AdamW + cast over all its ranks followed by
+ * `gathers` all-gathers of its shard_out into its n_full buffers, all on one
+ * stream -- the per-unit driver of "FSDP (Fully Sharded Data Parallel)",
+ * "The Per-Layer Communication" (one unit per wrapped layer, each
+ * reduce-scattered and gathered on its own) in one call. With
+ * fuse_first_gather != 0 the first gather of each unit is written by its
+ * update kernel (as fsdp_reduce_scatter_adam_cast_gather) and gathers - 1
+ * separate gathers follow.
+ *   units        host array of n_units descriptors (n_units >= 0).
+ *   hp           host; the same hyperparameters for every unit (one
+ *                optimizer over the model); step >= 1, grad_scale > 0.
+ *   gathers      0..FSDP_MAX_WORLD; units with gathers > 0 need n_full >= 1.
+ *   nonfinite_count  device uint32 or NULL, summed over all units.
+ * Every unit is validated as the single-unit entry points validate it, and
+ * no buffer written by one unit may overlap a buffer written by another,
+ * before anything is enqueued: an invalid unit makes the call return its
+ * status and enqueue nothing. FSDP_ERR_CUDA reports a launch that failed
+ * after the units before it were enqueued. */
+fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
+                            int gathers, int fuse_first_gather, uint32_t *nonfinite_count,
+                            void *stream);
 
 /* Human-readable name of a status. Never NULL. */
 const char *fsdp_status_string(fsdp_status status);

@@ -5,8 +5,8 @@ C ABI (include/fsdp.h). This package is the thin Python binding over it.
 from .fsdp import (OPTIMIZERS, AdamWHParams, FsdpError, StepConfig, View, fsdp_reduce_scatter_step, dtype_code, fsdp_all_gather, fsdp_flatten_pad,
                    fsdp_last_cuda_error, fsdp_padded_numel, fsdp_take_wait_timeouts, fsdp_reduce_scatter_adam_cast,
                    fsdp_reduce_scatter_adam_cast_gather, fsdp_status_string,
-                   fsdp_unflatten_views)
-from .unit import FlatParamUnit
+                   fsdp_unflatten_views, UnitDescs, fsdp_step_units)
+from .unit import FlatParamUnit, UnitSequence
 
 __all__ = [
     "AdamWHParams", "StepConfig", "OPTIMIZERS", "FsdpError", "View", "FlatParamUnit", "dtype_code",
@@ -14,4 +14,5 @@ __all__ = [
     "fsdp_padded_numel", "fsdp_unflatten_views", "fsdp_flatten_pad", "fsdp_reduce_scatter_adam_cast",
     "fsdp_reduce_scatter_adam_cast_gather",
     "fsdp_all_gather", "fsdp_status_string", "fsdp_last_cuda_error", "fsdp_take_wait_timeouts",
+    "UnitDescs", "fsdp_step_units", "UnitSequence",
 ]

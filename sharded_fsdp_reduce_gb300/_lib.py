@@ -36,6 +36,7 @@ EXPORTS = (
     "fsdp_status_string",
     "fsdp_last_cuda_error",
     "fsdp_take_wait_timeouts",
+    "fsdp_step_units",
 )
 
 
@@ -55,6 +56,13 @@ class FsdpStepConfig(ctypes.Structure):
     _fields_ = [("optimizer", ctypes.c_int32), ("reduce_dtype", ctypes.c_int32), ("lr", ctypes.c_float),
                 ("beta1", ctypes.c_float), ("beta2", ctypes.c_float), ("eps", ctypes.c_float),
                 ("weight_decay", ctypes.c_float), ("step", ctypes.c_int64), ("grad_scale", ctypes.c_float)]
+
+
+class FsdpUnit(ctypes.Structure):
+    _fields_ = [("grads", ctypes.c_void_p), ("full_bufs", ctypes.c_void_p), ("master", ctypes.c_void_p),
+                ("exp_avg", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p), ("shard_out", ctypes.c_void_p),
+                ("padded_numel", ctypes.c_int64), ("world", ctypes.c_int32), ("grad_dtype", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32), ("n_full", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -87,6 +95,8 @@ def load() -> ctypes.CDLL:
             "fsdp_status_string": (ctypes.c_char_p, [i32]),
             "fsdp_last_cuda_error": (i32, []),
             "fsdp_take_wait_timeouts": (i32, [ctypes.POINTER(ctypes.c_uint32)]),
+            "fsdp_step_units": (i32, [ctypes.POINTER(FsdpUnit), i32, ctypes.POINTER(FsdpAdamwHparams), i32, i32,
+                                      vp, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)

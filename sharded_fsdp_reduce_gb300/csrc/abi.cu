@@ -4,7 +4,9 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
+#include <vector>
 
 #include "host.cuh"
 
@@ -189,12 +191,15 @@ FSDP_API fsdp_status fsdp_flatten_pad(const void *const *srcs, const int64_t *nu
 
 namespace {
 
-// Validation and launch shared by the fused update with and without the fused
-// all-gather (full_bufs / n_dst; shard_out may then be NULL).
-fsdp_status rsa_entry(const void *const *grads, fsdp_dtype grad_dtype, int world, int64_t padded_numel,
-                      float *master, float *exp_avg, float *exp_avg_sq, void *shard_out, fsdp_dtype out_dtype,
-                      void *const *full_bufs, int n_dst, const fsdp_adamw_hparams *hp, int rank_begin,
-                      int rank_end, uint32_t *nonfinite_count, void *stream) {
+// Validation shared by the fused update with and without the fused all-gather
+// (full_bufs / n_dst; shard_out may then be NULL) and by the multi-unit step:
+// fills the kernel's arguments, or sets `empty` when the rank range holds no
+// element. Nothing is enqueued.
+fsdp_status prepare_rsa(const void *const *grads, fsdp_dtype grad_dtype, int world, int64_t padded_numel,
+                        float *master, float *exp_avg, float *exp_avg_sq, void *shard_out, fsdp_dtype out_dtype,
+                        void *const *full_bufs, int n_dst, const fsdp_adamw_hparams *hp, int rank_begin,
+                        int rank_end, uint32_t *nonfinite_count, RsaArgs &a, bool &empty) {
+    empty = false;
     if (!dtype_valid(grad_dtype) || !dtype_valid(out_dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
     if (world < 1 || world > FSDP_MAX_WORLD || !grads || !hp) return FSDP_ERR_INVALID_ARG;
     if (padded_numel < 0 || padded_numel % world != 0) return FSDP_ERR_INVALID_ARG;
@@ -204,7 +209,10 @@ fsdp_status rsa_entry(const void *const *grads, fsdp_dtype grad_dtype, int world
     if (mul_overflows(padded_numel, 4)) return FSDP_ERR_INVALID_ARG;
     const int64_t S = padded_numel / world;
     const int64_t begin = static_cast<int64_t>(rank_begin) * S, end = static_cast<int64_t>(rank_end) * S;
-    if (begin == end) return FSDP_OK;
+    if (begin == end) {
+        empty = true;
+        return FSDP_OK;
+    }
     if (!master || !exp_avg || !exp_avg_sq || (!shard_out && n_dst == 0)) return FSDP_ERR_INVALID_ARG;
     const size_t gs = static_cast<size_t>(dtype_size(grad_dtype)), os = static_cast<size_t>(dtype_size(out_dtype));
     const size_t state_bytes = static_cast<size_t>(padded_numel) * 4;
@@ -228,7 +236,6 @@ fsdp_status rsa_entry(const void *const *grads, fsdp_dtype grad_dtype, int world
     for (int i = 0; i < nw; ++i)
         for (int k = i + 1; k < nw; ++k)
             if (overlaps(written[i], wbytes[i], written[k], wbytes[k])) return FSDP_ERR_INVALID_ARG;
-    RsaArgs a;
     memset(&a, 0, sizeof(a));
     for (int q = 0; q < world; ++q) {
         if (!grads[q]) return FSDP_ERR_INVALID_ARG;
@@ -248,13 +255,74 @@ fsdp_status rsa_entry(const void *const *grads, fsdp_dtype grad_dtype, int world
     a.world = world;
     a.n_full = n_dst;
     for (int d = 0; d < n_dst; ++d) a.full[d] = full_bufs[d];
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return FSDP_OK;
+}
+
+fsdp_status launch_rsa(const RsaArgs &a, fsdp_dtype grad_dtype, fsdp_dtype out_dtype, cudaStream_t s) {
     switch (grad_dtype) {
         case FSDP_BF16: return launch_rsa_bf16(a, out_dtype, s);
         case FSDP_F16: return launch_rsa_f16(a, out_dtype, s);
         default: return launch_rsa_f32(a, out_dtype, s);
     }
 }
+
+fsdp_status rsa_entry(const void *const *grads, fsdp_dtype grad_dtype, int world, int64_t padded_numel,
+                      float *master, float *exp_avg, float *exp_avg_sq, void *shard_out, fsdp_dtype out_dtype,
+                      void *const *full_bufs, int n_dst, const fsdp_adamw_hparams *hp, int rank_begin,
+                      int rank_end, uint32_t *nonfinite_count, void *stream) {
+    RsaArgs a;
+    bool empty = false;
+    const fsdp_status st = prepare_rsa(grads, grad_dtype, world, padded_numel, master, exp_avg, exp_avg_sq,
+                                       shard_out, out_dtype, full_bufs, n_dst, hp, rank_begin, rank_end,
+                                       nonfinite_count, a, empty);
+    if (st != FSDP_OK || empty) return st;
+    return launch_rsa(a, grad_dtype, out_dtype, static_cast<cudaStream_t>(stream));
+}
+
+// Validation of an all-gather: fills its arguments or sets `empty`.
+fsdp_status prepare_gather(const void *shard_out, fsdp_dtype dtype, int world, int64_t padded_numel,
+                           void *const *full_bufs, int n_dst, GatherArgs &a, bool &empty) {
+    empty = false;
+    if (!dtype_valid(dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
+    if (world < 1 || padded_numel < 0 || padded_numel % world != 0) return FSDP_ERR_INVALID_ARG;
+    if (n_dst < 1 || n_dst > FSDP_MAX_WORLD || !full_bufs) return FSDP_ERR_INVALID_ARG;
+    const size_t es = static_cast<size_t>(dtype_size(dtype));
+    if (mul_overflows(padded_numel, static_cast<int64_t>(es))) return FSDP_ERR_INVALID_ARG;
+    if (padded_numel == 0) {
+        empty = true;
+        return FSDP_OK;
+    }
+    const size_t nbytes = static_cast<size_t>(padded_numel) * es;
+    if (!shard_out) return FSDP_ERR_INVALID_ARG;
+    if (!aligned(shard_out, es)) return FSDP_ERR_ALIGNMENT;
+    memset(&a, 0, sizeof(a));
+    a.src = shard_out;
+    a.nbytes = static_cast<int64_t>(nbytes);
+    a.n_dst = n_dst;
+    for (int d = 0; d < n_dst; ++d) {
+        if (!full_bufs[d]) return FSDP_ERR_INVALID_ARG;
+        if (!aligned(full_bufs[d], es)) return FSDP_ERR_ALIGNMENT;
+        if (overlaps(full_bufs[d], nbytes, shard_out, nbytes)) return FSDP_ERR_INVALID_ARG;
+        for (int e = 0; e < d; ++e)
+            if (overlaps(full_bufs[d], nbytes, full_bufs[e], nbytes)) return FSDP_ERR_INVALID_ARG;
+        a.dst[d] = full_bufs[d];
+    }
+    return FSDP_OK;
+}
+
+// One unit of fsdp_step_units, validated and ready to launch.
+struct UnitPlan {
+    RsaArgs rsa;
+    GatherArgs gather;
+    fsdp_dtype grad_dtype, out_dtype;
+    bool empty;
+    int separate_gathers;
+};
+
+struct Span {
+    uintptr_t lo, hi;
+    bool operator<(const Span &o) const { return lo < o.lo; }
+};
 
 }  // namespace
 
@@ -344,29 +412,68 @@ FSDP_API fsdp_status fsdp_reduce_scatter_step(const void *const *grads, fsdp_dty
 
 FSDP_API fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world, int64_t padded_numel,
                             void *const *full_bufs, int n_dst, void *stream) {
-    if (!dtype_valid(dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
-    if (world < 1 || padded_numel < 0 || padded_numel % world != 0) return FSDP_ERR_INVALID_ARG;
-    if (n_dst < 1 || n_dst > FSDP_MAX_WORLD || !full_bufs) return FSDP_ERR_INVALID_ARG;
-    const size_t es = static_cast<size_t>(dtype_size(dtype));
-    if (mul_overflows(padded_numel, static_cast<int64_t>(es))) return FSDP_ERR_INVALID_ARG;
-    if (padded_numel == 0) return FSDP_OK;
-    const size_t nbytes = static_cast<size_t>(padded_numel) * es;
-    if (!shard_out) return FSDP_ERR_INVALID_ARG;
-    if (!aligned(shard_out, es)) return FSDP_ERR_ALIGNMENT;
     GatherArgs a;
-    memset(&a, 0, sizeof(a));
-    a.src = shard_out;
-    a.nbytes = static_cast<int64_t>(nbytes);
-    a.n_dst = n_dst;
-    for (int d = 0; d < n_dst; ++d) {
-        if (!full_bufs[d]) return FSDP_ERR_INVALID_ARG;
-        if (!aligned(full_bufs[d], es)) return FSDP_ERR_ALIGNMENT;
-        if (overlaps(full_bufs[d], nbytes, shard_out, nbytes)) return FSDP_ERR_INVALID_ARG;
-        for (int e = 0; e < d; ++e)
-            if (overlaps(full_bufs[d], nbytes, full_bufs[e], nbytes)) return FSDP_ERR_INVALID_ARG;
-        a.dst[d] = full_bufs[d];
-    }
+    bool empty = false;
+    const fsdp_status st = prepare_gather(shard_out, dtype, world, padded_numel, full_bufs, n_dst, a, empty);
+    if (st != FSDP_OK || empty) return st;
     return launch_gather(a, static_cast<cudaStream_t>(stream));
+}
+
+FSDP_API fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
+                                     int gathers, int fuse_first_gather, uint32_t *nonfinite_count,
+                                     void *stream) {
+    if (n_units < 0 || (n_units > 0 && !units) || !hp) return FSDP_ERR_INVALID_ARG;
+    if (gathers < 0 || gathers > FSDP_MAX_WORLD) return FSDP_ERR_INVALID_ARG;
+    const bool fuse = fuse_first_gather != 0 && gathers > 0;
+    std::vector<UnitPlan> plan(static_cast<size_t>(n_units));
+    std::vector<Span> spans;
+    for (int u = 0; u < n_units; ++u) {
+        const fsdp_unit &x = units[u];
+        UnitPlan &p = plan[static_cast<size_t>(u)];
+        if (!dtype_valid(x.grad_dtype) || !dtype_valid(x.out_dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
+        p.grad_dtype = static_cast<fsdp_dtype>(x.grad_dtype);
+        p.out_dtype = static_cast<fsdp_dtype>(x.out_dtype);
+        if (x.n_full < 0 || x.n_full > FSDP_MAX_WORLD || (x.n_full > 0 && !x.full_bufs)) return FSDP_ERR_INVALID_ARG;
+        if (gathers > 0 && x.n_full < 1) return FSDP_ERR_INVALID_ARG;
+        if (x.padded_numel > 0 && !x.shard_out) return FSDP_ERR_INVALID_ARG;
+        fsdp_status st = prepare_rsa(x.grads, p.grad_dtype, x.world, x.padded_numel, x.master, x.exp_avg,
+                                     x.exp_avg_sq, x.shard_out, p.out_dtype, fuse ? x.full_bufs : nullptr,
+                                     fuse ? x.n_full : 0, hp, 0, x.world, nonfinite_count, p.rsa, p.empty);
+        if (st != FSDP_OK) return st;
+        p.separate_gathers = p.empty ? 0 : gathers - (fuse ? 1 : 0);
+        if (p.separate_gathers > 0) {
+            bool gempty = false;
+            st = prepare_gather(x.shard_out, p.out_dtype, x.world, x.padded_numel, x.full_bufs, x.n_full, p.gather,
+                                gempty);
+            if (st != FSDP_OK) return st;
+        }
+        if (p.empty) continue;
+        const uintptr_t sb = static_cast<uintptr_t>(x.padded_numel) * 4;
+        const uintptr_t ob = static_cast<uintptr_t>(x.padded_numel) * static_cast<uintptr_t>(dtype_size(p.out_dtype));
+        const void *state[3] = {x.master, x.exp_avg, x.exp_avg_sq};
+        for (const void *b : state) spans.push_back({reinterpret_cast<uintptr_t>(b), reinterpret_cast<uintptr_t>(b) + sb});
+        spans.push_back({reinterpret_cast<uintptr_t>(x.shard_out), reinterpret_cast<uintptr_t>(x.shard_out) + ob});
+        if (gathers > 0)
+            for (int d = 0; d < x.n_full; ++d)
+                spans.push_back({reinterpret_cast<uintptr_t>(x.full_bufs[d]),
+                                 reinterpret_cast<uintptr_t>(x.full_bufs[d]) + ob});
+    }
+    // no two written buffers overlap (within a unit that is already checked;
+    // this catches two units sharing memory)
+    std::sort(spans.begin(), spans.end());
+    for (size_t i = 1; i < spans.size(); ++i)
+        if (spans[i].lo < spans[i - 1].hi) return FSDP_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (const UnitPlan &p : plan) {
+        if (p.empty) continue;
+        fsdp_status st = launch_rsa(p.rsa, p.grad_dtype, p.out_dtype, s);
+        if (st != FSDP_OK) return st;
+        for (int k = 0; k < p.separate_gathers; ++k) {
+            st = launch_gather(p.gather, s);
+            if (st != FSDP_OK) return st;
+        }
+    }
+    return FSDP_OK;
 }
 
 FSDP_API const char *fsdp_status_string(fsdp_status status) {

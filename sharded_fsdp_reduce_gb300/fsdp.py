@@ -12,7 +12,7 @@ from typing import List, Optional, Sequence, Tuple
 import torch
 
 from . import _lib
-from ._lib import FsdpAdamwHparams, FsdpStepConfig, FsdpView
+from ._lib import FsdpAdamwHparams, FsdpStepConfig, FsdpUnit, FsdpView
 
 __all__ = [
     "AdamWHParams", "StepConfig", "OPTIMIZERS", "FsdpError", "View", "fsdp_reduce_scatter_step",
@@ -20,6 +20,7 @@ __all__ = [
     "fsdp_reduce_scatter_adam_cast", "fsdp_reduce_scatter_adam_cast_gather", "fsdp_all_gather",
     "fsdp_status_string",
     "fsdp_last_cuda_error", "fsdp_take_wait_timeouts", "dtype_code",
+    "UnitDescs", "fsdp_step_units",
 ]
 
 _DTYPES = {torch.float32: _lib.FSDP_F32, torch.bfloat16: _lib.FSDP_BF16, torch.float16: _lib.FSDP_F16}
@@ -305,3 +306,64 @@ def fsdp_all_gather(shard_out: torch.Tensor, full_bufs: Sequence[torch.Tensor], 
     _check(_lib.load().fsdp_all_gather(_dev(shard_out, "shard_out"), dtype_code(shard_out.dtype), int(world),
                                        P_pad, _ptrs(full_bufs, "full_bufs"), len(full_bufs), _stream(stream)),
            "fsdp_all_gather")
+
+
+class UnitDescs:
+    """The C descriptors (fsdp_unit) of a sequence of FSDP units, built once
+    for fsdp_step_units. A unit is any object holding FlatParamUnit's
+    buffers: grads (N tensors), full (gathered buffers), master, exp_avg,
+    exp_avg_sq, shard_out, world. The descriptors hold the buffers' addresses:
+    build new ones if a unit's buffers are replaced. The units are kept alive
+    while the descriptors exist."""
+
+    def __init__(self, units: Sequence):
+        self.units = list(units)
+        self.n = len(self.units)
+        self.array = (FsdpUnit * max(self.n, 1))()
+        self._keep = []
+        for k, u in enumerate(self.units):
+            P = u.master.numel()
+            gdt = u.grads[0].dtype if u.grads else torch.bfloat16
+            for i, g in enumerate(u.grads):
+                if g.numel() != P or g.dtype != gdt:
+                    raise ValueError(f"units[{k}].grads[{i}] must hold {P} elements of {gdt}")
+            for name in ("master", "exp_avg", "exp_avg_sq"):
+                t = getattr(u, name)
+                if t.dtype != torch.float32 or t.numel() != P:
+                    raise ValueError(f"units[{k}].{name} must be float32 with {P} elements")
+            odt = u.shard_out.dtype
+            if u.shard_out.numel() != P:
+                raise ValueError(f"units[{k}].shard_out must hold {P} elements")
+            for i, f in enumerate(u.full):
+                if f.numel() != P or f.dtype != odt:
+                    raise ValueError(f"units[{k}].full[{i}] must hold {P} elements of {odt}")
+            grads = _ptrs(u.grads, f"units[{k}].grads", host_ok=True)
+            full = _ptrs(u.full, f"units[{k}].full") if u.full else None
+            self._keep += [grads, full]
+            d = self.array[k]
+            d.grads = ctypes.addressof(grads)
+            d.full_bufs = ctypes.addressof(full) if full is not None else None
+            d.master = _mem(u.master, f"units[{k}].master")
+            d.exp_avg = _mem(u.exp_avg, f"units[{k}].exp_avg")
+            d.exp_avg_sq = _mem(u.exp_avg_sq, f"units[{k}].exp_avg_sq")
+            d.shard_out = _dev(u.shard_out, f"units[{k}].shard_out")
+            d.padded_numel = P
+            d.world = len(u.grads)
+            d.grad_dtype = dtype_code(gdt)
+            d.out_dtype = dtype_code(odt)
+            d.n_full = len(u.full)
+
+
+def fsdp_step_units(units, hparams: AdamWHParams, gathers: int = 1, fuse_first_gather: bool = False,
+                    nonfinite_count: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> None:
+    """The step of a whole model in one call: for each unit in order, its
+    fused reduce-scatter + AdamW + cast, then `gathers` all-gathers into its
+    full buffers (the first written by the update kernel itself with
+    fuse_first_gather). `units` is a UnitDescs or a sequence of units (then
+    descriptors are built for this call)."""
+    descs = units if isinstance(units, UnitDescs) else UnitDescs(units)
+    nf = _dev(nonfinite_count, "nonfinite_count") if nonfinite_count is not None else None
+    hp = hparams.to_c()
+    _check(_lib.load().fsdp_step_units(descs.array, descs.n, ctypes.byref(hp), int(gathers),
+                                       1 if fuse_first_gather else 0, nf, _stream(stream)), "fsdp_step_units")

@@ -29,8 +29,8 @@ from typing import Dict, List, Optional, Sequence, Tuple
 
 import torch
 
-from .fsdp import (AdamWHParams, View, fsdp_all_gather, fsdp_flatten_pad, fsdp_reduce_scatter_adam_cast,
-                   fsdp_reduce_scatter_adam_cast_gather, fsdp_unflatten_views)
+from .fsdp import (AdamWHParams, UnitDescs, View, fsdp_all_gather, fsdp_flatten_pad, fsdp_reduce_scatter_adam_cast,
+                   fsdp_reduce_scatter_adam_cast_gather, fsdp_step_units, fsdp_unflatten_views)
 
 
 class FlatParamUnit:
@@ -178,3 +178,26 @@ class _HostPipeline:
             fsdp_all_gather(u.shard_out, u.full, u.world, stream=compute)
         compute.wait_stream(self.copy_out)  # the step ends when its result is on the host
         self.i += 1
+
+
+class UnitSequence:
+    """The FSDP units of a model, stepped in order by one call into the
+    library (fsdp_step_units): per unit the fused update and its all-gathers,
+    all on one stream, with the per-unit loop in native code."""
+
+    def __init__(self, units: Sequence[FlatParamUnit]):
+        self.units = list(units)
+        self.descs = UnitDescs(self.units)
+
+    def step(self, hp: AdamWHParams, gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None,
+             stream=None, fuse_gather: bool = False) -> None:
+        fsdp_step_units(self.descs, hp, gathers, fuse_gather, nonfinite_count, stream)
+
+    def step_bytes(self, gathers: int = 1) -> Tuple[int, int]:
+        """Algorithmic bytes of one model step: (fused kernels, all-gathers)."""
+        rsa = ag = 0
+        for u in self.units:
+            a, b = u.step_bytes(gathers)
+            rsa += a
+            ag += b
+        return rsa, ag

@@ -265,3 +265,66 @@ def test_binding_refuses_unpinned_host_tensors(lib):
         F.fsdp_reduce_scatter_step(g, st[0], st[1], st[2], out, F.StepConfig("adamw", 1e-3))
     with pytest.raises(ValueError, match="shard_out"):
         F.fsdp_all_gather(out, [out.clone()], 2)
+
+
+def _unit(E, base, world=2, P=16, n_full=2, gd=1, od=1):
+    """An fsdp_unit descriptor over fake, non-overlapping addresses (never
+    dereferenced: every call below is rejected on the host)."""
+    arr = lambda *p: (ctypes.c_void_p * len(p))(*p)
+    g = arr(*[base + 0x100000 * (q + 1) for q in range(world)])
+    f = arr(*[base + 0x1000000 * (8 + d) for d in range(n_full)]) if n_full else None
+    u = E.FsdpUnit()
+    u.grads = ctypes.addressof(g)
+    u.full_bufs = ctypes.addressof(f) if f is not None else None
+    u.master, u.exp_avg, u.exp_avg_sq = base + 0x1000000, base + 0x2000000, base + 0x3000000
+    u.shard_out = base + 0x4000000
+    u.padded_numel, u.world, u.grad_dtype, u.out_dtype, u.n_full = P, world, gd, od, n_full
+    return u, (g, f)
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host-only: needs a machine without a GPU")
+def test_step_units_validates_every_unit_before_launching(lib):
+    # unit 0 is valid; the call must still fail on unit 1 without launching
+    # unit 0 (a launch here would report FSDP_ERR_CUDA: there is no device)
+    from sharded_fsdp_reduce_gb300 import _lib as E
+    hp = E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+    keep = []
+
+    def call(units, gathers=1, fuse=0, hpp=ctypes.byref(hp), n=None):
+        arr = (E.FsdpUnit * max(len(units), 1))(*units)
+        return lib.fsdp_step_units(arr, len(units) if n is None else n, hpp, gathers, fuse, None, None)
+
+    def unit(base, **kw):
+        u, k = _unit(E, base, **kw)
+        keep.append(k)
+        return u
+
+    A, B = FAKE, FAKE + 0x100000000
+    assert call([]) == E.FSDP_OK
+    assert lib.fsdp_step_units(None, 0, ctypes.byref(hp), 1, 0, None, None) == E.FSDP_OK
+    assert lib.fsdp_step_units(None, 1, ctypes.byref(hp), 1, 0, None, None) == E.FSDP_ERR_INVALID_ARG
+    assert call([unit(A)], hpp=None) == E.FSDP_ERR_INVALID_ARG
+    assert call([unit(A)], gathers=-1) == E.FSDP_ERR_INVALID_ARG
+    assert call([unit(A)], gathers=65) == E.FSDP_ERR_INVALID_ARG
+    assert call([unit(A), unit(B, gd=7)]) == E.FSDP_ERR_UNSUPPORTED_DTYPE
+    assert call([unit(A), unit(B, n_full=0)]) == E.FSDP_ERR_INVALID_ARG        # gathers without buffers
+    assert call([unit(A), unit(B, P=15)]) == E.FSDP_ERR_INVALID_ARG            # not a multiple of N
+    assert call([unit(A), unit(B, world=65)]) == E.FSDP_ERR_INVALID_ARG
+    bad = unit(B)
+    bad.master = B + 0x1000002
+    assert call([unit(A), bad]) == E.FSDP_ERR_ALIGNMENT
+    bad = unit(B)
+    bad.shard_out = None
+    assert call([unit(A), bad]) == E.FSDP_ERR_INVALID_ARG
+    bad = unit(B)
+    bad.exp_avg = A + 0x1000000                                                # shares unit 0's master
+    assert call([unit(A), bad]) == E.FSDP_ERR_INVALID_ARG
+    bad = unit(B)
+    bad.shard_out = A + 0x1000000 * 9                                          # unit 0's gathered buffer
+    assert call([unit(A), bad]) == E.FSDP_ERR_INVALID_ARG
+    bad = unit(B)
+    bad.master = B + 0x100000                                                  # master on its own gradient
+    assert call([unit(A), bad]) == E.FSDP_ERR_INVALID_ARG
+    assert call([unit(A, n_full=0), unit(B, n_full=0)], gathers=1, fuse=1) == E.FSDP_ERR_INVALID_ARG
+    assert call([unit(A, P=0), unit(B, P=0)]) == E.FSDP_OK                     # empty units: nothing to launch
+    assert lib.fsdp_last_cuda_error() == 0

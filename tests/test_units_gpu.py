@@ -1,0 +1,163 @@
+"""The multi-unit step (fsdp_step_units through UnitSequence): a model's FSDP
+units stepped in order by one native call. Each unit must end bit-identical
+to stepping it on its own with the single-unit entry points, and to the
+oracle; units of different N, dtypes and sizes, offloaded and HBM-resident,
+share one call.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fsdp_inputs as fi
+from gpu_util import host
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def F():
+    import __graft_entry__ as g
+    g.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import sharded_fsdp_reduce_gb300 as F
+    return F
+
+
+# (params, world, grad dtype, out dtype): a tiny odd unit, a GPT-2 small
+# block, an fp16 unit at N=2, and fp32 gradients at N=3 with a ragged pad
+MODEL = [
+    ((("w", (64, 64)), ("b", (3,))), 2, torch.bfloat16, torch.bfloat16),
+    (fi.CONFIGS["gpt2_small"].params, 8, torch.bfloat16, torch.bfloat16),
+    ((("w", (1280, 777)), ("b", (5,))), 2, torch.float16, torch.float16),
+    ((("w", (1001,)),), 3, torch.float32, torch.bfloat16),
+]
+
+
+def build_model(F, seed, state_on_host=()):
+    units = []
+    g = torch.Generator().manual_seed(seed)
+    for k, (params, world, gdt, odt) in enumerate(MODEL):
+        u = F.FlatParamUnit(params, world, gdt, odt, device=DEV, state_on_host=k in state_on_host)
+        flat = (torch.rand(u.numel, generator=g) * 0.2 - 0.1)
+        u.load_master([flat.to(DEV)])
+        units.append(u)
+    torch.cuda.synchronize()
+    return units
+
+
+def load_grads(units, t, seed):
+    g = torch.Generator().manual_seed(seed * 1000 + t)
+    for u in units:
+        for r in range(u.world):
+            x = torch.randn(u.numel, generator=g) * 1e-2
+            if u.grads[r].dtype == torch.float16:
+                x = x * 1024
+            u.load_grad(r, [x.to(DEV).to(u.grads[r].dtype)])
+
+
+def same(a, b):
+    iv = torch.int32 if a.element_size() == 4 else torch.int16
+    return torch.equal(a.detach().cpu().view(iv), b.detach().cpu().view(iv))
+
+
+def hp_for(F, u, t):
+    scale = 1024.0 if u.grads[0].dtype == torch.float16 else 1.0
+    return F.AdamWHParams(1e-3, weight_decay=0.01, step=t, grad_scale=scale)
+
+
+@pytest.mark.parametrize("gathers,fuse", [(1, False), (2, False), (1, True), (2, True), (0, False)])
+def test_units_match_single_unit_steps(F, gathers, fuse):
+    a = build_model(F, 1)
+    b = build_model(F, 1)
+    seq = F.UnitSequence(a)
+    for t in (1, 2, 3):
+        load_grads(a, t, 5)
+        load_grads(b, t, 5)
+        # one call for the whole model; the fp16 unit carries its loss scale
+        # in its own hyperparameters, so it steps separately in both runs
+        fp16 = [u for u in a if u.grads[0].dtype == torch.float16]
+        F.UnitSequence([u for u in a if u not in fp16]).step(hp_for(F, a[0], t), gathers=gathers, fuse_gather=fuse)
+        for u in fp16:
+            F.UnitSequence([u]).step(hp_for(F, u, t), gathers=gathers, fuse_gather=fuse)
+        for u in b:
+            u.step(hp_for(F, u, t), gathers=gathers, fuse_gather=fuse)
+    torch.cuda.synchronize()
+    assert len(seq.units) == len(MODEL)
+    for ua, ub in zip(a, b):
+        for x, y in ((ua.master, ub.master), (ua.exp_avg, ub.exp_avg), (ua.exp_avg_sq, ub.exp_avg_sq),
+                     (ua.shard_out, ub.shard_out)):
+            assert same(x, y)
+        for fa, fb in zip(ua.full, ub.full):
+            assert same(fa, fb)
+        if gathers:
+            for f in ua.full:
+                assert same(f, ua.shard_out)
+
+
+def test_units_match_oracle(F, orc):
+    units = build_model(F, 2)
+    units = [u for u in units if u.grads[0].dtype != torch.float16]  # one loss scale per call
+    seq = F.UnitSequence(units)
+    fmt = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}
+    st = [[host(u.master), np.zeros(u.padded_numel, np.float32), np.zeros(u.padded_numel, np.float32)]
+          for u in units]
+    for t in (1, 2):
+        load_grads(units, t, 9)
+        seq.step(hp_for(F, units[0], t), gathers=2)
+        torch.cuda.synchronize()
+        for u, (p, m, v) in zip(units, st):
+            g_o = [host(g) for g in u.grads]
+            shards_o, _ = orc.fsdp_step(g_o, fmt[u.grads[0].dtype], u.world, p, m, v, fmt[u.shard_out.dtype],
+                                        orc.hparams(1e-3, 0.9, 0.999, 1e-8, 0.01, t, 1.0))
+            np.testing.assert_array_equal(host(u.master).view(np.uint32), p.view(np.uint32))
+            np.testing.assert_array_equal(host(u.exp_avg).view(np.uint32), m.view(np.uint32))
+            np.testing.assert_array_equal(host(u.exp_avg_sq).view(np.uint32), v.view(np.uint32))
+            np.testing.assert_array_equal(host(u.shard_out), shards_o)
+            for f in u.full:
+                assert torch.equal(f, u.shard_out)
+
+
+def test_units_with_offloaded_state_and_a_shared_counter(F):
+    a = [u for u in build_model(F, 3, state_on_host={0, 1}) if u.grads[0].dtype != torch.float16]
+    b = [u for u in build_model(F, 3) if u.grads[0].dtype != torch.float16]
+    nf_a = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nf_b = torch.zeros(1, dtype=torch.int32, device=DEV)
+    load_grads(a, 1, 4)
+    load_grads(b, 1, 4)
+    for us in (a, b):  # two non-finite gradients in unit 0, one in unit 2
+        us[0].grads[0][5] = float("inf")
+        us[0].grads[1][7] = float("nan")
+        us[2].grads[1][0] = float("-inf")
+    F.UnitSequence(a).step(hp_for(F, a[0], 1), gathers=1, nonfinite_count=nf_a)
+    for u in b:
+        u.step(hp_for(F, u, 1), gathers=1, nonfinite_count=nf_b)
+    torch.cuda.synchronize()
+    assert int(nf_a.item()) == int(nf_b.item()) == 3
+    for ua, ub in zip(a, b):
+        for x, y in ((ua.master, ub.master), (ua.exp_avg, ub.exp_avg), (ua.shard_out, ub.shard_out)):
+            assert same(x, y)
+
+
+def test_units_rejects_shared_buffers_and_enqueues_nothing(F):
+    a = build_model(F, 4)
+    a[1].exp_avg = a[0].master  # two units writing one buffer (sizes differ: the binding catches it)
+    with pytest.raises(ValueError):
+        F.UnitSequence(a)
+    b = build_model(F, 4)
+    b[3].exp_avg = b[0].exp_avg.narrow(0, 0, b[3].padded_numel)  # same size: only the library sees it
+    before = [u.master.clone() for u in b]
+    with pytest.raises(F.FsdpError):
+        F.UnitSequence(b).step(hp_for(F, b[0], 1), gathers=1)
+    torch.cuda.synchronize()
+    for u, p in zip(b, before):
+        assert same(u.master, p)  # nothing ran, not even the units before the bad one
+
+
+def test_units_empty(F):
+    F.UnitSequence([]).step(F.AdamWHParams(1e-3, step=1), gathers=2)
+    e = F.FlatParamUnit([("x", (0,))], 2, torch.bfloat16, torch.bfloat16, device=DEV)
+    assert e.padded_numel == 0
+    F.UnitSequence([e]).step(F.AdamWHParams(1e-3, step=1), gathers=1)
+    torch.cuda.synchronize()
