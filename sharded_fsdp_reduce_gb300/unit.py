@@ -123,6 +123,36 @@ class FlatParamUnit:
             self._host = _HostPipeline(self)
         self._host.step(host_grads, host_out, hp, gathers, nonfinite_count, host_nonfinite)
 
+    # ---------------------------------------------------------------- snapshot / resume
+
+    def state_dict(self, rank: Optional[int] = None) -> Dict[str, torch.Tensor]:
+        """Host copies of the optimizer state: the whole unit (rank=None), or
+        rank r's shard [r*S, (r+1)*S) alone, the per-rank file of a sharded
+        checkpoint ("fairseq ... FSDP 实战指南", --use-sharded-state: each
+        rank saves its own shard). Synchronizes with the current stream."""
+        lo, hi = self._range(rank)
+        if self.device.type == "cuda":
+            torch.cuda.current_stream(self.device).synchronize()
+        return {name: getattr(self, name)[lo:hi].detach().to("cpu", copy=True)
+                for name in ("master", "exp_avg", "exp_avg_sq")}
+
+    def load_state_dict(self, state: Dict[str, torch.Tensor], rank: Optional[int] = None) -> None:
+        """Restore what state_dict(rank) returned (rank=None: the whole unit)."""
+        lo, hi = self._range(rank)
+        for name in ("master", "exp_avg", "exp_avg_sq"):
+            src = state[name]
+            if src.dtype != torch.float32 or src.numel() != hi - lo:
+                raise ValueError(f"{name} must be float32 with {hi - lo} elements")
+            getattr(self, name)[lo:hi].copy_(src.reshape(-1))
+
+    def _range(self, rank: Optional[int]) -> Tuple[int, int]:
+        if rank is None:
+            return 0, self.padded_numel
+        if not 0 <= int(rank) < self.world:
+            raise ValueError(f"rank must be in [0, {self.world})")
+        S = self.shard_numel
+        return int(rank) * S, (int(rank) + 1) * S
+
     def step_bytes(self, gathers: int = 1) -> Tuple[int, int]:
         """Algorithmic bytes of one step: (fused kernel, all-gathers)."""
         gs = self.grads[0].element_size()

@@ -731,3 +731,43 @@ def test_extreme_values_match_the_oracle(F, orc, gfmt, lr):
         wnan = ((shards_o & 0x7f80) == 0x7f80) & ((shards_o & 0x7f) != 0)
         assert np.array_equal(onan, wnan)
         np.testing.assert_array_equal(ob[~onan], shards_o[~wnan])
+
+
+# ------------------------------------------------------------------ snapshot / resume
+
+@pytest.mark.parametrize("sharded,host_state", [(False, False), (True, False), (True, True)])
+def test_resume_from_snapshot_is_bit_exact(F, sharded, host_state):
+    # four steps in one go against two steps, a snapshot (whole, or one file
+    # per rank shard), a fresh unit (optionally offloaded) restored from it,
+    # and two more steps
+    cfg = fi.CONFIGS["gpt2_small"]
+    N = cfg.world
+    a, b = new_unit(F, cfg), new_unit(F, cfg)
+    master = fi.gen_master(cfg, device=DEV)
+    a.load_master([master])
+    b.load_master([master])
+
+    def step(u, t):
+        for r in range(N):
+            u.grads[r].copy_(fi.gen_grad(cfg, r, t, device=DEV))
+        u.step(hp_for(F, cfg, t), gathers=1)
+
+    for t in (1, 2, 3, 4):
+        step(a, t)
+    for t in (1, 2):
+        step(b, t)
+    snap = [b.state_dict(rank=r) for r in range(N)] if sharded else b.state_dict()
+    del b
+    c = new_unit(F, cfg, state_on_host=host_state)
+    if sharded:
+        for r in reversed(range(N)):
+            c.load_state_dict(snap[r], rank=r)
+    else:
+        c.load_state_dict(snap)
+    for t in (3, 4):
+        step(c, t)
+    torch.cuda.synchronize()
+    for name in ("master", "exp_avg", "exp_avg_sq"):
+        assert torch.equal(getattr(a, name).cpu().view(torch.int32), getattr(c, name).cpu().view(torch.int32)), name
+    assert torch.equal(a.shard_out.view(torch.int16), c.shard_out.view(torch.int16))
+    assert torch.equal(a.full[0].view(torch.int16), c.full[0].view(torch.int16))

@@ -1,0 +1,58 @@
+"""Host logic of FlatParamUnit that needs no GPU: layout of a unit's buffers
+and the snapshot / resume of its optimizer state, whole or per rank shard."""
+import pytest
+import torch
+
+
+@pytest.fixture(scope="module")
+def F():
+    import __graft_entry__ as g
+    g.build()
+    import sharded_fsdp_reduce_gb300 as F
+    return F
+
+
+def cpu_unit(F, world=3):
+    return F.FlatParamUnit([("w", (4, 5)), ("b", (3,))], world, torch.bfloat16, torch.bfloat16, device="cpu")
+
+
+def test_unit_layout(F):
+    u = cpu_unit(F)
+    assert u.numel == 23 and u.padded_numel == 24 and u.shard_numel == 8
+    assert [v.offset for v in u.views] == [0, 20]
+    assert len(u.grads) == 3 and len(u.full) == 3
+    pv = u.param_views(torch.arange(24.0))
+    assert pv["w"].shape == (4, 5) and pv["b"].tolist() == [20.0, 21.0, 22.0]
+
+
+def test_state_dict_whole_and_sharded_round_trip(F):
+    a = cpu_unit(F)
+    for k, name in enumerate(("master", "exp_avg", "exp_avg_sq")):
+        getattr(a, name).copy_(torch.arange(24, dtype=torch.float32) + 100 * k)
+    whole = a.state_dict()
+    shards = [a.state_dict(rank=r) for r in range(3)]
+    assert shards[1]["exp_avg"].tolist() == [float(x) for x in range(108, 116)]
+    # the snapshot is a copy: later updates do not reach it
+    a.master.zero_()
+    assert whole["master"][5] == 5.0
+    b, c = cpu_unit(F), cpu_unit(F)
+    b.load_state_dict(whole)
+    for r in (2, 0, 1):
+        c.load_state_dict(shards[r], rank=r)
+    for name in ("master", "exp_avg", "exp_avg_sq"):
+        assert torch.equal(getattr(b, name), whole[name])
+        assert torch.equal(getattr(c, name), whole[name])
+
+
+def test_state_dict_rejects_bad_input(F):
+    u = cpu_unit(F)
+    with pytest.raises(ValueError):
+        u.state_dict(rank=3)
+    with pytest.raises(ValueError):
+        u.load_state_dict(u.state_dict(rank=0))            # a shard is not the whole unit
+    with pytest.raises(ValueError):
+        u.load_state_dict(u.state_dict(), rank=1)          # nor the whole unit a shard
+    bad = u.state_dict()
+    bad["exp_avg"] = bad["exp_avg"].double()
+    with pytest.raises(ValueError):
+        u.load_state_dict(bad)
