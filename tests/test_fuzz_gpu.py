@@ -124,3 +124,50 @@ def test_fuzz_variant_step(F, orc, seed):
             cmp(host(states[k]), s_o[k], f"state{k} " + tag)
         if out is not None:
             assert_out_close(host(out), shards_o, ofmt, "shard_out " + tag)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fuzz_step_units(F, orc, seed):
+    # a random model: 1-5 units of random N, size and dtypes, some offloaded,
+    # stepped by fsdp_step_units with random gathers and fusion
+    rng = np.random.default_rng(5000 + seed)
+    n_units = int(rng.integers(1, 6))
+    gathers = int(rng.integers(0, 3))
+    fuse = bool(rng.integers(0, 2))
+    units, st = [], []
+    for _ in range(n_units):
+        world = int(rng.choice([1, 2, 3, 8]))
+        P = int(rng.integers(1, 30000))
+        gfmt, ofmt = str(rng.choice(FMTS)), str(rng.choice(FMTS))
+        u = F.FlatParamUnit([("x", (P,))], world, fi.torch_dtype(gfmt), fi.torch_dtype(ofmt), device=DEV,
+                            n_full=int(rng.integers(1, world + 1)), state_on_host=bool(rng.integers(0, 2)))
+        p0 = orc.flatten_pad([rng.uniform(-0.1, 0.1, P).astype(np.float32)], world)
+        u.master.copy_(torch.from_numpy(p0))
+        units.append((u, gfmt, ofmt, P))
+        st.append([p0.copy(), np.zeros_like(p0), np.zeros_like(p0)])
+    seq = F.UnitSequence([u for u, *_ in units])
+    for t in (1, 2):
+        hp = F.AdamWHParams(1e-3, weight_decay=0.01, step=t)
+        rows_all = []
+        for u, gfmt, ofmt, P in units:
+            rows = []
+            for r in range(u.world):
+                x = torch.from_numpy(orc.flatten_pad([(rng.standard_normal(P) * 1e-2).astype(np.float32)], u.world))
+                x = x.to(fi.torch_dtype(gfmt))
+                u.grads[r].copy_(x.to(DEV))
+                rows.append(host(x))
+            rows_all.append(rows)
+        seq.step(hp, gathers=gathers, fuse_gather=fuse)
+        torch.cuda.synchronize()
+        for (u, gfmt, ofmt, P), rows, (p, m, v) in zip(units, rows_all, st):
+            shards_o, _ = orc.fsdp_step(rows, gfmt, u.world, p, m, v, ofmt,
+                                        orc.hparams(1e-3, 0.9, 0.999, 1e-8, 0.01, t, 1.0))
+            assert_state_close(host(u.master), p, f"seed {seed} master t={t}")
+            assert_state_close(host(u.exp_avg), m, f"seed {seed} exp_avg t={t}")
+            assert_state_close(host(u.exp_avg_sq), v, f"seed {seed} exp_avg_sq t={t}")
+            assert_out_close(host(u.shard_out), shards_o, ofmt, f"seed {seed} shard_out t={t}")
+            for f in u.full:
+                if gathers:
+                    assert torch.equal(f, u.shard_out)
+                else:
+                    assert not f.view(torch.uint8).any()  # never gathered: still zero
