@@ -29,8 +29,9 @@
  *  - Pointers named "device" are CUDA device addresses of the current device;
  *    pointer arrays themselves (grads, srcs, full_bufs) are HOST arrays of
  *    device addresses. The caller owns every buffer; the library allocates
- *    no device memory and keeps no state besides a per-device cache of the
- *    SM count.
+ *    no device memory and keeps no state besides launch caches (the SM
+ *    count and kernel occupancies per device) and the side streams of
+ *    fsdp_step_units.
  *  - Offload. Where an argument says "device or mapped host", the buffer
  *    may also be page-locked host memory mapped into the device's address
  *    space (cudaHostAlloc, or cudaHostRegister with mapping; the same
@@ -284,8 +285,8 @@ fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
 
 /* The step of a whole model (device): its FSDP units in order, each one's
  * fused reduce-scatter + AdamW + cast over all its ranks followed by
- * `gathers` all-gathers of its shard_out into its n_full buffers, all on one
- * stream -- the per-unit driver of "FSDP (Fully Sharded Data Parallel)",
+ * `gathers` all-gathers of its shard_out into its n_full buffers, in the
+ * order of `stream` -- the per-unit driver of "FSDP (Fully Sharded Data Parallel)",
  * "The Per-Layer Communication" (one unit per wrapped layer, each
  * reduce-scattered and gathered on its own) in one call. With
  * fuse_first_gather != 0 the first gather of each unit is written by its
@@ -300,7 +301,13 @@ fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
  * no buffer written by one unit may overlap a buffer written by another,
  * before anything is enqueued: an invalid unit makes the call return its
  * status and enqueue nothing. FSDP_ERR_CUDA reports a launch that failed
- * after the units before it were enqueued. */
+ * after the units before it were enqueued.
+ * Scheduling: the units share no written buffer, so with two or more of
+ * them their kernels are spread round-robin over two streams the library
+ * keeps per host thread and device (created on first use), which wait for
+ * the work already on `stream` and which `stream` waits for afterwards; a
+ * unit's kernels run in order on one of them and overlap the neighbouring
+ * unit's. Work enqueued on `stream` after the call sees every unit done. */
 fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
                             int gathers, int fuse_first_gather, uint32_t *nonfinite_count,
                             void *stream);

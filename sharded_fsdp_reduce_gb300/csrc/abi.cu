@@ -324,6 +324,59 @@ struct Span {
     bool operator<(const Span &o) const { return lo < o.lo; }
 };
 
+// Side streams of fsdp_step_units. The units of a model are independent, so
+// their launches are spread round-robin over kUnitStreams streams that fork
+// from the caller's stream (an event) and join back into it (one event per
+// side stream): one unit's kernels then overlap the ramp-up and tail of its
+// neighbours'. Per host thread and device, created on first use and kept (a
+// cache, like the SM count); per thread so that concurrent callers never
+// re-record each other's fork and join events.
+#ifndef FSDP_UNIT_STREAMS
+#define FSDP_UNIT_STREAMS 2
+#endif
+constexpr int kUnitStreams = FSDP_UNIT_STREAMS;
+
+struct SideStreams {
+    cudaStream_t s[kUnitStreams > 0 ? kUnitStreams : 1] = {};
+    cudaEvent_t fork = nullptr;
+    cudaEvent_t done[kUnitStreams > 0 ? kUnitStreams : 1] = {};
+    bool ready = false;
+    ~SideStreams() {
+        // at thread or process exit; errors (a context already gone) are moot
+        for (int i = 0; i < kUnitStreams; ++i) {
+            if (s[i]) cudaStreamDestroy(s[i]);
+            if (done[i]) cudaEventDestroy(done[i]);
+        }
+        if (fork) cudaEventDestroy(fork);
+    }
+};
+
+thread_local SideStreams t_side[kMaxDevices];
+
+fsdp_status side_streams(SideStreams *&out) {
+    int dev = 0;
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= kMaxDevices) return FSDP_ERR_INVALID_ARG;
+    SideStreams &x = t_side[dev];
+    if (!x.ready) {
+        cudaError_t e = cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming);
+        for (int i = 0; i < kUnitStreams && e == cudaSuccess; ++i) {
+            e = cudaStreamCreateWithFlags(&x.s[i], cudaStreamNonBlocking);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&x.done[i], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess) return cuda_status(e);
+        x.ready = true;
+    }
+    out = &x;
+    return FSDP_OK;
+}
+
+fsdp_status launch_unit(const UnitPlan &p, cudaStream_t s) {
+    fsdp_status st = launch_rsa(p.rsa, p.grad_dtype, p.out_dtype, s);
+    for (int k = 0; st == FSDP_OK && k < p.separate_gathers; ++k) st = launch_gather(p.gather, s);
+    return st;
+}
+
 }  // namespace
 
 extern "C" {
@@ -464,16 +517,37 @@ FSDP_API fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const 
     for (size_t i = 1; i < spans.size(); ++i)
         if (spans[i].lo < spans[i - 1].hi) return FSDP_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int busy = 0;
+    for (const UnitPlan &p : plan) busy += p.empty ? 0 : 1;
+    if (kUnitStreams < 2 || busy < 2) {
+        for (const UnitPlan &p : plan) {
+            if (p.empty) continue;
+            if (fsdp_status st = launch_unit(p, s); st != FSDP_OK) return st;
+        }
+        return FSDP_OK;
+    }
+    SideStreams *side = nullptr;
+    if (fsdp_status st = side_streams(side); st != FSDP_OK) return st;
+    const int ns = busy < kUnitStreams ? busy : kUnitStreams;
+    if (cudaError_t e = cudaEventRecord(side->fork, s); e != cudaSuccess) return cuda_status(e);
+    for (int i = 0; i < ns; ++i)
+        if (cudaError_t e = cudaStreamWaitEvent(side->s[i], side->fork, 0); e != cudaSuccess) return cuda_status(e);
+    fsdp_status result = FSDP_OK;
+    int k = 0;
     for (const UnitPlan &p : plan) {
         if (p.empty) continue;
-        fsdp_status st = launch_rsa(p.rsa, p.grad_dtype, p.out_dtype, s);
-        if (st != FSDP_OK) return st;
-        for (int k = 0; k < p.separate_gathers; ++k) {
-            st = launch_gather(p.gather, s);
-            if (st != FSDP_OK) return st;
-        }
+        result = launch_unit(p, side->s[k++ % ns]);
+        if (result != FSDP_OK) break;
     }
-    return FSDP_OK;
+    // join every side stream back into the caller's stream, also after a
+    // failed launch, so that what was enqueued stays ordered before the
+    // caller's later work
+    for (int i = 0; i < ns; ++i) {
+        cudaError_t e = cudaEventRecord(side->done[i], side->s[i]);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, side->done[i], 0);
+        if (e != cudaSuccess && result == FSDP_OK) result = cuda_status(e);
+    }
+    return result;
 }
 
 FSDP_API const char *fsdp_status_string(fsdp_status status) {

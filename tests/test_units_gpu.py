@@ -161,3 +161,28 @@ def test_units_empty(F):
     assert e.padded_numel == 0
     F.UnitSequence([e]).step(F.AdamWHParams(1e-3, step=1), gathers=1)
     torch.cuda.synchronize()
+
+
+def test_units_order_with_the_callers_stream(F):
+    # the units run on the library's side streams, forked from and joined
+    # back into the caller's stream: gradients written on that stream just
+    # before the call (behind a 0.1 s spin) must be the ones used, and work
+    # queued on it just after must see every unit finished. Only the
+    # caller's stream is synchronized.
+    a = [u for u in build_model(F, 6) if u.grads[0].dtype != torch.float16]
+    b = [u for u in build_model(F, 6) if u.grads[0].dtype != torch.float16]
+    load_grads(b, 1, 8)
+    for u in b:
+        u.step(hp_for(F, u, 1), gathers=1)
+    torch.cuda.synchronize()
+    seq = F.UnitSequence(a)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(200_000_000)  # ~0.1 s of spinning before the gradients land
+        load_grads(a, 1, 8)
+        seq.step(hp_for(F, a[0], 1), gathers=1, stream=s)
+        after = [(u.master.clone(), u.full[-1].clone()) for u in a]
+    s.synchronize()
+    for (m, f), ub in zip(after, b):
+        assert same(m, ub.master)
+        assert same(f, ub.full[-1])
