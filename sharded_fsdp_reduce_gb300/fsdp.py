@@ -69,7 +69,7 @@ class StepConfig:
     grad_scale: float = 1.0
     reduce_dtype: Optional[torch.dtype] = None
 
-    def to_c(self, grad_dtype: torch.dtype) -> FsdpStepConfig:
+    def to_c(self) -> FsdpStepConfig:
         rd = _lib.FSDP_F32 if self.reduce_dtype is None else dtype_code(self.reduce_dtype)
         return FsdpStepConfig(OPTIMIZERS[self.optimizer], rd, self.lr, self.beta1, self.beta2, self.eps,
                               self.weight_decay, int(self.step), self.grad_scale)
@@ -121,6 +121,30 @@ def _mem(t: torch.Tensor, name: str) -> int:
 def _ptrs(ts: Sequence[torch.Tensor], name: str, host_ok: bool = False):
     get = _mem if host_ok else _dev
     return (ctypes.c_void_p * len(ts))(*[get(t, f"{name}[{i}]") for i, t in enumerate(ts)])
+
+
+def _grad_dtype(grads: Sequence[torch.Tensor], P_pad: int, name: str = "grads") -> torch.dtype:
+    """The gradients' common dtype, after checking every buffer's length and dtype."""
+    gdt = grads[0].dtype if len(grads) else torch.bfloat16
+    for i, g in enumerate(grads):
+        if g.numel() != P_pad or g.dtype != gdt:
+            raise ValueError(f"{name}[{i}] must hold {P_pad} elements of {gdt}")
+    return gdt
+
+
+def _check_fp32_state(P_pad: int, prefix: str = "", **bufs: torch.Tensor) -> None:
+    for name, t in bufs.items():
+        if t.dtype != torch.float32 or t.numel() != P_pad:
+            raise ValueError(f"{prefix}{name} must be float32 with {P_pad} elements")
+
+
+def _counter(t: Optional[torch.Tensor]):
+    """Device address of the optional non-finite counter (a CUDA int32/uint32 tensor)."""
+    if t is None:
+        return None
+    if t.dtype not in (torch.int32, torch.uint32) or t.numel() < 1:
+        raise ValueError("nonfinite_count must be a CUDA int32/uint32 tensor")
+    return _dev(t, "nonfinite_count")
 
 
 def _views(c_views, n) -> List[View]:
@@ -200,27 +224,17 @@ def fsdp_reduce_scatter_adam_cast(grads: Sequence[torch.Tensor], master: torch.T
     """
     world = len(grads)
     P_pad = master.numel()
-    gdt = grads[0].dtype if world else torch.bfloat16
-    for i, g in enumerate(grads):
-        if g.numel() != P_pad or g.dtype != gdt:
-            raise ValueError(f"grads[{i}] must hold {P_pad} elements of {gdt}")
-    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
-        if t.dtype != torch.float32 or t.numel() != P_pad:
-            raise ValueError(f"{name} must be float32 with {P_pad} elements")
+    gdt = _grad_dtype(grads, P_pad)
+    _check_fp32_state(P_pad, master=master, exp_avg=exp_avg, exp_avg_sq=exp_avg_sq)
     if shard_out.numel() != P_pad:
         raise ValueError(f"shard_out must hold {P_pad} elements")
-    nf = 0
-    if nonfinite_count is not None:
-        if nonfinite_count.dtype not in (torch.int32, torch.uint32) or nonfinite_count.numel() < 1:
-            raise ValueError("nonfinite_count must be a CUDA int32/uint32 tensor")
-        nf = _dev(nonfinite_count, "nonfinite_count")
+    nf = _counter(nonfinite_count)
     hp = hparams.to_c()
-    rb = int(rank_begin)
     re = world if rank_end is None else int(rank_end)
     args = (_ptrs(grads, "grads", host_ok=True) if world else None, dtype_code(gdt), world, P_pad,
             _mem(master, "master"), _mem(exp_avg, "exp_avg"), _mem(exp_avg_sq, "exp_avg_sq"),
-            _dev(shard_out, "shard_out"), dtype_code(shard_out.dtype), ctypes.byref(hp), rb, re,
-            nf or None, _stream(stream))
+            _dev(shard_out, "shard_out"), dtype_code(shard_out.dtype), ctypes.byref(hp), int(rank_begin), re,
+            nf, _stream(stream))
     _check(_lib.load().fsdp_reduce_scatter_adam_cast(*args), "fsdp_reduce_scatter_adam_cast")
 
 
@@ -244,14 +258,9 @@ def fsdp_reduce_scatter_adam_cast_gather(grads: Sequence[torch.Tensor], master: 
             raise ValueError(f"full_bufs[{i}] must hold {P_pad} elements of {odt}")
     if shard_out is not None and (shard_out.numel() != P_pad or shard_out.dtype != odt):
         raise ValueError(f"shard_out must hold {P_pad} elements of {odt}")
-    gdt = grads[0].dtype if world else torch.bfloat16
-    for i, g in enumerate(grads):
-        if g.numel() != P_pad or g.dtype != gdt:
-            raise ValueError(f"grads[{i}] must hold {P_pad} elements of {gdt}")
-    for name, t in (("master", master), ("exp_avg", exp_avg), ("exp_avg_sq", exp_avg_sq)):
-        if t.dtype != torch.float32 or t.numel() != P_pad:
-            raise ValueError(f"{name} must be float32 with {P_pad} elements")
-    nf = _dev(nonfinite_count, "nonfinite_count") if nonfinite_count is not None else None
+    gdt = _grad_dtype(grads, P_pad)
+    _check_fp32_state(P_pad, master=master, exp_avg=exp_avg, exp_avg_sq=exp_avg_sq)
+    nf = _counter(nonfinite_count)
     hp = hparams.to_c()
     re = world if rank_end is None else int(rank_end)
     args = (_ptrs(grads, "grads", host_ok=True) if world else None, dtype_code(gdt), world, P_pad,
@@ -275,10 +284,7 @@ def fsdp_reduce_scatter_step(grads: Sequence[torch.Tensor], param: torch.Tensor,
     tensors (offload mode)."""
     world = len(grads)
     P_pad = param.numel()
-    gdt = grads[0].dtype if world else torch.bfloat16
-    for i, g in enumerate(grads):
-        if g.numel() != P_pad or g.dtype != gdt:
-            raise ValueError(f"grads[{i}] must hold {P_pad} elements of {gdt}")
+    gdt = _grad_dtype(grads, P_pad)
     sdt = param.dtype
     for name, t in (("state0", state0), ("state1", state1)):
         if t is not None and (t.dtype != sdt or t.numel() != P_pad):
@@ -286,8 +292,8 @@ def fsdp_reduce_scatter_step(grads: Sequence[torch.Tensor], param: torch.Tensor,
     if shard_out is not None and shard_out.numel() != P_pad:
         raise ValueError(f"shard_out must hold {P_pad} elements")
     odt = shard_out.dtype if shard_out is not None else sdt
-    nf = _dev(nonfinite_count, "nonfinite_count") if nonfinite_count is not None else None
-    cfg = config.to_c(gdt)
+    nf = _counter(nonfinite_count)
+    cfg = config.to_c()
     re = world if rank_end is None else int(rank_end)
     args = (_ptrs(grads, "grads", host_ok=True) if world else None, dtype_code(gdt), world, P_pad,
             _mem(param, "param"), _mem(state0, "state0"), _mem(state1, "state1") if state1 is not None else None,
@@ -323,14 +329,8 @@ class UnitDescs:
         self._keep = []
         for k, u in enumerate(self.units):
             P = u.master.numel()
-            gdt = u.grads[0].dtype if u.grads else torch.bfloat16
-            for i, g in enumerate(u.grads):
-                if g.numel() != P or g.dtype != gdt:
-                    raise ValueError(f"units[{k}].grads[{i}] must hold {P} elements of {gdt}")
-            for name in ("master", "exp_avg", "exp_avg_sq"):
-                t = getattr(u, name)
-                if t.dtype != torch.float32 or t.numel() != P:
-                    raise ValueError(f"units[{k}].{name} must be float32 with {P} elements")
+            gdt = _grad_dtype(u.grads, P, f"units[{k}].grads")
+            _check_fp32_state(P, f"units[{k}].", master=u.master, exp_avg=u.exp_avg, exp_avg_sq=u.exp_avg_sq)
             odt = u.shard_out.dtype
             if u.shard_out.numel() != P:
                 raise ValueError(f"units[{k}].shard_out must hold {P} elements")
@@ -363,7 +363,7 @@ def fsdp_step_units(units, hparams: AdamWHParams, gathers: int = 1, fuse_first_g
     fuse_first_gather). `units` is a UnitDescs or a sequence of units (then
     descriptors are built for this call)."""
     descs = units if isinstance(units, UnitDescs) else UnitDescs(units)
-    nf = _dev(nonfinite_count, "nonfinite_count") if nonfinite_count is not None else None
+    nf = _counter(nonfinite_count)
     hp = hparams.to_c()
     _check(_lib.load().fsdp_step_units(descs.array, descs.n, ctypes.byref(hp), int(gathers),
                                        1 if fuse_first_gather else 0, nf, _stream(stream)), "fsdp_step_units")
