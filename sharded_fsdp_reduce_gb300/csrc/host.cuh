@@ -49,6 +49,19 @@ inline fsdp_status check_launch() { return cuda_status(cudaGetLastError()); }
 
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Whether p is host memory (page-locked and mapped, or another host address
+// the device reaches): buffers there stream over the host link, which picks
+// the kernels' low-occupancy build. A pointer the runtime cannot classify
+// counts as device memory (its error is cleared).
+inline bool host_resident(const void *p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
+}
+
 // Byte ranges [a, a+na) and [b, b+nb) overlap.
 inline bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);

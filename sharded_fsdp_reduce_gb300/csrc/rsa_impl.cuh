@@ -39,14 +39,22 @@ namespace fsdp {
 namespace rsa {
 
 // Launch shape (compile-time tunables; the defaults are the measured best).
+// Two builds of the kernel differ only in their register budget: with the
+// state in HBM, 3 resident CTAs per SM (<= 80 registers, no spills) stream
+// faster than 2; with the state in host memory, the host link serves the
+// lower request rate of 2 CTAs per SM better.
 #ifndef FSDP_RSA_THREADS
 #define FSDP_RSA_THREADS 256
 #endif
 #ifndef FSDP_RSA_MIN_BLOCKS
-#define FSDP_RSA_MIN_BLOCKS 1
+#define FSDP_RSA_MIN_BLOCKS 3
+#endif
+#ifndef FSDP_RSA_MIN_BLOCKS_HOST_STATE
+#define FSDP_RSA_MIN_BLOCKS_HOST_STATE 1
 #endif
 constexpr int kThreads = FSDP_RSA_THREADS;
 constexpr int kMinBlocks = FSDP_RSA_MIN_BLOCKS;
+constexpr int kMinBlocksHostState = FSDP_RSA_MIN_BLOCKS_HOST_STATE;
 
 // AdamW on one element; each operation is rounded on its own (no FMA), in the
 // order of the documented definition.
@@ -189,8 +197,8 @@ __device__ __forceinline__ uint32_t vec_chunk(const RsaArgs &a, int world, int64
 // Grid-stride over nchunks 8-element chunks starting at vbegin, then the
 // scalar elements [begin, vbegin) and [vend, end). With nchunks = 0 and
 // vbegin = vend = end every element takes the scalar path.
-template <int NW, int GD, int OD, bool GATHER>
-__global__ void __launch_bounds__(kThreads, kMinBlocks)
+template <int NW, int GD, int OD, bool GATHER, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
     rsa_kernel(const __grid_constant__ RsaArgs a, int64_t vbegin, int64_t nchunks, int64_t vend) {
     const int world = NW > 0 ? NW : a.world;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
