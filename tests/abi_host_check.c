@@ -56,6 +56,25 @@ int main(void) {
     CHECK(fsdp_reduce_scatter_step(grads, FSDP_BF16, 2, 16, (void *)0x1000000, (void *)0x2000000,
                                    (void *)0x3000000 /* SGD takes one state */, FSDP_F32, (void *)0x4000000,
                                    FSDP_BF16, &cfg, 0, 2, NULL, NULL) == FSDP_ERR_INVALID_ARG);
+    /* the multi-unit step: nothing to do, then a unit rejected before launch */
+    CHECK(fsdp_step_units(NULL, 0, &hp, 2, 0, NULL, NULL) == FSDP_OK);
+    void *fulls[2] = {(void *)0x8000000, (void *)0x9000000};
+    fsdp_unit u;
+    memset(&u, 0, sizeof(u));
+    u.grads = grads;
+    u.full_bufs = fulls;
+    u.master = (float *)0x1000000;
+    u.exp_avg = (float *)0x2000000;
+    u.exp_avg_sq = (float *)0x3000000;
+    u.shard_out = (void *)0x4000000;
+    u.padded_numel = 15; /* not a multiple of world */
+    u.world = 2;
+    u.grad_dtype = FSDP_BF16;
+    u.out_dtype = FSDP_BF16;
+    u.n_full = 2;
+    CHECK(fsdp_step_units(&u, 1, &hp, 1, 1, NULL, NULL) == FSDP_ERR_INVALID_ARG);
+    u.padded_numel = 0; /* an empty unit is skipped */
+    CHECK(fsdp_step_units(&u, 1, &hp, 1, 1, NULL, NULL) == FSDP_OK);
     CHECK(fsdp_take_wait_timeouts(NULL) == FSDP_ERR_INVALID_ARG);
     CHECK(fsdp_last_cuda_error() == 0);
     printf("ok\n");
