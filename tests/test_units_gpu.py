@@ -186,3 +186,47 @@ def test_units_order_with_the_callers_stream(F):
     for (m, f), ub in zip(after, b):
         assert same(m, ub.master)
         assert same(f, ub.full[-1])
+
+
+def test_units_from_concurrent_host_threads(F):
+    # two host threads step their own models through the native driver on
+    # their own streams at once (side streams and their fork/join events are
+    # per thread); every unit ends as in a sequential run
+    import threading
+
+    def make(seed):
+        return [u for u in build_model(F, seed) if u.grads[0].dtype != torch.float16]
+
+    def run(units, stream, seed, errors):
+        try:
+            with torch.cuda.stream(stream):
+                seq = F.UnitSequence(units)
+                for t in range(1, 5):
+                    load_grads(units, t, seed)
+                    seq.step(hp_for(F, units[0], t), gathers=2, stream=stream, fuse_gather=(t % 2 == 0))
+            stream.synchronize()
+        except Exception as e:  # surfaced below
+            errors.append(e)
+
+    ref = [make(10), make(11)]
+    for units, seed in zip(ref, (20, 21)):
+        run(units, torch.cuda.current_stream(), seed, [])
+    torch.cuda.synchronize()
+    par = [make(10), make(11)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    errors = []
+    threads = [threading.Thread(target=run, args=(u, s, seed, errors))
+               for u, s, seed in zip(par, streams, (20, 21))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for ma, mb in zip(ref, par):
+        for ua, ub in zip(ma, mb):
+            for x, y in ((ua.master, ub.master), (ua.exp_avg, ub.exp_avg), (ua.exp_avg_sq, ub.exp_avg_sq),
+                         (ua.shard_out, ub.shard_out)):
+                assert same(x, y)
+            for fa, fb in zip(ua.full, ub.full):
+                assert same(fa, fb)
