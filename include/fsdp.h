@@ -278,7 +278,9 @@ fsdp_status fsdp_reduce_scatter_step(const void *const *grads, fsdp_dtype grad_d
  *   shard_out    device, padded_numel elements of dtype (any of the three).
  *   full_bufs    host array of n_dst device pointers (1 <= n_dst <=
  *                FSDP_MAX_WORLD), padded_numel elements each; they must not
- *                overlap shard_out or each other.
+ *                overlap shard_out or each other. Host memory is refused
+ *                (FSDP_ERR_INVALID_ARG) for shard_out and full_bufs alike:
+ *                the copy uses bulk transfers between device buffers.
  *   world        N; padded_numel must be a multiple of it. */
 fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
                             int64_t padded_numel, void *const *full_bufs, int n_dst, void *stream);
@@ -311,6 +313,35 @@ fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
 fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
                             int gathers, int fuse_first_gather, uint32_t *nonfinite_count,
                             void *stream);
+
+/* The buffers of one FSDP unit for fsdp_step_units_ex (the variant steps),
+ * laid out as fsdp_reduce_scatter_step takes them. Caller-owned. */
+typedef struct {
+    const void *const *grads;    /* host array of `world` pointers (device or mapped host), padded_numel each */
+    void *const *full_bufs;      /* host array of n_full device pointers, padded_numel elements of out_dtype */
+    void *param;                 /* state_dtype, device or mapped host, padded_numel */
+    void *state0;                /* state_dtype, device or mapped host, padded_numel */
+    void *state1;                /* state_dtype, device or mapped host; NULL for SGD */
+    void *shard_out;             /* device, out_dtype; fp32 state only (NULL for bf16/fp16 state) */
+    int64_t padded_numel;        /* a multiple of world (0: the unit is skipped) */
+    int32_t world;               /* N, 1..FSDP_MAX_WORLD */
+    int32_t grad_dtype;          /* fsdp_dtype */
+    int32_t state_dtype;         /* fsdp_dtype */
+    int32_t out_dtype;           /* fsdp_dtype; equal to state_dtype for bf16/fp16 state */
+    int32_t n_full;              /* 0..FSDP_MAX_WORLD */
+    int32_t reserved;            /* 0 */
+} fsdp_unit_ex;
+
+/* The multi-unit step with the variant update (device): as fsdp_step_units,
+ * but each unit takes fsdp_reduce_scatter_step's update under the one `cfg`
+ * (optimizer, reduction dtype, hyperparameters), followed by `gathers`
+ * all-gathers of its compute-dtype shards -- shard_out for fp32 state, the
+ * parameter itself for bf16/fp16 state -- into its n_full buffers. No gather
+ * is fused. Validation (every unit as fsdp_reduce_scatter_step validates it,
+ * no buffer written by two units, nothing enqueued on error), scheduling
+ * over the side streams and errors as fsdp_step_units. */
+fsdp_status fsdp_step_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
+                               int gathers, uint32_t *nonfinite_count, void *stream);
 
 /* Human-readable name of a status. Never NULL. */
 const char *fsdp_status_string(fsdp_status status);

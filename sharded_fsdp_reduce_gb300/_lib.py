@@ -37,6 +37,7 @@ EXPORTS = (
     "fsdp_last_cuda_error",
     "fsdp_take_wait_timeouts",
     "fsdp_step_units",
+    "fsdp_step_units_ex",
 )
 
 
@@ -63,6 +64,14 @@ class FsdpUnit(ctypes.Structure):
                 ("exp_avg", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p), ("shard_out", ctypes.c_void_p),
                 ("padded_numel", ctypes.c_int64), ("world", ctypes.c_int32), ("grad_dtype", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("n_full", ctypes.c_int32)]
+
+
+class FsdpUnitEx(ctypes.Structure):
+    _fields_ = [("grads", ctypes.c_void_p), ("full_bufs", ctypes.c_void_p), ("param", ctypes.c_void_p),
+                ("state0", ctypes.c_void_p), ("state1", ctypes.c_void_p), ("shard_out", ctypes.c_void_p),
+                ("padded_numel", ctypes.c_int64), ("world", ctypes.c_int32), ("grad_dtype", ctypes.c_int32),
+                ("state_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32), ("n_full", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -97,6 +106,8 @@ def load() -> ctypes.CDLL:
             "fsdp_take_wait_timeouts": (i32, [ctypes.POINTER(ctypes.c_uint32)]),
             "fsdp_step_units": (i32, [ctypes.POINTER(FsdpUnit), i32, ctypes.POINTER(FsdpAdamwHparams), i32, i32,
                                       vp, vp]),
+            "fsdp_step_units_ex": (i32, [ctypes.POINTER(FsdpUnitEx), i32, ctypes.POINTER(FsdpStepConfig), i32,
+                                         vp, vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)

@@ -307,12 +307,98 @@ fsdp_status prepare_gather(const void *shard_out, fsdp_dtype dtype, int world, i
             if (overlaps(full_bufs[d], nbytes, full_bufs[e], nbytes)) return FSDP_ERR_INVALID_ARG;
         a.dst[d] = full_bufs[d];
     }
+    // the bulk-copy pipeline moves device memory only: host buffers are refused
+    if (host_resident(shard_out)) return FSDP_ERR_INVALID_ARG;
+    for (int d = 0; d < n_dst; ++d)
+        if (host_resident(full_bufs[d])) return FSDP_ERR_INVALID_ARG;
     return FSDP_OK;
+}
+
+// Validation of a variant step (fsdp_reduce_scatter_step and the variant
+// multi-unit step): fills the kernel's arguments, or sets `empty`.
+struct StepPlan {
+    StepArgs args;
+    fsdp_dtype grad_dtype, out_dtype, state_dtype;
+    int optimizer;
+    bool empty;
+};
+
+fsdp_status prepare_step(const void *const *grads, fsdp_dtype grad_dtype, int world, int64_t padded_numel,
+                         void *param, void *state0, void *state1, fsdp_dtype state_dtype, void *shard_out,
+                         fsdp_dtype out_dtype, const fsdp_step_config *cfg, int rank_begin, int rank_end,
+                         uint32_t *nonfinite_count, StepPlan &p) {
+    p.empty = false;
+    if (!dtype_valid(grad_dtype) || !dtype_valid(out_dtype) || !dtype_valid(state_dtype))
+        return FSDP_ERR_UNSUPPORTED_DTYPE;
+    if (world < 1 || world > FSDP_MAX_WORLD || !grads || !cfg) return FSDP_ERR_INVALID_ARG;
+    if (cfg->optimizer < FSDP_OPT_ADAMW || cfg->optimizer > FSDP_OPT_ADADELTA) return FSDP_ERR_INVALID_ARG;
+    if (cfg->reduce_dtype != FSDP_F32 && cfg->reduce_dtype != grad_dtype) return FSDP_ERR_UNSUPPORTED_DTYPE;
+    if (state_dtype != FSDP_F32 && out_dtype != state_dtype) return FSDP_ERR_UNSUPPORTED_DTYPE;
+    if (padded_numel < 0 || padded_numel % world != 0) return FSDP_ERR_INVALID_ARG;
+    if (rank_begin < 0 || rank_begin > rank_end || rank_end > world) return FSDP_ERR_INVALID_ARG;
+    if (cfg->step < 1 || !(cfg->grad_scale > 0.0f) || !isfinite(cfg->grad_scale)) return FSDP_ERR_INVALID_ARG;
+    if (mul_overflows(padded_numel, 4)) return FSDP_ERR_INVALID_ARG;
+    const int64_t S = padded_numel / world;
+    const int64_t begin = static_cast<int64_t>(rank_begin) * S, end = static_cast<int64_t>(rank_end) * S;
+    if (begin == end) {
+        p.empty = true;
+        return FSDP_OK;
+    }
+    const bool sgd = cfg->optimizer == FSDP_OPT_SGD;
+    if (sgd ? state1 != nullptr : state1 == nullptr) return FSDP_ERR_INVALID_ARG;
+    if (state_dtype == FSDP_F32 ? shard_out == nullptr : shard_out != nullptr) return FSDP_ERR_INVALID_ARG;
+    if (!param || !state0) return FSDP_ERR_INVALID_ARG;
+    const size_t gs = static_cast<size_t>(dtype_size(grad_dtype)), ss = static_cast<size_t>(dtype_size(state_dtype));
+    const size_t os = static_cast<size_t>(dtype_size(out_dtype));
+    if (!aligned(param, ss) || !aligned(state0, ss) || !aligned(state1, ss) || !aligned(shard_out, os))
+        return FSDP_ERR_ALIGNMENT;
+    if (nonfinite_count && !aligned(nonfinite_count, 4)) return FSDP_ERR_ALIGNMENT;
+    const void *written[4] = {param, state0, state1, shard_out};
+    const size_t wbytes[4] = {padded_numel * ss, padded_numel * ss, state1 ? padded_numel * ss : 0,
+                              shard_out ? padded_numel * os : 0};
+    for (int i = 0; i < 4; ++i)
+        for (int k = i + 1; k < 4; ++k)
+            if (overlaps(written[i], wbytes[i], written[k], wbytes[k])) return FSDP_ERR_INVALID_ARG;
+    StepArgs &a = p.args;
+    memset(&a, 0, sizeof(a));
+    for (int q = 0; q < world; ++q) {
+        if (!grads[q]) return FSDP_ERR_INVALID_ARG;
+        if (!aligned(grads[q], gs)) return FSDP_ERR_ALIGNMENT;
+        for (int i = 0; i < 4; ++i)
+            if (overlaps(grads[q], padded_numel * gs, written[i], wbytes[i])) return FSDP_ERR_INVALID_ARG;
+        a.grads[q] = grads[q];
+    }
+    a.param = param;
+    a.s0 = state0;
+    a.s1 = state1;
+    a.out = shard_out;
+    a.nonfinite = nonfinite_count;
+    a.begin = begin;
+    a.end = end;
+    a.k = make_step_scalars(*cfg, world);
+    a.world = world;
+    a.reduce_lowp = cfg->reduce_dtype != FSDP_F32 ? 1 : 0;
+    p.grad_dtype = grad_dtype;
+    p.out_dtype = out_dtype;
+    p.state_dtype = state_dtype;
+    p.optimizer = cfg->optimizer;
+    return FSDP_OK;
+}
+
+fsdp_status launch_step(const StepPlan &p, cudaStream_t s) {
+    switch (p.optimizer) {
+        case FSDP_OPT_ADAMW: return launch_step_adamw(p.args, p.grad_dtype, p.out_dtype, p.state_dtype, s);
+        case FSDP_OPT_SGD: return launch_step_sgd(p.args, p.grad_dtype, p.out_dtype, p.state_dtype, s);
+        case FSDP_OPT_ADAMAX: return launch_step_adamax(p.args, p.grad_dtype, p.out_dtype, p.state_dtype, s);
+        default: return launch_step_adadelta(p.args, p.grad_dtype, p.out_dtype, p.state_dtype, s);
+    }
 }
 
 // One unit of fsdp_step_units, validated and ready to launch.
 struct UnitPlan {
+    bool variant;   // the variant step (StepPlan) rather than the fused AdamW kernel
     RsaArgs rsa;
+    StepPlan step;
     GatherArgs gather;
     fsdp_dtype grad_dtype, out_dtype;
     bool empty;
@@ -372,9 +458,53 @@ fsdp_status side_streams(SideStreams *&out) {
 }
 
 fsdp_status launch_unit(const UnitPlan &p, cudaStream_t s) {
-    fsdp_status st = launch_rsa(p.rsa, p.grad_dtype, p.out_dtype, s);
+    fsdp_status st = p.variant ? launch_step(p.step, s) : launch_rsa(p.rsa, p.grad_dtype, p.out_dtype, s);
     for (int k = 0; st == FSDP_OK && k < p.separate_gathers; ++k) st = launch_gather(p.gather, s);
     return st;
+}
+
+void add_span(std::vector<Span> &spans, const void *p, uintptr_t bytes) {
+    if (p && bytes) spans.push_back({reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + bytes});
+}
+
+// Enqueue validated units: refuse overlapping written buffers (two units
+// sharing memory), then launch each unit's kernels in order, spread over
+// the side streams when there are two or more units with work.
+fsdp_status run_units(const std::vector<UnitPlan> &plan, std::vector<Span> &spans, cudaStream_t s) {
+    std::sort(spans.begin(), spans.end());
+    for (size_t i = 1; i < spans.size(); ++i)
+        if (spans[i].lo < spans[i - 1].hi) return FSDP_ERR_INVALID_ARG;
+    int busy = 0;
+    for (const UnitPlan &p : plan) busy += p.empty ? 0 : 1;
+    if (kUnitStreams < 2 || busy < 2) {
+        for (const UnitPlan &p : plan) {
+            if (p.empty) continue;
+            if (fsdp_status st = launch_unit(p, s); st != FSDP_OK) return st;
+        }
+        return FSDP_OK;
+    }
+    SideStreams *side = nullptr;
+    if (fsdp_status st = side_streams(side); st != FSDP_OK) return st;
+    const int ns = busy < kUnitStreams ? busy : kUnitStreams;
+    if (cudaError_t e = cudaEventRecord(side->fork, s); e != cudaSuccess) return cuda_status(e);
+    for (int i = 0; i < ns; ++i)
+        if (cudaError_t e = cudaStreamWaitEvent(side->s[i], side->fork, 0); e != cudaSuccess) return cuda_status(e);
+    fsdp_status result = FSDP_OK;
+    int k = 0;
+    for (const UnitPlan &p : plan) {
+        if (p.empty) continue;
+        result = launch_unit(p, side->s[k++ % ns]);
+        if (result != FSDP_OK) break;
+    }
+    // join every side stream back into the caller's stream, also after a
+    // failed launch, so that what was enqueued stays ordered before the
+    // caller's later work
+    for (int i = 0; i < ns; ++i) {
+        cudaError_t e = cudaEventRecord(side->done[i], side->s[i]);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, side->done[i], 0);
+        if (e != cudaSuccess && result == FSDP_OK) result = cuda_status(e);
+    }
+    return result;
 }
 
 }  // namespace
@@ -407,60 +537,11 @@ FSDP_API fsdp_status fsdp_reduce_scatter_step(const void *const *grads, fsdp_dty
                                      fsdp_dtype state_dtype, void *shard_out, fsdp_dtype out_dtype,
                                      const fsdp_step_config *cfg, int rank_begin, int rank_end,
                                      uint32_t *nonfinite_count, void *stream) {
-    if (!dtype_valid(grad_dtype) || !dtype_valid(out_dtype) || !dtype_valid(state_dtype))
-        return FSDP_ERR_UNSUPPORTED_DTYPE;
-    if (world < 1 || world > FSDP_MAX_WORLD || !grads || !cfg) return FSDP_ERR_INVALID_ARG;
-    if (cfg->optimizer < FSDP_OPT_ADAMW || cfg->optimizer > FSDP_OPT_ADADELTA) return FSDP_ERR_INVALID_ARG;
-    if (cfg->reduce_dtype != FSDP_F32 && cfg->reduce_dtype != grad_dtype) return FSDP_ERR_UNSUPPORTED_DTYPE;
-    if (state_dtype != FSDP_F32 && out_dtype != state_dtype) return FSDP_ERR_UNSUPPORTED_DTYPE;
-    if (padded_numel < 0 || padded_numel % world != 0) return FSDP_ERR_INVALID_ARG;
-    if (rank_begin < 0 || rank_begin > rank_end || rank_end > world) return FSDP_ERR_INVALID_ARG;
-    if (cfg->step < 1 || !(cfg->grad_scale > 0.0f) || !isfinite(cfg->grad_scale)) return FSDP_ERR_INVALID_ARG;
-    if (mul_overflows(padded_numel, 4)) return FSDP_ERR_INVALID_ARG;
-    const int64_t S = padded_numel / world;
-    const int64_t begin = static_cast<int64_t>(rank_begin) * S, end = static_cast<int64_t>(rank_end) * S;
-    if (begin == end) return FSDP_OK;
-    const bool sgd = cfg->optimizer == FSDP_OPT_SGD;
-    if (sgd ? state1 != nullptr : state1 == nullptr) return FSDP_ERR_INVALID_ARG;
-    if (state_dtype == FSDP_F32 ? shard_out == nullptr : shard_out != nullptr) return FSDP_ERR_INVALID_ARG;
-    if (!param || !state0) return FSDP_ERR_INVALID_ARG;
-    const size_t gs = static_cast<size_t>(dtype_size(grad_dtype)), ss = static_cast<size_t>(dtype_size(state_dtype));
-    const size_t os = static_cast<size_t>(dtype_size(out_dtype));
-    if (!aligned(param, ss) || !aligned(state0, ss) || !aligned(state1, ss) || !aligned(shard_out, os))
-        return FSDP_ERR_ALIGNMENT;
-    if (nonfinite_count && !aligned(nonfinite_count, 4)) return FSDP_ERR_ALIGNMENT;
-    const void *written[4] = {param, state0, state1, shard_out};
-    const size_t wbytes[4] = {padded_numel * ss, padded_numel * ss, state1 ? padded_numel * ss : 0,
-                              shard_out ? padded_numel * os : 0};
-    for (int i = 0; i < 4; ++i)
-        for (int k = i + 1; k < 4; ++k)
-            if (overlaps(written[i], wbytes[i], written[k], wbytes[k])) return FSDP_ERR_INVALID_ARG;
-    StepArgs a;
-    memset(&a, 0, sizeof(a));
-    for (int q = 0; q < world; ++q) {
-        if (!grads[q]) return FSDP_ERR_INVALID_ARG;
-        if (!aligned(grads[q], gs)) return FSDP_ERR_ALIGNMENT;
-        for (int i = 0; i < 4; ++i)
-            if (overlaps(grads[q], padded_numel * gs, written[i], wbytes[i])) return FSDP_ERR_INVALID_ARG;
-        a.grads[q] = grads[q];
-    }
-    a.param = param;
-    a.s0 = state0;
-    a.s1 = state1;
-    a.out = shard_out;
-    a.nonfinite = nonfinite_count;
-    a.begin = begin;
-    a.end = end;
-    a.k = make_step_scalars(*cfg, world);
-    a.world = world;
-    a.reduce_lowp = cfg->reduce_dtype != FSDP_F32 ? 1 : 0;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    switch (cfg->optimizer) {
-        case FSDP_OPT_ADAMW: return launch_step_adamw(a, grad_dtype, out_dtype, state_dtype, s);
-        case FSDP_OPT_SGD: return launch_step_sgd(a, grad_dtype, out_dtype, state_dtype, s);
-        case FSDP_OPT_ADAMAX: return launch_step_adamax(a, grad_dtype, out_dtype, state_dtype, s);
-        default: return launch_step_adadelta(a, grad_dtype, out_dtype, state_dtype, s);
-    }
+    StepPlan p;
+    const fsdp_status st = prepare_step(grads, grad_dtype, world, padded_numel, param, state0, state1, state_dtype,
+                                        shard_out, out_dtype, cfg, rank_begin, rank_end, nonfinite_count, p);
+    if (st != FSDP_OK || p.empty) return st;
+    return launch_step(p, static_cast<cudaStream_t>(stream));
 }
 
 FSDP_API fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world, int64_t padded_numel,
@@ -483,6 +564,7 @@ FSDP_API fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const 
     for (int u = 0; u < n_units; ++u) {
         const fsdp_unit &x = units[u];
         UnitPlan &p = plan[static_cast<size_t>(u)];
+        p.variant = false;
         if (!dtype_valid(x.grad_dtype) || !dtype_valid(x.out_dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
         p.grad_dtype = static_cast<fsdp_dtype>(x.grad_dtype);
         p.out_dtype = static_cast<fsdp_dtype>(x.out_dtype);
@@ -503,51 +585,59 @@ FSDP_API fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const 
         if (p.empty) continue;
         const uintptr_t sb = static_cast<uintptr_t>(x.padded_numel) * 4;
         const uintptr_t ob = static_cast<uintptr_t>(x.padded_numel) * static_cast<uintptr_t>(dtype_size(p.out_dtype));
-        const void *state[3] = {x.master, x.exp_avg, x.exp_avg_sq};
-        for (const void *b : state) spans.push_back({reinterpret_cast<uintptr_t>(b), reinterpret_cast<uintptr_t>(b) + sb});
-        spans.push_back({reinterpret_cast<uintptr_t>(x.shard_out), reinterpret_cast<uintptr_t>(x.shard_out) + ob});
+        add_span(spans, x.master, sb);
+        add_span(spans, x.exp_avg, sb);
+        add_span(spans, x.exp_avg_sq, sb);
+        add_span(spans, x.shard_out, ob);
         if (gathers > 0)
-            for (int d = 0; d < x.n_full; ++d)
-                spans.push_back({reinterpret_cast<uintptr_t>(x.full_bufs[d]),
-                                 reinterpret_cast<uintptr_t>(x.full_bufs[d]) + ob});
+            for (int d = 0; d < x.n_full; ++d) add_span(spans, x.full_bufs[d], ob);
     }
-    // no two written buffers overlap (within a unit that is already checked;
-    // this catches two units sharing memory)
-    std::sort(spans.begin(), spans.end());
-    for (size_t i = 1; i < spans.size(); ++i)
-        if (spans[i].lo < spans[i - 1].hi) return FSDP_ERR_INVALID_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int busy = 0;
-    for (const UnitPlan &p : plan) busy += p.empty ? 0 : 1;
-    if (kUnitStreams < 2 || busy < 2) {
-        for (const UnitPlan &p : plan) {
-            if (p.empty) continue;
-            if (fsdp_status st = launch_unit(p, s); st != FSDP_OK) return st;
+    return run_units(plan, spans, static_cast<cudaStream_t>(stream));
+}
+
+FSDP_API fsdp_status fsdp_step_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
+                                        int gathers, uint32_t *nonfinite_count, void *stream) {
+    if (n_units < 0 || (n_units > 0 && !units) || !cfg) return FSDP_ERR_INVALID_ARG;
+    if (gathers < 0 || gathers > FSDP_MAX_WORLD) return FSDP_ERR_INVALID_ARG;
+    std::vector<UnitPlan> plan(static_cast<size_t>(n_units));
+    std::vector<Span> spans;
+    for (int u = 0; u < n_units; ++u) {
+        const fsdp_unit_ex &x = units[u];
+        UnitPlan &p = plan[static_cast<size_t>(u)];
+        p.variant = true;
+        if (!dtype_valid(x.grad_dtype) || !dtype_valid(x.out_dtype) || !dtype_valid(x.state_dtype))
+            return FSDP_ERR_UNSUPPORTED_DTYPE;
+        const fsdp_dtype gd = static_cast<fsdp_dtype>(x.grad_dtype), od = static_cast<fsdp_dtype>(x.out_dtype);
+        const fsdp_dtype sd = static_cast<fsdp_dtype>(x.state_dtype);
+        p.grad_dtype = gd;
+        p.out_dtype = od;
+        if (x.n_full < 0 || x.n_full > FSDP_MAX_WORLD || (x.n_full > 0 && !x.full_bufs)) return FSDP_ERR_INVALID_ARG;
+        if (gathers > 0 && x.n_full < 1) return FSDP_ERR_INVALID_ARG;
+        fsdp_status st = prepare_step(x.grads, gd, x.world, x.padded_numel, x.param, x.state0, x.state1, sd,
+                                      x.shard_out, od, cfg, 0, x.world, nonfinite_count, p.step);
+        if (st != FSDP_OK) return st;
+        p.empty = p.step.empty;
+        p.separate_gathers = p.empty ? 0 : gathers;
+        // the gathered shards: shard_out, or the parameter itself when the
+        // state is bf16/fp16 (then it is the compute-dtype shard)
+        const void *shard = sd == FSDP_F32 ? x.shard_out : x.param;
+        if (p.separate_gathers > 0) {
+            bool gempty = false;
+            st = prepare_gather(shard, od, x.world, x.padded_numel, x.full_bufs, x.n_full, p.gather, gempty);
+            if (st != FSDP_OK) return st;
         }
-        return FSDP_OK;
-    }
-    SideStreams *side = nullptr;
-    if (fsdp_status st = side_streams(side); st != FSDP_OK) return st;
-    const int ns = busy < kUnitStreams ? busy : kUnitStreams;
-    if (cudaError_t e = cudaEventRecord(side->fork, s); e != cudaSuccess) return cuda_status(e);
-    for (int i = 0; i < ns; ++i)
-        if (cudaError_t e = cudaStreamWaitEvent(side->s[i], side->fork, 0); e != cudaSuccess) return cuda_status(e);
-    fsdp_status result = FSDP_OK;
-    int k = 0;
-    for (const UnitPlan &p : plan) {
         if (p.empty) continue;
-        result = launch_unit(p, side->s[k++ % ns]);
-        if (result != FSDP_OK) break;
+        const uintptr_t P = static_cast<uintptr_t>(x.padded_numel);
+        const uintptr_t sb = P * static_cast<uintptr_t>(dtype_size(sd));
+        const uintptr_t ob = P * static_cast<uintptr_t>(dtype_size(od));
+        add_span(spans, x.param, sb);
+        add_span(spans, x.state0, sb);
+        add_span(spans, x.state1, sb);
+        add_span(spans, x.shard_out, ob);
+        if (gathers > 0)
+            for (int d = 0; d < x.n_full; ++d) add_span(spans, x.full_bufs[d], ob);
     }
-    // join every side stream back into the caller's stream, also after a
-    // failed launch, so that what was enqueued stays ordered before the
-    // caller's later work
-    for (int i = 0; i < ns; ++i) {
-        cudaError_t e = cudaEventRecord(side->done[i], side->s[i]);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, side->done[i], 0);
-        if (e != cudaSuccess && result == FSDP_OK) result = cuda_status(e);
-    }
-    return result;
+    return run_units(plan, spans, static_cast<cudaStream_t>(stream));
 }
 
 FSDP_API const char *fsdp_status_string(fsdp_status status) {

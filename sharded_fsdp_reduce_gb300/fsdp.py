@@ -12,7 +12,7 @@ from typing import List, Optional, Sequence, Tuple
 import torch
 
 from . import _lib
-from ._lib import FsdpAdamwHparams, FsdpStepConfig, FsdpUnit, FsdpView
+from ._lib import FsdpAdamwHparams, FsdpStepConfig, FsdpUnit, FsdpUnitEx, FsdpView
 
 __all__ = [
     "AdamWHParams", "StepConfig", "OPTIMIZERS", "FsdpError", "View", "fsdp_reduce_scatter_step",
@@ -20,7 +20,7 @@ __all__ = [
     "fsdp_reduce_scatter_adam_cast", "fsdp_reduce_scatter_adam_cast_gather", "fsdp_all_gather",
     "fsdp_status_string",
     "fsdp_last_cuda_error", "fsdp_take_wait_timeouts", "dtype_code",
-    "UnitDescs", "fsdp_step_units",
+    "UnitDescs", "fsdp_step_units", "fsdp_step_units_ex",
 ]
 
 _DTYPES = {torch.float32: _lib.FSDP_F32, torch.bfloat16: _lib.FSDP_BF16, torch.float16: _lib.FSDP_F16}
@@ -315,43 +315,57 @@ def fsdp_all_gather(shard_out: torch.Tensor, full_bufs: Sequence[torch.Tensor], 
 
 
 class UnitDescs:
-    """The C descriptors (fsdp_unit) of a sequence of FSDP units, built once
-    for fsdp_step_units. A unit is any object holding FlatParamUnit's
-    buffers: grads (N tensors), full (gathered buffers), master, exp_avg,
-    exp_avg_sq, shard_out, world. The descriptors hold the buffers' addresses:
-    build new ones if a unit's buffers are replaced. The units are kept alive
-    while the descriptors exist."""
+    """The C descriptors of a sequence of FSDP units, built once for
+    fsdp_step_units (fsdp_unit: fp32 master and AdamW state, built when every
+    unit has them) and fsdp_step_units_ex (fsdp_unit_ex: any unit). A unit is
+    any object holding FlatParamUnit's buffers: grads (N tensors), full
+    (gathered buffers), master (the parameter), exp_avg and exp_avg_sq (the
+    optimizer states; exp_avg_sq None for SGD), shard_out (for fp32 state;
+    the parameter itself for bf16/fp16 state). The descriptors hold the
+    buffers' addresses: build new ones if a unit's buffers are replaced. The
+    units are kept alive while the descriptors exist."""
 
     def __init__(self, units: Sequence):
         self.units = list(units)
         self.n = len(self.units)
-        self.array = (FsdpUnit * max(self.n, 1))()
+        self.array_ex = (FsdpUnitEx * max(self.n, 1))()
+        self.adamw = all(u.master.dtype == torch.float32 and u.exp_avg_sq is not None for u in self.units)
+        self.array = (FsdpUnit * max(self.n, 1))() if self.adamw else None
         self._keep = []
         for k, u in enumerate(self.units):
+            pre = f"units[{k}]."
             P = u.master.numel()
-            gdt = _grad_dtype(u.grads, P, f"units[{k}].grads")
-            _check_fp32_state(P, f"units[{k}].", master=u.master, exp_avg=u.exp_avg, exp_avg_sq=u.exp_avg_sq)
-            odt = u.shard_out.dtype
-            if u.shard_out.numel() != P:
-                raise ValueError(f"units[{k}].shard_out must hold {P} elements")
+            gdt = _grad_dtype(u.grads, P, pre + "grads")
+            sdt = u.master.dtype
+            for name in ("exp_avg", "exp_avg_sq"):
+                t = getattr(u, name)
+                if t is not None and (t.dtype != sdt or t.numel() != P):
+                    raise ValueError(f"{pre}{name} must hold {P} elements of {sdt}")
+            lowp = sdt != torch.float32
+            odt = sdt if lowp else u.shard_out.dtype
+            if not lowp and u.shard_out.numel() != P:
+                raise ValueError(f"{pre}shard_out must hold {P} elements")
             for i, f in enumerate(u.full):
                 if f.numel() != P or f.dtype != odt:
-                    raise ValueError(f"units[{k}].full[{i}] must hold {P} elements of {odt}")
-            grads = _ptrs(u.grads, f"units[{k}].grads", host_ok=True)
-            full = _ptrs(u.full, f"units[{k}].full") if u.full else None
+                    raise ValueError(f"{pre}full[{i}] must hold {P} elements of {odt}")
+            grads = _ptrs(u.grads, pre + "grads", host_ok=True)
+            full = _ptrs(u.full, pre + "full") if u.full else None
             self._keep += [grads, full]
-            d = self.array[k]
-            d.grads = ctypes.addressof(grads)
-            d.full_bufs = ctypes.addressof(full) if full is not None else None
-            d.master = _mem(u.master, f"units[{k}].master")
-            d.exp_avg = _mem(u.exp_avg, f"units[{k}].exp_avg")
-            d.exp_avg_sq = _mem(u.exp_avg_sq, f"units[{k}].exp_avg_sq")
-            d.shard_out = _dev(u.shard_out, f"units[{k}].shard_out")
-            d.padded_numel = P
-            d.world = len(u.grads)
-            d.grad_dtype = dtype_code(gdt)
-            d.out_dtype = dtype_code(odt)
-            d.n_full = len(u.full)
+            param = _mem(u.master, pre + "master")
+            s0 = _mem(u.exp_avg, pre + "exp_avg")
+            s1 = _mem(u.exp_avg_sq, pre + "exp_avg_sq") if u.exp_avg_sq is not None else None
+            out = None if lowp else _dev(u.shard_out, pre + "shard_out")
+            e = self.array_ex[k]
+            e.grads, e.full_bufs = ctypes.addressof(grads), ctypes.addressof(full) if full is not None else None
+            e.param, e.state0, e.state1, e.shard_out = param, s0, s1, out
+            e.padded_numel, e.world, e.n_full = P, len(u.grads), len(u.full)
+            e.grad_dtype, e.state_dtype, e.out_dtype = dtype_code(gdt), dtype_code(sdt), dtype_code(odt)
+            if self.adamw:
+                d = self.array[k]
+                d.grads, d.full_bufs = e.grads, e.full_bufs
+                d.master, d.exp_avg, d.exp_avg_sq, d.shard_out = param, s0, s1, out
+                d.padded_numel, d.world, d.n_full = P, len(u.grads), len(u.full)
+                d.grad_dtype, d.out_dtype = dtype_code(gdt), dtype_code(odt)
 
 
 def fsdp_step_units(units, hparams: AdamWHParams, gathers: int = 1, fuse_first_gather: bool = False,
@@ -363,7 +377,22 @@ def fsdp_step_units(units, hparams: AdamWHParams, gathers: int = 1, fuse_first_g
     fuse_first_gather). `units` is a UnitDescs or a sequence of units (then
     descriptors are built for this call)."""
     descs = units if isinstance(units, UnitDescs) else UnitDescs(units)
+    if not descs.adamw:
+        raise ValueError("fsdp_step_units needs fp32 master and AdamW state in every unit; use fsdp_step_units_ex")
     nf = _counter(nonfinite_count)
     hp = hparams.to_c()
     _check(_lib.load().fsdp_step_units(descs.array, descs.n, ctypes.byref(hp), int(gathers),
                                        1 if fuse_first_gather else 0, nf, _stream(stream)), "fsdp_step_units")
+
+
+def fsdp_step_units_ex(units, config: StepConfig, gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None) -> None:
+    """The variant step of a whole model in one call: for each unit in order,
+    fsdp_reduce_scatter_step's update under `config`, then `gathers`
+    all-gathers of its compute-dtype shards into its full buffers. `units` is
+    a UnitDescs or a sequence of units."""
+    descs = units if isinstance(units, UnitDescs) else UnitDescs(units)
+    nf = _counter(nonfinite_count)
+    cfg = config.to_c()
+    _check(_lib.load().fsdp_step_units_ex(descs.array_ex, descs.n, ctypes.byref(cfg), int(gathers), nf,
+                                          _stream(stream)), "fsdp_step_units_ex")

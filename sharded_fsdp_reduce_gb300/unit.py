@@ -8,6 +8,14 @@ the compute dtype). Shared by all ranks, as the concatenation of their shards:
 the fp32 master weights, exp_avg (m), exp_avg_sq (v) and the compute-dtype
 shards (shard_out); rank r's shard is [r*S, (r+1)*S).
 
+Optimizers and precisions: AdamW with fp32 master and state (the fused
+kernel, optionally with the first gather fused in) by default; with
+optimizer "sgd", "adamax" or "adadelta", or state_dtype bf16/fp16, the unit
+holds that optimizer's state (one buffer for SGD, two otherwise) in that
+dtype and steps through the variant kernel (fsdp_reduce_scatter_step). With
+bf16/fp16 state there is no fp32 master: the parameter buffer is the rank's
+compute-dtype shard and shard_out is that same buffer.
+
 Offload mode (state_on_host=True): master, exp_avg and exp_avg_sq live in
 pinned host memory instead of HBM ("FSDP (Fully Sharded Data Parallel)", "CPU
 Offloading"; "fairseq ... FSDP 实战指南", --cpu-offload keeps the optimizer
@@ -29,14 +37,16 @@ from typing import Dict, List, Optional, Sequence, Tuple
 
 import torch
 
-from .fsdp import (AdamWHParams, UnitDescs, View, fsdp_all_gather, fsdp_flatten_pad, fsdp_reduce_scatter_adam_cast,
-                   fsdp_reduce_scatter_adam_cast_gather, fsdp_step_units, fsdp_unflatten_views)
+from .fsdp import (OPTIMIZERS, AdamWHParams, StepConfig, UnitDescs, View, fsdp_all_gather, fsdp_flatten_pad,
+                   fsdp_reduce_scatter_adam_cast, fsdp_reduce_scatter_adam_cast_gather, fsdp_reduce_scatter_step,
+                   fsdp_step_units, fsdp_step_units_ex, fsdp_unflatten_views)
 
 
 class FlatParamUnit:
     def __init__(self, params: Sequence[Tuple[str, Tuple[int, ...]]], world: int, grad_dtype: torch.dtype,
                  out_dtype: torch.dtype, device="cuda", n_full: Optional[int] = None,
-                 state_on_host: bool = False):
+                 state_on_host: bool = False, optimizer: str = "adamw",
+                 state_dtype: torch.dtype = torch.float32):
         self.names = [n for n, _ in params]
         self.shapes = [tuple(s) for _, s in params]
         self.world = int(world)
@@ -46,13 +56,26 @@ class FlatParamUnit:
         self.device = torch.device(device)
         P = self.padded_numel
         self.grads = [torch.zeros(P, dtype=grad_dtype, device=self.device) for _ in range(self.world)]
+        if optimizer not in OPTIMIZERS:
+            raise ValueError(f"optimizer must be one of {sorted(OPTIMIZERS)}")
+        self.optimizer = optimizer
+        self.state_dtype = state_dtype
+        lowp = state_dtype != torch.float32
+        if lowp and out_dtype != state_dtype:
+            raise ValueError("with bf16/fp16 state the compute dtype is the state dtype (the parameter is the shard)")
+        if lowp and state_on_host:
+            raise ValueError("a bf16/fp16 parameter is the gathered shard and stays in HBM: no offload")
         self.state_on_host = bool(state_on_host)
-        if self.state_on_host:
-            state = [torch.zeros(P, dtype=torch.float32, pin_memory=True) for _ in range(3)]
-        else:
-            state = [torch.zeros(P, dtype=torch.float32, device=self.device) for _ in range(3)]
-        self.master, self.exp_avg, self.exp_avg_sq = state
-        self.shard_out = torch.zeros(P, dtype=out_dtype, device=self.device)
+
+        def state_buf():
+            if self.state_on_host:
+                return torch.zeros(P, dtype=state_dtype, pin_memory=True)
+            return torch.zeros(P, dtype=state_dtype, device=self.device)
+
+        self.master = state_buf()
+        self.exp_avg = state_buf()
+        self.exp_avg_sq = None if optimizer == "sgd" else state_buf()
+        self.shard_out = self.master if lowp else torch.zeros(P, dtype=out_dtype, device=self.device)
         nf = self.world if n_full is None else int(n_full)
         self.full = [torch.zeros(P, dtype=out_dtype, device=self.device) for _ in range(nf)]
         self._host = None
@@ -60,8 +83,9 @@ class FlatParamUnit:
     # ---------------------------------------------------------------- set-up
 
     def load_master(self, tensors: Sequence[torch.Tensor], stream=None) -> None:
-        """Flatten the unit's initial fp32 parameters into the master buffer."""
-        if not self.state_on_host:
+        """Flatten the unit's initial parameters into the master buffer (the
+        parameter buffer, rounded to nearest even for bf16/fp16 state)."""
+        if not self.state_on_host and all(t.dtype == self.master.dtype for t in tensors):
             fsdp_flatten_pad(list(tensors), self.world, out=self.master, stream=stream)
             return
         flat, _ = fsdp_flatten_pad(list(tensors), self.world, stream=stream)
@@ -80,10 +104,38 @@ class FlatParamUnit:
 
     # ---------------------------------------------------------------- the step
 
-    def reduce_scatter_adam_cast(self, hp: AdamWHParams, rank_begin: int = 0, rank_end: Optional[int] = None,
+    @property
+    def variant(self) -> bool:
+        """Whether the unit steps through the variant kernel (another
+        optimizer or bf16/fp16 state) rather than the fused AdamW kernel."""
+        return self.optimizer != "adamw" or self.state_dtype != torch.float32
+
+    def step_config(self, hp) -> StepConfig:
+        """The variant step's configuration for hp (a StepConfig naming this
+        unit's optimizer, or AdamWHParams for an AdamW unit)."""
+        if isinstance(hp, StepConfig):
+            if hp.optimizer != self.optimizer:
+                raise ValueError(f"this unit's optimizer is {self.optimizer}, not {hp.optimizer}")
+            return hp
+        if self.optimizer != "adamw":
+            raise ValueError(f"a {self.optimizer} unit steps with a StepConfig")
+        return StepConfig("adamw", hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.step, hp.grad_scale)
+
+    def reduce_scatter_adam_cast(self, hp, rank_begin: int = 0, rank_end: Optional[int] = None,
                                  nonfinite_count: Optional[torch.Tensor] = None, stream=None) -> None:
-        fsdp_reduce_scatter_adam_cast(self.grads, self.master, self.exp_avg, self.exp_avg_sq, self.shard_out,
-                                      hp, rank_begin, rank_end, nonfinite_count, stream)
+        """The unit's update: the fused AdamW kernel for AdamWHParams on fp32
+        state, else the variant kernel."""
+        self._update(self.grads, hp, rank_begin, rank_end, nonfinite_count, stream)
+
+    def _update(self, grads, hp, rank_begin=0, rank_end=None, nonfinite_count=None, stream=None) -> None:
+        if isinstance(hp, AdamWHParams) and not self.variant:
+            fsdp_reduce_scatter_adam_cast(grads, self.master, self.exp_avg, self.exp_avg_sq, self.shard_out,
+                                          hp, rank_begin, rank_end, nonfinite_count, stream)
+            return
+        lowp = self.state_dtype != torch.float32
+        fsdp_reduce_scatter_step(grads, self.master, self.exp_avg, self.exp_avg_sq,
+                                 None if lowp else self.shard_out, self.step_config(hp), rank_begin, rank_end,
+                                 nonfinite_count, stream)
 
     def all_gather(self, stream=None) -> None:
         fsdp_all_gather(self.shard_out, self.full, self.world, stream)
@@ -94,7 +146,10 @@ class FlatParamUnit:
 
         gathers=2 is reshard-after-forward (gathered before forward and again
         before backward), gathers=1 the no-reshard mode. With fuse_gather the
-        first gather is written by the update kernel itself."""
+        first gather is written by the update kernel itself (the fused AdamW
+        kernel only). hp: AdamWHParams, or a StepConfig for the variant step."""
+        if fuse_gather and gathers >= 1 and (self.variant or not isinstance(hp, AdamWHParams)):
+            raise ValueError("fuse_gather needs the fused AdamW kernel (fp32 state, AdamWHParams)")
         if fuse_gather and gathers >= 1:
             fsdp_reduce_scatter_adam_cast_gather(self.grads, self.master, self.exp_avg, self.exp_avg_sq,
                                                  self.shard_out, self.full, hp, nonfinite_count=nonfinite_count,
@@ -134,15 +189,18 @@ class FlatParamUnit:
         if self.device.type == "cuda":
             torch.cuda.current_stream(self.device).synchronize()
         return {name: getattr(self, name)[lo:hi].detach().to("cpu", copy=True)
-                for name in ("master", "exp_avg", "exp_avg_sq")}
+                for name in ("master", "exp_avg", "exp_avg_sq") if getattr(self, name) is not None}
 
     def load_state_dict(self, state: Dict[str, torch.Tensor], rank: Optional[int] = None) -> None:
         """Restore what state_dict(rank) returned (rank=None: the whole unit)."""
         lo, hi = self._range(rank)
-        for name in ("master", "exp_avg", "exp_avg_sq"):
+        names = [n for n in ("master", "exp_avg", "exp_avg_sq") if getattr(self, n) is not None]
+        if sorted(state) != sorted(names):
+            raise ValueError(f"state must hold exactly {names}")
+        for name in names:
             src = state[name]
-            if src.dtype != torch.float32 or src.numel() != hi - lo:
-                raise ValueError(f"{name} must be float32 with {hi - lo} elements")
+            if src.dtype != self.state_dtype or src.numel() != hi - lo:
+                raise ValueError(f"{name} must be {self.state_dtype} with {hi - lo} elements")
             getattr(self, name)[lo:hi].copy_(src.reshape(-1))
 
     def _range(self, rank: Optional[int]) -> Tuple[int, int]:
@@ -154,11 +212,15 @@ class FlatParamUnit:
         return int(rank) * S, (int(rank) + 1) * S
 
     def step_bytes(self, gathers: int = 1) -> Tuple[int, int]:
-        """Algorithmic bytes of one step: (fused kernel, all-gathers)."""
+        """Algorithmic bytes of one step: (update kernel, all-gathers). The
+        update reads N gradients, reads and writes the parameter and each
+        state, and writes the compute-dtype shard when the state is fp32."""
         gs = self.grads[0].element_size()
+        ss = self.master.element_size()
         os_ = self.shard_out.element_size()
         P = self.padded_numel
-        rsa = P * (self.world * gs + 3 * (4 + 4) + os_)
+        nbuf = 2 if self.exp_avg_sq is None else 3
+        rsa = P * (self.world * gs + nbuf * 2 * ss + (0 if self.state_dtype != torch.float32 else os_))
         ag = gathers * P * os_ * (1 + len(self.full))
         return rsa, ag
 
@@ -194,8 +256,7 @@ class _HostPipeline:
             compute.wait_event(self.out_read)   # shard_out / the counter are about to be rewritten
         if host_nonfinite is not None:
             nonfinite_count.zero_()
-        fsdp_reduce_scatter_adam_cast(gset, u.master, u.exp_avg, u.exp_avg_sq, u.shard_out, hp,
-                                      nonfinite_count=nonfinite_count, stream=compute)
+        u._update(gset, hp, nonfinite_count=nonfinite_count, stream=compute)
         self.read_done[k] = compute.record_event()
         self.copy_out.wait_event(self.read_done[k])
         with torch.cuda.stream(self.copy_out):
@@ -219,9 +280,20 @@ class UnitSequence:
         self.units = list(units)
         self.descs = UnitDescs(self.units)
 
-    def step(self, hp: AdamWHParams, gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None,
+    def step(self, hp, gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None,
              stream=None, fuse_gather: bool = False) -> None:
-        fsdp_step_units(self.descs, hp, gathers, fuse_gather, nonfinite_count, stream)
+        """hp: AdamWHParams (every unit AdamW; the fused kernel where the state
+        is fp32) or a StepConfig (the variant kernel in every unit)."""
+        if isinstance(hp, AdamWHParams) and all(not u.variant for u in self.units):
+            fsdp_step_units(self.descs, hp, gathers, fuse_gather, nonfinite_count, stream)
+            return
+        if fuse_gather:
+            raise ValueError("fuse_gather needs the fused AdamW kernel in every unit")
+        cfg = hp if isinstance(hp, StepConfig) else StepConfig(
+            "adamw", hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.step, hp.grad_scale)
+        for u in self.units:
+            u.step_config(cfg)  # every unit takes this optimizer
+        fsdp_step_units_ex(self.descs, cfg, gathers, nonfinite_count, stream)
 
     def step_bytes(self, gathers: int = 1) -> Tuple[int, int]:
         """Algorithmic bytes of one model step: (fused kernels, all-gathers)."""

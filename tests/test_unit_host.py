@@ -56,3 +56,44 @@ def test_state_dict_rejects_bad_input(F):
     bad["exp_avg"] = bad["exp_avg"].double()
     with pytest.raises(ValueError):
         u.load_state_dict(bad)
+
+
+def test_variant_units_layout_and_bytes(F):
+    # fp32 AdamW: N*2 + 3*(4+4) + 2 bytes per element (42 at N=8)
+    u = F.FlatParamUnit([("w", (16,))], 8, torch.bfloat16, torch.bfloat16, device="cpu")
+    assert not u.variant and u.step_bytes(2) == (16 * 42, 2 * 16 * 2 * 9)
+    # SGD keeps one state buffer: 16 + 2*(4+4) + 2 = 34 bytes per element
+    s = F.FlatParamUnit([("w", (16,))], 8, torch.bfloat16, torch.bfloat16, device="cpu", optimizer="sgd")
+    assert s.variant and s.exp_avg_sq is None and s.step_bytes(1)[0] == 16 * 34
+    # bf16 parameter + state: no fp32 master, the parameter is the shard; 16 + 3*(2+2) = 28
+    b = F.FlatParamUnit([("w", (16,))], 8, torch.bfloat16, torch.bfloat16, device="cpu",
+                        state_dtype=torch.bfloat16)
+    assert b.variant and b.shard_out is b.master and b.master.dtype == torch.bfloat16
+    assert b.step_bytes(1)[0] == 16 * 28
+    assert set(b.state_dict()) == {"master", "exp_avg", "exp_avg_sq"}
+    assert set(s.state_dict()) == {"master", "exp_avg"}
+    # configurations the kernels do not take
+    with pytest.raises(ValueError):
+        F.FlatParamUnit([("w", (16,))], 8, torch.bfloat16, torch.float16, device="cpu", state_dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        F.FlatParamUnit([("w", (16,))], 8, torch.bfloat16, torch.bfloat16, device="cpu", optimizer="lamb")
+    with pytest.raises(ValueError):
+        F.FlatParamUnit([("w", (16,))], 8, torch.bfloat16, torch.bfloat16, device="cpu",
+                        state_dtype=torch.bfloat16, state_on_host=True)
+    with pytest.raises(ValueError):  # the state dict must match the unit's state buffers and dtype
+        b.load_state_dict(u.state_dict())
+    with pytest.raises(ValueError):
+        s.load_state_dict(u.state_dict())
+
+
+def test_step_config_matches_the_unit(F):
+    s = F.FlatParamUnit([("w", (16,))], 8, torch.bfloat16, torch.bfloat16, device="cpu", optimizer="adamax")
+    with pytest.raises(ValueError):
+        s.step_config(F.StepConfig("sgd", 1e-3))
+    with pytest.raises(ValueError):
+        s.step_config(F.AdamWHParams(1e-3))               # an Adamax unit steps with a StepConfig
+    a = F.FlatParamUnit([("w", (16,))], 8, torch.bfloat16, torch.bfloat16, device="cpu",
+                        state_dtype=torch.bfloat16)
+    cfg = a.step_config(F.AdamWHParams(2e-3, 0.8, 0.99, 1e-6, 0.1, 3, 4.0))
+    assert (cfg.optimizer, cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay, cfg.step, cfg.grad_scale) == \
+        ("adamw", 2e-3, 0.8, 0.99, 1e-6, 0.1, 3, 4.0)
