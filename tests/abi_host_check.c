@@ -75,6 +75,24 @@ int main(void) {
     CHECK(fsdp_step_units(&u, 1, &hp, 1, 1, NULL, NULL) == FSDP_ERR_INVALID_ARG);
     u.padded_numel = 0; /* an empty unit is skipped */
     CHECK(fsdp_step_units(&u, 1, &hp, 1, 1, NULL, NULL) == FSDP_OK);
+    /* the variant multi-unit step: SGD takes one state */
+    fsdp_unit_ex v;
+    memset(&v, 0, sizeof(v));
+    v.grads = grads;
+    v.full_bufs = fulls;
+    v.param = (void *)0x1000000;
+    v.state0 = (void *)0x2000000;
+    v.state1 = (void *)0x3000000;
+    v.shard_out = (void *)0x4000000;
+    v.padded_numel = 16;
+    v.world = 2;
+    v.grad_dtype = FSDP_BF16;
+    v.state_dtype = FSDP_F32;
+    v.out_dtype = FSDP_BF16;
+    v.n_full = 2;
+    CHECK(fsdp_step_units_ex(&v, 1, &cfg, 1, NULL, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_step_units_ex(NULL, 0, &cfg, 1, NULL, NULL) == FSDP_OK);
+    CHECK(fsdp_step_units_ex(&v, 1, NULL, 1, NULL, NULL) == FSDP_ERR_INVALID_ARG);
     CHECK(fsdp_take_wait_timeouts(NULL) == FSDP_ERR_INVALID_ARG);
     CHECK(fsdp_last_cuda_error() == 0);
     printf("ok\n");

@@ -328,3 +328,41 @@ def test_step_units_validates_every_unit_before_launching(lib):
     assert call([unit(A, n_full=0), unit(B, n_full=0)], gathers=1, fuse=1) == E.FSDP_ERR_INVALID_ARG
     assert call([unit(A, P=0), unit(B, P=0)]) == E.FSDP_OK                     # empty units: nothing to launch
     assert lib.fsdp_last_cuda_error() == 0
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host-only: needs a machine without a GPU")
+def test_step_units_ex_validates_every_unit_before_launching(lib):
+    from sharded_fsdp_reduce_gb300 import _lib as E
+    keep = []
+
+    def unit(base, world=2, P=16, n_full=2, sdt=0, odt=1, opt_states=2, out=True):
+        arr = lambda *p: (ctypes.c_void_p * len(p))(*p)
+        g = arr(*[base + 0x100000 * (q + 1) for q in range(world)])
+        f = arr(*[base + 0x1000000 * (8 + d) for d in range(n_full)]) if n_full else None
+        keep.append((g, f))
+        u = E.FsdpUnitEx()
+        u.grads, u.full_bufs = ctypes.addressof(g), (ctypes.addressof(f) if f is not None else None)
+        u.param, u.state0 = base + 0x1000000, base + 0x2000000
+        u.state1 = base + 0x3000000 if opt_states == 2 else None
+        u.shard_out = base + 0x4000000 if out else None
+        u.padded_numel, u.world, u.n_full = P, world, n_full
+        u.grad_dtype, u.state_dtype, u.out_dtype = 1, sdt, odt
+        return u
+
+    def call(units, opt=0, gathers=1):
+        cfg = E.FsdpStepConfig(opt, 0, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+        arr = (E.FsdpUnitEx * max(len(units), 1))(*units)
+        return lib.fsdp_step_units_ex(arr, len(units), ctypes.byref(cfg), gathers, None, None)
+
+    A, B = FAKE, FAKE + 0x100000000
+    assert call([]) == E.FSDP_OK
+    assert call([unit(A), unit(B, sdt=7)]) == E.FSDP_ERR_UNSUPPORTED_DTYPE
+    assert call([unit(A), unit(B)], opt=1) == E.FSDP_ERR_INVALID_ARG          # SGD with a second state
+    assert call([unit(A, opt_states=1), unit(B, opt_states=1)], opt=2) == E.FSDP_ERR_INVALID_ARG  # Adamax without
+    assert call([unit(A), unit(B, sdt=1, odt=1)]) == E.FSDP_ERR_INVALID_ARG   # bf16 state with a shard_out
+    assert call([unit(A), unit(B, n_full=0)]) == E.FSDP_ERR_INVALID_ARG       # gathers without buffers
+    bad = unit(B)
+    bad.state0 = A + 0x2000000                                                 # unit 0's first state
+    assert call([unit(A), bad]) == E.FSDP_ERR_INVALID_ARG
+    assert call([unit(A, P=0), unit(B, P=0)]) == E.FSDP_OK                     # empty units: nothing to launch
+    assert lib.fsdp_last_cuda_error() == 0
