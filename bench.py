@@ -17,7 +17,12 @@ Printed (rank 0, one JSON line): value = algorithmic bytes of the step / step
 time (GB/s, whole job over all ranks); roofline of the fused kernel (its own
 CUDA-event time inside the timed region); e2e through the Python binding with
 pinned host buffers; the CPU oracle timed on the host cores; clocks sampled
-during the timed region.
+during the timed region. Beside them, on the same unit: the fused-gather and
+no-reshard steps (`variants`), the variant optimizers' kernels
+(`variant_kernels`), the fused kernel with its state in pinned host memory
+(`offload_state_on_host`), and the per-unit driver on a 12-unit GPT-2 small
+model (`driver_gpt2_small_model_12_units`); --no-variants, --no-offload and
+--no-driver skip them.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
