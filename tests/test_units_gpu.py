@@ -230,3 +230,30 @@ def test_units_from_concurrent_host_threads(F):
                 assert same(x, y)
             for fa, fb in zip(ua.full, ub.full):
                 assert same(fa, fb)
+
+
+def test_model_step_captured_in_a_cuda_graph(F):
+    # the native driver's launches, side streams and fork/join events inside
+    # a CUDA graph: replaying the captured step equals running it eagerly.
+    # The step's scalars are the kernels' by-value arguments, so a graph
+    # replays the step it captured (here step 2 from the same state).
+    a = [u for u in build_model(F, 12) if u.grads[0].dtype != torch.float16]
+    b = [u for u in build_model(F, 12) if u.grads[0].dtype != torch.float16]
+    seq_a, seq_b = F.UnitSequence(a), F.UnitSequence(b)
+    load_grads(a, 1, 13)
+    load_grads(b, 1, 13)
+    seq_a.step(hp_for(F, a[0], 1), gathers=2)  # eager step 1 (also warms every launch cache)
+    seq_b.step(hp_for(F, b[0], 1), gathers=2)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        seq_a.step(hp_for(F, a[0], 2), gathers=2, fuse_gather=True)
+    graph.replay()
+    seq_b.step(hp_for(F, b[0], 2), gathers=2, fuse_gather=True)
+    torch.cuda.synchronize()
+    for ua, ub in zip(a, b):
+        for x, y in ((ua.master, ub.master), (ua.exp_avg, ub.exp_avg), (ua.exp_avg_sq, ub.exp_avg_sq),
+                     (ua.shard_out, ub.shard_out)):
+            assert same(x, y)
+        for fa, fb in zip(ua.full, ub.full):
+            assert same(fa, fb)
