@@ -21,8 +21,8 @@ during the timed region. Beside them, on the same unit: the fused-gather and
 no-reshard steps (`variants`), the variant optimizers' kernels
 (`variant_kernels`), the fused kernel with its state in pinned host memory
 (`offload_state_on_host`), and the per-unit driver on a 12-unit GPT-2 small
-model (`driver_gpt2_small_model_12_units`); --no-variants, --no-offload and
---no-driver skip them.
+model (`driver_gpt2_small_model_12_units`; these two on one GPU only);
+--no-variants, --no-offload and --no-driver skip them.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
@@ -549,7 +549,7 @@ def run_ours(args):
     # place by the same fused kernel over the host link (12 B read and 12 B
     # written per element there; gradients and the shard stay in HBM)
     offload = None
-    if not args.no_variants and not args.no_offload:
+    if not args.no_variants and not args.no_offload and world_size == 1:  # pins 12 B/param of host memory
         try:
             hstate = [torch.zeros(P_pad, dtype=torch.float32, pin_memory=True) for _ in range(3)]
         except RuntimeError as e:  # not enough page-locked host memory
@@ -579,7 +579,7 @@ def run_ours(args):
     # units, the blocks of a GPT-2 small model): a Python loop over
     # FlatParamUnit.step against one native fsdp_step_units call per step
     driver = None
-    if not args.no_variants and not args.no_driver:
+    if not args.no_variants and not args.no_driver and world_size == 1:
         driver, n_launch = measure_driver(F, fi, dev, stream)
         launches += n_launch
 
