@@ -463,35 +463,47 @@ def run_ours(args):
     # forward). --e2e-read-params reads the compute-dtype parameters instead.
     # Consecutive steps overlap their copies and kernels.
     Ke = max(3, min(args.e2e_steps, K))
-    host_grads = [torch.empty(P_pad, dtype=gdt, pin_memory=True) for _ in range(N)]
-    for r in range(N):
-        host_grads[r].copy_(unit.grads[r])
-    counter = torch.zeros(1, dtype=torch.int32, device=dev)
-    if args.e2e_read_params:
-        host_out, host_nf = torch.empty(P_pad, dtype=odt, pin_memory=True), None
-        d2h = host_out.numel() * host_out.element_size()
-    else:
-        host_out, host_nf = None, torch.zeros(1, dtype=torch.int32, pin_memory=True)
-        d2h = host_nf.numel() * host_nf.element_size()
-    h2d = sum(g.numel() * g.element_size() for g in host_grads)
-    t += 1
-    unit.step_from_host(host_grads, host_out, hp(t), gathers=cfg.gathers, nonfinite_count=counter,
-                        host_nonfinite=host_nf)  # sets up the streams
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    if world_size > 1:
-        dist.barrier()
-    e0.record(stream)
-    for _ in range(Ke):
+    e2e_ms, e2e_unavailable = 0.0, None
+    try:  # N gradient buffers of pinned host memory (13.7 GB for the 70B unit)
+        host_grads = [torch.empty(P_pad, dtype=gdt, pin_memory=True) for _ in range(N)]
+    except RuntimeError as e:
+        host_grads, e2e_unavailable = None, "pinned host buffers: " + str(e).splitlines()[0][:160]
+    if world_size > 1:  # every rank runs the e2e steps or none does
+        ok = torch.tensor([0 if host_grads is None else 1], device=dev)
+        dist.all_reduce(ok, op=dist.ReduceOp.MIN)
+        if int(ok.item()) == 0 and host_grads is not None:
+            host_grads, e2e_unavailable = None, "another rank could not pin its host buffers"
+    h2d = d2h = 0
+    if host_grads is not None:
+        for r in range(N):
+            host_grads[r].copy_(unit.grads[r])
+        counter = torch.zeros(1, dtype=torch.int32, device=dev)
+        if args.e2e_read_params:
+            host_out, host_nf = torch.empty(P_pad, dtype=odt, pin_memory=True), None
+            d2h = host_out.numel() * host_out.element_size()
+        else:
+            host_out, host_nf = None, torch.zeros(1, dtype=torch.int32, pin_memory=True)
+            d2h = host_nf.numel() * host_nf.element_size()
+        h2d = sum(g.numel() * g.element_size() for g in host_grads)
         t += 1
         unit.step_from_host(host_grads, host_out, hp(t), gathers=cfg.gathers, nonfinite_count=counter,
-                            host_nonfinite=host_nf)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / Ke
-    if host_nf is not None and int(host_nf.item()) != 0:
-        raise RuntimeError("e2e steps reported non-finite gradients")
-    launches += Ke * (1 + cfg.gathers)
+                            host_nonfinite=host_nf)  # sets up the streams
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        if world_size > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(Ke):
+            t += 1
+            unit.step_from_host(host_grads, host_out, hp(t), gathers=cfg.gathers, nonfinite_count=counter,
+                                host_nonfinite=host_nf)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / Ke
+        if host_nf is not None and int(host_nf.item()) != 0:
+            raise RuntimeError("e2e steps reported non-finite gradients")
+        launches += Ke * (1 + cfg.gathers)
+        del host_grads, host_out, host_nf
 
     # ---- variants of the same step (same byte model): the first all-gather
     # fused into the update kernel; and the no-reshard mode (one gather kept
@@ -627,7 +639,8 @@ def run_ours(args):
             "fused_ms": round(rsa_ms, 4),
             "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
         },
-        "e2e": {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"unavailable": e2e_unavailable} if e2e_unavailable else {
+                "value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 3), "steps": Ke,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "d2h": "compute-dtype parameters" if args.e2e_read_params else "non-finite gradient count"},
