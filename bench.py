@@ -255,8 +255,9 @@ def timed_calls(fn, K: int, stream, flush: L2Flush) -> float:
 
 def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20):
     """Host enqueue time and device time per model step of n_units GPT-2 small
-    block units (one gather each), stepped by a Python loop over the units and
-    by one native fsdp_step_units call. Returns (result, timed launches)."""
+    block units (one gather each), stepped by a Python loop over the units, by
+    one native fsdp_step_units call, and by one launch of the step captured as
+    a CUDA graph. Returns (result, timed launches)."""
     import torch
 
     cfg = fi.CONFIGS["gpt2_small"]
@@ -283,8 +284,13 @@ def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20):
     def native():
         seq.step(hp(), gathers=cfg.gathers)
 
+    graph = seq.capture(gathers=cfg.gathers)
+
+    def captured():
+        graph.launch(hp())
+
     out = {}
-    for name, fn in (("python_loop", python_loop), ("native", native)):
+    for name, fn in (("python_loop", python_loop), ("native", native), ("cuda_graph", captured)):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
@@ -302,9 +308,10 @@ def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20):
     out["bytes_per_step"] = rsa_b + ag_b
     out["native_GBs"] = round((rsa_b + ag_b) / (out["native"]["device_ms_per_step"] * 1e-3) / 1e9, 1)
     out["launches_per_step"] = n_units * (1 + cfg.gathers)
-    del seq, units
+    graph.close()
+    del seq, units, graph
     torch.cuda.empty_cache()
-    return out, 2 * steps * n_units * (1 + cfg.gathers)
+    return out, 3 * steps * n_units * (1 + cfg.gathers)
 
 
 def max_over_ranks(values, device):

@@ -343,6 +343,31 @@ typedef struct {
 fsdp_status fsdp_step_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
                                int gathers, uint32_t *nonfinite_count, void *stream);
 
+/* A model step captured as a CUDA graph (opaque; host memory owned by the
+ * library, freed by fsdp_step_graph_destroy). */
+typedef struct fsdp_step_graph fsdp_step_graph;
+
+/* Capture the step fsdp_step_units would enqueue for these units, gathers,
+ * fusion and counter into a CUDA graph, instantiated on the current device.
+ * The units are validated as fsdp_step_units validates them; nothing runs.
+ * The graph holds the buffers' addresses: they must stay allocated, and a
+ * step launched from it touches exactly those buffers. Each launch writes
+ * its own step's scalars, so one graph serves every step ("capture
+ * launch-bound inner loops in graphs": one launch for the whole model).
+ *   graph_out    host; receives the handle (NULL on error). */
+fsdp_status fsdp_step_graph_create(const fsdp_unit *units, int n_units, int gathers, int fuse_first_gather,
+                                   uint32_t *nonfinite_count, fsdp_step_graph **graph_out);
+
+/* Launch the captured step on `stream` with the scalars of hp (computed as
+ * fsdp_reduce_scatter_adam_cast computes them, per unit for its world size).
+ * Stream-ordered and asynchronous like the other entry points; results are
+ * bit-identical to fsdp_step_units with the same hp. Not thread-safe for
+ * one graph (each launch rewrites its update nodes). */
+fsdp_status fsdp_step_graph_launch(fsdp_step_graph *graph, const fsdp_adamw_hparams *hp, void *stream);
+
+/* Free a captured step (NULL is a no-op). Launches already enqueued complete. */
+fsdp_status fsdp_step_graph_destroy(fsdp_step_graph *graph);
+
 /* Human-readable name of a status. Never NULL. */
 const char *fsdp_status_string(fsdp_status status);
 

@@ -38,6 +38,9 @@ EXPORTS = (
     "fsdp_take_wait_timeouts",
     "fsdp_step_units",
     "fsdp_step_units_ex",
+    "fsdp_step_graph_create",
+    "fsdp_step_graph_launch",
+    "fsdp_step_graph_destroy",
 )
 
 
@@ -108,6 +111,9 @@ def load() -> ctypes.CDLL:
                                       vp, vp]),
             "fsdp_step_units_ex": (i32, [ctypes.POINTER(FsdpUnitEx), i32, ctypes.POINTER(FsdpStepConfig), i32,
                                          vp, vp]),
+            "fsdp_step_graph_create": (i32, [ctypes.POINTER(FsdpUnit), i32, i32, i32, vp, ctypes.POINTER(vp)]),
+            "fsdp_step_graph_launch": (i32, [vp, ctypes.POINTER(FsdpAdamwHparams), vp]),
+            "fsdp_step_graph_destroy": (i32, [vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)

@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <new>
 #include <vector>
 
 #include "host.cuh"
@@ -457,8 +458,20 @@ fsdp_status side_streams(SideStreams *&out) {
     return FSDP_OK;
 }
 
-fsdp_status launch_unit(const UnitPlan &p, cudaStream_t s) {
+// Launch one unit's kernels on s. Under stream capture, *update_node (if
+// given) receives the graph node of the unit's update kernel: the one node
+// the capture's dependency set holds right after that launch.
+fsdp_status launch_unit(const UnitPlan &p, cudaStream_t s, cudaGraphNode_t *update_node = nullptr) {
     fsdp_status st = p.variant ? launch_step(p.step, s) : launch_rsa(p.rsa, p.grad_dtype, p.out_dtype, s);
+    if (st == FSDP_OK && update_node) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        const cudaGraphNode_t *deps = nullptr;
+        size_t nd = 0;
+        if (cudaError_t e = cudaStreamGetCaptureInfo(s, &cs, nullptr, nullptr, &deps, nullptr, &nd); e != cudaSuccess)
+            return cuda_status(e);
+        if (cs != cudaStreamCaptureStatusActive || nd != 1 || !deps) return FSDP_ERR_CUDA;
+        *update_node = deps[0];
+    }
     for (int k = 0; st == FSDP_OK && k < p.separate_gathers; ++k) st = launch_gather(p.gather, s);
     return st;
 }
@@ -470,16 +483,21 @@ void add_span(std::vector<Span> &spans, const void *p, uintptr_t bytes) {
 // Enqueue validated units: refuse overlapping written buffers (two units
 // sharing memory), then launch each unit's kernels in order, spread over
 // the side streams when there are two or more units with work.
-fsdp_status run_units(const std::vector<UnitPlan> &plan, std::vector<Span> &spans, cudaStream_t s) {
+// Under stream capture, `nodes` (if given) receives each unit's update node
+// (nullptr for an empty unit).
+fsdp_status run_units(const std::vector<UnitPlan> &plan, std::vector<Span> &spans, cudaStream_t s,
+                      std::vector<cudaGraphNode_t> *nodes = nullptr) {
     std::sort(spans.begin(), spans.end());
     for (size_t i = 1; i < spans.size(); ++i)
         if (spans[i].lo < spans[i - 1].hi) return FSDP_ERR_INVALID_ARG;
+    if (nodes) nodes->assign(plan.size(), nullptr);
+    auto node_of = [&](size_t u) { return nodes ? &(*nodes)[u] : nullptr; };
     int busy = 0;
     for (const UnitPlan &p : plan) busy += p.empty ? 0 : 1;
     if (kUnitStreams < 2 || busy < 2) {
-        for (const UnitPlan &p : plan) {
-            if (p.empty) continue;
-            if (fsdp_status st = launch_unit(p, s); st != FSDP_OK) return st;
+        for (size_t u = 0; u < plan.size(); ++u) {
+            if (plan[u].empty) continue;
+            if (fsdp_status st = launch_unit(plan[u], s, node_of(u)); st != FSDP_OK) return st;
         }
         return FSDP_OK;
     }
@@ -491,9 +509,9 @@ fsdp_status run_units(const std::vector<UnitPlan> &plan, std::vector<Span> &span
         if (cudaError_t e = cudaStreamWaitEvent(side->s[i], side->fork, 0); e != cudaSuccess) return cuda_status(e);
     fsdp_status result = FSDP_OK;
     int k = 0;
-    for (const UnitPlan &p : plan) {
-        if (p.empty) continue;
-        result = launch_unit(p, side->s[k++ % ns]);
+    for (size_t u = 0; u < plan.size(); ++u) {
+        if (plan[u].empty) continue;
+        result = launch_unit(plan[u], side->s[k++ % ns], node_of(u));
         if (result != FSDP_OK) break;
     }
     // join every side stream back into the caller's stream, also after a
@@ -505,6 +523,50 @@ fsdp_status run_units(const std::vector<UnitPlan> &plan, std::vector<Span> &span
         if (e != cudaSuccess && result == FSDP_OK) result = cuda_status(e);
     }
     return result;
+}
+
+// Validation of fsdp_step_units' units (and of a captured step's): one plan
+// per unit and the spans of every written buffer.
+fsdp_status plan_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp, int gathers,
+                       int fuse_first_gather, uint32_t *nonfinite_count, std::vector<UnitPlan> &plan,
+                       std::vector<Span> &spans) {
+    if (n_units < 0 || (n_units > 0 && !units) || !hp) return FSDP_ERR_INVALID_ARG;
+    if (gathers < 0 || gathers > FSDP_MAX_WORLD) return FSDP_ERR_INVALID_ARG;
+    const bool fuse = fuse_first_gather != 0 && gathers > 0;
+    plan.assign(static_cast<size_t>(n_units), UnitPlan());
+    spans.clear();
+    for (int u = 0; u < n_units; ++u) {
+        const fsdp_unit &x = units[u];
+        UnitPlan &p = plan[static_cast<size_t>(u)];
+        p.variant = false;
+        if (!dtype_valid(x.grad_dtype) || !dtype_valid(x.out_dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
+        p.grad_dtype = static_cast<fsdp_dtype>(x.grad_dtype);
+        p.out_dtype = static_cast<fsdp_dtype>(x.out_dtype);
+        if (x.n_full < 0 || x.n_full > FSDP_MAX_WORLD || (x.n_full > 0 && !x.full_bufs)) return FSDP_ERR_INVALID_ARG;
+        if (gathers > 0 && x.n_full < 1) return FSDP_ERR_INVALID_ARG;
+        if (x.padded_numel > 0 && !x.shard_out) return FSDP_ERR_INVALID_ARG;
+        fsdp_status st = prepare_rsa(x.grads, p.grad_dtype, x.world, x.padded_numel, x.master, x.exp_avg,
+                                     x.exp_avg_sq, x.shard_out, p.out_dtype, fuse ? x.full_bufs : nullptr,
+                                     fuse ? x.n_full : 0, hp, 0, x.world, nonfinite_count, p.rsa, p.empty);
+        if (st != FSDP_OK) return st;
+        p.separate_gathers = p.empty ? 0 : gathers - (fuse ? 1 : 0);
+        if (p.separate_gathers > 0) {
+            bool gempty = false;
+            st = prepare_gather(x.shard_out, p.out_dtype, x.world, x.padded_numel, x.full_bufs, x.n_full, p.gather,
+                                gempty);
+            if (st != FSDP_OK) return st;
+        }
+        if (p.empty) continue;
+        const uintptr_t sb = static_cast<uintptr_t>(x.padded_numel) * 4;
+        const uintptr_t ob = static_cast<uintptr_t>(x.padded_numel) * static_cast<uintptr_t>(dtype_size(p.out_dtype));
+        add_span(spans, x.master, sb);
+        add_span(spans, x.exp_avg, sb);
+        add_span(spans, x.exp_avg_sq, sb);
+        add_span(spans, x.shard_out, ob);
+        if (gathers > 0)
+            for (int d = 0; d < x.n_full; ++d) add_span(spans, x.full_bufs[d], ob);
+    }
+    return FSDP_OK;
 }
 
 }  // namespace
@@ -556,42 +618,10 @@ FSDP_API fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, in
 FSDP_API fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
                                      int gathers, int fuse_first_gather, uint32_t *nonfinite_count,
                                      void *stream) {
-    if (n_units < 0 || (n_units > 0 && !units) || !hp) return FSDP_ERR_INVALID_ARG;
-    if (gathers < 0 || gathers > FSDP_MAX_WORLD) return FSDP_ERR_INVALID_ARG;
-    const bool fuse = fuse_first_gather != 0 && gathers > 0;
-    std::vector<UnitPlan> plan(static_cast<size_t>(n_units));
+    std::vector<UnitPlan> plan;
     std::vector<Span> spans;
-    for (int u = 0; u < n_units; ++u) {
-        const fsdp_unit &x = units[u];
-        UnitPlan &p = plan[static_cast<size_t>(u)];
-        p.variant = false;
-        if (!dtype_valid(x.grad_dtype) || !dtype_valid(x.out_dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
-        p.grad_dtype = static_cast<fsdp_dtype>(x.grad_dtype);
-        p.out_dtype = static_cast<fsdp_dtype>(x.out_dtype);
-        if (x.n_full < 0 || x.n_full > FSDP_MAX_WORLD || (x.n_full > 0 && !x.full_bufs)) return FSDP_ERR_INVALID_ARG;
-        if (gathers > 0 && x.n_full < 1) return FSDP_ERR_INVALID_ARG;
-        if (x.padded_numel > 0 && !x.shard_out) return FSDP_ERR_INVALID_ARG;
-        fsdp_status st = prepare_rsa(x.grads, p.grad_dtype, x.world, x.padded_numel, x.master, x.exp_avg,
-                                     x.exp_avg_sq, x.shard_out, p.out_dtype, fuse ? x.full_bufs : nullptr,
-                                     fuse ? x.n_full : 0, hp, 0, x.world, nonfinite_count, p.rsa, p.empty);
-        if (st != FSDP_OK) return st;
-        p.separate_gathers = p.empty ? 0 : gathers - (fuse ? 1 : 0);
-        if (p.separate_gathers > 0) {
-            bool gempty = false;
-            st = prepare_gather(x.shard_out, p.out_dtype, x.world, x.padded_numel, x.full_bufs, x.n_full, p.gather,
-                                gempty);
-            if (st != FSDP_OK) return st;
-        }
-        if (p.empty) continue;
-        const uintptr_t sb = static_cast<uintptr_t>(x.padded_numel) * 4;
-        const uintptr_t ob = static_cast<uintptr_t>(x.padded_numel) * static_cast<uintptr_t>(dtype_size(p.out_dtype));
-        add_span(spans, x.master, sb);
-        add_span(spans, x.exp_avg, sb);
-        add_span(spans, x.exp_avg_sq, sb);
-        add_span(spans, x.shard_out, ob);
-        if (gathers > 0)
-            for (int d = 0; d < x.n_full; ++d) add_span(spans, x.full_bufs[d], ob);
-    }
+    const fsdp_status st = plan_units(units, n_units, hp, gathers, fuse_first_gather, nonfinite_count, plan, spans);
+    if (st != FSDP_OK) return st;
     return run_units(plan, spans, static_cast<cudaStream_t>(stream));
 }
 
@@ -638,6 +668,98 @@ FSDP_API fsdp_status fsdp_step_units_ex(const fsdp_unit_ex *units, int n_units, 
             for (int d = 0; d < x.n_full; ++d) add_span(spans, x.full_bufs[d], ob);
     }
     return run_units(plan, spans, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+// A captured model step (fsdp_step_graph_*): the instantiated graph and,
+// per unit, the node of its fused update kernel (nullptr for an empty unit)
+// and its world size, which the per-step scalars depend on.
+struct fsdp_step_graph {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    std::vector<cudaGraphNode_t> nodes;
+    std::vector<int> worlds;
+};
+
+extern "C" {
+
+FSDP_API fsdp_status fsdp_step_graph_create(const fsdp_unit *units, int n_units, int gathers, int fuse_first_gather,
+                                            uint32_t *nonfinite_count, fsdp_step_graph **graph_out) {
+    if (!graph_out) return FSDP_ERR_INVALID_ARG;
+    *graph_out = nullptr;
+    // placeholder hyperparameters for validation and capture; every launch
+    // writes the step's own scalars into the update nodes
+    const fsdp_adamw_hparams hp0 = {0.0f, 0.9f, 0.999f, 1e-8f, 0.0f, 1, 1.0f};
+    std::vector<UnitPlan> plan;
+    std::vector<Span> spans;
+    fsdp_status st = plan_units(units, n_units, &hp0, gathers, fuse_first_gather, nonfinite_count, plan, spans);
+    if (st != FSDP_OK) return st;
+    cudaStream_t cs = nullptr;
+    if (cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking); e != cudaSuccess) return cuda_status(e);
+    // relaxed: the first launch of a kernel build queries its occupancy and
+    // may set its shared-memory limit, which a stricter mode would refuse
+    if (cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed); e != cudaSuccess) {
+        cudaStreamDestroy(cs);
+        return cuda_status(e);
+    }
+    std::vector<cudaGraphNode_t> nodes;
+    st = run_units(plan, spans, cs, &nodes);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(cs, &graph);  // always end the capture
+    cudaStreamDestroy(cs);
+    if (st != FSDP_OK || ec != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        return st != FSDP_OK ? st : cuda_status(ec);
+    }
+    cudaGraphExec_t exec = nullptr;
+    if (cudaError_t e = cudaGraphInstantiate(&exec, graph, 0); e != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        return cuda_status(e);
+    }
+    fsdp_step_graph *g = new (std::nothrow) fsdp_step_graph;
+    if (!g) {
+        cudaGraphExecDestroy(exec);
+        cudaGraphDestroy(graph);
+        return FSDP_ERR_INVALID_ARG;
+    }
+    g->graph = graph;
+    g->exec = exec;
+    g->nodes = nodes;
+    g->worlds.resize(plan.size());
+    for (size_t u = 0; u < plan.size(); ++u) g->worlds[u] = units[u].world;
+    *graph_out = g;
+    return FSDP_OK;
+}
+
+FSDP_API fsdp_status fsdp_step_graph_launch(fsdp_step_graph *graph, const fsdp_adamw_hparams *hp, void *stream) {
+    if (!graph || !hp) return FSDP_ERR_INVALID_ARG;
+    if (hp->step < 1 || !(hp->grad_scale > 0.0f) || !isfinite(hp->grad_scale)) return FSDP_ERR_INVALID_ARG;
+    for (size_t u = 0; u < graph->nodes.size(); ++u) {
+        if (!graph->nodes[u]) continue;
+        // the node is a fused update kernel: (RsaArgs, int64 vbegin, int64
+        // nchunks, int64 vend). Only the scalars inside RsaArgs change.
+        cudaKernelNodeParams kp;
+        if (cudaError_t e = cudaGraphKernelNodeGetParams(graph->nodes[u], &kp); e != cudaSuccess)
+            return cuda_status(e);
+        if (!kp.kernelParams) return FSDP_ERR_INVALID_ARG;
+        RsaArgs a;
+        memcpy(&a, kp.kernelParams[0], sizeof(a));
+        a.s = make_scalars(*hp, graph->worlds[u]);
+        void *args[4] = {&a, kp.kernelParams[1], kp.kernelParams[2], kp.kernelParams[3]};
+        kp.kernelParams = args;
+        if (cudaError_t e = cudaGraphExecKernelNodeSetParams(graph->exec, graph->nodes[u], &kp); e != cudaSuccess)
+            return cuda_status(e);
+    }
+    return cuda_status(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));
+}
+
+FSDP_API fsdp_status fsdp_step_graph_destroy(fsdp_step_graph *graph) {
+    if (!graph) return FSDP_OK;
+    const cudaError_t e1 = graph->exec ? cudaGraphExecDestroy(graph->exec) : cudaSuccess;
+    const cudaError_t e2 = graph->graph ? cudaGraphDestroy(graph->graph) : cudaSuccess;
+    delete graph;
+    return e1 != cudaSuccess ? cuda_status(e1) : cuda_status(e2);
 }
 
 FSDP_API const char *fsdp_status_string(fsdp_status status) {

@@ -20,7 +20,7 @@ __all__ = [
     "fsdp_reduce_scatter_adam_cast", "fsdp_reduce_scatter_adam_cast_gather", "fsdp_all_gather",
     "fsdp_status_string",
     "fsdp_last_cuda_error", "fsdp_take_wait_timeouts", "dtype_code",
-    "UnitDescs", "fsdp_step_units", "fsdp_step_units_ex",
+    "UnitDescs", "fsdp_step_units", "fsdp_step_units_ex", "StepGraph",
 ]
 
 _DTYPES = {torch.float32: _lib.FSDP_F32, torch.bfloat16: _lib.FSDP_BF16, torch.float16: _lib.FSDP_F16}
@@ -396,3 +396,39 @@ def fsdp_step_units_ex(units, config: StepConfig, gathers: int = 1, nonfinite_co
     cfg = config.to_c()
     _check(_lib.load().fsdp_step_units_ex(descs.array_ex, descs.n, ctypes.byref(cfg), int(gathers), nf,
                                           _stream(stream)), "fsdp_step_units_ex")
+
+
+class StepGraph:
+    """A model step captured as a CUDA graph (fsdp_step_graph_create): one
+    launch runs every unit's fused update and gathers, with the scalars of
+    the step given to launch(). The units' buffers must stay allocated (the
+    graph holds their addresses; the units are kept alive here)."""
+
+    def __init__(self, units, gathers: int = 1, fuse_first_gather: bool = False,
+                 nonfinite_count: Optional[torch.Tensor] = None):
+        self.descs = units if isinstance(units, UnitDescs) else UnitDescs(units)
+        if not self.descs.adamw:
+            raise ValueError("a captured step needs fp32 master and AdamW state in every unit")
+        self._counter = nonfinite_count
+        self._handle = ctypes.c_void_p(None)
+        _check(_lib.load().fsdp_step_graph_create(self.descs.array, self.descs.n, int(gathers),
+                                                  1 if fuse_first_gather else 0, _counter(nonfinite_count),
+                                                  ctypes.byref(self._handle)), "fsdp_step_graph_create")
+
+    def launch(self, hparams: AdamWHParams, stream: Optional[torch.cuda.Stream] = None) -> None:
+        if not self._handle:
+            raise RuntimeError("the captured step was destroyed")
+        hp = hparams.to_c()
+        _check(_lib.load().fsdp_step_graph_launch(self._handle, ctypes.byref(hp), _stream(stream)),
+               "fsdp_step_graph_launch")
+
+    def close(self) -> None:
+        if self._handle:
+            _check(_lib.load().fsdp_step_graph_destroy(self._handle), "fsdp_step_graph_destroy")
+            self._handle = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

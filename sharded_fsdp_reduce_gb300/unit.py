@@ -37,7 +37,7 @@ from typing import Dict, List, Optional, Sequence, Tuple
 
 import torch
 
-from .fsdp import (OPTIMIZERS, AdamWHParams, StepConfig, UnitDescs, View, fsdp_all_gather, fsdp_flatten_pad,
+from .fsdp import (OPTIMIZERS, AdamWHParams, StepConfig, StepGraph, UnitDescs, View, fsdp_all_gather, fsdp_flatten_pad,
                    fsdp_reduce_scatter_adam_cast, fsdp_reduce_scatter_adam_cast_gather, fsdp_reduce_scatter_step,
                    fsdp_step_units, fsdp_step_units_ex, fsdp_unflatten_views)
 
@@ -294,6 +294,12 @@ class UnitSequence:
         for u in self.units:
             u.step_config(cfg)  # every unit takes this optimizer
         fsdp_step_units_ex(self.descs, cfg, gathers, nonfinite_count, stream)
+
+    def capture(self, gathers: int = 1, fuse_gather: bool = False,
+                nonfinite_count: Optional[torch.Tensor] = None) -> StepGraph:
+        """The model's step (every unit AdamW with fp32 state) captured as one
+        CUDA graph; StepGraph.launch(hp) runs it for any step."""
+        return StepGraph(self.descs, gathers, fuse_gather, nonfinite_count)
 
     def step_bytes(self, gathers: int = 1) -> Tuple[int, int]:
         """Algorithmic bytes of one model step: (fused kernels, all-gathers)."""

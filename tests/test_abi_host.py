@@ -366,3 +366,15 @@ def test_step_units_ex_validates_every_unit_before_launching(lib):
     assert call([unit(A), bad]) == E.FSDP_ERR_INVALID_ARG
     assert call([unit(A, P=0), unit(B, P=0)]) == E.FSDP_OK                     # empty units: nothing to launch
     assert lib.fsdp_last_cuda_error() == 0
+
+
+def test_step_graph_rejects_invalid_arguments_on_the_host(lib):
+    from sharded_fsdp_reduce_gb300 import _lib as E
+    out = ctypes.c_void_p(123)
+    assert lib.fsdp_step_graph_create(None, 0, 1, 0, None, None) == E.FSDP_ERR_INVALID_ARG     # no handle
+    assert lib.fsdp_step_graph_create(None, 1, 1, 0, None, ctypes.byref(out)) == E.FSDP_ERR_INVALID_ARG
+    assert out.value is None                                                                    # cleared
+    assert lib.fsdp_step_graph_create(None, 0, -1, 0, None, ctypes.byref(out)) == E.FSDP_ERR_INVALID_ARG
+    hp = E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+    assert lib.fsdp_step_graph_launch(None, ctypes.byref(hp), None) == E.FSDP_ERR_INVALID_ARG
+    assert lib.fsdp_step_graph_destroy(None) == E.FSDP_OK

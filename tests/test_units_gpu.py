@@ -257,3 +257,52 @@ def test_model_step_captured_in_a_cuda_graph(F):
             assert same(x, y)
         for fa, fb in zip(ua.full, ub.full):
             assert same(fa, fb)
+
+
+@pytest.mark.parametrize("gathers,fuse", [(2, False), (2, True), (1, True), (0, False)])
+def test_captured_step_matches_the_driver(F, gathers, fuse):
+    # one graph, launched for steps 1..4 with each step's scalars, against
+    # the native driver step by step; offloaded units included
+    a = [u for u in build_model(F, 14, state_on_host={1}) if u.grads[0].dtype != torch.float16]
+    b = [u for u in build_model(F, 14, state_on_host={1}) if u.grads[0].dtype != torch.float16]
+    nf_a = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nf_b = torch.zeros(1, dtype=torch.int32, device=DEV)
+    graph = F.UnitSequence(a).capture(gathers=gathers, fuse_gather=fuse, nonfinite_count=nf_a)
+    seq_b = F.UnitSequence(b)
+    s = torch.cuda.Stream()
+    for t in (1, 2, 3, 4):
+        load_grads(a, t, 15)
+        load_grads(b, t, 15)
+        torch.cuda.synchronize()
+        graph.launch(hp_for(F, a[0], t), stream=s)
+        seq_b.step(hp_for(F, b[0], t), gathers=gathers, fuse_gather=fuse, nonfinite_count=nf_b)
+        s.synchronize()
+        torch.cuda.synchronize()
+    for ua, ub in zip(a, b):
+        for x, y in ((ua.master, ub.master), (ua.exp_avg, ub.exp_avg), (ua.exp_avg_sq, ub.exp_avg_sq),
+                     (ua.shard_out, ub.shard_out)):
+            assert same(x, y)
+        for fa, fb in zip(ua.full, ub.full):
+            assert same(fa, fb)
+    assert int(nf_a.item()) == int(nf_b.item()) == 0
+    graph.close()
+    with pytest.raises(RuntimeError):
+        graph.launch(hp_for(F, a[0], 5))
+
+
+def test_captured_step_refusals(F):
+    a = [u for u in build_model(F, 16) if u.grads[0].dtype != torch.float16]
+    graph = F.UnitSequence(a).capture(gathers=1)
+    before = [u.master.clone() for u in a]
+    with pytest.raises(F.FsdpError):
+        graph.launch(F.AdamWHParams(1e-3, step=0))  # invalid step: nothing launched
+    torch.cuda.synchronize()
+    for u, p in zip(a, before):
+        assert same(u.master, p)
+    b = [u for u in build_model(F, 16) if u.grads[0].dtype != torch.float16]
+    b[2].exp_avg = b[0].exp_avg.narrow(0, 0, b[2].padded_numel)  # two units writing one buffer
+    with pytest.raises(F.FsdpError):
+        F.UnitSequence(b).capture(gathers=1)
+    v = F.FlatParamUnit([("w", (64,))], 2, torch.bfloat16, torch.bfloat16, device=DEV, optimizer="sgd")
+    with pytest.raises(ValueError):  # the captured step is the fused AdamW step
+        F.UnitSequence([v]).capture()
