@@ -93,6 +93,12 @@ int main(void) {
     CHECK(fsdp_step_units_ex(&v, 1, &cfg, 1, NULL, NULL) == FSDP_ERR_INVALID_ARG);
     CHECK(fsdp_step_units_ex(NULL, 0, &cfg, 1, NULL, NULL) == FSDP_OK);
     CHECK(fsdp_step_units_ex(&v, 1, NULL, 1, NULL, NULL) == FSDP_ERR_INVALID_ARG);
+    /* the captured step: no handle to fill, no graph to launch */
+    fsdp_step_graph *graph = (fsdp_step_graph *)&u; /* overwritten with NULL on error */
+    CHECK(fsdp_step_graph_create(NULL, 1, 1, 0, NULL, &graph) == FSDP_ERR_INVALID_ARG && graph == NULL);
+    CHECK(fsdp_step_graph_create(&u, 1, 1, 0, NULL, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_step_graph_launch(NULL, &hp, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_step_graph_destroy(NULL) == FSDP_OK);
     CHECK(fsdp_take_wait_timeouts(NULL) == FSDP_ERR_INVALID_ARG);
     CHECK(fsdp_last_cuda_error() == 0);
     printf("ok\n");
