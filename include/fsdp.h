@@ -365,6 +365,19 @@ fsdp_status fsdp_step_graph_create(const fsdp_unit *units, int n_units, int gath
  * one graph (each launch rewrites its update nodes). */
 fsdp_status fsdp_step_graph_launch(fsdp_step_graph *graph, const fsdp_adamw_hparams *hp, void *stream);
 
+/* The same for a model of variant units (fsdp_step_units_ex): captured with
+ * cfg's optimizer, whose kernels the graph holds; cfg is validated as
+ * fsdp_step_units_ex validates it. */
+fsdp_status fsdp_step_graph_create_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
+                                      int gathers, uint32_t *nonfinite_count, fsdp_step_graph **graph_out);
+
+/* Launch a captured variant step with cfg's scalars and reduction dtype.
+ * cfg->optimizer must be the one the graph was captured with, and
+ * reduce_dtype FSDP_F32 or every unit's gradient dtype; otherwise nothing
+ * is launched. A graph from fsdp_step_graph_create takes
+ * fsdp_step_graph_launch, one from fsdp_step_graph_create_ex this call. */
+fsdp_status fsdp_step_graph_launch_ex(fsdp_step_graph *graph, const fsdp_step_config *cfg, void *stream);
+
 /* Free a captured step (NULL is a no-op). Launches already enqueued complete. */
 fsdp_status fsdp_step_graph_destroy(fsdp_step_graph *graph);
 

@@ -41,6 +41,8 @@ EXPORTS = (
     "fsdp_step_graph_create",
     "fsdp_step_graph_launch",
     "fsdp_step_graph_destroy",
+    "fsdp_step_graph_create_ex",
+    "fsdp_step_graph_launch_ex",
 )
 
 
@@ -114,6 +116,9 @@ def load() -> ctypes.CDLL:
             "fsdp_step_graph_create": (i32, [ctypes.POINTER(FsdpUnit), i32, i32, i32, vp, ctypes.POINTER(vp)]),
             "fsdp_step_graph_launch": (i32, [vp, ctypes.POINTER(FsdpAdamwHparams), vp]),
             "fsdp_step_graph_destroy": (i32, [vp]),
+            "fsdp_step_graph_create_ex": (i32, [ctypes.POINTER(FsdpUnitEx), i32, ctypes.POINTER(FsdpStepConfig), i32,
+                                                vp, ctypes.POINTER(vp)]),
+            "fsdp_step_graph_launch_ex": (i32, [vp, ctypes.POINTER(FsdpStepConfig), vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)

@@ -569,6 +569,83 @@ fsdp_status plan_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hpa
     return FSDP_OK;
 }
 
+// Validation of fsdp_step_units_ex's units (and of a captured variant
+// step's): one plan per unit and the spans of every written buffer.
+fsdp_status plan_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg, int gathers,
+                          uint32_t *nonfinite_count, std::vector<UnitPlan> &plan, std::vector<Span> &spans) {
+    if (n_units < 0 || (n_units > 0 && !units) || !cfg) return FSDP_ERR_INVALID_ARG;
+    if (gathers < 0 || gathers > FSDP_MAX_WORLD) return FSDP_ERR_INVALID_ARG;
+    plan.assign(static_cast<size_t>(n_units), UnitPlan());
+    spans.clear();
+    for (int u = 0; u < n_units; ++u) {
+        const fsdp_unit_ex &x = units[u];
+        UnitPlan &p = plan[static_cast<size_t>(u)];
+        p.variant = true;
+        if (!dtype_valid(x.grad_dtype) || !dtype_valid(x.out_dtype) || !dtype_valid(x.state_dtype))
+            return FSDP_ERR_UNSUPPORTED_DTYPE;
+        const fsdp_dtype gd = static_cast<fsdp_dtype>(x.grad_dtype), od = static_cast<fsdp_dtype>(x.out_dtype);
+        const fsdp_dtype sd = static_cast<fsdp_dtype>(x.state_dtype);
+        p.grad_dtype = gd;
+        p.out_dtype = od;
+        if (x.n_full < 0 || x.n_full > FSDP_MAX_WORLD || (x.n_full > 0 && !x.full_bufs)) return FSDP_ERR_INVALID_ARG;
+        if (gathers > 0 && x.n_full < 1) return FSDP_ERR_INVALID_ARG;
+        fsdp_status st = prepare_step(x.grads, gd, x.world, x.padded_numel, x.param, x.state0, x.state1, sd,
+                                      x.shard_out, od, cfg, 0, x.world, nonfinite_count, p.step);
+        if (st != FSDP_OK) return st;
+        p.empty = p.step.empty;
+        p.separate_gathers = p.empty ? 0 : gathers;
+        // the gathered shards: shard_out, or the parameter itself when the
+        // state is bf16/fp16 (then it is the compute-dtype shard)
+        const void *shard = sd == FSDP_F32 ? x.shard_out : x.param;
+        if (p.separate_gathers > 0) {
+            bool gempty = false;
+            st = prepare_gather(shard, od, x.world, x.padded_numel, x.full_bufs, x.n_full, p.gather, gempty);
+            if (st != FSDP_OK) return st;
+        }
+        if (p.empty) continue;
+        const uintptr_t P = static_cast<uintptr_t>(x.padded_numel);
+        const uintptr_t sb = P * static_cast<uintptr_t>(dtype_size(sd));
+        const uintptr_t ob = P * static_cast<uintptr_t>(dtype_size(od));
+        add_span(spans, x.param, sb);
+        add_span(spans, x.state0, sb);
+        add_span(spans, x.state1, sb);
+        add_span(spans, x.shard_out, ob);
+        if (gathers > 0)
+            for (int d = 0; d < x.n_full; ++d) add_span(spans, x.full_bufs[d], ob);
+    }
+    return FSDP_OK;
+}
+
+// Capture the launches of validated units into an instantiated graph,
+// recording each unit's update node.
+fsdp_status capture_units(const std::vector<UnitPlan> &plan, std::vector<Span> &spans, cudaGraph_t &graph,
+                          cudaGraphExec_t &exec, std::vector<cudaGraphNode_t> &nodes) {
+    graph = nullptr;
+    exec = nullptr;
+    cudaStream_t cs = nullptr;
+    if (cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking); e != cudaSuccess) return cuda_status(e);
+    // relaxed: the first launch of a kernel build queries its occupancy and
+    // may set its shared-memory limit, which a stricter mode would refuse
+    if (cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed); e != cudaSuccess) {
+        cudaStreamDestroy(cs);
+        return cuda_status(e);
+    }
+    fsdp_status st = run_units(plan, spans, cs, &nodes);
+    const cudaError_t ec = cudaStreamEndCapture(cs, &graph);  // always end the capture
+    cudaStreamDestroy(cs);
+    if (st != FSDP_OK || ec != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        graph = nullptr;
+        return st != FSDP_OK ? st : cuda_status(ec);
+    }
+    if (cudaError_t e = cudaGraphInstantiate(&exec, graph, 0); e != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        graph = nullptr;
+        return cuda_status(e);
+    }
+    return FSDP_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -627,60 +704,73 @@ FSDP_API fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const 
 
 FSDP_API fsdp_status fsdp_step_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
                                         int gathers, uint32_t *nonfinite_count, void *stream) {
-    if (n_units < 0 || (n_units > 0 && !units) || !cfg) return FSDP_ERR_INVALID_ARG;
-    if (gathers < 0 || gathers > FSDP_MAX_WORLD) return FSDP_ERR_INVALID_ARG;
-    std::vector<UnitPlan> plan(static_cast<size_t>(n_units));
+    std::vector<UnitPlan> plan;
     std::vector<Span> spans;
-    for (int u = 0; u < n_units; ++u) {
-        const fsdp_unit_ex &x = units[u];
-        UnitPlan &p = plan[static_cast<size_t>(u)];
-        p.variant = true;
-        if (!dtype_valid(x.grad_dtype) || !dtype_valid(x.out_dtype) || !dtype_valid(x.state_dtype))
-            return FSDP_ERR_UNSUPPORTED_DTYPE;
-        const fsdp_dtype gd = static_cast<fsdp_dtype>(x.grad_dtype), od = static_cast<fsdp_dtype>(x.out_dtype);
-        const fsdp_dtype sd = static_cast<fsdp_dtype>(x.state_dtype);
-        p.grad_dtype = gd;
-        p.out_dtype = od;
-        if (x.n_full < 0 || x.n_full > FSDP_MAX_WORLD || (x.n_full > 0 && !x.full_bufs)) return FSDP_ERR_INVALID_ARG;
-        if (gathers > 0 && x.n_full < 1) return FSDP_ERR_INVALID_ARG;
-        fsdp_status st = prepare_step(x.grads, gd, x.world, x.padded_numel, x.param, x.state0, x.state1, sd,
-                                      x.shard_out, od, cfg, 0, x.world, nonfinite_count, p.step);
-        if (st != FSDP_OK) return st;
-        p.empty = p.step.empty;
-        p.separate_gathers = p.empty ? 0 : gathers;
-        // the gathered shards: shard_out, or the parameter itself when the
-        // state is bf16/fp16 (then it is the compute-dtype shard)
-        const void *shard = sd == FSDP_F32 ? x.shard_out : x.param;
-        if (p.separate_gathers > 0) {
-            bool gempty = false;
-            st = prepare_gather(shard, od, x.world, x.padded_numel, x.full_bufs, x.n_full, p.gather, gempty);
-            if (st != FSDP_OK) return st;
-        }
-        if (p.empty) continue;
-        const uintptr_t P = static_cast<uintptr_t>(x.padded_numel);
-        const uintptr_t sb = P * static_cast<uintptr_t>(dtype_size(sd));
-        const uintptr_t ob = P * static_cast<uintptr_t>(dtype_size(od));
-        add_span(spans, x.param, sb);
-        add_span(spans, x.state0, sb);
-        add_span(spans, x.state1, sb);
-        add_span(spans, x.shard_out, ob);
-        if (gathers > 0)
-            for (int d = 0; d < x.n_full; ++d) add_span(spans, x.full_bufs[d], ob);
-    }
+    const fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, plan, spans);
+    if (st != FSDP_OK) return st;
     return run_units(plan, spans, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
 
 // A captured model step (fsdp_step_graph_*): the instantiated graph and,
-// per unit, the node of its fused update kernel (nullptr for an empty unit)
-// and its world size, which the per-step scalars depend on.
+// per unit, the node of its update kernel (nullptr for an empty unit), its
+// world size and gradient dtype, which the per-step arguments depend on.
+// `variant` graphs hold the variant kernel of one optimizer.
 struct fsdp_step_graph {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
     std::vector<cudaGraphNode_t> nodes;
     std::vector<int> worlds;
+    std::vector<int> grad_dtypes;
+    bool variant = false;
+    int optimizer = 0;
 };
+
+namespace {
+
+fsdp_status make_graph(const std::vector<UnitPlan> &plan, std::vector<Span> &spans, bool variant, int optimizer,
+                       fsdp_step_graph **graph_out) {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    std::vector<cudaGraphNode_t> nodes;
+    if (fsdp_status st = capture_units(plan, spans, graph, exec, nodes); st != FSDP_OK) return st;
+    fsdp_step_graph *g = new (std::nothrow) fsdp_step_graph;
+    if (!g) {
+        cudaGraphExecDestroy(exec);
+        cudaGraphDestroy(graph);
+        return FSDP_ERR_INVALID_ARG;
+    }
+    g->graph = graph;
+    g->exec = exec;
+    g->nodes = nodes;
+    g->variant = variant;
+    g->optimizer = optimizer;
+    for (const UnitPlan &p : plan) {
+        g->worlds.push_back(p.variant ? p.step.args.world : p.rsa.world);
+        g->grad_dtypes.push_back(p.grad_dtype);
+    }
+    *graph_out = g;
+    return FSDP_OK;
+}
+
+// Write a step's arguments into one captured update node: the node's own
+// arguments (kernel params: the args struct, then int64 vbegin, nchunks,
+// vend) with only the step-dependent fields replaced.
+template <class Args, class Fill>
+fsdp_status set_update_node(fsdp_step_graph *graph, cudaGraphNode_t node, Fill fill) {
+    cudaKernelNodeParams kp;
+    if (cudaError_t e = cudaGraphKernelNodeGetParams(node, &kp); e != cudaSuccess) return cuda_status(e);
+    if (!kp.kernelParams) return FSDP_ERR_INVALID_ARG;
+    Args a;
+    memcpy(&a, kp.kernelParams[0], sizeof(a));
+    fill(a);
+    void *args[4] = {&a, kp.kernelParams[1], kp.kernelParams[2], kp.kernelParams[3]};
+    kp.kernelParams = args;
+    return cuda_status(cudaGraphExecKernelNodeSetParams(graph->exec, node, &kp));
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -695,61 +785,48 @@ FSDP_API fsdp_status fsdp_step_graph_create(const fsdp_unit *units, int n_units,
     std::vector<Span> spans;
     fsdp_status st = plan_units(units, n_units, &hp0, gathers, fuse_first_gather, nonfinite_count, plan, spans);
     if (st != FSDP_OK) return st;
-    cudaStream_t cs = nullptr;
-    if (cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking); e != cudaSuccess) return cuda_status(e);
-    // relaxed: the first launch of a kernel build queries its occupancy and
-    // may set its shared-memory limit, which a stricter mode would refuse
-    if (cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed); e != cudaSuccess) {
-        cudaStreamDestroy(cs);
-        return cuda_status(e);
-    }
-    std::vector<cudaGraphNode_t> nodes;
-    st = run_units(plan, spans, cs, &nodes);
-    cudaGraph_t graph = nullptr;
-    const cudaError_t ec = cudaStreamEndCapture(cs, &graph);  // always end the capture
-    cudaStreamDestroy(cs);
-    if (st != FSDP_OK || ec != cudaSuccess) {
-        if (graph) cudaGraphDestroy(graph);
-        return st != FSDP_OK ? st : cuda_status(ec);
-    }
-    cudaGraphExec_t exec = nullptr;
-    if (cudaError_t e = cudaGraphInstantiate(&exec, graph, 0); e != cudaSuccess) {
-        cudaGraphDestroy(graph);
-        return cuda_status(e);
-    }
-    fsdp_step_graph *g = new (std::nothrow) fsdp_step_graph;
-    if (!g) {
-        cudaGraphExecDestroy(exec);
-        cudaGraphDestroy(graph);
-        return FSDP_ERR_INVALID_ARG;
-    }
-    g->graph = graph;
-    g->exec = exec;
-    g->nodes = nodes;
-    g->worlds.resize(plan.size());
-    for (size_t u = 0; u < plan.size(); ++u) g->worlds[u] = units[u].world;
-    *graph_out = g;
-    return FSDP_OK;
+    return make_graph(plan, spans, false, FSDP_OPT_ADAMW, graph_out);
+}
+
+FSDP_API fsdp_status fsdp_step_graph_create_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
+                                               int gathers, uint32_t *nonfinite_count, fsdp_step_graph **graph_out) {
+    if (!graph_out) return FSDP_ERR_INVALID_ARG;
+    *graph_out = nullptr;
+    std::vector<UnitPlan> plan;
+    std::vector<Span> spans;
+    fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, plan, spans);
+    if (st != FSDP_OK) return st;
+    return make_graph(plan, spans, true, cfg->optimizer, graph_out);
 }
 
 FSDP_API fsdp_status fsdp_step_graph_launch(fsdp_step_graph *graph, const fsdp_adamw_hparams *hp, void *stream) {
-    if (!graph || !hp) return FSDP_ERR_INVALID_ARG;
+    if (!graph || !hp || graph->variant) return FSDP_ERR_INVALID_ARG;
     if (hp->step < 1 || !(hp->grad_scale > 0.0f) || !isfinite(hp->grad_scale)) return FSDP_ERR_INVALID_ARG;
     for (size_t u = 0; u < graph->nodes.size(); ++u) {
         if (!graph->nodes[u]) continue;
-        // the node is a fused update kernel: (RsaArgs, int64 vbegin, int64
-        // nchunks, int64 vend). Only the scalars inside RsaArgs change.
-        cudaKernelNodeParams kp;
-        if (cudaError_t e = cudaGraphKernelNodeGetParams(graph->nodes[u], &kp); e != cudaSuccess)
-            return cuda_status(e);
-        if (!kp.kernelParams) return FSDP_ERR_INVALID_ARG;
-        RsaArgs a;
-        memcpy(&a, kp.kernelParams[0], sizeof(a));
-        a.s = make_scalars(*hp, graph->worlds[u]);
-        void *args[4] = {&a, kp.kernelParams[1], kp.kernelParams[2], kp.kernelParams[3]};
-        kp.kernelParams = args;
-        if (cudaError_t e = cudaGraphExecKernelNodeSetParams(graph->exec, graph->nodes[u], &kp); e != cudaSuccess)
-            return cuda_status(e);
+        const int world = graph->worlds[u];
+        fsdp_status st = set_update_node<RsaArgs>(graph, graph->nodes[u],
+                                                  [&](RsaArgs &a) { a.s = make_scalars(*hp, world); });
+        if (st != FSDP_OK) return st;
+    }
+    return cuda_status(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));
+}
+
+FSDP_API fsdp_status fsdp_step_graph_launch_ex(fsdp_step_graph *graph, const fsdp_step_config *cfg, void *stream) {
+    if (!graph || !cfg || !graph->variant) return FSDP_ERR_INVALID_ARG;
+    if (cfg->optimizer != graph->optimizer) return FSDP_ERR_INVALID_ARG;
+    if (cfg->step < 1 || !(cfg->grad_scale > 0.0f) || !isfinite(cfg->grad_scale)) return FSDP_ERR_INVALID_ARG;
+    for (size_t u = 0; u < graph->nodes.size(); ++u)
+        if (graph->nodes[u] && cfg->reduce_dtype != FSDP_F32 && cfg->reduce_dtype != graph->grad_dtypes[u])
+            return FSDP_ERR_UNSUPPORTED_DTYPE;
+    for (size_t u = 0; u < graph->nodes.size(); ++u) {
+        if (!graph->nodes[u]) continue;
+        const int world = graph->worlds[u];
+        fsdp_status st = set_update_node<StepArgs>(graph, graph->nodes[u], [&](StepArgs &a) {
+            a.k = make_step_scalars(*cfg, world);
+            a.reduce_lowp = cfg->reduce_dtype != FSDP_F32 ? 1 : 0;
+        });
+        if (st != FSDP_OK) return st;
     }
     return cuda_status(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));
 }

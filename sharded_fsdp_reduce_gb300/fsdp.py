@@ -399,28 +399,45 @@ def fsdp_step_units_ex(units, config: StepConfig, gathers: int = 1, nonfinite_co
 
 
 class StepGraph:
-    """A model step captured as a CUDA graph (fsdp_step_graph_create): one
-    launch runs every unit's fused update and gathers, with the scalars of
-    the step given to launch(). The units' buffers must stay allocated (the
-    graph holds their addresses; the units are kept alive here)."""
+    """A model step captured as a CUDA graph (fsdp_step_graph_create, or
+    fsdp_step_graph_create_ex when `config` is given): one launch runs every
+    unit's update and gathers, with the scalars of the step given to
+    launch(). The units' buffers must stay allocated (the graph holds their
+    addresses; the units are kept alive here)."""
 
     def __init__(self, units, gathers: int = 1, fuse_first_gather: bool = False,
-                 nonfinite_count: Optional[torch.Tensor] = None):
+                 nonfinite_count: Optional[torch.Tensor] = None, config: Optional[StepConfig] = None):
         self.descs = units if isinstance(units, UnitDescs) else UnitDescs(units)
-        if not self.descs.adamw:
-            raise ValueError("a captured step needs fp32 master and AdamW state in every unit")
+        self.config = config
         self._counter = nonfinite_count
         self._handle = ctypes.c_void_p(None)
-        _check(_lib.load().fsdp_step_graph_create(self.descs.array, self.descs.n, int(gathers),
-                                                  1 if fuse_first_gather else 0, _counter(nonfinite_count),
-                                                  ctypes.byref(self._handle)), "fsdp_step_graph_create")
+        lib = _lib.load()
+        if config is None:
+            if not self.descs.adamw:
+                raise ValueError("a captured AdamW step needs fp32 master and AdamW state in every unit")
+            st = lib.fsdp_step_graph_create(self.descs.array, self.descs.n, int(gathers), 1 if fuse_first_gather else 0,
+                                            _counter(nonfinite_count), ctypes.byref(self._handle))
+        else:
+            if fuse_first_gather:
+                raise ValueError("the variant step has no fused gather")
+            cfg = config.to_c()
+            st = lib.fsdp_step_graph_create_ex(self.descs.array_ex, self.descs.n, ctypes.byref(cfg), int(gathers),
+                                               _counter(nonfinite_count), ctypes.byref(self._handle))
+        _check(st, "fsdp_step_graph_create")
 
-    def launch(self, hparams: AdamWHParams, stream: Optional[torch.cuda.Stream] = None) -> None:
+    def launch(self, hparams, stream: Optional[torch.cuda.Stream] = None) -> None:
+        """Run the captured step: hparams is AdamWHParams for an AdamW capture,
+        a StepConfig of the captured optimizer for a variant capture."""
         if not self._handle:
             raise RuntimeError("the captured step was destroyed")
-        hp = hparams.to_c()
-        _check(_lib.load().fsdp_step_graph_launch(self._handle, ctypes.byref(hp), _stream(stream)),
-               "fsdp_step_graph_launch")
+        lib = _lib.load()
+        if self.config is None:
+            hp = hparams.to_c()
+            st = lib.fsdp_step_graph_launch(self._handle, ctypes.byref(hp), _stream(stream))
+        else:
+            cfg = hparams.to_c()
+            st = lib.fsdp_step_graph_launch_ex(self._handle, ctypes.byref(cfg), _stream(stream))
+        _check(st, "fsdp_step_graph_launch")
 
     def close(self) -> None:
         if self._handle:

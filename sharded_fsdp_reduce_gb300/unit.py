@@ -296,10 +296,18 @@ class UnitSequence:
         fsdp_step_units_ex(self.descs, cfg, gathers, nonfinite_count, stream)
 
     def capture(self, gathers: int = 1, fuse_gather: bool = False,
-                nonfinite_count: Optional[torch.Tensor] = None) -> StepGraph:
-        """The model's step (every unit AdamW with fp32 state) captured as one
-        CUDA graph; StepGraph.launch(hp) runs it for any step."""
-        return StepGraph(self.descs, gathers, fuse_gather, nonfinite_count)
+                nonfinite_count: Optional[torch.Tensor] = None, config: Optional[StepConfig] = None) -> StepGraph:
+        """The model's step captured as one CUDA graph; StepGraph.launch runs it
+        for any step. Without `config`: the fused AdamW step (every unit
+        AdamW with fp32 state), launched with AdamWHParams. With a StepConfig
+        (required when a unit takes the variant step): the variant step of
+        that optimizer, launched with StepConfigs."""
+        if config is None and any(u.variant for u in self.units):
+            raise ValueError("units that take the variant step are captured with a StepConfig")
+        if config is not None:
+            for u in self.units:
+                u.step_config(config)  # every unit takes this optimizer
+        return StepGraph(self.descs, gathers, fuse_gather, nonfinite_count, config)
 
     def step_bytes(self, gathers: int = 1) -> Tuple[int, int]:
         """Algorithmic bytes of one model step: (fused kernels, all-gathers)."""

@@ -180,3 +180,36 @@ def test_variant_units_refuse_shared_buffers(F):
     torch.cuda.synchronize()
     for u, p in zip(a, before):
         assert same(u.master, p)  # nothing ran
+
+
+@pytest.mark.parametrize("opt", ["sgd", "adamax", "adadelta", "adamw"])
+def test_captured_variant_step_matches_the_driver(F, opt):
+    # one graph of the variant step, launched for steps 1..3 (with and
+    # without a gradient-dtype reduction), against fsdp_step_units_ex
+    shapes = [(8, 8 * 3000 + 5, torch.float32), (2, 4099, torch.bfloat16), (3, 1001, torch.float32)]
+    a = [make(F, opt, sdt, world=w, P=P, seed=20 + k) for k, (w, P, sdt) in enumerate(shapes)]
+    b = [make(F, opt, sdt, world=w, P=P, seed=20 + k) for k, (w, P, sdt) in enumerate(shapes)]
+    graph = F.UnitSequence(a).capture(gathers=2, config=cfg(F, opt, 1, False))
+    seq_b = F.UnitSequence(b)
+    for t in (1, 2, 3):
+        set_grads(a, t, 21)
+        set_grads(b, t, 21)
+        c = cfg(F, opt, t, t == 2)
+        graph.launch(c)
+        seq_b.step(c, gathers=2)
+    torch.cuda.synchronize()
+    for ua, ub in zip(a, b):
+        for name in ("master", "exp_avg", "exp_avg_sq", "shard_out"):
+            x, y = getattr(ua, name), getattr(ub, name)
+            if x is not None:
+                assert same(x, y), name
+        for fa, fb in zip(ua.full, ub.full):
+            assert same(fa, fb)
+    other = "adamax" if opt != "adamax" else "sgd"
+    with pytest.raises(F.FsdpError):  # the graph holds this optimizer's kernels
+        graph.launch(F.StepConfig(other, 1e-3, step=4))
+    with pytest.raises(F.FsdpError):  # a reduction in another dtype than the gradients'
+        graph.launch(F.StepConfig(opt, 1e-3, step=4, reduce_dtype=torch.float16))
+    with pytest.raises(ValueError):
+        F.UnitSequence(a).capture(gathers=1)  # variant units need a StepConfig
+    graph.close()
