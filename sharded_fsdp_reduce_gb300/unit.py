@@ -43,6 +43,17 @@ from .fsdp import (OPTIMIZERS, AdamWHParams, StepConfig, StepGraph, UnitDescs, V
 
 
 class FlatParamUnit:
+    """One FSDP unit's buffers and step.
+
+    params: (name, shape) per original parameter, in registration order (the
+    flatten order). world: N emulated ranks. grad_dtype / out_dtype: the
+    gradients' dtype and the compute dtype of the shards and gathered
+    buffers. n_full: gathered buffers (default N, one per rank).
+    state_on_host: fp32 master and state in pinned host memory (offload).
+    optimizer / state_dtype: the update ("adamw", "sgd", "adamax",
+    "adadelta") and the dtype of the parameter and state (fp32 keeps an fp32
+    master beside the compute-dtype shard; bf16/fp16 keeps none)."""
+
     def __init__(self, params: Sequence[Tuple[str, Tuple[int, ...]]], world: int, grad_dtype: torch.dtype,
                  out_dtype: torch.dtype, device="cuda", n_full: Optional[int] = None,
                  state_on_host: bool = False, optimizer: str = "adamw",
