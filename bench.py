@@ -404,7 +404,7 @@ def run_ours(args):
     dev = torch.device("cuda", local_rank)
     if world_size > 1:
         dist.init_process_group("nccl", device_id=dev)
-    if rank == 0 or not os.path.exists(os.path.join(ROOT, "sharded_fsdp_reduce_gb300", "libfsdpreduce.so")):
+    if rank == 0:  # one build (a no-op when up to date); the other ranks wait for it
         _build.build()
     if world_size > 1:
         dist.barrier()
