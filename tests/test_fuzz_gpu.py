@@ -171,3 +171,70 @@ def test_fuzz_step_units(F, orc, seed):
                     assert torch.equal(f, u.shard_out)
                 else:
                     assert not f.view(torch.uint8).any()  # never gathered: still zero
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_fuzz_step_graph(F, seed):
+    # a random model captured once (AdamW, or a random variant optimizer) and
+    # launched for a random sequence of steps with random hyperparameters,
+    # against the native driver on a twin model, bit for bit
+    rng = np.random.default_rng(7000 + seed)
+    variant = bool(seed % 2)
+    opt = str(rng.choice(["sgd", "adamax", "adadelta", "adamw"])) if variant else "adamw"
+    n_units = int(rng.integers(1, 5))
+    gathers = int(rng.integers(0, 3))
+    fuse = (not variant) and gathers > 0 and bool(rng.integers(0, 2))
+    specs = []
+    for _ in range(n_units):
+        world = int(rng.choice([1, 2, 3, 8]))
+        P = int(rng.integers(1, 20000))
+        gdt = fi.torch_dtype(str(rng.choice(["bf16", "f16", "f32"])))
+        sdt = fi.torch_dtype(str(rng.choice(["bf16", "f32"]))) if variant else torch.float32
+        odt = sdt if sdt != torch.float32 else fi.torch_dtype(str(rng.choice(FMTS)))
+        host = sdt == torch.float32 and bool(rng.integers(0, 2))
+        specs.append((world, P, gdt, sdt, odt, host, int(rng.integers(0, 1 << 30))))
+
+    def build():
+        units = []
+        for world, P, gdt, sdt, odt, host, s in specs:
+            u = F.FlatParamUnit([("x", (P,))], world, gdt, odt, device=DEV, optimizer=opt, state_dtype=sdt,
+                                state_on_host=host)
+            g = torch.Generator().manual_seed(s)
+            u.load_master([(torch.rand(P, generator=g) * 0.2 - 0.1).to(DEV)])
+            units.append(u)
+        torch.cuda.synchronize()
+        return units
+
+    a, b = build(), build()
+
+    def hp(t, lr, wd):
+        if variant:
+            return F.StepConfig(opt, lr, 0.9, 0.999, 1e-6, wd, t)
+        return F.AdamWHParams(lr, 0.9, 0.999, 1e-8, wd, t)
+
+    graph = F.UnitSequence(a).capture(gathers=gathers, fuse_gather=fuse, config=hp(1, 1e-3, 0.0) if variant else None)
+    seq_b = F.UnitSequence(b)
+    t = 0
+    for _ in range(int(rng.integers(1, 4))):
+        t += int(rng.integers(1, 3))
+        lr, wd = float(10 ** rng.uniform(-4, -2)), float(rng.choice([0.0, 0.01, 0.1]))
+        gg = torch.Generator().manual_seed(seed * 100 + t)
+        for ua, ub in zip(a, b):
+            for r in range(ua.world):
+                x = (torch.randn(ua.padded_numel, generator=gg) * 1e-2).to(ua.grads[r].dtype)
+                x[ua.numel:] = 0
+                ua.grads[r].copy_(x)
+                ub.grads[r].copy_(x)
+        graph.launch(hp(t, lr, wd))
+        seq_b.step(hp(t, lr, wd), gathers=gathers, fuse_gather=fuse)
+    torch.cuda.synchronize()
+    for ua, ub in zip(a, b):
+        for name in ("master", "exp_avg", "exp_avg_sq", "shard_out"):
+            x, y = getattr(ua, name), getattr(ub, name)
+            if x is not None:
+                iv = torch.int32 if x.element_size() == 4 else torch.int16
+                assert torch.equal(x.cpu().view(iv), y.cpu().view(iv)), (seed, name)
+        for fa, fb in zip(ua.full, ub.full):
+            iv = torch.int32 if fa.element_size() == 4 else torch.int16
+            assert torch.equal(fa.view(iv), fb.view(iv)), seed
+    graph.close()
