@@ -39,10 +39,10 @@ namespace fsdp {
 namespace rsa {
 
 // Launch shape (compile-time tunables; the defaults are the measured best).
-// Two builds of the kernel differ only in their register budget: with the
-// state in HBM, 3 resident CTAs per SM (<= 80 registers, no spills) stream
-// faster than 2; with the state in host memory, the host link serves the
-// lower request rate of 2 CTAs per SM better.
+// Two builds of the kernel: state in HBM, 3 resident CTAs per SM (<= 80
+// registers, no spills) and 8 consecutive elements per chunk; state in host
+// memory, a 1-CTA launch bound and lane-interleaved chunks (SPLIT below),
+// the layout the host link serves at full rate.
 #ifndef FSDP_RSA_THREADS
 #define FSDP_RSA_THREADS 256
 #endif
@@ -86,9 +86,18 @@ __device__ __forceinline__ uint32_t scalar_elem(const RsaArgs &a, int world, int
     return nonfinite(g);
 }
 
+// Element layout of a thread's 8-element chunk: two 4-element halves at
+// j_lo and j_hi. Consecutive (SPLIT false): j_hi = j_lo + 4, so each state
+// buffer is read as two adjacent 16-byte words per thread. Lane-interleaved
+// (SPLIT true, the build for state in host memory): in a warp's 256-element
+// block lane l owns [4l, 4l + 4) and [128 + 4l, 128 + 4l + 4), so every
+// warp-wide 16-byte state access covers 512 contiguous bytes; over the host
+// link that layout moved twice the bytes of the adjacent-words one (a probe
+// of the two patterns: 280-289 against 130-141 GB/s).
+
 // Average, AdamW and cast of one 8-element chunk whose gradient sum is acc.
-template <int OD, bool GATHER>
-__device__ __forceinline__ uint32_t finish_chunk(const RsaArgs &a, int64_t j0, const float *acc,
+template <int OD, bool GATHER, bool SPLIT>
+__device__ __forceinline__ uint32_t finish_chunk(const RsaArgs &a, int64_t j_lo, int64_t j_hi, const float *acc,
                                                  float4 p0, float4 p1, float4 m0, float4 m1,
                                                  float4 v0, float4 v1) {
     float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
@@ -101,30 +110,39 @@ __device__ __forceinline__ uint32_t finish_chunk(const RsaArgs &a, int64_t j0, c
         bad += nonfinite(g);
         adamw(g, p[e], m[e], v[e], a.s);
     }
-    st_state(a.master + j0, make_float4(p[0], p[1], p[2], p[3]));
-    st_state(a.master + j0 + 4, make_float4(p[4], p[5], p[6], p[7]));
-    st_state(a.m + j0, make_float4(m[0], m[1], m[2], m[3]));
-    st_state(a.m + j0 + 4, make_float4(m[4], m[5], m[6], m[7]));
-    st_state(a.v + j0, make_float4(v[0], v[1], v[2], v[3]));
-    st_state(a.v + j0 + 4, make_float4(v[4], v[5], v[6], v[7]));
+    st_state(a.master + j_lo, make_float4(p[0], p[1], p[2], p[3]));
+    st_state(a.master + j_hi, make_float4(p[4], p[5], p[6], p[7]));
+    st_state(a.m + j_lo, make_float4(m[0], m[1], m[2], m[3]));
+    st_state(a.m + j_hi, make_float4(m[4], m[5], m[6], m[7]));
+    st_state(a.v + j_lo, make_float4(v[0], v[1], v[2], v[3]));
+    st_state(a.v + j_hi, make_float4(v[4], v[5], v[6], v[7]));
     if constexpr (OD == FSDP_F32) {
         const float4 lo = make_float4(p[0], p[1], p[2], p[3]), hi = make_float4(p[4], p[5], p[6], p[7]);
         if (a.out != nullptr) {
-            st_state(static_cast<float *>(a.out) + j0, lo);
-            st_state(static_cast<float *>(a.out) + j0 + 4, hi);
+            st_state(static_cast<float *>(a.out) + j_lo, lo);
+            st_state(static_cast<float *>(a.out) + j_hi, hi);
         }
         if constexpr (GATHER) {
             for (int d = 0; d < a.n_full; ++d) {
-                st_state(static_cast<float *>(a.full[d]) + j0, lo);
-                st_state(static_cast<float *>(a.full[d]) + j0 + 4, hi);
+                st_state(static_cast<float *>(a.full[d]) + j_lo, lo);
+                st_state(static_cast<float *>(a.full[d]) + j_hi, hi);
             }
         }
     } else {
         const uint4 o = make_uint4(pack2<OD>(p[0], p[1]), pack2<OD>(p[2], p[3]),
                                    pack2<OD>(p[4], p[5]), pack2<OD>(p[6], p[7]));
-        if (a.out != nullptr) st_stream(static_cast<uint16_t *>(a.out) + j0, o);
+        auto put = [&](void *base) {
+            uint16_t *b = static_cast<uint16_t *>(base);
+            if constexpr (SPLIT) {
+                st_stream8(b + j_lo, make_uint2(o.x, o.y));
+                st_stream8(b + j_hi, make_uint2(o.z, o.w));
+            } else {
+                st_stream(b + j_lo, o);
+            }
+        };
+        if (a.out != nullptr) put(a.out);
         if constexpr (GATHER) {
-            for (int d = 0; d < a.n_full; ++d) st_stream(static_cast<uint16_t *>(a.full[d]) + j0, o);
+            for (int d = 0; d < a.n_full; ++d) put(a.full[d]);
         }
     }
     return bad;
@@ -137,14 +155,26 @@ template <int NW, int GD> struct GradRegs {
     uint4 w[NW > 0 ? NW : 1][kWords];
 };
 
+// One rank's gradients of a chunk (halves at j_lo and j_hi); bf16/fp16
+// halves are packed into one 16-byte register word.
+template <int GD, bool SPLIT>
+__device__ __forceinline__ void load_grad8(const void *gq, int64_t j_lo, int64_t j_hi, uint4 *w) {
+    if constexpr (GD == FSDP_F32) {
+        w[0] = ld_stream(static_cast<const float *>(gq) + j_lo);
+        w[1] = ld_stream(static_cast<const float *>(gq) + j_hi);
+    } else if constexpr (SPLIT) {
+        const uint2 lo = ld_stream8(static_cast<const uint16_t *>(gq) + j_lo);
+        const uint2 hi = ld_stream8(static_cast<const uint16_t *>(gq) + j_hi);
+        w[0] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    } else {
+        w[0] = ld_stream(static_cast<const uint16_t *>(gq) + j_lo);
+    }
+}
+
+// 8 consecutive elements from j0.
 template <int GD>
 __device__ __forceinline__ void load_grad8(const void *gq, int64_t j0, uint4 *w) {
-    if constexpr (GD == FSDP_F32) {
-        w[0] = ld_stream(static_cast<const float *>(gq) + j0);
-        w[1] = ld_stream(static_cast<const float *>(gq) + j0 + 4);
-    } else {
-        w[0] = ld_stream(static_cast<const uint16_t *>(gq) + j0);
-    }
+    load_grad8<GD, false>(gq, j0, j0 + 4, w);
 }
 
 template <int GD> __device__ __forceinline__ void widen8(const uint4 *w, float *f) {
@@ -157,18 +187,18 @@ template <int GD> __device__ __forceinline__ void widen8(const uint4 *w, float *
     }
 }
 
-template <int NW, int GD, int OD, bool GATHER>
-__device__ __forceinline__ uint32_t vec_chunk(const RsaArgs &a, int world, int64_t j0) {
+template <int NW, int GD, int OD, bool GATHER, bool SPLIT>
+__device__ __forceinline__ uint32_t vec_chunk(const RsaArgs &a, int world, int64_t j_lo, int64_t j_hi) {
     float acc[8];
     if constexpr (NW > 0) {
         // every load of the chunk (N gradient words, then the state) is in
         // flight before the first add
         GradRegs<NW, GD> r;
 #pragma unroll
-        for (int q = 0; q < NW; ++q) load_grad8<GD>(a.grads[q], j0, r.w[q]);
-        const float4 p0 = ld_state(a.master + j0), p1 = ld_state(a.master + j0 + 4);
-        const float4 m0 = ld_state(a.m + j0), m1 = ld_state(a.m + j0 + 4);
-        const float4 v0 = ld_state(a.v + j0), v1 = ld_state(a.v + j0 + 4);
+        for (int q = 0; q < NW; ++q) load_grad8<GD, SPLIT>(a.grads[q], j_lo, j_hi, r.w[q]);
+        const float4 p0 = ld_state(a.master + j_lo), p1 = ld_state(a.master + j_hi);
+        const float4 m0 = ld_state(a.m + j_lo), m1 = ld_state(a.m + j_hi);
+        const float4 v0 = ld_state(a.v + j_lo), v1 = ld_state(a.v + j_hi);
         widen8<GD>(r.w[0], acc);
 #pragma unroll
         for (int q = 1; q < NW; ++q) {
@@ -177,34 +207,47 @@ __device__ __forceinline__ uint32_t vec_chunk(const RsaArgs &a, int world, int64
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
         }
-        return finish_chunk<OD, GATHER>(a, j0, acc, p0, p1, m0, m1, v0, v1);
+        return finish_chunk<OD, GATHER, SPLIT>(a, j_lo, j_hi, acc, p0, p1, m0, m1, v0, v1);
     } else {
         for (int q = 0; q < world; ++q) {
             uint4 w[GradRegs<1, GD>::kWords];
-            load_grad8<GD>(a.grads[q], j0, w);
+            load_grad8<GD, SPLIT>(a.grads[q], j_lo, j_hi, w);
             float f[8];
             widen8<GD>(w, f);
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = q == 0 ? f[e] : __fadd_rn(acc[e], f[e]);
         }
-        const float4 p0 = ld_state(a.master + j0), p1 = ld_state(a.master + j0 + 4);
-        const float4 m0 = ld_state(a.m + j0), m1 = ld_state(a.m + j0 + 4);
-        const float4 v0 = ld_state(a.v + j0), v1 = ld_state(a.v + j0 + 4);
-        return finish_chunk<OD, GATHER>(a, j0, acc, p0, p1, m0, m1, v0, v1);
+        const float4 p0 = ld_state(a.master + j_lo), p1 = ld_state(a.master + j_hi);
+        const float4 m0 = ld_state(a.m + j_lo), m1 = ld_state(a.m + j_hi);
+        const float4 v0 = ld_state(a.v + j_lo), v1 = ld_state(a.v + j_hi);
+        return finish_chunk<OD, GATHER, SPLIT>(a, j_lo, j_hi, acc, p0, p1, m0, m1, v0, v1);
     }
 }
 
 // Grid-stride over nchunks 8-element chunks starting at vbegin, then the
 // scalar elements [begin, vbegin) and [vend, end). With nchunks = 0 and
-// vbegin = vend = end every element takes the scalar path.
-template <int NW, int GD, int OD, bool GATHER, int MINB>
+// vbegin = vend = end every element takes the scalar path. With SPLIT the
+// chunks are lane-interleaved within 256-element warp blocks (nchunks is a
+// multiple of 32, and blockDim and the stride are multiples of 32, so the 32
+// chunks k of a warp share one block).
+template <int NW, int GD, int OD, bool GATHER, int MINB, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, MINB)
     rsa_kernel(const __grid_constant__ RsaArgs a, int64_t vbegin, int64_t nchunks, int64_t vend) {
     const int world = NW > 0 ? NW : a.world;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     uint32_t bad = 0;
-    for (int64_t k = tid; k < nchunks; k += stride) bad += vec_chunk<NW, GD, OD, GATHER>(a, world, vbegin + 8 * k);
+    for (int64_t k = tid; k < nchunks; k += stride) {
+        int64_t j_lo, j_hi;
+        if constexpr (SPLIT) {
+            j_lo = vbegin + 256 * (k >> 5) + 4 * (k & 31);
+            j_hi = j_lo + 128;
+        } else {
+            j_lo = vbegin + 8 * k;
+            j_hi = j_lo + 4;
+        }
+        bad += vec_chunk<NW, GD, OD, GATHER, SPLIT>(a, world, j_lo, j_hi);
+    }
     const int64_t nhead = vbegin - a.begin;
     const int64_t nrest = nhead + (a.end - vend);
     for (int64_t e = tid; e < nrest; e += stride) {

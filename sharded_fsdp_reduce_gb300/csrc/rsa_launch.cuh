@@ -9,9 +9,10 @@
 // range (e.g. 4.97 ms against 5.39-5.53 ms on the 70B unit); one chunk per
 // thread with 3 CTAs per SM is 2.6 % faster again than two chunks with 2
 // (4.994 against 5.127 ms in one process, bit-identical results).
-// Occupancy: the build with 3 resident CTAs per SM for state in HBM, the
-// one with 2 when the master lives in host memory (offload), where the
-// higher request rate measured 20 % slower over the host link.
+// Builds: 3 resident CTAs per SM and consecutive chunks for state in HBM; a
+// 1-CTA launch bound and lane-interleaved chunks (SPLIT) when the master
+// lives in host memory (offload), the layout the host link serves at its
+// full two-way rate (61.6 against 95 ms on the 70B unit).
 #pragma once
 
 #include "host.cuh"
@@ -25,20 +26,23 @@ namespace rsa {
 #endif
 constexpr int kChunksPerThread = FSDP_RSA_CPT;
 
-template <int NW, int GD, int OD, bool GATHER, int MINB>
+template <int NW, int GD, int OD, bool GATHER, int MINB, bool SPLIT>
 fsdp_status launch_grid(const RsaArgs &a, cudaStream_t stream) {
     static std::atomic<int> occupancy{0};
     int blocks_per_sm = 1;
     const fsdp_status so =
-        cached_occupancy(occupancy, rsa_kernel<NW, GD, OD, GATHER, MINB>, kThreads, 0, &blocks_per_sm);
+        cached_occupancy(occupancy, rsa_kernel<NW, GD, OD, GATHER, MINB, SPLIT>, kThreads, 0, &blocks_per_sm);
     if (so != FSDP_OK) return so;
     bool vec = aligned(a.master, 16) && aligned(a.m, 16) && aligned(a.v, 16) && aligned(a.out, 16);
     for (int q = 0; q < a.world; ++q) vec = vec && aligned(a.grads[q], 16);
     for (int d = 0; d < a.n_full; ++d) vec = vec && aligned(a.full[d], 16);
     int64_t vbegin = a.end, vend = a.end, nchunks = 0;
     if (vec) {
+        // the vector part: whole 8-element chunks from an 8-aligned start
+        // (whole 256-element warp blocks with SPLIT)
+        constexpr int64_t kUnit = SPLIT ? 256 : 8;
         vbegin = (a.begin + 7) / 8 * 8;
-        vend = a.end / 8 * 8;
+        vend = vbegin + (a.end > vbegin ? (a.end - vbegin) / kUnit * kUnit : 0);
         if (vend > vbegin) {
             nchunks = (vend - vbegin) / 8;
         } else {
@@ -47,14 +51,14 @@ fsdp_status launch_grid(const RsaArgs &a, cudaStream_t stream) {
     }
     const int64_t items = nchunks + (vbegin - a.begin) + (a.end - vend);
     const int grid = grid_for(items, kThreads, kChunksPerThread, static_cast<int64_t>(sm_count()) * blocks_per_sm);
-    rsa_kernel<NW, GD, OD, GATHER, MINB><<<grid, kThreads, 0, stream>>>(a, vbegin, nchunks, vend);
+    rsa_kernel<NW, GD, OD, GATHER, MINB, SPLIT><<<grid, kThreads, 0, stream>>>(a, vbegin, nchunks, vend);
     return check_launch();
 }
 
 template <int NW, int GD, int OD, bool GATHER>
 fsdp_status launch_typed(const RsaArgs &a, cudaStream_t stream) {
-    return host_resident(a.master) ? launch_grid<NW, GD, OD, GATHER, kMinBlocksHostState>(a, stream)
-                                   : launch_grid<NW, GD, OD, GATHER, kMinBlocks>(a, stream);
+    return host_resident(a.master) ? launch_grid<NW, GD, OD, GATHER, kMinBlocksHostState, true>(a, stream)
+                                   : launch_grid<NW, GD, OD, GATHER, kMinBlocks, false>(a, stream);
 }
 
 template <int GD, int OD, bool GATHER>

@@ -258,3 +258,36 @@ def test_binding_keeps_outputs_in_device_memory(F):
         F.fsdp_reduce_scatter_adam_cast([torch.ones(P, dtype=torch.bfloat16)] * world, *st, out_d, hp)
     torch.cuda.synchronize()
     assert not out_d.any() and not st[0].any()
+
+
+@pytest.mark.parametrize("world,P,rb,re", [(8, 8 * 1000 + 3, 3, 7), (2, 4099, 1, 2), (8, 8 * 40000, 0, 5),
+                                           (4, 4 * 33, 1, 3)])
+def test_offload_rank_subrange_and_ragged_blocks(F, world, P, rb, re):
+    # host state over a rank subrange: the vector part starts off the
+    # 256-element block grid of the host-state layout and ends on a ragged
+    # tail; the blocks outside the range stay untouched
+    P_pad = F.fsdp_padded_numel(P, world)
+    S = P_pad // world
+    g = torch.Generator().manual_seed(world + P)
+    master0 = (torch.rand(P_pad, generator=g) * 0.2 - 0.1)
+    master0[P:] = 0
+    hs = [torch.zeros(P_pad, pin_memory=True) for _ in range(3)]
+    ds = [torch.zeros(P_pad, device=DEV) for _ in range(3)]
+    hs[0].copy_(master0)
+    ds[0].copy_(master0)
+    grads = [torch.zeros(P_pad, dtype=torch.bfloat16, device=DEV) for _ in range(world)]
+    ho, do = (torch.zeros(P_pad, dtype=torch.bfloat16, device=DEV) for _ in range(2))
+    for t in (1, 2):
+        for q in range(world):
+            x = (torch.randn(P_pad, generator=g) * 1e-2).to(torch.bfloat16)
+            x[P:] = 0
+            grads[q].copy_(x)
+        hp = F.AdamWHParams(1e-3, weight_decay=0.01, step=t)
+        F.fsdp_reduce_scatter_adam_cast(grads, *hs, ho, hp, rank_begin=rb, rank_end=re)
+        F.fsdp_reduce_scatter_adam_cast(grads, *ds, do, hp, rank_begin=rb, rank_end=re)
+    torch.cuda.synchronize()
+    for x, y in zip(hs, ds):
+        assert same_bits(x, y)
+    assert same_bits(ho, do)
+    assert torch.equal(hs[0][:rb * S], master0[:rb * S]) and torch.equal(hs[0][re * S:], master0[re * S:])
+    assert not ho[:rb * S].any() and not ho[re * S:].any()
