@@ -28,7 +28,8 @@
 // Same memory schedule as the main kernel: per thread and iteration 8
 // consecutive elements, every load of the chunk issued before any
 // arithmetic, a scalar path for heads, tails and unaligned pointers, and a
-// non-persistent grid of about one chunk per thread.
+// non-persistent grid of about one chunk per thread; for state in host
+// memory the chunks are lane-interleaved within 256-element warp blocks.
 #pragma once
 
 #include "host.cuh"
@@ -40,8 +41,9 @@ namespace step {
 // Launch shape as the main kernel: one chunk per thread, not persistent;
 // 3 resident CTAs per SM with the state in HBM (measured in the bench on the
 // 70B unit against two chunks at 2 CTAs per SM: the bf16 reduction 5.31 ->
-// 4.97 ms, Adadelta 4.98 -> 4.90 ms, the others within 1 %), 2 with the
-// parameter in host memory.
+// 4.97 ms, Adadelta 4.98 -> 4.90 ms, the others within 1 %); with the
+// parameter in host memory a 1-CTA launch bound and lane-interleaved chunks,
+// as the fused AdamW kernel's host-state build.
 #ifndef FSDP_STEP_CPT
 #define FSDP_STEP_CPT 1
 #endif
@@ -98,58 +100,69 @@ template <int GD> __device__ __forceinline__ float round_to(float x) {
     else return x;
 }
 
-// 8 consecutive values of a buffer in dtype DT <-> floats.
+// The 8 values of a chunk in a buffer of dtype DT <-> floats: halves at
+// j_lo and j_hi (consecutive: j_hi = j_lo + 4; SPLIT: the host-state build's
+// lane-interleaved chunks, as in the fused AdamW kernel).
 template <int DT> struct Words { uint4 w[DT == FSDP_F32 ? 2 : 1]; };
 
-template <int DT, bool STATE> __device__ __forceinline__ Words<DT> load8(const void *base, int64_t j0) {
+__device__ __forceinline__ uint2 ld_state8(const void *p) {
+    uint2 r;
+    asm volatile("ld.global.cs.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+template <int DT, bool SPLIT>
+__device__ __forceinline__ Words<DT> load_state8(const void *base, int64_t j_lo, int64_t j_hi) {
     Words<DT> r;
     if constexpr (DT == FSDP_F32) {
-        const float *p = static_cast<const float *>(base) + j0;
-        if constexpr (STATE) {
-            const float4 a = ld_state(p), b = ld_state(p + 4);
-            r.w[0] = make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(a.z), __float_as_uint(a.w));
-            r.w[1] = make_uint4(__float_as_uint(b.x), __float_as_uint(b.y), __float_as_uint(b.z), __float_as_uint(b.w));
-        } else {
-            r.w[0] = ld_stream(p);
-            r.w[1] = ld_stream(p + 4);
-        }
+        const float *p = static_cast<const float *>(base);
+        const float4 a = ld_state(p + j_lo), b = ld_state(p + j_hi);
+        r.w[0] = make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(a.z), __float_as_uint(a.w));
+        r.w[1] = make_uint4(__float_as_uint(b.x), __float_as_uint(b.y), __float_as_uint(b.z), __float_as_uint(b.w));
+    } else if constexpr (SPLIT) {
+        const uint16_t *p = static_cast<const uint16_t *>(base);
+        const uint2 lo = ld_state8(p + j_lo), hi = ld_state8(p + j_hi);
+        r.w[0] = make_uint4(lo.x, lo.y, hi.x, hi.y);
     } else {
-        const uint16_t *p = static_cast<const uint16_t *>(base) + j0;
-        if constexpr (STATE) {
-            const float4 a = ld_state(reinterpret_cast<const float *>(p));
-            r.w[0] = make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(a.z), __float_as_uint(a.w));
-        } else {
-            r.w[0] = ld_stream(p);
-        }
+        const float4 a = ld_state(reinterpret_cast<const float *>(static_cast<const uint16_t *>(base) + j_lo));
+        r.w[0] = make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(a.z), __float_as_uint(a.w));
     }
     return r;
 }
 
 template <int DT> __device__ __forceinline__ void widen(const Words<DT> &x, float *f) { rsa::widen8<DT>(x.w, f); }
 
-template <int DT> __device__ __forceinline__ void store8(void *base, int64_t j0, const float *f) {
+template <int DT, bool SPLIT>
+__device__ __forceinline__ void store8(void *base, int64_t j_lo, int64_t j_hi, const float *f) {
     if constexpr (DT == FSDP_F32) {
-        float *p = static_cast<float *>(base) + j0;
-        st_state(p, make_float4(f[0], f[1], f[2], f[3]));
-        st_state(p + 4, make_float4(f[4], f[5], f[6], f[7]));
+        float *p = static_cast<float *>(base);
+        st_state(p + j_lo, make_float4(f[0], f[1], f[2], f[3]));
+        st_state(p + j_hi, make_float4(f[4], f[5], f[6], f[7]));
     } else {
-        st_stream(static_cast<uint16_t *>(base) + j0,
-                  make_uint4(pack2<DT>(f[0], f[1]), pack2<DT>(f[2], f[3]), pack2<DT>(f[4], f[5]), pack2<DT>(f[6], f[7])));
+        const uint4 o = make_uint4(pack2<DT>(f[0], f[1]), pack2<DT>(f[2], f[3]), pack2<DT>(f[4], f[5]),
+                                   pack2<DT>(f[6], f[7]));
+        uint16_t *b = static_cast<uint16_t *>(base);
+        if constexpr (SPLIT) {
+            st_stream8(b + j_lo, make_uint2(o.x, o.y));
+            st_stream8(b + j_hi, make_uint2(o.z, o.w));
+        } else {
+            st_stream(b + j_lo, o);
+        }
     }
 }
 
-template <int OPT, int NW, int GD, int OD, int SD>
-__device__ __forceinline__ uint32_t vec_chunk(const StepArgs &a, int world, int64_t j0) {
+template <int OPT, int NW, int GD, int OD, int SD, bool SPLIT>
+__device__ __forceinline__ uint32_t vec_chunk(const StepArgs &a, int world, int64_t j_lo, int64_t j_hi) {
     constexpr int K = Opt<OPT>::kStates;
     float acc[8];
     Words<SD> pw, s0w, s1w;
     if constexpr (NW > 0) {
         rsa::GradRegs<NW, GD> r;
 #pragma unroll
-        for (int q = 0; q < NW; ++q) rsa::load_grad8<GD>(a.grads[q], j0, r.w[q]);
-        pw = load8<SD, true>(a.param, j0);
-        s0w = load8<SD, true>(a.s0, j0);
-        if constexpr (K == 2) s1w = load8<SD, true>(a.s1, j0);
+        for (int q = 0; q < NW; ++q) rsa::load_grad8<GD, SPLIT>(a.grads[q], j_lo, j_hi, r.w[q]);
+        pw = load_state8<SD, SPLIT>(a.param, j_lo, j_hi);
+        s0w = load_state8<SD, SPLIT>(a.s0, j_lo, j_hi);
+        if constexpr (K == 2) s1w = load_state8<SD, SPLIT>(a.s1, j_lo, j_hi);
         rsa::widen8<GD>(r.w[0], acc);
 #pragma unroll
         for (int q = 1; q < NW; ++q) {
@@ -164,7 +177,7 @@ __device__ __forceinline__ uint32_t vec_chunk(const StepArgs &a, int world, int6
     } else {
         for (int q = 0; q < world; ++q) {
             uint4 w[rsa::GradRegs<1, GD>::kWords];
-            rsa::load_grad8<GD>(a.grads[q], j0, w);
+            rsa::load_grad8<GD, SPLIT>(a.grads[q], j_lo, j_hi, w);
             float f[8];
             rsa::widen8<GD>(w, f);
 #pragma unroll
@@ -177,9 +190,9 @@ __device__ __forceinline__ uint32_t vec_chunk(const StepArgs &a, int world, int6
                 }
             }
         }
-        pw = load8<SD, true>(a.param, j0);
-        s0w = load8<SD, true>(a.s0, j0);
-        if constexpr (K == 2) s1w = load8<SD, true>(a.s1, j0);
+        pw = load_state8<SD, SPLIT>(a.param, j_lo, j_hi);
+        s0w = load_state8<SD, SPLIT>(a.s0, j_lo, j_hi);
+        if constexpr (K == 2) s1w = load_state8<SD, SPLIT>(a.s1, j_lo, j_hi);
     }
     float p[8], s0[8], s1[8];
     widen<SD>(pw, p);
@@ -197,10 +210,10 @@ __device__ __forceinline__ uint32_t vec_chunk(const StepArgs &a, int world, int6
         bad += rsa::nonfinite(g);
         update<OPT>(g, p[e], s0[e], s1[e], a.k);
     }
-    store8<SD>(a.param, j0, p);
-    store8<SD>(a.s0, j0, s0);
-    if constexpr (K == 2) store8<SD>(a.s1, j0, s1);
-    if constexpr (SD == FSDP_F32) store8<OD>(a.out, j0, p);
+    store8<SD, SPLIT>(a.param, j_lo, j_hi, p);
+    store8<SD, SPLIT>(a.s0, j_lo, j_hi, s0);
+    if constexpr (K == 2) store8<SD, SPLIT>(a.s1, j_lo, j_hi, s1);
+    if constexpr (SD == FSDP_F32) store8<OD, SPLIT>(a.out, j_lo, j_hi, p);
     return bad;
 }
 
@@ -223,14 +236,24 @@ __device__ __forceinline__ uint32_t scalar_elem(const StepArgs &a, int world, in
     return rsa::nonfinite(g);
 }
 
-template <int OPT, int NW, int GD, int OD, int SD, int MINB>
+template <int OPT, int NW, int GD, int OD, int SD, int MINB, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, MINB)
     step_kernel(const __grid_constant__ StepArgs a, int64_t vbegin, int64_t nchunks, int64_t vend) {
     const int world = NW > 0 ? NW : a.world;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     uint32_t bad = 0;
-    for (int64_t c = tid; c < nchunks; c += stride) bad += vec_chunk<OPT, NW, GD, OD, SD>(a, world, vbegin + 8 * c);
+    for (int64_t c = tid; c < nchunks; c += stride) {
+        int64_t j_lo, j_hi;
+        if constexpr (SPLIT) {  // lane-interleaved 256-element warp blocks
+            j_lo = vbegin + 256 * (c >> 5) + 4 * (c & 31);
+            j_hi = j_lo + 128;
+        } else {
+            j_lo = vbegin + 8 * c;
+            j_hi = j_lo + 4;
+        }
+        bad += vec_chunk<OPT, NW, GD, OD, SD, SPLIT>(a, world, j_lo, j_hi);
+    }
     const int64_t nhead = vbegin - a.begin;
     const int64_t nrest = nhead + (a.end - vend);
     for (int64_t e = tid; e < nrest; e += stride) {
@@ -243,19 +266,20 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
 }
 
-template <int OPT, int NW, int GD, int OD, int SD, int MINB>
+template <int OPT, int NW, int GD, int OD, int SD, int MINB, bool SPLIT>
 fsdp_status launch_grid(const StepArgs &a, cudaStream_t stream) {
     static std::atomic<int> occupancy{0};
     int blocks_per_sm = 1;
     const fsdp_status so =
-        cached_occupancy(occupancy, step_kernel<OPT, NW, GD, OD, SD, MINB>, kThreads, 0, &blocks_per_sm);
+        cached_occupancy(occupancy, step_kernel<OPT, NW, GD, OD, SD, MINB, SPLIT>, kThreads, 0, &blocks_per_sm);
     if (so != FSDP_OK) return so;
     bool vec = aligned(a.param, 16) && aligned(a.s0, 16) && aligned(a.s1, 16) && aligned(a.out, 16);
     for (int q = 0; q < a.world; ++q) vec = vec && aligned(a.grads[q], 16);
     int64_t vbegin = a.end, vend = a.end, nchunks = 0;
     if (vec) {
+        constexpr int64_t kUnit = SPLIT ? 256 : 8;  // whole chunks (whole warp blocks with SPLIT)
         vbegin = (a.begin + 7) / 8 * 8;
-        vend = a.end / 8 * 8;
+        vend = vbegin + (a.end > vbegin ? (a.end - vbegin) / kUnit * kUnit : 0);
         if (vend > vbegin) {
             nchunks = (vend - vbegin) / 8;
         } else {
@@ -264,14 +288,14 @@ fsdp_status launch_grid(const StepArgs &a, cudaStream_t stream) {
     }
     const int64_t items = nchunks + (vbegin - a.begin) + (a.end - vend);
     const int grid = grid_for(items, kThreads, kChunksPerThread, static_cast<int64_t>(sm_count()) * blocks_per_sm);
-    step_kernel<OPT, NW, GD, OD, SD, MINB><<<grid, kThreads, 0, stream>>>(a, vbegin, nchunks, vend);
+    step_kernel<OPT, NW, GD, OD, SD, MINB, SPLIT><<<grid, kThreads, 0, stream>>>(a, vbegin, nchunks, vend);
     return check_launch();
 }
 
 template <int OPT, int NW, int GD, int OD, int SD>
 fsdp_status launch_typed(const StepArgs &a, cudaStream_t stream) {
-    return host_resident(a.param) ? launch_grid<OPT, NW, GD, OD, SD, kMinBlocksHostState>(a, stream)
-                                  : launch_grid<OPT, NW, GD, OD, SD, kMinBlocks>(a, stream);
+    return host_resident(a.param) ? launch_grid<OPT, NW, GD, OD, SD, kMinBlocksHostState, true>(a, stream)
+                                  : launch_grid<OPT, NW, GD, OD, SD, kMinBlocks, false>(a, stream);
 }
 
 template <int OPT, int GD, int OD, int SD>

@@ -291,3 +291,42 @@ def test_offload_rank_subrange_and_ragged_blocks(F, world, P, rb, re):
     assert same_bits(ho, do)
     assert torch.equal(hs[0][:rb * S], master0[:rb * S]) and torch.equal(hs[0][re * S:], master0[re * S:])
     assert not ho[:rb * S].any() and not ho[re * S:].any()
+
+
+@pytest.mark.parametrize("opt,sdt", [("sgd", torch.float32), ("adamax", torch.float32), ("adamw", torch.bfloat16),
+                                     ("adadelta", torch.float16)])
+def test_offload_variant_rank_subrange(F, opt, sdt):
+    # the variant kernels' host-state build (lane-interleaved chunks) over a
+    # rank subrange that starts off the 256-element block grid
+    world, P, rb, re = 8, 8 * 3000 + 5, 3, 7
+    P_pad = F.fsdp_padded_numel(P, world)
+    S = P_pad // world
+    ns = 1 if opt == "sgd" else 2
+    g = torch.Generator().manual_seed(P + ns)
+    p0 = (torch.rand(P_pad, generator=g) * 0.2 - 0.1).to(sdt)
+    p0[P:] = 0
+    gdt = torch.float16 if sdt == torch.float16 else torch.bfloat16
+    hs = [torch.zeros(P_pad, dtype=sdt, pin_memory=True) for _ in range(1 + ns)]
+    ds = [torch.zeros(P_pad, dtype=sdt, device=DEV) for _ in range(1 + ns)]
+    hs[0].copy_(p0)
+    ds[0].copy_(p0)
+    out_h = torch.zeros(P_pad, dtype=torch.bfloat16, device=DEV) if sdt == torch.float32 else None
+    out_d = torch.zeros(P_pad, dtype=torch.bfloat16, device=DEV) if sdt == torch.float32 else None
+    grads = [torch.zeros(P_pad, dtype=gdt, device=DEV) for _ in range(world)]
+    lr = 1.0 if opt == "adadelta" else 1e-3
+    for t in (1, 2):
+        for q in range(world):
+            x = (torch.randn(P_pad, generator=g) * 1e-2).to(gdt)
+            x[P:] = 0
+            grads[q].copy_(x)
+        cfg = F.StepConfig(opt, lr, weight_decay=0.01, step=t)
+        F.fsdp_reduce_scatter_step(grads, hs[0], hs[1], hs[2] if ns == 2 else None, out_h, cfg, rank_begin=rb,
+                                   rank_end=re)
+        F.fsdp_reduce_scatter_step(grads, ds[0], ds[1], ds[2] if ns == 2 else None, out_d, cfg, rank_begin=rb,
+                                   rank_end=re)
+    torch.cuda.synchronize()
+    for x, y in zip(hs, ds):
+        assert same_bits(x, y), opt
+    if out_h is not None:
+        assert same_bits(out_h, out_d)
+    assert same_bits(hs[0][:rb * S], p0[:rb * S]) and same_bits(hs[0][re * S:], p0[re * S:])
