@@ -306,3 +306,50 @@ def test_captured_step_refusals(F):
     v = F.FlatParamUnit([("w", (64,))], 2, torch.bfloat16, torch.bfloat16, device=DEV, optimizer="sgd")
     with pytest.raises(ValueError):  # the captured step is the fused AdamW step
         F.UnitSequence([v]).capture()
+
+
+def test_resources_are_released(F):
+    # captured steps created and destroyed, and short-lived host threads that
+    # each create their side streams and events and exit: device memory
+    # returns to where it started and every step still matches the driver
+    import threading
+    a = [u for u in build_model(F, 30) if u.grads[0].dtype != torch.float16]
+    b = [u for u in build_model(F, 30) if u.grads[0].dtype != torch.float16]
+    seq_b = F.UnitSequence(b)
+    load_grads(a, 1, 31)
+    load_grads(b, 1, 31)
+    warm = F.UnitSequence(a).capture(gathers=1)  # first capture and launch of these builds
+    warm.close()
+    torch.cuda.Stream()  # torch's stream pool is set up on first use (not the library's memory)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    free0, _ = torch.cuda.mem_get_info()
+    for t in range(1, 41):
+        graph = F.UnitSequence(a).capture(gathers=1)
+        graph.launch(hp_for(F, a[0], t))
+        graph.close()
+        seq_b.step(hp_for(F, b[0], t), gathers=1)
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(t):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                F.UnitSequence(a).step(hp_for(F, a[0], t), gathers=1, stream=s)
+            s.synchronize()
+        except Exception as e:  # surfaced below
+            errors.append(e)
+
+    for t in range(41, 61):  # one thread per step, run one after another
+        th = threading.Thread(target=worker, args=(t,))
+        th.start()
+        th.join()
+        seq_b.step(hp_for(F, b[0], t), gathers=1)
+    torch.cuda.synchronize()
+    assert not errors, errors
+    torch.cuda.empty_cache()
+    free1, _ = torch.cuda.mem_get_info()
+    assert abs(free1 - free0) < 8 << 20, (free0, free1)
+    for ua, ub in zip(a, b):
+        assert same(ua.master, ub.master) and same(ua.full[0], ub.full[0])
