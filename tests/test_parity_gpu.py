@@ -115,8 +115,9 @@ def _sample_indices(P_pad, N, k, seed):
     return np.unique(np.concatenate(idx)).astype(np.int64)
 
 
-@pytest.mark.parametrize("name", ["gpt3_13b", "llama70b"])
-def test_full_size_sampled(F, orc, name):
+@pytest.mark.parametrize("name,fuse", [("gpt3_13b", False), ("llama70b", False), ("gpt3_13b", True)])
+def test_full_size_sampled(F, orc, name, fuse):
+    # fuse: the first all-gather written by the update kernel itself (f1)
     cfg = fi.CONFIGS[name]
     N = cfg.world
     unit = new_unit(F, cfg)
@@ -133,7 +134,7 @@ def test_full_size_sampled(F, orc, name):
             unit.load_grad(r, [g])
             del g
         g_s = [host(unit.grads[r][idx_t]) for r in range(N)]
-        unit.step(hp_for(F, cfg, t), gathers=cfg.gathers)
+        unit.step(hp_for(F, cfg, t), gathers=cfg.gathers, fuse_gather=fuse)
         s = orc.scalars(ohp_for(orc, cfg, t), N)
         g_avg = orc.all_reduce_avg(g_s, cfg.grad_dtype, N, s.c)
         orc.adamw(p_s, m_s, v_s, g_avg, s)
