@@ -389,11 +389,228 @@ def workload_config(args):
     return cfg, name
 
 
+class _Run:
+    """State shared by the legs of one bench run: the unit, its step counter
+    (every launch takes the next step t), the stream, the L2 flush and the
+    count of the library's launches inside timed regions."""
+
+    def __init__(self, args, dev, rank, world_size):
+        import torch
+
+        import fsdp_inputs as fi
+        import sharded_fsdp_reduce_gb300 as F
+
+        self.args, self.dev, self.rank, self.world_size = args, dev, rank, world_size
+        self.torch, self.F, self.fi = torch, F, fi
+        self.cfg, self.workload = workload_config(args)
+        cfg = self.cfg
+        self.N = cfg.world
+        self.gdt, self.odt = fi.torch_dtype(cfg.grad_dtype), fi.torch_dtype(cfg.out_dtype)
+        self.unit = F.FlatParamUnit(cfg.params, self.N, self.gdt, self.odt, device=dev)
+        self.P_pad = self.unit.padded_numel
+        seed = 100_000 * rank  # each GPU owns a different unit
+        self.unit.load_master([fi.gen_master(cfg, device=dev, seed_base=seed)])
+        for r in range(self.N):
+            self.unit.load_grad(r, [fi.gen_grad(cfg, r, 1, device=dev, seed_base=seed)])
+        torch.cuda.synchronize()
+        self.rsa_b, self.ag_b = self.unit.step_bytes(cfg.gathers)
+        self.stream = torch.cuda.current_stream()
+        self.K = args.steps
+        self.flush = L2Flush(dev, self.rsa_b)
+        self.t = 0
+        self.launches = 0
+
+    def hp(self, t):
+        c = self.cfg
+        return self.F.AdamWHParams(c.lr, c.beta1, c.beta2, c.eps, c.weight_decay, t, c.grad_scale)
+
+    def next_hp(self):
+        self.t += 1
+        return self.hp(self.t)
+
+    def barrier(self):
+        if self.world_size > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+
+def time_steps(run: _Run):
+    """The timed region: K steps (fused kernel + gathers) after W warm-up
+    steps; device time by CUDA events on the launching stream, clocks
+    sampled meanwhile. Returns (step ms, fused-kernel ms, clock summary)."""
+    torch, unit, cfg, K, flush, stream = run.torch, run.unit, run.cfg, run.K, run.flush, run.stream
+    for _ in range(run.args.warmup):
+        unit.step(run.next_hp(), gathers=cfg.gathers)
+    torch.cuda.synchronize()
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(run.dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clocks:
+        time.sleep(0.25)  # let the sampler start before the timed launches
+        start.record(stream)
+        for i in range(K):
+            hp = run.next_hp()
+            flush()
+            ev[i][0].record(stream)
+            unit.reduce_scatter_adam_cast(hp)
+            ev[i][1].record(stream)
+            for _ in range(cfg.gathers):
+                unit.all_gather()
+            ev[i][2].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    run.barrier()
+    if flush.active:  # the flushes between steps are not step time
+        step_ms = sum(a.elapsed_time(c) for a, _, c in ev) / K
+    else:
+        step_ms = start.elapsed_time(end) / K
+    rsa_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / K
+    run.launches += K * (1 + cfg.gathers)
+    return step_ms, rsa_ms, clocks.summary()
+
+
+def time_e2e(run: _Run):
+    """End to end through the binding's host-buffer step: every step copies
+    its N gradient buffers in from pinned host memory and reads the step's
+    result back, its non-finite-gradient count (the metric a trainer checks
+    every step; the gathered parameters stay on the GPU for the next
+    forward), or with --e2e-read-params the compute-dtype parameters.
+    Consecutive steps overlap their copies and kernels. Every rank runs it or
+    none does. Returns (ms per step, steps, h2d bytes, d2h bytes, reason it
+    is unavailable or None)."""
+    torch, unit, cfg, args, dev = run.torch, run.unit, run.cfg, run.args, run.dev
+    Ke = max(3, min(args.e2e_steps, run.K))
+    unavailable = None
+    try:  # N gradient buffers of pinned host memory (13.7 GB for the 70B unit)
+        host_grads = [torch.empty(run.P_pad, dtype=run.gdt, pin_memory=True) for _ in range(run.N)]
+    except RuntimeError as e:
+        host_grads, unavailable = None, "pinned host buffers: " + str(e).splitlines()[0][:160]
+    if run.world_size > 1:
+        import torch.distributed as dist
+        ok = torch.tensor([0 if host_grads is None else 1], device=dev)
+        dist.all_reduce(ok, op=dist.ReduceOp.MIN)
+        if int(ok.item()) == 0 and host_grads is not None:
+            host_grads, unavailable = None, "another rank could not pin its host buffers"
+    if host_grads is None:
+        return 0.0, Ke, 0, 0, unavailable
+    for r in range(run.N):
+        host_grads[r].copy_(unit.grads[r])
+    counter = torch.zeros(1, dtype=torch.int32, device=dev)
+    if args.e2e_read_params:
+        host_out, host_nf = torch.empty(run.P_pad, dtype=run.odt, pin_memory=True), None
+        d2h = host_out.numel() * host_out.element_size()
+    else:
+        host_out, host_nf = None, torch.zeros(1, dtype=torch.int32, pin_memory=True)
+        d2h = host_nf.numel() * host_nf.element_size()
+    h2d = sum(g.numel() * g.element_size() for g in host_grads)
+    unit.step_from_host(host_grads, host_out, run.next_hp(), gathers=cfg.gathers, nonfinite_count=counter,
+                        host_nonfinite=host_nf)  # sets up the streams
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    run.barrier()
+    e0.record(run.stream)
+    for _ in range(Ke):
+        unit.step_from_host(host_grads, host_out, run.next_hp(), gathers=cfg.gathers, nonfinite_count=counter,
+                            host_nonfinite=host_nf)
+    e1.record(run.stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    if host_nf is not None and int(host_nf.item()) != 0:
+        raise RuntimeError("e2e steps reported non-finite gradients")
+    run.launches += Ke * (1 + cfg.gathers)
+    return e2e_ms, Ke, h2d, d2h, None
+
+
+def time_fused_gather_variants(run: _Run):
+    """The same step with the first all-gather fused into the update kernel,
+    and the no-reshard mode (one gather, fused, kept for forward and
+    backward); both on the default step's byte model."""
+    unit, K = run.unit, run.K
+    variants = {}
+    for vname, vg in (("fused_gather", run.cfg.gathers), ("no_reshard_fused", 1)):
+        for _ in range(3):
+            unit.step(run.next_hp(), gathers=vg, fuse_gather=True)
+        t0 = run.t
+        vms = timed_calls(lambda i, vg=vg: unit.step(run.hp(t0 + 1 + i), gathers=vg, fuse_gather=True),
+                          K, run.stream, run.flush)
+        run.t += K
+        run.launches += K * vg
+        variants[vname] = {"gathers_per_step": vg, "ms_per_step": round(vms, 4)}
+    return variants
+
+
+def time_variant_kernels(run: _Run):
+    """The variant steps' kernels on the same unit, each on its own byte
+    model: N*grad + (1 + states)*(read + write) + out, each optimizer from its
+    own zero state."""
+    torch, F, unit, cfg, dev, P, N = run.torch, run.F, run.unit, run.cfg, run.dev, run.P_pad, run.N
+    gb = unit.grads[0].element_size()
+    low = [unit.master.to(torch.bfloat16), torch.zeros(P, dtype=torch.bfloat16, device=dev),
+           torch.zeros(P, dtype=torch.bfloat16, device=dev)]
+    vsets = {
+        "adamw_grad_dtype_reduce": ("adamw", True, unit.master, unit.exp_avg, unit.exp_avg_sq, unit.shard_out),
+        "adamw_bf16_state": ("adamw", False, low[0], low[1], low[2], None),
+        "sgd_momentum": ("sgd", False, unit.master, unit.exp_avg, None, unit.shard_out),
+        "adamax": ("adamax", False, unit.master, unit.exp_avg, unit.exp_avg_sq, unit.shard_out),
+        "adadelta": ("adadelta", False, unit.master, unit.exp_avg, unit.exp_avg_sq, unit.shard_out),
+    }
+    kernels = {}
+    for vname, (opt, lowp, prm, s0, s1, out) in vsets.items():
+        ss = prm.element_size()
+        nstates = 1 + (s0 is not None) + (s1 is not None)
+        nbytes = P * (N * gb + nstates * 2 * ss + (out.element_size() if out is not None else 0))
+        lrv = 1.0 if opt == "adadelta" else cfg.lr
+        for st in (s0, s1):
+            if st is not None:
+                st.zero_()
+
+        def launch(tt, opt=opt, lowp=lowp, prm=prm, s0=s0, s1=s1, out=out, lrv=lrv):
+            F.fsdp_reduce_scatter_step(unit.grads, prm, s0, s1, out,
+                                       F.StepConfig(opt, lrv, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay,
+                                                    tt, cfg.grad_scale, reduce_dtype=run.gdt if lowp else None))
+        for i in range(3):
+            launch(i + 1)
+        kms = timed_calls(lambda i, launch=launch: launch(i + 4), run.K, run.stream, run.flush)
+        run.launches += run.K
+        kernels[vname] = {"ms": round(kms, 4), "bytes_per_launch": nbytes,
+                          "achieved_GBs": round(nbytes / (kms * 1e-3) / 1e9, 1)}
+    return kernels
+
+
+def time_offload(run: _Run, rsa_ms: float):
+    """The offload mode: master, m and v in pinned host memory, updated in
+    place by the same fused kernel over the host link (12 B read and 12 B
+    written per element there; gradients and the shard stay in HBM)."""
+    torch, F, unit, P = run.torch, run.F, run.unit, run.P_pad
+    try:
+        hstate = [torch.zeros(P, dtype=torch.float32, pin_memory=True) for _ in range(3)]
+    except RuntimeError as e:  # not enough page-locked host memory
+        return {"unavailable": str(e).splitlines()[0][:200]}
+    hstate[0].copy_(unit.master)
+    torch.cuda.synchronize()
+
+    def launch(i):
+        F.fsdp_reduce_scatter_adam_cast(unit.grads, *hstate, unit.shard_out, run.hp(i + 1))
+
+    for i in range(3):
+        launch(i)
+    Ko = max(3, min(run.K, 5))
+    oms = timed_calls(lambda i: launch(i + 3), Ko, run.stream, run.flush)
+    run.launches += Ko
+    link_b = P * 3 * (4 + 4)
+    hbm_b = P * (run.N * unit.grads[0].element_size() + unit.shard_out.element_size())
+    return {"ms": round(oms, 3), "launches": Ko, "host_link_bytes_per_launch": link_b,
+            "hbm_bytes_per_launch": hbm_b,
+            "host_link_GBs": round(link_b / (oms * 1e-3) / 1e9, 1),
+            "host_link_GBs_per_direction": round(link_b / 2 / (oms * 1e-3) / 1e9, 1),
+            "slowdown_vs_device_state": round(oms / rsa_ms, 2)}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
-    import fsdp_inputs as fi
     import sharded_fsdp_reduce_gb300 as F
     from sharded_fsdp_reduce_gb300 import build as _build
 
@@ -410,197 +627,18 @@ def run_ours(args):
         dist.barrier()
     F._lib.load()
 
-    cfg, workload = workload_config(args)
-    N = cfg.world
-    gdt, odt = fi.torch_dtype(cfg.grad_dtype), fi.torch_dtype(cfg.out_dtype)
-    unit = F.FlatParamUnit(cfg.params, N, gdt, odt, device=dev)
-    P_pad = unit.padded_numel
-    seed = 100_000 * rank  # each GPU owns a different unit
-    unit.load_master([fi.gen_master(cfg, device=dev, seed_base=seed)])
-    for r in range(N):
-        unit.load_grad(r, [fi.gen_grad(cfg, r, 1, device=dev, seed_base=seed)])
-    torch.cuda.synchronize()
-    rsa_b, ag_b = unit.step_bytes(cfg.gathers)
-
-    def hp(t):
-        return F.AdamWHParams(cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay, t, cfg.grad_scale)
-
-    stream = torch.cuda.current_stream()
-    t = 0
-    for _ in range(args.warmup):
-        t += 1
-        unit.step(hp(t), gathers=cfg.gathers)
-    torch.cuda.synchronize()
-
-    # ---- timed region (device time, CUDA events on the launching stream)
-    K = args.steps
-    flush = L2Flush(dev, rsa_b)
-    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world_size > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clocks:
-        time.sleep(0.25)  # let the sampler start before the timed launches
-        start.record(stream)
-        for i in range(K):
-            t += 1
-            flush()
-            ev[i][0].record(stream)
-            unit.reduce_scatter_adam_cast(hp(t))
-            ev[i][1].record(stream)
-            for _ in range(cfg.gathers):
-                unit.all_gather()
-            ev[i][2].record(stream)
-        end.record(stream)
-        torch.cuda.synchronize()
-    if world_size > 1:
-        dist.barrier()
-    if flush.active:  # the flushes between steps are not step time
-        step_ms = sum(a.elapsed_time(c) for a, _, c in ev) / K
-    else:
-        step_ms = start.elapsed_time(end) / K
-    rsa_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / K
-    launches = K * (1 + cfg.gathers)  # kernels of ours in the timed regions (device step, then e2e)
-
-    # ---- end to end through the binding's host-buffer step: every step copies
-    # its N gradient buffers in from pinned host memory and reads the step's
-    # result back: its non-finite-gradient count (the metric a trainer checks
-    # every step; the gathered parameters stay on the GPU for the next
-    # forward). --e2e-read-params reads the compute-dtype parameters instead.
-    # Consecutive steps overlap their copies and kernels.
-    Ke = max(3, min(args.e2e_steps, K))
-    e2e_ms, e2e_unavailable = 0.0, None
-    try:  # N gradient buffers of pinned host memory (13.7 GB for the 70B unit)
-        host_grads = [torch.empty(P_pad, dtype=gdt, pin_memory=True) for _ in range(N)]
-    except RuntimeError as e:
-        host_grads, e2e_unavailable = None, "pinned host buffers: " + str(e).splitlines()[0][:160]
-    if world_size > 1:  # every rank runs the e2e steps or none does
-        ok = torch.tensor([0 if host_grads is None else 1], device=dev)
-        dist.all_reduce(ok, op=dist.ReduceOp.MIN)
-        if int(ok.item()) == 0 and host_grads is not None:
-            host_grads, e2e_unavailable = None, "another rank could not pin its host buffers"
-    h2d = d2h = 0
-    if host_grads is not None:
-        for r in range(N):
-            host_grads[r].copy_(unit.grads[r])
-        counter = torch.zeros(1, dtype=torch.int32, device=dev)
-        if args.e2e_read_params:
-            host_out, host_nf = torch.empty(P_pad, dtype=odt, pin_memory=True), None
-            d2h = host_out.numel() * host_out.element_size()
-        else:
-            host_out, host_nf = None, torch.zeros(1, dtype=torch.int32, pin_memory=True)
-            d2h = host_nf.numel() * host_nf.element_size()
-        h2d = sum(g.numel() * g.element_size() for g in host_grads)
-        t += 1
-        unit.step_from_host(host_grads, host_out, hp(t), gathers=cfg.gathers, nonfinite_count=counter,
-                            host_nonfinite=host_nf)  # sets up the streams
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        if world_size > 1:
-            dist.barrier()
-        e0.record(stream)
-        for _ in range(Ke):
-            t += 1
-            unit.step_from_host(host_grads, host_out, hp(t), gathers=cfg.gathers, nonfinite_count=counter,
-                                host_nonfinite=host_nf)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / Ke
-        if host_nf is not None and int(host_nf.item()) != 0:
-            raise RuntimeError("e2e steps reported non-finite gradients")
-        launches += Ke * (1 + cfg.gathers)
-        del host_grads, host_out, host_nf
-
-    # ---- variants of the same step (same byte model): the first all-gather
-    # fused into the update kernel; and the no-reshard mode (one gather kept
-    # for forward and backward, fused)
-    variants = {}
-    if not args.no_variants:
-        for vname, vg in (("fused_gather", cfg.gathers), ("no_reshard_fused", 1)):
-            for _ in range(3):
-                t += 1
-                unit.step(hp(t), gathers=vg, fuse_gather=True)
-            t0 = t
-            vms = timed_calls(lambda i, vg=vg: unit.step(hp(t0 + 1 + i), gathers=vg, fuse_gather=True),
-                              K, stream, flush)
-            t += K
-            launches += K * vg
-            variants[vname] = {"gathers_per_step": vg, "ms_per_step": round(vms, 4)}
-
-    # ---- the variant steps' kernels on the same unit (each on its own byte
-    # model: N*grad + (1 + states)*(read + write) + out)
-    kernels = {}
-    if not args.no_variants:
-        P = P_pad
-        gb = unit.grads[0].element_size()
-        low = [unit.master.to(torch.bfloat16), torch.zeros(P, dtype=torch.bfloat16, device=dev),
-               torch.zeros(P, dtype=torch.bfloat16, device=dev)]
-        vsets = {
-            "adamw_grad_dtype_reduce": ("adamw", True, unit.master, unit.exp_avg, unit.exp_avg_sq, unit.shard_out),
-            "adamw_bf16_state": ("adamw", False, low[0], low[1], low[2], None),
-            "sgd_momentum": ("sgd", False, unit.master, unit.exp_avg, None, unit.shard_out),
-            "adamax": ("adamax", False, unit.master, unit.exp_avg, unit.exp_avg_sq, unit.shard_out),
-            "adadelta": ("adadelta", False, unit.master, unit.exp_avg, unit.exp_avg_sq, unit.shard_out),
-        }
-        for vname, (opt, lowp, prm, s0, s1, out) in vsets.items():
-            ss = prm.element_size()
-            nstates = 1 + (s0 is not None) + (s1 is not None)
-            nbytes = P * (N * gb + nstates * 2 * ss + (out.element_size() if out is not None else 0))
-            lrv = 1.0 if opt == "adadelta" else cfg.lr
-            for st in (s0, s1):  # each optimizer starts from its own zero state
-                if st is not None:
-                    st.zero_()
-
-            def run(tt, opt=opt, lowp=lowp, prm=prm, s0=s0, s1=s1, out=out, lrv=lrv):
-                F.fsdp_reduce_scatter_step(unit.grads, prm, s0, s1, out,
-                                           F.StepConfig(opt, lrv, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay,
-                                                        tt, cfg.grad_scale, reduce_dtype=gdt if lowp else None))
-            for i in range(3):
-                run(i + 1)
-            kms = timed_calls(lambda i, run=run: run(i + 4), K, stream, flush)
-            launches += K
-            kernels[vname] = {"ms": round(kms, 4), "bytes_per_launch": nbytes,
-                              "achieved_GBs": round(nbytes / (kms * 1e-3) / 1e9, 1)}
-        del low
-
-    # ---- offload mode: master, m and v in pinned host memory, updated in
-    # place by the same fused kernel over the host link (12 B read and 12 B
-    # written per element there; gradients and the shard stay in HBM)
+    run = _Run(args, dev, rank, world_size)
+    step_ms, rsa_ms, clocks = time_steps(run)
+    e2e_ms, Ke, h2d, d2h, e2e_unavailable = time_e2e(run)
+    variants = time_fused_gather_variants(run) if not args.no_variants else {}
+    kernels = time_variant_kernels(run) if not args.no_variants else {}
     offload = None
     if not args.no_variants and not args.no_offload and world_size == 1:  # pins 12 B/param of host memory
-        try:
-            hstate = [torch.zeros(P_pad, dtype=torch.float32, pin_memory=True) for _ in range(3)]
-        except RuntimeError as e:  # not enough page-locked host memory
-            offload = {"unavailable": str(e).splitlines()[0][:200]}
-        else:
-            hstate[0].copy_(unit.master)
-            torch.cuda.synchronize()
-
-            def run_off(i):
-                F.fsdp_reduce_scatter_adam_cast(unit.grads, *hstate, unit.shard_out, hp(i + 1))
-
-            for i in range(3):
-                run_off(i)
-            Ko = max(3, min(K, 5))
-            oms = timed_calls(lambda i: run_off(i + 3), Ko, stream, flush)
-            launches += Ko
-            link_b = P_pad * 3 * (4 + 4)
-            hbm_b = P_pad * (N * unit.grads[0].element_size() + unit.shard_out.element_size())
-            offload = {"ms": round(oms, 3), "launches": Ko, "host_link_bytes_per_launch": link_b,
-                       "hbm_bytes_per_launch": hbm_b,
-                       "host_link_GBs": round(link_b / (oms * 1e-3) / 1e9, 1),
-                       "host_link_GBs_per_direction": round(link_b / 2 / (oms * 1e-3) / 1e9, 1),
-                       "slowdown_vs_device_state": round(oms / rsa_ms, 2)}
-            del hstate
-
-    # ---- the per-unit driver on a whole small model (12 GPT-2 small block
-    # units, the blocks of a GPT-2 small model): a Python loop over
-    # FlatParamUnit.step against one native fsdp_step_units call per step
+        offload = time_offload(run, rsa_ms)
     driver = None
     if not args.no_variants and not args.no_driver and world_size == 1:
-        driver, n_launch = measure_driver(F, fi, dev, stream)
-        launches += n_launch
+        driver, n_launch = measure_driver(F, run.fi, dev, run.stream)
+        run.launches += n_launch
 
     if world_size > 1:
         step_ms, rsa_ms, e2e_ms = max_over_ranks([step_ms, rsa_ms, e2e_ms], dev)
@@ -613,6 +651,8 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
+    unit, cfg, N, P_pad, rsa_b, ag_b = run.unit, run.cfg, run.N, run.P_pad, run.rsa_b, run.ag_b
+    workload, flush, K, launches = run.workload, run.flush, run.K, run.launches
     peak, peak_kind = measured_peak()
     achieved = rsa_b / (rsa_ms * 1e-3) / 1e9
     traffic = recorded_traffic(workload)
@@ -660,7 +700,7 @@ def run_ours(args):
                             for k, v in kernels.items()},
         "offload_state_on_host": offload,
         "driver_gpt2_small_model_12_units": driver,
-        "clocks": clocks.summary(),
+        "clocks": clocks,
     }
     if world_size == 1 and not args.no_cpu_baseline:
         n_s = min(unit.numel, args.cpu_sample)
