@@ -324,6 +324,16 @@ def max_over_ranks(values, device):
     return t.tolist()
 
 
+def all_ranks_agree(ok: bool, device) -> bool:
+    """True on every rank when every rank says ok (a MIN over the process
+    group), so that a leg runs on all ranks or on none."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([1 if ok else 0], device=device, dtype=torch.int32)
+    dist.all_reduce(t, op=dist.ReduceOp.MIN)
+    return bool(int(t.item()))
+
+
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
 
 def oracle_sample_run(cfg, n_elems: int, steps: int, warmup: int, time_budget_s: float | None):
@@ -486,12 +496,8 @@ def time_e2e(run: _Run):
         host_grads = [torch.empty(run.P_pad, dtype=run.gdt, pin_memory=True) for _ in range(run.N)]
     except RuntimeError as e:
         host_grads, unavailable = None, "pinned host buffers: " + str(e).splitlines()[0][:160]
-    if run.world_size > 1:
-        import torch.distributed as dist
-        ok = torch.tensor([0 if host_grads is None else 1], device=dev)
-        dist.all_reduce(ok, op=dist.ReduceOp.MIN)
-        if int(ok.item()) == 0 and host_grads is not None:
-            host_grads, unavailable = None, "another rank could not pin its host buffers"
+    if run.world_size > 1 and not all_ranks_agree(host_grads is not None, dev) and host_grads is not None:
+        host_grads, unavailable = None, "another rank could not pin its host buffers"
     if host_grads is None:
         return 0.0, Ke, 0, 0, unavailable
     for r in range(run.N):

@@ -1,6 +1,6 @@
 """The bench's multi-rank host logic on CPU with gloo, world size 2: the
-timing reduction takes the max over ranks, and the reference arm runs on
-rank 0 only."""
+timing reduction takes the max over ranks, a leg runs on every rank or on
+none, and the reference arm runs on rank 0 only."""
 import json
 import os
 import socket
@@ -28,7 +28,10 @@ def _worker(rank, world, port, out):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         got = bench.max_over_ranks([1.0 + rank, 10.0 - rank, 3.5], torch.device("cpu"))
-        out.put((rank, got))
+        # a leg runs on every rank or on none: rank 1 alone cannot, so none does
+        agree = (bench.all_ranks_agree(True, torch.device("cpu")),
+                 bench.all_ranks_agree(rank != 1, torch.device("cpu")))
+        out.put((rank, (got, agree)))
         dist.barrier()
     finally:
         dist.destroy_process_group()
@@ -45,7 +48,7 @@ def test_max_over_ranks_gloo_world2():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    assert res[0] == res[1] == [2.0, 10.0, 3.5]
+    assert res[0] == res[1] == ([2.0, 10.0, 3.5], (True, False))
 
 
 def test_reference_arm_prints_on_rank0_only(tmp_path):
