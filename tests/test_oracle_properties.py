@@ -1,0 +1,86 @@
+"""Property-based checks of the oracle (hypothesis; CPU only): over random
+world sizes, unit sizes, dtypes, hyperparameters and step counts, the
+invariants the pages fix must hold exactly.
+
+* "From all-reduce to sharded parameters": the N reduce-scatter blocks,
+  concatenated in rank order, are the all-reduce average, bit for bit.
+* FSDP training results are identical to DDP's ([FAIR] "与 PyTorch DDP 的对比"):
+  the sharded step equals the full-replica step on the averaged gradient.
+* The pad of a FlatParameter stays zero (zero gradients, zero state).
+* The compute-dtype cast is exact on values the dtype holds.
+"""
+import numpy as np
+import pytest
+
+hyp = pytest.importorskip("hypothesis")
+from hypothesis import given, settings, strategies as st  # noqa: E402
+
+FMT = ["bf16", "f16", "f32"]
+SETTINGS = dict(max_examples=60, deadline=None, derandomize=True)
+
+
+def _grads(orc, rng, world, P, fmt, scale):
+    P_pad = orc.padded_numel(P, world)
+    out = []
+    for _ in range(world):
+        g = np.zeros(P_pad, np.float32)
+        g[:P] = rng.standard_normal(P).astype(np.float32) * np.float32(1e-2 * scale)
+        out.append(orc.cast(g, fmt) if fmt != "f32" else g)
+    return out
+
+
+@given(world=st.integers(1, 9), P=st.integers(1, 3000), gfmt=st.sampled_from(FMT), seed=st.integers(0, 2**31))
+@settings(**SETTINGS)
+def test_reduce_scatter_blocks_form_the_all_reduce(orc, world, P, gfmt, seed):
+    rng = np.random.default_rng(seed)
+    grads = _grads(orc, rng, world, P, gfmt, 1.0)
+    c = orc.scalars(orc.hparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1), world).c
+    blocks = [orc.reduce_scatter(grads, gfmt, world, r, c) for r in range(world)]
+    np.testing.assert_array_equal(np.concatenate(blocks).view(np.uint32),
+                                  orc.all_reduce_avg(grads, gfmt, world, c).view(np.uint32))
+
+
+@given(world=st.integers(1, 9), P=st.integers(1, 2000), gfmt=st.sampled_from(FMT), ofmt=st.sampled_from(FMT),
+       steps=st.integers(1, 3), lr=st.floats(1e-5, 1e-1), wd=st.sampled_from([0.0, 0.01, 0.1]),
+       seed=st.integers(0, 2**31))
+@settings(**SETTINGS)
+def test_sharded_step_equals_ddp_and_the_pad_stays_zero(orc, world, P, gfmt, ofmt, steps, lr, wd, seed):
+    rng = np.random.default_rng(seed)
+    scale = 1024.0 if gfmt == "f16" else 1.0
+    p0 = orc.flatten_pad([rng.uniform(-0.1, 0.1, P).astype(np.float32)], world)
+    a = [p0.copy(), np.zeros_like(p0), np.zeros_like(p0)]
+    b = [p0.copy(), np.zeros_like(p0), np.zeros_like(p0)]
+    for t in range(1, steps + 1):
+        grads = _grads(orc, rng, world, P, gfmt, scale)
+        hp = orc.hparams(lr, 0.9, 0.999, 1e-8, wd, t, scale)
+        _, full_a = orc.fsdp_step(grads, gfmt, world, *a, ofmt, hp)
+        full_b = orc.ddp_step(grads, gfmt, world, *b, ofmt, hp)
+        np.testing.assert_array_equal(full_a.view(np.uint8), full_b.view(np.uint8))
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x.view(np.uint32), y.view(np.uint32))
+        assert not x[P:].any()
+
+
+@given(fmt=st.sampled_from(["bf16", "f16"]), seed=st.integers(0, 2**31))
+@settings(**SETTINGS)
+def test_cast_is_exact_on_representable_values(orc, fmt, seed):
+    rng = np.random.default_rng(seed)
+    bits = rng.integers(0, 1 << 16, 4096, dtype=np.uint32).astype(np.uint16)
+    x = orc.widen(bits, fmt)
+    finite = np.isfinite(x)
+    back = orc.cast(x, fmt)
+    np.testing.assert_array_equal(back[finite], bits[finite])
+
+
+@given(numels=st.lists(st.integers(0, 50), min_size=1, max_size=12), world=st.integers(1, 9))
+@settings(**SETTINGS)
+def test_flatten_layout(orc, numels, world):
+    parts = [np.arange(n, dtype=np.float32) + 1000 * k for k, n in enumerate(numels)]
+    flat = orc.flatten_pad(parts, world)
+    total = sum(numels)
+    assert flat.size == orc.padded_numel(total, world) and flat.size % world == 0
+    assert flat.size - total < world
+    offs = orc.view_offsets(numels)
+    for k, n in enumerate(numels):
+        np.testing.assert_array_equal(flat[offs[k]:offs[k] + n], parts[k])
+    assert not flat[total:].any()
