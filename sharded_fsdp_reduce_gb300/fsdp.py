@@ -99,11 +99,20 @@ def _stream(stream: Optional[torch.cuda.Stream]) -> int:
     return s.cuda_stream
 
 
+def _on_current_device(t: torch.Tensor, name: str) -> None:
+    """The kernels run on the current device: a tensor of another GPU would
+    reach them as a foreign address, so it is refused here."""
+    d, cur = t.get_device(), torch.cuda.current_device()
+    if d != cur:
+        raise ValueError(f"{name} is on cuda:{d} but the current device is cuda:{cur}")
+
+
 def _dev(t: torch.Tensor, name: str) -> int:
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    _on_current_device(t, name)
     return t.data_ptr()
 
 
@@ -115,6 +124,8 @@ def _mem(t: torch.Tensor, name: str) -> int:
         raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if t.is_cuda:
+        _on_current_device(t, name)
     return t.data_ptr()
 
 

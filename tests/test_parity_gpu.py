@@ -370,6 +370,33 @@ def test_invalid_calls_enqueue_nothing(F):
     assert F.fsdp_take_wait_timeouts() == 0
 
 
+def test_tensors_of_another_device_are_refused(F, monkeypatch):
+    # the kernels run on the current device, so a tensor of another GPU is
+    # refused by the binding before the library is called; with one GPU the
+    # current device is made to read as another ordinal
+    P = 64
+    grads = [torch.ones(P, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    master = torch.full((P,), 0.5, device=DEV)
+    m, v = torch.zeros(P, device=DEV), torch.zeros(P, device=DEV)
+    out = torch.zeros(P, dtype=torch.bfloat16, device=DEV)
+    full = [torch.zeros(P, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    hp = F.AdamWHParams(1e-3)
+    calls = [lambda: F.fsdp_reduce_scatter_adam_cast(grads, master, m, v, out, hp),
+             lambda: F.fsdp_reduce_scatter_adam_cast_gather(grads, master, m, v, out, full, hp),
+             lambda: F.fsdp_reduce_scatter_step(grads, master, m, v, out, F.StepConfig("adamw", 1e-3)),
+             lambda: F.fsdp_all_gather(out, full, 2),
+             lambda: F.fsdp_flatten_pad([master], 2)]
+    other = torch.cuda.current_device() + 1
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: other)
+    for call in calls:
+        with pytest.raises(ValueError, match="current device"):
+            call()
+    monkeypatch.undo()
+    torch.cuda.synchronize()
+    assert torch.equal(master, torch.full((P,), 0.5, device=DEV))
+    assert not m.any() and not v.any() and not out.any() and not any(f.any() for f in full)
+
+
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32, torch.float16])
 @pytest.mark.parametrize("numel,n_dst", [((1 << 20) + 3, 8), (5 * (1 << 19) + 1, 3), ((1 << 21) + 7, 1),
                                          (3 * (1 << 20), 13), ((1 << 20) + 4096 * 3 + 5, 2)])
