@@ -395,6 +395,16 @@ int fsdp_last_cuda_error(void);
  * resets it. The count is 0 in normal operation. */
 fsdp_status fsdp_take_wait_timeouts(uint32_t *count_out);
 
+/* Self-test of the failure path of those bounded waits, without a fault:
+ * launches one CTA on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream) that waits, with the library's bounded wait, on a shared-memory
+ * barrier that expects two arrivals and receives one. The wait gives up
+ * after about `limit_cycles` SM clock cycles and is counted as a gather's
+ * would be (read it with fsdp_take_wait_timeouts); the kernel then returns
+ * and the context stays usable. Asynchronous. limit_cycles must be in
+ * [1, 2^31] (FSDP_ERR_INVALID_ARG otherwise, nothing launched). */
+fsdp_status fsdp_check_bounded_wait(int64_t limit_cycles, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -3,7 +3,8 @@ AdamW + cast, all-gather and unflatten, as hand-written sm_103a CUDA behind a
 C ABI (include/fsdp.h). This package is the thin Python binding over it.
 """
 from .fsdp import (OPTIMIZERS, AdamWHParams, FsdpError, StepConfig, View, fsdp_reduce_scatter_step, dtype_code, fsdp_all_gather, fsdp_flatten_pad,
-                   fsdp_last_cuda_error, fsdp_padded_numel, fsdp_take_wait_timeouts, fsdp_reduce_scatter_adam_cast,
+                   fsdp_last_cuda_error, fsdp_padded_numel, fsdp_take_wait_timeouts, fsdp_check_bounded_wait,
+                   fsdp_reduce_scatter_adam_cast,
                    fsdp_reduce_scatter_adam_cast_gather, fsdp_status_string,
                    fsdp_unflatten_views, UnitDescs, fsdp_step_units, fsdp_step_units_ex, StepGraph)
 from .unit import FlatParamUnit, UnitSequence
@@ -14,5 +15,6 @@ __all__ = [
     "fsdp_padded_numel", "fsdp_unflatten_views", "fsdp_flatten_pad", "fsdp_reduce_scatter_adam_cast",
     "fsdp_reduce_scatter_adam_cast_gather",
     "fsdp_all_gather", "fsdp_status_string", "fsdp_last_cuda_error", "fsdp_take_wait_timeouts",
+    "fsdp_check_bounded_wait",
     "UnitDescs", "fsdp_step_units", "fsdp_step_units_ex", "StepGraph", "UnitSequence",
 ]

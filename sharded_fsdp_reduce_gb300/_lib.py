@@ -36,6 +36,7 @@ EXPORTS = (
     "fsdp_status_string",
     "fsdp_last_cuda_error",
     "fsdp_take_wait_timeouts",
+    "fsdp_check_bounded_wait",
     "fsdp_step_units",
     "fsdp_step_units_ex",
     "fsdp_step_graph_create",
@@ -109,6 +110,7 @@ def load() -> ctypes.CDLL:
             "fsdp_status_string": (ctypes.c_char_p, [i32]),
             "fsdp_last_cuda_error": (i32, []),
             "fsdp_take_wait_timeouts": (i32, [ctypes.POINTER(ctypes.c_uint32)]),
+            "fsdp_check_bounded_wait": (i32, [i64, vp]),
             "fsdp_step_units": (i32, [ctypes.POINTER(FsdpUnit), i32, ctypes.POINTER(FsdpAdamwHparams), i32, i32,
                                       vp, vp]),
             "fsdp_step_units_ex": (i32, [ctypes.POINTER(FsdpUnitEx), i32, ctypes.POINTER(FsdpStepConfig), i32,

@@ -860,4 +860,9 @@ FSDP_API fsdp_status fsdp_take_wait_timeouts(uint32_t *count_out) {
     return FSDP_OK;
 }
 
+FSDP_API fsdp_status fsdp_check_bounded_wait(int64_t limit_cycles, void *stream) {
+    if (limit_cycles < 1 || limit_cycles > (int64_t{1} << 31)) return FSDP_ERR_INVALID_ARG;
+    return launch_stalled_wait(static_cast<long long>(limit_cycles), static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

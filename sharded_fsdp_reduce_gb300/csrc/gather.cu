@@ -141,6 +141,18 @@ __global__ void __launch_bounds__(kTmaThreads)
     tma::bulk_wait<0>();
 }
 
+// A bounded wait on a barrier that nothing completes (two arrivals expected,
+// one made): it gives up after `limit` cycles and is counted like a gather's.
+// The failure path of the bounded waits, exercised without a fault.
+__global__ void __launch_bounds__(32) stalled_wait_kernel(long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    tma::mbar_init(&bar, 2);
+    tma::fence_mbar_init();
+    tma::mbar_arrive(&bar);
+    if (!tma::mbar_wait_bounded(&bar, 0, limit)) atomicAdd(&g_gather_wait_timeouts, 1u);
+}
+
 template <int ND>
 fsdp_status launch_tma(const GatherArgs &a, cudaStream_t stream) {
     static std::atomic<int> occupancy{0};
@@ -191,6 +203,11 @@ uint32_t take_gather_wait_timeouts() {
     if (cudaMemcpyFromSymbol(&n, g_gather_wait_timeouts, sizeof(n)) != cudaSuccess) return 0;
     cudaMemcpyToSymbol(g_gather_wait_timeouts, &zero, sizeof(zero));
     return n;
+}
+
+fsdp_status launch_stalled_wait(long long limit_cycles, cudaStream_t stream) {
+    stalled_wait_kernel<<<1, 32, 0, stream>>>(limit_cycles);
+    return check_launch();
 }
 
 fsdp_status launch_gather(const GatherArgs &a, cudaStream_t stream) {

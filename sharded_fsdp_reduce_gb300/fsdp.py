@@ -19,7 +19,7 @@ __all__ = [
     "fsdp_padded_numel", "fsdp_unflatten_views", "fsdp_flatten_pad",
     "fsdp_reduce_scatter_adam_cast", "fsdp_reduce_scatter_adam_cast_gather", "fsdp_all_gather",
     "fsdp_status_string",
-    "fsdp_last_cuda_error", "fsdp_take_wait_timeouts", "dtype_code",
+    "fsdp_last_cuda_error", "fsdp_take_wait_timeouts", "fsdp_check_bounded_wait", "dtype_code",
     "UnitDescs", "fsdp_step_units", "fsdp_step_units_ex", "StepGraph",
 ]
 
@@ -176,6 +176,13 @@ def fsdp_take_wait_timeouts() -> int:
     n = ctypes.c_uint32(0)
     _check(_lib.load().fsdp_take_wait_timeouts(ctypes.byref(n)), "fsdp_take_wait_timeouts")
     return int(n.value)
+
+
+def fsdp_check_bounded_wait(limit_cycles: int, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Self-test of the bounded waits' failure path: one kernel waits on a
+    barrier that nothing completes and gives up after about limit_cycles SM
+    cycles; fsdp_take_wait_timeouts() then counts it. Asynchronous."""
+    _check(_lib.load().fsdp_check_bounded_wait(int(limit_cycles), _stream(stream)), "fsdp_check_bounded_wait")
 
 
 def fsdp_padded_numel(numel: int, world: int) -> int:

@@ -100,6 +100,8 @@ int main(void) {
     CHECK(fsdp_step_graph_launch(NULL, &hp, NULL) == FSDP_ERR_INVALID_ARG);
     CHECK(fsdp_step_graph_destroy(NULL) == FSDP_OK);
     CHECK(fsdp_take_wait_timeouts(NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_check_bounded_wait(0, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_check_bounded_wait(((int64_t)1 << 31) + 1, NULL) == FSDP_ERR_INVALID_ARG);
     CHECK(fsdp_last_cuda_error() == 0);
     printf("ok\n");
     return 0;

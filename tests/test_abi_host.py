@@ -183,6 +183,12 @@ def test_take_wait_timeouts_rejects_null(lib):
     assert lib.fsdp_take_wait_timeouts(None) == E.FSDP_ERR_INVALID_ARG
 
 
+def test_check_bounded_wait_rejects_limits_out_of_range(lib):
+    from sharded_fsdp_reduce_gb300 import _lib as E
+    for limit in (0, -1, (1 << 31) + 1):
+        assert lib.fsdp_check_bounded_wait(limit, None) == E.FSDP_ERR_INVALID_ARG
+
+
 def test_fused_gather_rejects_invalid_arguments(lib):
     from sharded_fsdp_reduce_gb300 import _lib as E
     arr = lambda *p: (ctypes.c_void_p * len(p))(*p)

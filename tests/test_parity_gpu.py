@@ -370,6 +370,26 @@ def test_invalid_calls_enqueue_nothing(F):
     assert F.fsdp_take_wait_timeouts() == 0
 
 
+def test_a_bounded_wait_that_runs_out_is_counted_and_the_context_stays_usable(F):
+    # the failure path of the bulk-copy pipelines' bounded waits, without a
+    # fault: a wait on a barrier that nothing completes gives up after ~2^20
+    # cycles (about half a millisecond), is counted, and the kernel returns
+    assert F.fsdp_take_wait_timeouts() == 0
+    s = torch.cuda.Stream()
+    F.fsdp_check_bounded_wait(1 << 20)
+    F.fsdp_check_bounded_wait(1 << 20, stream=s)
+    assert F.fsdp_take_wait_timeouts() == 2
+    assert F.fsdp_take_wait_timeouts() == 0  # the read resets the count
+    assert F.fsdp_last_cuda_error() == 0
+    # the context still works: a bulk-copy gather right after
+    src = (torch.arange(1 << 20, device=DEV) % 251).to(torch.bfloat16)
+    fulls = [torch.zeros_like(src) for _ in range(3)]
+    F.fsdp_all_gather(src, fulls, 1)
+    torch.cuda.synchronize()
+    assert all(torch.equal(f, src) for f in fulls)
+    assert F.fsdp_take_wait_timeouts() == 0
+
+
 def test_tensors_of_another_device_are_refused(F, monkeypatch):
     # the kernels run on the current device, so a tensor of another GPU is
     # refused by the binding before the library is called; with one GPU the

@@ -97,3 +97,26 @@ def test_step_config_matches_the_unit(F):
     cfg = a.step_config(F.AdamWHParams(2e-3, 0.8, 0.99, 1e-6, 0.1, 3, 4.0))
     assert (cfg.optimizer, cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay, cfg.step, cfg.grad_scale) == \
         ("adamw", 2e-3, 0.8, 0.99, 1e-6, 0.1, 3, 4.0)
+
+
+@pytest.mark.parametrize("fail_at", [1, 3, 5, 8])
+def test_allocation_failure_reaches_the_caller(F, monkeypatch, fail_at):
+    # a simulated out-of-memory at the fail_at-th buffer a unit allocates
+    # (gradients, state, shard, gathered buffers): the error reaches the
+    # caller unchanged, and a unit built afterwards is whole and zeroed
+    real = torch.zeros
+    count = {"n": 0}
+
+    def zeros(*a, **k):
+        count["n"] += 1
+        if count["n"] == fail_at:
+            raise torch.OutOfMemoryError("simulated allocation failure")
+        return real(*a, **k)
+
+    monkeypatch.setattr(torch, "zeros", zeros)
+    with pytest.raises(torch.OutOfMemoryError, match="simulated"):
+        cpu_unit(F)
+    monkeypatch.undo()
+    u = cpu_unit(F)
+    bufs = u.grads + u.full + [u.master, u.exp_avg, u.exp_avg_sq, u.shard_out]
+    assert len(bufs) == 10 and all(b.numel() == u.padded_numel and not b.any() for b in bufs)
