@@ -162,6 +162,45 @@ def test_variant_full_size_sampled_bf16_state(F, orc):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("opt,lowp", [("adamw", True), ("sgd", False), ("adamax", False), ("adadelta", False)])
+def test_variant_full_size_sampled_fp32_state(F, orc, opt, lowp):
+    # the 70B unit at full size with fp32 parameter and state, each variant
+    # as the bench times it (AdamW with the bf16 reduce-scatter, SGD with
+    # momentum, Adamax, Adadelta at lr 1), compared on sampled elements
+    cfg = fi.CONFIGS["llama70b"]
+    N = cfg.world
+    P = fi.unit_numel(cfg)
+    grads = [torch.empty(P, dtype=torch.bfloat16, device=DEV) for _ in range(N)]
+    param = fi.gen_master(cfg, device=DEV)
+    s0 = torch.zeros(P, device=DEV)
+    s1 = None if opt == "sgd" else torch.zeros(P, device=DEV)
+    out = torch.zeros(P, dtype=torch.bfloat16, device=DEV)
+    rng = np.random.default_rng(9)
+    idx = np.unique(np.concatenate([rng.integers(0, P, 1 << 19), np.arange(P - 64, P), np.arange(64)]))
+    idx = idx[: len(idx) // N * N]
+    idx_t = torch.from_numpy(idx).to(DEV)
+    p_s = host(param[idx_t]).copy()
+    s_s = [np.zeros(len(idx), np.float32) for _ in range(1 if s1 is None else 2)]
+    lr = 1.0 if opt == "adadelta" else cfg.lr
+    for t in (1, 2, 3):
+        for r in range(N):
+            grads[r].copy_(fi.gen_grad(cfg, r, t, device=DEV))
+        g_s = [host(grads[r][idx_t]) for r in range(N)]
+        sc = F.StepConfig(opt, lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay, t,
+                          reduce_dtype=torch.bfloat16 if lowp else None)
+        F.fsdp_reduce_scatter_step(grads, param, s0, s1, out, sc)
+        out_s, _ = orc.step_ex(opt, lowp, g_s, "bf16", N, p_s, s_s[0], s_s[1] if s1 is not None else None, "f32",
+                               "bf16", orc.hparams(lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay, t))
+        torch.cuda.synchronize()
+        assert_state_close(host(param[idx_t]), p_s, f"{opt} param t={t}")
+        assert_state_close(host(s0[idx_t]), s_s[0], f"{opt} state0 t={t}")
+        if s1 is not None:
+            assert_state_close(host(s1[idx_t]), s_s[1], f"{opt} state1 t={t}")
+        assert_out_close(host(out[idx_t]), out_s, "bf16", f"{opt} shard_out t={t}")
+    del grads, param, s0, s1, out
+    torch.cuda.empty_cache()
+
+
 def test_variant_rejects_bad_arguments(F):
     P = 64
     grads = [torch.ones(P, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
