@@ -115,7 +115,7 @@ def _sample_indices(P_pad, N, k, seed):
     return np.unique(np.concatenate(idx)).astype(np.int64)
 
 
-@pytest.mark.parametrize("name,fuse", [("gpt3_13b", False), ("llama70b", False), ("gpt3_13b", True)])
+@pytest.mark.parametrize("name,fuse", [("gpt3_13b", False), ("llama70b", False), ("gpt3_13b", True), ("llama70b", True)])
 def test_full_size_sampled(F, orc, name, fuse):
     # fuse: the first all-gather written by the update kernel itself (f1)
     cfg = fi.CONFIGS[name]
