@@ -197,10 +197,12 @@ def test_offload_step_from_host(F):
         assert same_bits(f, b.shard_out)
 
 
-def test_offload_full_size_13b_sampled(F, orc):
-    # the 13B unit at full size with its 3.8 GB of state in host memory, in
-    # the bench's launch configuration; sampled elements against the oracle
-    cfg = fi.CONFIGS["gpt3_13b"]
+@pytest.mark.parametrize("name", ["gpt3_13b", "llama70b"])
+def test_offload_full_size_sampled(F, orc, name):
+    # the 13B and 70B units at full size with their state (3.8 and 10.3 GB)
+    # in host memory, in the bench's launch configuration; sampled elements
+    # against the oracle
+    cfg = fi.CONFIGS[name]
     N = cfg.world
     unit = new_unit(F, cfg, state_on_host=True)
     unit.load_master([fi.gen_master(cfg, device=DEV)])
