@@ -460,6 +460,48 @@ def test_step_from_host_matches_device_steps(F):
         assert torch.equal(f.view(torch.int16), b.shard_out.view(torch.int16))
 
 
+def test_step_from_host_full_size_sampled(F, orc):
+    # the 70B unit through the end-to-end path the bench times: its 13.7 GB
+    # of gradients copied in from pinned host memory every step, the
+    # non-finite count and the compute-dtype parameters read back; sampled
+    # elements against the oracle
+    cfg = fi.CONFIGS["llama70b"]
+    N = cfg.world
+    unit = new_unit(F, cfg)
+    unit.load_master([fi.gen_master(cfg, device=DEV)])
+    P_pad = unit.padded_numel
+    idx = _sample_indices(P_pad, N, 1 << 19, 11)
+    idx_c = torch.from_numpy(idx)
+    idx_t = idx_c.to(DEV)
+    p_s = host(unit.master[idx_t])
+    m_s = np.zeros_like(p_s)
+    v_s = np.zeros_like(p_s)
+    hgrads = [torch.empty(P_pad, dtype=torch.bfloat16, pin_memory=True) for _ in range(N)]
+    hout = torch.empty(P_pad, dtype=torch.bfloat16, pin_memory=True)
+    counter = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hnf = torch.full((1,), -1, dtype=torch.int32, pin_memory=True)
+    for t in range(1, cfg.steps + 1):
+        for r in range(N):
+            hgrads[r].copy_(fi.gen_grad(cfg, r, t, device=DEV))
+        g_s = [host(hgrads[r][idx_c]) for r in range(N)]
+        unit.step_from_host(hgrads, hout, hp_for(F, cfg, t), gathers=cfg.gathers, nonfinite_count=counter,
+                            host_nonfinite=hnf)
+        s = orc.scalars(ohp_for(orc, cfg, t), N)
+        orc.adamw(p_s, m_s, v_s, orc.all_reduce_avg(g_s, cfg.grad_dtype, N, s.c), s)
+        torch.cuda.synchronize()
+        assert int(hnf.item()) == 0
+        assert_state_close(host(unit.master[idx_t]), p_s, f"master t={t}")
+        assert_state_close(host(unit.exp_avg[idx_t]), m_s, f"exp_avg t={t}")
+        assert_state_close(host(unit.exp_avg_sq[idx_t]), v_s, f"exp_avg_sq t={t}")
+        out_s = orc.cast_out(p_s, cfg.out_dtype)
+        assert_out_close(host(hout[idx_c]), out_s, cfg.out_dtype, f"host_out t={t}")
+        assert torch.equal(hout.view(torch.int16), unit.shard_out.cpu().view(torch.int16))
+        for f in unit.full:
+            assert torch.equal(f, unit.shard_out)
+    del unit, hgrads, hout
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ fused all-gather (f1)
 
 @pytest.mark.parametrize("name", ["tiny", "gpt2_small", "gpt2_large"])
