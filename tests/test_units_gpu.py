@@ -119,6 +119,44 @@ def test_units_match_oracle(F, orc):
                 assert torch.equal(f, u.shard_out)
 
 
+def test_twelve_block_model_as_benched_matches_oracle(F, orc):
+    # the driver's bench model: 12 GPT-2 small block units (N=8, one gather
+    # each) on the two side streams, stepped twice by fsdp_step_units and
+    # twice by one launch of the captured step, bit for bit against the oracle
+    cfg = fi.CONFIGS["gpt2_small"]
+    gdt, odt = fi.torch_dtype(cfg.grad_dtype), fi.torch_dtype(cfg.out_dtype)
+    units = []
+    for k in range(12):
+        u = F.FlatParamUnit(cfg.params, cfg.world, gdt, odt, device=DEV)
+        u.load_master([fi.gen_master(cfg, device=DEV, seed_base=7000 + k)])
+        units.append(u)
+    seq = F.UnitSequence(units)
+    graph = seq.capture(gathers=cfg.gathers)
+    st = [[host(u.master), np.zeros(u.padded_numel, np.float32), np.zeros(u.padded_numel, np.float32)]
+          for u in units]
+    for t in (1, 2, 3, 4):
+        for k, u in enumerate(units):
+            for r in range(cfg.world):
+                u.load_grad(r, [fi.gen_grad(cfg, r, t, device=DEV, seed_base=7000 + k)])
+        hp = F.AdamWHParams(cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay, t, cfg.grad_scale)
+        if t <= 2:
+            seq.step(hp, gathers=cfg.gathers)
+        else:
+            graph.launch(hp)
+        torch.cuda.synchronize()
+        for u, (p, m, v) in zip(units, st):
+            shards_o, _ = orc.fsdp_step([host(g) for g in u.grads], cfg.grad_dtype, cfg.world, p, m, v,
+                                        cfg.out_dtype, orc.hparams(cfg.lr, cfg.beta1, cfg.beta2, cfg.eps,
+                                                                   cfg.weight_decay, t, cfg.grad_scale))
+            np.testing.assert_array_equal(host(u.master).view(np.uint32), p.view(np.uint32))
+            np.testing.assert_array_equal(host(u.exp_avg).view(np.uint32), m.view(np.uint32))
+            np.testing.assert_array_equal(host(u.exp_avg_sq).view(np.uint32), v.view(np.uint32))
+            np.testing.assert_array_equal(host(u.shard_out), shards_o)
+            for f in u.full:
+                assert torch.equal(f, u.shard_out)
+    graph.close()
+
+
 def test_units_with_offloaded_state_and_a_shared_counter(F):
     a = [u for u in build_model(F, 3, state_on_host={0, 1}) if u.grads[0].dtype != torch.float16]
     b = [u for u in build_model(F, 3) if u.grads[0].dtype != torch.float16]
