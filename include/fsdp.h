@@ -329,7 +329,7 @@ typedef struct {
     int32_t state_dtype;         /* fsdp_dtype */
     int32_t out_dtype;           /* fsdp_dtype; equal to state_dtype for bf16/fp16 state */
     int32_t n_full;              /* 0..FSDP_MAX_WORLD */
-    int32_t reserved;            /* 0 */
+    int32_t reserved;            /* must be 0 (FSDP_ERR_INVALID_ARG otherwise) */
 } fsdp_unit_ex;
 
 /* The multi-unit step with the variant update (device): as fsdp_step_units,

@@ -581,6 +581,7 @@ fsdp_status plan_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_ste
         const fsdp_unit_ex &x = units[u];
         UnitPlan &p = plan[static_cast<size_t>(u)];
         p.variant = true;
+        if (x.reserved != 0) return FSDP_ERR_INVALID_ARG;
         if (!dtype_valid(x.grad_dtype) || !dtype_valid(x.out_dtype) || !dtype_valid(x.state_dtype))
             return FSDP_ERR_UNSUPPORTED_DTYPE;
         const fsdp_dtype gd = static_cast<fsdp_dtype>(x.grad_dtype), od = static_cast<fsdp_dtype>(x.out_dtype);

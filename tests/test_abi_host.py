@@ -371,6 +371,9 @@ def test_step_units_ex_validates_every_unit_before_launching(lib):
     bad.state0 = A + 0x2000000                                                 # unit 0's first state
     assert call([unit(A), bad]) == E.FSDP_ERR_INVALID_ARG
     assert call([unit(A, P=0), unit(B, P=0)]) == E.FSDP_OK                     # empty units: nothing to launch
+    flagged = unit(B)
+    flagged.reserved = 1                                                       # a reserved field that is not 0
+    assert call([unit(A), flagged]) == E.FSDP_ERR_INVALID_ARG
     assert lib.fsdp_last_cuda_error() == 0
 
 
