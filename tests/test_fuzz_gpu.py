@@ -23,10 +23,10 @@ def F():
     return F
 
 
-def _case(seed):
+def _case(seed, max_p=40000):
     rng = np.random.default_rng(1000 + seed)
     world = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
-    P = int(rng.integers(1, 40000))
+    P = int(rng.integers(1, max_p))
     gfmt, ofmt = str(rng.choice(FMTS)), str(rng.choice(FMTS))
     rb = int(rng.integers(0, world))
     re = int(rng.integers(rb + 1, world + 1))
@@ -36,9 +36,10 @@ def _case(seed):
     return rng, world, P, gfmt, ofmt, rb, re, offset, gather, scale
 
 
-@pytest.mark.parametrize("seed", range(40))
-def test_fuzz_fused_step(F, orc, seed):
-    rng, world, P, gfmt, ofmt, rb, re, offset, gather, scale = _case(seed)
+@pytest.mark.parametrize("seed,max_p", [(s, 40000) for s in range(40)] + [(s, 3000000) for s in range(100, 108)])
+def test_fuzz_fused_step(F, orc, seed, max_p):
+    # max_p 3 M: units of up to ~1,500 CTAs of the vector path, many waves
+    rng, world, P, gfmt, ofmt, rb, re, offset, gather, scale = _case(seed, max_p)
     P_pad = orc.padded_numel(P, world)
     S = P_pad // world
     gdt, odt = fi.torch_dtype(gfmt), fi.torch_dtype(ofmt)
@@ -84,12 +85,12 @@ def test_fuzz_fused_step(F, orc, seed):
         assert not host(out)[:lo].view(np.uint8).any() and not host(out)[hi:].view(np.uint8).any()
 
 
-@pytest.mark.parametrize("seed", range(24))
-def test_fuzz_variant_step(F, orc, seed):
+@pytest.mark.parametrize("seed,max_p", [(s, 30000) for s in range(24)] + [(s, 2000000) for s in range(100, 106)])
+def test_fuzz_variant_step(F, orc, seed, max_p):
     rng = np.random.default_rng(5000 + seed)
     opt = str(rng.choice(["adamw", "sgd", "adamax", "adadelta"]))
     world = int(rng.choice([1, 2, 3, 8]))
-    P = int(rng.integers(1, 30000))
+    P = int(rng.integers(1, max_p))
     gfmt = str(rng.choice(FMTS))
     sfmt = str(rng.choice(["f32", "bf16", "f16"]))
     ofmt = str(rng.choice(FMTS)) if sfmt == "f32" else sfmt
