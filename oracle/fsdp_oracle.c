@@ -38,7 +38,7 @@
  * (built with -ffp-contract=off: no fused multiply-add). An fp64 shadow
  * (orc_*_f64) restates the same definitions in double to bound that rounding.
  *
- * Readings where the sources are silent (each is listed in the design notes):
+ * Readings where the sources are silent (readings of them, not statements in them):
  *  R1 padding: zeros appended at the end up to ceil(P/N)*N; no gaps between
  *     parameters.
  *  R2 reduction order: fp32, ranks 0..N-1, starting from G_0.
