@@ -390,7 +390,7 @@ int orc_ddp_step(const void *const *G, int grad_dtype, int64_t N, int64_t P_pad,
 }
 
 /* ------------------------------------------------------------------ */
-/* variants of the step (the "next" rows)                               */
+/* variants of the step: other optimizers, reduce and state precisions */
 /* ------------------------------------------------------------------ */
 
 /* Optimizers. [FAIR] "限制与兼容性说明": FSDP is compatible with the

@@ -1,4 +1,4 @@
-"""Pins of the oracle's variant paths (the "next" rows): SGD with momentum,
+"""Pins of the oracle's variant paths: SGD with momentum,
 Adamax, Adadelta, the reduce-scatter summed in the gradient dtype, and the
 low-precision parameter/state step. Each is checked against hand cases,
 closed forms, or torch's own implementations (torch.optim, torch's bf16/fp16

@@ -117,7 +117,7 @@ def _sample_indices(P_pad, N, k, seed):
 
 @pytest.mark.parametrize("name,fuse", [("gpt3_13b", False), ("llama70b", False), ("gpt3_13b", True), ("llama70b", True)])
 def test_full_size_sampled(F, orc, name, fuse):
-    # fuse: the first all-gather written by the update kernel itself (f1)
+    # fuse: the first all-gather written by the update kernel itself
     cfg = fi.CONFIGS[name]
     N = cfg.world
     unit = new_unit(F, cfg)
@@ -502,7 +502,7 @@ def test_step_from_host_full_size_sampled(F, orc):
     torch.cuda.empty_cache()
 
 
-# ------------------------------------------------------------------ fused all-gather (f1)
+# ------------------------------------------------------------------ fused all-gather
 
 @pytest.mark.parametrize("name", ["tiny", "gpt2_small", "gpt2_large"])
 def test_fused_gather_matches_oracle_and_unfused(F, orc, name):
