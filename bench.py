@@ -488,7 +488,8 @@ def time_e2e(run: _Run):
     forward), or with --e2e-read-params the compute-dtype parameters.
     Consecutive steps overlap their copies and kernels. Every rank runs it or
     none does. Returns (ms per step, steps, h2d bytes, d2h bytes, reason it
-    is unavailable or None)."""
+    is unavailable or None, ms of a bare copy of the gradients to the device
+    or None)."""
     torch, unit, cfg, args, dev = run.torch, run.unit, run.cfg, run.args, run.dev
     Ke = max(3, min(args.e2e_steps, run.K))
     unavailable = None
@@ -499,7 +500,7 @@ def time_e2e(run: _Run):
     if run.world_size > 1 and not all_ranks_agree(host_grads is not None, dev) and host_grads is not None:
         host_grads, unavailable = None, "another rank could not pin its host buffers"
     if host_grads is None:
-        return 0.0, Ke, 0, 0, unavailable
+        return 0.0, Ke, 0, 0, unavailable, None
     for r in range(run.N):
         host_grads[r].copy_(unit.grads[r])
     counter = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -525,7 +526,18 @@ def time_e2e(run: _Run):
     if host_nf is not None and int(host_nf.item()) != 0:
         raise RuntimeError("e2e steps reported non-finite gradients")
     run.launches += Ke * (1 + cfg.gathers)
-    return e2e_ms, Ke, h2d, d2h, None
+    # the host link's own bound, after the timed region: the bare copy of the
+    # same pinned gradients into the unit's gradient buffers (identical bytes)
+    bare = []
+    for _ in range(2):
+        e0.record(run.stream)
+        with torch.cuda.stream(run.stream):
+            for r in range(run.N):
+                unit.grads[r].copy_(host_grads[r], non_blocking=True)
+        e1.record(run.stream)
+        torch.cuda.synchronize()
+        bare.append(e0.elapsed_time(e1))
+    return e2e_ms, Ke, h2d, d2h, None, sum(bare) / len(bare)
 
 
 def time_fused_gather_variants(run: _Run):
@@ -635,7 +647,7 @@ def run_ours(args):
 
     run = _Run(args, dev, rank, world_size)
     step_ms, rsa_ms, clocks = time_steps(run)
-    e2e_ms, Ke, h2d, d2h, e2e_unavailable = time_e2e(run)
+    e2e_ms, Ke, h2d, d2h, e2e_unavailable, bare_h2d_ms = time_e2e(run)
     variants = time_fused_gather_variants(run) if not args.no_variants else {}
     kernels = time_variant_kernels(run) if not args.no_variants else {}
     offload = None
@@ -696,7 +708,9 @@ def run_ours(args):
                 "value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 3), "steps": Ke,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "d2h": "compute-dtype parameters" if args.e2e_read_params else "non-finite gradient count"},
+                "d2h": "compute-dtype parameters" if args.e2e_read_params else "non-finite gradient count",
+                "bare_h2d_ms": round(bare_h2d_ms, 3), "bare_h2d_GBs": round(h2d / (bare_h2d_ms * 1e-3) / 1e9, 1),
+                "bare_h2d_over_e2e": round(bare_h2d_ms / e2e_ms, 4)},
         "gpu_launches": launches,
         "variants": {k: dict(v, value=round(world_size * (rsa_b + P_pad * unit.shard_out.element_size()
                                                            * (1 + len(unit.full)) * v["gathers_per_step"])
