@@ -6,9 +6,11 @@
 
 #include <algorithm>
 #include <atomic>
+#include <memory>
 #include <new>
 #include <vector>
 
+#include "group.cuh"
 #include "host.cuh"
 
 // The library's exported symbols: the C ABI of include/fsdp.h and nothing else
@@ -458,21 +460,184 @@ fsdp_status side_streams(SideStreams *&out) {
     return FSDP_OK;
 }
 
+// Under stream capture: the graph node of the kernel just launched on s, the
+// one node the capture's dependency set holds right after that launch.
+fsdp_status last_captured_node(cudaStream_t s, cudaGraphNode_t *node) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaGraphNode_t *deps = nullptr;
+    size_t nd = 0;
+    if (cudaError_t e = cudaStreamGetCaptureInfo(s, &cs, nullptr, nullptr, &deps, nullptr, &nd); e != cudaSuccess)
+        return cuda_status(e);
+    if (cs != cudaStreamCaptureStatusActive || nd != 1 || !deps) return FSDP_ERR_CUDA;
+    *node = deps[0];
+    return FSDP_OK;
+}
+
 // Launch one unit's kernels on s. Under stream capture, *update_node (if
-// given) receives the graph node of the unit's update kernel: the one node
-// the capture's dependency set holds right after that launch.
+// given) receives the graph node of the unit's update kernel.
 fsdp_status launch_unit(const UnitPlan &p, cudaStream_t s, cudaGraphNode_t *update_node = nullptr) {
     fsdp_status st = p.variant ? launch_step(p.step, s) : launch_rsa(p.rsa, p.grad_dtype, p.out_dtype, s);
-    if (st == FSDP_OK && update_node) {
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        const cudaGraphNode_t *deps = nullptr;
-        size_t nd = 0;
-        if (cudaError_t e = cudaStreamGetCaptureInfo(s, &cs, nullptr, nullptr, &deps, nullptr, &nd); e != cudaSuccess)
-            return cuda_status(e);
-        if (cs != cudaStreamCaptureStatusActive || nd != 1 || !deps) return FSDP_ERR_CUDA;
-        *update_node = deps[0];
-    }
+    if (st == FSDP_OK && update_node) st = last_captured_node(s, update_node);
     for (int k = 0; st == FSDP_OK && k < p.separate_gathers; ++k) st = launch_gather(p.gather, s);
+    return st;
+}
+
+// A group of small units stepped by one batched update and `gathers`
+// batched all-gathers (group.cuh), and the plan's work items: a unit's own
+// kernels, or a group's.
+struct Group {
+    RsaGroupArgs rsa;
+    GatherGroupArgs gather;
+    int64_t rsa_grid = 0, gather_grid = 0;
+    int gathers = 0;
+    int first_unit = -1;
+    fsdp_dtype grad_dtype = FSDP_BF16, out_dtype = FSDP_BF16;
+};
+
+struct Work {
+    int unit = -1;            // plan index of a unit launched on its own
+    Group *group = nullptr;   // or the group launched together
+};
+
+// The update node of a captured work item and what its arguments hold: the
+// per-unit fused kernel (RsaArgs), the variant kernel (StepArgs) or the
+// batched update (RsaGroupArgs).
+enum NodeKind { kNodeUnit = 0, kNodeVariant = 1, kNodeGroup = 2 };
+struct UpdateNode {
+    cudaGraphNode_t node = nullptr;
+    int kind = kNodeUnit;
+    int world = 0;
+    int grad_dtype = 0;
+};
+
+// Whether a unit joins a batched launch: the fused AdamW update over all its
+// ranks with no fused gather, N in {2, 4, 8}, at most kGroupMaxNumel
+// elements, every base pointer 16-byte aligned (the vector path and the bulk
+// copies), the state in device memory and at most kGroupMaxWorld gathered
+// buffers. Larger units gain nothing from batching and keep their own
+// launches.
+bool groupable(const UnitPlan &p) {
+    if (p.variant || p.empty) return false;
+    const RsaArgs &a = p.rsa;
+    if (a.n_full != 0 || a.begin != 0 || a.end > kGroupMaxNumel) return false;
+    if (a.world != 2 && a.world != 4 && a.world != 8) return false;
+    if (!aligned(a.master, 16) || !aligned(a.m, 16) || !aligned(a.v, 16) || !aligned(a.out, 16)) return false;
+    for (int q = 0; q < a.world; ++q)
+        if (!aligned(a.grads[q], 16)) return false;
+    if (p.separate_gathers > 0) {
+        const GatherArgs &g = p.gather;
+        if (g.n_dst < 1 || g.n_dst > kGroupMaxWorld || !aligned(g.src, 16)) return false;
+        for (int d = 0; d < g.n_dst; ++d)
+            if (!aligned(g.dst[d], 16)) return false;
+    }
+    return !host_resident(a.master);
+}
+
+void add_to_group(Group &G, const UnitPlan &p) {
+    const RsaArgs &a = p.rsa;
+    const int k = G.rsa.n;
+    GroupUnit &gu = G.rsa.u[k];
+    memset(&gu, 0, sizeof(gu));
+    for (int q = 0; q < a.world; ++q) gu.grads[q] = a.grads[q];
+    gu.master = a.master;
+    gu.m = a.m;
+    gu.v = a.v;
+    gu.out = a.out;
+    gu.numel = a.end;
+    gu.cta_begin = G.rsa_grid;
+    gu.ncta = group_update_ctas(a.end);
+    G.rsa_grid += gu.ncta;
+    G.rsa.n = k + 1;
+    if (G.gathers > 0) {
+        GatherGroupUnit &gg = G.gather.u[k];
+        memset(&gg, 0, sizeof(gg));
+        gg.src = p.gather.src;
+        for (int d = 0; d < p.gather.n_dst; ++d) gg.dst[d] = p.gather.dst[d];
+        gg.nbytes = p.gather.nbytes;
+        gg.n_dst = p.gather.n_dst;
+        gg.tile_begin = G.gather_grid;
+        G.gather_grid += group_gather_tiles(p.gather.nbytes);
+        G.gather.n = k + 1;
+    }
+}
+
+// The work items of a plan, in the order of each item's first unit: units
+// that qualify are batched with the earlier ones of the same world size,
+// dtypes and gathers (kGroupMax per group), a group of one is launched as
+// that unit alone, and every other unit keeps its own kernels.
+void make_work(const std::vector<UnitPlan> &plan, std::vector<Work> &work,
+               std::vector<std::unique_ptr<Group>> &groups) {
+    work.clear();
+    groups.clear();
+    struct Open {  // the group now filling for one key
+        int world, gd, od, gathers, n_dst;
+        Group *g;
+    };
+    std::vector<Open> open;
+    for (size_t u = 0; u < plan.size(); ++u) {
+        const UnitPlan &p = plan[u];
+        if (p.empty) continue;
+        if (!groupable(p)) {
+            work.push_back({static_cast<int>(u), nullptr});
+            continue;
+        }
+        const int nd = p.separate_gathers > 0 ? p.gather.n_dst : 0;
+        Open *slot = nullptr;
+        for (Open &o : open)
+            if (o.world == p.rsa.world && o.gd == p.grad_dtype && o.od == p.out_dtype &&
+                o.gathers == p.separate_gathers && o.n_dst == nd)
+                slot = &o;
+        if (!slot || slot->g->rsa.n == kGroupMax) {
+            groups.push_back(std::unique_ptr<Group>(new Group()));
+            Group *g = groups.back().get();
+            memset(&g->rsa, 0, sizeof(g->rsa));
+            memset(&g->gather, 0, sizeof(g->gather));
+            g->rsa.s = p.rsa.s;  // every unit of a group has the same hyperparameters and N
+            g->rsa.nonfinite = p.rsa.nonfinite;
+            g->rsa.world = p.rsa.world;
+            g->gathers = p.separate_gathers;
+            g->first_unit = static_cast<int>(u);
+            g->grad_dtype = p.grad_dtype;
+            g->out_dtype = p.out_dtype;
+            work.push_back({-1, g});
+            if (slot) {
+                slot->g = g;
+            } else {
+                open.push_back({p.rsa.world, p.grad_dtype, p.out_dtype, p.separate_gathers, nd, g});
+            }
+            slot = nullptr;
+            for (Open &o : open)
+                if (o.g == g) slot = &o;
+        }
+        add_to_group(*slot->g, p);
+    }
+    for (Work &w : work)
+        if (w.group && w.group->rsa.n == 1) {
+            w.unit = w.group->first_unit;
+            w.group = nullptr;
+        }
+}
+
+// Launch one work item on s; under capture, *node receives its update node.
+fsdp_status launch_work(const std::vector<UnitPlan> &plan, const Work &w, cudaStream_t s, UpdateNode *node) {
+    if (!w.group) {
+        const UnitPlan &p = plan[static_cast<size_t>(w.unit)];
+        if (node) {
+            node->kind = p.variant ? kNodeVariant : kNodeUnit;
+            node->world = p.variant ? p.step.args.world : p.rsa.world;
+            node->grad_dtype = p.grad_dtype;
+        }
+        return launch_unit(p, s, node ? &node->node : nullptr);
+    }
+    const Group &G = *w.group;
+    fsdp_status st = launch_rsa_group(G.rsa, G.grad_dtype, G.out_dtype, G.rsa_grid, s);
+    if (st == FSDP_OK && node) {
+        node->kind = kNodeGroup;
+        node->world = G.rsa.world;
+        node->grad_dtype = G.grad_dtype;
+        st = last_captured_node(s, &node->node);
+    }
+    for (int k = 0; st == FSDP_OK && k < G.gathers; ++k) st = launch_gather_group(G.gather, G.gather_grid, s);
     return st;
 }
 
@@ -481,24 +646,24 @@ void add_span(std::vector<Span> &spans, const void *p, uintptr_t bytes) {
 }
 
 // Enqueue validated units: refuse overlapping written buffers (two units
-// sharing memory), then launch each unit's kernels in order, spread over
-// the side streams when there are two or more units with work.
-// Under stream capture, `nodes` (if given) receives each unit's update node
-// (nullptr for an empty unit).
+// sharing memory), then launch the work items (units, or groups of small
+// units batched into one launch per kernel) in order, spread over the side
+// streams when there are two or more. Under stream capture, `nodes` (if
+// given) receives each work item's update node.
 fsdp_status run_units(const std::vector<UnitPlan> &plan, std::vector<Span> &spans, cudaStream_t s,
-                      std::vector<cudaGraphNode_t> *nodes = nullptr) {
+                      std::vector<UpdateNode> *nodes = nullptr) {
     std::sort(spans.begin(), spans.end());
     for (size_t i = 1; i < spans.size(); ++i)
         if (spans[i].lo < spans[i - 1].hi) return FSDP_ERR_INVALID_ARG;
-    if (nodes) nodes->assign(plan.size(), nullptr);
-    auto node_of = [&](size_t u) { return nodes ? &(*nodes)[u] : nullptr; };
-    int busy = 0;
-    for (const UnitPlan &p : plan) busy += p.empty ? 0 : 1;
+    std::vector<Work> work;
+    std::vector<std::unique_ptr<Group>> groups;
+    make_work(plan, work, groups);
+    if (nodes) nodes->assign(work.size(), UpdateNode());
+    auto node_of = [&](size_t i) { return nodes ? &(*nodes)[i] : nullptr; };
+    const int busy = static_cast<int>(work.size());
     if (kUnitStreams < 2 || busy < 2) {
-        for (size_t u = 0; u < plan.size(); ++u) {
-            if (plan[u].empty) continue;
-            if (fsdp_status st = launch_unit(plan[u], s, node_of(u)); st != FSDP_OK) return st;
-        }
+        for (size_t i = 0; i < work.size(); ++i)
+            if (fsdp_status st = launch_work(plan, work[i], s, node_of(i)); st != FSDP_OK) return st;
         return FSDP_OK;
     }
     SideStreams *side = nullptr;
@@ -508,10 +673,8 @@ fsdp_status run_units(const std::vector<UnitPlan> &plan, std::vector<Span> &span
     for (int i = 0; i < ns; ++i)
         if (cudaError_t e = cudaStreamWaitEvent(side->s[i], side->fork, 0); e != cudaSuccess) return cuda_status(e);
     fsdp_status result = FSDP_OK;
-    int k = 0;
-    for (size_t u = 0; u < plan.size(); ++u) {
-        if (plan[u].empty) continue;
-        result = launch_unit(plan[u], side->s[k++ % ns], node_of(u));
+    for (size_t i = 0; i < work.size(); ++i) {
+        result = launch_work(plan, work[i], side->s[i % ns], node_of(i));
         if (result != FSDP_OK) break;
     }
     // join every side stream back into the caller's stream, also after a
@@ -618,9 +781,9 @@ fsdp_status plan_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_ste
 }
 
 // Capture the launches of validated units into an instantiated graph,
-// recording each unit's update node.
+// recording each work item's update node.
 fsdp_status capture_units(const std::vector<UnitPlan> &plan, std::vector<Span> &spans, cudaGraph_t &graph,
-                          cudaGraphExec_t &exec, std::vector<cudaGraphNode_t> &nodes) {
+                          cudaGraphExec_t &exec, std::vector<UpdateNode> &nodes) {
     graph = nullptr;
     exec = nullptr;
     cudaStream_t cs = nullptr;
@@ -715,15 +878,14 @@ FSDP_API fsdp_status fsdp_step_units_ex(const fsdp_unit_ex *units, int n_units, 
 }  // extern "C"
 
 // A captured model step (fsdp_step_graph_*): the instantiated graph and,
-// per unit, the node of its update kernel (nullptr for an empty unit), its
-// world size and gradient dtype, which the per-step arguments depend on.
-// `variant` graphs hold the variant kernel of one optimizer.
+// per work item (a unit, or a group of small units in one batched launch),
+// its update node with the kind of arguments it holds, its world size and
+// gradient dtype, which the per-step arguments depend on. `variant` graphs
+// hold the variant kernel of one optimizer.
 struct fsdp_step_graph {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
-    std::vector<cudaGraphNode_t> nodes;
-    std::vector<int> worlds;
-    std::vector<int> grad_dtypes;
+    std::vector<UpdateNode> nodes;
     bool variant = false;
     int optimizer = 0;
 };
@@ -734,7 +896,7 @@ fsdp_status make_graph(const std::vector<UnitPlan> &plan, std::vector<Span> &spa
                        fsdp_step_graph **graph_out) {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
-    std::vector<cudaGraphNode_t> nodes;
+    std::vector<UpdateNode> nodes;
     if (fsdp_status st = capture_units(plan, spans, graph, exec, nodes); st != FSDP_OK) return st;
     fsdp_step_graph *g = new (std::nothrow) fsdp_step_graph;
     if (!g) {
@@ -747,26 +909,26 @@ fsdp_status make_graph(const std::vector<UnitPlan> &plan, std::vector<Span> &spa
     g->nodes = nodes;
     g->variant = variant;
     g->optimizer = optimizer;
-    for (const UnitPlan &p : plan) {
-        g->worlds.push_back(p.variant ? p.step.args.world : p.rsa.world);
-        g->grad_dtypes.push_back(p.grad_dtype);
-    }
     *graph_out = g;
     return FSDP_OK;
 }
 
 // Write a step's arguments into one captured update node: the node's own
-// arguments (kernel params: the args struct, then int64 vbegin, nchunks,
-// vend) with only the step-dependent fields replaced.
-template <class Args, class Fill>
+// arguments (kernel params: the args struct first; for the per-unit kernels
+// then int64 vbegin, nchunks, vend; the batched update has no other) with
+// only the step-dependent fields replaced.
+template <class Args, int NPARAMS, class Fill>
 fsdp_status set_update_node(fsdp_step_graph *graph, cudaGraphNode_t node, Fill fill) {
     cudaKernelNodeParams kp;
     if (cudaError_t e = cudaGraphKernelNodeGetParams(node, &kp); e != cudaSuccess) return cuda_status(e);
     if (!kp.kernelParams) return FSDP_ERR_INVALID_ARG;
-    Args a;
-    memcpy(&a, kp.kernelParams[0], sizeof(a));
-    fill(a);
-    void *args[4] = {&a, kp.kernelParams[1], kp.kernelParams[2], kp.kernelParams[3]};
+    std::unique_ptr<Args> a(new (std::nothrow) Args);  // up to ~15 KB: not on the caller's stack
+    if (!a) return FSDP_ERR_INVALID_ARG;
+    memcpy(a.get(), kp.kernelParams[0], sizeof(Args));
+    fill(*a);
+    void *args[NPARAMS];
+    args[0] = a.get();
+    for (int i = 1; i < NPARAMS; ++i) args[i] = kp.kernelParams[i];
     kp.kernelParams = args;
     return cuda_status(cudaGraphExecKernelNodeSetParams(graph->exec, node, &kp));
 }
@@ -803,11 +965,11 @@ FSDP_API fsdp_status fsdp_step_graph_create_ex(const fsdp_unit_ex *units, int n_
 FSDP_API fsdp_status fsdp_step_graph_launch(fsdp_step_graph *graph, const fsdp_adamw_hparams *hp, void *stream) {
     if (!graph || !hp || graph->variant) return FSDP_ERR_INVALID_ARG;
     if (hp->step < 1 || !(hp->grad_scale > 0.0f) || !isfinite(hp->grad_scale)) return FSDP_ERR_INVALID_ARG;
-    for (size_t u = 0; u < graph->nodes.size(); ++u) {
-        if (!graph->nodes[u]) continue;
-        const int world = graph->worlds[u];
-        fsdp_status st = set_update_node<RsaArgs>(graph, graph->nodes[u],
-                                                  [&](RsaArgs &a) { a.s = make_scalars(*hp, world); });
+    for (const UpdateNode &n : graph->nodes) {
+        const AdamScalars sc = make_scalars(*hp, n.world);
+        fsdp_status st = n.kind == kNodeGroup
+                             ? set_update_node<RsaGroupArgs, 1>(graph, n.node, [&](RsaGroupArgs &a) { a.s = sc; })
+                             : set_update_node<RsaArgs, 4>(graph, n.node, [&](RsaArgs &a) { a.s = sc; });
         if (st != FSDP_OK) return st;
     }
     return cuda_status(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));
@@ -817,13 +979,11 @@ FSDP_API fsdp_status fsdp_step_graph_launch_ex(fsdp_step_graph *graph, const fsd
     if (!graph || !cfg || !graph->variant) return FSDP_ERR_INVALID_ARG;
     if (cfg->optimizer != graph->optimizer) return FSDP_ERR_INVALID_ARG;
     if (cfg->step < 1 || !(cfg->grad_scale > 0.0f) || !isfinite(cfg->grad_scale)) return FSDP_ERR_INVALID_ARG;
-    for (size_t u = 0; u < graph->nodes.size(); ++u)
-        if (graph->nodes[u] && cfg->reduce_dtype != FSDP_F32 && cfg->reduce_dtype != graph->grad_dtypes[u])
-            return FSDP_ERR_UNSUPPORTED_DTYPE;
-    for (size_t u = 0; u < graph->nodes.size(); ++u) {
-        if (!graph->nodes[u]) continue;
-        const int world = graph->worlds[u];
-        fsdp_status st = set_update_node<StepArgs>(graph, graph->nodes[u], [&](StepArgs &a) {
+    for (const UpdateNode &n : graph->nodes)
+        if (cfg->reduce_dtype != FSDP_F32 && cfg->reduce_dtype != n.grad_dtype) return FSDP_ERR_UNSUPPORTED_DTYPE;
+    for (const UpdateNode &n : graph->nodes) {
+        const int world = n.world;
+        fsdp_status st = set_update_node<StepArgs, 4>(graph, n.node, [&](StepArgs &a) {
             a.k = make_step_scalars(*cfg, world);
             a.reduce_lowp = cfg->reduce_dtype != FSDP_F32 ? 1 : 0;
         });

@@ -19,6 +19,7 @@
 // thread are. Fallback (unaligned pointers, small copies): every thread loads
 // one 16-byte word and stores it to every destination; a tail shorter than
 // 16 bytes moves in 2-byte units.
+#include "group.cuh"
 #include "host.cuh"
 #include "tma.cuh"
 
@@ -141,6 +142,56 @@ __global__ void __launch_bounds__(kTmaThreads)
     tma::bulk_wait<0>();
 }
 
+// The batched all-gather (group.cuh): one CTA per 16 KB tile of one unit,
+// the unit found by a binary search over the units' first tiles. Thread 0
+// bulk-loads the tile into shared memory and bulk-stores it to each of the
+// unit's destinations, as one CTA of gather_tma_kernel does for its tile;
+// the unit's first CTA also copies the bytes after its last whole 16-byte
+// word (2-byte units).
+__global__ void __launch_bounds__(kTmaThreads) gather_group_kernel(const __grid_constant__ GatherGroupArgs g) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t bar;
+    const int64_t b = blockIdx.x;
+    int lo = 0, hi = g.n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (g.u[mid].tile_begin <= b) {
+            lo = mid;
+        } else {
+            hi = mid - 1;
+        }
+    }
+    const GatherGroupUnit &U = g.u[lo];
+    const int64_t t = b - U.tile_begin;
+    const int64_t bulk = U.nbytes / 16 * 16;
+    const char *src = static_cast<const char *>(U.src);
+    if (t == 0) {
+        const int64_t tail_units = (U.nbytes - bulk) / 2;
+        for (int64_t k = threadIdx.x; k < tail_units; k += blockDim.x) {
+            const uint16_t x = *reinterpret_cast<const uint16_t *>(src + bulk + 2 * k);
+            for (int d = 0; d < U.n_dst; ++d)
+                *reinterpret_cast<uint16_t *>(static_cast<char *>(U.dst[d]) + bulk + 2 * k) = x;
+        }
+    }
+    if (threadIdx.x != 0) return;
+    const int64_t off = t * kGroupGatherTile;
+    if (off >= bulk) return;
+    const int64_t left = bulk - off;
+    const uint32_t bytes = static_cast<uint32_t>(left < kGroupGatherTile ? left : kGroupGatherTile);
+    tma::mbar_init(&bar, 1);
+    tma::fence_mbar_init();
+    tma::mbar_arrive_expect_tx(&bar, bytes);
+    tma::bulk_load(smem, src + off, bytes, &bar);
+    if (!tma::mbar_wait_bounded(&bar, 0, kWaitLimitCycles)) {
+        atomicAdd(&g_gather_wait_timeouts, 1u);
+        tma::bulk_wait<0>();
+        return;
+    }
+    for (int d = 0; d < U.n_dst; ++d) tma::bulk_store(static_cast<char *>(U.dst[d]) + off, smem, bytes);
+    tma::bulk_commit();
+    tma::bulk_wait<0>();
+}
+
 // A bounded wait on a barrier that nothing completes (two arrivals expected,
 // one made): it gives up after `limit` cycles and is counted like a gather's.
 // The failure path of the bounded waits, exercised without a fault.
@@ -203,6 +254,17 @@ uint32_t take_gather_wait_timeouts() {
     if (cudaMemcpyFromSymbol(&n, g_gather_wait_timeouts, sizeof(n)) != cudaSuccess) return 0;
     cudaMemcpyToSymbol(g_gather_wait_timeouts, &zero, sizeof(zero));
     return n;
+}
+
+int64_t group_gather_tiles(int64_t nbytes) {
+    const int64_t n = (nbytes / 16 * 16 + kGroupGatherTile - 1) / kGroupGatherTile;
+    return n > 0 ? n : 1;
+}
+
+fsdp_status launch_gather_group(const GatherGroupArgs &g, int64_t grid, cudaStream_t stream) {
+    if (g.n < 1 || g.n > kGroupMax || grid < 1 || grid > 0x7fffffff) return FSDP_ERR_INVALID_ARG;
+    gather_group_kernel<<<static_cast<unsigned>(grid), kTmaThreads, kGroupGatherTile, stream>>>(g);
+    return check_launch();
 }
 
 fsdp_status launch_stalled_wait(long long limit_cycles, cudaStream_t stream) {

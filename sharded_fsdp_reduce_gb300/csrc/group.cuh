@@ -1,0 +1,76 @@
+// group.cuh -- argument blocks of the batched launches: one launch of the
+// fused update, or of the all-gather, over many small units that share the
+// world size and the dtypes. A model of many small FSDP units (RegNet vision
+// models under VISSL are among FSDP's users: "Fully Sharded Data Parallel:
+// faster AI training with fewer GPUs", "Adoption paths for FSDP", "Computer
+// vision models in VISSL") would otherwise pay a kernel launch, a ramp-up and
+// a tail per unit, which for units of a few hundred thousand parameters cost
+// more than their bytes.
+//
+// The blocks travel by value as the kernel's only argument (kernel parameter
+// space, at most 32,764 bytes), so a batched launch needs no device memory of
+// its own. Each CTA finds its unit by a binary search over the units' first
+// CTA indices and then runs the per-unit kernel's code on it unchanged.
+#pragma once
+
+#include "common.cuh"
+
+namespace fsdp {
+
+constexpr int kGroupMax = 128;                          // units per batched launch
+constexpr int kGroupMaxWorld = 8;                       // gradient / destination pointers per unit
+constexpr int64_t kGroupMaxNumel = int64_t(1) << 22;    // units of up to 4 M elements are batched
+constexpr int kGroupGatherTile = 16384;                 // bytes per CTA of the batched gather
+
+// One unit of a batched update: all ranks' blocks [0, numel), every base
+// pointer 16-byte aligned, state in device memory.
+struct GroupUnit {
+    const void *grads[kGroupMaxWorld];  // world pointers used
+    float *master;
+    float *m;
+    float *v;
+    void *out;
+    int64_t numel;      // padded_numel
+    int64_t cta_begin;  // the unit's first CTA in the launch
+    int32_t ncta;       // its CTAs: max(1, ceil(numel / 8 / threads per CTA))
+    int32_t pad;
+};
+
+struct RsaGroupArgs {
+    AdamScalars s;  // first member: the block a captured step rewrites per step
+    uint32_t *nonfinite;
+    int32_t n;      // units
+    int32_t world;
+    GroupUnit u[kGroupMax];
+};
+
+// One unit of a batched all-gather: src and every destination 16-byte aligned.
+struct GatherGroupUnit {
+    const void *src;
+    void *dst[kGroupMaxWorld];  // n_dst pointers used
+    int64_t nbytes;
+    int64_t tile_begin;  // the unit's first CTA (one tile per CTA)
+    int32_t n_dst;
+    int32_t pad;
+};
+
+struct GatherGroupArgs {
+    int32_t n;
+    int32_t pad;
+    GatherGroupUnit u[kGroupMax];
+};
+
+static_assert(sizeof(RsaGroupArgs) < 32764, "kernel parameter space");
+static_assert(sizeof(GatherGroupArgs) < 32764, "kernel parameter space");
+
+// CTAs of one unit in a batched update, and tiles of one unit in a batched
+// gather (at least one each: a CTA also takes the elements or bytes after the
+// vector part).
+int32_t group_update_ctas(int64_t numel);
+int64_t group_gather_tiles(int64_t nbytes);
+
+// Launch `grid` CTAs of the batched kernels on stream s.
+fsdp_status launch_rsa_group(const RsaGroupArgs &g, int grad_dtype, int out_dtype, int64_t grid, cudaStream_t s);
+fsdp_status launch_gather_group(const GatherGroupArgs &g, int64_t grid, cudaStream_t s);
+
+}  // namespace fsdp

@@ -1,0 +1,195 @@
+"""Batched launches of small units: fsdp_step_units (and a captured step)
+runs the fused update and the all-gathers of up to 128 small units of one
+world size and dtype pair as one launch each. Every element sees the per-unit
+kernel's operations, so the results must equal stepping each unit on its own
+bit for bit, and the oracle.
+"""
+import types
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import host
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def F():
+    import __graft_entry__ as g
+    g.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import sharded_fsdp_reduce_gb300 as F
+    return F
+
+
+def make_units(F, specs, seed, **kw):
+    """Two identical sets of units (a, b) with random masters; specs are
+    (numel, world, grad dtype, out dtype)."""
+    g = torch.Generator().manual_seed(seed)
+    a, b = [], []
+    for numel, world, gdt, odt in specs:
+        x = torch.rand(numel, generator=g) * 0.2 - 0.1
+        for dst in (a, b):
+            u = F.FlatParamUnit([("w", (numel,))], world, gdt, odt, device=DEV, **kw)
+            u.load_master([x.to(DEV)])
+            dst.append(u)
+    torch.cuda.synchronize()
+    return a, b
+
+
+def load_grads(units_sets, t, seed):
+    g = torch.Generator().manual_seed(seed * 7919 + t)
+    for k in range(len(units_sets[0])):
+        u0 = units_sets[0][k]
+        for r in range(u0.world):
+            x = (torch.randn(u0.numel, generator=g) * 1e-2).to(DEV)
+            for units in units_sets:
+                units[k].load_grad(r, [x.to(units[k].grads[r].dtype)])
+
+
+def same(x, y):
+    iv = torch.int32 if x.element_size() == 4 else torch.int16
+    return torch.equal(x.view(iv), y.view(iv))
+
+
+def assert_units_equal(a, b, gathers):
+    for k, (ua, ub) in enumerate(zip(a, b)):
+        for name in ("master", "exp_avg", "exp_avg_sq", "shard_out"):
+            assert same(getattr(ua, name), getattr(ub, name)), (k, name)
+        for fa, fb in zip(ua.full, ub.full):
+            assert same(fa, fb), k
+        if gathers:
+            for f in ua.full:
+                assert same(f, ua.shard_out), k
+
+
+def hp(F, t):
+    return F.AdamWHParams(1e-3 * t, 0.9, 0.999, 1e-8, 0.01, t)
+
+
+@pytest.mark.parametrize("gathers", [0, 1, 2])
+def test_small_units_batched_equal_their_own_steps(F, gathers):
+    # 170 units: sizes from 1 element to 60 k (ragged tails, units smaller than
+    # one chunk), N in {2, 4, 8}, two dtype pairs; 150 of one kind, so that
+    # kind fills one group of 128 and starts a second
+    rng = np.random.default_rng(gathers)
+    specs = [(int(rng.integers(1, 60000)), 8, torch.bfloat16, torch.bfloat16) for _ in range(150)]
+    specs += [(int(n), int(w), torch.bfloat16, torch.float16)
+              for n, w in zip(rng.integers(1, 20000, 20), rng.choice([2, 4, 8], 20))]
+    specs[3] = (1, 8, torch.bfloat16, torch.bfloat16)
+    specs[4] = (7, 8, torch.bfloat16, torch.bfloat16)
+    a, b = make_units(F, specs, 11 + gathers)
+    seq = F.UnitSequence(a)
+    for t in (1, 2, 3):
+        load_grads([a, b], t, 3)
+        seq.step(hp(F, t), gathers=gathers)
+        for u in b:
+            u.step(hp(F, t), gathers=gathers)
+        torch.cuda.synchronize()
+        assert_units_equal(a, b, gathers)
+
+
+def _odd_unit(F, numel, world, offset, seed):
+    """A unit whose buffers start `offset` elements into their allocations
+    (offset 1: not 16-byte aligned, so it keeps its own launches)."""
+    g = torch.Generator().manual_seed(seed)
+    P = F.fsdp_padded_numel(numel, world)
+
+    def alloc(dt):
+        return torch.zeros(P + offset, dtype=dt, device=DEV)[offset:]
+
+    u = types.SimpleNamespace(world=world, numel=numel, padded_numel=P)
+    u.grads = [alloc(torch.bfloat16) for _ in range(world)]
+    u.master, u.exp_avg, u.exp_avg_sq = alloc(torch.float32), alloc(torch.float32), alloc(torch.float32)
+    u.shard_out = alloc(torch.bfloat16)
+    u.full = [alloc(torch.bfloat16) for _ in range(world)]
+    u.master[:numel].copy_((torch.rand(numel, generator=g) * 0.2 - 0.1).to(DEV))
+    return u
+
+
+def test_batched_and_own_launches_in_one_call(F):
+    # small aligned units batch; an unaligned unit, a unit of N = 3, a unit
+    # with host-resident state and a unit above the batching size keep their
+    # own kernels, all in one call, all equal to stepping each unit alone
+    specs = [(int(n), 4, torch.bfloat16, torch.bfloat16) for n in (5000, 333, 70000, 12, 4099, 65536)]
+    a, b = make_units(F, specs, 21)
+    for dst in (a, b):
+        dst.append(F.FlatParamUnit([("w", (3001,))], 3, torch.bfloat16, torch.bfloat16, device=DEV))
+        dst.append(F.FlatParamUnit([("w", (9000,))], 4, torch.bfloat16, torch.bfloat16, device=DEV,
+                                   state_on_host=True))
+        dst.append(F.FlatParamUnit([("w", ((1 << 22) + 8,))], 4, torch.bfloat16, torch.bfloat16, device=DEV))
+    for k in range(len(specs), len(a)):
+        x = torch.rand(a[k].numel) * 0.2 - 0.1
+        a[k].load_master([x.to(DEV)])
+        b[k].load_master([x.to(DEV)])
+    oa, ob = _odd_unit(F, 5000, 4, 1, 5), _odd_unit(F, 5000, 4, 1, 5)
+    a.insert(2, oa)
+    b.insert(2, ob)
+    torch.cuda.synchronize()
+    for t in (1, 2):
+        g = torch.Generator().manual_seed(100 + t)
+        for ua, ub in zip(a, b):
+            for r in range(ua.world):
+                x = (torch.randn(ua.numel, generator=g) * 1e-2).to(DEV, torch.bfloat16)
+                for u in (ua, ub):
+                    u.grads[r][:u.numel].copy_(x)
+        F.fsdp_step_units(a, hp(F, t), gathers=2)
+        for ub in b:
+            F.fsdp_step_units([ub], hp(F, t), gathers=2)  # one unit per call: its own kernels
+        torch.cuda.synchronize()
+        assert_units_equal(a, b, 2)
+
+
+@pytest.mark.parametrize("gathers", [1, 2])
+def test_batched_units_in_a_captured_step(F, gathers):
+    # the captured step holds batched update nodes; each launch rewrites their
+    # scalars, and four launches over changing hyperparameters equal the
+    # eager driver, bit for bit
+    rng = np.random.default_rng(40 + gathers)
+    specs = [(int(n), 8, torch.bfloat16, torch.bfloat16) for n in rng.integers(1, 50000, 60)]
+    specs += [(int(n), 2, torch.float16, torch.float16) for n in rng.integers(1, 50000, 10)]
+    a, b = make_units(F, specs, 31)
+    graph = F.UnitSequence(a).capture(gathers=gathers)
+    seq_b = F.UnitSequence(b)
+    for t in (1, 2, 3, 4):
+        load_grads([a, b], t, 9)
+        graph.launch(hp(F, t))
+        seq_b.step(hp(F, t), gathers=gathers)
+        torch.cuda.synchronize()
+        assert_units_equal(a, b, gathers)
+    graph.close()
+
+
+def test_batched_units_match_oracle_and_count_nonfinite(F, orc):
+    # a group of 40 units against the oracle, bit for bit; planted non-finite
+    # gradients are counted as the per-unit kernel counts them
+    rng = np.random.default_rng(7)
+    specs = [(int(n), 4, torch.bfloat16, torch.bfloat16) for n in rng.integers(1, 30000, 40)]
+    a, b = make_units(F, specs, 41)
+    st = [[host(u.master), np.zeros(u.padded_numel, np.float32), np.zeros(u.padded_numel, np.float32)] for u in a]
+    ca = torch.zeros(1, dtype=torch.int32, device=DEV)
+    cb = torch.zeros(1, dtype=torch.int32, device=DEV)
+    seq = F.UnitSequence(a)
+    for t in (1, 2):
+        load_grads([a, b], t, 17)
+        if t == 2:
+            for units in (a, b):
+                units[5].grads[1][0] = float("inf")
+                units[30].grads[3][units[30].numel - 1] = float("nan")
+        seq.step(hp(F, t), gathers=1, nonfinite_count=ca)
+        for u in b:
+            u.step(hp(F, t), gathers=1, nonfinite_count=cb)
+        torch.cuda.synchronize()
+        assert_units_equal(a, b, 1)
+        if t == 1:
+            for u, (p, m, v) in zip(a, st):
+                shards_o, _ = orc.fsdp_step([host(gr) for gr in u.grads], "bf16", u.world, p, m, v, "bf16",
+                                            orc.hparams(1e-3 * t, 0.9, 0.999, 1e-8, 0.01, t))
+                np.testing.assert_array_equal(host(u.master).view(np.uint32), p.view(np.uint32))
+                np.testing.assert_array_equal(host(u.exp_avg).view(np.uint32), m.view(np.uint32))
+                np.testing.assert_array_equal(host(u.exp_avg_sq).view(np.uint32), v.view(np.uint32))
+                np.testing.assert_array_equal(host(u.shard_out), shards_o)
+    assert int(ca.item()) == int(cb.item()) == 2
