@@ -21,8 +21,10 @@ during the timed region. Beside them, on the same unit: the fused-gather and
 no-reshard steps (`variants`), the variant optimizers' kernels
 (`variant_kernels`), the fused kernel with its state in pinned host memory
 (`offload_state_on_host`), and the per-unit driver on a 12-unit GPT-2 small
-model (`driver_gpt2_small_model_12_units`; these two on one GPU only);
---no-variants, --no-offload and --no-driver skip them.
+model (`driver_gpt2_small_model_12_units`) and on a model of 200 units of
+50,000 parameters (`driver_model_200_units_of_50k`, batched launches; these
+three on one GPU only); --no-variants, --no-offload and --no-driver skip
+them.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
@@ -253,21 +255,38 @@ def timed_calls(fn, K: int, stream, flush: L2Flush) -> float:
     return sum(a.elapsed_time(b) for a, b in evs) / K
 
 
-def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20):
+GROUP_MAX_UNITS = 128          # the library's batched launches: units per launch
+GROUP_MAX_NUMEL = 1 << 22      # and the largest unit they take
+
+
+def model_launches(n_units: int, numel: int, gathers: int) -> int:
+    """Kernel launches of one fsdp_step_units call (or captured step) over
+    n_units equal units of numel elements whose buffers qualify for batched
+    launches when small enough: one update and `gathers` gathers per unit, or
+    per group of up to GROUP_MAX_UNITS units (a group of one is a unit)."""
+    if numel > GROUP_MAX_NUMEL:
+        return n_units * (1 + gathers)
+    return -(-n_units // GROUP_MAX_UNITS) * (1 + gathers)
+
+
+def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20, numel: int = 0):
     """Host enqueue time and device time per model step of n_units GPT-2 small
-    block units (one gather each), stepped by a Python loop over the units, by
-    one native fsdp_step_units call, and by one launch of the step captured as
-    a CUDA graph. Returns (result, timed launches)."""
+    block units (or, with numel, n_units one-tensor units of numel elements
+    with the same N, dtypes and hyperparameters; one gather each), stepped by
+    a Python loop over the units, by one native fsdp_step_units call, and by
+    one launch of the step captured as a CUDA graph. Returns (result, timed
+    launches)."""
     import torch
 
     cfg = fi.CONFIGS["gpt2_small"]
     gdt, odt = fi.torch_dtype(cfg.grad_dtype), fi.torch_dtype(cfg.out_dtype)
+    params = [("flat", (numel,))] if numel else cfg.params
     units = []
     for k in range(n_units):
-        u = F.FlatParamUnit(cfg.params, cfg.world, gdt, odt, device=dev)
-        u.load_master([fi.gen_master(cfg, device=dev, seed_base=7000 + k)])
+        u = F.FlatParamUnit(params, cfg.world, gdt, odt, device=dev)
+        u.load_master([fi.gen_master(cfg, device=dev, seed_base=7000 + k, numel=u.numel)])
         for r in range(cfg.world):
-            u.load_grad(r, [fi.gen_grad(cfg, r, 1, device=dev, seed_base=7000 + k)])
+            u.load_grad(r, [fi.gen_grad(cfg, r, 1, device=dev, seed_base=7000 + k, numel=u.numel)])
         units.append(u)
     seq = F.UnitSequence(units)
     t = [0]
@@ -307,11 +326,14 @@ def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20):
     rsa_b, ag_b = seq.step_bytes(cfg.gathers)
     out["bytes_per_step"] = rsa_b + ag_b
     out["native_GBs"] = round((rsa_b + ag_b) / (out["native"]["device_ms_per_step"] * 1e-3) / 1e9, 1)
-    out["launches_per_step"] = n_units * (1 + cfg.gathers)
+    out["cuda_graph_GBs"] = round((rsa_b + ag_b) / (out["cuda_graph"]["device_ms_per_step"] * 1e-3) / 1e9, 1)
+    per_unit = n_units * (1 + cfg.gathers)
+    batched = model_launches(n_units, units[0].padded_numel, cfg.gathers)
+    out["launches_per_step"] = {"python_loop": per_unit, "native": batched, "cuda_graph": batched}
     graph.close()
     del seq, units, graph
     torch.cuda.empty_cache()
-    return out, 3 * steps * n_units * (1 + cfg.gathers)
+    return out, steps * (per_unit + 2 * batched)
 
 
 def max_over_ranks(values, device):
@@ -653,9 +675,11 @@ def run_ours(args):
     offload = None
     if not args.no_variants and not args.no_offload and world_size == 1:  # pins 12 B/param of host memory
         offload = time_offload(run, rsa_ms)
-    driver = None
+    driver = small_units = None
     if not args.no_variants and not args.no_driver and world_size == 1:
         driver, n_launch = measure_driver(F, run.fi, dev, run.stream)
+        run.launches += n_launch
+        small_units, n_launch = measure_driver(F, run.fi, dev, run.stream, n_units=200, numel=50000)
         run.launches += n_launch
 
     if world_size > 1:
@@ -720,6 +744,7 @@ def run_ours(args):
                             for k, v in kernels.items()},
         "offload_state_on_host": offload,
         "driver_gpt2_small_model_12_units": driver,
+        "driver_model_200_units_of_50k": small_units,
         "clocks": clocks,
     }
     if world_size == 1 and not args.no_cpu_baseline:
