@@ -309,7 +309,13 @@ fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
  * keeps per host thread and device (created on first use), which wait for
  * the work already on `stream` and which `stream` waits for afterwards; a
  * unit's kernels run in order on one of them and overlap the neighbouring
- * unit's. Work enqueued on `stream` after the call sees every unit done. */
+ * unit's. Work enqueued on `stream` after the call sees every unit done.
+ * Batching: small units are stepped together, up to 128 per launch of each
+ * kernel, when they share N (2, 4 or 8), the dtype pair, n_full (at most 8)
+ * and the gathers, and each has at most 2^22 elements, 16-byte aligned
+ * buffers, its state in device memory and no fused gather; every element
+ * sees the same operations as in the unit's own launch, so the results are
+ * the same bits. Every other unit keeps its own launches. */
 fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
                             int gathers, int fuse_first_gather, uint32_t *nonfinite_count,
                             void *stream);
@@ -352,8 +358,8 @@ typedef struct fsdp_step_graph fsdp_step_graph;
  * The units are validated as fsdp_step_units validates them; nothing runs.
  * The graph holds the buffers' addresses: they must stay allocated, and a
  * step launched from it touches exactly those buffers. Each launch writes
- * its own step's scalars, so one graph serves every step ("capture
- * launch-bound inner loops in graphs": one launch for the whole model).
+ * its own step's scalars, so one graph serves every step: one launch for
+ * the whole model, batched launches included.
  *   graph_out    host; receives the handle (NULL on error). */
 fsdp_status fsdp_step_graph_create(const fsdp_unit *units, int n_units, int gathers, int fuse_first_gather,
                                    uint32_t *nonfinite_count, fsdp_step_graph **graph_out);
