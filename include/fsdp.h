@@ -345,7 +345,9 @@ typedef struct {
  * parameter itself for bf16/fp16 state -- into its n_full buffers. No gather
  * is fused. Validation (every unit as fsdp_reduce_scatter_step validates it,
  * no buffer written by two units, nothing enqueued on error), scheduling
- * over the side streams and errors as fsdp_step_units. */
+ * over the side streams, batching of small units (those that also share
+ * the state dtype; the optimizer and reduction are the call's) and errors as
+ * fsdp_step_units. */
 fsdp_status fsdp_step_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
                                int gathers, uint32_t *nonfinite_count, void *stream);
 

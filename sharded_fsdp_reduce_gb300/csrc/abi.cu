@@ -482,16 +482,21 @@ fsdp_status launch_unit(const UnitPlan &p, cudaStream_t s, cudaGraphNode_t *upda
     return st;
 }
 
-// A group of small units stepped by one batched update and `gathers`
-// batched all-gathers (group.cuh), and the plan's work items: a unit's own
-// kernels, or a group's.
+// A group of small units stepped by one batched update (the fused AdamW
+// kernel's, or the variant kernel's) and `gathers` batched all-gathers
+// (group.cuh), and the plan's work items: a unit's own kernels, or a
+// group's.
 struct Group {
+    bool variant = false;
     RsaGroupArgs rsa;
+    StepGroupArgs step;
     GatherGroupArgs gather;
-    int64_t rsa_grid = 0, gather_grid = 0;
+    int n = 0;
+    int64_t update_grid = 0, gather_grid = 0;
     int gathers = 0;
     int first_unit = -1;
-    fsdp_dtype grad_dtype = FSDP_BF16, out_dtype = FSDP_BF16;
+    int optimizer = 0;
+    fsdp_dtype grad_dtype = FSDP_BF16, out_dtype = FSDP_BF16, state_dtype = FSDP_F32;
 };
 
 struct Work {
@@ -500,9 +505,9 @@ struct Work {
 };
 
 // The update node of a captured work item and what its arguments hold: the
-// per-unit fused kernel (RsaArgs), the variant kernel (StepArgs) or the
-// batched update (RsaGroupArgs).
-enum NodeKind { kNodeUnit = 0, kNodeVariant = 1, kNodeGroup = 2 };
+// per-unit fused kernel (RsaArgs), the per-unit variant kernel (StepArgs),
+// or the batched update of either (RsaGroupArgs, StepGroupArgs).
+enum NodeKind { kNodeUnit = 0, kNodeVariant = 1, kNodeGroup = 2, kNodeVariantGroup = 3 };
 struct UpdateNode {
     cudaGraphNode_t node = nullptr;
     int kind = kNodeUnit;
@@ -510,44 +515,125 @@ struct UpdateNode {
     int grad_dtype = 0;
 };
 
-// Whether a unit joins a batched launch: the fused AdamW update over all its
-// ranks with no fused gather, N in {2, 4, 8}, at most kGroupMaxNumel
-// elements, every base pointer 16-byte aligned (the vector path and the bulk
-// copies), the state in device memory and at most kGroupMaxWorld gathered
+// What batched units must share: the update (fused AdamW, or the variant
+// kernel with its optimizer, state dtype and reduction), N, the dtypes and
+// the gathers.
+struct GroupKey {
+    bool variant;
+    int optimizer, state_dtype, reduce_lowp, world, grad_dtype, out_dtype, gathers, n_dst;
+    bool operator==(const GroupKey &o) const {
+        return variant == o.variant && optimizer == o.optimizer && state_dtype == o.state_dtype &&
+               reduce_lowp == o.reduce_lowp && world == o.world && grad_dtype == o.grad_dtype &&
+               out_dtype == o.out_dtype && gathers == o.gathers && n_dst == o.n_dst;
+    }
+};
+
+GroupKey key_of(const UnitPlan &p) {
+    GroupKey k{};
+    k.variant = p.variant;
+    k.optimizer = p.variant ? p.step.optimizer : FSDP_OPT_ADAMW;
+    k.state_dtype = p.variant ? p.step.state_dtype : FSDP_F32;
+    k.reduce_lowp = p.variant ? p.step.args.reduce_lowp : 0;
+    k.world = p.variant ? p.step.args.world : p.rsa.world;
+    k.grad_dtype = p.grad_dtype;
+    k.out_dtype = p.out_dtype;
+    k.gathers = p.separate_gathers;
+    k.n_dst = p.separate_gathers > 0 ? p.gather.n_dst : 0;
+    return k;
+}
+
+// Whether a unit joins a batched launch: an update over all its ranks (no
+// fused gather), N in {2, 4, 8}, at most kGroupMaxNumel elements, every base
+// pointer 16-byte aligned (the vector path and the bulk copies), the
+// parameter or master in device memory and at most kGroupMaxWorld gathered
 // buffers. Larger units gain nothing from batching and keep their own
 // launches.
 bool groupable(const UnitPlan &p) {
-    if (p.variant || p.empty) return false;
-    const RsaArgs &a = p.rsa;
-    if (a.n_full != 0 || a.begin != 0 || a.end > kGroupMaxNumel) return false;
-    if (a.world != 2 && a.world != 4 && a.world != 8) return false;
-    if (!aligned(a.master, 16) || !aligned(a.m, 16) || !aligned(a.v, 16) || !aligned(a.out, 16)) return false;
-    for (int q = 0; q < a.world; ++q)
-        if (!aligned(a.grads[q], 16)) return false;
+    if (p.empty) return false;
+    const void *state = nullptr;
+    if (p.variant) {
+        const StepArgs &a = p.step.args;
+        if (a.begin != 0 || a.end > kGroupMaxNumel) return false;
+        if (a.world != 2 && a.world != 4 && a.world != 8) return false;
+        if (!aligned(a.param, 16) || !aligned(a.s0, 16) || !aligned(a.s1, 16) || !aligned(a.out, 16)) return false;
+        for (int q = 0; q < a.world; ++q)
+            if (!aligned(a.grads[q], 16)) return false;
+        state = a.param;
+    } else {
+        const RsaArgs &a = p.rsa;
+        if (a.n_full != 0 || a.begin != 0 || a.end > kGroupMaxNumel) return false;
+        if (a.world != 2 && a.world != 4 && a.world != 8) return false;
+        if (!aligned(a.master, 16) || !aligned(a.m, 16) || !aligned(a.v, 16) || !aligned(a.out, 16)) return false;
+        for (int q = 0; q < a.world; ++q)
+            if (!aligned(a.grads[q], 16)) return false;
+        state = a.master;
+    }
     if (p.separate_gathers > 0) {
         const GatherArgs &g = p.gather;
         if (g.n_dst < 1 || g.n_dst > kGroupMaxWorld || !aligned(g.src, 16)) return false;
         for (int d = 0; d < g.n_dst; ++d)
             if (!aligned(g.dst[d], 16)) return false;
     }
-    return !host_resident(a.master);
+    return !host_resident(state);
+}
+
+Group *new_group(std::vector<std::unique_ptr<Group>> &groups, const UnitPlan &p, int u) {
+    groups.push_back(std::unique_ptr<Group>(new Group()));
+    Group *g = groups.back().get();
+    memset(&g->rsa, 0, sizeof(g->rsa));
+    memset(&g->step, 0, sizeof(g->step));
+    memset(&g->gather, 0, sizeof(g->gather));
+    g->variant = p.variant;
+    if (p.variant) {  // every unit of a group has the same hyperparameters, N and reduction
+        g->step.k = p.step.args.k;
+        g->step.reduce_lowp = p.step.args.reduce_lowp;
+        g->step.world = p.step.args.world;
+        g->step.nonfinite = p.step.args.nonfinite;
+        g->optimizer = p.step.optimizer;
+        g->state_dtype = p.step.state_dtype;
+    } else {
+        g->rsa.s = p.rsa.s;
+        g->rsa.world = p.rsa.world;
+        g->rsa.nonfinite = p.rsa.nonfinite;
+    }
+    g->gathers = p.separate_gathers;
+    g->first_unit = u;
+    g->grad_dtype = p.grad_dtype;
+    g->out_dtype = p.out_dtype;
+    return g;
 }
 
 void add_to_group(Group &G, const UnitPlan &p) {
-    const RsaArgs &a = p.rsa;
-    const int k = G.rsa.n;
-    GroupUnit &gu = G.rsa.u[k];
-    memset(&gu, 0, sizeof(gu));
-    for (int q = 0; q < a.world; ++q) gu.grads[q] = a.grads[q];
-    gu.master = a.master;
-    gu.m = a.m;
-    gu.v = a.v;
-    gu.out = a.out;
-    gu.numel = a.end;
-    gu.cta_begin = G.rsa_grid;
-    gu.ncta = group_update_ctas(a.end);
-    G.rsa_grid += gu.ncta;
-    G.rsa.n = k + 1;
+    const int k = G.n;
+    if (G.variant) {
+        const StepArgs &a = p.step.args;
+        StepGroupUnit &gu = G.step.u[k];
+        memset(&gu, 0, sizeof(gu));
+        for (int q = 0; q < a.world; ++q) gu.grads[q] = a.grads[q];
+        gu.param = a.param;
+        gu.s0 = a.s0;
+        gu.s1 = a.s1;
+        gu.out = a.out;
+        gu.numel = a.end;
+        gu.cta_begin = G.update_grid;
+        gu.ncta = group_update_ctas(a.end);
+        G.update_grid += gu.ncta;
+        G.step.n = k + 1;
+    } else {
+        const RsaArgs &a = p.rsa;
+        GroupUnit &gu = G.rsa.u[k];
+        memset(&gu, 0, sizeof(gu));
+        for (int q = 0; q < a.world; ++q) gu.grads[q] = a.grads[q];
+        gu.master = a.master;
+        gu.m = a.m;
+        gu.v = a.v;
+        gu.out = a.out;
+        gu.numel = a.end;
+        gu.cta_begin = G.update_grid;
+        gu.ncta = group_update_ctas(a.end);
+        G.update_grid += gu.ncta;
+        G.rsa.n = k + 1;
+    }
     if (G.gathers > 0) {
         GatherGroupUnit &gg = G.gather.u[k];
         memset(&gg, 0, sizeof(gg));
@@ -559,21 +645,18 @@ void add_to_group(Group &G, const UnitPlan &p) {
         G.gather_grid += group_gather_tiles(p.gather.nbytes);
         G.gather.n = k + 1;
     }
+    G.n = k + 1;
 }
 
 // The work items of a plan, in the order of each item's first unit: units
-// that qualify are batched with the earlier ones of the same world size,
-// dtypes and gathers (kGroupMax per group), a group of one is launched as
-// that unit alone, and every other unit keeps its own kernels.
+// that qualify are batched with the earlier ones of the same key
+// (kGroupMax per group), a group of one is launched as that unit alone, and
+// every other unit keeps its own kernels.
 void make_work(const std::vector<UnitPlan> &plan, std::vector<Work> &work,
                std::vector<std::unique_ptr<Group>> &groups) {
     work.clear();
     groups.clear();
-    struct Open {  // the group now filling for one key
-        int world, gd, od, gathers, n_dst;
-        Group *g;
-    };
-    std::vector<Open> open;
+    std::vector<std::pair<GroupKey, Group *>> open;  // the group now filling, per key
     for (size_t u = 0; u < plan.size(); ++u) {
         const UnitPlan &p = plan[u];
         if (p.empty) continue;
@@ -581,41 +664,40 @@ void make_work(const std::vector<UnitPlan> &plan, std::vector<Work> &work,
             work.push_back({static_cast<int>(u), nullptr});
             continue;
         }
-        const int nd = p.separate_gathers > 0 ? p.gather.n_dst : 0;
-        Open *slot = nullptr;
-        for (Open &o : open)
-            if (o.world == p.rsa.world && o.gd == p.grad_dtype && o.od == p.out_dtype &&
-                o.gathers == p.separate_gathers && o.n_dst == nd)
-                slot = &o;
-        if (!slot || slot->g->rsa.n == kGroupMax) {
-            groups.push_back(std::unique_ptr<Group>(new Group()));
-            Group *g = groups.back().get();
-            memset(&g->rsa, 0, sizeof(g->rsa));
-            memset(&g->gather, 0, sizeof(g->gather));
-            g->rsa.s = p.rsa.s;  // every unit of a group has the same hyperparameters and N
-            g->rsa.nonfinite = p.rsa.nonfinite;
-            g->rsa.world = p.rsa.world;
-            g->gathers = p.separate_gathers;
-            g->first_unit = static_cast<int>(u);
-            g->grad_dtype = p.grad_dtype;
-            g->out_dtype = p.out_dtype;
+        const GroupKey key = key_of(p);
+        std::pair<GroupKey, Group *> *slot = nullptr;
+        for (auto &o : open)
+            if (o.first == key) slot = &o;
+        if (!slot || slot->second->n == kGroupMax) {
+            Group *g = new_group(groups, p, static_cast<int>(u));
             work.push_back({-1, g});
             if (slot) {
-                slot->g = g;
+                slot->second = g;
             } else {
-                open.push_back({p.rsa.world, p.grad_dtype, p.out_dtype, p.separate_gathers, nd, g});
+                open.push_back({key, g});
+                slot = &open.back();
             }
-            slot = nullptr;
-            for (Open &o : open)
-                if (o.g == g) slot = &o;
         }
-        add_to_group(*slot->g, p);
+        add_to_group(*slot->second, p);
     }
     for (Work &w : work)
-        if (w.group && w.group->rsa.n == 1) {
+        if (w.group && w.group->n == 1) {
             w.unit = w.group->first_unit;
             w.group = nullptr;
         }
+}
+
+fsdp_status launch_step_group(const Group &G, cudaStream_t s) {
+    switch (G.optimizer) {
+        case FSDP_OPT_ADAMW:
+            return launch_step_group_adamw(G.step, G.grad_dtype, G.out_dtype, G.state_dtype, G.update_grid, s);
+        case FSDP_OPT_SGD:
+            return launch_step_group_sgd(G.step, G.grad_dtype, G.out_dtype, G.state_dtype, G.update_grid, s);
+        case FSDP_OPT_ADAMAX:
+            return launch_step_group_adamax(G.step, G.grad_dtype, G.out_dtype, G.state_dtype, G.update_grid, s);
+        default:
+            return launch_step_group_adadelta(G.step, G.grad_dtype, G.out_dtype, G.state_dtype, G.update_grid, s);
+    }
 }
 
 // Launch one work item on s; under capture, *node receives its update node.
@@ -630,10 +712,11 @@ fsdp_status launch_work(const std::vector<UnitPlan> &plan, const Work &w, cudaSt
         return launch_unit(p, s, node ? &node->node : nullptr);
     }
     const Group &G = *w.group;
-    fsdp_status st = launch_rsa_group(G.rsa, G.grad_dtype, G.out_dtype, G.rsa_grid, s);
+    fsdp_status st = G.variant ? launch_step_group(G, s)
+                               : launch_rsa_group(G.rsa, G.grad_dtype, G.out_dtype, G.update_grid, s);
     if (st == FSDP_OK && node) {
-        node->kind = kNodeGroup;
-        node->world = G.rsa.world;
+        node->kind = G.variant ? kNodeVariantGroup : kNodeGroup;
+        node->world = G.variant ? G.step.world : G.rsa.world;
         node->grad_dtype = G.grad_dtype;
         st = last_captured_node(s, &node->node);
     }
@@ -981,12 +1064,19 @@ FSDP_API fsdp_status fsdp_step_graph_launch_ex(fsdp_step_graph *graph, const fsd
     if (cfg->step < 1 || !(cfg->grad_scale > 0.0f) || !isfinite(cfg->grad_scale)) return FSDP_ERR_INVALID_ARG;
     for (const UpdateNode &n : graph->nodes)
         if (cfg->reduce_dtype != FSDP_F32 && cfg->reduce_dtype != n.grad_dtype) return FSDP_ERR_UNSUPPORTED_DTYPE;
+    const int lowp = cfg->reduce_dtype != FSDP_F32 ? 1 : 0;
     for (const UpdateNode &n : graph->nodes) {
-        const int world = n.world;
-        fsdp_status st = set_update_node<StepArgs, 4>(graph, n.node, [&](StepArgs &a) {
-            a.k = make_step_scalars(*cfg, world);
-            a.reduce_lowp = cfg->reduce_dtype != FSDP_F32 ? 1 : 0;
-        });
+        const StepScalars k = make_step_scalars(*cfg, n.world);
+        fsdp_status st = n.kind == kNodeVariantGroup
+                             ? set_update_node<StepGroupArgs, 1>(graph, n.node,
+                                                                 [&](StepGroupArgs &a) {
+                                                                     a.k = k;
+                                                                     a.reduce_lowp = lowp;
+                                                                 })
+                             : set_update_node<StepArgs, 4>(graph, n.node, [&](StepArgs &a) {
+                                   a.k = k;
+                                   a.reduce_lowp = lowp;
+                               });
         if (st != FSDP_OK) return st;
     }
     return cuda_status(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));

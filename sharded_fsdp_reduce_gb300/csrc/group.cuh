@@ -60,7 +60,33 @@ struct GatherGroupArgs {
     GatherGroupUnit u[kGroupMax];
 };
 
+// One unit of a batched variant step (fsdp_reduce_scatter_step's update):
+// all ranks' blocks [0, numel), every base pointer 16-byte aligned, the
+// parameter in device memory.
+struct StepGroupUnit {
+    const void *grads[kGroupMaxWorld];  // world pointers used
+    void *param;
+    void *s0;
+    void *s1;   // NULL for SGD
+    void *out;  // NULL for bf16/fp16 state
+    int64_t numel;
+    int64_t cta_begin;
+    int32_t ncta;
+    int32_t pad;
+};
+
+struct StepGroupArgs {
+    StepScalars k;        // first members: the block a captured step rewrites per step
+    int32_t reduce_lowp;
+    int32_t world;
+    uint32_t *nonfinite;
+    int32_t n;
+    int32_t pad;
+    StepGroupUnit u[kGroupMax];
+};
+
 static_assert(sizeof(RsaGroupArgs) < 32764, "kernel parameter space");
+static_assert(sizeof(StepGroupArgs) < 32764, "kernel parameter space");
 static_assert(sizeof(GatherGroupArgs) < 32764, "kernel parameter space");
 
 // CTAs of one unit in a batched update, and tiles of one unit in a batched
@@ -72,5 +98,18 @@ int64_t group_gather_tiles(int64_t nbytes);
 // Launch `grid` CTAs of the batched kernels on stream s.
 fsdp_status launch_rsa_group(const RsaGroupArgs &g, int grad_dtype, int out_dtype, int64_t grid, cudaStream_t s);
 fsdp_status launch_gather_group(const GatherGroupArgs &g, int64_t grid, cudaStream_t s);
+
+// The batched variant step, one translation unit per optimizer
+// (step_group_<optimizer>.cu); (state, out) dtype pairs as the per-unit
+// variant kernel: fp32 state with any compute dtype, or bf16/fp16 state that
+// is its own shard.
+fsdp_status launch_step_group_adamw(const StepGroupArgs &g, int grad_dtype, int out_dtype, int state_dtype,
+                                    int64_t grid, cudaStream_t s);
+fsdp_status launch_step_group_sgd(const StepGroupArgs &g, int grad_dtype, int out_dtype, int state_dtype,
+                                  int64_t grid, cudaStream_t s);
+fsdp_status launch_step_group_adamax(const StepGroupArgs &g, int grad_dtype, int out_dtype, int state_dtype,
+                                     int64_t grid, cudaStream_t s);
+fsdp_status launch_step_group_adadelta(const StepGroupArgs &g, int grad_dtype, int out_dtype, int state_dtype,
+                                       int64_t grid, cudaStream_t s);
 
 }  // namespace fsdp

@@ -146,18 +146,18 @@ def test_batched_and_own_launches_in_one_call(F):
 @pytest.mark.parametrize("gathers", [1, 2])
 def test_batched_units_in_a_captured_step(F, gathers):
     # the captured step holds batched update nodes; each launch rewrites their
-    # scalars, and four launches over changing hyperparameters equal the
-    # eager driver, bit for bit
+    # scalars, and four launches over changing hyperparameters equal stepping
+    # each unit alone, bit for bit
     rng = np.random.default_rng(40 + gathers)
     specs = [(int(n), 8, torch.bfloat16, torch.bfloat16) for n in rng.integers(1, 50000, 60)]
     specs += [(int(n), 2, torch.float16, torch.float16) for n in rng.integers(1, 50000, 10)]
     a, b = make_units(F, specs, 31)
     graph = F.UnitSequence(a).capture(gathers=gathers)
-    seq_b = F.UnitSequence(b)
     for t in (1, 2, 3, 4):
         load_grads([a, b], t, 9)
         graph.launch(hp(F, t))
-        seq_b.step(hp(F, t), gathers=gathers)
+        for u in b:
+            u.step(hp(F, t), gathers=gathers)
         torch.cuda.synchronize()
         assert_units_equal(a, b, gathers)
     graph.close()
@@ -193,3 +193,101 @@ def test_batched_units_match_oracle_and_count_nonfinite(F, orc):
                 np.testing.assert_array_equal(host(u.exp_avg_sq).view(np.uint32), v.view(np.uint32))
                 np.testing.assert_array_equal(host(u.shard_out), shards_o)
     assert int(ca.item()) == int(cb.item()) == 2
+
+
+def make_variant_units(F, specs, seed, optimizer, state_dtype):
+    g = torch.Generator().manual_seed(seed)
+    a, b = [], []
+    for numel, world, gdt, odt in specs:
+        x = torch.rand(numel, generator=g) * 0.2 - 0.1
+        for dst in (a, b):
+            u = F.FlatParamUnit([("w", (numel,))], world, gdt, odt, device=DEV, optimizer=optimizer,
+                                state_dtype=state_dtype)
+            u.load_master([x.to(DEV)])
+            dst.append(u)
+    torch.cuda.synchronize()
+    return a, b
+
+
+def assert_variant_units_equal(a, b, gathers):
+    for k, (ua, ub) in enumerate(zip(a, b)):
+        for name in ("master", "exp_avg", "exp_avg_sq", "shard_out"):
+            x, y = getattr(ua, name), getattr(ub, name)
+            if x is not None:
+                assert same(x, y), (k, name)
+        for fa, fb in zip(ua.full, ub.full):
+            assert same(fa, fb), k
+        if gathers:
+            for f in ua.full:
+                assert same(f, ua.shard_out), k
+
+
+VHP = {"adamw": (1e-3, 0.9, 0.999, 1e-8, 0.01), "sgd": (1e-2, 0.9, 0.0, 0.0, 1e-2),
+       "adamax": (2e-3, 0.9, 0.999, 1e-8, 1e-2), "adadelta": (1.0, 0.9, 0.0, 1e-6, 1e-2)}
+
+
+def vcfg(F, opt, t, lowp_dtype=None):
+    lr, b1, b2, eps, wd = VHP[opt]
+    return F.StepConfig(opt, lr * (1 + 0.1 * t), b1, b2, eps, wd, t, reduce_dtype=lowp_dtype)
+
+
+@pytest.mark.parametrize("opt", ["sgd", "adamax", "adadelta", "adamw"])
+@pytest.mark.parametrize("state", ["f32", "bf16"])
+def test_small_variant_units_batched_equal_their_own_steps(F, opt, state):
+    # the variant step batched: every optimizer, fp32 or bf16 state, a
+    # bf16 reduce-scatter on the later steps, N in {2, 4, 8}, sizes from 1
+    # element to 40 k; bit-equal to each unit's own fsdp_reduce_scatter_step
+    rng = np.random.default_rng(sum(map(ord, opt + state)))
+    sdt = torch.float32 if state == "f32" else torch.bfloat16
+    specs = [(int(n), int(w), torch.bfloat16, torch.bfloat16)
+             for n, w in zip(rng.integers(1, 40000, 60), rng.choice([2, 4, 8], 60))]
+    specs[0] = (1, 8, torch.bfloat16, torch.bfloat16)
+    a, b = make_variant_units(F, specs, 51, opt, sdt)
+    seq = F.UnitSequence(a)
+    for t in (1, 2, 3):
+        load_grads([a, b], t, 23)
+        cfg = vcfg(F, opt, t, torch.bfloat16 if t > 1 else None)
+        seq.step(cfg, gathers=1)
+        for u in b:
+            u.step(cfg, gathers=1)
+        torch.cuda.synchronize()
+        assert_variant_units_equal(a, b, 1)
+
+
+def test_batched_variant_units_in_a_captured_step(F):
+    # a captured SGD step with batched variant nodes: each launch rewrites
+    # their scalars and reduction flag; equal to stepping each unit alone
+    rng = np.random.default_rng(61)
+    specs = [(int(n), 8, torch.bfloat16, torch.bfloat16) for n in rng.integers(1, 50000, 50)]
+    a, b = make_variant_units(F, specs, 62, "sgd", torch.float32)
+    graph = F.UnitSequence(a).capture(gathers=2, config=vcfg(F, "sgd", 1))
+    for t in (1, 2, 3, 4):
+        load_grads([a, b], t, 29)
+        cfg = vcfg(F, "sgd", t, torch.bfloat16 if t % 2 == 0 else None)
+        graph.launch(cfg)
+        for u in b:
+            u.step(cfg, gathers=2)
+        torch.cuda.synchronize()
+        assert_variant_units_equal(a, b, 2)
+    graph.close()
+
+
+def test_batched_variant_units_match_oracle(F, orc):
+    # a batched Adamax group with bf16 state against the oracle, bit for bit
+    rng = np.random.default_rng(71)
+    specs = [(int(n), 4, torch.bfloat16, torch.bfloat16) for n in rng.integers(1, 20000, 30)]
+    a, b = make_variant_units(F, specs, 72, "adamax", torch.bfloat16)
+    st = [[host(u.master).copy(), np.zeros(u.padded_numel, np.uint16), np.zeros(u.padded_numel, np.uint16)]
+          for u in a]
+    seq = F.UnitSequence(a)
+    lr, b1, b2, eps, wd = VHP["adamax"]
+    for t in (1, 2):
+        load_grads([a, b], t, 31)
+        seq.step(vcfg(F, "adamax", t), gathers=1)
+        torch.cuda.synchronize()
+        for u, (p, s0, s1) in zip(a, st):
+            orc.step_ex("adamax", False, [host(gr) for gr in u.grads], "bf16", u.world, p, s0, s1, "bf16", "bf16",
+                        orc.hparams(lr * (1 + 0.1 * t), b1, b2, eps, wd, t))
+            np.testing.assert_array_equal(host(u.master), p)
+            np.testing.assert_array_equal(host(u.exp_avg), s0)
+            np.testing.assert_array_equal(host(u.exp_avg_sq), s1)
