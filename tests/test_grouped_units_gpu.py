@@ -92,17 +92,21 @@ def test_small_units_batched_equal_their_own_steps(F, gathers):
         assert_units_equal(a, b, gathers)
 
 
-def _odd_unit(F, numel, world, offset, seed):
+def _odd_unit(F, numel, world, offset, seed, host_grads=False):
     """A unit whose buffers start `offset` elements into their allocations
-    (offset 1: not 16-byte aligned, so it keeps its own launches)."""
+    (offset 1: not 16-byte aligned, so it keeps its own launches); with
+    host_grads its gradients are pinned host memory the kernel reads over
+    the host link (the unit still batches when aligned)."""
     g = torch.Generator().manual_seed(seed)
     P = F.fsdp_padded_numel(numel, world)
 
-    def alloc(dt):
+    def alloc(dt, pinned=False):
+        if pinned:
+            return torch.zeros(P + offset, dtype=dt, pin_memory=True)[offset:]
         return torch.zeros(P + offset, dtype=dt, device=DEV)[offset:]
 
     u = types.SimpleNamespace(world=world, numel=numel, padded_numel=P)
-    u.grads = [alloc(torch.bfloat16) for _ in range(world)]
+    u.grads = [alloc(torch.bfloat16, host_grads) for _ in range(world)]
     u.master, u.exp_avg, u.exp_avg_sq = alloc(torch.float32), alloc(torch.float32), alloc(torch.float32)
     u.shard_out = alloc(torch.bfloat16)
     u.full = [alloc(torch.bfloat16) for _ in range(world)]
@@ -111,9 +115,10 @@ def _odd_unit(F, numel, world, offset, seed):
 
 
 def test_batched_and_own_launches_in_one_call(F):
-    # small aligned units batch; an unaligned unit, a unit of N = 3, a unit
-    # with host-resident state and a unit above the batching size keep their
-    # own kernels, all in one call, all equal to stepping each unit alone
+    # small aligned units batch (one of them reading its gradients from
+    # pinned host memory); an unaligned unit, a unit of N = 3, a unit with
+    # host-resident state and a unit above the batching size keep their own
+    # kernels, all in one call, all equal to stepping each unit alone
     specs = [(int(n), 4, torch.bfloat16, torch.bfloat16) for n in (5000, 333, 70000, 12, 4099, 65536)]
     a, b = make_units(F, specs, 21)
     for dst in (a, b):
@@ -128,6 +133,9 @@ def test_batched_and_own_launches_in_one_call(F):
     oa, ob = _odd_unit(F, 5000, 4, 1, 5), _odd_unit(F, 5000, 4, 1, 5)
     a.insert(2, oa)
     b.insert(2, ob)
+    ha, hb = _odd_unit(F, 7777, 4, 0, 6, host_grads=True), _odd_unit(F, 7777, 4, 0, 6, host_grads=True)
+    a.insert(4, ha)
+    b.insert(4, hb)
     torch.cuda.synchronize()
     for t in (1, 2):
         g = torch.Generator().manual_seed(100 + t)
