@@ -92,6 +92,22 @@ def test_small_units_batched_equal_their_own_steps(F, gathers):
         assert_units_equal(a, b, gathers)
 
 
+def test_a_full_group_and_a_group_of_one(F):
+    # 129 units of one kind: a full group of 128 and one unit left over,
+    # which is launched on its own; both bit-equal to each unit's own step
+    rng = np.random.default_rng(5)
+    specs = [(int(n), 2, torch.bfloat16, torch.bfloat16) for n in rng.integers(1, 3000, 129)]
+    a, b = make_units(F, specs, 13)
+    seq = F.UnitSequence(a)
+    for t in (1, 2):
+        load_grads([a, b], t, 37)
+        seq.step(hp(F, t), gathers=1)
+        for u in b:
+            u.step(hp(F, t), gathers=1)
+        torch.cuda.synchronize()
+        assert_units_equal(a, b, 1)
+
+
 def _odd_unit(F, numel, world, offset, seed, host_grads=False):
     """A unit whose buffers start `offset` elements into their allocations
     (offset 1: not 16-byte aligned, so it keeps its own launches); with
