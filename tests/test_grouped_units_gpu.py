@@ -278,6 +278,32 @@ def test_small_variant_units_batched_equal_their_own_steps(F, opt, state):
         assert_variant_units_equal(a, b, 1)
 
 
+@pytest.mark.parametrize("opt,state", [("sgd", "f16"), ("adamw", "f16"), ("adadelta", "f32")])
+def test_small_variant_units_fp16_with_loss_scale(F, opt, state):
+    # fp16 gradients carrying a static loss scale of 1024 (unscaled inside the
+    # step), fp16 or fp32 state, an fp16 reduce-scatter on the later steps
+    rng = np.random.default_rng(len(opt) + len(state))
+    sdt = torch.float16 if state == "f16" else torch.float32
+    specs = [(int(n), int(w), torch.float16, torch.float16)
+             for n, w in zip(rng.integers(1, 30000, 40), rng.choice([2, 4, 8], 40))]
+    a, b = make_variant_units(F, specs, 81, opt, sdt)
+    seq = F.UnitSequence(a)
+    lr, b1, b2, eps, wd = VHP[opt]
+    for t in (1, 2, 3):
+        g = torch.Generator().manual_seed(900 + t)
+        for ua, ub in zip(a, b):
+            for r in range(ua.world):
+                x = (torch.randn(ua.numel, generator=g) * 1e-2 * 1024).to(DEV, torch.float16)
+                ua.load_grad(r, [x])
+                ub.load_grad(r, [x])
+        cfg = F.StepConfig(opt, lr, b1, b2, eps, wd, t, 1024.0, reduce_dtype=torch.float16 if t > 1 else None)
+        seq.step(cfg, gathers=1)
+        for u in b:
+            u.step(cfg, gathers=1)
+        torch.cuda.synchronize()
+        assert_variant_units_equal(a, b, 1)
+
+
 def test_batched_variant_units_in_a_captured_step(F):
     # a captured SGD step with batched variant nodes: each launch rewrites
     # their scalars and reduction flag; equal to stepping each unit alone
