@@ -311,9 +311,9 @@ fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
  * unit's kernels run in order on one of them and overlap the neighbouring
  * unit's. Work enqueued on `stream` after the call sees every unit done.
  * Batching: small units are stepped together, up to 128 per launch of each
- * kernel, when they share N (2, 4 or 8), the dtype pair, n_full (at most 8)
- * and the gathers, and each has at most 2^22 elements, 16-byte aligned
- * buffers, its state in device memory and no fused gather; every element
+ * kernel, when they share N (2, 4 or 8), the dtype pair and the gathers,
+ * and each has at most 2^22 elements, at most 8 gathered buffers, 16-byte
+ * aligned buffers, its state in device memory and no fused gather; every element
  * sees the same operations as in the unit's own launch, so the results are
  * the same bits. Every other unit keeps its own launches. */
 fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,

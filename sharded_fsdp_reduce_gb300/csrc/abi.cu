@@ -517,14 +517,15 @@ struct UpdateNode {
 
 // What batched units must share: the update (fused AdamW, or the variant
 // kernel with its optimizer, state dtype and reduction), N, the dtypes and
-// the gathers.
+// the number of gathers (each unit keeps its own gathered buffers, 1 to
+// kGroupMaxWorld of them).
 struct GroupKey {
     bool variant;
-    int optimizer, state_dtype, reduce_lowp, world, grad_dtype, out_dtype, gathers, n_dst;
+    int optimizer, state_dtype, reduce_lowp, world, grad_dtype, out_dtype, gathers;
     bool operator==(const GroupKey &o) const {
         return variant == o.variant && optimizer == o.optimizer && state_dtype == o.state_dtype &&
                reduce_lowp == o.reduce_lowp && world == o.world && grad_dtype == o.grad_dtype &&
-               out_dtype == o.out_dtype && gathers == o.gathers && n_dst == o.n_dst;
+               out_dtype == o.out_dtype && gathers == o.gathers;
     }
 };
 
@@ -538,7 +539,6 @@ GroupKey key_of(const UnitPlan &p) {
     k.grad_dtype = p.grad_dtype;
     k.out_dtype = p.out_dtype;
     k.gathers = p.separate_gathers;
-    k.n_dst = p.separate_gathers > 0 ? p.gather.n_dst : 0;
     return k;
 }
 

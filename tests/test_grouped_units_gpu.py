@@ -92,6 +92,29 @@ def test_small_units_batched_equal_their_own_steps(F, gathers):
         assert_units_equal(a, b, gathers)
 
 
+def test_units_with_different_gather_fanouts_batch_together(F):
+    # one batch of units with 1 to 8 gathered buffers each (n_full); every
+    # buffer receives the unit's shards, bit-equal to each unit's own step
+    rng = np.random.default_rng(9)
+    g = torch.Generator().manual_seed(19)
+    a, b = [], []
+    for k in range(30):
+        numel, n_full = int(rng.integers(1, 20000)), int(rng.integers(1, 9))
+        x = torch.rand(numel, generator=g) * 0.2 - 0.1
+        for dst in (a, b):
+            u = F.FlatParamUnit([("w", (numel,))], 8, torch.bfloat16, torch.bfloat16, device=DEV, n_full=n_full)
+            u.load_master([x.to(DEV)])
+            dst.append(u)
+    seq = F.UnitSequence(a)
+    for t in (1, 2):
+        load_grads([a, b], t, 41)
+        seq.step(hp(F, t), gathers=2)
+        for u in b:
+            u.step(hp(F, t), gathers=2)
+        torch.cuda.synchronize()
+        assert_units_equal(a, b, 2)
+
+
 def test_a_full_group_and_a_group_of_one(F):
     # 129 units of one kind: a full group of 128 and one unit left over,
     # which is launched on its own; both bit-equal to each unit's own step
