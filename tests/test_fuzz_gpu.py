@@ -239,3 +239,63 @@ def test_fuzz_step_graph(F, seed):
             iv = torch.int32 if fa.element_size() == 4 else torch.int16
             assert torch.equal(fa.view(iv), fb.view(iv)), seed
     graph.close()
+
+
+def _same(x, y):
+    iv = torch.int32 if x.element_size() == 4 else torch.int16
+    return torch.equal(x.view(iv), y.view(iv))
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_fuzz_batched_models(F, seed):
+    # a random model of 2-160 units for the batched launches: mostly small
+    # units of N in {2, 4, 8} and two dtype pairs, 1-8 gathered buffers each,
+    # among them units that keep their own launches (N = 3, host-resident
+    # state, above the batching size); stepped by fsdp_step_units (even
+    # seeds) or a captured step (odd seeds) and compared bit for bit with
+    # each unit stepped alone
+    rng = np.random.default_rng(7000 + seed)
+    n_units = int(rng.integers(2, 161))
+    gathers = int(rng.integers(0, 3))
+    pairs = [(torch.bfloat16, torch.bfloat16), (torch.bfloat16, torch.float16), (torch.float32, torch.bfloat16)]
+    a, b = [], []
+    g = torch.Generator().manual_seed(seed)
+    for _ in range(n_units):
+        kind = rng.random()
+        world = 3 if kind < 0.05 else int(rng.choice([2, 4, 8], p=[0.2, 0.2, 0.6]))
+        P = int(rng.integers((1 << 22) + 1, (1 << 22) + 5000)) if kind > 0.98 else int(rng.integers(1, 60000))
+        host_state = 0.05 <= kind < 0.1
+        gdt, odt = pairs[int(rng.integers(0, 2 if seed % 3 else 3))]
+        n_full = int(rng.integers(1, 9))
+        x = torch.rand(P, generator=g) * 0.2 - 0.1
+        for dst in (a, b):
+            u = F.FlatParamUnit([("x", (P,))], world, gdt, odt, device=DEV, n_full=n_full, state_on_host=host_state)
+            u.load_master([x.to(DEV)])
+            dst.append(u)
+    torch.cuda.synchronize()
+    graph = F.UnitSequence(a).capture(gathers=gathers) if seed % 2 else None
+    seq = F.UnitSequence(a)
+    for t in (1, 2, 3):
+        gg = torch.Generator().manual_seed(100 * seed + t)
+        for ua, ub in zip(a, b):
+            for r in range(ua.world):
+                xg = (torch.randn(ua.numel, generator=gg) * 1e-2).to(DEV, ua.grads[r].dtype)
+                ua.load_grad(r, [xg])
+                ub.load_grad(r, [xg])
+        hp = F.AdamWHParams(1e-3 * t, 0.9, 0.999, 1e-8, 0.01, t)
+        if graph is not None:
+            graph.launch(hp)
+        else:
+            seq.step(hp, gathers=gathers)
+        for u in b:
+            u.step(hp, gathers=gathers)
+        torch.cuda.synchronize()
+        for k, (ua, ub) in enumerate(zip(a, b)):
+            for name in ("master", "exp_avg", "exp_avg_sq", "shard_out"):
+                assert _same(getattr(ua, name), getattr(ub, name)), (seed, k, name, t)
+            for fa, fb in zip(ua.full, ub.full):
+                assert _same(fa, fb), (seed, k, t)
+    if graph is not None:
+        graph.close()
+    del a, b
+    torch.cuda.empty_cache()
