@@ -1,0 +1,34 @@
+"""Host logic of bench.py that needs no GPU: the launch count it claims for
+the driver legs follows the library's batching rule (units of at most 2^22
+elements batched up to 128 per launch, a unit above that size launched on
+its own)."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_model_launches_follow_the_batching_rule():
+    # 12 GPT-2 small blocks (7.09 M elements): one update and one gather each
+    assert bench.model_launches(12, 7087872, 1) == 24
+    # 200 units of 50,000: groups of 128 and 72, an update and a gather each
+    assert bench.model_launches(200, 50000, 1) == 4
+    assert bench.model_launches(200, 50000, 2) == 6
+    assert bench.model_launches(200, 50000, 0) == 2
+    # 128 fill one group; 129 leave one unit, launched on its own
+    assert bench.model_launches(128, 1000, 1) == 2
+    assert bench.model_launches(129, 1000, 1) == 4
+    # the size limit is inclusive
+    assert bench.model_launches(3, 1 << 22, 1) == 2
+    assert bench.model_launches(3, (1 << 22) + 8, 1) == 6
+    assert bench.GROUP_MAX_UNITS == 128 and bench.GROUP_MAX_NUMEL == 1 << 22
+
+
+def test_batching_constants_match_the_library():
+    import re
+    src = open(os.path.join(ROOT, "sharded_fsdp_reduce_gb300", "csrc", "group.cuh")).read()
+    assert int(re.search(r"kGroupMax = (\d+);", src).group(1)) == bench.GROUP_MAX_UNITS
+    assert int(re.search(r"kGroupMaxNumel = int64_t\(1\) << (\d+);", src).group(1)) == 22
