@@ -256,7 +256,7 @@ def timed_calls(fn, K: int, stream, flush: L2Flush) -> float:
 
 
 GROUP_MAX_UNITS = 128          # the library's batched launches: units per launch
-GROUP_MAX_NUMEL = 1 << 22      # and the largest unit they take
+GROUP_MAX_NUMEL = 1 << 24      # and the largest unit they take
 
 
 def model_launches(n_units: int, numel: int, gathers: int) -> int:

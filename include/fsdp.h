@@ -312,7 +312,7 @@ fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
  * unit's. Work enqueued on `stream` after the call sees every unit done.
  * Batching: small units are stepped together, up to 128 per launch of each
  * kernel, when they share N (2, 4 or 8), the dtype pair and the gathers,
- * and each has at most 2^22 elements, at most 8 gathered buffers, 16-byte
+ * and each has at most 2^24 elements, at most 8 gathered buffers, 16-byte
  * aligned buffers, its state in device memory and no fused gather; every element
  * sees the same operations as in the unit's own launch, so the results are
  * the same bits. Every other unit keeps its own launches. */

@@ -19,7 +19,10 @@ namespace fsdp {
 
 constexpr int kGroupMax = 128;                          // units per batched launch
 constexpr int kGroupMaxWorld = 8;                       // gradient / destination pointers per unit
-constexpr int64_t kGroupMaxNumel = int64_t(1) << 22;    // units of up to 4 M elements are batched
+#ifndef FSDP_GROUP_MAX_NUMEL_LOG2
+#define FSDP_GROUP_MAX_NUMEL_LOG2 24
+#endif
+constexpr int64_t kGroupMaxNumel = int64_t(1) << FSDP_GROUP_MAX_NUMEL_LOG2;  // units up to this size are batched
 constexpr int kGroupGatherTile = 16384;                 // bytes per CTA of the batched gather
 
 // One unit of a batched update: all ranks' blocks [0, numel), every base

@@ -1,5 +1,5 @@
 """Host logic of bench.py that needs no GPU: the launch count it claims for
-the driver legs follows the library's batching rule (units of at most 2^22
+the driver legs follows the library's batching rule (units of at most 2^24
 elements batched up to 128 per launch, a unit above that size launched on
 its own)."""
 import os
@@ -12,8 +12,10 @@ import bench  # noqa: E402
 
 
 def test_model_launches_follow_the_batching_rule():
-    # 12 GPT-2 small blocks (7.09 M elements): one update and one gather each
-    assert bench.model_launches(12, 7087872, 1) == 24
+    # 12 GPT-2 small blocks (7.09 M elements): one group, an update and a gather
+    assert bench.model_launches(12, 7087872, 1) == 2
+    # units above the size limit: one update and one gather each
+    assert bench.model_launches(12, 855654400, 1) == 24
     # 200 units of 50,000: groups of 128 and 72, an update and a gather each
     assert bench.model_launches(200, 50000, 1) == 4
     assert bench.model_launches(200, 50000, 2) == 6
@@ -22,13 +24,13 @@ def test_model_launches_follow_the_batching_rule():
     assert bench.model_launches(128, 1000, 1) == 2
     assert bench.model_launches(129, 1000, 1) == 4
     # the size limit is inclusive
-    assert bench.model_launches(3, 1 << 22, 1) == 2
-    assert bench.model_launches(3, (1 << 22) + 8, 1) == 6
-    assert bench.GROUP_MAX_UNITS == 128 and bench.GROUP_MAX_NUMEL == 1 << 22
+    assert bench.model_launches(3, 1 << 24, 1) == 2
+    assert bench.model_launches(3, (1 << 24) + 8, 1) == 6
+    assert bench.GROUP_MAX_UNITS == 128 and bench.GROUP_MAX_NUMEL == 1 << 24
 
 
 def test_batching_constants_match_the_library():
     import re
     src = open(os.path.join(ROOT, "sharded_fsdp_reduce_gb300", "csrc", "group.cuh")).read()
     assert int(re.search(r"kGroupMax = (\d+);", src).group(1)) == bench.GROUP_MAX_UNITS
-    assert int(re.search(r"kGroupMaxNumel = int64_t\(1\) << (\d+);", src).group(1)) == 22
+    assert 1 << int(re.search(r"#define FSDP_GROUP_MAX_NUMEL_LOG2 (\d+)", src).group(1)) == bench.GROUP_MAX_NUMEL

@@ -263,7 +263,7 @@ def test_fuzz_batched_models(F, seed):
     for _ in range(n_units):
         kind = rng.random()
         world = 3 if kind < 0.05 else int(rng.choice([2, 4, 8], p=[0.2, 0.2, 0.6]))
-        P = int(rng.integers((1 << 22) + 1, (1 << 22) + 5000)) if kind > 0.98 else int(rng.integers(1, 60000))
+        P = int(rng.integers((1 << 24) + 1, (1 << 24) + 5000)) if kind > 0.98 else int(rng.integers(1, 60000))
         host_state = 0.05 <= kind < 0.1
         gdt, odt = pairs[int(rng.integers(0, 2 if seed % 3 else 3))]
         n_full = int(rng.integers(1, 9))

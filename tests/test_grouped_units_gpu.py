@@ -164,7 +164,7 @@ def test_batched_and_own_launches_in_one_call(F):
         dst.append(F.FlatParamUnit([("w", (3001,))], 3, torch.bfloat16, torch.bfloat16, device=DEV))
         dst.append(F.FlatParamUnit([("w", (9000,))], 4, torch.bfloat16, torch.bfloat16, device=DEV,
                                    state_on_host=True))
-        dst.append(F.FlatParamUnit([("w", ((1 << 22) + 8,))], 4, torch.bfloat16, torch.bfloat16, device=DEV))
+        dst.append(F.FlatParamUnit([("w", ((1 << 24) + 8,))], 4, torch.bfloat16, torch.bfloat16, device=DEV))
     for k in range(len(specs), len(a)):
         x = torch.rand(a[k].numel) * 0.2 - 0.1
         a[k].load_master([x.to(DEV)])
