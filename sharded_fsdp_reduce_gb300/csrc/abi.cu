@@ -546,8 +546,9 @@ GroupKey key_of(const UnitPlan &p) {
 // fused gather), N in {2, 4, 8}, at most kGroupMaxNumel elements, every base
 // pointer 16-byte aligned (the vector path and the bulk copies), the
 // parameter or master in device memory and at most kGroupMaxWorld gathered
-// buffers. Larger units gain nothing from batching and keep their own
-// launches.
+// buffers. Larger units fill the GPU on their own and keep their own
+// launches, whose gather (several tiles in flight per CTA, 3 CTAs per SM)
+// measured faster at those sizes than the batched gather's one-tile CTAs.
 bool groupable(const UnitPlan &p) {
     if (p.empty) return false;
     const void *state = nullptr;
