@@ -283,9 +283,13 @@ class _HostPipeline:
 
 
 class UnitSequence:
-    """The FSDP units of a model, stepped in order by one call into the
-    library (fsdp_step_units): per unit the fused update and its all-gathers,
-    all on one stream, with the per-unit loop in native code."""
+    """The FSDP units of a model, stepped by one call into the library
+    (fsdp_step_units, or fsdp_step_units_ex for the variant steps): per unit
+    the update and its all-gathers, ordered on the caller's stream. The
+    native loop spreads the units over two side streams and batches units of
+    up to 2^24 elements that share N, dtypes and gathers into one launch per
+    kernel (128 units at most); the results are those of stepping each unit
+    on its own."""
 
     def __init__(self, units: Sequence[FlatParamUnit]):
         self.units = list(units)
