@@ -8,6 +8,9 @@ invariants the pages fix must hold exactly.
   the sharded step equals the full-replica step on the averaged gradient.
 * The pad of a FlatParameter stays zero (zero gradients, zero state).
 * The compute-dtype cast is exact on values the dtype holds.
+* The same sharded-equals-replica identity for every variant optimizer and
+  state precision ([FAIR] "限制与兼容性说明": FSDP is exact for pointwise
+  optimizers).
 """
 import numpy as np
 import pytest
@@ -84,3 +87,38 @@ def test_flatten_layout(orc, numels, world):
     for k, n in enumerate(numels):
         np.testing.assert_array_equal(flat[offs[k]:offs[k] + n], parts[k])
     assert not flat[total:].any()
+
+
+OPTS = {"adamw": (0.9, 0.999, 1e-8), "sgd": (0.9, 0.0, 0.0), "adamax": (0.9, 0.999, 1e-8),
+        "adadelta": (0.9, 0.0, 1e-6)}
+
+
+@given(opt=st.sampled_from(sorted(OPTS)), world=st.integers(1, 9), P=st.integers(1, 1500),
+       gfmt=st.sampled_from(FMT), sfmt=st.sampled_from(FMT), steps=st.integers(1, 3),
+       lr=st.floats(1e-4, 1e-1), wd=st.sampled_from([0.0, 0.01]), seed=st.integers(0, 2**31))
+@settings(**SETTINGS)
+def test_variant_sharded_step_equals_one_replica(orc, opt, world, P, gfmt, sfmt, steps, lr, wd, seed):
+    # every optimizer and state precision: the N-rank step (each rank its own
+    # block) equals one replica stepped with the all-reduce average, bit for
+    # bit, and the pad stays zero
+    rng = np.random.default_rng(seed)
+    b1, b2, eps = OPTS[opt]
+    ns = 1 if opt == "sgd" else 2
+    P_pad = orc.padded_numel(P, world)
+    p32 = orc.flatten_pad([rng.uniform(-0.1, 0.1, P).astype(np.float32)], world)
+    p0 = p32 if sfmt == "f32" else orc.cast(p32, sfmt)
+    zero = np.zeros(P_pad, orc.np_storage(sfmt))
+    A = [p0.copy()] + [zero.copy() for _ in range(ns)]
+    B = [p0.copy()] + [zero.copy() for _ in range(ns)]
+    ofmt = sfmt
+    scale = 1024.0 if gfmt == "f16" else 1.0
+    for t in range(1, steps + 1):
+        grads = _grads(orc, rng, world, P, gfmt, scale)
+        hp = orc.hparams(lr, b1, b2, eps, wd, t, scale)
+        orc.step_ex(opt, False, grads, gfmt, world, A[0], A[1], A[2] if ns == 2 else None, sfmt, ofmt, hp)
+        g_avg = orc.all_reduce_avg(grads, gfmt, world, orc.scalars(hp, world).c)
+        hp1 = orc.hparams(lr, b1, b2, eps, wd, t, 1.0)
+        orc.step_ex(opt, False, [g_avg], "f32", 1, B[0], B[1], B[2] if ns == 2 else None, sfmt, ofmt, hp1)
+    for x, y in zip(A, B):
+        np.testing.assert_array_equal(x.view(np.uint8), y.view(np.uint8))
+    assert not A[0][P:].view(np.uint8).any()
