@@ -351,6 +351,21 @@ typedef struct {
 fsdp_status fsdp_step_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
                                int gathers, uint32_t *nonfinite_count, void *stream);
 
+/* How many kernel launches fsdp_step_units (and the step captured from the
+ * same arguments) makes for these units, gathers and fusion, with the small
+ * units batched as that call batches them: per unit or batch one update and
+ * one launch per separate gather, nothing for empty units. The units are
+ * validated as fsdp_step_units validates them (the same statuses); nothing
+ * is enqueued and nothing runs on the device.
+ *   hp             host; validated, not otherwise used.
+ *   launches_out   host; receives the count. */
+fsdp_status fsdp_step_units_launches(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
+                                     int gathers, int fuse_first_gather, int64_t *launches_out);
+
+/* The same for fsdp_step_units_ex. */
+fsdp_status fsdp_step_units_ex_launches(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
+                                        int gathers, int64_t *launches_out);
+
 /* A model step captured as a CUDA graph (opaque; host memory owned by the
  * library, freed by fsdp_step_graph_destroy). */
 typedef struct fsdp_step_graph fsdp_step_graph;

@@ -6,7 +6,8 @@ from .fsdp import (OPTIMIZERS, AdamWHParams, FsdpError, StepConfig, StepGraph, U
                    fsdp_all_gather, fsdp_check_bounded_wait, fsdp_flatten_pad, fsdp_last_cuda_error,
                    fsdp_padded_numel, fsdp_reduce_scatter_adam_cast, fsdp_reduce_scatter_adam_cast_gather,
                    fsdp_reduce_scatter_step, fsdp_status_string, fsdp_step_units, fsdp_step_units_ex,
-                   fsdp_take_wait_timeouts, fsdp_unflatten_views)
+                   fsdp_step_units_ex_launches, fsdp_step_units_launches, fsdp_take_wait_timeouts,
+                   fsdp_unflatten_views)
 from .unit import FlatParamUnit, UnitSequence
 
 __all__ = [
@@ -14,5 +15,6 @@ __all__ = [
     "fsdp_padded_numel", "fsdp_unflatten_views", "fsdp_flatten_pad", "fsdp_reduce_scatter_adam_cast",
     "fsdp_reduce_scatter_adam_cast_gather", "fsdp_reduce_scatter_step", "fsdp_all_gather",
     "fsdp_status_string", "fsdp_last_cuda_error", "fsdp_take_wait_timeouts", "fsdp_check_bounded_wait",
-    "UnitDescs", "fsdp_step_units", "fsdp_step_units_ex", "StepGraph",
+    "UnitDescs", "fsdp_step_units", "fsdp_step_units_ex", "StepGraph", "fsdp_step_units_launches",
+    "fsdp_step_units_ex_launches",
 ]

@@ -39,6 +39,8 @@ EXPORTS = (
     "fsdp_check_bounded_wait",
     "fsdp_step_units",
     "fsdp_step_units_ex",
+    "fsdp_step_units_launches",
+    "fsdp_step_units_ex_launches",
     "fsdp_step_graph_create",
     "fsdp_step_graph_launch",
     "fsdp_step_graph_destroy",
@@ -115,6 +117,10 @@ def load() -> ctypes.CDLL:
                                       vp, vp]),
             "fsdp_step_units_ex": (i32, [ctypes.POINTER(FsdpUnitEx), i32, ctypes.POINTER(FsdpStepConfig), i32,
                                          vp, vp]),
+            "fsdp_step_units_launches": (i32, [ctypes.POINTER(FsdpUnit), i32, ctypes.POINTER(FsdpAdamwHparams), i32,
+                                               i32, ctypes.POINTER(i64)]),
+            "fsdp_step_units_ex_launches": (i32, [ctypes.POINTER(FsdpUnitEx), i32, ctypes.POINTER(FsdpStepConfig),
+                                                  i32, ctypes.POINTER(i64)]),
             "fsdp_step_graph_create": (i32, [ctypes.POINTER(FsdpUnit), i32, i32, i32, vp, ctypes.POINTER(vp)]),
             "fsdp_step_graph_launch": (i32, [vp, ctypes.POINTER(FsdpAdamwHparams), vp]),
             "fsdp_step_graph_destroy": (i32, [vp]),

@@ -729,6 +729,28 @@ void add_span(std::vector<Span> &spans, const void *p, uintptr_t bytes) {
     if (p && bytes) spans.push_back({reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + bytes});
 }
 
+// Refuse overlapping written buffers (two units sharing memory).
+fsdp_status check_spans(std::vector<Span> &spans) {
+    std::sort(spans.begin(), spans.end());
+    for (size_t i = 1; i < spans.size(); ++i)
+        if (spans[i].lo < spans[i - 1].hi) return FSDP_ERR_INVALID_ARG;
+    return FSDP_OK;
+}
+
+// The kernel launches of validated units, batched as run_units batches them.
+fsdp_status count_launches(const std::vector<UnitPlan> &plan, std::vector<Span> &spans, int64_t *launches_out) {
+    if (!launches_out) return FSDP_ERR_INVALID_ARG;
+    if (fsdp_status st = check_spans(spans); st != FSDP_OK) return st;
+    std::vector<Work> work;
+    std::vector<std::unique_ptr<Group>> groups;
+    make_work(plan, work, groups);
+    int64_t n = 0;
+    for (const Work &w : work)
+        n += 1 + (w.group ? w.group->gathers : plan[static_cast<size_t>(w.unit)].separate_gathers);
+    *launches_out = n;
+    return FSDP_OK;
+}
+
 // Enqueue validated units: refuse overlapping written buffers (two units
 // sharing memory), then launch the work items (units, or groups of small
 // units batched into one launch per kernel) in order, spread over the side
@@ -736,9 +758,7 @@ void add_span(std::vector<Span> &spans, const void *p, uintptr_t bytes) {
 // given) receives each work item's update node.
 fsdp_status run_units(const std::vector<UnitPlan> &plan, std::vector<Span> &spans, cudaStream_t s,
                       std::vector<UpdateNode> *nodes = nullptr) {
-    std::sort(spans.begin(), spans.end());
-    for (size_t i = 1; i < spans.size(); ++i)
-        if (spans[i].lo < spans[i - 1].hi) return FSDP_ERR_INVALID_ARG;
+    if (fsdp_status st = check_spans(spans); st != FSDP_OK) return st;
     std::vector<Work> work;
     std::vector<std::unique_ptr<Group>> groups;
     make_work(plan, work, groups);
@@ -957,6 +977,26 @@ FSDP_API fsdp_status fsdp_step_units_ex(const fsdp_unit_ex *units, int n_units, 
     const fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, plan, spans);
     if (st != FSDP_OK) return st;
     return run_units(plan, spans, static_cast<cudaStream_t>(stream));
+}
+
+FSDP_API fsdp_status fsdp_step_units_launches(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
+                                              int gathers, int fuse_first_gather, int64_t *launches_out) {
+    if (!launches_out) return FSDP_ERR_INVALID_ARG;
+    std::vector<UnitPlan> plan;
+    std::vector<Span> spans;
+    const fsdp_status st = plan_units(units, n_units, hp, gathers, fuse_first_gather, nullptr, plan, spans);
+    if (st != FSDP_OK) return st;
+    return count_launches(plan, spans, launches_out);
+}
+
+FSDP_API fsdp_status fsdp_step_units_ex_launches(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
+                                                 int gathers, int64_t *launches_out) {
+    if (!launches_out) return FSDP_ERR_INVALID_ARG;
+    std::vector<UnitPlan> plan;
+    std::vector<Span> spans;
+    const fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nullptr, plan, spans);
+    if (st != FSDP_OK) return st;
+    return count_launches(plan, spans, launches_out);
 }
 
 }  // extern "C"

@@ -21,6 +21,7 @@ __all__ = [
     "fsdp_status_string",
     "fsdp_last_cuda_error", "fsdp_take_wait_timeouts", "fsdp_check_bounded_wait", "dtype_code",
     "UnitDescs", "fsdp_step_units", "fsdp_step_units_ex", "StepGraph",
+    "fsdp_step_units_launches", "fsdp_step_units_ex_launches",
 ]
 
 _DTYPES = {torch.float32: _lib.FSDP_F32, torch.bfloat16: _lib.FSDP_BF16, torch.float16: _lib.FSDP_F16}
@@ -414,6 +415,32 @@ def fsdp_step_units_ex(units, config: StepConfig, gathers: int = 1, nonfinite_co
     cfg = config.to_c()
     _check(_lib.load().fsdp_step_units_ex(descs.array_ex, descs.n, ctypes.byref(cfg), int(gathers), nf,
                                           _stream(stream)), "fsdp_step_units_ex")
+
+
+def fsdp_step_units_launches(units, gathers: int = 1, fuse_first_gather: bool = False,
+                             hparams: Optional[AdamWHParams] = None) -> int:
+    """How many kernel launches fsdp_step_units makes for these units (small
+    units batched); the units are validated, nothing is enqueued."""
+    descs = units if isinstance(units, UnitDescs) else UnitDescs(units)
+    if not descs.adamw:
+        raise ValueError("fsdp_step_units needs fp32 master and AdamW state in every unit; use the _ex query")
+    hp = (hparams if hparams is not None else AdamWHParams(1e-3)).to_c()
+    n = ctypes.c_int64(0)
+    _check(_lib.load().fsdp_step_units_launches(descs.array, descs.n, ctypes.byref(hp), int(gathers),
+                                                1 if fuse_first_gather else 0, ctypes.byref(n)),
+           "fsdp_step_units_launches")
+    return int(n.value)
+
+
+def fsdp_step_units_ex_launches(units, config: StepConfig, gathers: int = 1) -> int:
+    """How many kernel launches fsdp_step_units_ex makes for these units under
+    `config` (small units batched); nothing is enqueued."""
+    descs = units if isinstance(units, UnitDescs) else UnitDescs(units)
+    cfg = config.to_c()
+    n = ctypes.c_int64(0)
+    _check(_lib.load().fsdp_step_units_ex_launches(descs.array_ex, descs.n, ctypes.byref(cfg), int(gathers),
+                                                   ctypes.byref(n)), "fsdp_step_units_ex_launches")
+    return int(n.value)
 
 
 class StepGraph:

@@ -39,7 +39,8 @@ import torch
 
 from .fsdp import (OPTIMIZERS, AdamWHParams, StepConfig, StepGraph, UnitDescs, View, fsdp_all_gather, fsdp_flatten_pad,
                    fsdp_reduce_scatter_adam_cast, fsdp_reduce_scatter_adam_cast_gather, fsdp_reduce_scatter_step,
-                   fsdp_step_units, fsdp_step_units_ex, fsdp_unflatten_views)
+                   fsdp_step_units, fsdp_step_units_ex, fsdp_step_units_ex_launches, fsdp_step_units_launches,
+                   fsdp_unflatten_views)
 
 
 class FlatParamUnit:
@@ -323,6 +324,16 @@ class UnitSequence:
             for u in self.units:
                 u.step_config(config)  # every unit takes this optimizer
         return StepGraph(self.descs, gathers, fuse_gather, nonfinite_count, config)
+
+    def launches(self, gathers: int = 1, fuse_gather: bool = False, config: Optional[StepConfig] = None) -> int:
+        """Kernel launches of one model step as step() (or capture()) makes
+        it, small units batched; nothing runs."""
+        if config is None and all(not u.variant for u in self.units):
+            return fsdp_step_units_launches(self.descs, gathers, fuse_gather)
+        if fuse_gather:
+            raise ValueError("fuse_gather needs the fused AdamW kernel in every unit")
+        cfg = config if config is not None else StepConfig(self.units[0].optimizer, 1e-3)
+        return fsdp_step_units_ex_launches(self.descs, cfg, gathers)
 
     def step_bytes(self, gathers: int = 1) -> Tuple[int, int]:
         """Algorithmic bytes of one model step: (fused kernels, all-gathers)."""

@@ -387,3 +387,68 @@ def test_step_graph_rejects_invalid_arguments_on_the_host(lib):
     hp = E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
     assert lib.fsdp_step_graph_launch(None, ctypes.byref(hp), None) == E.FSDP_ERR_INVALID_ARG
     assert lib.fsdp_step_graph_destroy(None) == E.FSDP_OK
+
+
+def _fake_units(E, specs, ex=False):
+    """fsdp_unit (or fsdp_unit_ex) descriptors over never-dereferenced
+    addresses, one 4 GB region per unit so that no written buffers overlap;
+    specs are (padded_numel, world, n_full, misaligned)."""
+    keep, units = [], []
+    for u, (P, world, n_full, misaligned) in enumerate(specs):
+        base = FAKE + (u << 32) + (4 if misaligned else 0)
+        grads = (ctypes.c_void_p * world)(*[base + 0x80000000 + (q << 26) for q in range(world)])
+        full = (ctypes.c_void_p * n_full)(*[base + 0x40000000 + (d << 26) for d in range(n_full)])
+        keep += [grads, full]
+        x = E.FsdpUnitEx() if ex else E.FsdpUnit()
+        x.grads, x.full_bufs = ctypes.addressof(grads), ctypes.addressof(full)
+        if ex:
+            x.param, x.state0, x.state1 = base, base + 0x10000000, base + 0x20000000
+            x.state_dtype = 0
+        else:
+            x.master, x.exp_avg, x.exp_avg_sq = base, base + 0x10000000, base + 0x20000000
+        x.shard_out = base + 0x30000000
+        x.padded_numel, x.world, x.n_full = P, world, n_full
+        x.grad_dtype, x.out_dtype = 1, 1
+        units.append(x)
+    arr = ((E.FsdpUnitEx if ex else E.FsdpUnit) * max(len(units), 1))(*units)
+    return arr, keep
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host-only: fake addresses need a machine without a GPU")
+def test_step_units_launches_follow_the_batching(lib):
+    # the planning query: nothing is enqueued; small units batch 128 per
+    # launch, larger or misaligned units or N = 3 keep their own launches
+    from sharded_fsdp_reduce_gb300 import _lib as E
+    import bench
+    hp = E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+    out = ctypes.c_int64(-1)
+
+    def count(specs, gathers=1, fuse=0):
+        arr, keep = _fake_units(E, specs)
+        st = lib.fsdp_step_units_launches(arr, len(specs), ctypes.byref(hp), gathers, fuse, ctypes.byref(out))
+        assert st == E.FSDP_OK, st
+        return out.value
+
+    small = (50000, 8, 8, False)
+    for n, gathers in ((200, 1), (200, 2), (200, 0), (128, 1), (129, 1), (1, 1), (2, 1)):
+        assert count([small] * n, gathers) == bench.model_launches(n, 50000, gathers), (n, gathers)
+    assert count([(7087872, 8, 8, False)] * 12) == bench.model_launches(12, 7087872, 1) == 2
+    big = ((1 << 24) + 8, 8, 8, False)
+    assert count([big] * 3) == 6                                     # above the size limit: own launches
+    assert count([small] * 5 + [(50000, 8, 8, True)]) == 2 + 2       # a misaligned unit keeps its own
+    assert count([small] * 5 + [(50000 - 2, 2, 1, False)] * 3) == 2 + 2   # another N: a second batch
+    assert count([(3 * 1000, 3, 3, False)] * 4) == 8                 # N = 3 is not batched
+    assert count([small] * 5, gathers=2, fuse=1) == 5 * 2            # fused gather: own launches
+    assert count([small] * 3 + [(0, 8, 8, False)]) == 2              # an empty unit launches nothing
+    assert lib.fsdp_step_units_launches(None, 0, ctypes.byref(hp), 1, 0, None) == E.FSDP_ERR_INVALID_ARG
+    arr, keep = _fake_units(E, [small, small])
+    arr[1].master = arr[0].master                                     # two units writing one buffer
+    assert lib.fsdp_step_units_launches(arr, 2, ctypes.byref(hp), 1, 0, ctypes.byref(out)) == E.FSDP_ERR_INVALID_ARG
+    # the variant call
+    cfg = E.FsdpStepConfig(1, 0, 1e-2, 0.9, 0.0, 0.0, 0.0, 1, 1.0)  # SGD: one state
+    arr, keep = _fake_units(E, [small] * 150, ex=True)
+    for k in range(150):
+        arr[k].state1 = None
+    assert lib.fsdp_step_units_ex_launches(arr, 150, ctypes.byref(cfg), 1, ctypes.byref(out)) == E.FSDP_OK
+    assert out.value == 4
+    assert lib.fsdp_last_cuda_error() == 0

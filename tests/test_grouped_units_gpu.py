@@ -115,6 +115,20 @@ def test_units_with_different_gather_fanouts_batch_together(F):
         assert_units_equal(a, b, 2)
 
 
+def test_launch_counts_of_batched_models(F):
+    # the planning query on real buffers: 200 small units batch into 2
+    # launches per kernel, N = 3 units keep their own, the variant call too
+    a, _ = make_units(F, [(50000, 8, torch.bfloat16, torch.bfloat16)] * 200, 3)
+    seq = F.UnitSequence(a)
+    assert seq.launches(gathers=1) == 4 and seq.launches(gathers=2) == 6 and seq.launches(gathers=0) == 2
+    assert seq.launches(gathers=1, fuse_gather=True) == 200
+    c, _ = make_units(F, [(3000, 3, torch.bfloat16, torch.bfloat16)] * 4, 4)
+    assert F.UnitSequence(a[:10] + c).launches(gathers=1) == 2 + 8
+    v, _ = make_variant_units(F, [(20000, 4, torch.bfloat16, torch.bfloat16)] * 130, 5, "sgd", torch.float32)
+    assert F.UnitSequence(v).launches(gathers=1) == 4
+    assert F.UnitSequence(v).launches(gathers=1, config=vcfg(F, "sgd", 1)) == 4
+
+
 def test_a_full_group_and_a_group_of_one(F):
     # 129 units of one kind: a full group of 128 and one unit left over,
     # which is launched on its own; both bit-equal to each unit's own step
