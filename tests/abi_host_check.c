@@ -93,6 +93,12 @@ int main(void) {
     CHECK(fsdp_step_units_ex(&v, 1, &cfg, 1, NULL, NULL) == FSDP_ERR_INVALID_ARG);
     CHECK(fsdp_step_units_ex(NULL, 0, &cfg, 1, NULL, NULL) == FSDP_OK);
     CHECK(fsdp_step_units_ex(&v, 1, NULL, 1, NULL, NULL) == FSDP_ERR_INVALID_ARG);
+    /* the launch-count query: an empty model makes none; no output, or an
+     * invalid unit, is refused */
+    int64_t launches = -1;
+    CHECK(fsdp_step_units_launches(NULL, 0, &hp, 1, 0, &launches) == FSDP_OK && launches == 0);
+    CHECK(fsdp_step_units_launches(NULL, 0, &hp, 1, 0, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_step_units_ex_launches(&v, 1, &cfg, 1, &launches) == FSDP_ERR_INVALID_ARG);
     /* the captured step: no handle to fill, no graph to launch */
     fsdp_step_graph *graph = (fsdp_step_graph *)&u; /* overwritten with NULL on error */
     CHECK(fsdp_step_graph_create(NULL, 1, 1, 0, NULL, &graph) == FSDP_ERR_INVALID_ARG && graph == NULL);
