@@ -452,3 +452,46 @@ def test_step_units_launches_follow_the_batching(lib):
     assert lib.fsdp_step_units_ex_launches(arr, 150, ctypes.byref(cfg), 1, ctypes.byref(out)) == E.FSDP_OK
     assert out.value == 4
     assert lib.fsdp_last_cuda_error() == 0
+
+
+def _expected_launches(specs, gathers):
+    """The batching rule restated: units of N in {2, 4, 8}, at most 2^24
+    elements, 16-byte aligned and not empty batch with the earlier ones of
+    the same N (every fake unit here shares the dtypes and gathers), 128 per
+    batch; a batch of one is a unit on its own; one update and `gathers`
+    gathers per work item."""
+    items, open_ = 0, {}
+    for P, world, n_full, misaligned in specs:
+        if P == 0:
+            continue
+        if world not in (2, 4, 8) or P > (1 << 24) or misaligned or n_full > 8:
+            items += 1
+            continue
+        if open_.get(world, 128) == 128:
+            items += 1
+            open_[world] = 0
+        open_[world] += 1
+    return items * (1 + gathers)
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host-only: fake addresses need a machine without a GPU")
+@pytest.mark.parametrize("seed", range(20))
+def test_step_units_launches_random_models(lib, seed):
+    # random models of 1-400 units mixing batchable and non-batchable units:
+    # the library's count equals the rule restated above
+    import numpy as np
+    from sharded_fsdp_reduce_gb300 import _lib as E
+    rng = np.random.default_rng(seed)
+    specs = []
+    for _ in range(int(rng.integers(1, 401))):
+        world = int(rng.choice([2, 3, 4, 8]))
+        r = rng.random()
+        P = 0 if r < 0.03 else (int(rng.integers(1 << 24, (1 << 24) + 64)) // world * world if r < 0.06
+                                else int(rng.integers(1, 5000)) * world)
+        specs.append((P, world, int(rng.integers(1, world + 1)), bool(rng.random() < 0.05)))
+    gathers = int(rng.integers(0, 3))
+    arr, keep = _fake_units(E, specs)
+    hp = E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+    out = ctypes.c_int64(-1)
+    assert lib.fsdp_step_units_launches(arr, len(specs), ctypes.byref(hp), gathers, 0, ctypes.byref(out)) == E.FSDP_OK
+    assert out.value == _expected_launches(specs, gathers)
