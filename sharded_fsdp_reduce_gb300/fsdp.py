@@ -417,10 +417,11 @@ def fsdp_step_units_ex(units, config: StepConfig, gathers: int = 1, nonfinite_co
                                           _stream(stream)), "fsdp_step_units_ex")
 
 
-def fsdp_step_units_launches(units, gathers: int = 1, fuse_first_gather: bool = False,
-                             hparams: Optional[AdamWHParams] = None) -> int:
+def fsdp_step_units_launches(units, hparams: Optional[AdamWHParams] = None, gathers: int = 1,
+                             fuse_first_gather: bool = False) -> int:
     """How many kernel launches fsdp_step_units makes for these units (small
-    units batched); the units are validated, nothing is enqueued."""
+    units batched); the units are validated, nothing is enqueued. Arguments
+    as fsdp_step_units (hparams only validated; default lr 1e-3)."""
     descs = units if isinstance(units, UnitDescs) else UnitDescs(units)
     if not descs.adamw:
         raise ValueError("fsdp_step_units needs fp32 master and AdamW state in every unit; use the _ex query")

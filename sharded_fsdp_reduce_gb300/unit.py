@@ -329,7 +329,7 @@ class UnitSequence:
         """Kernel launches of one model step as step() (or capture()) makes
         it, small units batched; nothing runs."""
         if config is None and all(not u.variant for u in self.units):
-            return fsdp_step_units_launches(self.descs, gathers, fuse_gather)
+            return fsdp_step_units_launches(self.descs, gathers=gathers, fuse_first_gather=fuse_gather)
         if fuse_gather:
             raise ValueError("fuse_gather needs the fused AdamW kernel in every unit")
         cfg = config if config is not None else StepConfig(self.units[0].optimizer, 1e-3)
