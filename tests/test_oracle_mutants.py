@@ -64,6 +64,7 @@ MUTANTS = [
      "for (int64_t q = 1; q < N; ++q) acc = acc + grad_at(G[q], grad_dtype, j);"),
     ("lowp_state_truncates", "((uint16_t *)base)[j] = orc_f32_to_bf16(x);",
      "((uint16_t *)base)[j] = (uint16_t)(f32_bits(x) >> 16);"),
+    ("shadow_no_unscale", "G_avg[j] = acc / ((double)N * grad_scale);", "G_avg[j] = acc / (double)N;"),
 ]
 
 

@@ -467,3 +467,35 @@ def test_tiny_trajectory_within_fp64_shadow(orc):
         assert np.all(np.abs(p32 - p64) <= t * 4 * u * (np.abs(p64) + cfg.lr))
         assert np.all(np.abs(v32 - v64) <= (t * 6 * u + 2e-6) * v64 + 1e-45)
 
+
+
+def test_loss_scaled_fp16_trajectory_within_fp64_shadow(orc):
+    # GPT-2 Large's form ("static loss scale 1024 to unscale in-kernel", N = 2,
+    # fp16 gradients that carry the scale, reading R10): the fp32 step
+    # multiplies by c = fp32(1/(N*1024)), the fp64 shadow divides by N*1024 in
+    # double. Adam's update is almost blind to a gradient's scale, so the
+    # moments and the averaged gradient are checked too: a shadow that kept
+    # the scale would have m 1024x and v 1024^2 x the fp32 ones.
+    import fsdp_inputs as fi
+    cfg = fi.CONFIGS["gpt2_large"]
+    assert cfg.grad_dtype == "f16" and cfg.grad_scale == 1024.0 and cfg.world == 2
+    N, n = cfg.world, 1 << 16
+    P_pad = orc.padded_numel(n, N)
+    master = orc.flatten_pad([fi.gen_master(cfg, numel=n).numpy()], N)
+    p32, m32, v32 = master.copy(), np.zeros(P_pad, np.float32), np.zeros(P_pad, np.float32)
+    p64, m64, v64 = master.astype(np.float64), np.zeros(P_pad), np.zeros(P_pad)
+    mag = np.zeros(P_pad)  # the same recursion as m on |g|: the size of its terms, for a cancellation-safe bound
+    u = 2.0 ** -24
+    for t in range(1, 5):
+        gr = [orc.flatten_pad([fi.gen_grad(cfg, r, t, numel=n).view(torch.int16).numpy().view(np.uint16)], N)
+              for r in range(N)]
+        hp = orc.hparams(cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay, t, cfg.grad_scale)
+        orc.fsdp_step(gr, cfg.grad_dtype, N, p32, m32, v32, cfg.out_dtype, hp)
+        g64 = orc.all_reduce_avg_f64(gr, cfg.grad_dtype, N, cfg.grad_scale)
+        # the average of N unscaled N(0, 1e-3) draws: standard deviation 1e-3 / sqrt(N)
+        assert 0.9e-3 / np.sqrt(N) < np.std(g64) < 1.1e-3 / np.sqrt(N)
+        orc.adamw_f64(p64, m64, v64, g64, hp)
+        mag = cfg.beta1 * mag + (1 - cfg.beta1) * np.abs(g64)
+        assert np.all(np.abs(p32 - p64) <= t * 4 * u * (np.abs(p64) + cfg.lr))
+        assert np.all(np.abs(m32 - m64) <= t * 4 * u * mag)
+        assert np.all(np.abs(v32 - v64) <= (t * 6 * u + 2e-6) * v64 + 1e-45)

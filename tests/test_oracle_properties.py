@@ -15,8 +15,23 @@ invariants the pages fix must hold exactly.
 import numpy as np
 import pytest
 
-hyp = pytest.importorskip("hypothesis")
-from hypothesis import given, settings, strategies as st  # noqa: E402
+try:
+    from hypothesis import given, settings, strategies as st
+except ImportError:
+    # A machine without hypothesis skips each property test on its own (a
+    # skip at import would show up as a skipped module in every run, the
+    # GPU-only selection included, where these CPU tests are deselected).
+    class _AnyStrategy:
+        def __getattr__(self, name):
+            return lambda *args, **kwargs: None
+
+    st = _AnyStrategy()
+
+    def given(**kwargs):
+        return pytest.mark.skip(reason="hypothesis is not installed")
+
+    def settings(**kwargs):
+        return lambda f: f
 
 FMT = ["bf16", "f16", "f32"]
 SETTINGS = dict(max_examples=60, deadline=None, derandomize=True)
