@@ -30,8 +30,23 @@
  *    pointer arrays themselves (grads, srcs, full_bufs) are HOST arrays of
  *    device addresses. The caller owns every buffer; the library allocates
  *    no device memory and keeps no state besides launch caches (the SM
- *    count and kernel occupancies per device) and the side streams of
- *    fsdp_step_units.
+ *    count and kernel occupancies per device), the side streams of
+ *    fsdp_step_units, one device counter of bounded waits that gave up
+ *    (fsdp_take_wait_timeouts), and the host memory of the handles it
+ *    returns (fsdp_step_graph, fsdp_step_plan).
+ *  - Bounded waits. The all-gather's bulk-copy (TMA) pipeline waits on
+ *    shared-memory barriers for its loads; each wait gives up after about
+ *    one second of SM clocks. A wait that gives up makes its CTA return
+ *    early (after one more bounded wait on each load it still has in flight,
+ *    so that a copy that is only slow lands first): the gathered buffers of
+ *    that call are then incomplete. Every entry point that launches a gather
+ *    takes `wait_timeouts`, a device uint32 (or NULL) that each wait giving
+ *    up increments; the caller zeroes it and reads it after the call's work,
+ *    stream-ordered like nonfinite_count, with no device-wide
+ *    synchronization. A non-zero count means that call's gathered buffers,
+ *    and anything launched after it on the device, must not be trusted: a
+ *    bulk copy that does not complete within a second is a fault of the
+ *    device, not a slow copy. The count is 0 in normal operation.
  *  - Offload. Where an argument says "device or mapped host", the buffer
  *    may also be page-locked host memory mapped into the device's address
  *    space (cudaHostAlloc, or cudaHostRegister with mapping; the same
@@ -281,9 +296,12 @@ fsdp_status fsdp_reduce_scatter_step(const void *const *grads, fsdp_dtype grad_d
  *                overlap shard_out or each other. Host memory is refused
  *                (FSDP_ERR_INVALID_ARG) for shard_out and full_bufs alike:
  *                the copy uses bulk transfers between device buffers.
- *   world        N; padded_numel must be a multiple of it. */
+ *   world        N; padded_numel must be a multiple of it.
+ *   wait_timeouts  device uint32 or NULL: incremented by each bounded wait
+ *                of this call that gave up (see "Bounded waits" above). */
 fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
-                            int64_t padded_numel, void *const *full_bufs, int n_dst, void *stream);
+                            int64_t padded_numel, void *const *full_bufs, int n_dst,
+                            uint32_t *wait_timeouts, void *stream);
 
 /* The step of a whole model (device): its FSDP units in order, each one's
  * fused reduce-scatter + AdamW + cast over all its ranks followed by
@@ -299,10 +317,12 @@ fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
  *                optimizer over the model); step >= 1, grad_scale > 0.
  *   gathers      0..FSDP_MAX_WORLD; units with gathers > 0 need n_full >= 1.
  *   nonfinite_count  device uint32 or NULL, summed over all units.
+ *   wait_timeouts    device uint32 or NULL, the bounded waits of all the
+ *                units' gathers that gave up (see "Bounded waits" above).
  * Every unit is validated as the single-unit entry points validate it, and
- * no buffer written by one unit may overlap a buffer written by another,
- * before anything is enqueued: an invalid unit makes the call return its
- * status and enqueue nothing. FSDP_ERR_CUDA reports a launch that failed
+ * no buffer written by one unit may overlap a buffer written or a gradient
+ * read by another, before anything is enqueued: an invalid unit makes the
+ * call return its status and enqueue nothing. FSDP_ERR_CUDA reports a launch that failed
  * after the units before it were enqueued.
  * Scheduling: the units share no written buffer, so with two or more of
  * them their kernels are spread round-robin over two streams the library
@@ -318,7 +338,7 @@ fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
  * the same bits. Every other unit keeps its own launches. */
 fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
                             int gathers, int fuse_first_gather, uint32_t *nonfinite_count,
-                            void *stream);
+                            uint32_t *wait_timeouts, void *stream);
 
 /* The buffers of one FSDP unit for fsdp_step_units_ex (the variant steps),
  * laid out as fsdp_reduce_scatter_step takes them. Caller-owned. */
@@ -344,12 +364,14 @@ typedef struct {
  * all-gathers of its compute-dtype shards -- shard_out for fp32 state, the
  * parameter itself for bf16/fp16 state -- into its n_full buffers. No gather
  * is fused. Validation (every unit as fsdp_reduce_scatter_step validates it,
- * no buffer written by two units, nothing enqueued on error), scheduling
+ * no buffer written by two units or written by one and read by another,
+ * nothing enqueued on error), scheduling
  * over the side streams, batching of small units (those that also share
  * the state dtype; the optimizer and reduction are the call's) and errors as
  * fsdp_step_units. */
 fsdp_status fsdp_step_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
-                               int gathers, uint32_t *nonfinite_count, void *stream);
+                               int gathers, uint32_t *nonfinite_count, uint32_t *wait_timeouts,
+                               void *stream);
 
 /* How many kernel launches fsdp_step_units (and the step captured from the
  * same arguments) makes for these units, gathers and fusion, with the small
@@ -371,7 +393,7 @@ fsdp_status fsdp_step_units_ex_launches(const fsdp_unit_ex *units, int n_units, 
 typedef struct fsdp_step_graph fsdp_step_graph;
 
 /* Capture the step fsdp_step_units would enqueue for these units, gathers,
- * fusion and counter into a CUDA graph, instantiated on the current device.
+ * fusion and counters into a CUDA graph, instantiated on the current device.
  * The units are validated as fsdp_step_units validates them; nothing runs.
  * The graph holds the buffers' addresses: they must stay allocated, and a
  * step launched from it touches exactly those buffers. Each launch writes
@@ -379,7 +401,8 @@ typedef struct fsdp_step_graph fsdp_step_graph;
  * the whole model, batched launches included.
  *   graph_out    host; receives the handle (NULL on error). */
 fsdp_status fsdp_step_graph_create(const fsdp_unit *units, int n_units, int gathers, int fuse_first_gather,
-                                   uint32_t *nonfinite_count, fsdp_step_graph **graph_out);
+                                   uint32_t *nonfinite_count, uint32_t *wait_timeouts,
+                                   fsdp_step_graph **graph_out);
 
 /* Launch the captured step on `stream` with the scalars of hp (computed as
  * fsdp_reduce_scatter_adam_cast computes them, per unit for its world size).
@@ -392,7 +415,8 @@ fsdp_status fsdp_step_graph_launch(fsdp_step_graph *graph, const fsdp_adamw_hpar
  * cfg's optimizer, whose kernels the graph holds; cfg is validated as
  * fsdp_step_units_ex validates it. */
 fsdp_status fsdp_step_graph_create_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
-                                      int gathers, uint32_t *nonfinite_count, fsdp_step_graph **graph_out);
+                                      int gathers, uint32_t *nonfinite_count, uint32_t *wait_timeouts,
+                                      fsdp_step_graph **graph_out);
 
 /* Launch a captured variant step with cfg's scalars and reduction dtype.
  * cfg->optimizer must be the one the graph was captured with, and
@@ -404,18 +428,59 @@ fsdp_status fsdp_step_graph_launch_ex(fsdp_step_graph *graph, const fsdp_step_co
 /* Free a captured step (NULL is a no-op). Launches already enqueued complete. */
 fsdp_status fsdp_step_graph_destroy(fsdp_step_graph *graph);
 
+/* A model step validated once (opaque; host memory owned by the library,
+ * freed by fsdp_step_plan_destroy). */
+typedef struct fsdp_step_plan fsdp_step_plan;
+
+/* Validate the units of fsdp_step_units once, for repeated steps: every
+ * check fsdp_step_units makes on every call (arguments, alignment,
+ * residency of the state and of the gathered buffers, overlaps between
+ * units) runs here, together with the batching of small units; nothing is
+ * enqueued. The plan holds the buffers' addresses, as a captured step does:
+ * they must stay allocated, and a step launched from it touches exactly
+ * those buffers. The eager counterpart of fsdp_step_graph_create, for
+ * callers that do not capture graphs: the per-layer step of "FSDP (Fully
+ * Sharded Data Parallel)", "The Per-Layer Communication", with one unit per
+ * wrapped layer and the validation paid once per model, not once per step.
+ *   plan_out     host; receives the handle (NULL on error).
+ * Other arguments and statuses as fsdp_step_units. */
+fsdp_status fsdp_step_plan_create(const fsdp_unit *units, int n_units, int gathers, int fuse_first_gather,
+                                  uint32_t *nonfinite_count, uint32_t *wait_timeouts,
+                                  fsdp_step_plan **plan_out);
+
+/* The same for the units of fsdp_step_units_ex, validated with cfg (its
+ * optimizer is the plan's; its scalars are not kept). */
+fsdp_status fsdp_step_plan_create_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
+                                     int gathers, uint32_t *nonfinite_count, uint32_t *wait_timeouts,
+                                     fsdp_step_plan **plan_out);
+
+/* Enqueue one step of a plan from fsdp_step_plan_create on `stream` with
+ * the scalars of hp (step >= 1, grad_scale > 0, else FSDP_ERR_INVALID_ARG
+ * and nothing enqueued): the launches fsdp_step_units would make with the
+ * same arguments, bit-identical results, scheduling and errors as that
+ * call. Only hp is checked per call. Not thread-safe for one plan (each
+ * launch rewrites the plan's kernel arguments). */
+fsdp_status fsdp_step_plan_launch(fsdp_step_plan *plan, const fsdp_adamw_hparams *hp, void *stream);
+
+/* The same for a plan from fsdp_step_plan_create_ex: cfg->optimizer must be
+ * the plan's and reduce_dtype FSDP_F32 or every unit's gradient dtype;
+ * otherwise nothing is enqueued. */
+fsdp_status fsdp_step_plan_launch_ex(fsdp_step_plan *plan, const fsdp_step_config *cfg, void *stream);
+
+/* Free a plan (NULL is a no-op). Launches already enqueued complete. */
+fsdp_status fsdp_step_plan_destroy(fsdp_step_plan *plan);
+
 /* Human-readable name of a status. Never NULL. */
 const char *fsdp_status_string(fsdp_status status);
 
 /* cudaError_t value behind the calling thread's last FSDP_ERR_CUDA (0 if none). */
 int fsdp_last_cuda_error(void);
 
-/* Diagnostics of the bulk-copy (TMA) pipelines. Their waits on shared-memory
- * barriers are bounded (about one second); a wait that gives up makes its
- * kernel return early, leaving that call's output incomplete, and is counted
- * on the current device. This call synchronizes the current device, writes
- * the count accumulated since the previous call to *count_out (host) and
- * resets it. The count is 0 in normal operation. */
+/* Device-wide diagnostics of the bounded waits (see "Bounded waits" above):
+ * every wait that gives up, in any call, is also counted on the current
+ * device. This call synchronizes the current device, writes the count
+ * accumulated since the previous call to *count_out (host) and resets it.
+ * A caller that checks each call reads that call's wait_timeouts instead. */
 fsdp_status fsdp_take_wait_timeouts(uint32_t *count_out);
 
 /* Self-test of the failure path of those bounded waits, without a fault:
@@ -423,10 +488,11 @@ fsdp_status fsdp_take_wait_timeouts(uint32_t *count_out);
  * stream) that waits, with the library's bounded wait, on a shared-memory
  * barrier that expects two arrivals and receives one. The wait gives up
  * after about `limit_cycles` SM clock cycles and is counted as a gather's
- * would be (read it with fsdp_take_wait_timeouts); the kernel then returns
- * and the context stays usable. Asynchronous. limit_cycles must be in
- * [1, 2^31] (FSDP_ERR_INVALID_ARG otherwise, nothing launched). */
-fsdp_status fsdp_check_bounded_wait(int64_t limit_cycles, void *stream);
+ * would be: on the device (fsdp_take_wait_timeouts) and in wait_timeouts
+ * (device uint32 or NULL); the kernel then returns and the context stays
+ * usable. Asynchronous. limit_cycles must be in [1, 2^31]
+ * (FSDP_ERR_INVALID_ARG otherwise, nothing launched). */
+fsdp_status fsdp_check_bounded_wait(int64_t limit_cycles, uint32_t *wait_timeouts, void *stream);
 
 #ifdef __cplusplus
 }

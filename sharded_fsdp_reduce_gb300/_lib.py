@@ -46,6 +46,11 @@ EXPORTS = (
     "fsdp_step_graph_destroy",
     "fsdp_step_graph_create_ex",
     "fsdp_step_graph_launch_ex",
+    "fsdp_step_plan_create",
+    "fsdp_step_plan_create_ex",
+    "fsdp_step_plan_launch",
+    "fsdp_step_plan_launch_ex",
+    "fsdp_step_plan_destroy",
 )
 
 
@@ -108,25 +113,31 @@ def load() -> ctypes.CDLL:
                                                            ctypes.POINTER(FsdpAdamwHparams), i32, i32, vp, vp]),
             "fsdp_reduce_scatter_step": (i32, [vp, i32, i32, i64, vp, vp, vp, i32, vp, i32,
                                                ctypes.POINTER(FsdpStepConfig), i32, i32, vp, vp]),
-            "fsdp_all_gather": (i32, [vp, i32, i32, i64, vp, i32, vp]),
+            "fsdp_all_gather": (i32, [vp, i32, i32, i64, vp, i32, vp, vp]),
             "fsdp_status_string": (ctypes.c_char_p, [i32]),
             "fsdp_last_cuda_error": (i32, []),
             "fsdp_take_wait_timeouts": (i32, [ctypes.POINTER(ctypes.c_uint32)]),
-            "fsdp_check_bounded_wait": (i32, [i64, vp]),
+            "fsdp_check_bounded_wait": (i32, [i64, vp, vp]),
             "fsdp_step_units": (i32, [ctypes.POINTER(FsdpUnit), i32, ctypes.POINTER(FsdpAdamwHparams), i32, i32,
-                                      vp, vp]),
+                                      vp, vp, vp]),
             "fsdp_step_units_ex": (i32, [ctypes.POINTER(FsdpUnitEx), i32, ctypes.POINTER(FsdpStepConfig), i32,
-                                         vp, vp]),
+                                         vp, vp, vp]),
             "fsdp_step_units_launches": (i32, [ctypes.POINTER(FsdpUnit), i32, ctypes.POINTER(FsdpAdamwHparams), i32,
                                                i32, ctypes.POINTER(i64)]),
             "fsdp_step_units_ex_launches": (i32, [ctypes.POINTER(FsdpUnitEx), i32, ctypes.POINTER(FsdpStepConfig),
                                                   i32, ctypes.POINTER(i64)]),
-            "fsdp_step_graph_create": (i32, [ctypes.POINTER(FsdpUnit), i32, i32, i32, vp, ctypes.POINTER(vp)]),
+            "fsdp_step_graph_create": (i32, [ctypes.POINTER(FsdpUnit), i32, i32, i32, vp, vp, ctypes.POINTER(vp)]),
             "fsdp_step_graph_launch": (i32, [vp, ctypes.POINTER(FsdpAdamwHparams), vp]),
             "fsdp_step_graph_destroy": (i32, [vp]),
             "fsdp_step_graph_create_ex": (i32, [ctypes.POINTER(FsdpUnitEx), i32, ctypes.POINTER(FsdpStepConfig), i32,
-                                                vp, ctypes.POINTER(vp)]),
+                                                vp, vp, ctypes.POINTER(vp)]),
             "fsdp_step_graph_launch_ex": (i32, [vp, ctypes.POINTER(FsdpStepConfig), vp]),
+            "fsdp_step_plan_create": (i32, [ctypes.POINTER(FsdpUnit), i32, i32, i32, vp, vp, ctypes.POINTER(vp)]),
+            "fsdp_step_plan_create_ex": (i32, [ctypes.POINTER(FsdpUnitEx), i32, ctypes.POINTER(FsdpStepConfig), i32,
+                                               vp, vp, ctypes.POINTER(vp)]),
+            "fsdp_step_plan_launch": (i32, [vp, ctypes.POINTER(FsdpAdamwHparams), vp]),
+            "fsdp_step_plan_launch_ex": (i32, [vp, ctypes.POINTER(FsdpStepConfig), vp]),
+            "fsdp_step_plan_destroy": (i32, [vp]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)

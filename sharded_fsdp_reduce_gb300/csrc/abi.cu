@@ -283,12 +283,14 @@ fsdp_status rsa_entry(const void *const *grads, fsdp_dtype grad_dtype, int world
 }
 
 // Validation of an all-gather: fills its arguments or sets `empty`.
+// `timeouts` (device, may be NULL) counts the call's bounded waits that gave up.
 fsdp_status prepare_gather(const void *shard_out, fsdp_dtype dtype, int world, int64_t padded_numel,
-                           void *const *full_bufs, int n_dst, GatherArgs &a, bool &empty) {
+                           void *const *full_bufs, int n_dst, uint32_t *timeouts, GatherArgs &a, bool &empty) {
     empty = false;
     if (!dtype_valid(dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
     if (world < 1 || padded_numel < 0 || padded_numel % world != 0) return FSDP_ERR_INVALID_ARG;
     if (n_dst < 1 || n_dst > FSDP_MAX_WORLD || !full_bufs) return FSDP_ERR_INVALID_ARG;
+    if (timeouts && !aligned(timeouts, 4)) return FSDP_ERR_ALIGNMENT;
     const size_t es = static_cast<size_t>(dtype_size(dtype));
     if (mul_overflows(padded_numel, static_cast<int64_t>(es))) return FSDP_ERR_INVALID_ARG;
     if (padded_numel == 0) {
@@ -302,6 +304,7 @@ fsdp_status prepare_gather(const void *shard_out, fsdp_dtype dtype, int world, i
     a.src = shard_out;
     a.nbytes = static_cast<int64_t>(nbytes);
     a.n_dst = n_dst;
+    a.timeouts = timeouts;
     for (int d = 0; d < n_dst; ++d) {
         if (!full_bufs[d]) return FSDP_ERR_INVALID_ARG;
         if (!aligned(full_bufs[d], es)) return FSDP_ERR_ALIGNMENT;
@@ -598,6 +601,7 @@ Group *new_group(std::vector<std::unique_ptr<Group>> &groups, const UnitPlan &p,
         g->rsa.nonfinite = p.rsa.nonfinite;
     }
     g->gathers = p.separate_gathers;
+    g->gather.timeouts = p.gather.timeouts;  // the call's counter: the same for every unit
     g->first_unit = u;
     g->grad_dtype = p.grad_dtype;
     g->out_dtype = p.out_dtype;
@@ -729,45 +733,64 @@ void add_span(std::vector<Span> &spans, const void *p, uintptr_t bytes) {
     if (p && bytes) spans.push_back({reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + bytes});
 }
 
-// Refuse overlapping written buffers (two units sharing memory).
-fsdp_status check_spans(std::vector<Span> &spans) {
-    std::sort(spans.begin(), spans.end());
-    for (size_t i = 1; i < spans.size(); ++i)
-        if (spans[i].lo < spans[i - 1].hi) return FSDP_ERR_INVALID_ARG;
-    return FSDP_OK;
-}
-
-// The kernel launches of validated units, batched as run_units batches them.
-fsdp_status count_launches(const std::vector<UnitPlan> &plan, std::vector<Span> &spans, int64_t *launches_out) {
-    if (!launches_out) return FSDP_ERR_INVALID_ARG;
-    if (fsdp_status st = check_spans(spans); st != FSDP_OK) return st;
+// A model step's units after validation: one plan per unit, the byte ranges
+// the units write and read, and the work items (a unit's own kernels, or a
+// group of small units batched into one launch per kernel) in launch order.
+struct ModelPlan {
+    std::vector<UnitPlan> units;
+    std::vector<Span> writes;  // parameter / master, optimizer states, shard_out, gathered buffers
+    std::vector<Span> reads;   // gradients
     std::vector<Work> work;
     std::vector<std::unique_ptr<Group>> groups;
-    make_work(plan, work, groups);
-    int64_t n = 0;
-    for (const Work &w : work)
-        n += 1 + (w.group ? w.group->gathers : plan[static_cast<size_t>(w.unit)].separate_gathers);
-    *launches_out = n;
+};
+
+// Refuse a model whose units share memory that one of them writes: two
+// written ranges that overlap, or a gradient range that overlaps a written
+// range. Different units run at the same time (side streams, batched
+// launches), so either would race. Gradients shared by several units (read
+// only) are fine; a unit's gradients against its own written buffers are
+// also refused by that unit's own validation.
+fsdp_status check_spans(ModelPlan &m) {
+    std::vector<Span> &w = m.writes;
+    std::sort(w.begin(), w.end());
+    for (size_t i = 1; i < w.size(); ++i)
+        if (w[i].lo < w[i - 1].hi) return FSDP_ERR_INVALID_ARG;
+    // the written ranges are now disjoint and sorted by start, hence by end
+    // too: the first one that ends after a read range starts is the only
+    // one that can overlap it
+    for (const Span &r : m.reads) {
+        auto it = std::upper_bound(w.begin(), w.end(), r.lo, [](uintptr_t x, const Span &y) { return x < y.hi; });
+        if (it != w.end() && it->lo < r.hi) return FSDP_ERR_INVALID_ARG;
+    }
     return FSDP_OK;
 }
 
-// Enqueue validated units: refuse overlapping written buffers (two units
-// sharing memory), then launch the work items (units, or groups of small
-// units batched into one launch per kernel) in order, spread over the side
+// The last step of validating a model: the overlap checks, then the work items.
+fsdp_status finish_plan(ModelPlan &m) {
+    if (fsdp_status st = check_spans(m); st != FSDP_OK) return st;
+    make_work(m.units, m.work, m.groups);
+    return FSDP_OK;
+}
+
+// The kernel launches of a validated model.
+int64_t count_launches(const ModelPlan &m) {
+    int64_t n = 0;
+    for (const Work &w : m.work)
+        n += 1 + (w.group ? w.group->gathers : m.units[static_cast<size_t>(w.unit)].separate_gathers);
+    return n;
+}
+
+// Enqueue a validated model's work items in order, spread over the side
 // streams when there are two or more. Under stream capture, `nodes` (if
 // given) receives each work item's update node.
-fsdp_status run_units(const std::vector<UnitPlan> &plan, std::vector<Span> &spans, cudaStream_t s,
-                      std::vector<UpdateNode> *nodes = nullptr) {
-    if (fsdp_status st = check_spans(spans); st != FSDP_OK) return st;
-    std::vector<Work> work;
-    std::vector<std::unique_ptr<Group>> groups;
-    make_work(plan, work, groups);
+fsdp_status run_units(const ModelPlan &m, cudaStream_t s, std::vector<UpdateNode> *nodes = nullptr) {
+    const std::vector<Work> &work = m.work;
     if (nodes) nodes->assign(work.size(), UpdateNode());
     auto node_of = [&](size_t i) { return nodes ? &(*nodes)[i] : nullptr; };
     const int busy = static_cast<int>(work.size());
     if (kUnitStreams < 2 || busy < 2) {
         for (size_t i = 0; i < work.size(); ++i)
-            if (fsdp_status st = launch_work(plan, work[i], s, node_of(i)); st != FSDP_OK) return st;
+            if (fsdp_status st = launch_work(m.units, work[i], s, node_of(i)); st != FSDP_OK) return st;
         return FSDP_OK;
     }
     SideStreams *side = nullptr;
@@ -778,7 +801,7 @@ fsdp_status run_units(const std::vector<UnitPlan> &plan, std::vector<Span> &span
         if (cudaError_t e = cudaStreamWaitEvent(side->s[i], side->fork, 0); e != cudaSuccess) return cuda_status(e);
     fsdp_status result = FSDP_OK;
     for (size_t i = 0; i < work.size(); ++i) {
-        result = launch_work(plan, work[i], side->s[i % ns], node_of(i));
+        result = launch_work(m.units, work[i], side->s[i % ns], node_of(i));
         if (result != FSDP_OK) break;
     }
     // join every side stream back into the caller's stream, also after a
@@ -792,19 +815,20 @@ fsdp_status run_units(const std::vector<UnitPlan> &plan, std::vector<Span> &span
     return result;
 }
 
-// Validation of fsdp_step_units' units (and of a captured step's): one plan
-// per unit and the spans of every written buffer.
+// Validation of fsdp_step_units' units (and of a captured or planned
+// step's): a plan per unit, the written and read ranges, the work items.
 fsdp_status plan_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp, int gathers,
-                       int fuse_first_gather, uint32_t *nonfinite_count, std::vector<UnitPlan> &plan,
-                       std::vector<Span> &spans) {
+                       int fuse_first_gather, uint32_t *nonfinite_count, uint32_t *wait_timeouts, ModelPlan &m) {
     if (n_units < 0 || (n_units > 0 && !units) || !hp) return FSDP_ERR_INVALID_ARG;
     if (gathers < 0 || gathers > FSDP_MAX_WORLD) return FSDP_ERR_INVALID_ARG;
+    if (wait_timeouts && !aligned(wait_timeouts, 4)) return FSDP_ERR_ALIGNMENT;
     const bool fuse = fuse_first_gather != 0 && gathers > 0;
-    plan.assign(static_cast<size_t>(n_units), UnitPlan());
-    spans.clear();
+    m.units.assign(static_cast<size_t>(n_units), UnitPlan());
+    m.writes.clear();
+    m.reads.clear();
     for (int u = 0; u < n_units; ++u) {
         const fsdp_unit &x = units[u];
-        UnitPlan &p = plan[static_cast<size_t>(u)];
+        UnitPlan &p = m.units[static_cast<size_t>(u)];
         p.variant = false;
         if (!dtype_valid(x.grad_dtype) || !dtype_valid(x.out_dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
         p.grad_dtype = static_cast<fsdp_dtype>(x.grad_dtype);
@@ -819,34 +843,39 @@ fsdp_status plan_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hpa
         p.separate_gathers = p.empty ? 0 : gathers - (fuse ? 1 : 0);
         if (p.separate_gathers > 0) {
             bool gempty = false;
-            st = prepare_gather(x.shard_out, p.out_dtype, x.world, x.padded_numel, x.full_bufs, x.n_full, p.gather,
-                                gempty);
+            st = prepare_gather(x.shard_out, p.out_dtype, x.world, x.padded_numel, x.full_bufs, x.n_full,
+                                wait_timeouts, p.gather, gempty);
             if (st != FSDP_OK) return st;
         }
         if (p.empty) continue;
-        const uintptr_t sb = static_cast<uintptr_t>(x.padded_numel) * 4;
-        const uintptr_t ob = static_cast<uintptr_t>(x.padded_numel) * static_cast<uintptr_t>(dtype_size(p.out_dtype));
-        add_span(spans, x.master, sb);
-        add_span(spans, x.exp_avg, sb);
-        add_span(spans, x.exp_avg_sq, sb);
-        add_span(spans, x.shard_out, ob);
+        const uintptr_t P = static_cast<uintptr_t>(x.padded_numel);
+        const uintptr_t sb = P * 4;
+        const uintptr_t ob = P * static_cast<uintptr_t>(dtype_size(p.out_dtype));
+        const uintptr_t gb = P * static_cast<uintptr_t>(dtype_size(p.grad_dtype));
+        add_span(m.writes, x.master, sb);
+        add_span(m.writes, x.exp_avg, sb);
+        add_span(m.writes, x.exp_avg_sq, sb);
+        add_span(m.writes, x.shard_out, ob);
         if (gathers > 0)
-            for (int d = 0; d < x.n_full; ++d) add_span(spans, x.full_bufs[d], ob);
+            for (int d = 0; d < x.n_full; ++d) add_span(m.writes, x.full_bufs[d], ob);
+        for (int q = 0; q < x.world; ++q) add_span(m.reads, x.grads[q], gb);
     }
-    return FSDP_OK;
+    return finish_plan(m);
 }
 
-// Validation of fsdp_step_units_ex's units (and of a captured variant
-// step's): one plan per unit and the spans of every written buffer.
+// Validation of fsdp_step_units_ex's units (and of a captured or planned
+// variant step's).
 fsdp_status plan_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg, int gathers,
-                          uint32_t *nonfinite_count, std::vector<UnitPlan> &plan, std::vector<Span> &spans) {
+                          uint32_t *nonfinite_count, uint32_t *wait_timeouts, ModelPlan &m) {
     if (n_units < 0 || (n_units > 0 && !units) || !cfg) return FSDP_ERR_INVALID_ARG;
     if (gathers < 0 || gathers > FSDP_MAX_WORLD) return FSDP_ERR_INVALID_ARG;
-    plan.assign(static_cast<size_t>(n_units), UnitPlan());
-    spans.clear();
+    if (wait_timeouts && !aligned(wait_timeouts, 4)) return FSDP_ERR_ALIGNMENT;
+    m.units.assign(static_cast<size_t>(n_units), UnitPlan());
+    m.writes.clear();
+    m.reads.clear();
     for (int u = 0; u < n_units; ++u) {
         const fsdp_unit_ex &x = units[u];
-        UnitPlan &p = plan[static_cast<size_t>(u)];
+        UnitPlan &p = m.units[static_cast<size_t>(u)];
         p.variant = true;
         if (x.reserved != 0) return FSDP_ERR_INVALID_ARG;
         if (!dtype_valid(x.grad_dtype) || !dtype_valid(x.out_dtype) || !dtype_valid(x.state_dtype))
@@ -867,27 +896,66 @@ fsdp_status plan_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_ste
         const void *shard = sd == FSDP_F32 ? x.shard_out : x.param;
         if (p.separate_gathers > 0) {
             bool gempty = false;
-            st = prepare_gather(shard, od, x.world, x.padded_numel, x.full_bufs, x.n_full, p.gather, gempty);
+            st = prepare_gather(shard, od, x.world, x.padded_numel, x.full_bufs, x.n_full, wait_timeouts, p.gather,
+                                gempty);
             if (st != FSDP_OK) return st;
         }
         if (p.empty) continue;
         const uintptr_t P = static_cast<uintptr_t>(x.padded_numel);
         const uintptr_t sb = P * static_cast<uintptr_t>(dtype_size(sd));
         const uintptr_t ob = P * static_cast<uintptr_t>(dtype_size(od));
-        add_span(spans, x.param, sb);
-        add_span(spans, x.state0, sb);
-        add_span(spans, x.state1, sb);
-        add_span(spans, x.shard_out, ob);
+        const uintptr_t gb = P * static_cast<uintptr_t>(dtype_size(gd));
+        add_span(m.writes, x.param, sb);
+        add_span(m.writes, x.state0, sb);
+        add_span(m.writes, x.state1, sb);
+        add_span(m.writes, x.shard_out, ob);
         if (gathers > 0)
-            for (int d = 0; d < x.n_full; ++d) add_span(spans, x.full_bufs[d], ob);
+            for (int d = 0; d < x.n_full; ++d) add_span(m.writes, x.full_bufs[d], ob);
+        for (int q = 0; q < x.world; ++q) add_span(m.reads, x.grads[q], gb);
     }
+    return finish_plan(m);
+}
+
+// One step's scalars written into a validated model's update arguments, per
+// unit and per batched group for its world size: the fused AdamW update's,
+void set_adam_scalars(ModelPlan &m, const fsdp_adamw_hparams &hp) {
+    for (UnitPlan &p : m.units)
+        if (!p.empty) p.rsa.s = make_scalars(hp, p.rsa.world);
+    for (auto &g : m.groups) g->rsa.s = make_scalars(hp, g->rsa.world);
+}
+
+// and the variant update's (its scalars and the reduction flag).
+void set_step_scalars(ModelPlan &m, const fsdp_step_config &c) {
+    const int lowp = c.reduce_dtype != FSDP_F32 ? 1 : 0;
+    for (UnitPlan &p : m.units) {
+        if (p.empty) continue;
+        p.step.args.k = make_step_scalars(c, p.step.args.world);
+        p.step.args.reduce_lowp = lowp;
+    }
+    for (auto &g : m.groups) {
+        g->step.k = make_step_scalars(c, g->step.world);
+        g->step.reduce_lowp = lowp;
+    }
+}
+
+// The per-step arguments of a planned or captured step, checked as the
+// single-unit entry points check them.
+bool adam_step_valid(const fsdp_adamw_hparams &hp) {
+    return hp.step >= 1 && hp.grad_scale > 0.0f && isfinite(hp.grad_scale);
+}
+
+fsdp_status step_config_valid(const fsdp_step_config &c, int optimizer, const std::vector<int> &grad_dtypes) {
+    if (c.optimizer != optimizer) return FSDP_ERR_INVALID_ARG;
+    if (c.step < 1 || !(c.grad_scale > 0.0f) || !isfinite(c.grad_scale)) return FSDP_ERR_INVALID_ARG;
+    for (int gd : grad_dtypes)
+        if (c.reduce_dtype != FSDP_F32 && c.reduce_dtype != gd) return FSDP_ERR_UNSUPPORTED_DTYPE;
     return FSDP_OK;
 }
 
-// Capture the launches of validated units into an instantiated graph,
+// Capture the launches of a validated model into an instantiated graph,
 // recording each work item's update node.
-fsdp_status capture_units(const std::vector<UnitPlan> &plan, std::vector<Span> &spans, cudaGraph_t &graph,
-                          cudaGraphExec_t &exec, std::vector<UpdateNode> &nodes) {
+fsdp_status capture_units(const ModelPlan &m, cudaGraph_t &graph, cudaGraphExec_t &exec,
+                          std::vector<UpdateNode> &nodes) {
     graph = nullptr;
     exec = nullptr;
     cudaStream_t cs = nullptr;
@@ -898,7 +966,7 @@ fsdp_status capture_units(const std::vector<UnitPlan> &plan, std::vector<Span> &
         cudaStreamDestroy(cs);
         return cuda_status(e);
     }
-    fsdp_status st = run_units(plan, spans, cs, &nodes);
+    fsdp_status st = run_units(m, cs, &nodes);
     const cudaError_t ec = cudaStreamEndCapture(cs, &graph);  // always end the capture
     cudaStreamDestroy(cs);
     if (st != FSDP_OK || ec != cudaSuccess) {
@@ -912,6 +980,19 @@ fsdp_status capture_units(const std::vector<UnitPlan> &plan, std::vector<Span> &
         return cuda_status(e);
     }
     return FSDP_OK;
+}
+
+// Placeholder hyperparameters for validating and capturing a step whose
+// launches supply their own scalars.
+const fsdp_adamw_hparams kPlaceholderHp = {0.0f, 0.9f, 0.999f, 1e-8f, 0.0f, 1, 1.0f};
+
+// Gradient dtypes of a model's non-empty units (a launch's reduction dtype
+// must be fp32 or every one of them).
+std::vector<int> grad_dtypes_of(const ModelPlan &m) {
+    std::vector<int> d;
+    for (const UnitPlan &p : m.units)
+        if (!p.empty) d.push_back(p.grad_dtype);
+    return d;
 }
 
 }  // namespace
@@ -952,54 +1033,65 @@ FSDP_API fsdp_status fsdp_reduce_scatter_step(const void *const *grads, fsdp_dty
 }
 
 FSDP_API fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world, int64_t padded_numel,
-                            void *const *full_bufs, int n_dst, void *stream) {
+                            void *const *full_bufs, int n_dst, uint32_t *wait_timeouts, void *stream) {
     GatherArgs a;
     bool empty = false;
-    const fsdp_status st = prepare_gather(shard_out, dtype, world, padded_numel, full_bufs, n_dst, a, empty);
+    const fsdp_status st =
+        prepare_gather(shard_out, dtype, world, padded_numel, full_bufs, n_dst, wait_timeouts, a, empty);
     if (st != FSDP_OK || empty) return st;
     return launch_gather(a, static_cast<cudaStream_t>(stream));
 }
 
 FSDP_API fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
                                      int gathers, int fuse_first_gather, uint32_t *nonfinite_count,
-                                     void *stream) {
-    std::vector<UnitPlan> plan;
-    std::vector<Span> spans;
-    const fsdp_status st = plan_units(units, n_units, hp, gathers, fuse_first_gather, nonfinite_count, plan, spans);
+                                     uint32_t *wait_timeouts, void *stream) {
+    ModelPlan m;
+    const fsdp_status st =
+        plan_units(units, n_units, hp, gathers, fuse_first_gather, nonfinite_count, wait_timeouts, m);
     if (st != FSDP_OK) return st;
-    return run_units(plan, spans, static_cast<cudaStream_t>(stream));
+    return run_units(m, static_cast<cudaStream_t>(stream));
 }
 
 FSDP_API fsdp_status fsdp_step_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
-                                        int gathers, uint32_t *nonfinite_count, void *stream) {
-    std::vector<UnitPlan> plan;
-    std::vector<Span> spans;
-    const fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, plan, spans);
+                                        int gathers, uint32_t *nonfinite_count, uint32_t *wait_timeouts,
+                                        void *stream) {
+    ModelPlan m;
+    const fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, wait_timeouts, m);
     if (st != FSDP_OK) return st;
-    return run_units(plan, spans, static_cast<cudaStream_t>(stream));
+    return run_units(m, static_cast<cudaStream_t>(stream));
 }
 
 FSDP_API fsdp_status fsdp_step_units_launches(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
                                               int gathers, int fuse_first_gather, int64_t *launches_out) {
     if (!launches_out) return FSDP_ERR_INVALID_ARG;
-    std::vector<UnitPlan> plan;
-    std::vector<Span> spans;
-    const fsdp_status st = plan_units(units, n_units, hp, gathers, fuse_first_gather, nullptr, plan, spans);
+    ModelPlan m;
+    const fsdp_status st = plan_units(units, n_units, hp, gathers, fuse_first_gather, nullptr, nullptr, m);
     if (st != FSDP_OK) return st;
-    return count_launches(plan, spans, launches_out);
+    *launches_out = count_launches(m);
+    return FSDP_OK;
 }
 
 FSDP_API fsdp_status fsdp_step_units_ex_launches(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
                                                  int gathers, int64_t *launches_out) {
     if (!launches_out) return FSDP_ERR_INVALID_ARG;
-    std::vector<UnitPlan> plan;
-    std::vector<Span> spans;
-    const fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nullptr, plan, spans);
+    ModelPlan m;
+    const fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nullptr, nullptr, m);
     if (st != FSDP_OK) return st;
-    return count_launches(plan, spans, launches_out);
+    *launches_out = count_launches(m);
+    return FSDP_OK;
 }
 
 }  // extern "C"
+
+// A validated model step (fsdp_step_plan_*): the model's plan, whose update
+// arguments each launch rewrites with its step's scalars. `variant` plans
+// hold the variant update of one optimizer.
+struct fsdp_step_plan {
+    ModelPlan m;
+    bool variant = false;
+    int optimizer = 0;
+    std::vector<int> grad_dtypes;
+};
 
 // A captured model step (fsdp_step_graph_*): the instantiated graph and,
 // per work item (a unit, or a group of small units in one batched launch),
@@ -1016,12 +1108,11 @@ struct fsdp_step_graph {
 
 namespace {
 
-fsdp_status make_graph(const std::vector<UnitPlan> &plan, std::vector<Span> &spans, bool variant, int optimizer,
-                       fsdp_step_graph **graph_out) {
+fsdp_status make_graph(const ModelPlan &m, bool variant, int optimizer, fsdp_step_graph **graph_out) {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
     std::vector<UpdateNode> nodes;
-    if (fsdp_status st = capture_units(plan, spans, graph, exec, nodes); st != FSDP_OK) return st;
+    if (fsdp_status st = capture_units(m, graph, exec, nodes); st != FSDP_OK) return st;
     fsdp_step_graph *g = new (std::nothrow) fsdp_step_graph;
     if (!g) {
         cudaGraphExecDestroy(exec);
@@ -1034,6 +1125,17 @@ fsdp_status make_graph(const std::vector<UnitPlan> &plan, std::vector<Span> &spa
     g->variant = variant;
     g->optimizer = optimizer;
     *graph_out = g;
+    return FSDP_OK;
+}
+
+fsdp_status make_plan(ModelPlan &m, bool variant, int optimizer, fsdp_step_plan **plan_out) {
+    fsdp_step_plan *p = new (std::nothrow) fsdp_step_plan;
+    if (!p) return FSDP_ERR_INVALID_ARG;
+    p->m = std::move(m);
+    p->variant = variant;
+    p->optimizer = optimizer;
+    p->grad_dtypes = grad_dtypes_of(p->m);
+    *plan_out = p;
     return FSDP_OK;
 }
 
@@ -1062,33 +1164,32 @@ fsdp_status set_update_node(fsdp_step_graph *graph, cudaGraphNode_t node, Fill f
 extern "C" {
 
 FSDP_API fsdp_status fsdp_step_graph_create(const fsdp_unit *units, int n_units, int gathers, int fuse_first_gather,
-                                            uint32_t *nonfinite_count, fsdp_step_graph **graph_out) {
+                                            uint32_t *nonfinite_count, uint32_t *wait_timeouts,
+                                            fsdp_step_graph **graph_out) {
     if (!graph_out) return FSDP_ERR_INVALID_ARG;
     *graph_out = nullptr;
-    // placeholder hyperparameters for validation and capture; every launch
-    // writes the step's own scalars into the update nodes
-    const fsdp_adamw_hparams hp0 = {0.0f, 0.9f, 0.999f, 1e-8f, 0.0f, 1, 1.0f};
-    std::vector<UnitPlan> plan;
-    std::vector<Span> spans;
-    fsdp_status st = plan_units(units, n_units, &hp0, gathers, fuse_first_gather, nonfinite_count, plan, spans);
+    // every launch writes the step's own scalars into the update nodes
+    ModelPlan m;
+    fsdp_status st =
+        plan_units(units, n_units, &kPlaceholderHp, gathers, fuse_first_gather, nonfinite_count, wait_timeouts, m);
     if (st != FSDP_OK) return st;
-    return make_graph(plan, spans, false, FSDP_OPT_ADAMW, graph_out);
+    return make_graph(m, false, FSDP_OPT_ADAMW, graph_out);
 }
 
 FSDP_API fsdp_status fsdp_step_graph_create_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
-                                               int gathers, uint32_t *nonfinite_count, fsdp_step_graph **graph_out) {
+                                               int gathers, uint32_t *nonfinite_count, uint32_t *wait_timeouts,
+                                               fsdp_step_graph **graph_out) {
     if (!graph_out) return FSDP_ERR_INVALID_ARG;
     *graph_out = nullptr;
-    std::vector<UnitPlan> plan;
-    std::vector<Span> spans;
-    fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, plan, spans);
+    ModelPlan m;
+    fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, wait_timeouts, m);
     if (st != FSDP_OK) return st;
-    return make_graph(plan, spans, true, cfg->optimizer, graph_out);
+    return make_graph(m, true, cfg->optimizer, graph_out);
 }
 
 FSDP_API fsdp_status fsdp_step_graph_launch(fsdp_step_graph *graph, const fsdp_adamw_hparams *hp, void *stream) {
     if (!graph || !hp || graph->variant) return FSDP_ERR_INVALID_ARG;
-    if (hp->step < 1 || !(hp->grad_scale > 0.0f) || !isfinite(hp->grad_scale)) return FSDP_ERR_INVALID_ARG;
+    if (!adam_step_valid(*hp)) return FSDP_ERR_INVALID_ARG;
     for (const UpdateNode &n : graph->nodes) {
         const AdamScalars sc = make_scalars(*hp, n.world);
         fsdp_status st = n.kind == kNodeGroup
@@ -1101,10 +1202,9 @@ FSDP_API fsdp_status fsdp_step_graph_launch(fsdp_step_graph *graph, const fsdp_a
 
 FSDP_API fsdp_status fsdp_step_graph_launch_ex(fsdp_step_graph *graph, const fsdp_step_config *cfg, void *stream) {
     if (!graph || !cfg || !graph->variant) return FSDP_ERR_INVALID_ARG;
-    if (cfg->optimizer != graph->optimizer) return FSDP_ERR_INVALID_ARG;
-    if (cfg->step < 1 || !(cfg->grad_scale > 0.0f) || !isfinite(cfg->grad_scale)) return FSDP_ERR_INVALID_ARG;
-    for (const UpdateNode &n : graph->nodes)
-        if (cfg->reduce_dtype != FSDP_F32 && cfg->reduce_dtype != n.grad_dtype) return FSDP_ERR_UNSUPPORTED_DTYPE;
+    std::vector<int> gds;
+    for (const UpdateNode &n : graph->nodes) gds.push_back(n.grad_dtype);
+    if (fsdp_status st = step_config_valid(*cfg, graph->optimizer, gds); st != FSDP_OK) return st;
     const int lowp = cfg->reduce_dtype != FSDP_F32 ? 1 : 0;
     for (const UpdateNode &n : graph->nodes) {
         const StepScalars k = make_step_scalars(*cfg, n.world);
@@ -1131,6 +1231,48 @@ FSDP_API fsdp_status fsdp_step_graph_destroy(fsdp_step_graph *graph) {
     return e1 != cudaSuccess ? cuda_status(e1) : cuda_status(e2);
 }
 
+FSDP_API fsdp_status fsdp_step_plan_create(const fsdp_unit *units, int n_units, int gathers, int fuse_first_gather,
+                                           uint32_t *nonfinite_count, uint32_t *wait_timeouts,
+                                           fsdp_step_plan **plan_out) {
+    if (!plan_out) return FSDP_ERR_INVALID_ARG;
+    *plan_out = nullptr;
+    ModelPlan m;
+    fsdp_status st =
+        plan_units(units, n_units, &kPlaceholderHp, gathers, fuse_first_gather, nonfinite_count, wait_timeouts, m);
+    if (st != FSDP_OK) return st;
+    return make_plan(m, false, FSDP_OPT_ADAMW, plan_out);
+}
+
+FSDP_API fsdp_status fsdp_step_plan_create_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
+                                              int gathers, uint32_t *nonfinite_count, uint32_t *wait_timeouts,
+                                              fsdp_step_plan **plan_out) {
+    if (!plan_out) return FSDP_ERR_INVALID_ARG;
+    *plan_out = nullptr;
+    ModelPlan m;
+    fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, wait_timeouts, m);
+    if (st != FSDP_OK) return st;
+    return make_plan(m, true, cfg->optimizer, plan_out);
+}
+
+FSDP_API fsdp_status fsdp_step_plan_launch(fsdp_step_plan *plan, const fsdp_adamw_hparams *hp, void *stream) {
+    if (!plan || !hp || plan->variant) return FSDP_ERR_INVALID_ARG;
+    if (!adam_step_valid(*hp)) return FSDP_ERR_INVALID_ARG;
+    set_adam_scalars(plan->m, *hp);
+    return run_units(plan->m, static_cast<cudaStream_t>(stream));
+}
+
+FSDP_API fsdp_status fsdp_step_plan_launch_ex(fsdp_step_plan *plan, const fsdp_step_config *cfg, void *stream) {
+    if (!plan || !cfg || !plan->variant) return FSDP_ERR_INVALID_ARG;
+    if (fsdp_status st = step_config_valid(*cfg, plan->optimizer, plan->grad_dtypes); st != FSDP_OK) return st;
+    set_step_scalars(plan->m, *cfg);
+    return run_units(plan->m, static_cast<cudaStream_t>(stream));
+}
+
+FSDP_API fsdp_status fsdp_step_plan_destroy(fsdp_step_plan *plan) {
+    delete plan;
+    return FSDP_OK;
+}
+
 FSDP_API const char *fsdp_status_string(fsdp_status status) {
     switch (status) {
         case FSDP_OK: return "FSDP_OK";
@@ -1152,9 +1294,11 @@ FSDP_API fsdp_status fsdp_take_wait_timeouts(uint32_t *count_out) {
     return FSDP_OK;
 }
 
-FSDP_API fsdp_status fsdp_check_bounded_wait(int64_t limit_cycles, void *stream) {
+FSDP_API fsdp_status fsdp_check_bounded_wait(int64_t limit_cycles, uint32_t *wait_timeouts, void *stream) {
     if (limit_cycles < 1 || limit_cycles > (int64_t{1} << 31)) return FSDP_ERR_INVALID_ARG;
-    return launch_stalled_wait(static_cast<long long>(limit_cycles), static_cast<cudaStream_t>(stream));
+    if (wait_timeouts && !aligned(wait_timeouts, 4)) return FSDP_ERR_ALIGNMENT;
+    return launch_stalled_wait(static_cast<long long>(limit_cycles), wait_timeouts,
+                               static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

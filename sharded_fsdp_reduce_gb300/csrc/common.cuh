@@ -184,6 +184,7 @@ struct GatherArgs {
     void *dst[FSDP_MAX_WORLD];
     int64_t nbytes;
     int n_dst;
+    uint32_t *timeouts;  // the call's count of bounded waits that gave up (device, or NULL)
 };
 
 

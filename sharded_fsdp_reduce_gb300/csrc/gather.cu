@@ -73,8 +73,16 @@ constexpr int kTmaThreads = 32;
 constexpr int64_t kTmaMinBytes = 1 << 20;
 constexpr long long kWaitLimitCycles = 1ll << 31;  // ~1 s at 2 GHz
 
-// Bounded mbarrier waits that gave up (a kernel then returns early).
+// Bounded mbarrier waits that gave up (a kernel then returns early), over
+// every call on this device since the last fsdp_take_wait_timeouts.
 __device__ uint32_t g_gather_wait_timeouts;
+
+// A bounded wait gave up: count it on the device and, when the caller asked
+// for it, in the call's own counter.
+__device__ __forceinline__ void count_timeout(uint32_t *per_call) {
+    atomicAdd(&g_gather_wait_timeouts, 1u);
+    if (per_call != nullptr) atomicAdd(per_call, 1u);
+}
 
 template <int ND>
 __global__ void __launch_bounds__(kTmaThreads)
@@ -113,12 +121,20 @@ __global__ void __launch_bounds__(kTmaThreads)
         tma::bulk_load(smem + s * kTile, src + t * kTile, bytes, &bar[s]);
     };
 
-    for (int64_t it = 0; it < mine && it < kStages; ++it) load(it);
+    int64_t issued = 0;  // loads issued: iterations [0, issued)
+    for (; issued < mine && issued < kStages; ++issued) load(issued);
     uint32_t parity = 0;  // bit s: parity of stage s's next phase
     for (int64_t it = 0; it < mine; ++it) {
         const int s = static_cast<int>(it % kStages);
         if (!tma::mbar_wait_bounded(&bar[s], (parity >> s) & 1u, kWaitLimitCycles)) {
-            atomicAdd(&g_gather_wait_timeouts, 1u);
+            count_timeout(a.timeouts);
+            // The loads of iterations [it, issued) may still be writing this
+            // CTA's shared memory: give each one more bounded wait (iteration
+            // j completes phase j / kStages of its stage) so that a copy that
+            // is only slow lands before the CTA exits, then drain the stores.
+            for (int64_t j = it; j < issued; ++j)
+                (void)tma::mbar_wait_bounded(&bar[j % kStages], static_cast<uint32_t>((j / kStages) & 1),
+                                             kWaitLimitCycles);
             tma::bulk_wait<0>();
             return;
         }
@@ -137,6 +153,7 @@ __global__ void __launch_bounds__(kTmaThreads)
         if (it >= 1 && it - 1 + kStages < mine) {
             tma::bulk_wait_read<1>();
             load(it - 1 + kStages);
+            issued = it + kStages;
         }
     }
     tma::bulk_wait<0>();
@@ -183,7 +200,10 @@ __global__ void __launch_bounds__(kTmaThreads) gather_group_kernel(const __grid_
     tma::mbar_arrive_expect_tx(&bar, bytes);
     tma::bulk_load(smem, src + off, bytes, &bar);
     if (!tma::mbar_wait_bounded(&bar, 0, kWaitLimitCycles)) {
-        atomicAdd(&g_gather_wait_timeouts, 1u);
+        count_timeout(g.timeouts);
+        // one more bounded wait, so that a load that is only slow lands in
+        // shared memory before the CTA exits
+        (void)tma::mbar_wait_bounded(&bar, 0, kWaitLimitCycles);
         tma::bulk_wait<0>();
         return;
     }
@@ -193,15 +213,16 @@ __global__ void __launch_bounds__(kTmaThreads) gather_group_kernel(const __grid_
 }
 
 // A bounded wait on a barrier that nothing completes (two arrivals expected,
-// one made): it gives up after `limit` cycles and is counted like a gather's.
-// The failure path of the bounded waits, exercised without a fault.
-__global__ void __launch_bounds__(32) stalled_wait_kernel(long long limit) {
+// one made): it gives up after `limit` cycles and is counted like a gather's,
+// on the device and in the call's counter. The failure path of the bounded
+// waits, exercised without a fault.
+__global__ void __launch_bounds__(32) stalled_wait_kernel(long long limit, uint32_t *per_call) {
     __shared__ __align__(8) uint64_t bar;
     if (threadIdx.x != 0) return;
     tma::mbar_init(&bar, 2);
     tma::fence_mbar_init();
     tma::mbar_arrive(&bar);
-    if (!tma::mbar_wait_bounded(&bar, 0, limit)) atomicAdd(&g_gather_wait_timeouts, 1u);
+    if (!tma::mbar_wait_bounded(&bar, 0, limit)) count_timeout(per_call);
 }
 
 template <int ND>
@@ -267,8 +288,8 @@ fsdp_status launch_gather_group(const GatherGroupArgs &g, int64_t grid, cudaStre
     return check_launch();
 }
 
-fsdp_status launch_stalled_wait(long long limit_cycles, cudaStream_t stream) {
-    stalled_wait_kernel<<<1, 32, 0, stream>>>(limit_cycles);
+fsdp_status launch_stalled_wait(long long limit_cycles, uint32_t *per_call, cudaStream_t stream) {
+    stalled_wait_kernel<<<1, 32, 0, stream>>>(limit_cycles, per_call);
     return check_launch();
 }
 

@@ -24,6 +24,11 @@ constexpr int kGroupMaxWorld = 8;                       // gradient / destinatio
 #endif
 constexpr int64_t kGroupMaxNumel = int64_t(1) << FSDP_GROUP_MAX_NUMEL_LOG2;  // units up to this size are batched
 constexpr int kGroupGatherTile = 16384;                 // bytes per CTA of the batched gather
+// Threads per CTA of both batched updates. A unit's CTA count is sized from
+// it on the host (group_update_ctas), so each batched kernel asserts that it
+// launches exactly this many: a build that changed one kernel's block size
+// alone would otherwise leave chunks of every unit unvisited.
+constexpr int kGroupThreads = 256;
 
 // One unit of a batched update: all ranks' blocks [0, numel), every base
 // pointer 16-byte aligned, state in device memory.
@@ -60,6 +65,7 @@ struct GatherGroupUnit {
 struct GatherGroupArgs {
     int32_t n;
     int32_t pad;
+    uint32_t *timeouts;  // the call's count of bounded waits that gave up (device, or NULL)
     GatherGroupUnit u[kGroupMax];
 };
 
@@ -92,9 +98,9 @@ static_assert(sizeof(RsaGroupArgs) < 32764, "kernel parameter space");
 static_assert(sizeof(StepGroupArgs) < 32764, "kernel parameter space");
 static_assert(sizeof(GatherGroupArgs) < 32764, "kernel parameter space");
 
-// CTAs of one unit in a batched update, and tiles of one unit in a batched
-// gather (at least one each: a CTA also takes the elements or bytes after the
-// vector part).
+// CTAs of one unit in a batched update (kGroupThreads chunks each), and
+// tiles of one unit in a batched gather (at least one each: a CTA also takes
+// the elements or bytes after the vector part).
 int32_t group_update_ctas(int64_t numel);
 int64_t group_gather_tiles(int64_t nbytes);
 

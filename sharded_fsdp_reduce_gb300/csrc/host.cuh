@@ -102,7 +102,7 @@ fsdp_status launch_gather(const GatherArgs &a, cudaStream_t stream);
 
 // Read and reset the count of bounded waits that gave up in the gather kernels.
 uint32_t take_gather_wait_timeouts();
-fsdp_status launch_stalled_wait(long long limit_cycles, cudaStream_t stream);
+fsdp_status launch_stalled_wait(long long limit_cycles, uint32_t *per_call, cudaStream_t stream);
 
 fsdp_status launch_flatten(const FlattenArgs &a, cudaStream_t stream);
 

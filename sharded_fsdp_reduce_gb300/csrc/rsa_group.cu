@@ -13,6 +13,8 @@
 namespace fsdp {
 namespace {
 
+static_assert(rsa::kThreads == kGroupThreads, "the batched update's CTAs are sized for kGroupThreads threads");
+
 // Launch bound: the per-unit kernel's 3 CTAs per SM (80 registers, no
 // spills), except with fp32 gradients at N = 8, whose 16 gradient words per
 // chunk plus the unit lookup spill 128 bytes per thread at that budget; 2 CTAs
@@ -95,7 +97,7 @@ fsdp_status launch_gd(const RsaGroupArgs &g, int out_dtype, int64_t grid, cudaSt
 }  // namespace
 
 int32_t group_update_ctas(int64_t numel) {
-    const int64_t per_cta = int64_t(8) * rsa::kThreads;
+    const int64_t per_cta = int64_t(8) * kGroupThreads;
     const int64_t n = (numel / 8 * 8 + per_cta - 1) / per_cta;
     return static_cast<int32_t>(n > 0 ? n : 1);
 }

@@ -14,6 +14,8 @@
 namespace fsdp {
 namespace step {
 
+static_assert(kThreads == kGroupThreads, "the batched update's CTAs are sized for kGroupThreads threads");
+
 // Launch bound: the per-unit kernel's (3 CTAs per SM), except with fp32
 // gradients at N = 8, whose 16 gradient words per chunk plus the unit lookup
 // spill 48-128 bytes per thread at that budget; 2 CTAs per SM (128

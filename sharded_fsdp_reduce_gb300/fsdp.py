@@ -20,7 +20,7 @@ __all__ = [
     "fsdp_reduce_scatter_adam_cast", "fsdp_reduce_scatter_adam_cast_gather", "fsdp_all_gather",
     "fsdp_status_string",
     "fsdp_last_cuda_error", "fsdp_take_wait_timeouts", "fsdp_check_bounded_wait", "dtype_code",
-    "UnitDescs", "fsdp_step_units", "fsdp_step_units_ex", "StepGraph",
+    "UnitDescs", "fsdp_step_units", "fsdp_step_units_ex", "StepGraph", "StepPlan",
     "fsdp_step_units_launches", "fsdp_step_units_ex_launches",
 ]
 
@@ -150,13 +150,14 @@ def _check_fp32_state(P_pad: int, prefix: str = "", **bufs: torch.Tensor) -> Non
             raise ValueError(f"{prefix}{name} must be float32 with {P_pad} elements")
 
 
-def _counter(t: Optional[torch.Tensor]):
-    """Device address of the optional non-finite counter (a CUDA int32/uint32 tensor)."""
+def _counter(t: Optional[torch.Tensor], name: str = "nonfinite_count"):
+    """Device address of an optional counter (a CUDA int32/uint32 tensor): the
+    non-finite gradient count, or a call's count of bounded waits that gave up."""
     if t is None:
         return None
     if t.dtype not in (torch.int32, torch.uint32) or t.numel() < 1:
-        raise ValueError("nonfinite_count must be a CUDA int32/uint32 tensor")
-    return _dev(t, "nonfinite_count")
+        raise ValueError(f"{name} must be a CUDA int32/uint32 tensor")
+    return _dev(t, name)
 
 
 def _views(c_views, n) -> List[View]:
@@ -173,17 +174,21 @@ def fsdp_last_cuda_error() -> int:
 
 
 def fsdp_take_wait_timeouts() -> int:
-    """Bounded in-kernel waits that gave up since the last call (synchronizes the device)."""
+    """Bounded in-kernel waits that gave up since the last call, on the whole
+    device (synchronizes the device). A call's own count: its wait_timeouts."""
     n = ctypes.c_uint32(0)
     _check(_lib.load().fsdp_take_wait_timeouts(ctypes.byref(n)), "fsdp_take_wait_timeouts")
     return int(n.value)
 
 
-def fsdp_check_bounded_wait(limit_cycles: int, stream: Optional[torch.cuda.Stream] = None) -> None:
+def fsdp_check_bounded_wait(limit_cycles: int, stream: Optional[torch.cuda.Stream] = None,
+                            wait_timeouts: Optional[torch.Tensor] = None) -> None:
     """Self-test of the bounded waits' failure path: one kernel waits on a
     barrier that nothing completes and gives up after about limit_cycles SM
-    cycles; fsdp_take_wait_timeouts() then counts it. Asynchronous."""
-    _check(_lib.load().fsdp_check_bounded_wait(int(limit_cycles), _stream(stream)), "fsdp_check_bounded_wait")
+    cycles; fsdp_take_wait_timeouts() then counts it, and so does
+    wait_timeouts (a CUDA int32/uint32 counter) when given. Asynchronous."""
+    _check(_lib.load().fsdp_check_bounded_wait(int(limit_cycles), _counter(wait_timeouts, "wait_timeouts"),
+                                               _stream(stream)), "fsdp_check_bounded_wait")
 
 
 def fsdp_padded_numel(numel: int, world: int) -> int:
@@ -322,14 +327,17 @@ def fsdp_reduce_scatter_step(grads: Sequence[torch.Tensor], param: torch.Tensor,
 
 
 def fsdp_all_gather(shard_out: torch.Tensor, full_bufs: Sequence[torch.Tensor], world: int,
-                    stream: Optional[torch.cuda.Stream] = None) -> None:
-    """Copy the rank-ordered shards (shard_out, [P_pad]) into every full buffer."""
+                    stream: Optional[torch.cuda.Stream] = None, wait_timeouts: Optional[torch.Tensor] = None) -> None:
+    """Copy the rank-ordered shards (shard_out, [P_pad]) into every full buffer.
+    wait_timeouts: optional CUDA int32/uint32 counter, incremented by each of
+    this call's bounded waits that gave up (non-zero: the copy is incomplete)."""
     P_pad = shard_out.numel()
     for i, f in enumerate(full_bufs):
         if f.numel() != P_pad or f.dtype != shard_out.dtype:
             raise ValueError(f"full_bufs[{i}] must hold {P_pad} elements of {shard_out.dtype}")
     _check(_lib.load().fsdp_all_gather(_dev(shard_out, "shard_out"), dtype_code(shard_out.dtype), int(world),
-                                       P_pad, _ptrs(full_bufs, "full_bufs"), len(full_bufs), _stream(stream)),
+                                       P_pad, _ptrs(full_bufs, "full_bufs"), len(full_bufs),
+                                       _counter(wait_timeouts, "wait_timeouts"), _stream(stream)),
            "fsdp_all_gather")
 
 
@@ -389,31 +397,35 @@ class UnitDescs:
 
 def fsdp_step_units(units, hparams: AdamWHParams, gathers: int = 1, fuse_first_gather: bool = False,
                     nonfinite_count: Optional[torch.Tensor] = None,
-                    stream: Optional[torch.cuda.Stream] = None) -> None:
+                    stream: Optional[torch.cuda.Stream] = None, wait_timeouts: Optional[torch.Tensor] = None) -> None:
     """The step of a whole model in one call: for each unit in order, its
     fused reduce-scatter + AdamW + cast, then `gathers` all-gathers into its
     full buffers (the first written by the update kernel itself with
     fuse_first_gather). `units` is a UnitDescs or a sequence of units (then
-    descriptors are built for this call)."""
+    descriptors are built for this call). Every call validates every unit;
+    StepPlan validates once for repeated steps."""
     descs = units if isinstance(units, UnitDescs) else UnitDescs(units)
     if not descs.adamw:
         raise ValueError("fsdp_step_units needs fp32 master and AdamW state in every unit; use fsdp_step_units_ex")
     nf = _counter(nonfinite_count)
+    wt = _counter(wait_timeouts, "wait_timeouts")
     hp = hparams.to_c()
     _check(_lib.load().fsdp_step_units(descs.array, descs.n, ctypes.byref(hp), int(gathers),
-                                       1 if fuse_first_gather else 0, nf, _stream(stream)), "fsdp_step_units")
+                                       1 if fuse_first_gather else 0, nf, wt, _stream(stream)), "fsdp_step_units")
 
 
 def fsdp_step_units_ex(units, config: StepConfig, gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None,
-                       stream: Optional[torch.cuda.Stream] = None) -> None:
+                       stream: Optional[torch.cuda.Stream] = None,
+                       wait_timeouts: Optional[torch.Tensor] = None) -> None:
     """The variant step of a whole model in one call: for each unit in order,
     fsdp_reduce_scatter_step's update under `config`, then `gathers`
     all-gathers of its compute-dtype shards into its full buffers. `units` is
     a UnitDescs or a sequence of units."""
     descs = units if isinstance(units, UnitDescs) else UnitDescs(units)
     nf = _counter(nonfinite_count)
+    wt = _counter(wait_timeouts, "wait_timeouts")
     cfg = config.to_c()
-    _check(_lib.load().fsdp_step_units_ex(descs.array_ex, descs.n, ctypes.byref(cfg), int(gathers), nf,
+    _check(_lib.load().fsdp_step_units_ex(descs.array_ex, descs.n, ctypes.byref(cfg), int(gathers), nf, wt,
                                           _stream(stream)), "fsdp_step_units_ex")
 
 
@@ -444,50 +456,49 @@ def fsdp_step_units_ex_launches(units, config: StepConfig, gathers: int = 1) -> 
     return int(n.value)
 
 
-class StepGraph:
-    """A model step captured as a CUDA graph (fsdp_step_graph_create, or
-    fsdp_step_graph_create_ex when `config` is given): one launch runs every
-    unit's update and gathers, with the scalars of the step given to
-    launch(). The units' buffers must stay allocated (the graph holds their
-    addresses; the units are kept alive here)."""
+class _StepHandle:
+    """A model step prepared once by the library (a captured graph or a
+    validated plan) and launched with each step's scalars. The units'
+    buffers must stay allocated (the library holds their addresses; the units
+    are kept alive here)."""
+
+    _CREATE, _CREATE_EX, _LAUNCH, _LAUNCH_EX, _DESTROY = "", "", "", "", ""
 
     def __init__(self, units, gathers: int = 1, fuse_first_gather: bool = False,
-                 nonfinite_count: Optional[torch.Tensor] = None, config: Optional[StepConfig] = None):
+                 nonfinite_count: Optional[torch.Tensor] = None, config: Optional[StepConfig] = None,
+                 wait_timeouts: Optional[torch.Tensor] = None):
         self.descs = units if isinstance(units, UnitDescs) else UnitDescs(units)
         self.config = config
-        self._counter = nonfinite_count
+        self._counters = (nonfinite_count, wait_timeouts)
         self._handle = ctypes.c_void_p(None)
         lib = _lib.load()
+        nf, wt = _counter(nonfinite_count), _counter(wait_timeouts, "wait_timeouts")
         if config is None:
             if not self.descs.adamw:
-                raise ValueError("a captured AdamW step needs fp32 master and AdamW state in every unit")
-            st = lib.fsdp_step_graph_create(self.descs.array, self.descs.n, int(gathers), 1 if fuse_first_gather else 0,
-                                            _counter(nonfinite_count), ctypes.byref(self._handle))
+                raise ValueError("an AdamW model step needs fp32 master and AdamW state in every unit")
+            st = getattr(lib, self._CREATE)(self.descs.array, self.descs.n, int(gathers),
+                                            1 if fuse_first_gather else 0, nf, wt, ctypes.byref(self._handle))
         else:
             if fuse_first_gather:
                 raise ValueError("the variant step has no fused gather")
             cfg = config.to_c()
-            st = lib.fsdp_step_graph_create_ex(self.descs.array_ex, self.descs.n, ctypes.byref(cfg), int(gathers),
-                                               _counter(nonfinite_count), ctypes.byref(self._handle))
-        _check(st, "fsdp_step_graph_create")
+            st = getattr(lib, self._CREATE_EX)(self.descs.array_ex, self.descs.n, ctypes.byref(cfg), int(gathers),
+                                               nf, wt, ctypes.byref(self._handle))
+        _check(st, self._CREATE)
 
     def launch(self, hparams, stream: Optional[torch.cuda.Stream] = None) -> None:
-        """Run the captured step: hparams is AdamWHParams for an AdamW capture,
-        a StepConfig of the captured optimizer for a variant capture."""
+        """Run one step: hparams is AdamWHParams for an AdamW step, a
+        StepConfig of the same optimizer for a variant step."""
         if not self._handle:
-            raise RuntimeError("the captured step was destroyed")
+            raise RuntimeError("the model step was destroyed")
         lib = _lib.load()
-        if self.config is None:
-            hp = hparams.to_c()
-            st = lib.fsdp_step_graph_launch(self._handle, ctypes.byref(hp), _stream(stream))
-        else:
-            cfg = hparams.to_c()
-            st = lib.fsdp_step_graph_launch_ex(self._handle, ctypes.byref(cfg), _stream(stream))
-        _check(st, "fsdp_step_graph_launch")
+        c = hparams.to_c()
+        name = self._LAUNCH if self.config is None else self._LAUNCH_EX
+        _check(getattr(lib, name)(self._handle, ctypes.byref(c), _stream(stream)), name)
 
     def close(self) -> None:
         if self._handle:
-            _check(_lib.load().fsdp_step_graph_destroy(self._handle), "fsdp_step_graph_destroy")
+            _check(getattr(_lib.load(), self._DESTROY)(self._handle), self._DESTROY)
             self._handle = ctypes.c_void_p(None)
 
     def __del__(self):
@@ -495,3 +506,22 @@ class StepGraph:
             self.close()
         except Exception:
             pass
+
+
+class StepGraph(_StepHandle):
+    """A model step captured as a CUDA graph (fsdp_step_graph_create, or
+    fsdp_step_graph_create_ex when `config` is given): one launch runs every
+    unit's update and gathers, with the scalars of the step given to
+    launch()."""
+
+    _CREATE, _CREATE_EX = "fsdp_step_graph_create", "fsdp_step_graph_create_ex"
+    _LAUNCH, _LAUNCH_EX, _DESTROY = "fsdp_step_graph_launch", "fsdp_step_graph_launch_ex", "fsdp_step_graph_destroy"
+
+
+class StepPlan(_StepHandle):
+    """A model step validated once (fsdp_step_plan_create, or
+    fsdp_step_plan_create_ex when `config` is given): launch() enqueues the
+    launches fsdp_step_units would make, checking only the step's scalars."""
+
+    _CREATE, _CREATE_EX = "fsdp_step_plan_create", "fsdp_step_plan_create_ex"
+    _LAUNCH, _LAUNCH_EX, _DESTROY = "fsdp_step_plan_launch", "fsdp_step_plan_launch_ex", "fsdp_step_plan_destroy"

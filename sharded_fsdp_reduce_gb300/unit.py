@@ -37,7 +37,8 @@ from typing import Dict, List, Optional, Sequence, Tuple
 
 import torch
 
-from .fsdp import (OPTIMIZERS, AdamWHParams, StepConfig, StepGraph, UnitDescs, View, fsdp_all_gather, fsdp_flatten_pad,
+from .fsdp import (OPTIMIZERS, AdamWHParams, StepConfig, StepGraph, StepPlan, UnitDescs, View, fsdp_all_gather,
+                   fsdp_flatten_pad,
                    fsdp_reduce_scatter_adam_cast, fsdp_reduce_scatter_adam_cast_gather, fsdp_reduce_scatter_step,
                    fsdp_step_units, fsdp_step_units_ex, fsdp_step_units_ex_launches, fsdp_step_units_launches,
                    fsdp_unflatten_views)
@@ -149,17 +150,20 @@ class FlatParamUnit:
                                  None if lowp else self.shard_out, self.step_config(hp), rank_begin, rank_end,
                                  nonfinite_count, stream)
 
-    def all_gather(self, stream=None) -> None:
-        fsdp_all_gather(self.shard_out, self.full, self.world, stream)
+    def all_gather(self, stream=None, wait_timeouts: Optional[torch.Tensor] = None) -> None:
+        fsdp_all_gather(self.shard_out, self.full, self.world, stream, wait_timeouts=wait_timeouts)
 
     def step(self, hp: AdamWHParams, gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None,
-             stream=None, fuse_gather: bool = False) -> None:
+             stream=None, fuse_gather: bool = False, wait_timeouts: Optional[torch.Tensor] = None) -> None:
         """Reduce-scatter + AdamW + cast, then ``gathers`` all-gathers, in stream order.
 
         gathers=2 is reshard-after-forward (gathered before forward and again
         before backward), gathers=1 the no-reshard mode. With fuse_gather the
         first gather is written by the update kernel itself (the fused AdamW
-        kernel only). hp: AdamWHParams, or a StepConfig for the variant step."""
+        kernel only). hp: AdamWHParams, or a StepConfig for the variant step.
+        wait_timeouts: optional CUDA int32 counter of the gathers' bounded
+        waits that gave up (zeroed by the caller; non-zero after the step's
+        work: the gathered buffers are incomplete and the device is suspect)."""
         if fuse_gather and gathers >= 1 and (self.variant or not isinstance(hp, AdamWHParams)):
             raise ValueError("fuse_gather needs the fused AdamW kernel (fp32 state, AdamWHParams)")
         if fuse_gather and gathers >= 1:
@@ -170,11 +174,12 @@ class FlatParamUnit:
         else:
             self.reduce_scatter_adam_cast(hp, nonfinite_count=nonfinite_count, stream=stream)
         for _ in range(gathers):
-            self.all_gather(stream)
+            self.all_gather(stream, wait_timeouts)
 
     def step_from_host(self, host_grads: Sequence[torch.Tensor], host_out: Optional[torch.Tensor], hp: AdamWHParams,
                        gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None,
-                       host_nonfinite: Optional[torch.Tensor] = None) -> None:
+                       host_nonfinite: Optional[torch.Tensor] = None,
+                       wait_timeouts: Optional[torch.Tensor] = None) -> None:
         """One step whose N gradient buffers come from pinned host memory.
         Its results go back to pinned host memory as asked: host_out receives
         the compute-dtype parameters (shard_out, all ranks' shards);
@@ -183,12 +188,13 @@ class FlatParamUnit:
         Asynchronous; consecutive calls overlap: the host-to-device copy of a
         step runs on its own stream into a second set of gradient buffers
         while the previous step's kernels and device-to-host copies run. The
-        host buffers are complete once the current stream is synchronized."""
+        host buffers are complete once the current stream is synchronized.
+        wait_timeouts: as in step()."""
         if host_nonfinite is not None and nonfinite_count is None:
             raise ValueError("host_nonfinite needs a device nonfinite_count")
         if self._host is None:
             self._host = _HostPipeline(self)
-        self._host.step(host_grads, host_out, hp, gathers, nonfinite_count, host_nonfinite)
+        self._host.step(host_grads, host_out, hp, gathers, nonfinite_count, host_nonfinite, wait_timeouts)
 
     # ---------------------------------------------------------------- snapshot / resume
 
@@ -251,7 +257,7 @@ class _HostPipeline:
         self.copy_out = torch.cuda.Stream(device=unit.device)
         self.i = 0
 
-    def step(self, host_grads, host_out, hp, gathers, nonfinite_count, host_nonfinite):
+    def step(self, host_grads, host_out, hp, gathers, nonfinite_count, host_nonfinite, wait_timeouts=None):
         u = self.unit
         if len(host_grads) != u.world:
             raise ValueError(f"need {u.world} host gradient buffers")
@@ -278,41 +284,78 @@ class _HostPipeline:
                 host_nonfinite.copy_(nonfinite_count, non_blocking=True)
         self.out_read = self.copy_out.record_event()
         for _ in range(gathers):
-            fsdp_all_gather(u.shard_out, u.full, u.world, stream=compute)
+            fsdp_all_gather(u.shard_out, u.full, u.world, stream=compute, wait_timeouts=wait_timeouts)
         compute.wait_stream(self.copy_out)  # the step ends when its result is on the host
         self.i += 1
 
 
 class UnitSequence:
-    """The FSDP units of a model, stepped by one call into the library
-    (fsdp_step_units, or fsdp_step_units_ex for the variant steps): per unit
-    the update and its all-gathers, ordered on the caller's stream. The
+    """The FSDP units of a model, stepped by one call into the library: per
+    unit the update and its all-gathers, ordered on the caller's stream. The
     native loop spreads the units over two side streams and batches units of
     up to 2^24 elements that share N, dtypes and gathers into one launch per
     kernel (128 units at most); the results are those of stepping each unit
-    on its own."""
+    on its own.
+
+    step() validates the model once and keeps that plan (StepPlan) for the
+    steps that follow with the same gathers, fusion, optimizer and counters,
+    so a step pays only its launches; step_unplanned() validates every
+    unit on every call (fsdp_step_units / fsdp_step_units_ex). Both hold the
+    units' buffer addresses from construction: build a new UnitSequence if a
+    unit's buffers are replaced. One host thread at a time steps a given
+    sequence (each planned step rewrites the plan's kernel arguments)."""
 
     def __init__(self, units: Sequence[FlatParamUnit]):
         self.units = list(units)
         self.descs = UnitDescs(self.units)
+        self._plan = None       # the last StepPlan made by step()
+        self._plan_key = None   # what it was made for
 
-    def step(self, hp, gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None,
-             stream=None, fuse_gather: bool = False) -> None:
-        """hp: AdamWHParams (every unit AdamW; the fused kernel where the state
-        is fp32) or a StepConfig (the variant kernel in every unit)."""
-        if isinstance(hp, AdamWHParams) and all(not u.variant for u in self.units):
-            fsdp_step_units(self.descs, hp, gathers, fuse_gather, nonfinite_count, stream)
-            return
+    def _adamw_fused(self, hp) -> bool:
+        return isinstance(hp, AdamWHParams) and all(not u.variant for u in self.units)
+
+    def _variant_config(self, hp, fuse_gather: bool) -> StepConfig:
         if fuse_gather:
             raise ValueError("fuse_gather needs the fused AdamW kernel in every unit")
         cfg = hp if isinstance(hp, StepConfig) else StepConfig(
             "adamw", hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.step, hp.grad_scale)
         for u in self.units:
             u.step_config(cfg)  # every unit takes this optimizer
-        fsdp_step_units_ex(self.descs, cfg, gathers, nonfinite_count, stream)
+        return cfg
+
+    def step(self, hp, gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None,
+             stream=None, fuse_gather: bool = False, wait_timeouts: Optional[torch.Tensor] = None) -> None:
+        """hp: AdamWHParams (every unit AdamW; the fused kernel where the state
+        is fp32) or a StepConfig (the variant kernel in every unit).
+        nonfinite_count / wait_timeouts: optional CUDA int32 counters, summed
+        over the units (see FlatParamUnit.step)."""
+        ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        if self._adamw_fused(hp):
+            config, kind = None, "adamw"
+        else:
+            config = self._variant_config(hp, fuse_gather)
+            kind = config.optimizer
+        key = (kind, int(gathers), bool(fuse_gather), ptr(nonfinite_count), ptr(wait_timeouts))
+        if key != self._plan_key:
+            if self._plan is not None:
+                self._plan.close()
+                self._plan, self._plan_key = None, None
+            self._plan = StepPlan(self.descs, gathers, fuse_gather, nonfinite_count, config, wait_timeouts)
+            self._plan_key = key
+        self._plan.launch(hp if config is None else config, stream)
+
+    def step_unplanned(self, hp, gathers: int = 1, nonfinite_count: Optional[torch.Tensor] = None,
+                       stream=None, fuse_gather: bool = False, wait_timeouts: Optional[torch.Tensor] = None) -> None:
+        """The same step through the call that validates every unit each time."""
+        if self._adamw_fused(hp):
+            fsdp_step_units(self.descs, hp, gathers, fuse_gather, nonfinite_count, stream, wait_timeouts)
+            return
+        cfg = self._variant_config(hp, fuse_gather)
+        fsdp_step_units_ex(self.descs, cfg, gathers, nonfinite_count, stream, wait_timeouts)
 
     def capture(self, gathers: int = 1, fuse_gather: bool = False,
-                nonfinite_count: Optional[torch.Tensor] = None, config: Optional[StepConfig] = None) -> StepGraph:
+                nonfinite_count: Optional[torch.Tensor] = None, config: Optional[StepConfig] = None,
+                wait_timeouts: Optional[torch.Tensor] = None) -> StepGraph:
         """The model's step captured as one CUDA graph; StepGraph.launch runs it
         for any step. Without `config`: the fused AdamW step (every unit
         AdamW with fp32 state), launched with AdamWHParams. With a StepConfig
@@ -323,7 +366,7 @@ class UnitSequence:
         if config is not None:
             for u in self.units:
                 u.step_config(config)  # every unit takes this optimizer
-        return StepGraph(self.descs, gathers, fuse_gather, nonfinite_count, config)
+        return StepGraph(self.descs, gathers, fuse_gather, nonfinite_count, config, wait_timeouts)
 
     def launches(self, gathers: int = 1, fuse_gather: bool = False, config: Optional[StepConfig] = None) -> int:
         """Kernel launches of one model step as step() (or capture()) makes

@@ -45,7 +45,7 @@ int main(void) {
                                         (float *)0x3000000, (void *)0x4000000, FSDP_BF16, &hp, 0, 2, NULL,
                                         NULL) == FSDP_ERR_UNSUPPORTED_DTYPE);
     void *dst[1] = {(void *)0x5000001};
-    CHECK(fsdp_all_gather((const void *)0x4000000, FSDP_BF16, 2, 16, dst, 1, NULL) == FSDP_ERR_ALIGNMENT);
+    CHECK(fsdp_all_gather((const void *)0x4000000, FSDP_BF16, 2, 16, dst, 1, NULL, NULL) == FSDP_ERR_ALIGNMENT);
     fsdp_step_config cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.optimizer = FSDP_OPT_SGD;
@@ -57,7 +57,7 @@ int main(void) {
                                    (void *)0x3000000 /* SGD takes one state */, FSDP_F32, (void *)0x4000000,
                                    FSDP_BF16, &cfg, 0, 2, NULL, NULL) == FSDP_ERR_INVALID_ARG);
     /* the multi-unit step: nothing to do, then a unit rejected before launch */
-    CHECK(fsdp_step_units(NULL, 0, &hp, 2, 0, NULL, NULL) == FSDP_OK);
+    CHECK(fsdp_step_units(NULL, 0, &hp, 2, 0, NULL, NULL, NULL) == FSDP_OK);
     void *fulls[2] = {(void *)0x8000000, (void *)0x9000000};
     fsdp_unit u;
     memset(&u, 0, sizeof(u));
@@ -72,9 +72,9 @@ int main(void) {
     u.grad_dtype = FSDP_BF16;
     u.out_dtype = FSDP_BF16;
     u.n_full = 2;
-    CHECK(fsdp_step_units(&u, 1, &hp, 1, 1, NULL, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_step_units(&u, 1, &hp, 1, 1, NULL, NULL, NULL) == FSDP_ERR_INVALID_ARG);
     u.padded_numel = 0; /* an empty unit is skipped */
-    CHECK(fsdp_step_units(&u, 1, &hp, 1, 1, NULL, NULL) == FSDP_OK);
+    CHECK(fsdp_step_units(&u, 1, &hp, 1, 1, NULL, NULL, NULL) == FSDP_OK);
     /* the variant multi-unit step: SGD takes one state */
     fsdp_unit_ex v;
     memset(&v, 0, sizeof(v));
@@ -90,9 +90,9 @@ int main(void) {
     v.state_dtype = FSDP_F32;
     v.out_dtype = FSDP_BF16;
     v.n_full = 2;
-    CHECK(fsdp_step_units_ex(&v, 1, &cfg, 1, NULL, NULL) == FSDP_ERR_INVALID_ARG);
-    CHECK(fsdp_step_units_ex(NULL, 0, &cfg, 1, NULL, NULL) == FSDP_OK);
-    CHECK(fsdp_step_units_ex(&v, 1, NULL, 1, NULL, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_step_units_ex(&v, 1, &cfg, 1, NULL, NULL, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_step_units_ex(NULL, 0, &cfg, 1, NULL, NULL, NULL) == FSDP_OK);
+    CHECK(fsdp_step_units_ex(&v, 1, NULL, 1, NULL, NULL, NULL) == FSDP_ERR_INVALID_ARG);
     /* the launch-count query: an empty model makes none; no output, or an
      * invalid unit, is refused */
     int64_t launches = -1;
@@ -101,13 +101,21 @@ int main(void) {
     CHECK(fsdp_step_units_ex_launches(&v, 1, &cfg, 1, &launches) == FSDP_ERR_INVALID_ARG);
     /* the captured step: no handle to fill, no graph to launch */
     fsdp_step_graph *graph = (fsdp_step_graph *)&u; /* overwritten with NULL on error */
-    CHECK(fsdp_step_graph_create(NULL, 1, 1, 0, NULL, &graph) == FSDP_ERR_INVALID_ARG && graph == NULL);
-    CHECK(fsdp_step_graph_create(&u, 1, 1, 0, NULL, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_step_graph_create(NULL, 1, 1, 0, NULL, NULL, &graph) == FSDP_ERR_INVALID_ARG && graph == NULL);
+    CHECK(fsdp_step_graph_create(&u, 1, 1, 0, NULL, NULL, NULL) == FSDP_ERR_INVALID_ARG);
     CHECK(fsdp_step_graph_launch(NULL, &hp, NULL) == FSDP_ERR_INVALID_ARG);
     CHECK(fsdp_step_graph_destroy(NULL) == FSDP_OK);
+    /* the validated plan: no handle to fill, no plan to launch */
+    fsdp_step_plan *plan = (fsdp_step_plan *)&u; /* overwritten with NULL on error */
+    CHECK(fsdp_step_plan_create(NULL, 1, 1, 0, NULL, NULL, &plan) == FSDP_ERR_INVALID_ARG && plan == NULL);
+    CHECK(fsdp_step_plan_create(&u, 1, 1, 0, NULL, NULL, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_step_plan_create_ex(&v, 1, &cfg, 1, NULL, NULL, &plan) == FSDP_ERR_INVALID_ARG && plan == NULL);
+    CHECK(fsdp_step_plan_launch(NULL, &hp, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_step_plan_launch_ex(NULL, &cfg, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_step_plan_destroy(NULL) == FSDP_OK);
     CHECK(fsdp_take_wait_timeouts(NULL) == FSDP_ERR_INVALID_ARG);
-    CHECK(fsdp_check_bounded_wait(0, NULL) == FSDP_ERR_INVALID_ARG);
-    CHECK(fsdp_check_bounded_wait(((int64_t)1 << 31) + 1, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_check_bounded_wait(0, NULL, NULL) == FSDP_ERR_INVALID_ARG);
+    CHECK(fsdp_check_bounded_wait(((int64_t)1 << 31) + 1, NULL, NULL) == FSDP_ERR_INVALID_ARG);
     CHECK(fsdp_last_cuda_error() == 0);
     printf("ok\n");
     return 0;

@@ -145,7 +145,7 @@ def test_rsa_rejects_invalid_arguments(lib):
 def test_all_gather_rejects_invalid_arguments(lib):
     from sharded_fsdp_reduce_gb300 import _lib as E
     arr = lambda *p: (ctypes.c_void_p * len(p))(*p)
-    ag = lambda src, dt, world, P, dsts, n: lib.fsdp_all_gather(src, dt, world, P, dsts, n, None)
+    ag = lambda src, dt, world, P, dsts, n, wt=None: lib.fsdp_all_gather(src, dt, world, P, dsts, n, wt, None)
     assert ag(FAKE, 9, 2, 16, arr(FAKE + 4096), 1) == E.FSDP_ERR_UNSUPPORTED_DTYPE
     assert ag(FAKE, 1, 0, 16, arr(FAKE + 4096), 1) == E.FSDP_ERR_INVALID_ARG
     assert ag(FAKE, 1, 2, 15, arr(FAKE + 4096), 1) == E.FSDP_ERR_INVALID_ARG
@@ -158,6 +158,7 @@ def test_all_gather_rejects_invalid_arguments(lib):
     assert ag(FAKE, 1, 2, 16, arr(FAKE + 4096, FAKE + 4100), 2) == E.FSDP_ERR_INVALID_ARG  # dsts overlap
     assert ag(FAKE, 1, 2, 16, arr(FAKE + 4096, None), 2) == E.FSDP_ERR_INVALID_ARG
     assert ag(FAKE, 1, 2, 0, arr(FAKE + 4096), 1) == E.FSDP_OK                   # empty: no-op
+    assert ag(FAKE, 1, 2, 16, arr(FAKE + 4096), 1, FAKE + 2) == E.FSDP_ERR_ALIGNMENT  # counter off 4 bytes
 
 
 def test_flatten_rejects_invalid_arguments(lib):
@@ -186,7 +187,8 @@ def test_take_wait_timeouts_rejects_null(lib):
 def test_check_bounded_wait_rejects_limits_out_of_range(lib):
     from sharded_fsdp_reduce_gb300 import _lib as E
     for limit in (0, -1, (1 << 31) + 1):
-        assert lib.fsdp_check_bounded_wait(limit, None) == E.FSDP_ERR_INVALID_ARG
+        assert lib.fsdp_check_bounded_wait(limit, None, None) == E.FSDP_ERR_INVALID_ARG
+    assert lib.fsdp_check_bounded_wait(1 << 20, FAKE + 1, None) == E.FSDP_ERR_ALIGNMENT
 
 
 def test_fused_gather_rejects_invalid_arguments(lib):
@@ -298,7 +300,7 @@ def test_step_units_validates_every_unit_before_launching(lib):
 
     def call(units, gathers=1, fuse=0, hpp=ctypes.byref(hp), n=None):
         arr = (E.FsdpUnit * max(len(units), 1))(*units)
-        return lib.fsdp_step_units(arr, len(units) if n is None else n, hpp, gathers, fuse, None, None)
+        return lib.fsdp_step_units(arr, len(units) if n is None else n, hpp, gathers, fuse, None, None, None)
 
     def unit(base, **kw):
         u, k = _unit(E, base, **kw)
@@ -307,8 +309,9 @@ def test_step_units_validates_every_unit_before_launching(lib):
 
     A, B = FAKE, FAKE + 0x100000000
     assert call([]) == E.FSDP_OK
-    assert lib.fsdp_step_units(None, 0, ctypes.byref(hp), 1, 0, None, None) == E.FSDP_OK
-    assert lib.fsdp_step_units(None, 1, ctypes.byref(hp), 1, 0, None, None) == E.FSDP_ERR_INVALID_ARG
+    assert lib.fsdp_step_units(None, 0, ctypes.byref(hp), 1, 0, None, None, None) == E.FSDP_OK
+    assert lib.fsdp_step_units(None, 1, ctypes.byref(hp), 1, 0, None, None, None) == E.FSDP_ERR_INVALID_ARG
+    assert lib.fsdp_step_units(None, 0, ctypes.byref(hp), 1, 0, None, FAKE + 2, None) == E.FSDP_ERR_ALIGNMENT
     assert call([unit(A)], hpp=None) == E.FSDP_ERR_INVALID_ARG
     assert call([unit(A)], gathers=-1) == E.FSDP_ERR_INVALID_ARG
     assert call([unit(A)], gathers=65) == E.FSDP_ERR_INVALID_ARG
@@ -358,7 +361,7 @@ def test_step_units_ex_validates_every_unit_before_launching(lib):
     def call(units, opt=0, gathers=1):
         cfg = E.FsdpStepConfig(opt, 0, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
         arr = (E.FsdpUnitEx * max(len(units), 1))(*units)
-        return lib.fsdp_step_units_ex(arr, len(units), ctypes.byref(cfg), gathers, None, None)
+        return lib.fsdp_step_units_ex(arr, len(units), ctypes.byref(cfg), gathers, None, None, None)
 
     A, B = FAKE, FAKE + 0x100000000
     assert call([]) == E.FSDP_OK
@@ -380,10 +383,10 @@ def test_step_units_ex_validates_every_unit_before_launching(lib):
 def test_step_graph_rejects_invalid_arguments_on_the_host(lib):
     from sharded_fsdp_reduce_gb300 import _lib as E
     out = ctypes.c_void_p(123)
-    assert lib.fsdp_step_graph_create(None, 0, 1, 0, None, None) == E.FSDP_ERR_INVALID_ARG     # no handle
-    assert lib.fsdp_step_graph_create(None, 1, 1, 0, None, ctypes.byref(out)) == E.FSDP_ERR_INVALID_ARG
-    assert out.value is None                                                                    # cleared
-    assert lib.fsdp_step_graph_create(None, 0, -1, 0, None, ctypes.byref(out)) == E.FSDP_ERR_INVALID_ARG
+    assert lib.fsdp_step_graph_create(None, 0, 1, 0, None, None, None) == E.FSDP_ERR_INVALID_ARG     # no handle
+    assert lib.fsdp_step_graph_create(None, 1, 1, 0, None, None, ctypes.byref(out)) == E.FSDP_ERR_INVALID_ARG
+    assert out.value is None                                                                          # cleared
+    assert lib.fsdp_step_graph_create(None, 0, -1, 0, None, None, ctypes.byref(out)) == E.FSDP_ERR_INVALID_ARG
     hp = E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
     assert lib.fsdp_step_graph_launch(None, ctypes.byref(hp), None) == E.FSDP_ERR_INVALID_ARG
     assert lib.fsdp_step_graph_destroy(None) == E.FSDP_OK
@@ -495,3 +498,84 @@ def test_step_units_launches_random_models(lib, seed):
     out = ctypes.c_int64(-1)
     assert lib.fsdp_step_units_launches(arr, len(specs), ctypes.byref(hp), gathers, 0, ctypes.byref(out)) == E.FSDP_OK
     assert out.value == _expected_launches(specs, gathers)
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host-only: fake addresses need a machine without a GPU")
+def test_a_unit_may_not_read_what_another_unit_writes(lib):
+    # units run at the same time (side streams, batched launches): a unit
+    # whose gradients lie in another unit's master, state, shard or gathered
+    # buffer would race, so the model is refused; gradients shared by two
+    # units (both only read them) are fine
+    from sharded_fsdp_reduce_gb300 import _lib as E
+    hp = E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+    out = ctypes.c_int64(-1)
+    small = (50000, 8, 8, False)
+
+    def count(arr, n, ex=False):
+        if ex:
+            cfg = E.FsdpStepConfig(0, 0, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+            return lib.fsdp_step_units_ex_launches(arr, n, ctypes.byref(cfg), 1, ctypes.byref(out))
+        return lib.fsdp_step_units_launches(arr, n, ctypes.byref(hp), 1, 0, ctypes.byref(out))
+
+    for ex in (False, True):
+        arr, keep = _fake_units(E, [small] * 3, ex=ex)
+        assert count(arr, 3, ex) == E.FSDP_OK and out.value == 2
+        g1 = ctypes.cast(arr[1].grads, ctypes.POINTER(ctypes.c_void_p))
+        written = (arr[0].param, arr[0].state0, arr[0].shard_out) if ex else \
+            (arr[0].master, arr[0].exp_avg, arr[0].shard_out)
+        fulls0 = ctypes.cast(arr[0].full_bufs, ctypes.POINTER(ctypes.c_void_p))
+        for target in (*written, fulls0[3], written[1] + 2 * 1000):  # starts inside, or at, a written range
+            saved = g1[5]
+            g1[5] = target
+            assert count(arr, 3, ex) == E.FSDP_ERR_INVALID_ARG, (ex, hex(target))
+            g1[5] = saved
+        # the range just before unit 0's master, ending where it starts: no overlap
+        g1[5] = written[0] - 2 * 50000
+        assert count(arr, 3, ex) == E.FSDP_OK
+        # unit 2 reads unit 1's gradients (read only): allowed
+        g2 = ctypes.cast(arr[2].grads, ctypes.POINTER(ctypes.c_void_p))
+        for q in range(8):
+            g2[q] = g1[q]
+        assert count(arr, 3, ex) == E.FSDP_OK and out.value == 2
+    assert lib.fsdp_last_cuda_error() == 0
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host-only: fake addresses need a machine without a GPU")
+def test_step_plan_validates_once_and_checks_only_the_scalars_per_launch(lib):
+    from sharded_fsdp_reduce_gb300 import _lib as E
+    small = (50000, 8, 8, False)
+    plan = ctypes.c_void_p(123)
+    # invalid models: refused at creation, the handle cleared
+    assert lib.fsdp_step_plan_create(None, 0, 1, 0, None, None, None) == E.FSDP_ERR_INVALID_ARG
+    assert lib.fsdp_step_plan_create(None, 1, 1, 0, None, None, ctypes.byref(plan)) == E.FSDP_ERR_INVALID_ARG
+    assert plan.value is None
+    arr, keep = _fake_units(E, [small, small])
+    arr[1].exp_avg = arr[0].master                                        # two units writing one buffer
+    assert lib.fsdp_step_plan_create(arr, 2, 1, 0, None, None, ctypes.byref(plan)) == E.FSDP_ERR_INVALID_ARG
+    assert plan.value is None
+    assert lib.fsdp_step_plan_create(arr, 1, 1, 0, None, FAKE + 2, ctypes.byref(plan)) == E.FSDP_ERR_ALIGNMENT
+    # a valid model: created without touching a device
+    arr, keep = _fake_units(E, [small] * 3)
+    assert lib.fsdp_step_plan_create(arr, 3, 1, 0, None, None, ctypes.byref(plan)) == E.FSDP_OK and plan.value
+    bad = [E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 0, 1.0),            # step 0
+           E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 0.0),            # grad_scale 0
+           E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, float("inf"))]
+    for hp in bad:
+        assert lib.fsdp_step_plan_launch(plan, ctypes.byref(hp), None) == E.FSDP_ERR_INVALID_ARG
+    assert lib.fsdp_step_plan_launch(plan, None, None) == E.FSDP_ERR_INVALID_ARG
+    cfg = E.FsdpStepConfig(0, 0, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+    assert lib.fsdp_step_plan_launch_ex(plan, ctypes.byref(cfg), None) == E.FSDP_ERR_INVALID_ARG  # not a variant plan
+    assert lib.fsdp_last_cuda_error() == 0                                   # nothing was launched
+    assert lib.fsdp_step_plan_destroy(plan) == E.FSDP_OK
+    assert lib.fsdp_step_plan_destroy(None) == E.FSDP_OK
+    # a variant plan: the launch's optimizer and reduction dtype are checked
+    arr, keep = _fake_units(E, [small] * 2, ex=True)
+    assert lib.fsdp_step_plan_create_ex(arr, 2, ctypes.byref(cfg), 1, None, None, ctypes.byref(plan)) == E.FSDP_OK
+    other = E.FsdpStepConfig(2, 0, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)      # Adamax
+    assert lib.fsdp_step_plan_launch_ex(plan, ctypes.byref(other), None) == E.FSDP_ERR_INVALID_ARG
+    f16 = E.FsdpStepConfig(0, 2, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)        # fp16 sum of bf16 gradients
+    assert lib.fsdp_step_plan_launch_ex(plan, ctypes.byref(f16), None) == E.FSDP_ERR_UNSUPPORTED_DTYPE
+    hp = E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+    assert lib.fsdp_step_plan_launch(plan, ctypes.byref(hp), None) == E.FSDP_ERR_INVALID_ARG  # not an AdamW plan
+    assert lib.fsdp_last_cuda_error() == 0
+    assert lib.fsdp_step_plan_destroy(plan) == E.FSDP_OK

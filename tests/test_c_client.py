@@ -60,7 +60,7 @@ def test_c_client_runs_the_step_on_the_gpu(tmp_path, orc):
     raw = out.read_bytes()
     f32 = np.frombuffer(raw, np.float32, 3 * PPAD).reshape(3, PPAD)
     b16 = np.frombuffer(raw, np.uint16, 3 * PPAD, offset=12 * PPAD).reshape(3, PPAD)
-    nf = int(np.frombuffer(raw, np.uint32, 1, offset=18 * PPAD)[0])
+    nf, wt = (int(x) for x in np.frombuffer(raw, np.uint32, 2, offset=18 * PPAD))
     # the same inputs, rebuilt here, through the oracle
     j = np.arange(PPAD)
     p = np.where(j < P, ((j * 5) % 201 - 100) / np.float32(2048.0), 0).astype(np.float32)
@@ -81,3 +81,4 @@ def test_c_client_runs_the_step_on_the_gpu(tmp_path, orc):
     np.testing.assert_array_equal(b16[1], full)
     np.testing.assert_array_equal(b16[2], full)
     assert nf == 0
+    assert wt == 0  # no bounded wait of the gathers gave up

@@ -376,15 +376,32 @@ def test_a_bounded_wait_that_runs_out_is_counted_and_the_context_stays_usable(F)
     # cycles (about half a millisecond), is counted, and the kernel returns
     assert F.fsdp_take_wait_timeouts() == 0
     s = torch.cuda.Stream()
-    F.fsdp_check_bounded_wait(1 << 20)
-    F.fsdp_check_bounded_wait(1 << 20, stream=s)
+    # each call's own counter, read in its stream's order: a copy to pinned
+    # host memory and a wait on that one stream, no device-wide synchronize
+    wt, wt_s = (torch.zeros(1, dtype=torch.int32, device=DEV) for _ in range(2))
+    got, got_s = (torch.full((1,), -1, dtype=torch.int32, pin_memory=True) for _ in range(2))
+    cur = torch.cuda.current_stream()
+    F.fsdp_check_bounded_wait(1 << 20, wait_timeouts=wt)
+    got.copy_(wt, non_blocking=True)
+    s.wait_stream(cur)  # wt_s was zeroed on the current stream
+    F.fsdp_check_bounded_wait(1 << 20, stream=s, wait_timeouts=wt_s)
+    with torch.cuda.stream(s):
+        got_s.copy_(wt_s, non_blocking=True)
+    cur.synchronize()
+    assert int(got.item()) == 1
+    s.synchronize()
+    assert int(got_s.item()) == 1
+    # and on the device, over both calls
     assert F.fsdp_take_wait_timeouts() == 2
     assert F.fsdp_take_wait_timeouts() == 0  # the read resets the count
     assert F.fsdp_last_cuda_error() == 0
-    # the context still works: a bulk-copy gather right after
+    # the context still works: a bulk-copy gather right after, with its own
+    # counter at 0
     src = (torch.arange(1 << 20, device=DEV) % 251).to(torch.bfloat16)
     fulls = [torch.zeros_like(src) for _ in range(3)]
-    F.fsdp_all_gather(src, fulls, 1)
+    wt.zero_()
+    F.fsdp_all_gather(src, fulls, 1, wait_timeouts=wt)
+    assert int(wt.item()) == 0
     torch.cuda.synchronize()
     assert all(torch.equal(f, src) for f in fulls)
     assert F.fsdp_take_wait_timeouts() == 0
