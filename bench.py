@@ -15,16 +15,21 @@ flushed before every timed step, outside that step's CUDA events.
 
 Printed (rank 0, one JSON line): value = algorithmic bytes of the step / step
 time (GB/s, whole job over all ranks); roofline of the fused kernel (its own
-CUDA-event time inside the timed region); e2e through the Python binding with
-pinned host buffers; the CPU oracle timed on the host cores; clocks sampled
-during the timed region. Beside them, on the same unit: the fused-gather and
-no-reshard steps (`variants`), the variant optimizers' kernels
+CUDA-event time inside the timed region; mean and median); e2e with the
+gradients in pinned host memory, the faster of the binding's copy pipeline
+and the C ABI call reading the host buffers in place (the other beside it);
+the CPU oracle timed on the host cores; clocks sampled during the timed
+region. Beside them, on the same unit: the fused-gather and no-reshard steps
+on their own byte models (`variants`), the variant optimizers' kernels
 (`variant_kernels`), the fused kernel with its state in pinned host memory
-(`offload_state_on_host`), and the per-unit driver on a 12-unit GPT-2 small
-model (`driver_gpt2_small_model_12_units`) and on a model of 200 units of
-50,000 parameters (`driver_model_200_units_of_50k`, batched launches; these
-three on one GPU only); --no-variants, --no-offload and --no-driver skip
-them.
+(`offload_state_on_host`), the per-unit driver on a 12-unit GPT-2 small model
+(`driver_gpt2_small_model_12_units`) and on a model of 200 units of 50,000
+parameters (`driver_model_200_units_of_50k`, batched launches: a model
+validated once, validated every call, and captured); then, with that unit
+freed, the fused kernel alone on the GPT-3 13B, GPT-2 Large and GPT-2 small
+block units (`per_config`, each with its own clocks). The last four run on
+one GPU only; --no-variants, --no-offload, --no-driver and --no-per-config
+skip them.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
@@ -122,25 +127,65 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """Per-launch DRAM traffic of the fused kernel from a committed ncu summary,
-    or None when there is none for this workload or the kernel changed since."""
-    path = os.path.join(ROOT, "profiles", f"rsa_{workload}_ncu.md")
-    if not os.path.exists(path):
-        return None
+# The committed ncu summary that holds each workload's fused-kernel DRAM
+# traffic. The 13B unit runs the same kernel build as the 70B unit (N = 8,
+# bf16 gradients and output), so both take the small-case captures of that
+# build; the GPT-2 units are small enough to be captured whole.
+TRAFFIC_SUMMARY = {
+    "llama70b_block_unit_n8": "rsa_n8_bf16_numel33m_67m_ncu.md",
+    "gpt3_13b_block_unit_n8": "rsa_n8_bf16_numel33m_67m_ncu.md",
+    "gpt2_large_block_unit_n2_fp16": "rsa_gpt2_large_block_unit_n2_fp16_ncu.md",
+    "gpt2_small_block_unit_n8": "rsa_gpt2_small_block_unit_n8_ncu.md",
+}
+
+
+def read_summary(path: str) -> dict:
+    """The `- key: value` lines of an ncu summary."""
     vals = {}
     with open(path) as f:
         for line in f:
-            line = line.strip().lstrip("-").strip()  # markdown list items
-            if ":" in line and line.startswith(("traffic_bytes_per_launch", "kernel_source_sha256")):
+            line = line.strip()
+            if not line.startswith("- "):
+                continue
+            line = line[2:]
+            if ":" in line:
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip().strip("`")
+    return vals
+
+
+def recorded_traffic(workload: str, padded_numel: int):
+    """Per-launch DRAM traffic (read + write bytes) of the fused kernel on a
+    unit of padded_numel elements, from a committed ncu summary; None when
+    there is none for this workload or the kernel changed since.
+
+    A summary gives either the traffic of the whole unit (`captured_numel`:
+    one size, equal to padded_numel) or captures of two smaller cases of the
+    same kernel build (`captured_numel: n1, n2`, `traffic_bytes: T1, T2`).
+    Traffic is then per-element bytes plus a fixed part (the stores still
+    dirty in L2 when the kernel ends, which the next kernel writes back), so
+    the two points give both and the full launch is read off the same line:
+    T2 + (T2 - T1) / (n2 - n1) * (padded_numel - n2)."""
+    name = TRAFFIC_SUMMARY.get(workload.split("_numel")[0])
+    if name is None:
+        return None
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    vals = read_summary(path)
     if vals.get("kernel_source_sha256") != kernel_source_hash():
         return None
     try:
-        return float(vals["traffic_bytes_per_launch"])
+        ns = [int(x) for x in vals["captured_numel"].split(",")]
+        ts = [float(x) for x in vals["traffic_bytes"].split(",")]
     except (KeyError, ValueError):
         return None
+    if len(ns) == 1 and len(ts) == 1:
+        return ts[0] if ns[0] == padded_numel else None
+    if len(ns) != 2 or len(ts) != 2 or ns[1] <= ns[0]:
+        return None
+    slope = (ts[1] - ts[0]) / (ns[1] - ns[0])
+    return round(ts[1] + slope * (padded_numel - ns[1]))
 
 
 class ClockSampler:
@@ -255,6 +300,33 @@ def timed_calls(fn, K: int, stream, flush: L2Flush) -> float:
     return sum(a.elapsed_time(b) for a, b in evs) / K
 
 
+def timed_launches(fn, K: int, stream, flush: L2Flush):
+    """Device time of each of K calls of fn(i) (ms): back to back with an
+    event between consecutive calls, or, with the flush active, a pair of
+    events around each call (the flush outside them)."""
+    import torch
+
+    torch.cuda.synchronize()
+    if not flush.active:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+        ev[0].record(stream)
+        for i in range(K):
+            fn(i)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        return [ev[i].elapsed_time(ev[i + 1]) for i in range(K)]
+    pairs = []
+    for i in range(K):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn(i)
+        b.record(stream)
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in pairs]
+
+
 GROUP_MAX_UNITS = 128          # the library's batched launches: units per launch
 GROUP_MAX_NUMEL = 1 << 24      # and the largest unit they take
 
@@ -273,9 +345,10 @@ def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20, numel
     """Host enqueue time and device time per model step of n_units GPT-2 small
     block units (or, with numel, n_units one-tensor units of numel elements
     with the same N, dtypes and hyperparameters; one gather each), stepped by
-    a Python loop over the units, by one native fsdp_step_units call, and by
-    one launch of the step captured as a CUDA graph. Returns (result, timed
-    launches)."""
+    a Python loop over the units, by the native step of a model validated
+    once (UnitSequence.step: a StepPlan launch), by one fsdp_step_units call
+    that validates every unit each time, and by one launch of the step
+    captured as a CUDA graph. Returns (result, timed launches)."""
     import torch
 
     cfg = fi.CONFIGS["gpt2_small"]
@@ -303,13 +376,17 @@ def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20, numel
     def native():
         seq.step(hp(), gathers=cfg.gathers)
 
+    def native_unplanned():
+        seq.step_unplanned(hp(), gathers=cfg.gathers)
+
     graph = seq.capture(gathers=cfg.gathers)
 
     def captured():
         graph.launch(hp())
 
     out = {}
-    for name, fn in (("python_loop", python_loop), ("native", native), ("cuda_graph", captured)):
+    for name, fn in (("python_loop", python_loop), ("native", native), ("native_unplanned", native_unplanned),
+                     ("cuda_graph", captured)):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
@@ -325,15 +402,18 @@ def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20, numel
                      "device_ms_per_step": round(a.elapsed_time(b) / steps, 4)}
     rsa_b, ag_b = seq.step_bytes(cfg.gathers)
     out["bytes_per_step"] = rsa_b + ag_b
-    out["native_GBs"] = round((rsa_b + ag_b) / (out["native"]["device_ms_per_step"] * 1e-3) / 1e9, 1)
-    out["cuda_graph_GBs"] = round((rsa_b + ag_b) / (out["cuda_graph"]["device_ms_per_step"] * 1e-3) / 1e9, 1)
+    for name in ("native", "native_unplanned", "cuda_graph"):
+        out[name + "_GBs"] = round((rsa_b + ag_b) / (out[name]["device_ms_per_step"] * 1e-3) / 1e9, 1)
+    out["native_over_cuda_graph"] = round(out["native"]["device_ms_per_step"]
+                                          / out["cuda_graph"]["device_ms_per_step"], 3)
     per_unit = n_units * (1 + cfg.gathers)
     batched = model_launches(n_units, units[0].padded_numel, cfg.gathers)
-    out["launches_per_step"] = {"python_loop": per_unit, "native": batched, "cuda_graph": batched}
+    out["launches_per_step"] = {"python_loop": per_unit, "native": batched, "native_unplanned": batched,
+                                "cuda_graph": batched}
     graph.close()
     del seq, units, graph
     torch.cuda.empty_cache()
-    return out, steps * (per_unit + 2 * batched)
+    return out, steps * (per_unit + 3 * batched)
 
 
 def max_over_ranks(values, device):
@@ -451,6 +531,7 @@ class _Run:
         self.flush = L2Flush(dev, self.rsa_b)
         self.t = 0
         self.launches = 0
+        self.rsa_ms_median = None
 
     def hp(self, t):
         c = self.cfg
@@ -497,22 +578,34 @@ def time_steps(run: _Run):
         step_ms = sum(a.elapsed_time(c) for a, _, c in ev) / K
     else:
         step_ms = start.elapsed_time(end) / K
-    rsa_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / K
+    rsa_each = [a.elapsed_time(b) for a, b, _ in ev]
+    run.rsa_ms_median = statistics.median(rsa_each)
+    rsa_ms = sum(rsa_each) / K
     run.launches += K * (1 + cfg.gathers)
     return step_ms, rsa_ms, clocks.summary()
 
 
 def time_e2e(run: _Run):
-    """End to end through the binding's host-buffer step: every step copies
-    its N gradient buffers in from pinned host memory and reads the step's
-    result back, its non-finite-gradient count (the metric a trainer checks
-    every step; the gathered parameters stay on the GPU for the next
-    forward), or with --e2e-read-params the compute-dtype parameters.
-    Consecutive steps overlap their copies and kernels. Every rank runs it or
-    none does. Returns (ms per step, steps, h2d bytes, d2h bytes, reason it
-    is unavailable or None, ms of a bare copy of the gradients to the device
-    or None)."""
-    torch, unit, cfg, args, dev = run.torch, run.unit, run.cfg, run.args, run.dev
+    """End to end with the N gradient buffers in pinned host memory: every
+    step brings its gradients from the host and reads the step's result
+    back, its non-finite-gradient count (the metric a trainer checks every
+    step; the gathered parameters stay on the GPU for the next forward), or
+    with --e2e-read-params the compute-dtype parameters. Two forms, timed one
+    after the other on the same host buffers:
+
+    * copy_pipeline -- the binding's host-buffer step
+      (FlatParamUnit.step_from_host): copies to device buffers on a copy
+      stream, double-buffered so that a step's copies overlap the previous
+      step's kernels;
+    * zero_copy -- the C ABI call given the host buffers themselves (its
+      gradients are "device or mapped host"): the fused kernel reads them
+      over the host link, then the gathers run; no staging buffers.
+
+    Every rank runs it or none does. Returns a dict: per form its ms per
+    step, the steps timed, the bytes each way, and the ms of a bare copy of
+    the gradients to the device (the host link's own bound); or
+    {"unavailable": reason}."""
+    torch, F, unit, cfg, args, dev = run.torch, run.F, run.unit, run.cfg, run.args, run.dev
     Ke = max(3, min(args.e2e_steps, run.K))
     unavailable = None
     try:  # N gradient buffers of pinned host memory (13.7 GB for the 70B unit)
@@ -522,7 +615,7 @@ def time_e2e(run: _Run):
     if run.world_size > 1 and not all_ranks_agree(host_grads is not None, dev) and host_grads is not None:
         host_grads, unavailable = None, "another rank could not pin its host buffers"
     if host_grads is None:
-        return 0.0, Ke, 0, 0, unavailable, None
+        return {"unavailable": unavailable}
     for r in range(run.N):
         host_grads[r].copy_(unit.grads[r])
     counter = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -533,22 +626,42 @@ def time_e2e(run: _Run):
         host_out, host_nf = None, torch.zeros(1, dtype=torch.int32, pin_memory=True)
         d2h = host_nf.numel() * host_nf.element_size()
     h2d = sum(g.numel() * g.element_size() for g in host_grads)
-    unit.step_from_host(host_grads, host_out, run.next_hp(), gathers=cfg.gathers, nonfinite_count=counter,
-                        host_nonfinite=host_nf)  # sets up the streams
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    run.barrier()
-    e0.record(run.stream)
-    for _ in range(Ke):
+
+    def pipeline_step():
         unit.step_from_host(host_grads, host_out, run.next_hp(), gathers=cfg.gathers, nonfinite_count=counter,
                             host_nonfinite=host_nf)
-    e1.record(run.stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / Ke
-    if host_nf is not None and int(host_nf.item()) != 0:
-        raise RuntimeError("e2e steps reported non-finite gradients")
-    run.launches += Ke * (1 + cfg.gathers)
-    # the host link's own bound, after the timed region: the bare copy of the
+
+    def zero_copy_step():
+        # the result is read back right after the update, so that it travels
+        # while the gathers run
+        hp = run.next_hp()
+        if host_nf is not None:
+            counter.zero_()
+        F.fsdp_reduce_scatter_adam_cast(host_grads, unit.master, unit.exp_avg, unit.exp_avg_sq, unit.shard_out,
+                                        hp, nonfinite_count=counter)
+        if host_nf is not None:
+            host_nf.copy_(counter, non_blocking=True)
+        else:
+            host_out.copy_(unit.shard_out, non_blocking=True)
+        for _ in range(cfg.gathers):
+            unit.all_gather()
+
+    out = {"steps": Ke, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    for name, fn in (("copy_pipeline", pipeline_step), ("zero_copy", zero_copy_step)):
+        fn()  # sets up the streams, warms the host mappings
+        torch.cuda.synchronize()
+        run.barrier()
+        e0.record(run.stream)
+        for _ in range(Ke):
+            fn()
+        e1.record(run.stream)
+        torch.cuda.synchronize()
+        out[name + "_ms"] = e0.elapsed_time(e1) / Ke
+        if host_nf is not None and int(host_nf.item()) != 0:
+            raise RuntimeError("e2e steps reported non-finite gradients")
+        run.launches += Ke * (1 + cfg.gathers)
+    # the host link's own bound, after the timed regions: the bare copy of the
     # same pinned gradients into the unit's gradient buffers (identical bytes)
     bare = []
     for _ in range(2):
@@ -559,24 +672,46 @@ def time_e2e(run: _Run):
         e1.record(run.stream)
         torch.cuda.synchronize()
         bare.append(e0.elapsed_time(e1))
-    return e2e_ms, Ke, h2d, d2h, None, sum(bare) / len(bare)
+    out["bare_h2d_ms"] = sum(bare) / len(bare)
+    return out
 
 
 def time_fused_gather_variants(run: _Run):
-    """The same step with the first all-gather fused into the update kernel,
-    and the no-reshard mode (one gather, fused, kept for forward and
-    backward); both on the default step's byte model."""
-    unit, K = run.unit, run.K
+    """Two forms of the step with the gather fused into the update kernel,
+    each on its own algorithmic bytes:
+
+    * fused_gather -- the first gather written by the update kernel (the
+      shard and every gathered buffer stored from registers, shard_out not
+      read back), the second a separate gather: N*grad + 24 + (1 + n_full)*out
+      bytes per element, plus (gathers - 1) * (1 + n_full) * out;
+    * no_reshard_fused -- one fused gather kept for forward and backward,
+      and no compute-dtype shard written (shard_out NULL: the gathered
+      parameters are what is kept): N*grad + 24 + n_full*out."""
+    F, unit, K, P, N = run.F, run.unit, run.K, run.P_pad, run.N
+    gs, os_, nfull = unit.grads[0].element_size(), unit.shard_out.element_size(), len(unit.full)
+    update = P * (N * gs + 3 * (4 + 4))
+    g = run.cfg.gathers
+
+    def fused(t):
+        unit.step(run.hp(t), gathers=g, fuse_gather=True)
+
+    def no_reshard(t):
+        F.fsdp_reduce_scatter_adam_cast_gather(unit.grads, unit.master, unit.exp_avg, unit.exp_avg_sq, None,
+                                               unit.full, run.hp(t))
+
+    forms = (("fused_gather", fused, g, update + P * os_ * (1 + nfull) * g),
+             ("no_reshard_fused", no_reshard, 1, update + P * os_ * nfull))
     variants = {}
-    for vname, vg in (("fused_gather", run.cfg.gathers), ("no_reshard_fused", 1)):
+    for vname, fn, launches, nbytes in forms:
         for _ in range(3):
-            unit.step(run.next_hp(), gathers=vg, fuse_gather=True)
+            run.t += 1
+            fn(run.t)
         t0 = run.t
-        vms = timed_calls(lambda i, vg=vg: unit.step(run.hp(t0 + 1 + i), gathers=vg, fuse_gather=True),
-                          K, run.stream, run.flush)
+        vms = timed_calls(lambda i, fn=fn: fn(t0 + 1 + i), K, run.stream, run.flush)
         run.t += K
-        run.launches += K * vg
-        variants[vname] = {"gathers_per_step": vg, "ms_per_step": round(vms, 4)}
+        run.launches += K * launches
+        variants[vname] = {"gathers_per_step": 1 if vname == "no_reshard_fused" else g,
+                           "launches_per_step": launches, "ms_per_step": round(vms, 4), "bytes_per_step": nbytes}
     return variants
 
 
@@ -647,6 +782,82 @@ def time_offload(run: _Run, rsa_ms: float):
             "slowdown_vs_device_state": round(oms / rsa_ms, 2)}
 
 
+PER_CONFIG = ("gpt3_13b", "gpt2_large", "gpt2_small")
+PER_CONFIG_MAX_LAUNCHES = 5000
+
+
+def time_per_config(run: _Run, peak: float):
+    """The fused kernel alone on each other block unit of the set (GPT-3
+    13B, GPT-2 Large, GPT-2 small), built one at a time after the run's own
+    unit is freed: CUDA events around every launch (L2 flushed before each
+    launch of a unit that moves less than 16x L2), enough launches for about
+    --per-config-seconds of device time (at least --steps), so that the
+    clocks are sampled under load. Returns {workload: record}."""
+    torch, F, fi, dev, stream = run.torch, run.F, run.fi, run.dev, run.stream
+    out = {}
+    for name in PER_CONFIG:
+        if name == run.cfg.name:
+            continue
+        cfg = fi.CONFIGS[name]
+        workload = WORKLOAD_NAMES[name]
+        unit = F.FlatParamUnit(cfg.params, cfg.world, fi.torch_dtype(cfg.grad_dtype), fi.torch_dtype(cfg.out_dtype),
+                               device=dev)
+        unit.load_master([fi.gen_master(cfg, device=dev)])
+        for r in range(cfg.world):
+            unit.load_grad(r, [fi.gen_grad(cfg, r, 1, device=dev)])
+        P = unit.padded_numel
+        rsa_b, _ = unit.step_bytes(cfg.gathers)
+        flush = L2Flush(dev, rsa_b)
+
+        def launch(t, unit=unit, cfg=cfg):
+            unit.reduce_scatter_adam_cast(F.AdamWHParams(cfg.lr, cfg.beta1, cfg.beta2, cfg.eps, cfg.weight_decay,
+                                                         t, cfg.grad_scale))
+
+        warm = timed_launches(lambda i: launch(i + 1), 3, stream, flush)
+        want = int(run.args.per_config_seconds * 1e3 / max(min(warm), 1e-3)) + 1
+        K = min(PER_CONFIG_MAX_LAUNCHES, max(run.K, want))
+        torch.cuda.synchronize()
+        with ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clocks:
+            time.sleep(0.25)  # let the sampler start before the timed launches
+            each = timed_launches(lambda i: launch(4 + i), K, stream, flush)
+        run.launches += 3 + K
+        mean = sum(each) / K
+        achieved = rsa_b / (mean * 1e-3) / 1e9
+        out[workload] = {
+            "padded_numel": P, "world": cfg.world, "grad_dtype": cfg.grad_dtype, "out_dtype": cfg.out_dtype,
+            "launches": K, "ms": round(mean, 5), "ms_median": round(statistics.median(each), 5),
+            "bytes_per_launch": rsa_b, "achieved_GBs": round(achieved, 1),
+            "frac": round(achieved / peak, 4), "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+            "traffic": recorded_traffic(workload, P), "l2": flush.describe(), "clocks": clocks.summary(),
+        }
+        del unit, flush
+        torch.cuda.empty_cache()
+    return out
+
+
+def e2e_record(e2e: dict, total_bytes: int, args) -> dict:
+    """The bench line's e2e: the faster of the two host-buffer forms, the
+    other beside it, each with its share of the bare host-to-device copy."""
+    if "unavailable" in e2e:
+        return {"unavailable": e2e["unavailable"]}
+    forms = ("copy_pipeline", "zero_copy")
+    best = min(forms, key=lambda k: e2e[k + "_ms"])
+    other = forms[1 - forms.index(best)]
+    bare = e2e["bare_h2d_ms"]
+
+    def form(k):
+        ms = e2e[k + "_ms"]
+        return {"value": round(total_bytes / (ms * 1e-3) / 1e9, 2), "ms_per_step": round(ms, 3),
+                "bare_h2d_over_e2e": round(bare / ms, 4)}
+
+    rec = {"unit": "GB/s", **form(best), "path": best, "steps": e2e["steps"],
+           "h2d_bytes_per_step": e2e["h2d_bytes_per_step"], "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+           "d2h": "compute-dtype parameters" if args.e2e_read_params else "non-finite gradient count",
+           "bare_h2d_ms": round(bare, 3), "bare_h2d_GBs": round(e2e["h2d_bytes_per_step"] / (bare * 1e-3) / 1e9, 1)}
+    rec[other] = form(other)
+    return rec
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -669,7 +880,7 @@ def run_ours(args):
 
     run = _Run(args, dev, rank, world_size)
     step_ms, rsa_ms, clocks = time_steps(run)
-    e2e_ms, Ke, h2d, d2h, e2e_unavailable, bare_h2d_ms = time_e2e(run)
+    e2e = time_e2e(run)
     variants = time_fused_gather_variants(run) if not args.no_variants else {}
     kernels = time_variant_kernels(run) if not args.no_variants else {}
     offload = None
@@ -683,7 +894,10 @@ def run_ours(args):
         run.launches += n_launch
 
     if world_size > 1:
-        step_ms, rsa_ms, e2e_ms = max_over_ranks([step_ms, rsa_ms, e2e_ms], dev)
+        step_ms, rsa_ms = max_over_ranks([step_ms, rsa_ms], dev)
+        if "unavailable" not in e2e:
+            e2e["copy_pipeline_ms"], e2e["zero_copy_ms"] = max_over_ranks(
+                [e2e["copy_pipeline_ms"], e2e["zero_copy_ms"]], dev)
         for v in variants.values():
             v["ms_per_step"] = max_over_ranks([v["ms_per_step"]], dev)[0]
 
@@ -694,17 +908,23 @@ def run_ours(args):
         return
 
     unit, cfg, N, P_pad, rsa_b, ag_b = run.unit, run.cfg, run.N, run.P_pad, run.rsa_b, run.ag_b
-    workload, flush, K, launches = run.workload, run.flush, run.K, run.launches
+    workload, flush = run.workload, run.flush
     peak, peak_kind = measured_peak()
     achieved = rsa_b / (rsa_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(workload)
+    traffic = recorded_traffic(workload, P_pad)
     total_bytes = (rsa_b + ag_b) * world_size
+    unit_numel = unit.numel
+    per_config = None
+    if world_size == 1 and not args.no_per_config:
+        run.unit = unit = None  # the other block units are built after this one is freed
+        torch.cuda.empty_cache()
+        per_config = time_per_config(run, peak)
     result = {
         "metric": METRIC,
         "value": round(total_bytes / (step_ms * 1e-3) / 1e9, 2),
         "unit": "GB/s",
         "n_gpus": world_size,
-        "steps": K,
+        "steps": run.K,
         "warmup": args.warmup,
         "ms_per_step": round(step_ms, 4),
         "higher_is_better": True,
@@ -713,7 +933,7 @@ def run_ours(args):
         "dtype": "f32",
         "data": "synthetic (seeded; no dataset or weights)",
         "config": {
-            "workload": workload, "params": unit.numel, "padded_numel": P_pad, "world": N,
+            "workload": workload, "params": unit_numel, "padded_numel": P_pad, "world": N,
             "grad_dtype": cfg.grad_dtype, "out_dtype": cfg.out_dtype, "gathers_per_step": cfg.gathers,
             "bytes_per_step": rsa_b + ag_b, "fused_bytes_per_launch": rsa_b,
             "l2": flush.describe(),
@@ -725,30 +945,23 @@ def run_ours(args):
             "bound": "hbm", "kernel": "rsa_kernel (fused reduce-scatter + AdamW + cast)",
             "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
-            "fused_ms": round(rsa_ms, 4),
+            "fused_ms": round(rsa_ms, 4), "fused_ms_median": round(run.rsa_ms_median, 4),
             "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
         },
-        "e2e": {"unavailable": e2e_unavailable} if e2e_unavailable else {
-                "value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 3), "steps": Ke,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "d2h": "compute-dtype parameters" if args.e2e_read_params else "non-finite gradient count",
-                "bare_h2d_ms": round(bare_h2d_ms, 3), "bare_h2d_GBs": round(h2d / (bare_h2d_ms * 1e-3) / 1e9, 1),
-                "bare_h2d_over_e2e": round(bare_h2d_ms / e2e_ms, 4)},
-        "gpu_launches": launches,
-        "variants": {k: dict(v, value=round(world_size * (rsa_b + P_pad * unit.shard_out.element_size()
-                                                           * (1 + len(unit.full)) * v["gathers_per_step"])
-                                            / (v["ms_per_step"] * 1e-3) / 1e9, 2))
+        "e2e": e2e_record(e2e, total_bytes, args),
+        "gpu_launches": run.launches,
+        "variants": {k: dict(v, value=round(world_size * v["bytes_per_step"] / (v["ms_per_step"] * 1e-3) / 1e9, 2),
+                             frac=round(v["bytes_per_step"] / (v["ms_per_step"] * 1e-3) / 1e9 / peak, 4))
                      for k, v in variants.items()},
-        "variant_kernels": {k: dict(v, frac=round(v["achieved_GBs"] / measured_peak()[0], 4))
-                            for k, v in kernels.items()},
+        "variant_kernels": {k: dict(v, frac=round(v["achieved_GBs"] / peak, 4)) for k, v in kernels.items()},
         "offload_state_on_host": offload,
         "driver_gpt2_small_model_12_units": driver,
         "driver_model_200_units_of_50k": small_units,
+        "per_config": per_config,
         "clocks": clocks,
     }
     if world_size == 1 and not args.no_cpu_baseline:
-        n_s = min(unit.numel, args.cpu_sample)
+        n_s = min(unit_numel, args.cpu_sample)
         gbs, el, done, threads = oracle_sample_run(cfg, n_s, 1, 1, args.cpu_seconds)
         result["cpu_baseline"] = {
             "value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
@@ -804,6 +1017,10 @@ def main(argv=None):
                     help="skip the per-unit driver timing on a 12-unit GPT-2 small model")
     ap.add_argument("--no-offload", action="store_true",
                     help="skip the offload-mode timing (state in pinned host memory)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the fused kernel's timing on the other block units (13B, GPT-2 Large, GPT-2 small)")
+    ap.add_argument("--per-config-seconds", type=float, default=0.6,
+                    help="device time of each of those units' timed launches (clocks are sampled meanwhile)")
     ap.add_argument("--cpu-sample", type=int, default=1 << 24, help="elements in the CPU-baseline sample")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline time budget")
     ap.add_argument("--ref-sample", type=int, default=1 << 22, help="elements per reference-arm step")

@@ -71,8 +71,34 @@ def test_reference_arm_prints_on_rank0_only(tmp_path):
 def test_recorded_traffic_matches_current_kernel_source():
     # the committed ncu summary of the fused kernel carries the hash of the
     # kernel sources it was measured on; bench.py reports its traffic only
-    # while that hash matches
+    # while that hash matches. The 70B and 13B units take it from two small
+    # captures of the same kernel build, read off the line through them;
+    # it must stay within 1 % of the algorithmic 42 B per element
     import bench
-    t = bench.recorded_traffic("llama70b_block_unit_n8")
-    assert t is not None, "profiles/ summary missing or taken on another version of the kernel"
-    assert 0.99 * 42 * 855654400 <= t <= 1.01 * 42 * 855654400
+    for workload, P in (("llama70b_block_unit_n8", 855654400), ("gpt3_13b_block_unit_n8", 314639360)):
+        t = bench.recorded_traffic(workload, P)
+        assert t is not None, "profiles/ summary missing or taken on another version of the kernel"
+        assert 0.99 * 42 * P <= t <= 1.01 * 42 * P, (workload, t / (42 * P))
+    # the --numel cases of the 70B workload take the same line; another size
+    # of a one-point summary does not
+    assert bench.recorded_traffic("llama70b_block_unit_n8_numel67108864", 67108864) == 2766466816
+
+
+def test_recorded_traffic_line_through_two_captures(tmp_path, monkeypatch):
+    # the line through two captures, and the refusals: a changed kernel, a
+    # one-point summary asked for another size, an unknown workload
+    import bench
+    (tmp_path / "profiles").mkdir()
+    f = tmp_path / "profiles" / "rsa_n8_bf16_numel33m_67m_ncu.md"
+    h = bench.kernel_source_hash()
+    f.write_text(f"- captured_numel: 100, 200\n- traffic_bytes: 1000, 1900\n- kernel_source_sha256: `{h}`\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: h)
+    assert bench.recorded_traffic("llama70b_block_unit_n8", 1200) == 1900 + 9 * 1000
+    f.write_text("- captured_numel: 100, 200\n- traffic_bytes: 1000, 1900\n- kernel_source_sha256: `0`\n")
+    assert bench.recorded_traffic("llama70b_block_unit_n8", 1200) is None
+    g = tmp_path / "profiles" / "rsa_gpt2_small_block_unit_n8_ncu.md"
+    g.write_text(f"- captured_numel: 7087872\n- traffic_bytes: 297000000\n- kernel_source_sha256: `{h}`\n")
+    assert bench.recorded_traffic("gpt2_small_block_unit_n8", 7087872) == 297000000
+    assert bench.recorded_traffic("gpt2_small_block_unit_n8", 50000) is None
+    assert bench.recorded_traffic("tiny_unit_4099_n2", 4100) is None
