@@ -349,8 +349,11 @@ class UnitDescs:
     (gathered buffers), master (the parameter), exp_avg and exp_avg_sq (the
     optimizer states; exp_avg_sq None for SGD), shard_out (for fp32 state;
     the parameter itself for bf16/fp16 state). The descriptors hold the
-    buffers' addresses: build new ones if a unit's buffers are replaced. The
-    units are kept alive while the descriptors exist."""
+    buffers' addresses: build new ones if a unit's buffers are replaced.
+    The units and the very tensors whose addresses are held are kept alive
+    while the descriptors exist, so that a buffer replaced in a unit is not
+    freed and its memory handed to another allocation while a plan or a
+    captured step made from these descriptors still writes to it."""
 
     def __init__(self, units: Sequence):
         self.units = list(units)
@@ -377,7 +380,8 @@ class UnitDescs:
                     raise ValueError(f"{pre}full[{i}] must hold {P} elements of {odt}")
             grads = _ptrs(u.grads, pre + "grads", host_ok=True)
             full = _ptrs(u.full, pre + "full") if u.full else None
-            self._keep += [grads, full]
+            self._keep += [grads, full, list(u.grads), list(u.full), u.master, u.exp_avg, u.exp_avg_sq,
+                           u.shard_out]
             param = _mem(u.master, pre + "master")
             s0 = _mem(u.exp_avg, pre + "exp_avg")
             s1 = _mem(u.exp_avg_sq, pre + "exp_avg_sq") if u.exp_avg_sq is not None else None

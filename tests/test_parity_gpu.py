@@ -519,6 +519,50 @@ def test_step_from_host_full_size_sampled(F, orc):
     torch.cuda.empty_cache()
 
 
+def test_zero_copy_step_full_size_sampled(F, orc):
+    # the bench's other end-to-end form on the 70B unit: the 13.7 GB of
+    # gradients stay in pinned host memory and the fused kernel reads them
+    # in place through the C ABI (gradients are "device or mapped host"),
+    # then the two gathers; the count comes back each step; sampled elements
+    # against the oracle
+    cfg = fi.CONFIGS["llama70b"]
+    N = cfg.world
+    unit = new_unit(F, cfg)
+    unit.load_master([fi.gen_master(cfg, device=DEV)])
+    P_pad = unit.padded_numel
+    idx = _sample_indices(P_pad, N, 1 << 19, 17)
+    idx_c = torch.from_numpy(idx)
+    idx_t = idx_c.to(DEV)
+    p_s = host(unit.master[idx_t])
+    m_s = np.zeros_like(p_s)
+    v_s = np.zeros_like(p_s)
+    hgrads = [torch.empty(P_pad, dtype=torch.bfloat16, pin_memory=True) for _ in range(N)]
+    counter = torch.zeros(1, dtype=torch.int32, device=DEV)
+    hnf = torch.full((1,), -1, dtype=torch.int32, pin_memory=True)
+    for t in (1, 2):
+        for r in range(N):
+            hgrads[r].copy_(fi.gen_grad(cfg, r, t, device=DEV))
+        g_s = [host(hgrads[r][idx_c]) for r in range(N)]
+        counter.zero_()
+        F.fsdp_reduce_scatter_adam_cast(hgrads, unit.master, unit.exp_avg, unit.exp_avg_sq, unit.shard_out,
+                                        hp_for(F, cfg, t), nonfinite_count=counter)
+        hnf.copy_(counter, non_blocking=True)
+        for _ in range(cfg.gathers):
+            unit.all_gather()
+        s = orc.scalars(ohp_for(orc, cfg, t), N)
+        orc.adamw(p_s, m_s, v_s, orc.all_reduce_avg(g_s, cfg.grad_dtype, N, s.c), s)
+        torch.cuda.synchronize()
+        assert int(hnf.item()) == 0
+        assert_state_close(host(unit.master[idx_t]), p_s, f"master t={t}")
+        assert_state_close(host(unit.exp_avg[idx_t]), m_s, f"exp_avg t={t}")
+        assert_state_close(host(unit.exp_avg_sq[idx_t]), v_s, f"exp_avg_sq t={t}")
+        assert_out_close(host(unit.shard_out[idx_t]), orc.cast_out(p_s, cfg.out_dtype), cfg.out_dtype, f"t={t}")
+        for f in unit.full:
+            assert torch.equal(f, unit.shard_out)
+    del unit, hgrads
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ fused all-gather
 
 @pytest.mark.parametrize("name", ["tiny", "gpt2_small", "gpt2_large"])

@@ -195,3 +195,22 @@ def test_wait_timeouts_counter_reads_zero_on_every_step_path(F):
     graph.close()
     with pytest.raises(ValueError):
         units[0].all_gather(wait_timeouts=torch.zeros(1, dtype=torch.float32, device=DEV))
+
+
+def test_descriptors_keep_the_buffers_they_point_at_alive(F):
+    # a plan or a captured step writes to the addresses its descriptors were
+    # made with; a buffer replaced in a unit afterwards must not be freed and
+    # handed to another allocation while they exist
+    units = build(F, 8)[:3]
+    seq = F.UnitSequence(units)
+    seq.step(F.AdamWHParams(1e-3, step=1), gathers=1)
+    old = units[1].exp_avg
+    ptr = old.data_ptr()
+    units[1].exp_avg = torch.zeros_like(old)  # replaced after the descriptors were made
+    del old
+    fresh = [torch.empty_like(units[1].exp_avg) for _ in range(4)]
+    assert all(t.data_ptr() != ptr for t in fresh)
+    kept = [t for t in seq.descs._keep if isinstance(t, torch.Tensor)]
+    assert any(t.data_ptr() == ptr for t in kept)
+    seq.step(F.AdamWHParams(1e-3, step=2), gathers=1)  # still writes the old buffer, which is still allocated
+    torch.cuda.synchronize()
