@@ -327,7 +327,7 @@ def timed_launches(fn, K: int, stream, flush: L2Flush):
     return [a.elapsed_time(b) for a, b in pairs]
 
 
-GROUP_MAX_UNITS = 128          # the library's batched launches: units per launch
+GROUP_MAX_UNITS = 256          # the library's batched launches: units per launch
 GROUP_MAX_NUMEL = 1 << 24      # and the largest unit they take
 
 
@@ -348,7 +348,10 @@ def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20, numel
     a Python loop over the units, by the native step of a model validated
     once (UnitSequence.step: a StepPlan launch), by one fsdp_step_units call
     that validates every unit each time, and by one launch of the step
-    captured as a CUDA graph. Returns (result, timed launches)."""
+    captured as a CUDA graph; beside them the planned step with the gather
+    fused into the update (`native_fused_gather`, its own byte model: no
+    separate gather, the shard and every gathered buffer written by the
+    update). Returns (result, timed launches)."""
     import torch
 
     cfg = fi.CONFIGS["gpt2_small"]
@@ -379,6 +382,9 @@ def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20, numel
     def native_unplanned():
         seq.step_unplanned(hp(), gathers=cfg.gathers)
 
+    def native_fused_gather():
+        seq.step(hp(), gathers=cfg.gathers, fuse_gather=True)
+
     graph = seq.capture(gathers=cfg.gathers)
 
     def captured():
@@ -386,7 +392,7 @@ def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20, numel
 
     out = {}
     for name, fn in (("python_loop", python_loop), ("native", native), ("native_unplanned", native_unplanned),
-                     ("cuda_graph", captured)):
+                     ("cuda_graph", captured), ("native_fused_gather", native_fused_gather)):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
@@ -406,14 +412,21 @@ def measure_driver(F, fi, dev, stream, n_units: int = 12, steps: int = 20, numel
         out[name + "_GBs"] = round((rsa_b + ag_b) / (out[name]["device_ms_per_step"] * 1e-3) / 1e9, 1)
     out["native_over_cuda_graph"] = round(out["native"]["device_ms_per_step"]
                                           / out["cuda_graph"]["device_ms_per_step"], 3)
+    fused_b = sum(u.padded_numel * (u.world * u.grads[0].element_size() + 3 * (4 + 4)
+                                     + u.shard_out.element_size() * (1 + len(u.full))) for u in units)
+    fused_b += sum(u.padded_numel * u.shard_out.element_size() * (1 + len(u.full)) for u in units) * (cfg.gathers - 1)
+    out["native_fused_gather_bytes_per_step"] = fused_b
+    out["native_fused_gather_GBs"] = round(fused_b / (out["native_fused_gather"]["device_ms_per_step"] * 1e-3)
+                                           / 1e9, 1)
     per_unit = n_units * (1 + cfg.gathers)
     batched = model_launches(n_units, units[0].padded_numel, cfg.gathers)
+    fused = seq.launches(gathers=cfg.gathers, fuse_gather=True)
     out["launches_per_step"] = {"python_loop": per_unit, "native": batched, "native_unplanned": batched,
-                                "cuda_graph": batched}
+                                "cuda_graph": batched, "native_fused_gather": fused}
     graph.close()
     del seq, units, graph
     torch.cuda.empty_cache()
-    return out, steps * (per_unit + 3 * batched)
+    return out, steps * (per_unit + 3 * batched + fused)
 
 
 def max_over_ranks(values, device):

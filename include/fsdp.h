@@ -330,12 +330,13 @@ fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
  * the work already on `stream` and which `stream` waits for afterwards; a
  * unit's kernels run in order on one of them and overlap the neighbouring
  * unit's. Work enqueued on `stream` after the call sees every unit done.
- * Batching: small units are stepped together, up to 128 per launch of each
- * kernel, when they share N (2, 4 or 8), the dtype pair and the gathers,
- * and each has at most 2^24 elements, at most 8 gathered buffers, 16-byte
- * aligned buffers, its state in device memory and no fused gather; every element
- * sees the same operations as in the unit's own launch, so the results are
- * the same bits. Every other unit keeps its own launches. */
+ * Batching: small units are stepped together, up to 256 per launch of each
+ * kernel (128 when the first gather is fused into the update), when they
+ * share N (2, 4 or 8), the dtype pair and the gathers, and each has at most
+ * 2^24 elements, at most 8 gathered buffers, 16-byte aligned buffers and
+ * its state in device memory; every element sees the same operations as in
+ * the unit's own launch, so the results are the same bits. Every other unit
+ * keeps its own launches. */
 fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
                             int gathers, int fuse_first_gather, uint32_t *nonfinite_count,
                             uint32_t *wait_timeouts, void *stream);

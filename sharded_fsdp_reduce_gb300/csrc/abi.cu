@@ -491,7 +491,9 @@ fsdp_status launch_unit(const UnitPlan &p, cudaStream_t s, cudaGraphNode_t *upda
 // group's.
 struct Group {
     bool variant = false;
+    bool fused = false;        // the fused AdamW update with the first gather fused in
     RsaGroupArgs rsa;
+    RsaFusedGroupArgs fused_rsa;
     StepGroupArgs step;
     GatherGroupArgs gather;
     int n = 0;
@@ -509,8 +511,9 @@ struct Work {
 
 // The update node of a captured work item and what its arguments hold: the
 // per-unit fused kernel (RsaArgs), the per-unit variant kernel (StepArgs),
-// or the batched update of either (RsaGroupArgs, StepGroupArgs).
-enum NodeKind { kNodeUnit = 0, kNodeVariant = 1, kNodeGroup = 2, kNodeVariantGroup = 3 };
+// or the batched update of either (RsaGroupArgs, StepGroupArgs), or the
+// batched fused kernel with the first gather fused in (RsaFusedGroupArgs).
+enum NodeKind { kNodeUnit = 0, kNodeVariant = 1, kNodeGroup = 2, kNodeVariantGroup = 3, kNodeFusedGroup = 4 };
 struct UpdateNode {
     cudaGraphNode_t node = nullptr;
     int kind = kNodeUnit;
@@ -523,10 +526,10 @@ struct UpdateNode {
 // the number of gathers (each unit keeps its own gathered buffers, 1 to
 // kGroupMaxWorld of them).
 struct GroupKey {
-    bool variant;
+    bool variant, fused;
     int optimizer, state_dtype, reduce_lowp, world, grad_dtype, out_dtype, gathers;
     bool operator==(const GroupKey &o) const {
-        return variant == o.variant && optimizer == o.optimizer && state_dtype == o.state_dtype &&
+        return variant == o.variant && fused == o.fused && optimizer == o.optimizer && state_dtype == o.state_dtype &&
                reduce_lowp == o.reduce_lowp && world == o.world && grad_dtype == o.grad_dtype &&
                out_dtype == o.out_dtype && gathers == o.gathers;
     }
@@ -535,6 +538,7 @@ struct GroupKey {
 GroupKey key_of(const UnitPlan &p) {
     GroupKey k{};
     k.variant = p.variant;
+    k.fused = !p.variant && p.rsa.n_full > 0;
     k.optimizer = p.variant ? p.step.optimizer : FSDP_OPT_ADAMW;
     k.state_dtype = p.variant ? p.step.state_dtype : FSDP_F32;
     k.reduce_lowp = p.variant ? p.step.args.reduce_lowp : 0;
@@ -545,11 +549,12 @@ GroupKey key_of(const UnitPlan &p) {
     return k;
 }
 
-// Whether a unit joins a batched launch: an update over all its ranks (no
-// fused gather), N in {2, 4, 8}, at most kGroupMaxNumel elements, every base
-// pointer 16-byte aligned (the vector path and the bulk copies), the
-// parameter or master in device memory and at most kGroupMaxWorld gathered
-// buffers. Larger units fill the GPU on their own and keep their own
+// Whether a unit joins a batched launch: an update over all its ranks, N in
+// {2, 4, 8}, at most kGroupMaxNumel elements, every base pointer 16-byte
+// aligned (the vector path and the bulk copies), the parameter or master in
+// device memory and at most kGroupMaxWorld gathered buffers. A fused first
+// gather (the fused AdamW update only) batches with the units that fuse it
+// too. Larger units fill the GPU on their own and keep their own
 // launches, whose gather (several tiles in flight per CTA, 3 CTAs per SM)
 // measured faster at those sizes than the batched gather's one-tile CTAs.
 bool groupable(const UnitPlan &p) {
@@ -565,11 +570,13 @@ bool groupable(const UnitPlan &p) {
         state = a.param;
     } else {
         const RsaArgs &a = p.rsa;
-        if (a.n_full != 0 || a.begin != 0 || a.end > kGroupMaxNumel) return false;
+        if (a.n_full > kGroupMaxWorld || a.begin != 0 || a.end > kGroupMaxNumel) return false;
         if (a.world != 2 && a.world != 4 && a.world != 8) return false;
         if (!aligned(a.master, 16) || !aligned(a.m, 16) || !aligned(a.v, 16) || !aligned(a.out, 16)) return false;
         for (int q = 0; q < a.world; ++q)
             if (!aligned(a.grads[q], 16)) return false;
+        for (int d = 0; d < a.n_full; ++d)
+            if (!aligned(a.full[d], 16)) return false;
         state = a.master;
     }
     if (p.separate_gathers > 0) {
@@ -585,6 +592,7 @@ Group *new_group(std::vector<std::unique_ptr<Group>> &groups, const UnitPlan &p,
     groups.push_back(std::unique_ptr<Group>(new Group()));
     Group *g = groups.back().get();
     memset(&g->rsa, 0, sizeof(g->rsa));
+    memset(&g->fused_rsa, 0, sizeof(g->fused_rsa));
     memset(&g->step, 0, sizeof(g->step));
     memset(&g->gather, 0, sizeof(g->gather));
     g->variant = p.variant;
@@ -595,6 +603,11 @@ Group *new_group(std::vector<std::unique_ptr<Group>> &groups, const UnitPlan &p,
         g->step.nonfinite = p.step.args.nonfinite;
         g->optimizer = p.step.optimizer;
         g->state_dtype = p.step.state_dtype;
+    } else if (p.rsa.n_full > 0) {
+        g->fused = true;
+        g->fused_rsa.s = p.rsa.s;
+        g->fused_rsa.world = p.rsa.world;
+        g->fused_rsa.nonfinite = p.rsa.nonfinite;
     } else {
         g->rsa.s = p.rsa.s;
         g->rsa.world = p.rsa.world;
@@ -624,6 +637,22 @@ void add_to_group(Group &G, const UnitPlan &p) {
         gu.ncta = group_update_ctas(a.end);
         G.update_grid += gu.ncta;
         G.step.n = k + 1;
+    } else if (G.fused) {
+        const RsaArgs &a = p.rsa;
+        FusedGroupUnit &gu = G.fused_rsa.u[k];
+        memset(&gu, 0, sizeof(gu));
+        for (int q = 0; q < a.world; ++q) gu.grads[q] = a.grads[q];
+        for (int d = 0; d < a.n_full; ++d) gu.full[d] = a.full[d];
+        gu.master = a.master;
+        gu.m = a.m;
+        gu.v = a.v;
+        gu.out = a.out;
+        gu.numel = a.end;
+        gu.cta_begin = G.update_grid;
+        gu.ncta = group_update_ctas(a.end);
+        gu.n_full = a.n_full;
+        G.update_grid += gu.ncta;
+        G.fused_rsa.n = k + 1;
     } else {
         const RsaArgs &a = p.rsa;
         GroupUnit &gu = G.rsa.u[k];
@@ -673,7 +702,7 @@ void make_work(const std::vector<UnitPlan> &plan, std::vector<Work> &work,
         std::pair<GroupKey, Group *> *slot = nullptr;
         for (auto &o : open)
             if (o.first == key) slot = &o;
-        if (!slot || slot->second->n == kGroupMax) {
+        if (!slot || slot->second->n == (slot->second->fused ? kFusedGroupMax : kGroupMax)) {
             Group *g = new_group(groups, p, static_cast<int>(u));
             work.push_back({-1, g});
             if (slot) {
@@ -718,10 +747,11 @@ fsdp_status launch_work(const std::vector<UnitPlan> &plan, const Work &w, cudaSt
     }
     const Group &G = *w.group;
     fsdp_status st = G.variant ? launch_step_group(G, s)
+                     : G.fused ? launch_rsa_fused_group(G.fused_rsa, G.grad_dtype, G.out_dtype, G.update_grid, s)
                                : launch_rsa_group(G.rsa, G.grad_dtype, G.out_dtype, G.update_grid, s);
     if (st == FSDP_OK && node) {
-        node->kind = G.variant ? kNodeVariantGroup : kNodeGroup;
-        node->world = G.variant ? G.step.world : G.rsa.world;
+        node->kind = G.variant ? kNodeVariantGroup : G.fused ? kNodeFusedGroup : kNodeGroup;
+        node->world = G.variant ? G.step.world : G.fused ? G.fused_rsa.world : G.rsa.world;
         node->grad_dtype = G.grad_dtype;
         st = last_captured_node(s, &node->node);
     }
@@ -921,7 +951,13 @@ fsdp_status plan_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_ste
 void set_adam_scalars(ModelPlan &m, const fsdp_adamw_hparams &hp) {
     for (UnitPlan &p : m.units)
         if (!p.empty) p.rsa.s = make_scalars(hp, p.rsa.world);
-    for (auto &g : m.groups) g->rsa.s = make_scalars(hp, g->rsa.world);
+    for (auto &g : m.groups) {
+        if (g->fused) {
+            g->fused_rsa.s = make_scalars(hp, g->fused_rsa.world);
+        } else {
+            g->rsa.s = make_scalars(hp, g->rsa.world);
+        }
+    }
 }
 
 // and the variant update's (its scalars and the reduction flag).
@@ -1192,9 +1228,11 @@ FSDP_API fsdp_status fsdp_step_graph_launch(fsdp_step_graph *graph, const fsdp_a
     if (!adam_step_valid(*hp)) return FSDP_ERR_INVALID_ARG;
     for (const UpdateNode &n : graph->nodes) {
         const AdamScalars sc = make_scalars(*hp, n.world);
-        fsdp_status st = n.kind == kNodeGroup
-                             ? set_update_node<RsaGroupArgs, 1>(graph, n.node, [&](RsaGroupArgs &a) { a.s = sc; })
-                             : set_update_node<RsaArgs, 4>(graph, n.node, [&](RsaArgs &a) { a.s = sc; });
+        fsdp_status st =
+            n.kind == kNodeGroup ? set_update_node<RsaGroupArgs, 1>(graph, n.node, [&](RsaGroupArgs &a) { a.s = sc; })
+            : n.kind == kNodeFusedGroup
+                ? set_update_node<RsaFusedGroupArgs, 1>(graph, n.node, [&](RsaFusedGroupArgs &a) { a.s = sc; })
+                : set_update_node<RsaArgs, 4>(graph, n.node, [&](RsaArgs &a) { a.s = sc; });
         if (st != FSDP_OK) return st;
     }
     return cuda_status(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));

@@ -17,7 +17,16 @@
 
 namespace fsdp {
 
-constexpr int kGroupMax = 128;                          // units per batched launch
+// Units per batched launch. 256 units' descriptors take 30.8 KB of the
+// 32,764 bytes of kernel parameter space (the asserts below). Measured
+// against 128 (the same results bit for bit): a model of 500 units of 20 k
+// elements 0.104 against 0.121 ms per step (4 launches instead of 8); 200
+// and 256 units of 50 k unchanged (their two groups of 128 already overlapped
+// on the two side streams).
+#ifndef FSDP_GROUP_MAX
+#define FSDP_GROUP_MAX 256
+#endif
+constexpr int kGroupMax = FSDP_GROUP_MAX;
 constexpr int kGroupMaxWorld = 8;                       // gradient / destination pointers per unit
 #ifndef FSDP_GROUP_MAX_NUMEL_LOG2
 #define FSDP_GROUP_MAX_NUMEL_LOG2 24
@@ -50,6 +59,34 @@ struct RsaGroupArgs {
     int32_t n;      // units
     int32_t world;
     GroupUnit u[kGroupMax];
+};
+
+// One unit of a batched update with the first all-gather fused in (the
+// update also stores every output word to the unit's gathered buffers):
+// GroupUnit's fields and the gathered buffers' pointers. The descriptor is
+// 184 bytes, so a launch takes up to kFusedGroupMax units (23.6 KB of
+// parameter space).
+constexpr int kFusedGroupMax = 128;
+
+struct FusedGroupUnit {
+    const void *grads[kGroupMaxWorld];  // world pointers used
+    void *full[kGroupMaxWorld];         // n_full pointers used
+    float *master;
+    float *m;
+    float *v;
+    void *out;          // the compute-dtype shard (shard_out)
+    int64_t numel;      // padded_numel
+    int64_t cta_begin;  // the unit's first CTA in the launch
+    int32_t ncta;       // its CTAs, as group_update_ctas counts them
+    int32_t n_full;     // 1..kGroupMaxWorld
+};
+
+struct RsaFusedGroupArgs {
+    AdamScalars s;  // first member: the block a captured step rewrites per step
+    uint32_t *nonfinite;
+    int32_t n;      // units
+    int32_t world;
+    FusedGroupUnit u[kFusedGroupMax];
 };
 
 // One unit of a batched all-gather: src and every destination 16-byte aligned.
@@ -97,6 +134,7 @@ struct StepGroupArgs {
 static_assert(sizeof(RsaGroupArgs) < 32764, "kernel parameter space");
 static_assert(sizeof(StepGroupArgs) < 32764, "kernel parameter space");
 static_assert(sizeof(GatherGroupArgs) < 32764, "kernel parameter space");
+static_assert(sizeof(RsaFusedGroupArgs) < 32764, "kernel parameter space");
 
 // CTAs of one unit in a batched update (kGroupThreads chunks each), and
 // tiles of one unit in a batched gather (at least one each: a CTA also takes
@@ -107,6 +145,9 @@ int64_t group_gather_tiles(int64_t nbytes);
 // Launch `grid` CTAs of the batched kernels on stream s.
 fsdp_status launch_rsa_group(const RsaGroupArgs &g, int grad_dtype, int out_dtype, int64_t grid, cudaStream_t s);
 fsdp_status launch_gather_group(const GatherGroupArgs &g, int64_t grid, cudaStream_t s);
+// The batched update with the first gather fused in (rsa_group_fused.cu).
+fsdp_status launch_rsa_fused_group(const RsaFusedGroupArgs &g, int grad_dtype, int out_dtype, int64_t grid,
+                                   cudaStream_t s);
 
 // The batched variant step, one translation unit per optimizer
 // (step_group_<optimizer>.cu); (state, out) dtype pairs as the per-unit

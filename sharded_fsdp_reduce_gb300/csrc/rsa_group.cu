@@ -57,10 +57,10 @@ __global__ void __launch_bounds__(rsa::kThreads, group_min_blocks<NW, GD>())
     const int64_t nchunks = U.numel / 8;
     const int64_t k = local * rsa::kThreads + threadIdx.x;
     uint32_t bad = 0;
-    if (k < nchunks) bad += rsa::vec_chunk<NW, GD, OD, false, false>(a, NW, 8 * k, 8 * k + 4);
+    if (k < nchunks) bad += rsa::vec_chunk<NW, GD, OD, false, false>(a, NW, 8 * k, 8 * k + 4, nullptr, 0);
     if (local == U.ncta - 1) {
         for (int64_t j = 8 * nchunks + threadIdx.x; j < U.numel; j += blockDim.x)
-            bad += rsa::scalar_elem<GD, OD, false>(a, NW, j);
+            bad += rsa::scalar_elem<GD, OD, false>(a, NW, j, nullptr, 0);
     }
     if (g.nonfinite != nullptr) {
         const uint32_t total = __reduce_add_sync(0xffffffffu, bad);

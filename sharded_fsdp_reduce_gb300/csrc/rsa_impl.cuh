@@ -68,9 +68,14 @@ __device__ __forceinline__ void adamw(float g, float &p, float &m, float &v, con
 
 __device__ __forceinline__ uint32_t nonfinite(float g) { return isfinite(g) ? 0u : 1u; }
 
+// The gathered buffers of a fused gather: n_full pointers at `full` (the
+// per-unit kernel's own arguments, or one unit's descriptor in a batched
+// launch); unused without GATHER.
+
 // One element through the plain path.
 template <int GD, int OD, bool GATHER>
-__device__ __forceinline__ uint32_t scalar_elem(const RsaArgs &a, int world, int64_t j) {
+__device__ __forceinline__ uint32_t scalar_elem(const RsaArgs &a, int world, int64_t j, void *const *full,
+                                                int n_full) {
     float acc = Dtype<GD>::load(a.grads[0], j);
     for (int q = 1; q < world; ++q) acc = __fadd_rn(acc, Dtype<GD>::load(a.grads[q], j));
     const float g = __fmul_rn(acc, a.s.c);
@@ -81,7 +86,7 @@ __device__ __forceinline__ uint32_t scalar_elem(const RsaArgs &a, int world, int
     a.v[j] = v;
     if (a.out != nullptr) Dtype<OD>::store(a.out, j, p);
     if constexpr (GATHER) {
-        for (int d = 0; d < a.n_full; ++d) Dtype<OD>::store(a.full[d], j, p);
+        for (int d = 0; d < n_full; ++d) Dtype<OD>::store(full[d], j, p);
     }
     return nonfinite(g);
 }
@@ -99,7 +104,7 @@ __device__ __forceinline__ uint32_t scalar_elem(const RsaArgs &a, int world, int
 template <int OD, bool GATHER, bool SPLIT>
 __device__ __forceinline__ uint32_t finish_chunk(const RsaArgs &a, int64_t j_lo, int64_t j_hi, const float *acc,
                                                  float4 p0, float4 p1, float4 m0, float4 m1,
-                                                 float4 v0, float4 v1) {
+                                                 float4 v0, float4 v1, void *const *full, int n_full) {
     float p[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
     float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
     float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -123,9 +128,9 @@ __device__ __forceinline__ uint32_t finish_chunk(const RsaArgs &a, int64_t j_lo,
             st_state(static_cast<float *>(a.out) + j_hi, hi);
         }
         if constexpr (GATHER) {
-            for (int d = 0; d < a.n_full; ++d) {
-                st_state(static_cast<float *>(a.full[d]) + j_lo, lo);
-                st_state(static_cast<float *>(a.full[d]) + j_hi, hi);
+            for (int d = 0; d < n_full; ++d) {
+                st_state(static_cast<float *>(full[d]) + j_lo, lo);
+                st_state(static_cast<float *>(full[d]) + j_hi, hi);
             }
         }
     } else {
@@ -142,7 +147,7 @@ __device__ __forceinline__ uint32_t finish_chunk(const RsaArgs &a, int64_t j_lo,
         };
         if (a.out != nullptr) put(a.out);
         if constexpr (GATHER) {
-            for (int d = 0; d < a.n_full; ++d) put(a.full[d]);
+            for (int d = 0; d < n_full; ++d) put(full[d]);
         }
     }
     return bad;
@@ -188,7 +193,8 @@ template <int GD> __device__ __forceinline__ void widen8(const uint4 *w, float *
 }
 
 template <int NW, int GD, int OD, bool GATHER, bool SPLIT>
-__device__ __forceinline__ uint32_t vec_chunk(const RsaArgs &a, int world, int64_t j_lo, int64_t j_hi) {
+__device__ __forceinline__ uint32_t vec_chunk(const RsaArgs &a, int world, int64_t j_lo, int64_t j_hi,
+                                              void *const *full, int n_full) {
     float acc[8];
     if constexpr (NW > 0) {
         // every load of the chunk (N gradient words, then the state) is in
@@ -207,7 +213,7 @@ __device__ __forceinline__ uint32_t vec_chunk(const RsaArgs &a, int world, int64
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
         }
-        return finish_chunk<OD, GATHER, SPLIT>(a, j_lo, j_hi, acc, p0, p1, m0, m1, v0, v1);
+        return finish_chunk<OD, GATHER, SPLIT>(a, j_lo, j_hi, acc, p0, p1, m0, m1, v0, v1, full, n_full);
     } else {
         for (int q = 0; q < world; ++q) {
             uint4 w[GradRegs<1, GD>::kWords];
@@ -220,7 +226,7 @@ __device__ __forceinline__ uint32_t vec_chunk(const RsaArgs &a, int world, int64
         const float4 p0 = ld_state(a.master + j_lo), p1 = ld_state(a.master + j_hi);
         const float4 m0 = ld_state(a.m + j_lo), m1 = ld_state(a.m + j_hi);
         const float4 v0 = ld_state(a.v + j_lo), v1 = ld_state(a.v + j_hi);
-        return finish_chunk<OD, GATHER, SPLIT>(a, j_lo, j_hi, acc, p0, p1, m0, m1, v0, v1);
+        return finish_chunk<OD, GATHER, SPLIT>(a, j_lo, j_hi, acc, p0, p1, m0, m1, v0, v1, full, n_full);
     }
 }
 
@@ -246,13 +252,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
             j_lo = vbegin + 8 * k;
             j_hi = j_lo + 4;
         }
-        bad += vec_chunk<NW, GD, OD, GATHER, SPLIT>(a, world, j_lo, j_hi);
+        bad += vec_chunk<NW, GD, OD, GATHER, SPLIT>(a, world, j_lo, j_hi, a.full, a.n_full);
     }
     const int64_t nhead = vbegin - a.begin;
     const int64_t nrest = nhead + (a.end - vend);
     for (int64_t e = tid; e < nrest; e += stride) {
         const int64_t j = e < nhead ? a.begin + e : vend + (e - nhead);
-        bad += scalar_elem<GD, OD, GATHER>(a, world, j);
+        bad += scalar_elem<GD, OD, GATHER>(a, world, j, a.full, a.n_full);
     }
     if (a.nonfinite != nullptr) {
         const uint32_t total = __reduce_add_sync(0xffffffffu, bad);

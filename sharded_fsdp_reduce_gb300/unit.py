@@ -294,7 +294,7 @@ class UnitSequence:
     unit the update and its all-gathers, ordered on the caller's stream. The
     native loop spreads the units over two side streams and batches units of
     up to 2^24 elements that share N, dtypes and gathers into one launch per
-    kernel (128 units at most); the results are those of stepping each unit
+    kernel (256 units at most); the results are those of stepping each unit
     on its own.
 
     step() validates the model once and keeps that plan (StepPlan) for the

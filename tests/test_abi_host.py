@@ -419,8 +419,9 @@ def _fake_units(E, specs, ex=False):
 
 @pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host-only: fake addresses need a machine without a GPU")
 def test_step_units_launches_follow_the_batching(lib):
-    # the planning query: nothing is enqueued; small units batch 128 per
-    # launch, larger or misaligned units or N = 3 keep their own launches
+    # the planning query: nothing is enqueued; small units batch
+    # bench.GROUP_MAX_UNITS (the header's batch size) per launch, larger or
+    # misaligned units or N = 3 keep their own launches
     from sharded_fsdp_reduce_gb300 import _lib as E
     import bench
     hp = E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
@@ -433,7 +434,8 @@ def test_step_units_launches_follow_the_batching(lib):
         return out.value
 
     small = (50000, 8, 8, False)
-    for n, gathers in ((200, 1), (200, 2), (200, 0), (128, 1), (129, 1), (1, 1), (2, 1)):
+    G = bench.GROUP_MAX_UNITS
+    for n, gathers in ((200, 1), (200, 2), (200, 0), (G, 1), (G + 1, 1), (2 * G + 3, 1), (1, 1), (2, 1)):
         assert count([small] * n, gathers) == bench.model_launches(n, 50000, gathers), (n, gathers)
     assert count([(7087872, 8, 8, False)] * 12) == bench.model_launches(12, 7087872, 1) == 2
     big = ((1 << 24) + 8, 8, 8, False)
@@ -441,7 +443,9 @@ def test_step_units_launches_follow_the_batching(lib):
     assert count([small] * 5 + [(50000, 8, 8, True)]) == 2 + 2       # a misaligned unit keeps its own
     assert count([small] * 5 + [(50000 - 2, 2, 1, False)] * 3) == 2 + 2   # another N: a second batch
     assert count([(3 * 1000, 3, 3, False)] * 4) == 8                 # N = 3 is not batched
-    assert count([small] * 5, gathers=2, fuse=1) == 5 * 2            # fused gather: own launches
+    assert count([small] * 5, gathers=2, fuse=1) == 2                # fused gather: one batch, then a gather
+    assert count([small] * 300, gathers=1, fuse=1) == 3              # fused batches take 128 units each
+    assert count([small] * 5 + [(50000, 8, 8, True)], gathers=1, fuse=1) == 1 + 1  # misaligned: its own
     assert count([small] * 3 + [(0, 8, 8, False)]) == 2              # an empty unit launches nothing
     assert lib.fsdp_step_units_launches(None, 0, ctypes.byref(hp), 1, 0, None) == E.FSDP_ERR_INVALID_ARG
     arr, keep = _fake_units(E, [small, small])
@@ -449,10 +453,10 @@ def test_step_units_launches_follow_the_batching(lib):
     assert lib.fsdp_step_units_launches(arr, 2, ctypes.byref(hp), 1, 0, ctypes.byref(out)) == E.FSDP_ERR_INVALID_ARG
     # the variant call
     cfg = E.FsdpStepConfig(1, 0, 1e-2, 0.9, 0.0, 0.0, 0.0, 1, 1.0)  # SGD: one state
-    arr, keep = _fake_units(E, [small] * 150, ex=True)
-    for k in range(150):
+    arr, keep = _fake_units(E, [small] * (G + 22), ex=True)
+    for k in range(G + 22):
         arr[k].state1 = None
-    assert lib.fsdp_step_units_ex_launches(arr, 150, ctypes.byref(cfg), 1, ctypes.byref(out)) == E.FSDP_OK
+    assert lib.fsdp_step_units_ex_launches(arr, G + 22, ctypes.byref(cfg), 1, ctypes.byref(out)) == E.FSDP_OK
     assert out.value == 4
     assert lib.fsdp_last_cuda_error() == 0
 
@@ -460,9 +464,11 @@ def test_step_units_launches_follow_the_batching(lib):
 def _expected_launches(specs, gathers):
     """The batching rule restated: units of N in {2, 4, 8}, at most 2^24
     elements, 16-byte aligned and not empty batch with the earlier ones of
-    the same N (every fake unit here shares the dtypes and gathers), 128 per
-    batch; a batch of one is a unit on its own; one update and `gathers`
-    gathers per work item."""
+    the same N (every fake unit here shares the dtypes and gathers), the
+    header's batch size per batch; a batch of one is a unit on its own; one
+    update and `gathers` gathers per work item."""
+    import bench
+    G = bench.GROUP_MAX_UNITS
     items, open_ = 0, {}
     for P, world, n_full, misaligned in specs:
         if P == 0:
@@ -470,7 +476,7 @@ def _expected_launches(specs, gathers):
         if world not in (2, 4, 8) or P > (1 << 24) or misaligned or n_full > 8:
             items += 1
             continue
-        if open_.get(world, 128) == 128:
+        if open_.get(world, G) == G:
             items += 1
             open_[world] = 0
         open_[world] += 1

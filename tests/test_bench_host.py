@@ -1,6 +1,6 @@
 """Host logic of bench.py that needs no GPU: the launch count it claims for
 the driver legs follows the library's batching rule (units of at most 2^24
-elements batched up to 128 per launch, a unit above that size launched on
+elements batched up to 256 per launch, a unit above that size launched on
 its own)."""
 import os
 import sys
@@ -16,21 +16,23 @@ def test_model_launches_follow_the_batching_rule():
     assert bench.model_launches(12, 7087872, 1) == 2
     # units above the size limit: one update and one gather each
     assert bench.model_launches(12, 855654400, 1) == 24
-    # 200 units of 50,000: groups of 128 and 72, an update and a gather each
-    assert bench.model_launches(200, 50000, 1) == 4
-    assert bench.model_launches(200, 50000, 2) == 6
-    assert bench.model_launches(200, 50000, 0) == 2
-    # 128 fill one group; 129 leave one unit, launched on its own
-    assert bench.model_launches(128, 1000, 1) == 2
-    assert bench.model_launches(129, 1000, 1) == 4
+    # 200 units of 50,000: one group, an update and a gather
+    assert bench.model_launches(200, 50000, 1) == 2
+    assert bench.model_launches(200, 50000, 2) == 3
+    assert bench.model_launches(200, 50000, 0) == 1
+    # 500 units: groups of 256 and 244
+    assert bench.model_launches(500, 20000, 1) == 4
+    # 256 fill one group; 257 leave one unit, launched on its own
+    assert bench.model_launches(256, 1000, 1) == 2
+    assert bench.model_launches(257, 1000, 1) == 4
     # the size limit is inclusive
     assert bench.model_launches(3, 1 << 24, 1) == 2
     assert bench.model_launches(3, (1 << 24) + 8, 1) == 6
-    assert bench.GROUP_MAX_UNITS == 128 and bench.GROUP_MAX_NUMEL == 1 << 24
+    assert bench.GROUP_MAX_UNITS == 256 and bench.GROUP_MAX_NUMEL == 1 << 24
 
 
 def test_batching_constants_match_the_library():
     import re
     src = open(os.path.join(ROOT, "sharded_fsdp_reduce_gb300", "csrc", "group.cuh")).read()
-    assert int(re.search(r"kGroupMax = (\d+);", src).group(1)) == bench.GROUP_MAX_UNITS
+    assert int(re.search(r"#define FSDP_GROUP_MAX (\d+)", src).group(1)) == bench.GROUP_MAX_UNITS
     assert 1 << int(re.search(r"#define FSDP_GROUP_MAX_NUMEL_LOG2 (\d+)", src).group(1)) == bench.GROUP_MAX_NUMEL

@@ -248,15 +248,17 @@ def _same(x, y):
 
 @pytest.mark.parametrize("seed", range(10))
 def test_fuzz_batched_models(F, seed):
-    # a random model of 2-160 units for the batched launches: mostly small
+    # a random model of 2-320 units for the batched launches: mostly small
     # units of N in {2, 4, 8} and two dtype pairs, 1-8 gathered buffers each,
     # among them units that keep their own launches (N = 3, host-resident
-    # state, above the batching size); stepped by fsdp_step_units (even
-    # seeds) or a captured step (odd seeds) and compared bit for bit with
-    # each unit stepped alone
+    # state, above the batching size), the first gather fused into the
+    # update in half the seeds that gather; stepped by the planned native
+    # step (even seeds) or a captured step (odd seeds) and compared bit for
+    # bit with each unit stepped alone
     rng = np.random.default_rng(7000 + seed)
-    n_units = int(rng.integers(2, 161))
+    n_units = int(rng.integers(2, 321))
     gathers = int(rng.integers(0, 3))
+    fuse = gathers > 0 and bool(rng.random() < 0.5)
     pairs = [(torch.bfloat16, torch.bfloat16), (torch.bfloat16, torch.float16), (torch.float32, torch.bfloat16)]
     a, b = [], []
     g = torch.Generator().manual_seed(seed)
@@ -273,7 +275,7 @@ def test_fuzz_batched_models(F, seed):
             u.load_master([x.to(DEV)])
             dst.append(u)
     torch.cuda.synchronize()
-    graph = F.UnitSequence(a).capture(gathers=gathers) if seed % 2 else None
+    graph = F.UnitSequence(a).capture(gathers=gathers, fuse_gather=fuse) if seed % 2 else None
     seq = F.UnitSequence(a)
     for t in (1, 2, 3):
         gg = torch.Generator().manual_seed(100 * seed + t)
@@ -286,9 +288,9 @@ def test_fuzz_batched_models(F, seed):
         if graph is not None:
             graph.launch(hp)
         else:
-            seq.step(hp, gathers=gathers)
+            seq.step(hp, gathers=gathers, fuse_gather=fuse)
         for u in b:
-            u.step(hp, gathers=gathers)
+            u.step(hp, gathers=gathers, fuse_gather=fuse)
         torch.cuda.synchronize()
         for k, (ua, ub) in enumerate(zip(a, b)):
             for name in ("master", "exp_avg", "exp_avg_sq", "shard_out"):

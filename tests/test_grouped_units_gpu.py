@@ -1,5 +1,5 @@
 """Batched launches of small units: fsdp_step_units (and a captured step)
-runs the fused update and the all-gathers of up to 128 small units of one
+runs the fused update and the all-gathers of up to 256 small units of one
 world size and dtype pair as one launch each. Every element sees the per-unit
 kernel's operations, so the results must equal stepping each unit on its own
 bit for bit, and the oracle.
@@ -72,11 +72,11 @@ def hp(F, t):
 
 @pytest.mark.parametrize("gathers", [0, 1, 2])
 def test_small_units_batched_equal_their_own_steps(F, gathers):
-    # 170 units: sizes from 1 element to 60 k (ragged tails, units smaller than
-    # one chunk), N in {2, 4, 8}, two dtype pairs; 150 of one kind, so that
-    # kind fills one group of 128 and starts a second
+    # 300 units: sizes from 1 element to 60 k (ragged tails, units smaller than
+    # one chunk), N in {2, 4, 8}, two dtype pairs; 280 of one kind, so that
+    # kind fills one group of 256 and starts a second
     rng = np.random.default_rng(gathers)
-    specs = [(int(rng.integers(1, 60000)), 8, torch.bfloat16, torch.bfloat16) for _ in range(150)]
+    specs = [(int(rng.integers(1, 60000)), 8, torch.bfloat16, torch.bfloat16) for _ in range(280)]
     specs += [(int(n), int(w), torch.bfloat16, torch.float16)
               for n, w in zip(rng.integers(1, 20000, 20), rng.choice([2, 4, 8], 20))]
     specs[3] = (1, 8, torch.bfloat16, torch.bfloat16)
@@ -115,25 +115,61 @@ def test_units_with_different_gather_fanouts_batch_together(F):
         assert_units_equal(a, b, 2)
 
 
+@pytest.mark.parametrize("gathers", [1, 2])
+def test_fused_gather_units_batched_equal_their_own_steps(F, gathers):
+    # units whose first gather is written by the update kernel batch too, up
+    # to 128 per launch: 150 units, 140 of one kind (a full fused batch and a
+    # second), sizes from 1 to 60 k elements, 1-8 gathered buffers each, two
+    # dtype pairs; the planned step and the captured step, each bit-equal to
+    # every unit's own fused step
+    rng = np.random.default_rng(30 + gathers)
+    g = torch.Generator().manual_seed(23)
+    a, b, c = [], [], []
+    for k in range(150):
+        numel, n_full = int(rng.integers(1, 60000)), int(rng.integers(1, 9))
+        world, odt = (8, torch.bfloat16) if k < 140 else (int(rng.choice([2, 4])), torch.float16)
+        x = torch.rand(numel, generator=g) * 0.2 - 0.1
+        for dst in (a, b, c):
+            u = F.FlatParamUnit([("w", (numel,))], world, torch.bfloat16, odt, device=DEV, n_full=n_full)
+            u.load_master([x.to(DEV)])
+            dst.append(u)
+    seq = F.UnitSequence(a)
+    assert seq.launches(gathers=gathers, fuse_gather=True) < 10 * gathers
+    graph = F.UnitSequence(c).capture(gathers=gathers, fuse_gather=True)
+    for t in (1, 2, 3):
+        load_grads([a, b, c], t, 47)
+        seq.step(hp(F, t), gathers=gathers, fuse_gather=True)
+        graph.launch(hp(F, t))
+        for u in b:
+            u.step(hp(F, t), gathers=gathers, fuse_gather=True)
+        torch.cuda.synchronize()
+        assert_units_equal(a, b, gathers)
+        assert_units_equal(c, b, gathers)
+    graph.close()
+
+
 def test_launch_counts_of_batched_models(F):
-    # the planning query on real buffers: 200 small units batch into 2
-    # launches per kernel, N = 3 units keep their own, the variant call too
-    a, _ = make_units(F, [(50000, 8, torch.bfloat16, torch.bfloat16)] * 200, 3)
+    # the planning query on real buffers: 300 small units batch into 2
+    # launches per kernel (groups of 256 and 44), N = 3 units keep their own,
+    # the variant call too
+    a, _ = make_units(F, [(20000, 8, torch.bfloat16, torch.bfloat16)] * 300, 3)
     seq = F.UnitSequence(a)
     assert seq.launches(gathers=1) == 4 and seq.launches(gathers=2) == 6 and seq.launches(gathers=0) == 2
-    assert seq.launches(gathers=1, fuse_gather=True) == 200
+    assert F.UnitSequence(a[:200]).launches(gathers=1) == 2
+    assert seq.launches(gathers=1, fuse_gather=True) == 3  # fused batches of 128, 128 and 44
+    assert seq.launches(gathers=2, fuse_gather=True) == 6  # each with its separate second gather
     c, _ = make_units(F, [(3000, 3, torch.bfloat16, torch.bfloat16)] * 4, 4)
     assert F.UnitSequence(a[:10] + c).launches(gathers=1) == 2 + 8
-    v, _ = make_variant_units(F, [(20000, 4, torch.bfloat16, torch.bfloat16)] * 130, 5, "sgd", torch.float32)
+    v, _ = make_variant_units(F, [(20000, 4, torch.bfloat16, torch.bfloat16)] * 260, 5, "sgd", torch.float32)
     assert F.UnitSequence(v).launches(gathers=1) == 4
     assert F.UnitSequence(v).launches(gathers=1, config=vcfg(F, "sgd", 1)) == 4
 
 
 def test_a_full_group_and_a_group_of_one(F):
-    # 129 units of one kind: a full group of 128 and one unit left over,
+    # 257 units of one kind: a full group of 256 and one unit left over,
     # which is launched on its own; both bit-equal to each unit's own step
     rng = np.random.default_rng(5)
-    specs = [(int(n), 2, torch.bfloat16, torch.bfloat16) for n in rng.integers(1, 3000, 129)]
+    specs = [(int(n), 2, torch.bfloat16, torch.bfloat16) for n in rng.integers(1, 3000, 257)]
     a, b = make_units(F, specs, 13)
     seq = F.UnitSequence(a)
     for t in (1, 2):

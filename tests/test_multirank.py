@@ -79,9 +79,12 @@ def test_recorded_traffic_matches_current_kernel_source():
         t = bench.recorded_traffic(workload, P)
         assert t is not None, "profiles/ summary missing or taken on another version of the kernel"
         assert 0.99 * 42 * P <= t <= 1.01 * 42 * P, (workload, t / (42 * P))
-    # the --numel cases of the 70B workload take the same line; another size
-    # of a one-point summary does not
-    assert bench.recorded_traffic("llama70b_block_unit_n8_numel67108864", 67108864) == 2766466816
+    # the --numel cases of the 70B workload take the same line, which passes
+    # through the captured points
+    vals = bench.read_summary(os.path.join(ROOT, "profiles", bench.TRAFFIC_SUMMARY["llama70b_block_unit_n8"]))
+    n2 = int(vals["captured_numel"].split(",")[1])
+    t2 = float(vals["traffic_bytes"].split(",")[1])
+    assert bench.recorded_traffic(f"llama70b_block_unit_n8_numel{n2}", n2) == t2
 
 
 def test_recorded_traffic_line_through_two_captures(tmp_path, monkeypatch):
