@@ -545,6 +545,8 @@ class _Run:
         self.t = 0
         self.launches = 0
         self.rsa_ms_median = None
+        # the timed steps' gathers count their bounded waits that gave up here
+        self.wait_timeouts = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def hp(self, t):
         c = self.cfg
@@ -582,7 +584,7 @@ def time_steps(run: _Run):
             unit.reduce_scatter_adam_cast(hp)
             ev[i][1].record(stream)
             for _ in range(cfg.gathers):
-                unit.all_gather()
+                unit.all_gather(wait_timeouts=run.wait_timeouts)
             ev[i][2].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
@@ -906,6 +908,8 @@ def run_ours(args):
         small_units, n_launch = measure_driver(F, run.fi, dev, run.stream, n_units=200, numel=50000)
         run.launches += n_launch
 
+    if int(run.wait_timeouts.item()) != 0:
+        raise RuntimeError("a bounded wait of the timed steps' gathers gave up: their results are not trustworthy")
     if world_size > 1:
         step_ms, rsa_ms = max_over_ranks([step_ms, rsa_ms], dev)
         if "unavailable" not in e2e:
@@ -963,6 +967,7 @@ def run_ours(args):
         },
         "e2e": e2e_record(e2e, total_bytes, args),
         "gpu_launches": run.launches,
+        "wait_timeouts": int(run.wait_timeouts.item()),
         "variants": {k: dict(v, value=round(world_size * v["bytes_per_step"] / (v["ms_per_step"] * 1e-3) / 1e9, 2),
                              frac=round(v["bytes_per_step"] / (v["ms_per_step"] * 1e-3) / 1e9 / peak, 4))
                      for k, v in variants.items()},
