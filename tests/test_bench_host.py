@@ -36,3 +36,22 @@ def test_batching_constants_match_the_library():
     src = open(os.path.join(ROOT, "sharded_fsdp_reduce_gb300", "csrc", "group.cuh")).read()
     assert int(re.search(r"#define FSDP_GROUP_MAX (\d+)", src).group(1)) == bench.GROUP_MAX_UNITS
     assert 1 << int(re.search(r"#define FSDP_GROUP_MAX_NUMEL_LOG2 (\d+)", src).group(1)) == bench.GROUP_MAX_NUMEL
+
+
+def test_e2e_reports_the_faster_form_with_the_other_beside_it():
+    import argparse
+    a = argparse.Namespace(e2e_read_params=False)
+    e = {"steps": 10, "h2d_bytes_per_step": 13690470400, "d2h_bytes_per_step": 4,
+         "copy_pipeline_ms": 86.4, "zero_copy_ms": 69.3, "bare_h2d_ms": 79.4}
+    r = bench.e2e_record(e, 66741043200, a)
+    assert r["path"] == "zero_copy" and r["ms_per_step"] == 69.3
+    assert r["value"] == round(66741043200 / 69.3e-3 / 1e9, 2)
+    assert r["copy_pipeline"]["ms_per_step"] == 86.4 and "zero_copy" not in r
+    assert r["bare_h2d_over_e2e"] == round(79.4 / 69.3, 4)
+    assert r["h2d_bytes_per_step"] == 13690470400 and r["d2h_bytes_per_step"] == 4
+    e.update(copy_pipeline_ms=66.4, zero_copy_ms=69.2)
+    r = bench.e2e_record(e, 66741043200, argparse.Namespace(e2e_read_params=True))
+    assert r["path"] == "copy_pipeline" and r["zero_copy"]["ms_per_step"] == 69.2
+    assert r["d2h"] == "compute-dtype parameters"
+    assert bench.e2e_record({"unavailable": "pinned host buffers: out of memory"}, 1, a) == {
+        "unavailable": "pinned host buffers: out of memory"}
