@@ -443,6 +443,9 @@ typedef struct fsdp_step_plan fsdp_step_plan;
  * callers that do not capture graphs: the per-layer step of "FSDP (Fully
  * Sharded Data Parallel)", "The Per-Layer Communication", with one unit per
  * wrapped layer and the validation paid once per model, not once per step.
+ * The plan belongs to the device that is current when it is made: a launch
+ * with another device current is refused (FSDP_ERR_INVALID_ARG, nothing
+ * enqueued), since the buffers' addresses are that device's.
  *   plan_out     host; receives the handle (NULL on error).
  * Other arguments and statuses as fsdp_step_units. */
 fsdp_status fsdp_step_plan_create(const fsdp_unit *units, int n_units, int gathers, int fuse_first_gather,

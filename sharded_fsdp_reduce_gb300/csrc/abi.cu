@@ -1121,12 +1121,14 @@ FSDP_API fsdp_status fsdp_step_units_ex_launches(const fsdp_unit_ex *units, int 
 
 // A validated model step (fsdp_step_plan_*): the model's plan, whose update
 // arguments each launch rewrites with its step's scalars. `variant` plans
-// hold the variant update of one optimizer.
+// hold the variant update of one optimizer. `device` is the device that was
+// current when the plan was made: its buffers' addresses belong to it.
 struct fsdp_step_plan {
     ModelPlan m;
     bool variant = false;
     int optimizer = 0;
     std::vector<int> grad_dtypes;
+    int device = -1;
 };
 
 // A captured model step (fsdp_step_graph_*): the instantiated graph and,
@@ -1171,6 +1173,10 @@ fsdp_status make_plan(ModelPlan &m, bool variant, int optimizer, fsdp_step_plan 
     p->variant = variant;
     p->optimizer = optimizer;
     p->grad_dtypes = grad_dtypes_of(p->m);
+    if (cudaGetDevice(&p->device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        p->device = -1;
+    }
     *plan_out = p;
     return FSDP_OK;
 }
@@ -1292,9 +1298,20 @@ FSDP_API fsdp_status fsdp_step_plan_create_ex(const fsdp_unit_ex *units, int n_u
     return make_plan(m, true, cfg->optimizer, plan_out);
 }
 
+// Whether the device current now is the one a plan was made on.
+static bool on_plan_device(const fsdp_step_plan *plan) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        dev = -1;
+    }
+    return dev == plan->device;
+}
+
 FSDP_API fsdp_status fsdp_step_plan_launch(fsdp_step_plan *plan, const fsdp_adamw_hparams *hp, void *stream) {
     if (!plan || !hp || plan->variant) return FSDP_ERR_INVALID_ARG;
     if (!adam_step_valid(*hp)) return FSDP_ERR_INVALID_ARG;
+    if (!on_plan_device(plan)) return FSDP_ERR_INVALID_ARG;
     set_adam_scalars(plan->m, *hp);
     return run_units(plan->m, static_cast<cudaStream_t>(stream));
 }
@@ -1302,6 +1319,7 @@ FSDP_API fsdp_status fsdp_step_plan_launch(fsdp_step_plan *plan, const fsdp_adam
 FSDP_API fsdp_status fsdp_step_plan_launch_ex(fsdp_step_plan *plan, const fsdp_step_config *cfg, void *stream) {
     if (!plan || !cfg || !plan->variant) return FSDP_ERR_INVALID_ARG;
     if (fsdp_status st = step_config_valid(*cfg, plan->optimizer, plan->grad_dtypes); st != FSDP_OK) return st;
+    if (!on_plan_device(plan)) return FSDP_ERR_INVALID_ARG;
     set_step_scalars(plan->m, *cfg);
     return run_units(plan->m, static_cast<cudaStream_t>(stream));
 }
