@@ -33,15 +33,14 @@ reshard-after-forward, once more for the backward).
 from __future__ import annotations
 
 import math
-from typing import Dict, List, Optional, Sequence, Tuple
+from typing import Dict, Optional, Sequence, Tuple
 
 import torch
 
-from .fsdp import (OPTIMIZERS, AdamWHParams, StepConfig, StepGraph, StepPlan, UnitDescs, View, fsdp_all_gather,
-                   fsdp_flatten_pad,
-                   fsdp_reduce_scatter_adam_cast, fsdp_reduce_scatter_adam_cast_gather, fsdp_reduce_scatter_step,
-                   fsdp_step_units, fsdp_step_units_ex, fsdp_step_units_ex_launches, fsdp_step_units_launches,
-                   fsdp_unflatten_views)
+from .fsdp import (OPTIMIZERS, AdamWHParams, StepConfig, StepGraph, StepPlan, UnitDescs, fsdp_all_gather,
+                   fsdp_flatten_pad, fsdp_reduce_scatter_adam_cast, fsdp_reduce_scatter_adam_cast_gather,
+                   fsdp_reduce_scatter_step, fsdp_step_units, fsdp_step_units_ex, fsdp_step_units_ex_launches,
+                   fsdp_step_units_launches, fsdp_unflatten_views)
 
 
 class FlatParamUnit:
