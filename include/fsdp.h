@@ -61,7 +61,10 @@
  *  - Arguments are validated on the host before anything is launched; an
  *    invalid call returns an error status and enqueues nothing. A launch
  *    failure returns FSDP_ERR_CUDA; fsdp_last_cuda_error() then gives the
- *    cudaError_t value. Nothing aborts, traps or prints.
+ *    cudaError_t value. The calls that take a whole model (fsdp_step_units*,
+ *    the plans and the captured steps) keep host bookkeeping of their own;
+ *    if the host cannot provide it they return FSDP_ERR_HOST_MEMORY, with
+ *    nothing enqueued. Nothing aborts, traps or prints.
  *  - Element pointers must be aligned to their element size. Any such
  *    alignment works; 16-byte-aligned bases take the vectorised path.
  */
@@ -82,7 +85,8 @@ typedef enum {
     FSDP_ERR_INVALID_ARG = 1,       /* null pointer, bad size, bad range, aliasing, ... */
     FSDP_ERR_ALIGNMENT = 2,         /* a pointer not aligned to its element size */
     FSDP_ERR_CUDA = 3,              /* a CUDA call or kernel launch failed */
-    FSDP_ERR_UNSUPPORTED_DTYPE = 4  /* dtype not accepted by this entry point */
+    FSDP_ERR_UNSUPPORTED_DTYPE = 4, /* dtype not accepted by this entry point */
+    FSDP_ERR_HOST_MEMORY = 5        /* host memory for the library's bookkeeping of a model ran out */
 } fsdp_status;
 
 typedef enum { FSDP_F32 = 0, FSDP_BF16 = 1, FSDP_F16 = 2 } fsdp_dtype;

@@ -20,6 +20,7 @@ FSDP_ERR_INVALID_ARG = 1
 FSDP_ERR_ALIGNMENT = 2
 FSDP_ERR_CUDA = 3
 FSDP_ERR_UNSUPPORTED_DTYPE = 4
+FSDP_ERR_HOST_MEMORY = 5
 
 FSDP_F32, FSDP_BF16, FSDP_F16 = 0, 1, 2
 FSDP_OPT_ADAMW, FSDP_OPT_SGD, FSDP_OPT_ADAMAX, FSDP_OPT_ADADELTA = 0, 1, 2, 3

@@ -64,6 +64,19 @@ AdamScalars make_scalars(const fsdp_adamw_hparams &h, int world) {
 
 bool mul_overflows(int64_t a, int64_t b) { return a != 0 && b > INT64_MAX / a; }
 
+// Run the body of an entry point that allocates host memory for the
+// library's own bookkeeping (the per-unit plans, batches and captured-step
+// records): running out of it is reported as FSDP_ERR_HOST_MEMORY, never as
+// an exception leaving the C ABI.
+template <class Body>
+fsdp_status guarded(Body &&body) noexcept {
+    try {
+        return body();
+    } catch (...) {
+        return FSDP_ERR_HOST_MEMORY;
+    }
+}
+
 StepScalars make_step_scalars(const fsdp_step_config &c, int world) {
     const double t = static_cast<double>(c.step);
     StepScalars k;
@@ -994,6 +1007,8 @@ fsdp_status capture_units(const ModelPlan &m, cudaGraph_t &graph, cudaGraphExec_
                           std::vector<UpdateNode> &nodes) {
     graph = nullptr;
     exec = nullptr;
+    // sized before the capture begins, so that nothing allocates while it is open
+    nodes.assign(m.work.size(), UpdateNode());
     cudaStream_t cs = nullptr;
     if (cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking); e != cudaSuccess) return cuda_status(e);
     // relaxed: the first launch of a kernel build queries its occupancy and
@@ -1081,40 +1096,48 @@ FSDP_API fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, in
 FSDP_API fsdp_status fsdp_step_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
                                      int gathers, int fuse_first_gather, uint32_t *nonfinite_count,
                                      uint32_t *wait_timeouts, void *stream) {
-    ModelPlan m;
-    const fsdp_status st =
-        plan_units(units, n_units, hp, gathers, fuse_first_gather, nonfinite_count, wait_timeouts, m);
-    if (st != FSDP_OK) return st;
-    return run_units(m, static_cast<cudaStream_t>(stream));
+    return guarded([&]() -> fsdp_status {
+        ModelPlan m;
+        const fsdp_status st =
+            plan_units(units, n_units, hp, gathers, fuse_first_gather, nonfinite_count, wait_timeouts, m);
+        if (st != FSDP_OK) return st;
+        return run_units(m, static_cast<cudaStream_t>(stream));
+    });
 }
 
 FSDP_API fsdp_status fsdp_step_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
                                         int gathers, uint32_t *nonfinite_count, uint32_t *wait_timeouts,
                                         void *stream) {
-    ModelPlan m;
-    const fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, wait_timeouts, m);
-    if (st != FSDP_OK) return st;
-    return run_units(m, static_cast<cudaStream_t>(stream));
+    return guarded([&]() -> fsdp_status {
+        ModelPlan m;
+        const fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, wait_timeouts, m);
+        if (st != FSDP_OK) return st;
+        return run_units(m, static_cast<cudaStream_t>(stream));
+    });
 }
 
 FSDP_API fsdp_status fsdp_step_units_launches(const fsdp_unit *units, int n_units, const fsdp_adamw_hparams *hp,
                                               int gathers, int fuse_first_gather, int64_t *launches_out) {
-    if (!launches_out) return FSDP_ERR_INVALID_ARG;
-    ModelPlan m;
-    const fsdp_status st = plan_units(units, n_units, hp, gathers, fuse_first_gather, nullptr, nullptr, m);
-    if (st != FSDP_OK) return st;
-    *launches_out = count_launches(m);
-    return FSDP_OK;
+    return guarded([&]() -> fsdp_status {
+        if (!launches_out) return FSDP_ERR_INVALID_ARG;
+        ModelPlan m;
+        const fsdp_status st = plan_units(units, n_units, hp, gathers, fuse_first_gather, nullptr, nullptr, m);
+        if (st != FSDP_OK) return st;
+        *launches_out = count_launches(m);
+        return FSDP_OK;
+    });
 }
 
 FSDP_API fsdp_status fsdp_step_units_ex_launches(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
                                                  int gathers, int64_t *launches_out) {
-    if (!launches_out) return FSDP_ERR_INVALID_ARG;
-    ModelPlan m;
-    const fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nullptr, nullptr, m);
-    if (st != FSDP_OK) return st;
-    *launches_out = count_launches(m);
-    return FSDP_OK;
+    return guarded([&]() -> fsdp_status {
+        if (!launches_out) return FSDP_ERR_INVALID_ARG;
+        ModelPlan m;
+        const fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nullptr, nullptr, m);
+        if (st != FSDP_OK) return st;
+        *launches_out = count_launches(m);
+        return FSDP_OK;
+    });
 }
 
 }  // extern "C"
@@ -1159,7 +1182,7 @@ fsdp_status make_graph(const ModelPlan &m, bool variant, int optimizer, fsdp_ste
     }
     g->graph = graph;
     g->exec = exec;
-    g->nodes = nodes;
+    g->nodes = std::move(nodes);
     g->variant = variant;
     g->optimizer = optimizer;
     *graph_out = g;
@@ -1208,63 +1231,71 @@ extern "C" {
 FSDP_API fsdp_status fsdp_step_graph_create(const fsdp_unit *units, int n_units, int gathers, int fuse_first_gather,
                                             uint32_t *nonfinite_count, uint32_t *wait_timeouts,
                                             fsdp_step_graph **graph_out) {
-    if (!graph_out) return FSDP_ERR_INVALID_ARG;
-    *graph_out = nullptr;
-    // every launch writes the step's own scalars into the update nodes
-    ModelPlan m;
-    fsdp_status st =
-        plan_units(units, n_units, &kPlaceholderHp, gathers, fuse_first_gather, nonfinite_count, wait_timeouts, m);
-    if (st != FSDP_OK) return st;
-    return make_graph(m, false, FSDP_OPT_ADAMW, graph_out);
+    return guarded([&]() -> fsdp_status {
+        if (!graph_out) return FSDP_ERR_INVALID_ARG;
+        *graph_out = nullptr;
+        // every launch writes the step's own scalars into the update nodes
+        ModelPlan m;
+        fsdp_status st =
+            plan_units(units, n_units, &kPlaceholderHp, gathers, fuse_first_gather, nonfinite_count, wait_timeouts, m);
+        if (st != FSDP_OK) return st;
+        return make_graph(m, false, FSDP_OPT_ADAMW, graph_out);
+    });
 }
 
 FSDP_API fsdp_status fsdp_step_graph_create_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
                                                int gathers, uint32_t *nonfinite_count, uint32_t *wait_timeouts,
                                                fsdp_step_graph **graph_out) {
-    if (!graph_out) return FSDP_ERR_INVALID_ARG;
-    *graph_out = nullptr;
-    ModelPlan m;
-    fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, wait_timeouts, m);
-    if (st != FSDP_OK) return st;
-    return make_graph(m, true, cfg->optimizer, graph_out);
+    return guarded([&]() -> fsdp_status {
+        if (!graph_out) return FSDP_ERR_INVALID_ARG;
+        *graph_out = nullptr;
+        ModelPlan m;
+        fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, wait_timeouts, m);
+        if (st != FSDP_OK) return st;
+        return make_graph(m, true, cfg->optimizer, graph_out);
+    });
 }
 
 FSDP_API fsdp_status fsdp_step_graph_launch(fsdp_step_graph *graph, const fsdp_adamw_hparams *hp, void *stream) {
-    if (!graph || !hp || graph->variant) return FSDP_ERR_INVALID_ARG;
-    if (!adam_step_valid(*hp)) return FSDP_ERR_INVALID_ARG;
-    for (const UpdateNode &n : graph->nodes) {
-        const AdamScalars sc = make_scalars(*hp, n.world);
-        fsdp_status st =
-            n.kind == kNodeGroup ? set_update_node<RsaGroupArgs, 1>(graph, n.node, [&](RsaGroupArgs &a) { a.s = sc; })
-            : n.kind == kNodeFusedGroup
-                ? set_update_node<RsaFusedGroupArgs, 1>(graph, n.node, [&](RsaFusedGroupArgs &a) { a.s = sc; })
-                : set_update_node<RsaArgs, 4>(graph, n.node, [&](RsaArgs &a) { a.s = sc; });
-        if (st != FSDP_OK) return st;
-    }
-    return cuda_status(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));
+    return guarded([&]() -> fsdp_status {
+        if (!graph || !hp || graph->variant) return FSDP_ERR_INVALID_ARG;
+        if (!adam_step_valid(*hp)) return FSDP_ERR_INVALID_ARG;
+        for (const UpdateNode &n : graph->nodes) {
+            const AdamScalars sc = make_scalars(*hp, n.world);
+            fsdp_status st =
+                n.kind == kNodeGroup ? set_update_node<RsaGroupArgs, 1>(graph, n.node, [&](RsaGroupArgs &a) { a.s = sc; })
+                : n.kind == kNodeFusedGroup
+                    ? set_update_node<RsaFusedGroupArgs, 1>(graph, n.node, [&](RsaFusedGroupArgs &a) { a.s = sc; })
+                    : set_update_node<RsaArgs, 4>(graph, n.node, [&](RsaArgs &a) { a.s = sc; });
+            if (st != FSDP_OK) return st;
+        }
+        return cuda_status(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));
+    });
 }
 
 FSDP_API fsdp_status fsdp_step_graph_launch_ex(fsdp_step_graph *graph, const fsdp_step_config *cfg, void *stream) {
-    if (!graph || !cfg || !graph->variant) return FSDP_ERR_INVALID_ARG;
-    std::vector<int> gds;
-    for (const UpdateNode &n : graph->nodes) gds.push_back(n.grad_dtype);
-    if (fsdp_status st = step_config_valid(*cfg, graph->optimizer, gds); st != FSDP_OK) return st;
-    const int lowp = cfg->reduce_dtype != FSDP_F32 ? 1 : 0;
-    for (const UpdateNode &n : graph->nodes) {
-        const StepScalars k = make_step_scalars(*cfg, n.world);
-        fsdp_status st = n.kind == kNodeVariantGroup
-                             ? set_update_node<StepGroupArgs, 1>(graph, n.node,
-                                                                 [&](StepGroupArgs &a) {
-                                                                     a.k = k;
-                                                                     a.reduce_lowp = lowp;
-                                                                 })
-                             : set_update_node<StepArgs, 4>(graph, n.node, [&](StepArgs &a) {
-                                   a.k = k;
-                                   a.reduce_lowp = lowp;
-                               });
-        if (st != FSDP_OK) return st;
-    }
-    return cuda_status(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));
+    return guarded([&]() -> fsdp_status {
+        if (!graph || !cfg || !graph->variant) return FSDP_ERR_INVALID_ARG;
+        std::vector<int> gds;
+        for (const UpdateNode &n : graph->nodes) gds.push_back(n.grad_dtype);
+        if (fsdp_status st = step_config_valid(*cfg, graph->optimizer, gds); st != FSDP_OK) return st;
+        const int lowp = cfg->reduce_dtype != FSDP_F32 ? 1 : 0;
+        for (const UpdateNode &n : graph->nodes) {
+            const StepScalars k = make_step_scalars(*cfg, n.world);
+            fsdp_status st = n.kind == kNodeVariantGroup
+                                 ? set_update_node<StepGroupArgs, 1>(graph, n.node,
+                                                                     [&](StepGroupArgs &a) {
+                                                                         a.k = k;
+                                                                         a.reduce_lowp = lowp;
+                                                                     })
+                                 : set_update_node<StepArgs, 4>(graph, n.node, [&](StepArgs &a) {
+                                       a.k = k;
+                                       a.reduce_lowp = lowp;
+                                   });
+            if (st != FSDP_OK) return st;
+        }
+        return cuda_status(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));
+    });
 }
 
 FSDP_API fsdp_status fsdp_step_graph_destroy(fsdp_step_graph *graph) {
@@ -1278,24 +1309,28 @@ FSDP_API fsdp_status fsdp_step_graph_destroy(fsdp_step_graph *graph) {
 FSDP_API fsdp_status fsdp_step_plan_create(const fsdp_unit *units, int n_units, int gathers, int fuse_first_gather,
                                            uint32_t *nonfinite_count, uint32_t *wait_timeouts,
                                            fsdp_step_plan **plan_out) {
-    if (!plan_out) return FSDP_ERR_INVALID_ARG;
-    *plan_out = nullptr;
-    ModelPlan m;
-    fsdp_status st =
-        plan_units(units, n_units, &kPlaceholderHp, gathers, fuse_first_gather, nonfinite_count, wait_timeouts, m);
-    if (st != FSDP_OK) return st;
-    return make_plan(m, false, FSDP_OPT_ADAMW, plan_out);
+    return guarded([&]() -> fsdp_status {
+        if (!plan_out) return FSDP_ERR_INVALID_ARG;
+        *plan_out = nullptr;
+        ModelPlan m;
+        fsdp_status st =
+            plan_units(units, n_units, &kPlaceholderHp, gathers, fuse_first_gather, nonfinite_count, wait_timeouts, m);
+        if (st != FSDP_OK) return st;
+        return make_plan(m, false, FSDP_OPT_ADAMW, plan_out);
+    });
 }
 
 FSDP_API fsdp_status fsdp_step_plan_create_ex(const fsdp_unit_ex *units, int n_units, const fsdp_step_config *cfg,
                                               int gathers, uint32_t *nonfinite_count, uint32_t *wait_timeouts,
                                               fsdp_step_plan **plan_out) {
-    if (!plan_out) return FSDP_ERR_INVALID_ARG;
-    *plan_out = nullptr;
-    ModelPlan m;
-    fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, wait_timeouts, m);
-    if (st != FSDP_OK) return st;
-    return make_plan(m, true, cfg->optimizer, plan_out);
+    return guarded([&]() -> fsdp_status {
+        if (!plan_out) return FSDP_ERR_INVALID_ARG;
+        *plan_out = nullptr;
+        ModelPlan m;
+        fsdp_status st = plan_units_ex(units, n_units, cfg, gathers, nonfinite_count, wait_timeouts, m);
+        if (st != FSDP_OK) return st;
+        return make_plan(m, true, cfg->optimizer, plan_out);
+    });
 }
 
 // Whether the device current now is the one a plan was made on.
@@ -1336,6 +1371,7 @@ FSDP_API const char *fsdp_status_string(fsdp_status status) {
         case FSDP_ERR_ALIGNMENT: return "FSDP_ERR_ALIGNMENT: pointer not aligned to its element size";
         case FSDP_ERR_CUDA: return "FSDP_ERR_CUDA: a CUDA call or kernel launch failed";
         case FSDP_ERR_UNSUPPORTED_DTYPE: return "FSDP_ERR_UNSUPPORTED_DTYPE: unsupported dtype";
+        case FSDP_ERR_HOST_MEMORY: return "FSDP_ERR_HOST_MEMORY: host memory for the call's bookkeeping ran out";
         default: return "FSDP_ERR_UNKNOWN: unknown status";
     }
 }

@@ -78,10 +78,10 @@ def test_unflatten_views_edge_cases():
 
 def test_status_strings(lib):
     from sharded_fsdp_reduce_gb300 import _lib
-    for code in range(5):
+    for code in range(6):
         assert lib.fsdp_status_string(code).decode().startswith(
             ["FSDP_OK", "FSDP_ERR_INVALID_ARG", "FSDP_ERR_ALIGNMENT", "FSDP_ERR_CUDA",
-             "FSDP_ERR_UNSUPPORTED_DTYPE"][code])
+             "FSDP_ERR_UNSUPPORTED_DTYPE", "FSDP_ERR_HOST_MEMORY"][code])
     assert lib.fsdp_status_string(99).decode().startswith("FSDP_ERR_UNKNOWN")
     assert lib.fsdp_last_cuda_error() == 0
     assert _lib.FSDP_OK == 0
@@ -585,3 +585,35 @@ def test_step_plan_validates_once_and_checks_only_the_scalars_per_launch(lib):
     assert lib.fsdp_step_plan_launch(plan, ctypes.byref(hp), None) == E.FSDP_ERR_INVALID_ARG  # not an AdamW plan
     assert lib.fsdp_last_cuda_error() == 0
     assert lib.fsdp_step_plan_destroy(plan) == E.FSDP_OK
+
+
+def test_running_out_of_host_memory_is_a_status_not_an_abort(tmp_path):
+    # a model the library cannot even hold its bookkeeping for (2^31 - 1
+    # units): every call that plans a model returns FSDP_ERR_HOST_MEMORY and
+    # the process goes on. Run in a child whose address space is capped, so
+    # that the allocation fails whatever the machine's overcommit policy.
+    import subprocess
+    import sys
+    code = r"""
+import ctypes, resource, sys
+resource.setrlimit(resource.RLIMIT_AS, (16 << 30, 16 << 30))
+sys.path.insert(0, ROOT)
+from sharded_fsdp_reduce_gb300 import _lib as E
+lib = E.load()
+hp = E.FsdpAdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+cfg = E.FsdpStepConfig(0, 0, 1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1.0)
+arr, arr_ex = (E.FsdpUnit * 1)(), (E.FsdpUnitEx * 1)()
+n = 2**31 - 1
+out, handle = ctypes.c_int64(-1), ctypes.c_void_p(None)
+got = [lib.fsdp_step_units_launches(arr, n, ctypes.byref(hp), 1, 0, ctypes.byref(out)),
+       lib.fsdp_step_units_ex_launches(arr_ex, n, ctypes.byref(cfg), 1, ctypes.byref(out)),
+       lib.fsdp_step_units(arr, n, ctypes.byref(hp), 1, 0, None, None, None),
+       lib.fsdp_step_units_ex(arr_ex, n, ctypes.byref(cfg), 1, None, None, None),
+       lib.fsdp_step_plan_create(arr, n, 1, 0, None, None, ctypes.byref(handle)),
+       lib.fsdp_step_plan_create_ex(arr_ex, n, ctypes.byref(cfg), 1, None, None, ctypes.byref(handle)),
+       lib.fsdp_step_graph_create(arr, n, 1, 0, None, None, ctypes.byref(handle))]
+print(got, out.value, handle.value)
+""".replace("ROOT", repr(ROOT))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == "[5, 5, 5, 5, 5, 5, 5] -1 None", r.stdout
