@@ -1178,7 +1178,7 @@ fsdp_status make_graph(const ModelPlan &m, bool variant, int optimizer, fsdp_ste
     if (!g) {
         cudaGraphExecDestroy(exec);
         cudaGraphDestroy(graph);
-        return FSDP_ERR_INVALID_ARG;
+        return FSDP_ERR_HOST_MEMORY;
     }
     g->graph = graph;
     g->exec = exec;
@@ -1191,7 +1191,7 @@ fsdp_status make_graph(const ModelPlan &m, bool variant, int optimizer, fsdp_ste
 
 fsdp_status make_plan(ModelPlan &m, bool variant, int optimizer, fsdp_step_plan **plan_out) {
     fsdp_step_plan *p = new (std::nothrow) fsdp_step_plan;
-    if (!p) return FSDP_ERR_INVALID_ARG;
+    if (!p) return FSDP_ERR_HOST_MEMORY;
     p->m = std::move(m);
     p->variant = variant;
     p->optimizer = optimizer;
@@ -1213,8 +1213,8 @@ fsdp_status set_update_node(fsdp_step_graph *graph, cudaGraphNode_t node, Fill f
     cudaKernelNodeParams kp;
     if (cudaError_t e = cudaGraphKernelNodeGetParams(node, &kp); e != cudaSuccess) return cuda_status(e);
     if (!kp.kernelParams) return FSDP_ERR_INVALID_ARG;
-    std::unique_ptr<Args> a(new (std::nothrow) Args);  // up to ~15 KB: not on the caller's stack
-    if (!a) return FSDP_ERR_INVALID_ARG;
+    std::unique_ptr<Args> a(new (std::nothrow) Args);  // up to ~31 KB: not on the caller's stack
+    if (!a) return FSDP_ERR_HOST_MEMORY;
     memcpy(a.get(), kp.kernelParams[0], sizeof(Args));
     fill(*a);
     void *args[NPARAMS];
