@@ -835,7 +835,7 @@ def time_per_config(run: _Run, peak: float):
         with ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clocks:
             time.sleep(0.25)  # let the sampler start before the timed launches
             each = timed_launches(lambda i: launch(4 + i), K, stream, flush)
-        run.launches += 3 + K
+        run.launches += K  # the timed launches (the three warm-up launches are not counted)
         mean = sum(each) / K
         achieved = rsa_b / (mean * 1e-3) / 1e9
         out[workload] = {
