@@ -336,7 +336,7 @@ fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, int world,
  * unit's. Work enqueued on `stream` after the call sees every unit done.
  * Batching: small units are stepped together, up to 256 per launch of each
  * kernel (128 when the first gather is fused into the update), when they
- * share N (2, 4 or 8), the dtype pair and the gathers, and each has at most
+ * share N (1, 2, 4 or 8), the dtype pair and the gathers, and each has at most
  * 2^24 elements, at most 8 gathered buffers, 16-byte aligned buffers and
  * its state in device memory; every element sees the same operations as in
  * the unit's own launch, so the results are the same bits. Every other unit

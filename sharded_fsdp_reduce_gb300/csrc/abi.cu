@@ -563,7 +563,9 @@ GroupKey key_of(const UnitPlan &p) {
 }
 
 // Whether a unit joins a batched launch: an update over all its ranks, N in
-// {2, 4, 8}, at most kGroupMaxNumel elements, every base pointer 16-byte
+// {1, 2, 4, 8} (the builds the batched kernels are instantiated for: a
+// compile-time N keeps the gradient pointers in registers), at most
+// kGroupMaxNumel elements, every base pointer 16-byte
 // aligned (the vector path and the bulk copies), the parameter or master in
 // device memory and at most kGroupMaxWorld gathered buffers. A fused first
 // gather (the fused AdamW update only) batches with the units that fuse it
@@ -576,7 +578,7 @@ bool groupable(const UnitPlan &p) {
     if (p.variant) {
         const StepArgs &a = p.step.args;
         if (a.begin != 0 || a.end > kGroupMaxNumel) return false;
-        if (a.world != 2 && a.world != 4 && a.world != 8) return false;
+        if (a.world != 1 && a.world != 2 && a.world != 4 && a.world != 8) return false;
         if (!aligned(a.param, 16) || !aligned(a.s0, 16) || !aligned(a.s1, 16) || !aligned(a.out, 16)) return false;
         for (int q = 0; q < a.world; ++q)
             if (!aligned(a.grads[q], 16)) return false;
@@ -584,7 +586,7 @@ bool groupable(const UnitPlan &p) {
     } else {
         const RsaArgs &a = p.rsa;
         if (a.n_full > kGroupMaxWorld || a.begin != 0 || a.end > kGroupMaxNumel) return false;
-        if (a.world != 2 && a.world != 4 && a.world != 8) return false;
+        if (a.world != 1 && a.world != 2 && a.world != 4 && a.world != 8) return false;
         if (!aligned(a.master, 16) || !aligned(a.m, 16) || !aligned(a.v, 16) || !aligned(a.out, 16)) return false;
         for (int q = 0; q < a.world; ++q)
             if (!aligned(a.grads[q], 16)) return false;

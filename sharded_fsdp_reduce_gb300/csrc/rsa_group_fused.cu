@@ -77,6 +77,7 @@ fsdp_status launch_nw(const RsaFusedGroupArgs &g, int64_t grid, cudaStream_t s) 
 template <int GD, int OD>
 fsdp_status launch_od(const RsaFusedGroupArgs &g, int64_t grid, cudaStream_t s) {
     switch (g.world) {
+        case 1: return launch_nw<1, GD, OD>(g, grid, s);
         case 2: return launch_nw<2, GD, OD>(g, grid, s);
         case 4: return launch_nw<4, GD, OD>(g, grid, s);
         case 8: return launch_nw<8, GD, OD>(g, grid, s);

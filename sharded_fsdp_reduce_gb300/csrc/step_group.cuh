@@ -74,6 +74,7 @@ template <int OPT, int GD, int OD, int SD>
 fsdp_status launch_group_world(const StepGroupArgs &g, int64_t grid, cudaStream_t s) {
     const unsigned blocks = static_cast<unsigned>(grid);
     switch (g.world) {
+        case 1: step_group_kernel<OPT, 1, GD, OD, SD><<<blocks, kThreads, 0, s>>>(g); break;
         case 2: step_group_kernel<OPT, 2, GD, OD, SD><<<blocks, kThreads, 0, s>>>(g); break;
         case 4: step_group_kernel<OPT, 4, GD, OD, SD><<<blocks, kThreads, 0, s>>>(g); break;
         case 8: step_group_kernel<OPT, 8, GD, OD, SD><<<blocks, kThreads, 0, s>>>(g); break;

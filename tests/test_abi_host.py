@@ -443,6 +443,7 @@ def test_step_units_launches_follow_the_batching(lib):
     assert count([small] * 5 + [(50000, 8, 8, True)]) == 2 + 2       # a misaligned unit keeps its own
     assert count([small] * 5 + [(50000 - 2, 2, 1, False)] * 3) == 2 + 2   # another N: a second batch
     assert count([(3 * 1000, 3, 3, False)] * 4) == 8                 # N = 3 is not batched
+    assert count([(1000, 1, 1, False)] * 4) == 2                     # N = 1 is (a single rank)
     assert count([small] * 5, gathers=2, fuse=1) == 2                # fused gather: one batch, then a gather
     assert count([small] * 300, gathers=1, fuse=1) == 3              # fused batches take 128 units each
     assert count([small] * 5 + [(50000, 8, 8, True)], gathers=1, fuse=1) == 1 + 1  # misaligned: its own
@@ -462,7 +463,7 @@ def test_step_units_launches_follow_the_batching(lib):
 
 
 def _expected_launches(specs, gathers):
-    """The batching rule restated: units of N in {2, 4, 8}, at most 2^24
+    """The batching rule restated: units of N in {1, 2, 4, 8}, at most 2^24
     elements, 16-byte aligned and not empty batch with the earlier ones of
     the same N (every fake unit here shares the dtypes and gathers), the
     header's batch size per batch; a batch of one is a unit on its own; one
@@ -473,7 +474,7 @@ def _expected_launches(specs, gathers):
     for P, world, n_full, misaligned in specs:
         if P == 0:
             continue
-        if world not in (2, 4, 8) or P > (1 << 24) or misaligned or n_full > 8:
+        if world not in (1, 2, 4, 8) or P > (1 << 24) or misaligned or n_full > 8:
             items += 1
             continue
         if open_.get(world, G) == G:
@@ -493,7 +494,7 @@ def test_step_units_launches_random_models(lib, seed):
     rng = np.random.default_rng(seed)
     specs = []
     for _ in range(int(rng.integers(1, 401))):
-        world = int(rng.choice([2, 3, 4, 8]))
+        world = int(rng.choice([1, 2, 3, 4, 8]))
         r = rng.random()
         P = 0 if r < 0.03 else (int(rng.integers(1 << 24, (1 << 24) + 64)) // world * world if r < 0.06
                                 else int(rng.integers(1, 5000)) * world)

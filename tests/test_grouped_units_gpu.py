@@ -73,12 +73,12 @@ def hp(F, t):
 @pytest.mark.parametrize("gathers", [0, 1, 2])
 def test_small_units_batched_equal_their_own_steps(F, gathers):
     # 300 units: sizes from 1 element to 60 k (ragged tails, units smaller than
-    # one chunk), N in {2, 4, 8}, two dtype pairs; 280 of one kind, so that
+    # one chunk), N in {1, 2, 4, 8}, two dtype pairs; 280 of one kind, so that
     # kind fills one group of 256 and starts a second
     rng = np.random.default_rng(gathers)
     specs = [(int(rng.integers(1, 60000)), 8, torch.bfloat16, torch.bfloat16) for _ in range(280)]
     specs += [(int(n), int(w), torch.bfloat16, torch.float16)
-              for n, w in zip(rng.integers(1, 20000, 20), rng.choice([2, 4, 8], 20))]
+              for n, w in zip(rng.integers(1, 20000, 20), rng.choice([1, 2, 4, 8], 20))]
     specs[3] = (1, 8, torch.bfloat16, torch.bfloat16)
     specs[4] = (7, 8, torch.bfloat16, torch.bfloat16)
     a, b = make_units(F, specs, 11 + gathers)
@@ -332,12 +332,12 @@ def vcfg(F, opt, t, lowp_dtype=None):
 @pytest.mark.parametrize("state", ["f32", "bf16"])
 def test_small_variant_units_batched_equal_their_own_steps(F, opt, state):
     # the variant step batched: every optimizer, fp32 or bf16 state, a
-    # bf16 reduce-scatter on the later steps, N in {2, 4, 8}, sizes from 1
+    # bf16 reduce-scatter on the later steps, N in {1, 2, 4, 8}, sizes from 1
     # element to 40 k; bit-equal to each unit's own fsdp_reduce_scatter_step
     rng = np.random.default_rng(sum(map(ord, opt + state)))
     sdt = torch.float32 if state == "f32" else torch.bfloat16
     specs = [(int(n), int(w), torch.bfloat16, torch.bfloat16)
-             for n, w in zip(rng.integers(1, 40000, 60), rng.choice([2, 4, 8], 60))]
+             for n, w in zip(rng.integers(1, 40000, 60), rng.choice([1, 2, 4, 8], 60))]
     specs[0] = (1, 8, torch.bfloat16, torch.bfloat16)
     a, b = make_variant_units(F, specs, 51, opt, sdt)
     seq = F.UnitSequence(a)
@@ -358,7 +358,7 @@ def test_small_variant_units_fp16_with_loss_scale(F, opt, state):
     rng = np.random.default_rng(len(opt) + len(state))
     sdt = torch.float16 if state == "f16" else torch.float32
     specs = [(int(n), int(w), torch.float16, torch.float16)
-             for n, w in zip(rng.integers(1, 30000, 40), rng.choice([2, 4, 8], 40))]
+             for n, w in zip(rng.integers(1, 30000, 40), rng.choice([1, 2, 4, 8], 40))]
     a, b = make_variant_units(F, specs, 81, opt, sdt)
     seq = F.UnitSequence(a)
     lr, b1, b2, eps, wd = VHP[opt]
