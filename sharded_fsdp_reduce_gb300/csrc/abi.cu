@@ -1,11 +1,13 @@
 // abi.cu -- the extern "C" entry points of libfsdpreduce.so (declared in
 // include/fsdp.h): argument validation, the per-step scalars, and dispatch to
 // the kernels. Every check runs on the host before anything is enqueued.
+#include <cuda.h>  // the driver's pointer-attribute types: the call itself goes through the runtime's lookup
 #include <math.h>
 #include <string.h>
 
 #include <algorithm>
 #include <atomic>
+#include <iterator>
 #include <memory>
 #include <new>
 #include <vector>
@@ -41,6 +43,57 @@ int sm_count() {
         g_sm_count[slot].store(n, std::memory_order_relaxed);
     }
     return n;
+}
+
+namespace {
+
+// cuPointerGetAttributes, found once through the runtime's driver entry-point
+// lookup (the library links no driver library of its own); null if the
+// lookup fails.
+using PointerAttributesFn = CUresult (*)(unsigned int, CUpointer_attribute *, void **, CUdeviceptr);
+PointerAttributesFn pointer_attributes_fn() {
+    static const PointerAttributesFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuPointerGetAttributes", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !f) {
+            (void)cudaGetLastError();
+            return static_cast<PointerAttributesFn>(nullptr);
+        }
+        return reinterpret_cast<PointerAttributesFn>(f);
+    }();
+    return fn;
+}
+
+}  // namespace
+
+// One driver query gives a pointer's memory type, whether it is managed and
+// the address range of its allocation; where that query is not available
+// (no driver entry point, no current context) the runtime's query answers
+// for this pointer alone. The classes match host_resident(): host memory
+// (page-locked) and addresses the runtime does not know are host; device
+// and managed memory are not.
+bool ResidencyMemo::host_resident(const void *p) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    auto next = device_.upper_bound(a);  // the first kept allocation that starts after p
+    if (next != device_.begin() && a < std::prev(next)->second) return false;
+    if (const PointerAttributesFn fn = pointer_attributes_fn()) {
+        // each value in a zeroed 8-byte word, whatever width the driver writes
+        uint64_t type = 0, managed = 0, start = 0, size = 0;
+        CUpointer_attribute attrs[4] = {CU_POINTER_ATTRIBUTE_MEMORY_TYPE, CU_POINTER_ATTRIBUTE_IS_MANAGED,
+                                        CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, CU_POINTER_ATTRIBUTE_RANGE_SIZE};
+        void *data[4] = {&type, &managed, &start, &size};
+        if (fn(4, attrs, data, static_cast<CUdeviceptr>(a)) == CUDA_SUCCESS) {
+            if (managed != 0) return false;
+            if (type == CU_MEMORYTYPE_DEVICE) {
+                if (size > 0 && start <= a && a - start < size) device_[start] = start + size;
+                return false;
+            }
+            return type == CU_MEMORYTYPE_HOST || type == 0;
+        }
+    }
+    return fsdp::host_resident(p);
 }
 
 namespace {
@@ -298,7 +351,8 @@ fsdp_status rsa_entry(const void *const *grads, fsdp_dtype grad_dtype, int world
 // Validation of an all-gather: fills its arguments or sets `empty`.
 // `timeouts` (device, may be NULL) counts the call's bounded waits that gave up.
 fsdp_status prepare_gather(const void *shard_out, fsdp_dtype dtype, int world, int64_t padded_numel,
-                           void *const *full_bufs, int n_dst, uint32_t *timeouts, GatherArgs &a, bool &empty) {
+                           void *const *full_bufs, int n_dst, uint32_t *timeouts, ResidencyMemo &res,
+                           GatherArgs &a, bool &empty) {
     empty = false;
     if (!dtype_valid(dtype)) return FSDP_ERR_UNSUPPORTED_DTYPE;
     if (world < 1 || padded_numel < 0 || padded_numel % world != 0) return FSDP_ERR_INVALID_ARG;
@@ -327,9 +381,9 @@ fsdp_status prepare_gather(const void *shard_out, fsdp_dtype dtype, int world, i
         a.dst[d] = full_bufs[d];
     }
     // the bulk-copy pipeline moves device memory only: host buffers are refused
-    if (host_resident(shard_out)) return FSDP_ERR_INVALID_ARG;
+    if (res.host_resident(shard_out)) return FSDP_ERR_INVALID_ARG;
     for (int d = 0; d < n_dst; ++d)
-        if (host_resident(full_bufs[d])) return FSDP_ERR_INVALID_ARG;
+        if (res.host_resident(full_bufs[d])) return FSDP_ERR_INVALID_ARG;
     return FSDP_OK;
 }
 
@@ -572,7 +626,7 @@ GroupKey key_of(const UnitPlan &p) {
 // too. Larger units fill the GPU on their own and keep their own
 // launches, whose gather (several tiles in flight per CTA, 3 CTAs per SM)
 // measured faster at those sizes than the batched gather's one-tile CTAs.
-bool groupable(const UnitPlan &p) {
+bool groupable(const UnitPlan &p, ResidencyMemo &res) {
     if (p.empty) return false;
     const void *state = nullptr;
     if (p.variant) {
@@ -600,7 +654,7 @@ bool groupable(const UnitPlan &p) {
         for (int d = 0; d < g.n_dst; ++d)
             if (!aligned(g.dst[d], 16)) return false;
     }
-    return !host_resident(state);
+    return !res.host_resident(state);
 }
 
 Group *new_group(std::vector<std::unique_ptr<Group>> &groups, const UnitPlan &p, int u) {
@@ -702,14 +756,14 @@ void add_to_group(Group &G, const UnitPlan &p) {
 // (kGroupMax per group), a group of one is launched as that unit alone, and
 // every other unit keeps its own kernels.
 void make_work(const std::vector<UnitPlan> &plan, std::vector<Work> &work,
-               std::vector<std::unique_ptr<Group>> &groups) {
+               std::vector<std::unique_ptr<Group>> &groups, ResidencyMemo &res) {
     work.clear();
     groups.clear();
     std::vector<std::pair<GroupKey, Group *>> open;  // the group now filling, per key
     for (size_t u = 0; u < plan.size(); ++u) {
         const UnitPlan &p = plan[u];
         if (p.empty) continue;
-        if (!groupable(p)) {
+        if (!groupable(p, res)) {
             work.push_back({static_cast<int>(u), nullptr});
             continue;
         }
@@ -811,9 +865,9 @@ fsdp_status check_spans(ModelPlan &m) {
 }
 
 // The last step of validating a model: the overlap checks, then the work items.
-fsdp_status finish_plan(ModelPlan &m) {
+fsdp_status finish_plan(ModelPlan &m, ResidencyMemo &res) {
     if (fsdp_status st = check_spans(m); st != FSDP_OK) return st;
-    make_work(m.units, m.work, m.groups);
+    make_work(m.units, m.work, m.groups, res);
     return FSDP_OK;
 }
 
@@ -871,6 +925,7 @@ fsdp_status plan_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hpa
     m.units.assign(static_cast<size_t>(n_units), UnitPlan());
     m.writes.clear();
     m.reads.clear();
+    ResidencyMemo res;
     for (int u = 0; u < n_units; ++u) {
         const fsdp_unit &x = units[u];
         UnitPlan &p = m.units[static_cast<size_t>(u)];
@@ -889,7 +944,7 @@ fsdp_status plan_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hpa
         if (p.separate_gathers > 0) {
             bool gempty = false;
             st = prepare_gather(x.shard_out, p.out_dtype, x.world, x.padded_numel, x.full_bufs, x.n_full,
-                                wait_timeouts, p.gather, gempty);
+                                wait_timeouts, res, p.gather, gempty);
             if (st != FSDP_OK) return st;
         }
         if (p.empty) continue;
@@ -905,7 +960,7 @@ fsdp_status plan_units(const fsdp_unit *units, int n_units, const fsdp_adamw_hpa
             for (int d = 0; d < x.n_full; ++d) add_span(m.writes, x.full_bufs[d], ob);
         for (int q = 0; q < x.world; ++q) add_span(m.reads, x.grads[q], gb);
     }
-    return finish_plan(m);
+    return finish_plan(m, res);
 }
 
 // Validation of fsdp_step_units_ex's units (and of a captured or planned
@@ -918,6 +973,7 @@ fsdp_status plan_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_ste
     m.units.assign(static_cast<size_t>(n_units), UnitPlan());
     m.writes.clear();
     m.reads.clear();
+    ResidencyMemo res;
     for (int u = 0; u < n_units; ++u) {
         const fsdp_unit_ex &x = units[u];
         UnitPlan &p = m.units[static_cast<size_t>(u)];
@@ -941,8 +997,8 @@ fsdp_status plan_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_ste
         const void *shard = sd == FSDP_F32 ? x.shard_out : x.param;
         if (p.separate_gathers > 0) {
             bool gempty = false;
-            st = prepare_gather(shard, od, x.world, x.padded_numel, x.full_bufs, x.n_full, wait_timeouts, p.gather,
-                                gempty);
+            st = prepare_gather(shard, od, x.world, x.padded_numel, x.full_bufs, x.n_full, wait_timeouts, res,
+                                p.gather, gempty);
             if (st != FSDP_OK) return st;
         }
         if (p.empty) continue;
@@ -958,7 +1014,7 @@ fsdp_status plan_units_ex(const fsdp_unit_ex *units, int n_units, const fsdp_ste
             for (int d = 0; d < x.n_full; ++d) add_span(m.writes, x.full_bufs[d], ob);
         for (int q = 0; q < x.world; ++q) add_span(m.reads, x.grads[q], gb);
     }
-    return finish_plan(m);
+    return finish_plan(m, res);
 }
 
 // One step's scalars written into a validated model's update arguments, per
@@ -1089,8 +1145,9 @@ FSDP_API fsdp_status fsdp_all_gather(const void *shard_out, fsdp_dtype dtype, in
                             void *const *full_bufs, int n_dst, uint32_t *wait_timeouts, void *stream) {
     GatherArgs a;
     bool empty = false;
+    ResidencyMemo res;
     const fsdp_status st =
-        prepare_gather(shard_out, dtype, world, padded_numel, full_bufs, n_dst, wait_timeouts, a, empty);
+        prepare_gather(shard_out, dtype, world, padded_numel, full_bufs, n_dst, wait_timeouts, res, a, empty);
     if (st != FSDP_OK || empty) return st;
     return launch_gather(a, static_cast<cudaStream_t>(stream));
 }

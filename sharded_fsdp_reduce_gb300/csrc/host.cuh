@@ -4,6 +4,7 @@
 #pragma once
 
 #include <atomic>
+#include <map>
 
 #include "common.cuh"
 
@@ -61,6 +62,20 @@ inline bool host_resident(const void *p) {
     }
     return at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
 }
+
+// host_resident() for the many buffers of one call, with one runtime query
+// per device allocation rather than per pointer: once a pointer is found in
+// device memory, the driver's address range of its allocation is kept, and
+// every later pointer inside that range is device memory without a query.
+// Lives for one validation pass, during which the caller's allocations stay
+// as they are; its answers are host_resident()'s.
+class ResidencyMemo {
+  public:
+    bool host_resident(const void *p);
+
+  private:
+    std::map<uintptr_t, uintptr_t> device_;  // start -> end of allocations found in device memory
+};
 
 // Byte ranges [a, a+na) and [b, b+nb) overlap.
 inline bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
