@@ -87,7 +87,13 @@ bool ResidencyMemo::host_resident(const void *p) {
         if (fn(4, attrs, data, static_cast<CUdeviceptr>(a)) == CUDA_SUCCESS) {
             if (managed != 0) return false;
             if (type == CU_MEMORYTYPE_DEVICE) {
-                if (size > 0 && start <= a && a - start < size) device_[start] = start + size;
+                if (size > 0 && start <= a && a - start < size) {
+                    try {
+                        device_[start] = start + size;
+                    } catch (...) {
+                        // out of host memory: the range is not kept, and later pointers are queried
+                    }
+                }
                 return false;
             }
             return type == CU_MEMORYTYPE_HOST || type == 0;
