@@ -105,6 +105,40 @@ def test_plan_matches_unplanned_call_and_captured_graph(F, gathers, fuse):
     graph.close()
 
 
+def test_a_plan_launched_from_other_host_threads(F):
+    # a plan made on this thread, then launched from a new host thread at
+    # each later step (that thread's own side streams and events; one launch
+    # at a time, as the header requires of one plan): the same bits as the
+    # same model planned and launched on this thread
+    import threading
+    a, b = build(F, 17), build(F, 17)
+    sa, sb = F.UnitSequence(a), F.UnitSequence(b)
+    for t in (1, 2, 3, 4):
+        load_grads([a, b], t)
+        hp = F.AdamWHParams(1e-3, weight_decay=0.01, step=t)
+        sa.step(hp, gathers=2)
+        if t == 1:
+            sb.step(hp, gathers=2)
+            first = sb._plan
+            continue
+        errors = []
+
+        def launch():
+            try:
+                sb.step(hp, gathers=2)
+                torch.cuda.synchronize()
+            except Exception as e:  # reported on the main thread
+                errors.append(e)
+
+        th = threading.Thread(target=launch)
+        th.start()
+        th.join()
+        assert not errors, errors
+    torch.cuda.synchronize()
+    assert sb._plan is first
+    assert_models_equal(a, b)
+
+
 @pytest.mark.parametrize("optimizer,state_dtype,lowp_reduce", [("adamw", torch.float32, True),
                                                                ("sgd", torch.float32, False),
                                                                ("adamax", torch.bfloat16, False),

@@ -182,3 +182,79 @@ def test_host_state_among_carved_units_keeps_its_own_launches(E):
     assert lib.fsdp_step_units_launches(arr, U, ctypes.byref(hp(E, 1)), 1, 0, ctypes.byref(n)) == E.FSDP_OK
     assert n.value == 2 + 2
     del keep
+
+
+_EXPANDABLE_SCRIPT = r"""
+import ctypes, sys
+import torch
+sys.path.insert(0, sys.argv[1])
+sys.path.insert(0, sys.argv[2])
+import sharded_fsdp_reduce_gb300 as F
+from sharded_fsdp_reduce_gb300 import _lib as E
+import test_residency_gpu as T
+
+def same(a, b):
+    iv = torch.int32 if a.element_size() == 4 else torch.int16
+    return torch.equal(a.view(iv), b.view(iv))
+
+# FlatParamUnits (each buffer its own torch allocation, inside the
+# allocator's expandable segments): the planned and the unplanned model step
+# equal each unit's own step
+g = torch.Generator().manual_seed(3)
+specs = [(int(n), w) for n, w in zip(torch.randint(1, 30000, (30,), generator=g), [1, 2, 8] * 10)]
+a, b, c = ([F.FlatParamUnit([("w", (n,))], w, torch.bfloat16, torch.bfloat16, device="cuda") for n, w in specs]
+           for _ in range(3))
+for k, (n, w) in enumerate(specs):
+    x = (torch.rand(n, generator=g) * 0.2 - 0.1).cuda()
+    for u in (a[k], b[k], c[k]):
+        u.load_master([x])
+seq_a, seq_b = F.UnitSequence(a), F.UnitSequence(b)
+assert seq_a.launches(gathers=1) < 2 * len(specs)
+for t in (1, 2, 3):
+    for k, (n, w) in enumerate(specs):
+        for r in range(w):
+            gr = (torch.randn(n, generator=g) * 1e-2).cuda().to(torch.bfloat16)
+            for u in (a[k], b[k], c[k]):
+                u.load_grad(r, [gr])
+    hp = F.AdamWHParams(1e-3, weight_decay=0.01, step=t)
+    seq_a.step(hp, gathers=1)
+    seq_b.step_unplanned(hp, gathers=1)
+    for u in c:
+        u.step(hp, gathers=1)
+torch.cuda.synchronize()
+for ua, ub, uc in zip(a, b, c):
+    for name in ("master", "exp_avg", "exp_avg_sq", "shard_out"):
+        assert same(getattr(ua, name), getattr(uc, name)) and same(getattr(ub, name), getattr(uc, name)), name
+    for fa, fc in zip(ua.full, uc.full):
+        assert same(fa, fc)
+
+# raw descriptors over one expandable-segment allocation: one batch; a
+# pinned host gathered buffer in the last unit is refused
+lib = E.load()
+U, P, world = 16, 2 * 1024, 2
+arena = T.Arena(U * T.unit_bytes(P, world))
+units = T.make_model(U, P, world, 4, arena)
+arr, keep = T.descs(E, units, P, world)
+n = ctypes.c_int64(-1)
+assert lib.fsdp_step_units_launches(arr, U, ctypes.byref(T.hp(E, 1)), 1, 0, ctypes.byref(n)) == E.FSDP_OK
+assert n.value == 2, n.value
+units[-1]["full"][0] = torch.zeros(P, dtype=torch.bfloat16, pin_memory=True)
+arr, keep = T.descs(E, units, P, world)
+assert lib.fsdp_step_units(arr, U, ctypes.byref(T.hp(E, 1)), 1, 0, None, None, None) == E.FSDP_ERR_INVALID_ARG
+print("expandable ok")
+"""
+
+
+def test_models_under_the_allocators_expandable_segments(E):
+    # the caching allocator's expandable segments map device memory into one
+    # reserved address range (driver virtual memory management): the
+    # residency answers and the batching must hold there too. The allocator
+    # mode is fixed when CUDA starts, so this runs in a child process.
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, PYTORCH_CUDA_ALLOC_CONF="expandable_segments:True")
+    r = subprocess.run([sys.executable, "-c", _EXPANDABLE_SCRIPT, os.path.dirname(here), here],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "expandable ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
